@@ -1,0 +1,226 @@
+"""Float64 CPU oracle of the WaveFilter per-layer, per-step KV filtering path.
+
+TEST INFRASTRUCTURE ONLY.  This module is the checker the CUDA path is held
+to.  Only the test suite, the package smoke check and the benchmark's CPU
+baseline leg may import it; the product path never calls it and shares no
+code with it.
+
+Source: "WaveFilter: Enhancing the Long-Context Capability of Diffusion LLMs
+via Wavelet-Guided KV Cache Filtering" (arXiv 2606.00724).  The pages give
+eq. (3) (cached attention, §2.1), eq. (5) (one DWT level, §2.2), the DWT
+pyramid {A_L, D_L..D_1} (§2.2), the DWT of the cached prompt keys with a
+basis psi (§3.1), and a prose pipeline (§1, Fig. 2 (b)-(d), §3 overview):
+extract low-frequency key features, score them against the queries with
+attention, keep a Top-K of candidate regions, refine those regions
+recursively across scales down to tokens, build a sparse KV cache from the
+final tokens plus the generation positions and attend over it.  §3.2 and
+Appendix A are not on the pages, so the following readings are taken (each
+one plainest consistent with the rest):
+
+  * psi is the orthonormal Haar pair g = [1/sqrt2, 1/sqrt2],
+    h = [1/sqrt2, -1/sqrt2]; eq. (5) pairs 0-based samples (2n, 2n+1), so
+    A_j[p] covers tokens [p 2^j, (p+1) 2^j).
+  * Score of a candidate = attention mass: for each query of the generation
+    block, softmax over the current candidate set of Q . A_j / sqrt(d), then
+    summed over the queries.  Raw orthonormal coefficients are used.
+  * Candidates at level j < L are the two children {2p, 2p+1} of every level
+    j+1 survivor; k_j survivors are kept per level, k_0 = final budget B.
+  * Top-K order: larger score first, equal scores -> lower position first.
+  * The sparse cache is the selected prompt tokens (ascending) followed by
+    all generation positions; eq. (3) attention over it, no mask.
+
+Everything is float64 numpy, one unit (sequence, layer, head) at a time,
+with no blocking or fusion beyond the definitions above.
+"""
+
+from __future__ import annotations
+
+import math
+from typing import Dict, List, Sequence
+
+import numpy as np
+
+SQRT2 = math.sqrt(2.0)
+
+__all__ = [
+    "haar_analysis_step",
+    "haar_synthesis_step",
+    "haar_dwt",
+    "haar_idwt",
+    "haar_pyramid",
+    "attention_mass",
+    "top_k",
+    "recursive_filter",
+    "sparse_attention",
+    "wavefilter_step",
+    "wavefilter_step_batched",
+]
+
+
+def haar_analysis_step(x: np.ndarray):
+    """One level of eq. (5) (WaveFilter §2.2) along axis 0 with Haar filters.
+
+    A_1[n] = (x[2n] + x[2n+1]) / sqrt2 (low-pass g), D_1[n] = (x[2n] -
+    x[2n+1]) / sqrt2 (high-pass h); the factor-2 downsampling of eq. (5) is
+    the step of 2 in n.  Axis 0 must have even length.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    if x.shape[0] % 2:
+        raise ValueError("length must be even")
+    even, odd = x[0::2], x[1::2]
+    return (even + odd) / SQRT2, (even - odd) / SQRT2
+
+
+def haar_synthesis_step(a: np.ndarray, d: np.ndarray) -> np.ndarray:
+    """Inverse of :func:`haar_analysis_step` (orthonormal Haar synthesis)."""
+    a = np.asarray(a, dtype=np.float64)
+    d = np.asarray(d, dtype=np.float64)
+    out = np.empty((2 * a.shape[0],) + a.shape[1:], dtype=np.float64)
+    out[0::2] = (a + d) / SQRT2
+    out[1::2] = (a - d) / SQRT2
+    return out
+
+
+def haar_dwt(x: np.ndarray, levels: int):
+    """L-level pyramid of WaveFilter §2.2: returns (A_L, [D_1, ..., D_L]).
+
+    The approximation A_j is fed back into eq. (5) for the next level.
+    """
+    a = np.asarray(x, dtype=np.float64)
+    details = []
+    for _ in range(levels):
+        a, d = haar_analysis_step(a)
+        details.append(d)
+    return a, details
+
+
+def haar_idwt(a_l: np.ndarray, details: Sequence[np.ndarray]) -> np.ndarray:
+    """Rebuild the signal from (A_L, [D_1..D_L]) (used for self-tests)."""
+    a = np.asarray(a_l, dtype=np.float64)
+    for d in reversed(list(details)):
+        a = haar_synthesis_step(a, d)
+    return a
+
+
+def haar_pyramid(x: np.ndarray, levels: int) -> List[np.ndarray]:
+    """Approximations [A_0 = x, A_1, ..., A_L] (WaveFilter §2.2, §3.1).
+
+    A_L of the prompt keys is the low-frequency component K_low of §3.1.
+    """
+    out = [np.asarray(x, dtype=np.float64)]
+    for _ in range(levels):
+        out.append(haar_analysis_step(out[-1])[0])
+    return out
+
+
+def attention_mass(q: np.ndarray, keys: np.ndarray) -> np.ndarray:
+    """Importance of each candidate key (WaveFilter Fig. 2(c), §1).
+
+    z[i, c] = Q[i] . keys[c] / sqrt(d) (the eq. (3) logits), a softmax over
+    the candidates for every query i, and the per-candidate sum over the
+    queries.  Returns s[c] (non-negative, summing to the number of queries).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    keys = np.asarray(keys, dtype=np.float64)
+    d = q.shape[-1]
+    z = q @ keys.T / math.sqrt(d)
+    z = z - z.max(axis=1, keepdims=True)
+    p = np.exp(z)
+    p /= p.sum(axis=1, keepdims=True)
+    return p.sum(axis=0)
+
+
+def top_k(scores: np.ndarray, positions: np.ndarray, k: int):
+    """Top-k candidate positions (WaveFilter Fig. 2(c)-(d) "Top-K").
+
+    Order: larger score first; equal scores -> lower position first.
+    Returns (selected positions sorted ascending, boundary gap), where the
+    gap is (s_(k) - s_(k+1)) / s_(k) for the scores sorted in that order, or
+    +inf when every candidate is kept.
+    """
+    scores = np.asarray(scores, dtype=np.float64)
+    positions = np.asarray(positions, dtype=np.int64)
+    if not 1 <= k:
+        raise ValueError("k must be >= 1")
+    order = np.lexsort((positions, -scores))  # last key is primary
+    if k >= len(positions):
+        return np.sort(positions), math.inf
+    kth, nxt = scores[order[k - 1]], scores[order[k]]
+    gap = (kth - nxt) / kth if kth > 0 else 0.0
+    return np.sort(positions[order[:k]]), gap
+
+
+def recursive_filter(q: np.ndarray, kp: np.ndarray, levels: int,
+                     k_per_level: Sequence[int]) -> Dict:
+    """Coarse Top-K plus multi-scale recursive filtering (WaveFilter §3.1-§3.2,
+    Fig. 2(b)-(d)).
+
+    Level L: candidates are all N_p / 2^L positions of A_L; keep k_L.
+    Level j = L-1 .. 0: candidates are the children {2p, 2p+1} of the level
+    j+1 survivors, scored against A_j; keep k_j.  Level 0 yields the final
+    token set S (k_0 = B tokens, ascending).
+
+    Returns {"idx": S, "levels": {j: {"cand", "scores", "sel", "gap"}}}.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    pyr = haar_pyramid(kp, levels)
+    if len(k_per_level) != levels + 1:
+        raise ValueError("k_per_level needs levels + 1 entries")
+    per_level = {}
+    cand = np.arange(pyr[levels].shape[0], dtype=np.int64)
+    sel = None
+    for j in range(levels, -1, -1):
+        if j < levels:
+            cand = np.sort(np.concatenate([2 * sel, 2 * sel + 1]))
+        if k_per_level[j] > len(cand):
+            raise ValueError(f"k_{j}={k_per_level[j]} exceeds {len(cand)} candidates")
+        s = attention_mass(q, pyr[j][cand])
+        sel, gap = top_k(s, cand, int(k_per_level[j]))
+        per_level[j] = {"cand": cand, "scores": s, "sel": sel, "gap": gap}
+    return {"idx": sel, "levels": per_level}
+
+
+def sparse_attention(q, kp, vp, kg, vg, idx):
+    """Eq. (3) of WaveFilter §2.1 over the sparse cache (Fig. 2(d)).
+
+    Keys/values are the prompt rows at ``idx`` followed by every generation
+    row; O = softmax(Q K^T / sqrt(d)) V with no mask.  Also returns the
+    natural-log normaliser lse[i] = log sum_j exp(Q[i] . K_j / sqrt(d)).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    idx = np.asarray(idx, dtype=np.int64)
+    k = np.concatenate([np.asarray(kp, np.float64)[idx], np.asarray(kg, np.float64)])
+    v = np.concatenate([np.asarray(vp, np.float64)[idx], np.asarray(vg, np.float64)])
+    z = q @ k.T / math.sqrt(q.shape[-1])
+    m = z.max(axis=1, keepdims=True)
+    e = np.exp(z - m)
+    denom = e.sum(axis=1, keepdims=True)
+    out = (e / denom) @ v
+    lse = (m + np.log(denom))[:, 0]
+    return out, lse
+
+
+def wavefilter_step(q, kp, vp, kg, vg, levels: int, k_per_level: Sequence[int]) -> Dict:
+    """Whole path for one unit: DWT -> coarse Top-K -> recursive filtering ->
+    sparse cache -> eq. (3) attention.  Returns the selection record plus
+    "out" [G, d], "lse" [G] and "a_l" (the level-L approximation)."""
+    sel = recursive_filter(q, kp, levels, k_per_level)
+    out, lse = sparse_attention(q, kp, vp, kg, vg, sel["idx"])
+    sel["out"] = out
+    sel["lse"] = lse
+    sel["a_l"] = haar_pyramid(kp, levels)[levels]
+    return sel
+
+
+def wavefilter_step_batched(inputs: Dict[str, np.ndarray], levels: int,
+                            k_per_level: Sequence[int]) -> List[Dict]:
+    """Apply :func:`wavefilter_step` to every unit of [b, H, rows, d] arrays
+    (units are independent).  Returns a flat list in (b, h) order."""
+    b, h = inputs["Q"].shape[:2]
+    res = []
+    for bi in range(b):
+        for hi in range(h):
+            res.append(wavefilter_step(inputs["Q"][bi, hi], inputs["Kp"][bi, hi],
+                                       inputs["Vp"][bi, hi], inputs["Kg"][bi, hi],
+                                       inputs["Vg"][bi, hi], levels, k_per_level))
+    return res

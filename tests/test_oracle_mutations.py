@@ -1,0 +1,111 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that the pins
+of ``test_oracle.py`` catch each one.  A pin set that lets a dropped term, a
+wrong index, a transposed softmax or a reversed tie-break through is too weak.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle.wavefilter_oracle as wo
+import test_oracle as pins
+
+
+def _analysis_unscaled(x):
+    x = np.asarray(x, dtype=np.float64)
+    return x[0::2] + x[1::2], x[0::2] - x[1::2]
+
+
+def _analysis_misaligned(x):
+    x = np.roll(np.asarray(x, dtype=np.float64), 1, axis=0)
+    return (x[0::2] + x[1::2]) / math.sqrt(2), (x[0::2] - x[1::2]) / math.sqrt(2)
+
+
+def _mass_wrong_axis(q, keys):
+    z = np.asarray(q, np.float64) @ np.asarray(keys, np.float64).T / math.sqrt(q.shape[-1])
+    p = np.exp(z - z.max(axis=0, keepdims=True))
+    return (p / p.sum(axis=0, keepdims=True)).sum(axis=0)
+
+
+def _mass_no_scale(q, keys):
+    z = np.asarray(q, np.float64) @ np.asarray(keys, np.float64).T
+    p = np.exp(z - z.max(axis=1, keepdims=True))
+    return (p / p.sum(axis=1, keepdims=True)).sum(axis=0)
+
+
+def _mass_max_over_queries(q, keys):
+    z = np.asarray(q, np.float64) @ np.asarray(keys, np.float64).T / math.sqrt(q.shape[-1])
+    p = np.exp(z - z.max(axis=1, keepdims=True))
+    return (p / p.sum(axis=1, keepdims=True)).max(axis=0)
+
+
+def _topk_high_tiebreak(scores, positions, k):
+    scores = np.asarray(scores, np.float64)
+    positions = np.asarray(positions, np.int64)
+    order = np.lexsort((-positions, -scores))
+    if k >= len(positions):
+        return np.sort(positions), math.inf
+    return np.sort(positions[order[:k]]), 0.0
+
+
+def _topk_smallest(scores, positions, k):
+    scores = np.asarray(scores, np.float64)
+    positions = np.asarray(positions, np.int64)
+    order = np.lexsort((positions, scores))
+    if k >= len(positions):
+        return np.sort(positions), math.inf
+    return np.sort(positions[order[:k]]), 0.0
+
+
+def _attn_drop_generation_rows(q, kp, vp, kg, vg, idx):
+    return _ORIG_ATTN(q, kp, vp, kg[:0], vg[:0], idx)
+
+
+def _attn_no_scale(q, kp, vp, kg, vg, idx):
+    return _ORIG_ATTN(np.asarray(q, np.float64) * math.sqrt(np.shape(q)[-1]), kp, vp, kg, vg, idx)
+
+
+_ORIG_ATTN = wo.sparse_attention
+
+PIN_TESTS = [
+    lambda: pins.test_haar_worked_example(),
+    lambda: pins.test_haar_parseval(3),
+    lambda: pins.test_haar_delta_lands_in_its_block(5),
+    lambda: pins.test_haar_lowpass_is_scaled_span_sum(3),
+    lambda: pins.test_attention_mass_worked_example(),
+    lambda: pins.test_attention_mass_matches_sdpa_probabilities(3, 17, 8),
+    lambda: pins.test_attention_mass_sums_to_number_of_queries(),
+    lambda: pins.test_top_k_matches_bruteforce_with_ties(),
+    lambda: pins.test_top_k_all_equal_takes_lowest_positions(),
+    lambda: pins.test_recursive_filter_keep_all_is_token_topk(),
+    lambda: pins.test_recursive_filter_all_equal_keys_picks_lowest(),
+    lambda: pins.test_sparse_attention_worked_example(),
+    lambda: pins.test_full_budget_is_full_attention(),
+    lambda: pins.test_sparse_attention_uses_only_selected_rows(),
+    lambda: pins.test_lse_closed_forms(),
+]
+
+MUTANTS = [
+    ("haar_analysis_step", _analysis_unscaled),
+    ("haar_analysis_step", _analysis_misaligned),
+    ("attention_mass", _mass_wrong_axis),
+    ("attention_mass", _mass_no_scale),
+    ("attention_mass", _mass_max_over_queries),
+    ("top_k", _topk_high_tiebreak),
+    ("top_k", _topk_smallest),
+    ("sparse_attention", _attn_drop_generation_rows),
+    ("sparse_attention", _attn_no_scale),
+]
+
+
+@pytest.mark.parametrize("target,mutant", MUTANTS, ids=[m.__name__ for _, m in MUTANTS])
+def test_pins_catch_mutant(monkeypatch, target, mutant):
+    monkeypatch.setattr(wo, target, mutant)
+    caught = 0
+    for pin in PIN_TESTS:
+        try:
+            pin()
+        except (AssertionError, ValueError):
+            caught += 1
+    assert caught > 0, f"no pin catches the mutant {mutant.__name__}"
