@@ -1,0 +1,214 @@
+/*
+ * wavefilter.h — C ABI of the GB300 (sm_103a) WaveFilter KV-filtering path.
+ *
+ * Method: "WaveFilter: Enhancing the Long-Context Capability of Diffusion
+ * LLMs via Wavelet-Guided KV Cache Filtering" (arXiv 2606.00724).  One call
+ * chain filters the cached prompt keys of one layer at one denoising step
+ * t > 1 and attends over the resulting sparse cache:
+ *
+ *   wf_dwt_lowpass        §2.2 eq. (5) pyramid, §3.1: Haar DWT of K~[I_p]
+ *   wf_score_topk         Fig. 2(c): query/low-frequency scoring + Top-K
+ *   wf_recursive_filter   Fig. 2(d), §3 overview: coarse-to-fine refinement
+ *   wf_sparse_gather_attn §2.1 eq. (3) over the sparse cache S ∪ I_g
+ *   wf_step               all four, in order, on one stream
+ *
+ * Readings fixed where the pages are silent: orthonormal Haar filters
+ * g = [1/√2, 1/√2] on 0-based pairs (2n, 2n+1), so coarse position p at
+ * level j covers tokens [p·2^j, (p+1)·2^j); the score of a candidate is its
+ * attention mass (per-query softmax of Q·A_j/√d over the current candidate
+ * set, summed over the queries); candidates at level j < L are the children
+ * {2p, 2p+1} of the level-(j+1) survivors; Top-K prefers the larger score
+ * and, on equal scores, the lower position; no attention mask.
+ *
+ * Shapes (row-major, contiguous; U = batch·heads independent units):
+ *   Kp, Vp : [batch, heads, n_prompt, head_dim]   prompt keys/values  (I_p)
+ *   Kg, Vg : [batch, heads, n_gen,    head_dim]   generation keys/values (I_g)
+ *   Q      : [batch, heads, n_gen,    head_dim]   generation-block queries
+ * Element type of Q/K/V: dims.dtype (WF_BF16 or WF_F32).  All arithmetic
+ * accumulates in fp32; every float output is fp32.
+ *
+ * Ownership and execution: the caller owns every buffer.  All pointers are
+ * DEVICE pointers except those documented as host (k_per_level, dims).
+ * Every device pointer must be 16-byte aligned.  The library never allocates
+ * device memory and never synchronises: each entry point validates its
+ * arguments on the host, then enqueues kernels on `stream` (a cudaStream_t;
+ * NULL = legacy default stream) and returns.  On any validation error
+ * nothing is enqueued.  Launch failures are reported as WF_ERR_CUDA.
+ * Data-dependent faults found on the device (an index outside [0, n_prompt)
+ * or a duplicate survivor) never cause an out-of-bounds access: the offending
+ * entry is skipped and a code is recorded in the workspace status word,
+ * readable with wf_read_device_status().
+ *
+ * Determinism: identical inputs give bit-identical outputs (fixed reduction
+ * orders, no floating-point atomics).
+ */
+#ifndef WAVEFILTER_H_
+#define WAVEFILTER_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+enum {
+  WF_OK = 0,
+  WF_ERR_NULL = 1,          /* a required pointer is NULL                        */
+  WF_ERR_SHAPE = 2,         /* inconsistent sizes / per-level k (see wf_step)    */
+  WF_ERR_UNSUPPORTED = 3,   /* head_dim not 64/128, unknown dtype, n_gen > 64    */
+  WF_ERR_WORKSPACE = 4,     /* workspace smaller than wf_workspace_bytes()       */
+  WF_ERR_CUDA = 5,          /* a CUDA launch or query failed                     */
+  WF_ERR_DEVICE_CHECK = 6,  /* a device-side check failed (device status word)   */
+  WF_ERR_ALIGNMENT = 7      /* a device pointer is not 16-byte aligned           */
+};
+
+/* Element types of Q, K, V. */
+enum { WF_BF16 = 0, WF_F32 = 1 };
+
+/* Device status word codes (bit flags, OR-ed by the kernels). */
+enum {
+  WF_DEV_OK = 0,
+  WF_DEV_BAD_INDEX = 1,      /* an index outside [0, n_prompt) (or its level range) */
+  WF_DEV_DUP_INDEX = 2,      /* a duplicate coarse survivor                         */
+  WF_DEV_WAIT_TIMEOUT = 4    /* a bounded wait on an asynchronous copy gave up      */
+};
+
+/* Limits of this build. */
+#define WF_MAX_LEVELS 12
+#define WF_MAX_GEN 64
+
+/* Problem dimensions (host struct, read during the call only).
+ *   batch, heads       : U = batch·heads independent (sequence, head) units
+ *   n_prompt           : N_p = |I_p|, must be a multiple of 2^levels
+ *   n_gen              : G = |I_g| = number of generation-block queries, 1..64
+ *   head_dim           : d ∈ {64, 128}
+ *   levels             : L, 1..12 (Haar levels; A_L has N_p/2^L positions)
+ *   dtype              : WF_BF16 or WF_F32 (element type of Q/K/V) */
+typedef struct {
+  int32_t batch, heads, n_prompt, n_gen, head_dim, levels, dtype;
+} wf_dims;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* wf_status_string(int status);
+
+/* Default per-level survivor counts (host helper; not on the device path).
+ * k_out[j], j = 0..levels: k_L = ceil(2·budget / 2^L) capped at N_p/2^L,
+ * k_j = min(2^(L-j)·k_L, N_p/2^j) for 0 < j < L, k_0 = budget.
+ * Returns WF_ERR_SHAPE if budget < 1 or n_prompt is not a multiple of 2^L. */
+int wf_default_k_per_level(int32_t n_prompt, int32_t levels, int32_t budget,
+                           int32_t* k_out);
+
+/* Bytes of device workspace wf_step (and each stage) needs for these sizes.
+ * k_per_level: host array of levels+1 entries (see wf_recursive_filter).
+ * Stores the byte count in *bytes.  Errors: WF_ERR_NULL/SHAPE/UNSUPPORTED. */
+int wf_workspace_bytes(const wf_dims* dims, const int32_t* k_per_level,
+                       size_t* bytes);
+
+/* Clears the device status word at the start of `workspace` (async). */
+int wf_clear_device_status(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Copies the device status word to *status_out and synchronises `stream`
+ * (the one synchronising call of this library).  Returns WF_OK or
+ * WF_ERR_CUDA; *status_out holds WF_DEV_* flags. */
+int wf_read_device_status(const void* workspace, size_t workspace_bytes,
+                          void* stream, int32_t* status_out);
+
+/* Step 1 — multi-level orthonormal Haar DWT along the token axis, low-pass
+ * branch only (WaveFilter §2.2 eq. (5) iterated into the pyramid of §2.2;
+ * §3.1 applies it to the cached prompt keys K~[I_p]).
+ *   A_j[p] = (A_{j-1}[2p] + A_{j-1}[2p+1]) / √2,  A_0 = Kp, per channel,
+ * i.e. A_L[p] = 2^(-L/2) · Σ_{n = p·2^L}^{(p+1)·2^L - 1} Kp[n].
+ *   Kp    : device, [U, N_p, d] of dims.dtype
+ *   AL    : device, out, [U, N_p/2^L, d] fp32
+ *   A_all : device, out, nullable.  If non-NULL, every level j = 1..L is
+ *           written, level-major: block j holds [U, N_p/2^j, d] fp32 and
+ *           blocks follow each other for j = 1, 2, ..., L.
+ * Errors: WF_ERR_NULL, WF_ERR_SHAPE, WF_ERR_UNSUPPORTED, WF_ERR_ALIGNMENT,
+ * WF_ERR_CUDA. */
+int wf_dwt_lowpass(const wf_dims* dims, const void* Kp, float* AL, float* A_all,
+                   void* stream);
+
+/* Step 2 — importance of each coarse position and coarse Top-K (WaveFilter
+ * Fig. 2(c); §1: "attention identifies the initial key tokens").
+ *   z[i,p] = Q[i]·A_L[p] / √d;  s[p] = Σ_i softmax_p(z[i,·])[p];
+ *   idx_L  = the k_L positions with the largest s (ties: lower p first).
+ *   Q        : device, [U, G, d] of dims.dtype
+ *   AL       : device, [U, N_p/2^L, d] fp32 (output of wf_dwt_lowpass)
+ *   k_L      : 1 ≤ k_L ≤ N_p/2^L
+ *   idx_L    : device, out, [U, k_L] int32, ascending
+ *   scores_L : device, out, nullable, [U, N_p/2^L] fp32 (s)
+ *   workspace: device, ≥ wf_workspace_bytes() (only its status word is used)
+ * Errors: as wf_dwt_lowpass plus WF_ERR_WORKSPACE. */
+int wf_score_topk(const wf_dims* dims, const void* Q, const float* AL,
+                  int32_t k_L, int32_t* idx_L, float* scores_L,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Step 3 — multi-scale recursive filtering down to token resolution
+ * (WaveFilter Fig. 2(d); §1 "multi-scale recursive filtering").  For
+ * j = L-1 .. 0: candidates C_j = {2p, 2p+1 : p ∈ S_{j+1}}, scored like
+ * step 2 against A_j[C_j] (softmax over C_j), S_j = Top-k_j(C_j).
+ *   Q, Kp       : device, as above (A_j is formed from the Kp rows of the
+ *                 coarse survivors' spans; nothing else of Kp is read)
+ *   idx_L       : device, [U, k_L] int32, the level-L survivors S_L (any
+ *                 order, distinct, each in [0, N_p/2^L))
+ *   k_per_level : HOST, levels+1 entries, k_per_level[j] = k_j:
+ *                 k_L = entries of idx_L per unit, 1 ≤ k_j ≤ 2·k_{j+1},
+ *                 k_0 = B = the final budget
+ *   idx         : device, out, [U, B] int32, the token set S = S_0, ascending
+ * Errors: as wf_score_topk. */
+int wf_recursive_filter(const wf_dims* dims, const void* Q, const void* Kp,
+                        const int32_t* idx_L, const int32_t* k_per_level,
+                        int32_t* idx, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/* Steps 4 and 5 — gather the sparse cache and attend (WaveFilter §2.1
+ * eq. (3) with the cached index set replaced by S ∪ I_g, Fig. 2(d)).
+ * Keys/values are Kp/Vp rows at idx[0..B) followed by all G rows of Kg/Vg:
+ *   O[i] = Σ_j softmax_j(Q[i]·K_j/√d) V_j,  lse[i] = log Σ_j exp(Q[i]·K_j/√d)
+ *   idx    : device, [U, B] int32 in [0, N_p) (order free; an out-of-range
+ *            entry is skipped and flagged WF_DEV_BAD_INDEX)
+ *   budget : B ≥ 0 (B = 0 attends over I_g alone)
+ *   O      : device, out, [U, G, d] fp32
+ *   lse    : device, out, nullable, [U, G] fp32 (natural log)
+ * Errors: as wf_score_topk. */
+int wf_sparse_gather_attn(const wf_dims* dims, const void* Q, const void* Kp,
+                          const void* Vp, const void* Kg, const void* Vg,
+                          const int32_t* idx, int32_t budget, float* O,
+                          float* lse, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* The whole per-layer, per-step path: steps 1-5 in order on `stream`.
+ *   k_per_level : HOST, levels+1 entries (k_0 = budget), constraints as in
+ *                 wf_recursive_filter plus 1 ≤ k_L ≤ N_p/2^L
+ *   O, lse      : outputs of step 5 (lse nullable)
+ *   idx_out     : device, out, nullable, [U, B] int32 — the selected tokens
+ *   workspace   : device scratch of ≥ wf_workspace_bytes() bytes; holds A_L,
+ *                 S_L and (for large budgets) token logits; contents are
+ *                 overwritten.  Concurrent calls need separate workspaces.
+ * Errors: WF_ERR_NULL, WF_ERR_SHAPE, WF_ERR_UNSUPPORTED, WF_ERR_ALIGNMENT,
+ * WF_ERR_WORKSPACE, WF_ERR_CUDA. */
+int wf_step(const wf_dims* dims, const void* Q, const void* Kp, const void* Vp,
+            const void* Kg, const void* Vg, const int32_t* k_per_level,
+            float* O, float* lse, int32_t* idx_out, void* workspace,
+            size_t workspace_bytes, void* stream);
+
+/* wf_step with host-resident inputs and outputs: copies Q/Kp/Vp/Kg/Vg from
+ * HOST memory into the caller's device staging buffers (one
+ * cudaMemcpyAsync each), runs wf_step, and copies O (and lse if both
+ * pointers are given) back to HOST memory, all on `stream`.  Pinned host
+ * memory gives asynchronous copies.  Device staging buffers d_* must have
+ * the sizes of the corresponding inputs/outputs.  Does not synchronise. */
+int wf_step_host(const wf_dims* dims, const void* h_Q, const void* h_Kp,
+                 const void* h_Vp, const void* h_Kg, const void* h_Vg,
+                 const int32_t* k_per_level, float* h_O, float* h_lse,
+                 void* d_Q, void* d_Kp, void* d_Vp, void* d_Kg, void* d_Vg,
+                 float* d_O, float* d_lse, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WAVEFILTER_H_ */

@@ -1,0 +1,136 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared
+symbol, and rejects bad arguments before anything reaches the GPU.  No call
+here launches a kernel, so the suite runs without a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from wavelet_guided_sparse_gb300 import binding as bd
+from wavelet_guided_sparse_gb300 import workloads as wl
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "wavefilter.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(bd.LIB_PATH):
+        from wavelet_guided_sparse_gb300 import build
+        build.build()
+    return bd.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(wf_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_path(lib):
+    names = _declared()
+    for want in ("wf_dwt_lowpass", "wf_score_topk", "wf_recursive_filter",
+                 "wf_sparse_gather_attn", "wf_step", "wf_workspace_bytes"):
+        assert want in names
+    assert set(names) == set(bd.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert lib.wf_status_string(code)
+    assert lib.wf_status_string(0) == b"ok"
+    assert lib.wf_status_string(99) == b"unknown status"
+
+
+@pytest.mark.parametrize("name", sorted(wl.CONFIGS))
+def test_default_k_matches_generator(lib, name):
+    cfg = wl.CONFIGS[name]
+    if cfg.k_coarse is not None:
+        pytest.skip("explicit coarse k")
+    assert bd.default_k_per_level(cfg.n_prompt, cfg.levels, cfg.budget) == cfg.k_per_level()
+
+
+def test_default_k_rejects_bad_input(lib):
+    out = (ctypes.c_int32 * 4)()
+    assert lib.wf_default_k_per_level(1004, 3, 64, out) == 2  # 1004 % 8 != 0
+    assert lib.wf_default_k_per_level(1024, 3, 0, out) == 2
+    assert lib.wf_default_k_per_level(1024, 0, 64, out) == 2
+    assert lib.wf_default_k_per_level(1024, 3, 64, None) == 1
+
+
+def _dims(**kw):
+    base = dict(batch=1, heads=32, n_prompt=4096, n_gen=32, head_dim=128, levels=4, dtype=0)
+    base.update(kw)
+    return bd.Dims(**base)
+
+
+def _ws(dims, k):
+    n = ctypes.c_size_t(0)
+    st = bd.lib().wf_workspace_bytes(ctypes.byref(dims), bd._k_array(k), ctypes.byref(n))
+    return st, n.value
+
+
+def test_workspace_bytes_validation(lib):
+    k = [512, 512, 256, 128, 64]
+    st, n = _ws(_dims(), k)
+    assert st == 0 and n >= 32 * 256 * 128 * 4
+    assert _ws(_dims(head_dim=96), k)[0] == 3
+    assert _ws(_dims(dtype=7), k)[0] == 3
+    assert _ws(_dims(n_gen=65), k)[0] == 3
+    assert _ws(_dims(n_prompt=4008), k)[0] == 2
+    assert _ws(_dims(levels=0), k)[0] == 2
+    assert _ws(_dims(), [512, 512, 256, 128, 300])[0] == 2   # k_L > N_p / 2^L
+    assert _ws(_dims(), [512, 512, 256, 100, 64])[0] == 2    # k_2 > 2 k_3
+    assert _ws(_dims(), [1025, 512, 256, 128, 64])[0] == 2   # B > 2 k_1
+    assert _ws(_dims(), [0, 512, 256, 128, 64])[0] == 2
+    assert lib.wf_workspace_bytes(None, bd._k_array(k), ctypes.byref(ctypes.c_size_t())) == 1
+
+
+def test_entry_points_reject_before_launch(lib):
+    # Every failure below is decided on the host; no kernel is enqueued.
+    dims = _dims()
+    k = bd._k_array([512, 512, 256, 128, 64])
+    p16 = ctypes.c_void_p(1 << 20)  # aligned dummy (never dereferenced on these paths)
+    p17 = ctypes.c_void_p((1 << 20) + 4)
+    st = lib.wf_step(ctypes.byref(dims), p16, p16, p16, p16, p16, k, p16, None, None,
+                     p16, 16, None)
+    assert st == 4  # workspace too small
+    st = lib.wf_step(ctypes.byref(dims), p17, p16, p16, p16, p16, k, p16, None, None,
+                     p16, 1 << 40, None)
+    assert st == 7  # misaligned Q
+    st = lib.wf_step(ctypes.byref(dims), None, p16, p16, p16, p16, k, p16, None, None,
+                     p16, 1 << 40, None)
+    assert st == 1
+    st = lib.wf_step(ctypes.byref(_dims(n_prompt=4100)), p16, p16, p16, p16, p16, k, p16,
+                     None, None, p16, 1 << 40, None)
+    assert st == 2
+    assert lib.wf_dwt_lowpass(ctypes.byref(dims), None, p16, None, None) == 1
+    assert lib.wf_dwt_lowpass(ctypes.byref(dims), p17, p16, None, None) == 7
+    assert lib.wf_score_topk(ctypes.byref(dims), p16, p16, 0, p16, None, p16, 1 << 20, None) == 2
+    assert lib.wf_score_topk(ctypes.byref(dims), p16, p16, 257, p16, None, p16, 1 << 20, None) == 2
+    assert lib.wf_score_topk(ctypes.byref(dims), p16, p16, 64, p16, None, p16, 8, None) == 4
+    assert lib.wf_recursive_filter(ctypes.byref(dims), p16, p16, p16,
+                                   bd._k_array([2000, 512, 256, 128, 64]), p16, p16, 1 << 40,
+                                   None) == 2
+    assert lib.wf_sparse_gather_attn(ctypes.byref(dims), p16, p16, p16, p16, p16, p16, -1, p16,
+                                     None, p16, 1 << 20, None) == 2
+    assert lib.wf_sparse_gather_attn(ctypes.byref(dims), p16, p16, p16, p16, p16, None, 5, p16,
+                                     None, p16, 1 << 20, None) == 1
+    assert lib.wf_clear_device_status(None, 256, None) == 1
+    assert lib.wf_clear_device_status(p16, 8, None) == 4
+
+
+def test_product_path_has_no_oracle_dependency():
+    # The package must never import the oracle (test infrastructure only).
+    pkg = os.path.dirname(bd.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(root, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f

@@ -1,0 +1,333 @@
+"""GPU parity: every step of the CUDA path against the float64 oracle on the
+same seeded inputs, called through the C ABI.
+
+Bars: DWT coefficients within 1e-3 relative; selected index sets identical
+wherever the oracle's boundary gap exceeds 1e-4 relative (otherwise the
+oracle's eq. (3) is evaluated on the GPU's set); attention output within
+2e-2 max-abs.  Workloads: the five synthetic configurations (full sizes, with
+sampled units for the large ones) plus small edge cases.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.wavefilter_oracle as wo
+from gpu_common import (AL_RTOL, GAP_TOL, OUT_ATOL, WORKERS, check_index_set,
+                        compare_step_unit, oracle_unit, run_step, to_device, unit_inputs)
+from wavelet_guided_sparse_gb300 import binding as bd
+from wavelet_guided_sparse_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+_CACHE = {}
+
+
+def layer_inputs(name, layer=0):
+    key = (name, layer)
+    if key not in _CACHE:
+        cfg = wl.CONFIGS[name]
+        big = cfg.units_per_layer * cfg.n_prompt > 1 << 20
+        _CACHE.clear() if big else None
+        _CACHE[key] = wl.generate_layer(cfg, layer, workers=WORKERS if big else 0)
+    return _CACHE[key]
+
+
+def _rand_inputs(seed, b, h, n, g, d, dtype):
+    rng = np.random.default_rng(seed)
+    arrs = {"Q": rng.standard_normal((b, h, g, d)) * 1.5,
+            "Kp": rng.standard_normal((b, h, n, d)) * 1.5,
+            "Vp": rng.standard_normal((b, h, n, d)),
+            "Kg": rng.standard_normal((b, h, g, d)) * 1.5,
+            "Vg": rng.standard_normal((b, h, g, d))}
+    rnd = wl.round_to_bf16 if dtype == "bf16" else (lambda x: x.astype(np.float32))
+    return {k: rnd(v) for k, v in arrs.items()}
+
+
+# ------------------------------------------------------------------ step 1: DWT
+
+@pytest.mark.parametrize("name", ["tiny", "llada8b_layer"])
+def test_dwt_all_levels_match_oracle(name):
+    cfg = wl.CONFIGS[name]
+    arrs = layer_inputs(name)
+    dev = to_device(arrs, cfg.dtype)
+    al, levels = bd.dwt_lowpass(dev["Kp"], cfg.levels, all_levels=True)
+    torch.cuda.synchronize()
+    for b in range(cfg.batch):
+        for h in range(cfg.heads):
+            pyr = wo.haar_pyramid(arrs["Kp"][b, h], cfg.levels)
+            for j in range(1, cfg.levels + 1):
+                got = levels[j - 1][b, h].cpu().numpy()
+                ref = pyr[j]
+                tol = AL_RTOL * np.abs(ref) + 1e-6 * np.sqrt((ref ** 2).mean())
+                assert (np.abs(got - ref) <= tol).all(), (b, h, j)
+            np.testing.assert_array_equal(al[b, h].cpu().numpy(), levels[-1][b, h].cpu().numpy())
+
+
+@pytest.mark.parametrize("n,levels,dtype,d", [(64, 1, "bf16", 128), (96, 5, "f32", 64),
+                                             (3 * 128, 7, "bf16", 64), (4096, 12, "f32", 128)])
+def test_dwt_shapes(n, levels, dtype, d):
+    arrs = _rand_inputs(n + levels, 2, 3, n, 4, d, dtype)
+    dev = to_device(arrs, dtype)
+    al = bd.dwt_lowpass(dev["Kp"], levels).cpu().numpy()
+    for b in range(2):
+        for h in range(3):
+            ref = wo.haar_pyramid(arrs["Kp"][b, h], levels)[levels]
+            tol = AL_RTOL * np.abs(ref) + 1e-6 * np.sqrt((ref ** 2).mean())
+            assert (np.abs(al[b, h] - ref) <= tol).all()
+
+
+# ------------------------------------------------------- step 2: coarse Top-K
+
+@pytest.mark.parametrize("name", ["tiny", "llada8b_layer"])
+def test_score_topk_matches_oracle(name):
+    cfg = wl.CONFIGS[name]
+    ks = cfg.k_per_level()
+    arrs = layer_inputs(name)
+    dev = to_device(arrs, cfg.dtype)
+    dims = bd.make_dims(dev["Q"], dev["Kp"], cfg.levels)
+    ws = bd.alloc_workspace(dims, ks, dev["Q"].device)
+    al = bd.dwt_lowpass(dev["Kp"], cfg.levels)
+    idx, scores = bd.score_topk(dev["Q"], al, cfg.n_prompt, cfg.levels, ks[-1], ws,
+                                return_scores=True)
+    idx, scores = idx.cpu().numpy(), scores.cpu().numpy()
+    decisive = 0
+    for b in range(cfg.batch):
+        for h in range(cfg.heads):
+            res = wo.recursive_filter(arrs["Q"][b, h], arrs["Kp"][b, h], cfg.levels, ks)
+            top = res["levels"][cfg.levels]
+            np.testing.assert_allclose(scores[b, h], top["scores"], rtol=1e-4,
+                                       atol=1e-6 * top["scores"].max())
+            assert (np.diff(idx[b, h]) > 0).all()
+            if top["gap"] > GAP_TOL:
+                decisive += 1
+                np.testing.assert_array_equal(idx[b, h], top["sel"])
+    assert decisive >= 1
+    assert bd.read_device_status(ws) == 0
+
+
+# ------------------------------------------------- step 3: recursive filtering
+
+def _filter_case(arrs, levels, ks, dtype):
+    dev = to_device(arrs, dtype)
+    b, h = arrs["Q"].shape[:2]
+    ress = [[wo.recursive_filter(arrs["Q"][i, j], arrs["Kp"][i, j], levels, ks)
+             for j in range(h)] for i in range(b)]
+    idx_l = np.stack([[ress[i][j]["levels"][levels]["sel"] for j in range(h)] for i in range(b)])
+    dims = bd.make_dims(dev["Q"], dev["Kp"], levels)
+    ws = bd.alloc_workspace(dims, ks, dev["Q"].device)
+    # Feed the coarse survivors in scrambled order: the kernel sorts them.
+    rng = np.random.default_rng(0)
+    scrambled = np.stack([[rng.permutation(idx_l[i, j]) for j in range(h)] for i in range(b)])
+    gidx = bd.recursive_filter(dev["Q"], dev["Kp"],
+                               torch.from_numpy(scrambled.astype(np.int32)).cuda(), levels, ks, ws)
+    gidx = gidx.cpu().numpy()
+    assert bd.read_device_status(ws) == 0
+    exact = 0
+    for i in range(b):
+        for j in range(h):
+            lv = ress[i][j]["levels"]
+            check_index_set(gidx[i, j], arrs["Kp"].shape[2], ks[0])
+            if all(lv[l]["gap"] > GAP_TOL for l in range(levels)):
+                exact += 1
+                np.testing.assert_array_equal(gidx[i, j], ress[i][j]["idx"], err_msg=f"({i},{j})")
+    return exact, b * h
+
+
+@pytest.mark.parametrize("name", ["tiny", "llada8b_layer"])
+def test_recursive_filter_matches_oracle(name):
+    cfg = wl.CONFIGS[name]
+    exact, total = _filter_case(layer_inputs(name), cfg.levels, cfg.k_per_level(), cfg.dtype)
+    assert exact >= total // 2
+
+
+@pytest.mark.parametrize("n,levels,ks,g,d,dtype,bh", [
+    (256, 3, [9, 14, 10, 8], 5, 64, "f32", (1, 3)),           # every level selects
+    (512, 4, [40, 30, 20, 12, 8], 20, 128, "bf16", (2, 2)),   # ragged G, selective levels
+    (1024, 2, [100, 90, 60], 1, 64, "bf16", (1, 2)),          # one query
+    (2048, 3, [300, 200, 150, 120], 64, 128, "bf16", (1, 2)), # G = 64, cluster > 1
+    (4096, 5, [512, 300, 160, 80, 64, 40], 32, 128, "bf16", (1, 2)),
+    (8192, 6, [1500, 800, 450, 230, 120, 60, 32], 48, 64, "bf16", (1, 2)),
+])
+def test_recursive_filter_nontrivial_levels(n, levels, ks, g, d, dtype, bh):
+    arrs = _rand_inputs(n * g + levels, bh[0], bh[1], n, g, d, dtype)
+    exact, total = _filter_case(arrs, levels, ks, dtype)
+    assert exact >= 1
+
+
+def test_recursive_filter_keep_everything_is_identity():
+    n, levels, g, d = 256, 3, 8, 64
+    arrs = _rand_inputs(3, 1, 2, n, g, d, "bf16")
+    ks = [n] + [n >> j for j in range(1, levels + 1)]
+    dev = to_device(arrs, "bf16")
+    dims = bd.make_dims(dev["Q"], dev["Kp"], levels)
+    ws = bd.alloc_workspace(dims, ks, dev["Q"].device)
+    idx_l = torch.arange(n >> levels, dtype=torch.int32, device="cuda").repeat(1, 2, 1)
+    got = bd.recursive_filter(dev["Q"], dev["Kp"], idx_l.contiguous(), levels, ks, ws)
+    np.testing.assert_array_equal(got.cpu().numpy(), np.tile(np.arange(n), (1, 2, 1)))
+
+
+def test_recursive_filter_flags_duplicates_and_range():
+    n, levels, g, d = 256, 3, 8, 64
+    arrs = _rand_inputs(4, 1, 1, n, g, d, "bf16")
+    ks = [8, 8, 6, 4]
+    dev = to_device(arrs, "bf16")
+    dims = bd.make_dims(dev["Q"], dev["Kp"], levels)
+    ws = bd.alloc_workspace(dims, ks, dev["Q"].device)
+    dup = torch.tensor([[[3, 3, 5, 7]]], dtype=torch.int32, device="cuda")
+    bd.recursive_filter(dev["Q"], dev["Kp"], dup, levels, ks, ws)
+    assert bd.read_device_status(ws) & bd.DEV_DUP_INDEX
+    bd.clear_device_status(ws)
+    bad = torch.tensor([[[3, 99, 5, -1]]], dtype=torch.int32, device="cuda")
+    out = bd.recursive_filter(dev["Q"], dev["Kp"], bad, levels, ks, ws).cpu().numpy()
+    assert bd.read_device_status(ws) & bd.DEV_BAD_INDEX
+    assert ((out >= 0) & (out < n)).all()
+
+
+# ---------------------------------------------------- steps 4-5: attention
+
+@pytest.mark.parametrize("name", ["tiny", "llada8b_layer"])
+def test_attention_on_oracle_index_set(name):
+    cfg = wl.CONFIGS[name]
+    ks = cfg.k_per_level()
+    arrs = layer_inputs(name)
+    dev = to_device(arrs, cfg.dtype)
+    sel = np.stack([[wo.recursive_filter(arrs["Q"][b, h], arrs["Kp"][b, h], cfg.levels, ks)["idx"]
+                     for h in range(cfg.heads)] for b in range(cfg.batch)]).astype(np.int32)
+    dims = bd.make_dims(dev["Q"], dev["Kp"], cfg.levels)
+    ws = bd.alloc_workspace(dims, ks, dev["Q"].device)
+    out, lse = bd.sparse_gather_attn(dev["Q"], dev["Kp"], dev["Vp"], dev["Kg"], dev["Vg"],
+                                     torch.from_numpy(sel).cuda(), cfg.levels, ws, with_lse=True)
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    for b in range(cfg.batch):
+        for h in range(cfg.heads):
+            u = unit_inputs(arrs, b, h)
+            ro, rl = wo.sparse_attention(u["Q"], u["Kp"], u["Vp"], u["Kg"], u["Vg"], sel[b, h])
+            assert np.abs(out[b, h] - ro).max() <= OUT_ATOL
+            assert np.abs(lse[b, h] - rl).max() <= OUT_ATOL
+
+
+@pytest.mark.parametrize("budget,g,d,dtype", [(0, 32, 128, "bf16"), (1, 1, 64, "bf16"),
+                                              (37, 20, 128, "bf16"), (500, 64, 128, "bf16"),
+                                              (3000, 48, 64, "bf16"), (0, 7, 64, "f32"),
+                                              (77, 33, 128, "f32"), (1023, 64, 64, "f32")])
+def test_attention_edge_sizes(budget, g, d, dtype):
+    n = 4096
+    arrs = _rand_inputs(budget + g, 1, 2, n, g, d, dtype)
+    rng = np.random.default_rng(budget)
+    sel = np.stack([[np.sort(rng.choice(n, budget, replace=False)) for _ in range(2)]])
+    dev = to_device(arrs, dtype)
+    ws = bd.alloc_status_workspace(dev["Q"].device)
+    idx = torch.from_numpy(sel.astype(np.int32)).cuda() if budget else None
+    out, lse = bd.sparse_gather_attn(dev["Q"], dev["Kp"], dev["Vp"], dev["Kg"], dev["Vg"], idx,
+                                     2, ws, with_lse=True)
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    for h in range(2):
+        u = unit_inputs(arrs, 0, h)
+        ro, rl = wo.sparse_attention(u["Q"], u["Kp"], u["Vp"], u["Kg"], u["Vg"], sel[0, h])
+        assert np.abs(out[0, h] - ro).max() <= OUT_ATOL
+        assert np.abs(lse[0, h] - rl).max() <= OUT_ATOL
+    assert bd.read_device_status(ws) == 0
+
+
+def test_attention_skips_and_flags_bad_indices():
+    n, g, d = 512, 16, 128
+    arrs = _rand_inputs(8, 1, 1, n, g, d, "bf16")
+    dev = to_device(arrs, "bf16")
+    ws = bd.alloc_status_workspace(dev["Q"].device)
+    idx = torch.tensor([[[5, 9, -3, 700, 100, 101, 102, n]]], dtype=torch.int32, device="cuda")
+    out = bd.sparse_gather_attn(dev["Q"], dev["Kp"], dev["Vp"], dev["Kg"], dev["Vg"], idx, 2, ws)
+    assert bd.read_device_status(ws) & bd.DEV_BAD_INDEX
+    u = unit_inputs(arrs, 0, 0)
+    ro, _ = wo.sparse_attention(u["Q"], u["Kp"], u["Vp"], u["Kg"], u["Vg"], [5, 9, 100, 101, 102])
+    assert np.abs(out.cpu().numpy()[0, 0] - ro).max() <= OUT_ATOL
+
+
+def test_full_budget_is_full_attention():
+    n, levels, g, d = 512, 3, 32, 128
+    arrs = _rand_inputs(11, 1, 2, n, g, d, "bf16")
+    ks = [n] + [n >> j for j in range(1, levels + 1)]
+    out, lse, idx, status = run_step(to_device(arrs, "bf16"), levels, ks)
+    assert status == 0
+    for h in range(2):
+        np.testing.assert_array_equal(idx[0, h].cpu().numpy(), np.arange(n))
+        u = unit_inputs(arrs, 0, h)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(u["Q"]).double()[None, None],
+            torch.from_numpy(np.concatenate([u["Kp"], u["Kg"]])).double()[None, None],
+            torch.from_numpy(np.concatenate([u["Vp"], u["Vg"]])).double()[None, None])[0, 0]
+        assert np.abs(out[0, h].cpu().numpy() - ref.numpy()).max() <= OUT_ATOL
+
+
+# ---------------------------------------------------------- whole step, configs
+
+def _step_config(name, units=None, layer=0):
+    cfg = wl.CONFIGS[name]
+    ks = cfg.k_per_level()
+    arrs = layer_inputs(name, layer)
+    dev = to_device(arrs, cfg.dtype)
+    out, lse, idx, status = run_step(dev, cfg.levels, ks)
+    assert status == 0
+    out, lse, idx = out.cpu().numpy(), lse.cpu().numpy(), idx.cpu().numpy()
+    del dev
+    torch.cuda.empty_cache()
+    units = units or [(b, h) for b in range(cfg.batch) for h in range(cfg.heads)]
+    kinds = []
+    for b, h in units:
+        kinds.append(compare_step_unit(arrs, b, h, cfg.levels, ks, idx[b, h], out[b, h], lse[b, h]))
+    # Every unit: a valid index set.
+    for b in range(cfg.batch):
+        for h in range(cfg.heads):
+            check_index_set(idx[b, h], cfg.n_prompt, ks[0])
+    return kinds
+
+
+@pytest.mark.parametrize("name", ["tiny", "llada8b_layer"])
+def test_step_matches_oracle_all_units(name):
+    kinds = _step_config(name)
+    assert kinds.count("exact") >= len(kinds) // 2
+
+
+def test_step_long_prompt_sampled():
+    kinds = _step_config("long_prompt", units=[(0, 0), (0, 13), (0, 31)])
+    assert len(kinds) == 3
+
+
+def test_step_full_step_layer_sampled():
+    # The 32 layers of the full step share one launch shape; layer 0 and 31 are checked.
+    for layer in (0, 31):
+        kinds = _step_config("full_step", units=[(0, 0), (0, 17)], layer=layer)
+        assert len(kinds) == 2
+
+
+@pytest.mark.parametrize("tag", ["1pct", "2p5pct", "5pct", "10pct"])
+def test_step_batched_long_sampled(tag):
+    kinds = _step_config(f"batched_long_{tag}", units=[(0, 5), (1, 30)])
+    assert len(kinds) == 2
+
+
+def test_step_is_deterministic():
+    cfg = wl.CONFIGS["llada8b_layer"]
+    dev = to_device(layer_inputs("llada8b_layer"), cfg.dtype)
+    a = run_step(dev, cfg.levels, cfg.k_per_level())
+    b = run_step(dev, cfg.levels, cfg.k_per_level())
+    assert torch.equal(a[0], b[0]) and torch.equal(a[2], b[2]) and torch.equal(a[1], b[1])
+
+
+def test_step_host_matches_device_step():
+    cfg = wl.CONFIGS["llada8b_layer"]
+    ks = cfg.k_per_level()
+    arrs = layer_inputs("llada8b_layer")
+    dev = to_device(arrs, cfg.dtype)
+    ref = run_step(dev, cfg.levels, ks)[0]
+    host = {k: v.cpu().pin_memory() for k, v in dev.items()}
+    host["O"] = torch.empty(ref.shape, dtype=torch.float32).pin_memory()
+    stage = {k: torch.empty_like(v) for k, v in dev.items()}
+    stage["O"] = torch.empty_like(ref)
+    dims = bd.make_dims(dev["Q"], dev["Kp"], cfg.levels)
+    ws = bd.alloc_workspace(dims, ks, dev["Q"].device)
+    bd.step_host(dims, host, ks, stage, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(host["O"], ref.cpu())

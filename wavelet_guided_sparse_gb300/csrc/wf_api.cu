@@ -1,0 +1,321 @@
+// C ABI of the WaveFilter KV-filtering path: argument validation, workspace
+// layout and the step driver.  Kernels live in wf_dwt.cu (step 1), wf_score.cu
+// (step 2), wf_filter.cu (step 3) and wf_attn.cu (steps 4-5).
+//
+// Every entry point validates on the host first and enqueues nothing on a
+// validation error.  Nothing here allocates device memory or synchronises,
+// except wf_read_device_status(), which is documented as synchronising.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "wavefilter.h"
+#include "wf_internal.h"
+
+namespace {
+
+using wf::LaunchDims;
+
+constexpr size_t kAlign = 256;
+constexpr size_t kHeaderBytes = 256;  // status word + padding
+
+size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t elem_bytes(int dtype) { return dtype == WF_BF16 ? 2 : 4; }
+
+int check_dims(const wf_dims* d, LaunchDims* ld) {
+  if (d == nullptr) return WF_ERR_NULL;
+  if (d->dtype != WF_BF16 && d->dtype != WF_F32) return WF_ERR_UNSUPPORTED;
+  if (d->head_dim != 64 && d->head_dim != 128) return WF_ERR_UNSUPPORTED;
+  if (d->batch < 1 || d->heads < 1 || d->n_prompt < 1 || d->n_gen < 1) return WF_ERR_SHAPE;
+  if (d->levels < 1 || d->levels > WF_MAX_LEVELS) return WF_ERR_SHAPE;
+  if (d->n_gen > WF_MAX_GEN) return WF_ERR_UNSUPPORTED;
+  if (d->n_prompt % (1 << d->levels) != 0) return WF_ERR_SHAPE;
+  const int64_t units = static_cast<int64_t>(d->batch) * d->heads;
+  if (units > 65535) return WF_ERR_UNSUPPORTED;  // one grid row per unit
+  ld->units = units;
+  ld->n_prompt = d->n_prompt;
+  ld->n_gen = d->n_gen;
+  ld->head_dim = d->head_dim;
+  ld->levels = d->levels;
+  ld->dtype = d->dtype;
+  return WF_OK;
+}
+
+// Per-level survivor counts: 1 <= k_L <= N_p/2^L, 1 <= k_j <= 2 k_{j+1}.
+int check_k(const LaunchDims& ld, const int32_t* k) {
+  if (k == nullptr) return WF_ERR_NULL;
+  const int P = ld.n_prompt >> ld.levels;
+  if (k[ld.levels] < 1 || k[ld.levels] > P) return WF_ERR_SHAPE;
+  for (int j = ld.levels - 1; j >= 0; --j)
+    if (k[j] < 1 || static_cast<int64_t>(k[j]) > 2 * static_cast<int64_t>(k[j + 1]))
+      return WF_ERR_SHAPE;
+  return WF_OK;
+}
+
+// Workspace layout shared by every entry point: [status header | A_L | S_L | S | t].
+struct Layout {
+  size_t al, idx_l, idx, t, total;
+};
+
+Layout layout(const LaunchDims& ld, const int32_t* k, const wf::FilterPlan* fp) {
+  Layout L;
+  size_t o = kHeaderBytes;
+  L.al = o;
+  o = align_up(o + sizeof(float) * ld.units * (ld.n_prompt >> ld.levels) * ld.head_dim);
+  L.idx_l = o;
+  o = align_up(o + sizeof(int32_t) * ld.units * (k ? k[ld.levels] : 0));
+  L.idx = o;
+  o = align_up(o + sizeof(int32_t) * ld.units * (k ? k[0] : 0));
+  L.t = o;
+  o = align_up(o + (fp ? fp->t_bytes : 0));
+  L.total = o;
+  return L;
+}
+
+int32_t* status_word(void* ws) { return static_cast<int32_t*>(ws); }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? WF_OK : WF_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* wf_status_string(int status) {
+  switch (status) {
+    case WF_OK: return "ok";
+    case WF_ERR_NULL: return "a required pointer is NULL";
+    case WF_ERR_SHAPE: return "inconsistent sizes or per-level k";
+    case WF_ERR_UNSUPPORTED: return "unsupported head_dim, dtype, n_gen or size";
+    case WF_ERR_WORKSPACE: return "workspace too small";
+    case WF_ERR_CUDA: return "CUDA launch or query failed";
+    case WF_ERR_DEVICE_CHECK: return "device-side check failed";
+    case WF_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
+    default: return "unknown status";
+  }
+}
+
+int wf_default_k_per_level(int32_t n_prompt, int32_t levels, int32_t budget, int32_t* k_out) {
+  if (k_out == nullptr) return WF_ERR_NULL;
+  if (levels < 1 || levels > WF_MAX_LEVELS || budget < 1 || n_prompt < 1) return WF_ERR_SHAPE;
+  if (n_prompt % (1 << levels) != 0) return WF_ERR_SHAPE;
+  const int64_t top = n_prompt >> levels;
+  int64_t kl = (2 * static_cast<int64_t>(budget) + (1 << levels) - 1) >> levels;
+  if (kl > top) kl = top;
+  if (kl < 1) kl = 1;
+  k_out[levels] = static_cast<int32_t>(kl);
+  for (int j = levels - 1; j >= 1; --j) {
+    const int64_t a = kl << (levels - j), b = n_prompt >> j;
+    k_out[j] = static_cast<int32_t>(a < b ? a : b);
+  }
+  k_out[0] = budget;
+  if (budget > 2 * static_cast<int64_t>(k_out[1 < levels ? 1 : levels])) return WF_ERR_SHAPE;
+  return WF_OK;
+}
+
+int wf_workspace_bytes(const wf_dims* dims, const int32_t* k_per_level, size_t* bytes) {
+  LaunchDims ld;
+  int st = check_dims(dims, &ld);
+  if (st != WF_OK) return st;
+  if (bytes == nullptr) return WF_ERR_NULL;
+  st = check_k(ld, k_per_level);
+  if (st != WF_OK) return st;
+  wf::FilterPlan fp;
+  if (!wf::plan_filter(ld, k_per_level, &fp)) return WF_ERR_UNSUPPORTED;
+  *bytes = layout(ld, k_per_level, &fp).total;
+  return WF_OK;
+}
+
+int wf_clear_device_status(void* workspace, size_t workspace_bytes, void* stream) {
+  if (workspace == nullptr) return WF_ERR_NULL;
+  if (workspace_bytes < kHeaderBytes) return WF_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(workspace, 0, sizeof(int32_t),
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+int wf_read_device_status(const void* workspace, size_t workspace_bytes, void* stream,
+                          int32_t* status_out) {
+  if (workspace == nullptr || status_out == nullptr) return WF_ERR_NULL;
+  if (workspace_bytes < kHeaderBytes) return WF_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return WF_ERR_CUDA;
+  *status_out = v;
+  return WF_OK;
+}
+
+int wf_dwt_lowpass(const wf_dims* dims, const void* Kp, float* AL, float* A_all, void* stream) {
+  LaunchDims ld;
+  int st = check_dims(dims, &ld);
+  if (st != WF_OK) return st;
+  if (Kp == nullptr || AL == nullptr) return WF_ERR_NULL;
+  if (!aligned16(Kp) || !aligned16(AL) || (A_all && !aligned16(A_all))) return WF_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = wf::launch_dwt_lowpass(ld, Kp, AL, ld.levels, s);
+  if (e == cudaSuccess && A_all != nullptr) {
+    // Test aid: every level j = 1..L, each from its own pass over Kp.
+    size_t off = 0;
+    for (int j = 1; j <= ld.levels && e == cudaSuccess; ++j) {
+      e = wf::launch_dwt_lowpass(ld, Kp, A_all + off, j, s);
+      off += static_cast<size_t>(ld.units) * (ld.n_prompt >> j) * ld.head_dim;
+    }
+  }
+  return cuda_status(e);
+}
+
+int wf_score_topk(const wf_dims* dims, const void* Q, const float* AL, int32_t k_L,
+                  int32_t* idx_L, float* scores_L, void* workspace, size_t workspace_bytes,
+                  void* stream) {
+  LaunchDims ld;
+  int st = check_dims(dims, &ld);
+  if (st != WF_OK) return st;
+  if (Q == nullptr || AL == nullptr || idx_L == nullptr || workspace == nullptr)
+    return WF_ERR_NULL;
+  if (!aligned16(Q) || !aligned16(AL) || !aligned16(idx_L) || !aligned16(workspace) ||
+      (scores_L && !aligned16(scores_L)))
+    return WF_ERR_ALIGNMENT;
+  if (k_L < 1 || k_L > (ld.n_prompt >> ld.levels)) return WF_ERR_SHAPE;
+  if (workspace_bytes < kHeaderBytes) return WF_ERR_WORKSPACE;
+  wf::ScorePlan sp;
+  if (!wf::plan_score(ld, &sp)) return WF_ERR_UNSUPPORTED;
+  return cuda_status(wf::launch_score_topk(ld, sp, Q, AL, k_L, idx_L, scores_L,
+                                           status_word(workspace),
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+int wf_recursive_filter(const wf_dims* dims, const void* Q, const void* Kp, const int32_t* idx_L,
+                        const int32_t* k_per_level, int32_t* idx, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  LaunchDims ld;
+  int st = check_dims(dims, &ld);
+  if (st != WF_OK) return st;
+  if (Q == nullptr || Kp == nullptr || idx_L == nullptr || idx == nullptr ||
+      workspace == nullptr)
+    return WF_ERR_NULL;
+  if (!aligned16(Q) || !aligned16(Kp) || !aligned16(idx_L) || !aligned16(idx) ||
+      !aligned16(workspace))
+    return WF_ERR_ALIGNMENT;
+  st = check_k(ld, k_per_level);
+  if (st != WF_OK) return st;
+  wf::FilterPlan fp;
+  if (!wf::plan_filter(ld, k_per_level, &fp)) return WF_ERR_UNSUPPORTED;
+  const Layout L = layout(ld, k_per_level, &fp);
+  if (workspace_bytes < L.total) return WF_ERR_WORKSPACE;
+  float* t_ws = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.t);
+  return cuda_status(wf::launch_recursive_filter(ld, fp, Q, Kp, idx_L, k_per_level, idx, t_ws,
+                                                 status_word(workspace),
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
+int wf_sparse_gather_attn(const wf_dims* dims, const void* Q, const void* Kp, const void* Vp,
+                          const void* Kg, const void* Vg, const int32_t* idx, int32_t budget,
+                          float* O, float* lse, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  LaunchDims ld;
+  int st = check_dims(dims, &ld);
+  if (st != WF_OK) return st;
+  if (Q == nullptr || Kp == nullptr || Vp == nullptr || Kg == nullptr || Vg == nullptr ||
+      O == nullptr || workspace == nullptr || (budget > 0 && idx == nullptr))
+    return WF_ERR_NULL;
+  if (!aligned16(Q) || !aligned16(Kp) || !aligned16(Vp) || !aligned16(Kg) || !aligned16(Vg) ||
+      !aligned16(O) || !aligned16(workspace) || (idx && !aligned16(idx)) ||
+      (lse && !aligned16(lse)))
+    return WF_ERR_ALIGNMENT;
+  if (budget < 0) return WF_ERR_SHAPE;
+  if (workspace_bytes < kHeaderBytes) return WF_ERR_WORKSPACE;
+  wf::AttnPlan ap;
+  if (!wf::plan_attn(ld, budget, &ap)) return WF_ERR_UNSUPPORTED;
+  return cuda_status(wf::launch_sparse_attn(ld, ap, Q, Kp, Vp, Kg, Vg, idx, budget, O, lse,
+                                            status_word(workspace),
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+int wf_step(const wf_dims* dims, const void* Q, const void* Kp, const void* Vp, const void* Kg,
+            const void* Vg, const int32_t* k_per_level, float* O, float* lse, int32_t* idx_out,
+            void* workspace, size_t workspace_bytes, void* stream) {
+  LaunchDims ld;
+  int st = check_dims(dims, &ld);
+  if (st != WF_OK) return st;
+  if (Q == nullptr || Kp == nullptr || Vp == nullptr || Kg == nullptr || Vg == nullptr ||
+      O == nullptr || workspace == nullptr)
+    return WF_ERR_NULL;
+  if (!aligned16(Q) || !aligned16(Kp) || !aligned16(Vp) || !aligned16(Kg) || !aligned16(Vg) ||
+      !aligned16(O) || !aligned16(workspace) || (lse && !aligned16(lse)) ||
+      (idx_out && !aligned16(idx_out)))
+    return WF_ERR_ALIGNMENT;
+  st = check_k(ld, k_per_level);
+  if (st != WF_OK) return st;
+  wf::FilterPlan fp;
+  wf::ScorePlan sp;
+  wf::AttnPlan ap;
+  const int budget = k_per_level[0];
+  if (!wf::plan_filter(ld, k_per_level, &fp) || !wf::plan_score(ld, &sp) ||
+      !wf::plan_attn(ld, budget, &ap))
+    return WF_ERR_UNSUPPORTED;
+  const Layout L = layout(ld, k_per_level, &fp);
+  if (workspace_bytes < L.total) return WF_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  float* al = reinterpret_cast<float*>(ws + L.al);
+  int32_t* idx_l = reinterpret_cast<int32_t*>(ws + L.idx_l);
+  int32_t* idx = idx_out != nullptr ? idx_out : reinterpret_cast<int32_t*>(ws + L.idx);
+  float* t_ws = reinterpret_cast<float*>(ws + L.t);
+  int32_t* status = status_word(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = wf::launch_dwt_lowpass(ld, Kp, al, ld.levels, s);
+  if (e == cudaSuccess)
+    e = wf::launch_score_topk(ld, sp, Q, al, k_per_level[ld.levels], idx_l, nullptr, status, s);
+  if (e == cudaSuccess)
+    e = wf::launch_recursive_filter(ld, fp, Q, Kp, idx_l, k_per_level, idx, t_ws, status, s);
+  if (e == cudaSuccess)
+    e = wf::launch_sparse_attn(ld, ap, Q, Kp, Vp, Kg, Vg, idx, budget, O, lse, status, s);
+  return cuda_status(e);
+}
+
+int wf_step_host(const wf_dims* dims, const void* h_Q, const void* h_Kp, const void* h_Vp,
+                 const void* h_Kg, const void* h_Vg, const int32_t* k_per_level, float* h_O,
+                 float* h_lse, void* d_Q, void* d_Kp, void* d_Vp, void* d_Kg, void* d_Vg,
+                 float* d_O, float* d_lse, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  LaunchDims ld;
+  int st = check_dims(dims, &ld);
+  if (st != WF_OK) return st;
+  if (h_Q == nullptr || h_Kp == nullptr || h_Vp == nullptr || h_Kg == nullptr ||
+      h_Vg == nullptr || h_O == nullptr || d_Q == nullptr || d_Kp == nullptr ||
+      d_Vp == nullptr || d_Kg == nullptr || d_Vg == nullptr || d_O == nullptr)
+    return WF_ERR_NULL;
+  st = check_k(ld, k_per_level);
+  if (st != WF_OK) return st;
+  const size_t e = elem_bytes(ld.dtype);
+  const size_t gen_bytes = static_cast<size_t>(ld.units) * ld.n_gen * ld.head_dim * e;
+  const size_t prompt_bytes = static_cast<size_t>(ld.units) * ld.n_prompt * ld.head_dim * e;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Validate the device side before any copy is enqueued.
+  size_t need = 0;
+  st = wf_workspace_bytes(dims, k_per_level, &need);
+  if (st != WF_OK) return st;
+  if (workspace == nullptr) return WF_ERR_NULL;
+  if (workspace_bytes < need) return WF_ERR_WORKSPACE;
+  cudaError_t ce = cudaMemcpyAsync(d_Q, h_Q, gen_bytes, cudaMemcpyHostToDevice, s);
+  if (ce == cudaSuccess) ce = cudaMemcpyAsync(d_Kp, h_Kp, prompt_bytes, cudaMemcpyHostToDevice, s);
+  if (ce == cudaSuccess) ce = cudaMemcpyAsync(d_Vp, h_Vp, prompt_bytes, cudaMemcpyHostToDevice, s);
+  if (ce == cudaSuccess) ce = cudaMemcpyAsync(d_Kg, h_Kg, gen_bytes, cudaMemcpyHostToDevice, s);
+  if (ce == cudaSuccess) ce = cudaMemcpyAsync(d_Vg, h_Vg, gen_bytes, cudaMemcpyHostToDevice, s);
+  if (ce != cudaSuccess) return WF_ERR_CUDA;
+  const bool want_lse = h_lse != nullptr && d_lse != nullptr;
+  st = wf_step(dims, d_Q, d_Kp, d_Vp, d_Kg, d_Vg, k_per_level, d_O, want_lse ? d_lse : nullptr,
+               nullptr, workspace, workspace_bytes, stream);
+  if (st != WF_OK) return st;
+  const size_t o_bytes = sizeof(float) * ld.units * ld.n_gen * ld.head_dim;
+  ce = cudaMemcpyAsync(h_O, d_O, o_bytes, cudaMemcpyDeviceToHost, s);
+  if (ce == cudaSuccess && want_lse)
+    ce = cudaMemcpyAsync(h_lse, d_lse, sizeof(float) * ld.units * ld.n_gen,
+                         cudaMemcpyDeviceToHost, s);
+  return cuda_status(ce);
+}
+
+}  // extern "C"

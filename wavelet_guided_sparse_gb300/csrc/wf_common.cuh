@@ -1,0 +1,317 @@
+// Device helpers shared by the WaveFilter kernels (sm_103a).
+//
+// Contents: 16-byte vector loads with bf16 -> fp32 widening, warp/block scans,
+// thread-block-cluster helpers (DSMEM), mbarrier + bulk-copy (TMA engine)
+// helpers with bounded waits, and the cluster-wide exact Top-K used by the
+// coarse selection and every recursive-filtering level.
+#pragma once
+
+#include <cooperative_groups.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "wavefilter.h"
+
+namespace wf {
+
+namespace cg = cooperative_groups;
+
+constexpr int kThreads = 256;  // every kernel of this library uses 256-thread CTAs
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxCluster = 8;
+// Bounded waits: an mbarrier that has not completed after this many polls
+// sets WF_DEV_WAIT_TIMEOUT and the CTA gives up instead of spinning forever.
+constexpr uint32_t kWaitPolls = 1u << 24;
+
+// ---------------------------------------------------------------- status word
+__device__ __forceinline__ void raise_flag(int32_t* status, int code) {
+  if (status != nullptr) atomicOr(status, code);
+}
+
+// ------------------------------------------------------------------ loads
+template <typename T>
+struct Elem;
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr int kPer16B = 8;
+};
+template <>
+struct Elem<float> {
+  static constexpr int kPer16B = 4;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Loads 16 bytes (read-only path) and widens them to fp32.
+__device__ __forceinline__ void load16_f32(const __nv_bfloat16* p, float* f) {
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+  f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+  f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+  f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+  f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+__device__ __forceinline__ void load16_f32(const float* p, float* f) {
+  const float4 v = __ldg(reinterpret_cast<const float4*>(p));
+  f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+}
+__device__ __forceinline__ uint4 ldg16(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ void widen16(const uint4& v, const __nv_bfloat16*, float* f) {
+  f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+  f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+  f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+  f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+__device__ __forceinline__ void widen16(const uint4& v, const float*, float* f) {
+  f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+  f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+}
+
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f32(float x) { return x; }
+
+// ------------------------------------------------------------------ reductions
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Inclusive prefix sum over the warp.
+__device__ __forceinline__ int warp_incl_scan(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+  }
+  return v;
+}
+
+// Block-wide exclusive scan of one int per thread; returns the exclusive
+// prefix and writes the block total to *total.  `scratch` holds kWarps + 1
+// ints.  Contains three __syncthreads(), so back-to-back calls may reuse
+// the same scratch.
+__device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int incl = warp_incl_scan(v);
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kWarps ? scratch[lane] : 0;
+    const int wi = warp_incl_scan(w);
+    if (lane < kWarps) scratch[lane] = wi - w;
+    if (lane == kWarps - 1) scratch[kWarps] = wi;
+  }
+  __syncthreads();
+  const int excl = scratch[warp] + incl - v;
+  *total = scratch[kWarps];
+  __syncthreads();
+  return excl;
+}
+
+// ------------------------------------------------------------------ shared memory
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ------------------------------------------------------------------ mbarrier + bulk copy
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on an mbarrier phase.  Returns false (and raises
+// WF_DEV_WAIT_TIMEOUT) if the phase did not complete within kWaitPolls polls.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  int32_t* status) {
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+  }
+  raise_flag(status, WF_DEV_WAIT_TIMEOUT);
+  return false;
+}
+// One bulk global -> shared copy through the TMA engine; completion is
+// signalled on `bar` as transaction bytes.  dst, src and bytes must be
+// multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ------------------------------------------------------------------ cluster Top-K
+//
+// Exact selection of the k largest 32-bit keys spread over the CTAs of a
+// cluster.  Candidates live in each CTA's shared memory in ascending
+// position order, and every position held by rank r is below every position
+// held by rank r+1, so "lower position wins a tie" is "lower rank, then lower
+// local index wins".  Keys are the IEEE bit patterns of non-negative floats,
+// whose unsigned order equals their numeric order.
+//
+// Three radix rounds (11, 11, 10 bits, most significant first) find the k-th
+// largest key T; every key > T is taken, plus the first (k - #{key > T}) keys
+// equal to T in (rank, index) order.  Per-CTA histograms are summed over the
+// cluster through DSMEM.
+struct TopkSmem {
+  uint32_t hist[2][2048];  // double-buffered digit histograms (read by peers)
+  uint32_t total[2048];    // cluster-summed histogram of the current round
+  int32_t cnt[2];          // [0] = local #{key > T}, [1] = local #{key == T}
+  int32_t scan[kWarps + 1];
+  int32_t bcast[4];
+};
+
+struct TopkResult {
+  int local_taken;  // selected candidates in this CTA
+  int offset;       // selected candidates in lower ranks
+};
+
+// Marks take[i] = 1 for selected local candidates (i < n).  Must be called
+// by every thread of every CTA of the cluster (it contains cluster barriers).
+__device__ inline TopkResult cluster_topk(const uint32_t* keys, int n, int k, uint8_t* take,
+                                          TopkSmem& sm) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int tid = threadIdx.x;
+  const int nranks = static_cast<int>(cluster.num_blocks());
+  const int me = static_cast<int>(cluster.block_rank());
+  uint32_t prefix = 0, pmask = 0;
+  int need = k;
+#pragma unroll 1
+  for (int round = 0; round < 3; ++round) {
+    const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
+    const int nb = round == 2 ? 1024 : 2048;
+    uint32_t* hist = sm.hist[round & 1];
+    for (int b = tid; b < nb; b += kThreads) hist[b] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kThreads) {
+      const uint32_t key = keys[i];
+      if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
+    }
+    cluster.sync();
+    for (int b = tid; b < nb; b += kThreads) {
+      uint32_t t = 0;
+      for (int r = 0; r < nranks; ++r) t += cluster.map_shared_rank(hist, r)[b];
+      sm.total[b] = t;
+    }
+    __syncthreads();
+    // Find the digit d* with #{digit > d*} < need <= #{digit >= d*}.
+    // Each thread owns nb / kThreads consecutive bins (8 or 4); bins are
+    // scanned from the top through an exclusive block scan of reversed owners.
+    const int per = nb / kThreads;
+    const int owner = kThreads - 1 - tid;  // thread 0 owns the highest bins
+    int mine = 0;
+    for (int b = 0; b < per; ++b) mine += static_cast<int>(sm.total[owner * per + b]);
+    int tot;
+    const int above_owner = block_excl_scan(mine, sm.scan, &tot);  // bins above this owner
+    if (above_owner < need && above_owner + mine >= need) {
+      int acc = above_owner;
+      for (int b = per - 1; b >= 0; --b) {
+        const int c = static_cast<int>(sm.total[owner * per + b]);
+        if (acc + c >= need) {
+          sm.bcast[0] = owner * per + b;
+          sm.bcast[1] = acc;
+          break;
+        }
+        acc += c;
+      }
+    }
+    __syncthreads();
+    const uint32_t digit = static_cast<uint32_t>(sm.bcast[0]);
+    need -= sm.bcast[1];
+    prefix |= digit << shift;
+    pmask |= static_cast<uint32_t>(nb - 1) << shift;
+    __syncthreads();
+  }
+  const uint32_t thr = prefix;
+  // Local counts of keys above and equal to the threshold.
+  int gt = 0, eq = 0;
+  for (int i = tid; i < n; i += kThreads) {
+    gt += keys[i] > thr;
+    eq += keys[i] == thr;
+  }
+  int tot_gt, tot_eq;
+  (void)block_excl_scan(gt, sm.scan, &tot_gt);
+  (void)block_excl_scan(eq, sm.scan, &tot_eq);
+  if (tid == 0) {
+    sm.cnt[0] = tot_gt;
+    sm.cnt[1] = tot_eq;
+  }
+  cluster.sync();
+  // Tie quota of every rank, in rank order; offsets of lower ranks.
+  int quota_me = 0, offset = 0, ties_before = 0;
+  for (int r = 0; r < nranks; ++r) {
+    const int32_t* c = cluster.map_shared_rank(sm.cnt, r);
+    const int g = c[0], e = c[1];
+    int q = need - ties_before;
+    q = q < 0 ? 0 : (q > e ? e : q);
+    if (r < me) offset += g + q;
+    if (r == me) quota_me = q;
+    ties_before += e;
+  }
+  // Mark: key > T, or key == T among the first quota_me ties (index order).
+  int carry = 0;
+  for (int base = 0; base < n; base += kThreads) {
+    const int i = base + tid;
+    const uint32_t key = i < n ? keys[i] : 0u;
+    const int is_eq = (i < n) && key == thr;
+    int tot;
+    const int before = block_excl_scan(is_eq, sm.scan, &tot);
+    if (i < n) take[i] = static_cast<uint8_t>(key > thr || (is_eq && carry + before < quota_me));
+    carry += tot;
+  }
+  return TopkResult{tot_gt + quota_me, offset};
+}
+
+// Stable compaction of the taken entries of two parallel int arrays.
+// Returns the new count.  Block-wide (contains __syncthreads()).
+__device__ inline int compact2(const int32_t* a_in, const int32_t* b_in, const uint8_t* take,
+                               int n, int32_t* a_out, int32_t* b_out, int32_t* scan) {
+  int carry = 0;
+  for (int base = 0; base < n; base += kThreads) {
+    const int i = base + threadIdx.x;
+    const int t = i < n ? take[i] : 0;
+    int tot;
+    const int pos = block_excl_scan(t, scan, &tot);
+    if (t) {
+      a_out[carry + pos] = a_in[i];
+      b_out[carry + pos] = b_in[i];
+    }
+    carry += tot;
+  }
+  __syncthreads();
+  return carry;
+}
+
+}  // namespace wf

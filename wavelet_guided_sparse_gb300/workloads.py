@@ -204,13 +204,21 @@ def generate_unit(cfg: WorkloadConfig, seq: int, layer: int, head: int) -> Dict[
     }
 
 
+def _unit_job(args):
+    cfg, s, layer, h = args
+    return generate_unit(cfg, s, layer, h)
+
+
 def generate_layer(cfg: WorkloadConfig, layer: int = 0,
                    seqs: Optional[Sequence[int]] = None,
-                   heads: Optional[Sequence[int]] = None) -> Dict[str, np.ndarray]:
+                   heads: Optional[Sequence[int]] = None,
+                   workers: int = 0) -> Dict[str, np.ndarray]:
     """Stack units of one layer into [b, H, rows, d] float32 arrays.
 
     ``seqs`` / ``heads`` select a subset (default: all); a unit's values do
-    not depend on which other units are generated with it.
+    not depend on which other units are generated with it.  ``workers`` > 1
+    draws units in a spawn-started process pool (safe after CUDA is
+    initialised in the parent).
     """
     seqs = list(range(cfg.batch)) if seqs is None else list(seqs)
     heads = list(range(cfg.heads)) if heads is None else list(heads)
@@ -219,9 +227,21 @@ def generate_layer(cfg: WorkloadConfig, layer: int = 0,
               "Kg": cfg.n_gen, "Vg": cfg.n_gen}
     for name, rows in shapes.items():
         out[name] = np.empty((len(seqs), len(heads), rows, cfg.head_dim), dtype=np.float32)
-    for bi, s in enumerate(seqs):
-        for hi, h in enumerate(heads):
-            unit = generate_unit(cfg, s, layer, h)
-            for name in shapes:
-                out[name][bi, hi] = unit[name]
+    jobs = [(cfg, s, layer, h) for s in seqs for h in heads]
+    if workers and workers > 1 and len(jobs) > 1:
+        import concurrent.futures
+        import multiprocessing
+        ctx = multiprocessing.get_context("spawn")
+        with concurrent.futures.ProcessPoolExecutor(max_workers=workers, mp_context=ctx) as pool:
+            units = pool.map(_unit_job, jobs)
+            for i, unit in enumerate(units):
+                bi, hi = divmod(i, len(heads))
+                for name in shapes:
+                    out[name][bi, hi] = unit[name]
+        return out
+    for i, job in enumerate(jobs):
+        unit = _unit_job(job)
+        bi, hi = divmod(i, len(heads))
+        for name in shapes:
+            out[name][bi, hi] = unit[name]
     return out
