@@ -93,6 +93,10 @@ typedef struct {
 /* Human-readable name of a status code (static string, never NULL). */
 const char* wf_status_string(int status);
 
+/* Name and description of the last CUDA error that made an entry point of
+ * this thread return WF_ERR_CUDA (thread-local; "no error" initially). */
+const char* wf_last_error_string(void);
+
 /* Default per-level survivor counts (host helper; not on the device path).
  * k_out[j], j = 0..levels: k_L = ceil(2·budget / 2^L) capped at N_p/2^L,
  * k_j = min(2^(L-j)·k_L, N_p/2^j) for 0 < j < L, k_0 = budget.

@@ -25,7 +25,7 @@ DEV_BAD_INDEX, DEV_DUP_INDEX, DEV_WAIT_TIMEOUT = 1, 2, 4
 MAX_LEVELS = 12
 
 # Every symbol the header declares (checked by the host tests).
-EXPORTS = ("wf_status_string", "wf_default_k_per_level", "wf_workspace_bytes",
+EXPORTS = ("wf_status_string", "wf_last_error_string", "wf_default_k_per_level", "wf_workspace_bytes",
            "wf_clear_device_status", "wf_read_device_status", "wf_dwt_lowpass",
            "wf_score_topk", "wf_recursive_filter", "wf_sparse_gather_attn", "wf_step",
            "wf_step_host")
@@ -53,6 +53,7 @@ _DIMSP = ctypes.POINTER(Dims)
 
 _SIGS = {
     "wf_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "wf_last_error_string": (ctypes.c_char_p, []),
     "wf_default_k_per_level": (ctypes.c_int, [_i32, _i32, _i32, _i32p]),
     "wf_workspace_bytes": (ctypes.c_int, [_DIMSP, _i32p, ctypes.POINTER(_sz)]),
     "wf_clear_device_status": (ctypes.c_int, [_vp, _sz, _vp]),
@@ -87,7 +88,10 @@ def lib() -> ctypes.CDLL:
 
 def _check(fn: str, status: int) -> None:
     if status != WF_OK:
-        raise WfError(fn, status)
+        err = WfError(fn, status)
+        if status == 5:
+            err.args = (f"{err.args[0]} ({lib().wf_last_error_string().decode()})",)
+        raise err
 
 
 def _ptr(t: Optional[torch.Tensor]):

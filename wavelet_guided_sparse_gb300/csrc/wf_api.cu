@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 
 #include "wavefilter.h"
@@ -78,11 +79,26 @@ Layout layout(const LaunchDims& ld, const int32_t* k, const wf::FilterPlan* fp) 
 
 int32_t* status_word(void* ws) { return static_cast<int32_t*>(ws); }
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? WF_OK : WF_ERR_CUDA; }
+thread_local char g_last_error[256] = "no error";
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return WF_OK;
+  wf::note_cuda_error(e);
+  return WF_ERR_CUDA;
+}
 
 }  // namespace
 
+namespace wf {
+void note_cuda_error(cudaError_t e) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
+                cudaGetErrorString(e));
+}
+}  // namespace wf
+
 extern "C" {
+
+const char* wf_last_error_string(void) { return g_last_error; }
 
 const char* wf_status_string(int status) {
   switch (status) {

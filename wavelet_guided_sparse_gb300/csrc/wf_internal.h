@@ -65,10 +65,15 @@ cudaError_t launch_sparse_attn(const LaunchDims& ld, const AttnPlan& plan, const
                                const int32_t* idx, int budget, float* o, float* lse,
                                int32_t* status, cudaStream_t stream);
 
-// Largest dynamic shared memory a CTA may use on sm_103a.
-constexpr size_t kMaxSmem = 227 * 1024;
+// Dynamic shared memory the planners allow per CTA (the sm_103a opt-in limit
+// is 227 KB; a little is left for static shared memory).
+constexpr size_t kMaxSmem = 225 * 1024;
 
-// Raises a kernel's dynamic shared-memory limit to kMaxSmem, once per device.
+// Records the last CUDA error of this thread for wf_last_error_string().
+void note_cuda_error(cudaError_t e);
+
+// Raises a kernel's dynamic shared-memory limit to the device's opt-in
+// maximum minus the kernel's static shared memory, once per device.
 template <auto Kern>
 inline cudaError_t ensure_max_smem() {
   static std::atomic<uint64_t> done{0};
@@ -77,8 +82,14 @@ inline cudaError_t ensure_max_smem() {
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  int optin = 0;
+  e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, Kern);
+  if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kMaxSmem));
+                           optin - static_cast<int>(fa.sharedSizeBytes));
   if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
   return e;
 }
