@@ -1,0 +1,454 @@
+#!/usr/bin/env python
+"""Throughput of the WaveFilter per-layer, per-step KV-filtering path.
+
+One step = one pass of the whole path (Haar low-pass, coarse scoring + Top-K,
+recursive filtering, sparse gather + eq. (3) attention) over one layer of the
+workload, through the C ABI.  Metric: cached prompt tokens filtered+attended
+per second per layer-step (batch * layers * N_p per step), plus the achieved
+HBM bandwidth of the dominant kernel against the measured peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+  python bench.py --impl reference ...   # the float64 CPU oracle as the reference arm
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the units of the path are independent; there is no data-path collective)
+and rank 0 prints one JSON line with the whole-job throughput.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from wavelet_guided_sparse_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "cached prompt tokens filtered+attended/sec per layer-step; HBM GB/s vs peak"
+DEFAULT_CONFIG = "llada8b_layer"
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes (read + write) of one dwt_lowpass launch on the default workload,
+# from an ncu capture of the kernel source with this SHA-256 prefix; null
+# once the kernel has changed since the counters were taken.
+DWT_TRAFFIC = {"source_sha": None, "bytes_per_launch": None}
+
+
+def _rank_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def _workload_desc(cfg: wl.WorkloadConfig) -> str:
+    ks = cfg.k_per_level()
+    return (f"{cfg.name}: batch={cfg.batch}, layers=1 of {cfg.layers}, H={cfg.heads}, "
+            f"d={cfg.head_dim}, N_p={cfg.n_prompt}, G={cfg.n_gen}, {cfg.dtype}, "
+            f"Haar L={cfg.levels}, k_L={ks[-1]}, budget B={cfg.budget}")
+
+
+def _config_obj(cfg, extra=None):
+    ks = cfg.k_per_level()
+    obj = {"workload": _workload_desc(cfg), "batch": cfg.batch, "layers_per_step": 1,
+           "heads": cfg.heads, "head_dim": cfg.head_dim, "n_prompt": cfg.n_prompt,
+           "n_gen": cfg.n_gen, "levels": cfg.levels, "k_per_level": ks,
+           "budget": cfg.budget, "parallelism": "replicas"}
+    if extra:
+        obj.update(extra)
+    return obj
+
+
+def tokens_per_step(cfg) -> int:
+    return cfg.batch * 1 * cfg.n_prompt
+
+
+def path_bytes(cfg) -> dict:
+    """Algorithmic HBM bytes of one step (one layer), by stage."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    U, d, n, g, L = cfg.units_per_layer, cfg.head_dim, cfg.n_prompt, cfg.n_gen, cfg.levels
+    ks = cfg.k_per_level()
+    P, B = n >> L, ks[0]
+    rows = ks[L] << L
+    return {
+        "dwt": U * (n * d * e + P * d * 4),
+        "score": U * (P * d * 4 + g * d * e + ks[L] * 4),
+        "filter": U * (rows * d * e + g * d * e + ks[L] * 4 + B * 4),
+        "attn": U * (2 * B * d * e + 2 * g * d * e + g * d * e + B * 4 + g * d * 4),
+    }
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _dwt_traffic():
+    src = os.path.join(ROOT, "wavelet_guided_sparse_gb300", "csrc", "wf_dwt.cu")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    if DWT_TRAFFIC["source_sha"] == sha:
+        return DWT_TRAFFIC["bytes_per_launch"]
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the GPU works."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: str):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", device_index],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        # Samples under load: power above the midpoint of the observed range.
+        lo, hi = min(power), max(power)
+        loaded = [s for s, p in zip(sm, power) if p >= (lo + hi) / 2] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": hi}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def _oracle_unit(args):
+    q, kp, vp, kg, vg, levels, ks = args
+    import oracle.wavefilter_oracle as wo
+    wo.wavefilter_step(q, kp, vp, kg, vg, levels, ks)
+    return 1
+
+
+def _oracle_pool(workers):
+    import concurrent.futures
+    import multiprocessing
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    ctx = multiprocessing.get_context("spawn")
+    return concurrent.futures.ProcessPoolExecutor(max_workers=workers, mp_context=ctx)
+
+
+def _unit_jobs(arrs, cfg, units):
+    ks = cfg.k_per_level()
+    jobs = []
+    for u in units:
+        b, h = divmod(u, cfg.heads)
+        jobs.append((arrs["Q"][b, h], arrs["Kp"][b, h], arrs["Vp"][b, h], arrs["Kg"][b, h],
+                     arrs["Vg"][b, h], cfg.levels, ks))
+    return jobs
+
+
+def cpu_oracle_rate(arrs, cfg, budget_s: float, workers: int):
+    """Oracle tokens/s on a bounded sample: whole units, all host cores."""
+    U = cfg.units_per_layer
+    with _oracle_pool(workers) as pool:
+        list(pool.map(_oracle_unit, _unit_jobs(arrs, cfg, [0] * workers)))  # start workers
+        done, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < budget_s:
+            n = min(U, max(workers, 1))
+            units = [(done + i) % U for i in range(n)]
+            list(pool.map(_oracle_unit, _unit_jobs(arrs, cfg, units)))
+            done += n
+        elapsed = time.perf_counter() - t0
+    tokens = done / U * tokens_per_step(cfg)
+    return tokens / elapsed, done, elapsed
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args, cfg):
+    rank, world, _ = _rank_env()
+    if rank != 0:
+        return 0
+    arrs = wl.generate_layer(cfg, 0, workers=min(16, os.cpu_count() or 1))
+    workers = os.cpu_count() or 1
+    U = cfg.units_per_layer
+    # Size each step's sample so the whole run takes about two minutes.
+    with _oracle_pool(workers) as pool:
+        list(pool.map(_oracle_unit, _unit_jobs(arrs, cfg, [0] * workers)))
+        t0 = time.perf_counter()
+        list(pool.map(_oracle_unit, _unit_jobs(arrs, cfg, list(range(min(U, workers))))))
+        per_round = time.perf_counter() - t0
+        rounds = max(1, min(math.ceil(U / workers),
+                            int(120.0 / max(per_round * (args.steps + args.warmup), 1e-9))))
+        sample_units = min(U, rounds * workers)
+        for i in range(args.warmup):
+            list(pool.map(_oracle_unit, _unit_jobs(arrs, cfg, list(range(sample_units)))))
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            units = [(i * sample_units + j) % U for j in range(sample_units)]
+            list(pool.map(_oracle_unit, _unit_jobs(arrs, cfg, units)))
+        elapsed = time.perf_counter() - t0
+    frac = sample_units / U
+    value = args.steps * frac * tokens_per_step(cfg) / elapsed
+    sample = (f"{sample_units} of {U} (sequence, head) units per step, float64 numpy oracle, "
+              f"{workers} single-threaded worker processes")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed / args.steps * 1e3 / frac, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded generator with planted needle spans)",
+            "config": _config_obj(cfg),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": workers,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, cfg):
+    import torch
+    import torch.distributed as dist
+
+    from wavelet_guided_sparse_gb300 import binding as bd
+
+    rank, world, local = _rank_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    bd.lib()
+    ks = cfg.k_per_level()
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    arrs = wl.generate_layer(cfg, 0, workers=min(16, os.cpu_count() or 1))
+    base = {k: torch.from_numpy(v).to(device=dev, dtype=dt) for k, v in arrs.items()}
+    per_copy = sum(t.numel() * t.element_size() for t in base.values())
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    touched = path_bytes(cfg)
+    touched_bytes = sum(touched.values())
+    n_copies = max(2, math.ceil(4 * l2 / max(touched_bytes, 1)))
+    copies = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(n_copies - 1)]
+    dims = bd.make_dims(base["Q"], base["Kp"], cfg.levels)
+    ws = bd.alloc_workspace(dims, ks, dev)
+    out = torch.empty(base["Q"].shape, dtype=torch.float32, device=dev)
+    lse = torch.empty(base["Q"].shape[:3], dtype=torch.float32, device=dev)
+    idx = torch.empty((cfg.batch, cfg.heads, ks[0]), dtype=torch.int32, device=dev)
+
+    def step(c, stream=None):
+        bd.step(c["Q"], c["Kp"], c["Vp"], c["Kg"], c["Vg"], cfg.levels, ks, ws, out=out,
+                lse=lse, idx_out=idx, stream=stream)
+
+    for c in copies:  # eager pass (sets kernel attributes before capture)
+        step(c)
+    torch.cuda.synchronize()
+    graphs = []
+    cap_stream = torch.cuda.Stream(device=dev)
+    for c in copies:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap_stream):
+            step(c)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    smi_index = vis.split(",")[local] if vis else str(local)
+    sampler = ClockSampler(smi_index) if rank == 0 else None
+    time.sleep(0.3)
+
+    # ---- warm-up + timed region (CUDA graph of wf_step per input copy)
+    for i in range(args.warmup):
+        graphs[i % n_copies].replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        graphs[i % n_copies].replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        tt = torch.tensor([t_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_ms = float(tt.item())
+    ms_per_step = t_ms / args.steps
+    value = world * tokens_per_step(cfg) * args.steps / (t_ms / 1e3)
+
+    # ---- per-stage kernel durations (same launches, events on the launch stream)
+    stage_ms = {"dwt": [], "score": [], "filter": [], "attn": []}
+    al = torch.empty((cfg.batch, cfg.heads, cfg.n_prompt >> cfg.levels, cfg.head_dim),
+                     dtype=torch.float32, device=dev)
+    idx_l = torch.empty((cfg.batch, cfg.heads, ks[-1]), dtype=torch.int32, device=dev)
+    lib = bd.lib()
+    sp = bd._stream(stream)
+    karr = bd._k_array(ks)
+    n_stage_steps = max(args.steps, 20)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_stage_steps)]
+    for i in range(n_stage_steps):
+        c = copies[i % n_copies]
+        e = evs[i]
+        e[0].record(stream)
+        lib.wf_dwt_lowpass(bd.ctypes.byref(dims), bd._ptr(c["Kp"]), bd._ptr(al), None, sp)
+        e[1].record(stream)
+        lib.wf_score_topk(bd.ctypes.byref(dims), bd._ptr(c["Q"]), bd._ptr(al), ks[-1],
+                          bd._ptr(idx_l), None, bd._ptr(ws), ws.numel(), sp)
+        e[2].record(stream)
+        lib.wf_recursive_filter(bd.ctypes.byref(dims), bd._ptr(c["Q"]), bd._ptr(c["Kp"]),
+                                bd._ptr(idx_l), karr, bd._ptr(idx), bd._ptr(ws), ws.numel(), sp)
+        e[3].record(stream)
+        lib.wf_sparse_gather_attn(bd.ctypes.byref(dims), bd._ptr(c["Q"]), bd._ptr(c["Kp"]),
+                                  bd._ptr(c["Vp"]), bd._ptr(c["Kg"]), bd._ptr(c["Vg"]),
+                                  bd._ptr(idx), ks[0], bd._ptr(out), bd._ptr(lse), bd._ptr(ws),
+                                  ws.numel(), sp)
+        e[4].record(stream)
+    torch.cuda.synchronize()
+    for e in evs[3:]:  # the first launches include one-time effects
+        for j, name in enumerate(("dwt", "score", "filter", "attn")):
+            stage_ms[name].append(e[j].elapsed_time(e[j + 1]))
+    stage_us = {k: 1e3 * statistics.mean(v) for k, v in stage_ms.items()}
+
+    # ---- end to end through the host-buffer entry point (pinned host memory)
+    host = {k: v.cpu().pin_memory() for k, v in base.items()}
+    host["O"] = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    stage = {k: torch.empty_like(v) for k, v in base.items()}
+    stage["O"] = torch.empty_like(out)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in ("Q", "Kp", "Vp", "Kg", "Vg"))
+    d2h = host["O"].numel() * host["O"].element_size()
+    e2e_steps = max(10, min(args.steps, 200))
+    for _ in range(3):
+        bd.step_host(dims, host, ks, stage, ws, stream=stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        bd.step_host(dims, host, ks, stage, ws, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = world * tokens_per_step(cfg) * e2e_steps / (e2e_ms / 1e3)
+    clocks = sampler.stop() if sampler else None
+    status = bd.read_device_status(ws)
+
+    if rank != 0:
+        dist.barrier()
+        return 0
+    peak, peak_kind = _peaks()
+    dwt_bytes = touched["dwt"]
+    achieved = dwt_bytes / (stage_us["dwt"] * 1e-6) / 1e9
+    total_bytes = sum(touched.values())
+    cpu_rate, cpu_units, cpu_s = (None, 0, 0.0)
+    workers = os.cpu_count() or 1
+    if world == 1 and not args.no_cpu_baseline:
+        cpu_rate, cpu_units, cpu_s = cpu_oracle_rate(arrs, cfg, args.cpu_seconds, workers)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": cfg.dtype, "data": "synthetic (seeded generator with planted needle spans)",
+        "config": _config_obj(cfg, {
+            "l2": f"rotating {n_copies} device input copies ({n_copies * per_copy / 2**20:.0f} MiB,"
+                  f" {n_copies} x {touched_bytes / 2**20:.1f} MiB touched per step > "
+                  f"{l2 / 2**20:.0f} MiB L2)",
+            "timing": "CUDA events around K replays of one CUDA graph (wf_step) per copy"}),
+        "roofline": {"kernel": "dwt_lowpass_kernel", "bound": "hbm",
+                     "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "traffic": _dwt_traffic(),
+                     "algorithmic_bytes_per_launch": dwt_bytes,
+                     "launch_us": stage_us["dwt"]},
+        "path_roofline": {"bytes_per_step": total_bytes,
+                          "achieved": total_bytes / (ms_per_step * 1e-3) / 1e9,
+                          "peak": peak, "unit": "GB/s",
+                          "frac": total_bytes / (ms_per_step * 1e-3) / 1e9 / peak},
+        "stages_us": stage_us,
+        "cpu_baseline": None if cpu_rate is None else {
+            "value": cpu_rate, "unit": "tokens/s", "cores": workers, "kind": "oracle",
+            "sample": f"{cpu_units} (sequence, head) units of this workload in {cpu_s:.1f} s, "
+                      f"float64 numpy oracle, {workers} single-threaded worker processes"},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "entry_point": "wf_step_host (pinned host Q/Kp/Vp/Kg/Vg in, O out)"},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(wl.CONFIGS))
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    cfg = wl.CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

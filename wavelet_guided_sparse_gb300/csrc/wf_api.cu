@@ -1,6 +1,6 @@
 // C ABI of the WaveFilter KV-filtering path: argument validation, workspace
-// layout and the step driver.  Kernels live in wf_dwt.cu (step 1), wf_score.cu
-// (step 2), wf_filter.cu (step 3) and wf_attn.cu (steps 4-5).
+// layout and the step driver.  Kernels live in wf_dwt.cu (step 1) and
+// wf_path.cu (steps 2-5, one cluster kernel whose phases the entry points select).
 //
 // Every entry point validates on the host first and enqueues nothing on a
 // validation error.  Nothing here allocates device memory or synchronises,
@@ -62,7 +62,7 @@ struct Layout {
   size_t al, idx_l, idx, t, total;
 };
 
-Layout layout(const LaunchDims& ld, const int32_t* k, const wf::FilterPlan* fp) {
+Layout layout(const LaunchDims& ld, const int32_t* k, const wf::PathPlan* fp) {
   Layout L;
   size_t o = kHeaderBytes;
   L.al = o;
@@ -139,9 +139,15 @@ int wf_workspace_bytes(const wf_dims* dims, const int32_t* k_per_level, size_t* 
   if (bytes == nullptr) return WF_ERR_NULL;
   st = check_k(ld, k_per_level);
   if (st != WF_OK) return st;
-  wf::FilterPlan fp;
-  if (!wf::plan_filter(ld, k_per_level, &fp)) return WF_ERR_UNSUPPORTED;
-  *bytes = layout(ld, k_per_level, &fp).total;
+  const int sms = wf::device_sm_count();
+  wf::PathPlan all, filt;
+  if (!wf::plan_path(ld, wf::kPhaseAll, k_per_level, k_per_level[ld.levels], k_per_level[0], sms,
+                     &all) ||
+      !wf::plan_path(ld, wf::kPhaseFilter, k_per_level, k_per_level[ld.levels], k_per_level[0],
+                     sms, &filt))
+    return WF_ERR_UNSUPPORTED;
+  const wf::PathPlan& big = all.t_bytes >= filt.t_bytes ? all : filt;
+  *bytes = layout(ld, k_per_level, &big).total;
   return WF_OK;
 }
 
@@ -197,11 +203,17 @@ int wf_score_topk(const wf_dims* dims, const void* Q, const float* AL, int32_t k
     return WF_ERR_ALIGNMENT;
   if (k_L < 1 || k_L > (ld.n_prompt >> ld.levels)) return WF_ERR_SHAPE;
   if (workspace_bytes < kHeaderBytes) return WF_ERR_WORKSPACE;
-  wf::ScorePlan sp;
-  if (!wf::plan_score(ld, &sp)) return WF_ERR_UNSUPPORTED;
-  return cuda_status(wf::launch_score_topk(ld, sp, Q, AL, k_L, idx_L, scores_L,
-                                           status_word(workspace),
-                                           static_cast<cudaStream_t>(stream)));
+  wf::PathPlan plan;
+  if (!wf::plan_path(ld, wf::kPhaseScore, nullptr, k_L, 0, wf::device_sm_count(), &plan))
+    return WF_ERR_UNSUPPORTED;
+  wf::PathArgs a = {};
+  a.q = Q;
+  a.al = AL;
+  a.idx_l_out = idx_L;
+  a.scores_out = scores_L;
+  a.status = status_word(workspace);
+  a.k_l = k_L;
+  return cuda_status(wf::launch_path(ld, plan, a, static_cast<cudaStream_t>(stream)));
 }
 
 int wf_recursive_filter(const wf_dims* dims, const void* Q, const void* Kp, const int32_t* idx_L,
@@ -218,14 +230,23 @@ int wf_recursive_filter(const wf_dims* dims, const void* Q, const void* Kp, cons
     return WF_ERR_ALIGNMENT;
   st = check_k(ld, k_per_level);
   if (st != WF_OK) return st;
-  wf::FilterPlan fp;
-  if (!wf::plan_filter(ld, k_per_level, &fp)) return WF_ERR_UNSUPPORTED;
-  const Layout L = layout(ld, k_per_level, &fp);
+  wf::PathPlan plan;
+  if (!wf::plan_path(ld, wf::kPhaseFilter, k_per_level, k_per_level[ld.levels], k_per_level[0],
+                     wf::device_sm_count(), &plan))
+    return WF_ERR_UNSUPPORTED;
+  const Layout L = layout(ld, k_per_level, &plan);
   if (workspace_bytes < L.total) return WF_ERR_WORKSPACE;
-  float* t_ws = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.t);
-  return cuda_status(wf::launch_recursive_filter(ld, fp, Q, Kp, idx_L, k_per_level, idx, t_ws,
-                                                 status_word(workspace),
-                                                 static_cast<cudaStream_t>(stream)));
+  wf::PathArgs a = {};
+  a.q = Q;
+  a.kp = Kp;
+  a.idx_l_in = idx_L;
+  a.idx_out = idx;
+  a.status = status_word(workspace);
+  a.t_ws = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.t);
+  a.k = k_per_level;
+  a.k_l = k_per_level[ld.levels];
+  a.budget = k_per_level[0];
+  return cuda_status(wf::launch_path(ld, plan, a, static_cast<cudaStream_t>(stream)));
 }
 
 int wf_sparse_gather_attn(const wf_dims* dims, const void* Q, const void* Kp, const void* Vp,
@@ -244,11 +265,21 @@ int wf_sparse_gather_attn(const wf_dims* dims, const void* Q, const void* Kp, co
     return WF_ERR_ALIGNMENT;
   if (budget < 0) return WF_ERR_SHAPE;
   if (workspace_bytes < kHeaderBytes) return WF_ERR_WORKSPACE;
-  wf::AttnPlan ap;
-  if (!wf::plan_attn(ld, budget, &ap)) return WF_ERR_UNSUPPORTED;
-  return cuda_status(wf::launch_sparse_attn(ld, ap, Q, Kp, Vp, Kg, Vg, idx, budget, O, lse,
-                                            status_word(workspace),
-                                            static_cast<cudaStream_t>(stream)));
+  wf::PathPlan plan;
+  if (!wf::plan_path(ld, wf::kPhaseAttend, nullptr, 0, budget, wf::device_sm_count(), &plan))
+    return WF_ERR_UNSUPPORTED;
+  wf::PathArgs a = {};
+  a.q = Q;
+  a.kp = Kp;
+  a.vp = Vp;
+  a.kg = Kg;
+  a.vg = Vg;
+  a.idx_in = idx;
+  a.o = O;
+  a.lse = lse;
+  a.status = status_word(workspace);
+  a.budget = budget;
+  return cuda_status(wf::launch_path(ld, plan, a, static_cast<cudaStream_t>(stream)));
 }
 
 int wf_step(const wf_dims* dims, const void* Q, const void* Kp, const void* Vp, const void* Kg,
@@ -266,30 +297,34 @@ int wf_step(const wf_dims* dims, const void* Q, const void* Kp, const void* Vp, 
     return WF_ERR_ALIGNMENT;
   st = check_k(ld, k_per_level);
   if (st != WF_OK) return st;
-  wf::FilterPlan fp;
-  wf::ScorePlan sp;
-  wf::AttnPlan ap;
   const int budget = k_per_level[0];
-  if (!wf::plan_filter(ld, k_per_level, &fp) || !wf::plan_score(ld, &sp) ||
-      !wf::plan_attn(ld, budget, &ap))
+  wf::PathPlan plan;
+  if (!wf::plan_path(ld, wf::kPhaseAll, k_per_level, k_per_level[ld.levels], budget,
+                     wf::device_sm_count(), &plan))
     return WF_ERR_UNSUPPORTED;
-  const Layout L = layout(ld, k_per_level, &fp);
+  const Layout L = layout(ld, k_per_level, &plan);
   if (workspace_bytes < L.total) return WF_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   float* al = reinterpret_cast<float*>(ws + L.al);
-  int32_t* idx_l = reinterpret_cast<int32_t*>(ws + L.idx_l);
-  int32_t* idx = idx_out != nullptr ? idx_out : reinterpret_cast<int32_t*>(ws + L.idx);
-  float* t_ws = reinterpret_cast<float*>(ws + L.t);
-  int32_t* status = status_word(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = wf::launch_dwt_lowpass(ld, Kp, al, ld.levels, s);
-  if (e == cudaSuccess)
-    e = wf::launch_score_topk(ld, sp, Q, al, k_per_level[ld.levels], idx_l, nullptr, status, s);
-  if (e == cudaSuccess)
-    e = wf::launch_recursive_filter(ld, fp, Q, Kp, idx_l, k_per_level, idx, t_ws, status, s);
-  if (e == cudaSuccess)
-    e = wf::launch_sparse_attn(ld, ap, Q, Kp, Vp, Kg, Vg, idx, budget, O, lse, status, s);
-  return cuda_status(e);
+  if (e != cudaSuccess) return cuda_status(e);
+  wf::PathArgs a = {};
+  a.q = Q;
+  a.kp = Kp;
+  a.vp = Vp;
+  a.kg = Kg;
+  a.vg = Vg;
+  a.al = al;
+  a.idx_out = idx_out;
+  a.o = O;
+  a.lse = lse;
+  a.status = status_word(workspace);
+  a.t_ws = reinterpret_cast<float*>(ws + L.t);
+  a.k = k_per_level;
+  a.k_l = k_per_level[ld.levels];
+  a.budget = budget;
+  return cuda_status(wf::launch_path(ld, plan, a, s));
 }
 
 int wf_step_host(const wf_dims* dims, const void* h_Q, const void* h_Kp, const void* h_Vp,

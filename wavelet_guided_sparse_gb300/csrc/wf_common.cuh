@@ -59,6 +59,16 @@ __device__ __forceinline__ void load16_f32(const float* p, float* f) {
 __device__ __forceinline__ uint4 ldg16(const void* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
+// Streaming 16-byte load (read-only path, no L1 allocation).  Being volatile,
+// consecutive calls are issued in program order, so a run of them keeps that
+// many requests in flight before the first result is used.
+__device__ __forceinline__ uint4 ldg16_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
 __device__ __forceinline__ void widen16(const uint4& v, const __nv_bfloat16*, float* f) {
   f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
   f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
@@ -172,6 +182,59 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// ------------------------------------------------------------------ cluster exchanges
+//
+// Every exchange between the CTAs of a cluster is push-based: a CTA stores
+// its contribution straight into its peers' shared memory (distributed
+// shared memory stores do not stall the writer), one cluster barrier
+// (release/acquire) makes the data visible, and every CTA then reads its own
+// shared memory.  A buffer written by peers is not written again before
+// every CTA has passed at least one more cluster barrier after reading it.
+
+template <typename P>
+__device__ __forceinline__ P* peer(P* local, int rank) {
+  return cg::this_cluster().map_shared_rank(local, rank);
+}
+
+// (m, l) online-softmax pair merge; pairs with m = -inf (empty) are skipped.
+__device__ __forceinline__ void merge_ml(float& m, float& l, float m2, float l2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = m2;
+    l = l2;
+    return;
+  }
+  const float mx = fmaxf(m, m2);
+  l = l * expf(m - mx) + l2 * expf(m2 - mx);
+  m = mx;
+}
+
+constexpr int kMaxQ = 64;  // maximum queries per unit
+
+// All-reduce of per-query softmax statistics over the cluster.  loc_m/loc_l
+// hold this CTA's (max, sum of exp) per query; on return gm/ginv hold the
+// cluster-wide max and 1 / sum.  stat_in: [kMaxCluster][2][kMaxQ] floats.
+__device__ inline void cluster_merge_stats(const float* loc_m, const float* loc_l, int G,
+                                           float* stat_in, float* gm, float* ginv) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int cs = static_cast<int>(cluster.num_blocks());
+  const int me = static_cast<int>(cluster.block_rank());
+  for (int e = threadIdx.x; e < G * cs; e += kThreads) {
+    const int q = e % G, r = e / G;
+    float* dst = peer(stat_in, r) + me * 2 * kMaxQ;
+    dst[q] = loc_m[q];
+    dst[kMaxQ + q] = loc_l[q];
+  }
+  cluster.sync();
+  for (int q = threadIdx.x; q < G; q += kThreads) {
+    float m = -INFINITY, l = 0.f;
+    for (int r = 0; r < cs; ++r) merge_ml(m, l, stat_in[r * 2 * kMaxQ + q], stat_in[r * 2 * kMaxQ + kMaxQ + q]);
+    gm[q] = m;
+    ginv[q] = 1.f / l;
+  }
+  __syncthreads();
+}
+
 // ------------------------------------------------------------------ cluster Top-K
 //
 // Exact selection of the k largest 32-bit keys spread over the CTAs of a
@@ -183,12 +246,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 //
 // Three radix rounds (11, 11, 10 bits, most significant first) find the k-th
 // largest key T; every key > T is taken, plus the first (k - #{key > T}) keys
-// equal to T in (rank, index) order.  Per-CTA histograms are summed over the
-// cluster through DSMEM.
+// equal to T in (rank, index) order.  Two variants: gather-all (every CTA
+// receives every key and selects locally; one cluster barrier) for small
+// candidate sets, and distributed (histograms reduce-scattered and
+// all-gathered through DSMEM; two barriers per round) for large ones.
 struct TopkSmem {
-  uint32_t hist[2][2048];  // double-buffered digit histograms (read by peers)
-  uint32_t total[2048];    // cluster-summed histogram of the current round
-  int32_t cnt[2];          // [0] = local #{key > T}, [1] = local #{key == T}
+  uint32_t hist[2048];     // local digit histogram
+  uint32_t total[2048];    // cluster-wide histogram of the current round
+  uint32_t part_in[2048];  // distributed: histogram slices pushed by the peers
+  int32_t cnt_in[kMaxCluster][2];  // distributed: (#> T, #== T) pushed by each rank
+  int32_t nloc_in[kMaxCluster];    // gather-all: candidate count of each rank
+  int32_t red[2 * kMaxCluster];    // gather-all: per-rank (#> T, #== T)
   int32_t scan[kWarps + 1];
   int32_t bcast[4];
 };
@@ -198,64 +266,160 @@ struct TopkResult {
   int offset;       // selected candidates in lower ranks
 };
 
-// Marks take[i] = 1 for selected local candidates (i < n).  Must be called
-// by every thread of every CTA of the cluster (it contains cluster barriers).
-__device__ inline TopkResult cluster_topk(const uint32_t* keys, int n, int k, uint8_t* take,
-                                          TopkSmem& sm) {
-  cg::cluster_group cluster = cg::this_cluster();
+// Digit d* of a histogram with #{digit > d*} < need <= #{digit >= d*}.
+// Returns d* and stores #{digit > d*} in *above.  Block-wide.
+__device__ inline uint32_t find_digit(const uint32_t* total, int nb, int need, TopkSmem& sm,
+                                      int* above) {
   const int tid = threadIdx.x;
-  const int nranks = static_cast<int>(cluster.num_blocks());
+  const int per = nb / kThreads;
+  const int owner = kThreads - 1 - tid;  // thread 0 owns the highest bins
+  int mine = 0;
+  for (int b = 0; b < per; ++b) mine += static_cast<int>(total[owner * per + b]);
+  int tot;
+  const int above_owner = block_excl_scan(mine, sm.scan, &tot);
+  if (above_owner < need && above_owner + mine >= need) {
+    int acc = above_owner;
+    for (int b = per - 1; b >= 0; --b) {
+      const int c = static_cast<int>(total[owner * per + b]);
+      if (acc + c >= need) {
+        sm.bcast[0] = owner * per + b;
+        sm.bcast[1] = acc;
+        break;
+      }
+      acc += c;
+    }
+  }
+  __syncthreads();
+  *above = sm.bcast[1];
+  const uint32_t d = static_cast<uint32_t>(sm.bcast[0]);
+  __syncthreads();
+  return d;
+}
+
+__device__ __forceinline__ int round_shift(int round) { return round == 0 ? 21 : (round == 1 ? 10 : 0); }
+__device__ __forceinline__ int round_bins(int round) { return round == 2 ? 1024 : 2048; }
+
+// Marks take[i] for local candidates given the threshold, this CTA's tie
+// quota; block-wide.
+__device__ inline void mark_taken(const uint32_t* keys, int n, uint32_t thr, int quota,
+                                  uint8_t* take, TopkSmem& sm) {
+  int carry = 0;
+  for (int base = 0; base < n; base += kThreads) {
+    const int i = base + threadIdx.x;
+    const uint32_t key = i < n ? keys[i] : 0u;
+    const int is_eq = (i < n) && key == thr;
+    int tot;
+    const int before = block_excl_scan(is_eq, sm.scan, &tot);
+    if (i < n) take[i] = static_cast<uint8_t>(key > thr || (is_eq && carry + before < quota));
+    carry += tot;
+  }
+  __syncthreads();
+}
+
+// Gather-all variant.  keys_all: [cs][cap] u32 in every CTA; n <= cap.
+__device__ inline TopkResult topk_gather_all(const uint32_t* keys, int n, int k, uint8_t* take,
+                                             TopkSmem& sm, uint32_t* keys_all, int cap) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int cs = static_cast<int>(cluster.num_blocks());
   const int me = static_cast<int>(cluster.block_rank());
+  const int tid = threadIdx.x;
+  for (int e = tid; e < n * cs; e += kThreads) {
+    const int i = e % n, r = e / n;
+    peer(keys_all, r)[me * cap + i] = keys[i];
+  }
+  if (tid < cs) peer(sm.nloc_in, tid)[me] = n;
+  cluster.sync();
   uint32_t prefix = 0, pmask = 0;
   int need = k;
 #pragma unroll 1
   for (int round = 0; round < 3; ++round) {
-    const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
-    const int nb = round == 2 ? 1024 : 2048;
-    uint32_t* hist = sm.hist[round & 1];
-    for (int b = tid; b < nb; b += kThreads) hist[b] = 0;
+    const int shift = round_shift(round), nb = round_bins(round);
+    for (int b = tid; b < nb; b += kThreads) sm.hist[b] = 0;
     __syncthreads();
-    for (int i = tid; i < n; i += kThreads) {
-      const uint32_t key = keys[i];
-      if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
-    }
-    cluster.sync();
-    for (int b = tid; b < nb; b += kThreads) {
-      uint32_t t = 0;
-      for (int r = 0; r < nranks; ++r) t += cluster.map_shared_rank(hist, r)[b];
-      sm.total[b] = t;
-    }
-    __syncthreads();
-    // Find the digit d* with #{digit > d*} < need <= #{digit >= d*}.
-    // Each thread owns nb / kThreads consecutive bins (8 or 4); bins are
-    // scanned from the top through an exclusive block scan of reversed owners.
-    const int per = nb / kThreads;
-    const int owner = kThreads - 1 - tid;  // thread 0 owns the highest bins
-    int mine = 0;
-    for (int b = 0; b < per; ++b) mine += static_cast<int>(sm.total[owner * per + b]);
-    int tot;
-    const int above_owner = block_excl_scan(mine, sm.scan, &tot);  // bins above this owner
-    if (above_owner < need && above_owner + mine >= need) {
-      int acc = above_owner;
-      for (int b = per - 1; b >= 0; --b) {
-        const int c = static_cast<int>(sm.total[owner * per + b]);
-        if (acc + c >= need) {
-          sm.bcast[0] = owner * per + b;
-          sm.bcast[1] = acc;
-          break;
-        }
-        acc += c;
+    for (int r = 0; r < cs; ++r) {
+      const int nr = sm.nloc_in[r];
+      const uint32_t* kr = keys_all + r * cap;
+      for (int i = tid; i < nr; i += kThreads) {
+        const uint32_t key = kr[i];
+        if ((key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & (nb - 1)], 1u);
       }
     }
     __syncthreads();
-    const uint32_t digit = static_cast<uint32_t>(sm.bcast[0]);
-    need -= sm.bcast[1];
+    int above;
+    const uint32_t digit = find_digit(sm.hist, nb, need, sm, &above);
+    need -= above;
     prefix |= digit << shift;
     pmask |= static_cast<uint32_t>(nb - 1) << shift;
-    __syncthreads();
   }
   const uint32_t thr = prefix;
-  // Local counts of keys above and equal to the threshold.
+  if (tid < 2 * kMaxCluster) sm.red[tid] = 0;
+  __syncthreads();
+  for (int r = 0; r < cs; ++r) {
+    const int nr = sm.nloc_in[r];
+    const uint32_t* kr = keys_all + r * cap;
+    int gt = 0, eq = 0;
+    for (int i = tid; i < nr; i += kThreads) {
+      gt += kr[i] > thr;
+      eq += kr[i] == thr;
+    }
+    gt = __reduce_add_sync(0xffffffffu, gt);
+    eq = __reduce_add_sync(0xffffffffu, eq);
+    if ((tid & 31) == 0) {
+      atomicAdd(&sm.red[2 * r], gt);
+      atomicAdd(&sm.red[2 * r + 1], eq);
+    }
+  }
+  __syncthreads();
+  int quota_me = 0, offset = 0, ties_before = 0;
+  for (int r = 0; r < cs; ++r) {
+    const int g = sm.red[2 * r], e = sm.red[2 * r + 1];
+    int q = need - ties_before;
+    q = q < 0 ? 0 : (q > e ? e : q);
+    if (r < me) offset += g + q;
+    if (r == me) quota_me = q;
+    ties_before += e;
+  }
+  const int gt_me = sm.red[2 * me];
+  mark_taken(keys, n, thr, quota_me, take, sm);
+  return TopkResult{gt_me + quota_me, offset};
+}
+
+// Distributed variant (any candidate count).
+__device__ inline TopkResult topk_distributed(const uint32_t* keys, int n, int k, uint8_t* take,
+                                              TopkSmem& sm) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int cs = static_cast<int>(cluster.num_blocks());
+  const int me = static_cast<int>(cluster.block_rank());
+  const int tid = threadIdx.x;
+  uint32_t prefix = 0, pmask = 0;
+  int need = k;
+#pragma unroll 1
+  for (int round = 0; round < 3; ++round) {
+    const int shift = round_shift(round), nb = round_bins(round);
+    const int sl = nb / cs;  // bins owned by each rank
+    for (int b = tid; b < nb; b += kThreads) sm.hist[b] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kThreads) {
+      const uint32_t key = keys[i];
+      if ((key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    for (int b = tid; b < nb; b += kThreads) peer(sm.part_in, b / sl)[me * sl + (b % sl)] = sm.hist[b];
+    cluster.sync();
+    for (int e = tid; e < sl * cs; e += kThreads) {
+      const int bl = e % sl, r = e / sl;
+      uint32_t t = 0;
+      for (int src = 0; src < cs; ++src) t += sm.part_in[src * sl + bl];
+      peer(sm.total, r)[me * sl + bl] = t;
+    }
+    cluster.sync();
+    int above;
+    const uint32_t digit = find_digit(sm.total, nb, need, sm, &above);
+    need -= above;
+    prefix |= digit << shift;
+    pmask |= static_cast<uint32_t>(nb - 1) << shift;
+  }
+  const uint32_t thr = prefix;
   int gt = 0, eq = 0;
   for (int i = tid; i < n; i += kThreads) {
     gt += keys[i] > thr;
@@ -264,34 +428,41 @@ __device__ inline TopkResult cluster_topk(const uint32_t* keys, int n, int k, ui
   int tot_gt, tot_eq;
   (void)block_excl_scan(gt, sm.scan, &tot_gt);
   (void)block_excl_scan(eq, sm.scan, &tot_eq);
-  if (tid == 0) {
-    sm.cnt[0] = tot_gt;
-    sm.cnt[1] = tot_eq;
+  if (tid < cs) {
+    int32_t* dst = peer(&sm.cnt_in[0][0], tid) + 2 * me;
+    dst[0] = tot_gt;
+    dst[1] = tot_eq;
   }
   cluster.sync();
-  // Tie quota of every rank, in rank order; offsets of lower ranks.
   int quota_me = 0, offset = 0, ties_before = 0;
-  for (int r = 0; r < nranks; ++r) {
-    const int32_t* c = cluster.map_shared_rank(sm.cnt, r);
-    const int g = c[0], e = c[1];
+  for (int r = 0; r < cs; ++r) {
+    const int g = sm.cnt_in[r][0], e = sm.cnt_in[r][1];
     int q = need - ties_before;
     q = q < 0 ? 0 : (q > e ? e : q);
     if (r < me) offset += g + q;
     if (r == me) quota_me = q;
     ties_before += e;
   }
-  // Mark: key > T, or key == T among the first quota_me ties (index order).
-  int carry = 0;
-  for (int base = 0; base < n; base += kThreads) {
-    const int i = base + tid;
-    const uint32_t key = i < n ? keys[i] : 0u;
-    const int is_eq = (i < n) && key == thr;
-    int tot;
-    const int before = block_excl_scan(is_eq, sm.scan, &tot);
-    if (i < n) take[i] = static_cast<uint8_t>(key > thr || (is_eq && carry + before < quota_me));
-    carry += tot;
-  }
+  mark_taken(keys, n, thr, quota_me, take, sm);
   return TopkResult{tot_gt + quota_me, offset};
+}
+
+// Exclusive prefix over the cluster of one int per CTA (pushed to every
+// peer).  Returns the sum over lower ranks; *total gets the cluster sum.
+// cnt_in: [kMaxCluster] ints.  Contains one cluster barrier.
+__device__ inline int cluster_excl_count(int mine, int32_t* cnt_in, int* total) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int cs = static_cast<int>(cluster.num_blocks());
+  const int me = static_cast<int>(cluster.block_rank());
+  if (threadIdx.x < cs) peer(cnt_in, threadIdx.x)[me] = mine;
+  cluster.sync();
+  int before = 0, all = 0;
+  for (int r = 0; r < cs; ++r) {
+    if (r < me) before += cnt_in[r];
+    all += cnt_in[r];
+  }
+  *total = all;
+  return before;
 }
 
 // Stable compaction of the taken entries of two parallel int arrays.

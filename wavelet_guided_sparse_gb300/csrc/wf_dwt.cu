@@ -39,7 +39,12 @@ __global__ void __launch_bounds__(kThreads) dwt_lowpass_kernel(const T* __restri
   for (int r0 = 0; r0 < rows; r0 += UNROLL) {
     uint4 raw[UNROLL];
 #pragma unroll
-    for (int i = 0; i < UNROLL; ++i) raw[i] = ldg16(src + static_cast<int64_t>(r0 + i) * D);
+    for (int i = 0; i < UNROLL; ++i) raw[i] = ldg16_stream(src + static_cast<int64_t>(r0 + i) * D);
+    // The arithmetic below consumes these (ordered) pass-through values, so
+    // all UNROLL loads are issued before the first add waits on memory.
+#pragma unroll
+    for (int i = 0; i < UNROLL; ++i)
+      asm volatile("" : "+r"(raw[i].x), "+r"(raw[i].y), "+r"(raw[i].z), "+r"(raw[i].w));
     // Pairwise within the group keeps the fp32 error of long spans small.
 #pragma unroll
     for (int i = 0; i < UNROLL; i += 2) {

@@ -1,12 +1,12 @@
 // Host-side interface between the C-ABI layer (wf_api.cu) and the kernel
-// launchers (wf_dwt.cu, wf_score.cu, wf_filter.cu, wf_attn.cu).
+// launchers (wf_dwt.cu: step 1; wf_path.cu: steps 2-5).
 #pragma once
 
 #include <cuda_runtime.h>
 #include <stddef.h>
+#include <stdint.h>
 
 #include <atomic>
-#include <stdint.h>
 
 #include "wavefilter.h"
 
@@ -22,48 +22,52 @@ struct LaunchDims {
   int dtype;
 };
 
-// Plan of the recursive filter (cluster size, per-CTA capacity, where the
-// token logits live); a pure function of the sizes.
-struct FilterPlan {
+// Phases of the fused path kernel (wf_path.cu).
+enum : int { kPhaseScore = 1, kPhaseFilter = 2, kPhaseAttend = 4, kPhaseAll = 7 };
+
+// Launch plan of the path kernel; a pure function of the sizes and the
+// device's SM count.
+struct PathPlan {
+  int mode;          // kPhase* bit set
   int cluster;       // CTAs per unit
-  int spans_cap;     // max coarse survivors per CTA
-  int rows_cap;      // spans_cap << levels
-  int sorted_cap;    // power of two >= k_L (bitonic sort width)
+  int per_cta_p;     // score: coarse positions per CTA
+  int rows_cap;      // filter: token rows per CTA (capacity)
+  int sorted_cap;    // filter: power of two >= k_L
+  int keys_cap;      // candidates per CTA (capacity)
+  int gather_all;    // Top-K variant
+  int klist_cap;     // attend: key slots per CTA (capacity)
+  int tile_keys;     // attend: keys per staged tile
   bool t_in_smem;    // token logits in shared memory (else workspace)
   size_t smem_bytes; // dynamic shared memory per CTA
-  size_t t_bytes;    // workspace bytes for token logits (0 if in smem)
+  size_t t_bytes;    // workspace bytes for token logits (0 if in shared memory)
 };
 
-struct ScorePlan {
-  int cluster;
-  int per_cta;
-  size_t smem_bytes;
+// Pointers of one path launch (device memory unless noted).
+struct PathArgs {
+  const void *q, *kp, *vp, *kg, *vg;
+  const float* al;
+  const int32_t* idx_l_in;
+  const int32_t* idx_in;
+  int32_t* idx_l_out;
+  float* scores_out;
+  int32_t* idx_out;
+  float* o;
+  float* lse;
+  int32_t* status;
+  float* t_ws;
+  const int32_t* k;  // host, levels + 1 entries (filter phase), else null
+  int k_l;
+  int budget;
 };
 
-struct AttnPlan {
-  int cluster;
-  int tile_keys;
-  int n_tiles;
-  size_t smem_bytes;
-};
-
-bool plan_filter(const LaunchDims& ld, const int32_t* k, FilterPlan* plan);
-bool plan_score(const LaunchDims& ld, ScorePlan* plan);
-bool plan_attn(const LaunchDims& ld, int budget, AttnPlan* plan);
+int device_sm_count();
+bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int budget,
+               int sm_count, PathPlan* plan);
 
 cudaError_t launch_dwt_lowpass(const LaunchDims& ld, const void* kp, float* out, int levels,
                                cudaStream_t stream);
-cudaError_t launch_score_topk(const LaunchDims& ld, const ScorePlan& plan, const void* q,
-                              const float* al, int k_l, int32_t* idx_l, float* scores,
-                              int32_t* status, cudaStream_t stream);
-cudaError_t launch_recursive_filter(const LaunchDims& ld, const FilterPlan& plan, const void* q,
-                                    const void* kp, const int32_t* idx_l, const int32_t* k,
-                                    int32_t* idx, float* t_ws, int32_t* status,
-                                    cudaStream_t stream);
-cudaError_t launch_sparse_attn(const LaunchDims& ld, const AttnPlan& plan, const void* q,
-                               const void* kp, const void* vp, const void* kg, const void* vg,
-                               const int32_t* idx, int budget, float* o, float* lse,
-                               int32_t* status, cudaStream_t stream);
+cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathArgs& args,
+                        cudaStream_t stream);
 
 // Dynamic shared memory the planners allow per CTA (the sm_103a opt-in limit
 // is 227 KB; a little is left for static shared memory).

@@ -1,0 +1,1088 @@
+// Steps 2-5 of the WaveFilter path in one thread-block-cluster kernel.
+//
+// WaveFilter (arXiv 2606.00724):
+//  * step 2, Fig. 2(c) / §1: score the low-frequency keys A_L against the
+//    generation-block queries with the eq. (3) logits and keep a coarse Top-K;
+//  * step 3, Fig. 2(d) / §1: multi-scale recursive filtering — children of
+//    the survivors are re-scored level by level down to tokens;
+//  * steps 4-5, Fig. 2(d) / §2.1 eq. (3): the selected prompt tokens plus all
+//    generation positions form a sparse KV cache that the queries attend.
+// Score of a candidate c among the candidate set C at level j (attention
+// mass): z[i,c] = Q[i]·A_j[c]/√d,  s[c] = Σ_i softmax_{c∈C}(z[i,·])[c].
+//
+// One cluster of `cs` CTAs handles one (sequence, head) unit; the kernel runs
+// any contiguous subset of the phases (score / filter / attend), which is how
+// wf_score_topk, wf_recursive_filter, wf_sparse_gather_attn and wf_step share
+// it.  Between phases the work is rebalanced across the cluster through
+// DSMEM: the coarse survivors are all-gathered (every CTA then takes an equal
+// slice) and the final tokens are pushed to the CTA that attends over their
+// slot of the key list.
+//
+// Phase details:
+//  score  — each CTA owns P/cs coarse positions; z by fp32 FMAs (A_L is fp32),
+//           per-query (max, sum) merged over the cluster, exact Top-K.
+//  filter — by linearity Q·A_j[c] = 2^(-j/2) Σ_{n∈span(c)} Q·Kp[n]: token
+//           logits t = Kp[rows]·Q^T are computed once (bf16 tensor cores,
+//           exact products, fp32 sums) for the rows under this CTA's coarse
+//           survivors, staged by TMA-engine bulk copies in a two-stage
+//           mbarrier pipeline; every level sums t over the candidates' leaves.
+//  attend — split-KV: each CTA gathers the K/V rows of its key slot range by
+//           bulk copies, runs Q·K^T and P·V on tensor cores with an online
+//           softmax, and the partial (max, sum, O) rows are pushed to the CTA
+//           that finalises those query rows.
+#include <algorithm>
+#include <climits>
+#include <cmath>
+
+#include "wf_common.cuh"
+#include "wf_internal.h"
+#include "wf_mma.cuh"
+
+namespace wf {
+
+namespace {
+
+constexpr int kTileRows = 64;  // filter: token rows per staged tile
+constexpr float kLn2 = 0.6931471805599453f;
+
+enum : int { kModeScore = 1, kModeFilter = 2, kModeAttend = 4 };
+
+struct PathParams {
+  const void* q;
+  const void* kp;
+  const void* vp;
+  const void* kg;
+  const void* vg;
+  const float* al;           // score: A_L [U, P, d] fp32
+  const int32_t* idx_l_in;   // filter without score: S_L [U, k_L]
+  const int32_t* idx_in;     // attend without filter: S [U, B]
+  int32_t* idx_l_out;        // score without filter: S_L out [U, k_L]
+  float* scores_out;         // nullable [U, P]
+  int32_t* idx_out;          // nullable in path mode [U, B]
+  float* o;
+  float* lse;                // nullable [U, G]
+  int32_t* status;
+  float* t_ws;               // token logits in global memory (nullptr: shared)
+  int mode;
+  int n_prompt, G, levels, P, kL, budget, n_keys;
+  int cs, per_cta_p, rows_cap, sorted_cap, keys_cap, gather_all, klist_cap, tile_keys;
+  int k[WF_MAX_LEVELS + 1];
+  float scale[WF_MAX_LEVELS + 1];  // 2^(-j/2)/sqrt(d)
+  float inv_sqrt_d, scale_log2;
+};
+
+template <typename T, int D>
+struct PathSmem {
+  static constexpr int kRowBytes = D * static_cast<int>(sizeof(T)) + 16;  // padded row pitch
+  static constexpr int kRowF = D + 4;                                      // fp32 row pitch
+  size_t bars, qs, stat_in, gm, part, cnt_a, cnt_b, misc, sl_all, sp, sr, cp, cr, keys, take,
+      topk, keys_all, klist;
+  size_t s_qf, s_as, s_z;          // score phase
+  size_t f_kst, f_t;               // filter phase
+  size_t a_kst, a_vst, a_work, a_recv, a_rml;  // attend phase
+  size_t total;
+  __host__ __device__ explicit PathSmem(const PathParams& p) {
+    size_t o = 0;
+    auto take_bytes = [&](size_t bytes) {
+      const size_t at = o;
+      o = (o + bytes + 15) & ~size_t(15);
+      return at;
+    };
+    bars = take_bytes(2 * sizeof(uint64_t));
+    qs = take_bytes(static_cast<size_t>(kMaxQ) * kRowBytes);
+    stat_in = take_bytes(sizeof(float) * kMaxCluster * 2 * kMaxQ);
+    gm = take_bytes(sizeof(float) * 2 * kMaxQ);
+    part = take_bytes(sizeof(float) * 2 * kWarps * kMaxQ);
+    cnt_a = take_bytes(sizeof(int32_t) * kMaxCluster);
+    cnt_b = take_bytes(sizeof(int32_t) * kMaxCluster);
+    misc = take_bytes(sizeof(int32_t) * 8);
+    sl_all = take_bytes(sizeof(int32_t) * p.sorted_cap);
+    sp = take_bytes(sizeof(int32_t) * p.rows_cap);
+    sr = take_bytes(sizeof(int32_t) * p.rows_cap);
+    cp = take_bytes(sizeof(int32_t) * p.rows_cap);
+    cr = take_bytes(sizeof(int32_t) * p.rows_cap);
+    keys = take_bytes(sizeof(uint32_t) * p.keys_cap);
+    take = take_bytes(p.keys_cap);
+    topk = take_bytes(sizeof(TopkSmem));
+    keys_all = take_bytes(p.gather_all ? sizeof(uint32_t) * p.cs * p.keys_cap : 0);
+    klist = take_bytes(sizeof(int32_t) * p.klist_cap);
+    const size_t u = o;
+    size_t end = u;
+    if (p.mode & kModeScore) {
+      o = u;
+      s_qf = sizeof(T) == 4 ? qs : take_bytes(sizeof(float) * kMaxQ * kRowF);
+      s_as = take_bytes(sizeof(float) * 32 * kRowF);
+      s_z = take_bytes(sizeof(float) * static_cast<size_t>(p.G) * p.per_cta_p);
+      end = end > o ? end : o;
+    }
+    if (p.mode & kModeFilter) {
+      o = u;
+      f_kst = take_bytes(static_cast<size_t>(2) * kTileRows * kRowBytes);
+      f_t = p.t_ws == nullptr ? take_bytes(sizeof(float) * static_cast<size_t>(p.rows_cap) * p.G) : 0;
+      end = end > o ? end : o;
+    }
+    if (p.mode & kModeAttend) {
+      o = u;
+      const size_t stage = static_cast<size_t>(2) * p.tile_keys * kRowBytes;
+      if (sizeof(T) == 2) {  // warp partials overwrite the stages after the last tile
+        const size_t work = sizeof(float) * (kWarps * 16 * D + 2 * kWarps * 16);
+        a_kst = o;
+        a_vst = o + stage;
+        a_work = o;
+        take_bytes(2 * stage > work ? 2 * stage : work);
+      } else {
+        a_kst = take_bytes(stage);
+        a_vst = take_bytes(stage);
+        a_work = take_bytes(sizeof(float) * (kMaxQ * 33 + 3 * kMaxQ));
+      }
+      const int rpo = (p.G + p.cs - 1) / p.cs;  // query rows finalised per CTA
+      a_recv = take_bytes(sizeof(float) * static_cast<size_t>(p.cs) * rpo * D);
+      a_rml = take_bytes(sizeof(float) * static_cast<size_t>(p.cs) * rpo * 2);
+      end = end > o ? end : o;
+    }
+    total = end;
+  }
+};
+
+struct Ctx {
+  int cs, rank, tid, lane, warp;
+  int64_t unit;
+};
+
+// ------------------------------------------------------------------ small helpers
+__device__ __forceinline__ int key_slot_start(int r, int cs, int n_keys) {
+  return static_cast<int>((static_cast<int64_t>(r) * n_keys) / cs);
+}
+__device__ __forceinline__ int key_slot_owner(int g, int cs, int n_keys) {
+  int r = cs - 1;
+  while (r > 0 && key_slot_start(r, cs, n_keys) > g) --r;
+  return r;
+}
+
+// Selection among this CTA's candidates (keys[0..n)), exact over the cluster.
+__device__ __forceinline__ TopkResult cluster_select(const PathParams& p, const uint32_t* keys,
+                                                     int n, int k, uint8_t* take, TopkSmem& tk,
+                                                     uint32_t* keys_all) {
+  if (p.gather_all) return topk_gather_all(keys, n, k, take, tk, keys_all, p.keys_cap);
+  return topk_distributed(keys, n, k, take, tk);
+}
+
+// ------------------------------------------------------------------ token logits tile
+// bf16: t rows [row0, row0 + 64) from the staged key rows.  Warp w: 16-row
+// block (w & 3), n-blocks (w >> 2) + 2i of 8 queries each.
+template <int D>
+__device__ __forceinline__ void token_logits_tile(const unsigned char* kst,
+                                                  const uint32_t (&bq)[4][D / 16][2], float* t,
+                                                  int row0, int rows_valid, int G) {
+  constexpr int RB = D * 2 + 16;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int mb = warp & 3, ng = warp >> 2;
+  const int NB = (G + 7) >> 3;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
+  const uint32_t abase = smem_u32(kst) + (mb * 16 + (lane & 15)) * RB + (lane >> 4) * 16;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    uint32_t a[4];
+    ldsm_x4(abase + ks * 32, a);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (ng + 2 * i < NB) mma_bf16(acc[i], a, bq[i][ks]);
+  }
+  const int r_lo = mb * 16 + (lane >> 2);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int nb = ng + 2 * i;
+    if (nb >= NB) continue;
+    const int q0 = nb * 8 + (lane & 3) * 2;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = r_lo + 8 * h;
+      if (r >= rows_valid) continue;
+      float* dst = t + static_cast<int64_t>(row0 + r) * G;
+      if (q0 < G) dst[q0] = acc[i][2 * h];
+      if (q0 + 1 < G) dst[q0 + 1] = acc[i][2 * h + 1];
+    }
+  }
+}
+
+// fp32: plain FMAs.  Thread -> row (tid & 63), queries (tid >> 6) + 4i.
+template <int D>
+__device__ __forceinline__ void token_logits_tile_f32(const unsigned char* kst, const float* qs,
+                                                      float* t, int row0, int rows_valid, int G) {
+  constexpr int RF = D + 4;
+  const int r = threadIdx.x & 63, g = threadIdx.x >> 6;
+  if (r >= rows_valid) return;
+  const float* krow = reinterpret_cast<const float*>(kst) + r * RF;
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+#pragma unroll 2
+  for (int c = 0; c < D; c += 4) {
+    const float4 a = *reinterpret_cast<const float4*>(krow + c);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float4 b = *reinterpret_cast<const float4*>(qs + (g + 4 * i) * RF + c);
+      acc[i] = fmaf(a.x, b.x, acc[i]);
+      acc[i] = fmaf(a.y, b.y, acc[i]);
+      acc[i] = fmaf(a.z, b.z, acc[i]);
+      acc[i] = fmaf(a.w, b.w, acc[i]);
+    }
+  }
+  float* dst = t + static_cast<int64_t>(row0 + r) * G;
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    if (g + 4 * i < G) dst[g + 4 * i] = acc[i];
+}
+
+__device__ __forceinline__ void online_update(float& m, float& l, float z) {
+  if (z > m) {
+    l = l * expf(m - z) + 1.f;
+    m = z;
+  } else {
+    l += expf(z - m);
+  }
+}
+
+__device__ __forceinline__ float safe_exp2_diff(float m, float mx) {
+  return m == -INFINITY ? 0.f : exp2f(m - mx);
+}
+
+// Prompt row of key slot g (g < B) of this unit, or -1 if out of range.
+__device__ __forceinline__ int prompt_row(const PathParams& p, const Ctx& c, const int32_t* klist,
+                                          int k0, int g) {
+  const int row = (p.mode & kModeFilter) ? klist[g - k0] : __ldg(p.idx_in + c.unit * p.budget + g);
+  return (row >= 0 && row < p.n_prompt) ? row : -1;
+}
+
+// ============================================================== the kernel
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant__ PathParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  cg::cluster_group cluster = cg::this_cluster();
+  Ctx c;
+  c.cs = static_cast<int>(cluster.num_blocks());
+  c.rank = static_cast<int>(cluster.block_rank());
+  c.tid = threadIdx.x;
+  c.lane = c.tid & 31;
+  c.warp = c.tid >> 5;
+  c.unit = blockIdx.y;
+  const int tid = c.tid, lane = c.lane, warp = c.warp, cs = c.cs, rank = c.rank;
+  const int64_t unit = c.unit;
+  const int G = p.G, levels = p.levels;
+  const PathSmem<T, D> L(p);
+  constexpr int RB = PathSmem<T, D>::kRowBytes;
+  constexpr int RF = PathSmem<T, D>::kRowF;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  unsigned char* qs = smem + L.qs;
+  float* stat_in = reinterpret_cast<float*>(smem + L.stat_in);
+  float* gm = reinterpret_cast<float*>(smem + L.gm);
+  float* ginv = gm + kMaxQ;
+  float* part_m = reinterpret_cast<float*>(smem + L.part);
+  float* part_l = part_m + kWarps * kMaxQ;
+  int32_t* cnt_a = reinterpret_cast<int32_t*>(smem + L.cnt_a);
+  int32_t* cnt_b = reinterpret_cast<int32_t*>(smem + L.cnt_b);
+  int32_t* misc = reinterpret_cast<int32_t*>(smem + L.misc);
+  int32_t* sl_all = reinterpret_cast<int32_t*>(smem + L.sl_all);
+  int32_t* sp = reinterpret_cast<int32_t*>(smem + L.sp);
+  int32_t* sr = reinterpret_cast<int32_t*>(smem + L.sr);
+  int32_t* cp = reinterpret_cast<int32_t*>(smem + L.cp);
+  int32_t* cr = reinterpret_cast<int32_t*>(smem + L.cr);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + L.keys);
+  uint8_t* take = smem + L.take;
+  TopkSmem& tk = *reinterpret_cast<TopkSmem*>(smem + L.topk);
+  uint32_t* keys_all = reinterpret_cast<uint32_t*>(smem + L.keys_all);
+  int32_t* klist = reinterpret_cast<int32_t*>(smem + L.klist);
+
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+    misc[0] = 0;  // 1 once a bounded wait gave up
+  }
+  // Queries (input dtype, padded rows; rows >= G are zero).
+  {
+    const T* qsrc = static_cast<const T*>(p.q) + unit * G * D;
+    constexpr int V = Elem<T>::kPer16B;
+    for (int e = tid; e < kMaxQ * (D / V); e += kThreads) {
+      const int r = e / (D / V), col = (e % (D / V)) * V;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < G) v = ldg16(qsrc + r * D + col);
+      *reinterpret_cast<uint4*>(qs + r * RB + col * sizeof(T)) = v;
+    }
+  }
+  __syncthreads();
+  uint32_t bar_phase[2] = {0u, 0u};  // completed uses of each mbarrier
+
+  // ================================================================ score
+  if (p.mode & kModeScore) {
+    const int Pc = p.per_cta_p;
+    float* qf = reinterpret_cast<float*>(smem + L.s_qf);
+    float* as = reinterpret_cast<float*>(smem + L.s_as);
+    float* z = reinterpret_cast<float*>(smem + L.s_z);
+    if constexpr (sizeof(T) == 2) {
+      for (int e = tid; e < kMaxQ * D / 2; e += kThreads) {
+        const int r = e / (D / 2), col = (e % (D / 2)) * 2;
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(qs + r * RB + col * 2);
+        qf[r * RF + col] = bf16_lo(w);
+        qf[r * RF + col + 1] = bf16_hi(w);
+      }
+    }
+    const float* asrc = p.al + (unit * p.P + static_cast<int64_t>(rank) * Pc) * D;
+    for (int c0 = 0; c0 < Pc; c0 += 32) {
+      __syncthreads();
+      const int rows = min(32, Pc - c0);
+      for (int e = tid; e < rows * (D / 4); e += kThreads) {
+        const int r = e / (D / 4), col = (e % (D / 4)) * 4;
+        *reinterpret_cast<float4*>(as + r * RF + col) =
+            __ldg(reinterpret_cast<const float4*>(asrc + static_cast<int64_t>(c0 + r) * D + col));
+      }
+      __syncthreads();
+      if (lane < rows && warp < G) {  // thread -> A_L row (lane), queries warp + 8i
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        const float* arow = as + lane * RF;
+#pragma unroll 4
+        for (int col = 0; col < D; col += 4) {
+          const float4 a = *reinterpret_cast<const float4*>(arow + col);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 b = *reinterpret_cast<const float4*>(qf + (warp + 8 * i) * RF + col);
+            acc[i] = fmaf(a.x, b.x, acc[i]);
+            acc[i] = fmaf(a.y, b.y, acc[i]);
+            acc[i] = fmaf(a.z, b.z, acc[i]);
+            acc[i] = fmaf(a.w, b.w, acc[i]);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int qi = warp + 8 * i;
+          if (qi < G) z[qi * Pc + c0 + lane] = acc[i] * p.inv_sqrt_d;
+        }
+      }
+    }
+    __syncthreads();
+    for (int qi = warp; qi < G; qi += kWarps) {
+      float m = -INFINITY;
+      for (int j = lane; j < Pc; j += 32) m = fmaxf(m, z[qi * Pc + j]);
+      m = warp_max(m);
+      float l = 0.f;
+      for (int j = lane; j < Pc; j += 32) l += expf(z[qi * Pc + j] - m);
+      l = warp_sum(l);
+      if (lane == 0) {
+        part_m[qi] = m;
+        part_l[qi] = l;
+      }
+    }
+    __syncthreads();
+    cluster_merge_stats(part_m, part_l, G, stat_in, gm, ginv);
+    for (int j = tid; j < Pc; j += kThreads) {
+      float s = 0.f;
+      for (int qi = 0; qi < G; ++qi) s += expf(z[qi * Pc + j] - gm[qi]) * ginv[qi];
+      keys[j] = __float_as_uint(s);
+      if (p.scores_out != nullptr) p.scores_out[unit * p.P + rank * Pc + j] = s;
+    }
+    __syncthreads();
+    const TopkResult res = cluster_select(p, keys, Pc, p.kL, take, tk, keys_all);
+    const bool to_peers = (p.mode & kModeFilter) != 0;
+    int carry = 0;
+    for (int base = 0; base < Pc; base += kThreads) {
+      const int j = base + tid;
+      const int tkn = j < Pc ? take[j] : 0;
+      int tot;
+      const int pos = block_excl_scan(tkn, tk.scan, &tot);
+      const int slot = res.offset + carry + pos;
+      if (tkn && slot < p.kL) {
+        const int coarse = rank * Pc + j;
+        if (to_peers) {
+          for (int r = 0; r < cs; ++r) peer(sl_all, r)[slot] = coarse;
+        } else {
+          p.idx_l_out[unit * p.kL + slot] = coarse;
+        }
+      }
+      carry += tot;
+    }
+    if (to_peers) cluster.sync();  // every CTA now holds the sorted coarse survivors
+  } else if (p.mode & kModeFilter) {
+    // Coarse survivors from the caller: load, sort ascending, validate.
+    const int kL = p.kL, P = p.P;
+    for (int i = tid; i < p.sorted_cap; i += kThreads)
+      sl_all[i] = i < kL ? p.idx_l_in[unit * kL + i] : INT_MAX;
+    __syncthreads();
+    for (int kk = 2; kk <= p.sorted_cap; kk <<= 1) {
+      for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+        for (int i = tid; i < p.sorted_cap; i += kThreads) {
+          const int ixj = i ^ jj;
+          if (ixj > i) {
+            const int a = sl_all[i], b = sl_all[ixj];
+            if ((a > b) == ((i & kk) == 0)) {
+              sl_all[i] = b;
+              sl_all[ixj] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    int bad = 0;
+    for (int i = tid; i < kL; i += kThreads) {
+      const int v = sl_all[i];
+      if (v < 0 || v >= P) bad |= WF_DEV_BAD_INDEX;
+      if (i > 0 && sl_all[i - 1] == v) bad |= WF_DEV_DUP_INDEX;
+    }
+    __syncthreads();
+    for (int i = tid; i < kL; i += kThreads) sl_all[i] = min(max(sl_all[i], 0), P - 1);
+    if (bad && rank == 0) raise_flag(p.status, bad);
+    __syncthreads();
+  }
+
+  // ================================================================ filter
+  if (p.mode & kModeFilter) {
+    const int kL = p.kL;
+    const int s0 = static_cast<int>((static_cast<int64_t>(rank) * kL) / cs);
+    const int s1 = static_cast<int>((static_cast<int64_t>(rank + 1) * kL) / cs);
+    const int ns = s1 - s0;
+    const int R = ns << levels;
+    unsigned char* kst = smem + L.f_kst;
+    float* t = p.t_ws == nullptr
+                   ? reinterpret_cast<float*>(smem + L.f_t)
+                   : p.t_ws + (static_cast<int64_t>(unit) * cs + rank) * p.rows_cap * G;
+    const T* kp = static_cast<const T*>(p.kp);
+    const int ntiles = (R + kTileRows - 1) / kTileRows;
+    auto issue = [&](int tile, int stage) {  // warp 0 only
+      const int r0 = tile * kTileRows;
+      const int nr = min(kTileRows, R - r0);
+      if (lane == 0) mbar_arrive_expect_tx(&bars[stage], nr * D * static_cast<int>(sizeof(T)));
+      __syncwarp();
+      for (int i = lane; i < nr; i += 32) {
+        const int lr = r0 + i;
+        const int64_t grow = unit * p.n_prompt +
+                             (static_cast<int64_t>(sl_all[s0 + (lr >> levels)]) << levels) +
+                             (lr & ((1 << levels) - 1));
+        bulk_g2s(kst + (stage * kTileRows + i) * RB, kp + grow * D, D * sizeof(T), &bars[stage]);
+      }
+    };
+    if (warp == 0) {
+      if (ntiles > 0) issue(0, 0);
+      if (ntiles > 1) issue(1, 1);
+    }
+    uint32_t bq[4][D / 16][2];
+    if constexpr (sizeof(T) == 2) {
+      const int NB = (G + 7) >> 3, ng = warp >> 2;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int nb = min(ng + 2 * i, NB - 1);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          ldsm_x2(smem_u32(qs) + (nb * 8 + (lane & 7)) * RB + ks * 32 + ((lane >> 3) & 1) * 16,
+                  bq[i][ks]);
+      }
+    }
+    for (int tile = 0; tile < ntiles; ++tile) {
+      const int stage = tile & 1;
+      int ok = 1;
+      if (misc[0] == 0) ok = mbar_wait_bounded(&bars[stage], bar_phase[stage] & 1, p.status) ? 1 : 0;
+      ++bar_phase[stage];
+      if (__syncthreads_or(!ok) && tid == 0) misc[0] = 1;
+      const unsigned char* buf = kst + stage * kTileRows * RB;
+      const int rows_valid = min(kTileRows, R - tile * kTileRows);
+      if constexpr (sizeof(T) == 2) {
+        token_logits_tile<D>(buf, bq, t, tile * kTileRows, rows_valid, G);
+      } else {
+        token_logits_tile_f32<D>(buf, reinterpret_cast<const float*>(qs), t, tile * kTileRows,
+                                 rows_valid, G);
+      }
+      __syncthreads();
+      if (warp == 0 && tile + 2 < ntiles && misc[0] == 0) {
+        fence_proxy_async();
+        issue(tile + 2, stage);
+      }
+    }
+    __syncthreads();
+
+    int n_surv = ns;
+    for (int i = tid; i < ns; i += kThreads) {
+      sp[i] = sl_all[s0 + i];
+      sr[i] = i << levels;
+    }
+    __syncthreads();
+    for (int j = levels - 1; j >= 0; --j) {
+      for (int i = tid; i < n_surv; i += kThreads) {
+        const int pos = sp[i], row = sr[i];
+        cp[2 * i] = 2 * pos;
+        cp[2 * i + 1] = 2 * pos + 1;
+        cr[2 * i] = row;
+        cr[2 * i + 1] = row + (1 << j);
+      }
+      const int n_cand = 2 * n_surv;
+      __syncthreads();
+      if (p.k[j] >= 2 * p.k[j + 1]) {  // every candidate survives: no scoring
+        int32_t* x = sp; sp = cp; cp = x;
+        x = sr; sr = cr; cr = x;
+        n_surv = n_cand;
+        continue;
+      }
+      const int leaves = 1 << j;
+      const float sc = p.scale[j];
+      float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+      for (int ci = warp; ci < n_cand; ci += kWarps) {
+        const float* tp = t + static_cast<int64_t>(cr[ci]) * G;
+        if (lane < G) {
+          float acc = 0.f;
+          for (int i = 0; i < leaves; ++i) acc += tp[i * G + lane];
+          online_update(m0, l0, acc * sc);
+        }
+        if (lane + 32 < G) {
+          float acc = 0.f;
+          for (int i = 0; i < leaves; ++i) acc += tp[i * G + lane + 32];
+          online_update(m1, l1, acc * sc);
+        }
+      }
+      part_m[warp * kMaxQ + lane] = m0;
+      part_l[warp * kMaxQ + lane] = l0;
+      part_m[warp * kMaxQ + lane + 32] = m1;
+      part_l[warp * kMaxQ + lane + 32] = l1;
+      __syncthreads();
+      float cta_m = -INFINITY, cta_l = 0.f;
+      if (tid < G)
+        for (int w = 0; w < kWarps; ++w) merge_ml(cta_m, cta_l, part_m[w * kMaxQ + tid], part_l[w * kMaxQ + tid]);
+      __syncthreads();
+      if (tid < G) {
+        part_m[tid] = cta_m;
+        part_l[tid] = cta_l;
+      }
+      __syncthreads();
+      cluster_merge_stats(part_m, part_l, G, stat_in, gm, ginv);
+      for (int ci = warp; ci < n_cand; ci += kWarps) {
+        const float* tp = t + static_cast<int64_t>(cr[ci]) * G;
+        float s = 0.f;
+        if (lane < G) {
+          float acc = 0.f;
+          for (int i = 0; i < leaves; ++i) acc += tp[i * G + lane];
+          s += expf(acc * sc - gm[lane]) * ginv[lane];
+        }
+        if (lane + 32 < G) {
+          float acc = 0.f;
+          for (int i = 0; i < leaves; ++i) acc += tp[i * G + lane + 32];
+          s += expf(acc * sc - gm[lane + 32]) * ginv[lane + 32];
+        }
+        s = warp_sum(s);
+        if (lane == 0) keys[ci] = __float_as_uint(s);
+      }
+      __syncthreads();
+      (void)cluster_select(p, keys, n_cand, p.k[j], take, tk, keys_all);
+      n_surv = compact2(cp, cr, take, n_cand, sp, sr, tk.scan);
+    }
+    // Tokens of this CTA: sp[0, n_surv), ascending.
+    int all;
+    const int offset = cluster_excl_count(n_surv, cnt_a, &all);
+    const int B = p.budget;
+    if (p.mode & kModeAttend) {
+      for (int i = tid; i < n_surv; i += kThreads) {
+        const int g = offset + i;
+        if (g >= B) continue;
+        const int owner = key_slot_owner(g, cs, p.n_keys);
+        peer(klist, owner)[g - key_slot_start(owner, cs, p.n_keys)] = sp[i];
+        if (p.idx_out != nullptr) p.idx_out[unit * B + g] = sp[i];
+      }
+      cluster.sync();
+    } else {
+      for (int i = tid; i < n_surv; i += kThreads)
+        if (offset + i < B) p.idx_out[unit * B + offset + i] = sp[i];
+    }
+  }
+
+  // ================================================================ attend
+  if (p.mode & kModeAttend) {
+    const int B = p.budget, TK = p.tile_keys;
+    const int k0 = key_slot_start(rank, cs, p.n_keys);
+    const int k1 = key_slot_start(rank + 1, cs, p.n_keys);
+    const int ntiles = (k1 - k0 + TK - 1) / TK;
+    unsigned char* kst = smem + L.a_kst;
+    unsigned char* vst = smem + L.a_vst;
+    float* work = reinterpret_cast<float*>(smem + L.a_work);
+    float* recv_o = reinterpret_cast<float*>(smem + L.a_recv);
+    float* recv_ml = reinterpret_cast<float*>(smem + L.a_rml);
+    const int rpo = (G + cs - 1) / cs;
+    const T* kgp = static_cast<const T*>(p.kg) + unit * G * D;
+    const T* vgp = static_cast<const T*>(p.vg) + unit * G * D;
+    const T* kpp = static_cast<const T*>(p.kp) + unit * p.n_prompt * D;
+    const T* vpp = static_cast<const T*>(p.vp) + unit * p.n_prompt * D;
+    if (!(p.mode & kModeFilter)) {  // report bad caller indices of this slot range
+      for (int g = k0 + tid; g < min(k1, B); g += kThreads)
+        if (prompt_row(p, c, klist, k0, g) < 0) raise_flag(p.status, WF_DEV_BAD_INDEX);
+    }
+    // Every slot of a tile is filled (invalid slots with a finite dummy row),
+    // so masked probabilities multiply finite values.
+    auto issue = [&](int tile, int stage) {  // warp 0 only
+      const int base = k0 + tile * TK;
+      if (lane == 0) mbar_arrive_expect_tx(&bars[stage], 2u * TK * D * sizeof(T));
+      __syncwarp();
+      for (int i = lane; i < TK; i += 32) {
+        const int g = base + i;
+        const T* ks = kgp;
+        const T* vs = vgp;
+        if (g < k1) {
+          if (g >= B) {
+            ks = kgp + static_cast<int64_t>(g - B) * D;
+            vs = vgp + static_cast<int64_t>(g - B) * D;
+          } else {
+            const int row = prompt_row(p, c, klist, k0, g);
+            if (row >= 0) {
+              ks = kpp + static_cast<int64_t>(row) * D;
+              vs = vpp + static_cast<int64_t>(row) * D;
+            }
+          }
+        }
+        bulk_g2s(kst + (stage * TK + i) * RB, ks, D * sizeof(T), &bars[stage]);
+        bulk_g2s(vst + (stage * TK + i) * RB, vs, D * sizeof(T), &bars[stage]);
+      }
+    };
+    __syncthreads();  // filter-phase readers of the union are done
+    if (warp == 0 && misc[0] == 0) {
+      fence_proxy_async();
+      if (ntiles > 0) issue(0, 0);
+      if (ntiles > 1) issue(1, 1);
+    }
+    auto valid = [&](int g) -> bool {
+      if (g >= k1) return false;
+      if (g >= B) return true;
+      return prompt_row(p, c, klist, k0, g) >= 0;
+    };
+
+    if constexpr (sizeof(T) == 2) {
+      const int MB = G <= 16 ? 1 : (G <= 32 ? 2 : 4);
+      const int mb = warp % MB, kgrp = warp / MB;  // 16 keys per warp per tile
+      uint32_t qa[D / 16][4];
+      {
+        const uint32_t qbase = smem_u32(qs) + (mb * 16 + (lane & 15)) * RB + (lane >> 4) * 16;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) ldsm_x4(qbase + ks * 32, qa[ks]);
+      }
+      float oacc[D / 8][4];
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) oacc[i][e] = 0.f;
+      float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+      for (int tile = 0; tile < ntiles; ++tile) {
+        const int stage = tile & 1;
+        int ok = 1;
+        if (misc[0] == 0) ok = mbar_wait_bounded(&bars[stage], bar_phase[stage] & 1, p.status) ? 1 : 0;
+        ++bar_phase[stage];
+        if (__syncthreads_or(!ok) && tid == 0) misc[0] = 1;
+        const uint32_t kb = smem_u32(kst + (stage * TK + kgrp * 16) * RB);
+        const uint32_t vb = smem_u32(vst + (stage * TK + kgrp * 16) * RB);
+        float s[2][4];
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[nb][e] = 0.f;
+        const uint32_t kaddr = kb + ((lane & 7) + ((lane >> 4) << 3)) * RB + ((lane >> 3) & 1) * 16;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          uint32_t b[4];
+          ldsm_x4(kaddr + ks * 32, b);
+          mma_bf16(s[0], qa[ks], b);
+          mma_bf16(s[1], qa[ks], b + 2);
+        }
+        const int jbase = k0 + tile * TK + kgrp * 16 + (lane & 3) * 2;
+        float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const bool v = valid(jbase + nb * 8 + e);
+            s[nb][e] = v ? s[nb][e] * p.scale_log2 : -INFINITY;
+            s[nb][e + 2] = v ? s[nb][e + 2] * p.scale_log2 : -INFINITY;
+            mx_lo = fmaxf(mx_lo, s[nb][e]);
+            mx_hi = fmaxf(mx_hi, s[nb][e + 2]);
+          }
+        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+        const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+        const float base_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
+        const float base_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
+        const float corr_lo = exp2f(m_lo - base_lo), corr_hi = exp2f(m_hi - base_hi);
+        float sum_lo = 0.f, sum_hi = 0.f;
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            s[nb][e] = exp2f(s[nb][e] - base_lo);
+            s[nb][e + 2] = exp2f(s[nb][e + 2] - base_hi);
+            sum_lo += s[nb][e];
+            sum_hi += s[nb][e + 2];
+          }
+        sum_lo += __shfl_xor_sync(0xffffffffu, sum_lo, 1);
+        sum_lo += __shfl_xor_sync(0xffffffffu, sum_lo, 2);
+        sum_hi += __shfl_xor_sync(0xffffffffu, sum_hi, 1);
+        sum_hi += __shfl_xor_sync(0xffffffffu, sum_hi, 2);
+        l_lo = l_lo * corr_lo + sum_lo;
+        l_hi = l_hi * corr_hi + sum_hi;
+        m_lo = mn_lo;
+        m_hi = mn_hi;
+        uint32_t pa[4];
+        pa[0] = pack_bf16(s[0][0], s[0][1]);
+        pa[1] = pack_bf16(s[0][2], s[0][3]);
+        pa[2] = pack_bf16(s[1][0], s[1][1]);
+        pa[3] = pack_bf16(s[1][2], s[1][3]);
+        const uint32_t vaddr = vb + (lane & 15) * RB + (lane >> 4) * 16;
+#pragma unroll
+        for (int dn = 0; dn < D / 8; dn += 2) {
+          oacc[dn][0] *= corr_lo; oacc[dn][1] *= corr_lo;
+          oacc[dn][2] *= corr_hi; oacc[dn][3] *= corr_hi;
+          oacc[dn + 1][0] *= corr_lo; oacc[dn + 1][1] *= corr_lo;
+          oacc[dn + 1][2] *= corr_hi; oacc[dn + 1][3] *= corr_hi;
+          uint32_t b[4];
+          ldsm_x4_t(vaddr + dn * 16, b);
+          mma_bf16(oacc[dn], pa, b);
+          mma_bf16(oacc[dn + 1], pa, b + 2);
+        }
+        __syncthreads();
+        if (warp == 0 && tile + 2 < ntiles && misc[0] == 0) {
+          fence_proxy_async();
+          issue(tile + 2, stage);
+        }
+      }
+      // Warp partials -> shared memory (overwrites the stages).
+      float* opart = work;                    // [kWarps][16][D]
+      float* mpart = work + kWarps * 16 * D;  // [kWarps][16]
+      float* lpart = mpart + kWarps * 16;
+      __syncthreads();
+      const int r_lo = lane >> 2;
+#pragma unroll
+      for (int dn = 0; dn < D / 8; ++dn) {
+        const int col = dn * 8 + (lane & 3) * 2;
+        *reinterpret_cast<float2*>(opart + (warp * 16 + r_lo) * D + col) =
+            make_float2(oacc[dn][0], oacc[dn][1]);
+        *reinterpret_cast<float2*>(opart + (warp * 16 + r_lo + 8) * D + col) =
+            make_float2(oacc[dn][2], oacc[dn][3]);
+      }
+      if ((lane & 3) == 0) {
+        mpart[warp * 16 + r_lo] = m_lo;
+        lpart[warp * 16 + r_lo] = l_lo;
+        mpart[warp * 16 + r_lo + 8] = m_hi;
+        lpart[warp * 16 + r_lo + 8] = l_hi;
+      }
+      __syncthreads();
+      // CTA partial of row qi, pushed straight to the CTA that finalises it.
+      const int KGW = kWarps / MB;
+      for (int e = tid; e < G * (D / 4); e += kThreads) {
+        const int qi = e / (D / 4), col = (e % (D / 4)) * 4;
+        const int qmb = qi >> 4, r = qi & 15;
+        float mx = -INFINITY;
+        for (int g = 0; g < KGW; ++g) mx = fmaxf(mx, mpart[(qmb + MB * g) * 16 + r]);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float l = 0.f;
+        for (int g = 0; g < KGW; ++g) {
+          const int w = qmb + MB * g;
+          const float f = safe_exp2_diff(mpart[w * 16 + r], mx);
+          const float4 v = *reinterpret_cast<const float4*>(opart + (w * 16 + r) * D + col);
+          acc.x += f * v.x; acc.y += f * v.y; acc.z += f * v.z; acc.w += f * v.w;
+          l += f * lpart[w * 16 + r];
+        }
+        const int owner = qi / rpo, ro = qi - owner * rpo;
+        *reinterpret_cast<float4*>(peer(recv_o, owner) + (rank * rpo + ro) * D + col) = acc;
+        if (col == 0) {
+          float* dst = peer(recv_ml, owner) + (rank * rpo + ro) * 2;
+          dst[0] = mx;
+          dst[1] = l;
+        }
+      }
+    } else {
+      // ------------------------------------------------ fp32 FMA path
+      float* sS = work;                    // [kMaxQ][33] logits / probabilities
+      float* m_run = work + kMaxQ * 33;
+      float* l_run = m_run + kMaxQ;
+      float* corr_s = l_run + kMaxQ;
+      const float* qf = reinterpret_cast<const float*>(qs);
+      constexpr int C4 = D / 4;
+      constexpr int QG = kThreads / C4;
+      constexpr int QPT = kMaxQ / QG;
+      float oacc[QPT][4];
+#pragma unroll
+      for (int i = 0; i < QPT; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) oacc[i][e] = 0.f;
+      if (tid < kMaxQ) {
+        m_run[tid] = -INFINITY;
+        l_run[tid] = 0.f;
+      }
+      __syncthreads();
+      for (int tile = 0; tile < ntiles; ++tile) {
+        const int stage = tile & 1;
+        int ok = 1;
+        if (misc[0] == 0) ok = mbar_wait_bounded(&bars[stage], bar_phase[stage] & 1, p.status) ? 1 : 0;
+        ++bar_phase[stage];
+        if (__syncthreads_or(!ok) && tid == 0) misc[0] = 1;
+        const float* kb = reinterpret_cast<const float*>(kst + stage * TK * RB);
+        const float* vb = reinterpret_cast<const float*>(vst + stage * TK * RB);
+        {
+          const int kk = tid & 31, g = tid >> 5;
+          const bool v = valid(k0 + tile * TK + kk);
+          for (int qi = g; qi < G; qi += 8) {
+            float acc = 0.f;
+            for (int col = 0; col < D; col += 4) {
+              const float4 a = *reinterpret_cast<const float4*>(kb + kk * RF + col);
+              const float4 b = *reinterpret_cast<const float4*>(qf + qi * RF + col);
+              acc = fmaf(a.x, b.x, acc);
+              acc = fmaf(a.y, b.y, acc);
+              acc = fmaf(a.z, b.z, acc);
+              acc = fmaf(a.w, b.w, acc);
+            }
+            sS[qi * 33 + kk] = v ? acc * p.scale_log2 : -INFINITY;
+          }
+        }
+        __syncthreads();
+        for (int qi = warp; qi < G; qi += kWarps) {
+          const float sv = sS[qi * 33 + lane];
+          const float mo = m_run[qi];
+          const float mn = fmaxf(mo, warp_max(sv));
+          const float base = mn == -INFINITY ? 0.f : mn;
+          const float pv = exp2f(sv - base);
+          const float sum = warp_sum(pv);
+          sS[qi * 33 + lane] = pv;
+          if (lane == 0) {
+            const float corr = exp2f(mo - base);
+            corr_s[qi] = corr;
+            l_run[qi] = l_run[qi] * corr + sum;
+            m_run[qi] = mn;
+          }
+        }
+        __syncthreads();
+        {
+          const int c4 = tid % C4, qg = tid / C4;
+#pragma unroll
+          for (int i = 0; i < QPT; ++i) {
+            const int qi = qg + QG * i;
+            if (qi >= G) continue;
+            const float corr = corr_s[qi];
+            float a0 = oacc[i][0] * corr, a1 = oacc[i][1] * corr, a2 = oacc[i][2] * corr,
+                  a3 = oacc[i][3] * corr;
+            for (int kk = 0; kk < TK; ++kk) {
+              const float pv = sS[qi * 33 + kk];
+              const float4 vv = *reinterpret_cast<const float4*>(vb + kk * RF + c4 * 4);
+              a0 = fmaf(pv, vv.x, a0);
+              a1 = fmaf(pv, vv.y, a1);
+              a2 = fmaf(pv, vv.z, a2);
+              a3 = fmaf(pv, vv.w, a3);
+            }
+            oacc[i][0] = a0; oacc[i][1] = a1; oacc[i][2] = a2; oacc[i][3] = a3;
+          }
+        }
+        __syncthreads();
+        if (warp == 0 && tile + 2 < ntiles && misc[0] == 0) {
+          fence_proxy_async();
+          issue(tile + 2, stage);
+        }
+      }
+      const int c4 = tid % C4, qg = tid / C4;
+#pragma unroll
+      for (int i = 0; i < QPT; ++i) {
+        const int qi = qg + QG * i;
+        if (qi >= G) continue;
+        const int owner = qi / rpo, ro = qi - owner * rpo;
+        *reinterpret_cast<float4*>(peer(recv_o, owner) + (rank * rpo + ro) * D + c4 * 4) =
+            make_float4(oacc[i][0], oacc[i][1], oacc[i][2], oacc[i][3]);
+        if (c4 == 0) {
+          float* dst = peer(recv_ml, owner) + (rank * rpo + ro) * 2;
+          dst[0] = m_run[qi];
+          dst[1] = l_run[qi];
+        }
+      }
+    }
+    cluster.sync();
+    // Finalise this CTA's query rows [rank * rpo, ...): merge the cs partials.
+    const int q0 = rank * rpo, q1 = min(G, q0 + rpo);
+    for (int e = tid; e < (q1 - q0) * D; e += kThreads) {
+      const int ro = e / D, col = e % D;
+      float mx = -INFINITY;
+      for (int r = 0; r < cs; ++r) mx = fmaxf(mx, recv_ml[(r * rpo + ro) * 2]);
+      float acc = 0.f, l = 0.f;
+      for (int r = 0; r < cs; ++r) {
+        const float f = safe_exp2_diff(recv_ml[(r * rpo + ro) * 2], mx);
+        acc += f * recv_o[(r * rpo + ro) * D + col];
+        l += f * recv_ml[(r * rpo + ro) * 2 + 1];
+      }
+      const int qi = q0 + ro;
+      p.o[(unit * G + qi) * D + col] = acc / l;
+      if (col == 0 && p.lse != nullptr) p.lse[unit * G + qi] = (mx + log2f(l)) * kLn2;
+    }
+  }
+  cluster.sync();  // peers may still read or write this CTA's shared memory
+}
+
+template <typename T, int D>
+cudaError_t launch_typed(int64_t units, const PathParams& prm, size_t smem, cudaStream_t stream) {
+  const cudaError_t e = ensure_max_smem<path_kernel<T, D>>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(prm.cs, static_cast<unsigned>(units), 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = prm.cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, path_kernel<T, D>, prm);
+}
+
+size_t smem_bytes(const LaunchDims& ld, const PathParams& p) {
+  if (ld.dtype == WF_BF16)
+    return ld.head_dim == 128 ? PathSmem<__nv_bfloat16, 128>(p).total
+                              : PathSmem<__nv_bfloat16, 64>(p).total;
+  return ld.head_dim == 128 ? PathSmem<float, 128>(p).total : PathSmem<float, 64>(p).total;
+}
+
+int pow2_floor(int x) {
+  int p = 1;
+  while (p * 2 <= x) p *= 2;
+  return p;
+}
+
+}  // namespace
+
+int device_sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    (void)cudaGetLastError();
+    return 152;  // GB300
+  }
+  int v = cached[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+    (void)cudaGetLastError();
+    return 152;
+  }
+  cached[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+// Plans a launch of the phases in `mode` (see PathPlan).  k may be null when
+// the filter phase is not run (kL and budget come from the arguments).
+bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int budget,
+               int sm_count, PathPlan* plan) {
+  PathParams p = {};
+  p.mode = mode;
+  p.G = ld.n_gen;
+  p.levels = ld.levels;
+  p.n_prompt = ld.n_prompt;
+  p.P = ld.n_prompt >> ld.levels;
+  p.kL = k_l;
+  p.budget = budget;
+  p.n_keys = budget + ld.n_gen;
+  // One wave of clusters (one CTA per SM): the largest power-of-two cluster
+  // with units * cs <= SMs, capped by the work each phase can split.
+  int cs = pow2_floor(std::max(1, static_cast<int>(std::min<int64_t>(kMaxCluster, sm_count / std::max<int64_t>(1, ld.units)))));
+  if (mode & kModeScore) {
+    while (cs > 1 && (p.P % cs != 0 || p.P / cs < 8)) cs /= 2;
+  }
+  if (mode & kModeFilter) {
+    while (cs > 1 && k_l < cs) cs /= 2;
+  }
+  if (mode & kModeAttend) {
+    while (cs > 1 && p.n_keys < 16 * cs) cs /= 2;
+  }
+  p.cs = cs;
+  p.per_cta_p = (mode & kModeScore) ? p.P / cs : 0;
+  const int spans_cap = (mode & kModeFilter) ? (k_l + cs - 1) / cs : 0;
+  p.rows_cap = spans_cap << ld.levels;
+  int sc = 1;
+  while (sc < std::max(k_l, 1)) sc <<= 1;
+  p.sorted_cap = (mode & kModeFilter) ? sc : 0;
+  p.keys_cap = std::max(p.per_cta_p, p.rows_cap);
+  p.gather_all = static_cast<int64_t>(cs) * p.keys_cap <= 8192 ? 1 : 0;
+  p.klist_cap = (mode & kModeAttend) ? (p.n_keys + cs - 1) / cs + 1 : 0;
+  if (ld.dtype == WF_BF16) {
+    const int mb = ld.n_gen <= 16 ? 1 : (ld.n_gen <= 32 ? 2 : 4);
+    p.tile_keys = 16 * (kWarps / mb);
+  } else {
+    p.tile_keys = 32;
+  }
+  // Token logits in shared memory when they fit, else in the workspace.
+  p.t_ws = nullptr;
+  size_t smem = smem_bytes(ld, p);
+  bool t_in_smem = true;
+  if ((mode & kModeFilter) && smem > kMaxSmem) {
+    p.t_ws = reinterpret_cast<float*>(16);  // placeholder: only its nullness matters here
+    smem = smem_bytes(ld, p);
+    t_in_smem = false;
+  }
+  plan->cluster = cs;
+  plan->smem_bytes = smem;
+  plan->t_in_smem = t_in_smem;
+  plan->t_bytes = t_in_smem ? 0
+                            : sizeof(float) * static_cast<size_t>(ld.units) * cs * p.rows_cap *
+                                  ld.n_gen;
+  plan->per_cta_p = p.per_cta_p;
+  plan->rows_cap = p.rows_cap;
+  plan->sorted_cap = p.sorted_cap;
+  plan->keys_cap = p.keys_cap;
+  plan->gather_all = p.gather_all;
+  plan->klist_cap = p.klist_cap;
+  plan->tile_keys = p.tile_keys;
+  plan->mode = mode;
+  return smem <= kMaxSmem;
+}
+
+cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathArgs& a,
+                        cudaStream_t stream) {
+  PathParams p = {};
+  p.q = a.q;
+  p.kp = a.kp;
+  p.vp = a.vp;
+  p.kg = a.kg;
+  p.vg = a.vg;
+  p.al = a.al;
+  p.idx_l_in = a.idx_l_in;
+  p.idx_in = a.idx_in;
+  p.idx_l_out = a.idx_l_out;
+  p.scores_out = a.scores_out;
+  p.idx_out = a.idx_out;
+  p.o = a.o;
+  p.lse = a.lse;
+  p.status = a.status;
+  p.t_ws = plan.t_in_smem ? nullptr : a.t_ws;
+  p.mode = plan.mode;
+  p.n_prompt = ld.n_prompt;
+  p.G = ld.n_gen;
+  p.levels = ld.levels;
+  p.P = ld.n_prompt >> ld.levels;
+  p.kL = a.k_l;
+  p.budget = a.budget;
+  p.n_keys = a.budget + ld.n_gen;
+  p.cs = plan.cluster;
+  p.per_cta_p = plan.per_cta_p;
+  p.rows_cap = plan.rows_cap;
+  p.sorted_cap = plan.sorted_cap;
+  p.keys_cap = plan.keys_cap;
+  p.gather_all = plan.gather_all;
+  p.klist_cap = plan.klist_cap;
+  p.tile_keys = plan.tile_keys;
+  for (int j = 0; j <= ld.levels; ++j) {
+    p.k[j] = a.k != nullptr ? a.k[j] : 0;
+    p.scale[j] = static_cast<float>(std::pow(2.0, -0.5 * j) / std::sqrt(static_cast<double>(ld.head_dim)));
+  }
+  p.inv_sqrt_d = static_cast<float>(1.0 / std::sqrt(static_cast<double>(ld.head_dim)));
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(ld.head_dim)));
+  if (ld.dtype == WF_BF16) {
+    if (ld.head_dim == 128) return launch_typed<__nv_bfloat16, 128>(ld.units, p, plan.smem_bytes, stream);
+    return launch_typed<__nv_bfloat16, 64>(ld.units, p, plan.smem_bytes, stream);
+  }
+  if (ld.head_dim == 128) return launch_typed<float, 128>(ld.units, p, plan.smem_bytes, stream);
+  return launch_typed<float, 64>(ld.units, p, plan.smem_bytes, stream);
+}
+
+}  // namespace wf
