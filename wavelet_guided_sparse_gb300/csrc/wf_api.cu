@@ -178,12 +178,12 @@ int wf_dwt_lowpass(const wf_dims* dims, const void* Kp, float* AL, float* A_all,
   if (Kp == nullptr || AL == nullptr) return WF_ERR_NULL;
   if (!aligned16(Kp) || !aligned16(AL) || (A_all && !aligned16(A_all))) return WF_ERR_ALIGNMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = wf::launch_dwt_lowpass(ld, Kp, AL, ld.levels, s);
+  cudaError_t e = wf::launch_dwt_lowpass(ld, Kp, AL, ld.levels, nullptr, s);
   if (e == cudaSuccess && A_all != nullptr) {
     // Test aid: every level j = 1..L, each from its own pass over Kp.
     size_t off = 0;
     for (int j = 1; j <= ld.levels && e == cudaSuccess; ++j) {
-      e = wf::launch_dwt_lowpass(ld, Kp, A_all + off, j, s);
+      e = wf::launch_dwt_lowpass(ld, Kp, A_all + off, j, nullptr, s);
       off += static_cast<size_t>(ld.units) * (ld.n_prompt >> j) * ld.head_dim;
     }
   }
@@ -307,7 +307,7 @@ int wf_step(const wf_dims* dims, const void* Q, const void* Kp, const void* Vp, 
   char* ws = static_cast<char*>(workspace);
   float* al = reinterpret_cast<float*>(ws + L.al);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = wf::launch_dwt_lowpass(ld, Kp, al, ld.levels, s);
+  cudaError_t e = wf::launch_dwt_lowpass(ld, Kp, al, ld.levels, status_word(workspace), s);
   if (e != cudaSuccess) return cuda_status(e);
   wf::PathArgs a = {};
   a.q = Q;

@@ -5,12 +5,17 @@
 // on pairs (2n, 2n+1) the level-L approximation is a scaled span sum:
 //   A_L[p] = 2^(-L/2) · Σ_{n in [p·2^L, (p+1)·2^L)} Kp[n].
 //
-// Design (HBM-bound, one read of Kp): every thread owns one 16-byte column
-// chunk of one span (8 bf16 or 4 fp32 channels) and walks the span's 2^L
-// rows with up to 16 independent 16-byte loads in flight, accumulating in
-// fp32 registers.  Adjacent lanes own adjacent chunks of the same row, so a
-// warp instruction reads whole 256-byte rows (d = 128, bf16).  Spans are
-// contiguous in memory, so a unit's Kp is streamed front to back exactly once.
+// Design (HBM-bound, one read of Kp): spans of consecutive units are
+// contiguous in memory, so the whole input is one byte stream.  A persistent
+// grid of one CTA per SM splits the spans evenly; each CTA streams its
+// contiguous byte range through a ring of three 64 KB shared-memory stages
+// filled by single bulk copies (TMA engine, mbarrier completion), so 128-192
+// KB per SM are in flight independent of register pressure.  Threads reduce
+// the staged rows in fp32: for spans of up to 16 rows one thread owns one
+// (span, 16-byte column chunk) pair; longer spans are summed in 16-row blocks
+// whose partials are combined in a fixed order, with a running sum carried
+// across stages for spans longer than a stage.
+#include <algorithm>
 #include <cmath>
 
 #include "wf_common.cuh"
@@ -18,81 +23,181 @@
 
 namespace wf {
 
-// UNROLL (even, >= 2) rows per group; 2^levels must be a multiple of UNROLL.
-template <typename T, int D, int UNROLL>
-__global__ void __launch_bounds__(kThreads) dwt_lowpass_kernel(const T* __restrict__ kp,
-                                                               float* __restrict__ out,
-                                                               int64_t n_spans, int levels,
-                                                               float scale) {
-  constexpr int V = Elem<T>::kPer16B;  // channels per 16-byte chunk
-  constexpr int C = D / V;             // chunks per row
-  const int64_t item = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-  const int64_t span = item / C;
-  const int chunk = static_cast<int>(item % C);
-  if (span >= n_spans) return;
-  const int rows = 1 << levels;
-  const T* src = kp + (span << levels) * D + chunk * V;
-  float acc[V];
+namespace {
+
+constexpr int kStageBytes = 64 * 1024;
+constexpr int kStages = 3;
+
+template <typename T, int D>
+struct DwtSmem {
+  static constexpr int kRowBytes = D * static_cast<int>(sizeof(T));
+  static constexpr int kRows = kStageBytes / kRowBytes;  // rows per stage
+  static constexpr int V = Elem<T>::kPer16B;
+  static constexpr int C = D / V;                        // 16-byte chunks per row
+  static constexpr size_t kBars = 0;
+  static constexpr size_t kRing = 128;
+  static constexpr size_t kPart = kRing + static_cast<size_t>(kStages) * kStageBytes;
+  static constexpr size_t kCarry = kPart + sizeof(float) * (kRows / 16) * C * V;
+  static constexpr size_t kTotal = kCarry + sizeof(float) * C * V;
+};
+
+template <typename T>
+__device__ __forceinline__ void add_chunk(const unsigned char* p, float* acc) {
+  const uint4 v = *reinterpret_cast<const uint4*>(p);
+  float f[Elem<T>::kPer16B];
+  widen16(v, static_cast<const T*>(nullptr), f);
 #pragma unroll
-  for (int v = 0; v < V; ++v) acc[v] = 0.f;
-#pragma unroll 1
-  for (int r0 = 0; r0 < rows; r0 += UNROLL) {
-    uint4 raw[UNROLL];
-#pragma unroll
-    for (int i = 0; i < UNROLL; ++i) raw[i] = ldg16_stream(src + static_cast<int64_t>(r0 + i) * D);
-    // The arithmetic below consumes these (ordered) pass-through values, so
-    // all UNROLL loads are issued before the first add waits on memory.
-#pragma unroll
-    for (int i = 0; i < UNROLL; ++i)
-      asm volatile("" : "+r"(raw[i].x), "+r"(raw[i].y), "+r"(raw[i].z), "+r"(raw[i].w));
-    // Pairwise within the group keeps the fp32 error of long spans small.
-#pragma unroll
-    for (int i = 0; i < UNROLL; i += 2) {
-      float a[V], b[V];
-      widen16(raw[i], static_cast<const T*>(nullptr), a);
-      widen16(raw[i + 1], static_cast<const T*>(nullptr), b);
-#pragma unroll
-      for (int v = 0; v < V; ++v) acc[v] += a[v] + b[v];
-    }
-  }
-  float4* dst = reinterpret_cast<float4*>(out + span * D + chunk * V);
-#pragma unroll
-  for (int v = 0; v < V; v += 4)
-    dst[v / 4] = make_float4(acc[v] * scale, acc[v + 1] * scale, acc[v + 2] * scale,
-                             acc[v + 3] * scale);
+  for (int i = 0; i < Elem<T>::kPer16B; ++i) acc[i] += f[i];
 }
 
 template <typename T, int D>
-static cudaError_t launch_dwt_typed(const void* kp, float* out, int64_t units, int n_prompt,
-                                    int levels, cudaStream_t stream) {
-  constexpr int C = D / Elem<T>::kPer16B;
-  const int64_t n_spans = units * (n_prompt >> levels);
-  const int64_t items = n_spans * C;
-  const int64_t blocks = (items + kThreads - 1) / kThreads;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const float scale = static_cast<float>(std::pow(2.0, -0.5 * levels));  // 2^(-L/2)
-  const T* k = static_cast<const T*>(kp);
-  const dim3 grid(static_cast<unsigned>(blocks));
-  switch (levels) {
-    case 1: dwt_lowpass_kernel<T, D, 2><<<grid, kThreads, 0, stream>>>(k, out, n_spans, levels, scale); break;
-    case 2: dwt_lowpass_kernel<T, D, 4><<<grid, kThreads, 0, stream>>>(k, out, n_spans, levels, scale); break;
-    case 3: dwt_lowpass_kernel<T, D, 8><<<grid, kThreads, 0, stream>>>(k, out, n_spans, levels, scale); break;
-    default: dwt_lowpass_kernel<T, D, 16><<<grid, kThreads, 0, stream>>>(k, out, n_spans, levels, scale); break;
+__global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __restrict__ kp,
+                                                                 float* __restrict__ out,
+                                                                 int64_t n_spans,
+                                                                 int64_t spans_per_cta,
+                                                                 int levels, float scale,
+                                                                 int32_t* status) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  using S = DwtSmem<T, D>;
+  constexpr int RB = S::kRowBytes, SR = S::kRows, V = S::V, C = S::C;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBars);
+  unsigned char* ring = smem + S::kRing;
+  float* part = reinterpret_cast<float*>(smem + S::kPart);
+  float* carry = reinterpret_cast<float*>(smem + S::kCarry);
+  __shared__ int aborted;
+  const int tid = threadIdx.x;
+  const int64_t s_begin = static_cast<int64_t>(blockIdx.x) * spans_per_cta;
+  const int64_t s_end = min(n_spans, s_begin + spans_per_cta);
+  if (s_begin >= s_end) return;  // whole CTA, before any barrier
+  const int span_rows = 1 << levels;
+  const int64_t rows_total = (s_end - s_begin) << levels;
+  const int64_t n_stages = (rows_total + SR - 1) / SR;
+  const unsigned char* src = reinterpret_cast<const unsigned char*>(kp + (s_begin << levels) * D);
+  float* dst = out + s_begin * D;
+
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+    aborted = 0;
   }
+  __syncthreads();
+  auto issue = [&](int64_t st) {  // thread 0 only
+    const int64_t rows = min(static_cast<int64_t>(SR), rows_total - st * SR);
+    const uint32_t bytes = static_cast<uint32_t>(rows * RB);
+    uint64_t* bar = &bars[st % kStages];
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(ring + (st % kStages) * kStageBytes, src + st * static_cast<int64_t>(SR) * RB, bytes,
+             bar);
+  };
+  if (tid == 0)
+    for (int64_t st = 0; st < kStages && st < n_stages; ++st) issue(st);
+
+  for (int64_t st = 0; st < n_stages; ++st) {
+    int ok = 1;
+    if (aborted == 0)
+      ok = mbar_wait_bounded(&bars[st % kStages], static_cast<uint32_t>((st / kStages) & 1), status)
+               ? 1
+               : 0;
+    if (__syncthreads_or(!ok) && tid == 0) aborted = 1;
+    const unsigned char* buf = ring + (st % kStages) * kStageBytes;
+    const int rows_in = static_cast<int>(min(static_cast<int64_t>(SR), rows_total - st * SR));
+    const int64_t first_row = st * SR;
+    if (span_rows <= 16) {
+      // One thread per (span, chunk) of this stage; a stage holds whole spans.
+      const int spans_in = rows_in >> levels;
+      const int64_t span0 = first_row >> levels;
+      for (int item = tid; item < spans_in * C; item += kThreads) {
+        const int sl = item / C, c = item % C;
+        float acc[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[v] = 0.f;
+        const unsigned char* p = buf + (sl << levels) * RB + c * 16;
+        for (int r = 0; r < span_rows; ++r) add_chunk<T>(p + r * RB, acc);
+        float4* o = reinterpret_cast<float4*>(dst + (span0 + sl) * D + c * V);
+#pragma unroll
+        for (int v = 0; v < V; v += 4)
+          o[v / 4] = make_float4(acc[v] * scale, acc[v + 1] * scale, acc[v + 2] * scale,
+                                 acc[v + 3] * scale);
+      }
+    } else {
+      // 16-row block partials, then per-span combination in block order.
+      const int nblk = rows_in / 16;
+      for (int item = tid; item < nblk * C; item += kThreads) {
+        const int b = item / C, c = item % C;
+        float acc[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[v] = 0.f;
+        const unsigned char* p = buf + (b * 16) * RB + c * 16;
+#pragma unroll 4
+        for (int r = 0; r < 16; ++r) add_chunk<T>(p + r * RB, acc);
+#pragma unroll
+        for (int v = 0; v < V; ++v) part[(b * C + c) * V + v] = acc[v];
+      }
+      __syncthreads();
+      const int64_t sp0 = first_row >> levels;
+      const int64_t sp1 = (first_row + rows_in - 1) >> levels;
+      const int nsp = static_cast<int>(sp1 - sp0 + 1);
+      for (int item = tid; item < nsp * C; item += kThreads) {
+        const int sl = item / C, c = item % C;
+        const int64_t span = sp0 + sl;
+        const int64_t r_lo = max(span << levels, first_row);
+        const int64_t r_hi = min((span + 1) << levels, first_row + rows_in);
+        const bool carried = (span << levels) < first_row;
+        float acc[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[v] = carried ? carry[c * V + v] : 0.f;
+        for (int b = static_cast<int>((r_lo - first_row) / 16); b < (r_hi - first_row) / 16; ++b)
+#pragma unroll
+          for (int v = 0; v < V; ++v) acc[v] += part[(b * C + c) * V + v];
+        if (((span + 1) << levels) <= first_row + rows_in) {
+          float4* o = reinterpret_cast<float4*>(dst + span * D + c * V);
+#pragma unroll
+          for (int v = 0; v < V; v += 4)
+            o[v / 4] = make_float4(acc[v] * scale, acc[v + 1] * scale, acc[v + 2] * scale,
+                                   acc[v + 3] * scale);
+        } else {
+#pragma unroll
+          for (int v = 0; v < V; ++v) carry[c * V + v] = acc[v];
+        }
+      }
+    }
+    __syncthreads();  // stage consumed (and carry / partials settled)
+    if (tid == 0 && st + kStages < n_stages && aborted == 0) {
+      fence_proxy_async();
+      issue(st + kStages);
+    }
+  }
+}
+
+template <typename T, int D>
+cudaError_t launch_typed(const void* kp, float* out, int64_t units, int n_prompt, int levels,
+                         int32_t* status, cudaStream_t stream) {
+  const cudaError_t e = ensure_max_smem<dwt_stream_kernel<T, D>>();
+  if (e != cudaSuccess) return e;
+  const int64_t n_spans = units * (n_prompt >> levels);
+  const int64_t grid = std::min<int64_t>(device_sm_count(), n_spans);
+  const int64_t per = (n_spans + grid - 1) / grid;
+  const int64_t blocks = (n_spans + per - 1) / per;
+  const float scale = static_cast<float>(std::pow(2.0, -0.5 * levels));  // 2^(-L/2)
+  dwt_stream_kernel<T, D><<<static_cast<unsigned>(blocks), kThreads, DwtSmem<T, D>::kTotal,
+                            stream>>>(static_cast<const T*>(kp), out, n_spans, per, levels, scale,
+                                      status);
   return cudaGetLastError();
 }
 
+}  // namespace
+
 cudaError_t launch_dwt_lowpass(const LaunchDims& ld, const void* kp, float* out, int levels,
-                               cudaStream_t stream) {
-  const int64_t units = ld.units;
+                               int32_t* status, cudaStream_t stream) {
   if (ld.dtype == WF_BF16) {
     if (ld.head_dim == 128)
-      return launch_dwt_typed<__nv_bfloat16, 128>(kp, out, units, ld.n_prompt, levels, stream);
-    return launch_dwt_typed<__nv_bfloat16, 64>(kp, out, units, ld.n_prompt, levels, stream);
+      return launch_typed<__nv_bfloat16, 128>(kp, out, ld.units, ld.n_prompt, levels, status,
+                                              stream);
+    return launch_typed<__nv_bfloat16, 64>(kp, out, ld.units, ld.n_prompt, levels, status, stream);
   }
   if (ld.head_dim == 128)
-    return launch_dwt_typed<float, 128>(kp, out, units, ld.n_prompt, levels, stream);
-  return launch_dwt_typed<float, 64>(kp, out, units, ld.n_prompt, levels, stream);
+    return launch_typed<float, 128>(kp, out, ld.units, ld.n_prompt, levels, status, stream);
+  return launch_typed<float, 64>(kp, out, ld.units, ld.n_prompt, levels, status, stream);
 }
 
 }  // namespace wf

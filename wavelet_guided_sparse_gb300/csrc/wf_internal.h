@@ -65,7 +65,7 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
                int sm_count, PathPlan* plan);
 
 cudaError_t launch_dwt_lowpass(const LaunchDims& ld, const void* kp, float* out, int levels,
-                               cudaStream_t stream);
+                               int32_t* status, cudaStream_t stream);
 cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathArgs& args,
                         cudaStream_t stream);
 
