@@ -134,3 +134,14 @@ def test_product_path_has_no_oracle_dependency():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(root, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+@pytest.mark.parametrize("name", sorted(wl.CONFIGS))
+def test_every_workload_is_planned(lib, name):
+    # Every configuration fits the kernels' shared-memory plans (no launch).
+    cfg = wl.CONFIGS[name]
+    dims = bd.Dims(cfg.batch, cfg.heads, cfg.n_prompt, cfg.n_gen, cfg.head_dim, cfg.levels,
+                   0 if cfg.dtype == "bf16" else 1)
+    st, n = _ws(dims, cfg.k_per_level())
+    assert st == 0, name
+    assert n >= cfg.units_per_layer * (cfg.n_prompt >> cfg.levels) * cfg.head_dim * 4

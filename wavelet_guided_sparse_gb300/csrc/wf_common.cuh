@@ -196,7 +196,8 @@ __device__ __forceinline__ P* peer(P* local, int rank) {
   return cg::this_cluster().map_shared_rank(local, rank);
 }
 
-// (m, l) online-softmax pair merge; pairs with m = -inf (empty) are skipped.
+// (m, l) softmax-statistics merge in the log2 domain (l = Σ 2^(z - m));
+// pairs with m = -inf (empty) are skipped.
 __device__ __forceinline__ void merge_ml(float& m, float& l, float m2, float l2) {
   if (m2 == -INFINITY) return;
   if (m == -INFINITY) {
@@ -205,15 +206,15 @@ __device__ __forceinline__ void merge_ml(float& m, float& l, float m2, float l2)
     return;
   }
   const float mx = fmaxf(m, m2);
-  l = l * expf(m - mx) + l2 * expf(m2 - mx);
+  l = l * exp2f(m - mx) + l2 * exp2f(m2 - mx);
   m = mx;
 }
 
 constexpr int kMaxQ = 64;  // maximum queries per unit
 
-// All-reduce of per-query softmax statistics over the cluster.  loc_m/loc_l
-// hold this CTA's (max, sum of exp) per query; on return gm/ginv hold the
-// cluster-wide max and 1 / sum.  stat_in: [kMaxCluster][2][kMaxQ] floats.
+// All-reduce of per-query softmax statistics (log2 domain) over the cluster.
+// loc_m/loc_l hold this CTA's (max, Σ 2^(z - max)) per query; on return
+// gm/ginv hold the cluster-wide max and 1 / sum.  stat_in: [kMaxCluster][2][kMaxQ] floats.
 __device__ inline void cluster_merge_stats(const float* loc_m, const float* loc_l, int G,
                                            float* stat_in, float* gm, float* ginv) {
   cg::cluster_group cluster = cg::this_cluster();

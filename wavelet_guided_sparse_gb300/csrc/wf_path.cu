@@ -42,7 +42,9 @@ namespace wf {
 
 namespace {
 
-constexpr int kTileRows = 64;  // filter: token rows per staged tile
+constexpr int kTileRows = 64;    // filter: token rows per staged tile
+constexpr int kScoreChunk = 64;  // score: coarse positions per staged chunk
+constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 enum : int { kModeScore = 1, kModeFilter = 2, kModeAttend = 4 };
@@ -75,7 +77,7 @@ template <typename T, int D>
 struct PathSmem {
   static constexpr int kRowBytes = D * static_cast<int>(sizeof(T)) + 16;  // padded row pitch
   static constexpr int kRowF = D + 4;                                      // fp32 row pitch
-  size_t bars, qs, stat_in, gm, part, cnt_a, cnt_b, misc, sl_all, sp, sr, cp, cr, keys, take,
+  size_t bars, qs, stat_in, gm, loc, part, cnt_a, cnt_b, misc, sl_all, sp, sr, cp, cr, keys, take,
       topk, keys_all, klist;
   size_t s_qf, s_as, s_z;          // score phase
   size_t f_kst, f_t;               // filter phase
@@ -92,6 +94,7 @@ struct PathSmem {
     qs = take_bytes(static_cast<size_t>(kMaxQ) * kRowBytes);
     stat_in = take_bytes(sizeof(float) * kMaxCluster * 2 * kMaxQ);
     gm = take_bytes(sizeof(float) * 2 * kMaxQ);
+    loc = take_bytes(sizeof(float) * 2 * kMaxQ);
     part = take_bytes(sizeof(float) * 2 * kWarps * kMaxQ);
     cnt_a = take_bytes(sizeof(int32_t) * kMaxCluster);
     cnt_b = take_bytes(sizeof(int32_t) * kMaxCluster);
@@ -110,15 +113,16 @@ struct PathSmem {
     size_t end = u;
     if (p.mode & kModeScore) {
       o = u;
-      s_qf = sizeof(T) == 4 ? qs : take_bytes(sizeof(float) * kMaxQ * kRowF);
-      s_as = take_bytes(sizeof(float) * 32 * kRowF);
-      s_z = take_bytes(sizeof(float) * static_cast<size_t>(p.G) * p.per_cta_p);
+      s_qf = 0;
+      // A_L chunk: three bf16 planes (bf16 inputs) or one fp32 tile, 64 rows.
+      s_as = take_bytes(static_cast<size_t>(sizeof(T) == 2 ? 3 : 1) * kScoreChunk * kRowBytes);
+      s_z = take_bytes(sizeof(float) * static_cast<size_t>(kScoreChunk) * (p.G | 1));
       end = end > o ? end : o;
     }
     if (p.mode & kModeFilter) {
       o = u;
       f_kst = take_bytes(static_cast<size_t>(2) * kTileRows * kRowBytes);
-      f_t = p.t_ws == nullptr ? take_bytes(sizeof(float) * static_cast<size_t>(p.rows_cap) * p.G) : 0;
+      f_t = p.t_ws == nullptr ? take_bytes(sizeof(float) * static_cast<size_t>(p.rows_cap) * (p.G | 1)) : 0;
       end = end > o ? end : o;
     }
     if (p.mode & kModeAttend) {
@@ -167,13 +171,18 @@ __device__ __forceinline__ TopkResult cluster_select(const PathParams& p, const 
   return topk_distributed(keys, n, k, take, tk);
 }
 
-// ------------------------------------------------------------------ token logits tile
-// bf16: t rows [row0, row0 + 64) from the staged key rows.  Warp w: 16-row
-// block (w & 3), n-blocks (w >> 2) + 2i of 8 queries each.
+// ------------------------------------------------------------------ logits tiles
+// bf16: out[r][i] = scale * Σ_planes rows[r]·Q[i] for the 64 staged rows
+// (out row pitch `pitch` floats).  `nplanes` bf16 row tiles of 64 rows each,
+// `plane_bytes` apart, are accumulated (one plane for key rows; three planes
+// hi + mid + lo reproduce an fp32 row exactly).  Warp w: 16-row block (w & 3),
+// n-blocks (w >> 2) + 2i of 8 queries each.
 template <int D>
-__device__ __forceinline__ void token_logits_tile(const unsigned char* kst,
-                                                  const uint32_t (&bq)[4][D / 16][2], float* t,
-                                                  int row0, int rows_valid, int G) {
+__device__ __forceinline__ void logits_tile_bf16(const unsigned char* rows, int nplanes,
+                                                 int plane_bytes,
+                                                 const uint32_t (&bq)[4][D / 16][2], float* out,
+                                                 int row0, int rows_valid, int G, int pitch,
+                                                 float scale) {
   constexpr int RB = D * 2 + 16;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int mb = warp & 3, ng = warp >> 2;
@@ -183,14 +192,17 @@ __device__ __forceinline__ void token_logits_tile(const unsigned char* kst,
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
-  const uint32_t abase = smem_u32(kst) + (mb * 16 + (lane & 15)) * RB + (lane >> 4) * 16;
+  for (int pl = 0; pl < nplanes; ++pl) {
+    const uint32_t abase =
+        smem_u32(rows + pl * plane_bytes) + (mb * 16 + (lane & 15)) * RB + (lane >> 4) * 16;
 #pragma unroll
-  for (int ks = 0; ks < D / 16; ++ks) {
-    uint32_t a[4];
-    ldsm_x4(abase + ks * 32, a);
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t a[4];
+      ldsm_x4(abase + ks * 32, a);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (ng + 2 * i < NB) mma_bf16(acc[i], a, bq[i][ks]);
+      for (int i = 0; i < 4; ++i)
+        if (ng + 2 * i < NB) mma_bf16(acc[i], a, bq[i][ks]);
+    }
   }
   const int r_lo = mb * 16 + (lane >> 2);
 #pragma unroll
@@ -202,17 +214,35 @@ __device__ __forceinline__ void token_logits_tile(const unsigned char* kst,
     for (int h = 0; h < 2; ++h) {
       const int r = r_lo + 8 * h;
       if (r >= rows_valid) continue;
-      float* dst = t + static_cast<int64_t>(row0 + r) * G;
-      if (q0 < G) dst[q0] = acc[i][2 * h];
-      if (q0 + 1 < G) dst[q0 + 1] = acc[i][2 * h + 1];
+      float* dst = out + static_cast<int64_t>(row0 + r) * pitch;
+      if (q0 < G) dst[q0] = acc[i][2 * h] * scale;
+      if (q0 + 1 < G) dst[q0 + 1] = acc[i][2 * h + 1] * scale;
     }
+  }
+}
+
+// Q B-fragments (8 queries x 16 dims per n-block) of this warp's n-blocks.
+template <int D>
+__device__ __forceinline__ void load_q_frags(const unsigned char* qs, int G,
+                                             uint32_t (&bq)[4][D / 16][2]) {
+  constexpr int RB = D * 2 + 16;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int NB = (G + 7) >> 3, ng = warp >> 2;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int nb = min(ng + 2 * i, NB - 1);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks)
+      ldsm_x2(smem_u32(qs) + (nb * 8 + (lane & 7)) * RB + ks * 32 + ((lane >> 3) & 1) * 16,
+              bq[i][ks]);
   }
 }
 
 // fp32: plain FMAs.  Thread -> row (tid & 63), queries (tid >> 6) + 4i.
 template <int D>
-__device__ __forceinline__ void token_logits_tile_f32(const unsigned char* kst, const float* qs,
-                                                      float* t, int row0, int rows_valid, int G) {
+__device__ __forceinline__ void logits_tile_f32(const unsigned char* kst, const float* qs,
+                                                float* t, int row0, int rows_valid, int G,
+                                                int pitch, float scale) {
   constexpr int RF = D + 4;
   const int r = threadIdx.x & 63, g = threadIdx.x >> 6;
   if (r >= rows_valid) return;
@@ -232,18 +262,19 @@ __device__ __forceinline__ void token_logits_tile_f32(const unsigned char* kst, 
       acc[i] = fmaf(a.w, b.w, acc[i]);
     }
   }
-  float* dst = t + static_cast<int64_t>(row0 + r) * G;
+  float* dst = t + static_cast<int64_t>(row0 + r) * pitch;
 #pragma unroll
   for (int i = 0; i < 16; ++i)
-    if (g + 4 * i < G) dst[g + 4 * i] = acc[i];
+    if (g + 4 * i < G) dst[g + 4 * i] = acc[i] * scale;
 }
 
+// Running (max, Σ 2^(z - max)) update (log2 domain).
 __device__ __forceinline__ void online_update(float& m, float& l, float z) {
   if (z > m) {
-    l = l * expf(m - z) + 1.f;
+    l = l * exp2f(m - z) + 1.f;
     m = z;
   } else {
-    l += expf(z - m);
+    l += exp2f(z - m);
   }
 }
 
@@ -281,6 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   float* stat_in = reinterpret_cast<float*>(smem + L.stat_in);
   float* gm = reinterpret_cast<float*>(smem + L.gm);
   float* ginv = gm + kMaxQ;
+  float* loc_m = reinterpret_cast<float*>(smem + L.loc);
+  float* loc_l = loc_m + kMaxQ;
+  const int TS = G | 1;  // odd row pitch of logit tiles: conflict-free row-wise passes
   float* part_m = reinterpret_cast<float*>(smem + L.part);
   float* part_l = part_m + kWarps * kMaxQ;
   int32_t* cnt_a = reinterpret_cast<int32_t*>(smem + L.cnt_a);
@@ -320,71 +354,90 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   // ================================================================ score
   if (p.mode & kModeScore) {
     const int Pc = p.per_cta_p;
-    float* qf = reinterpret_cast<float*>(smem + L.s_qf);
-    float* as = reinterpret_cast<float*>(smem + L.s_as);
-    float* z = reinterpret_cast<float*>(smem + L.s_z);
-    if constexpr (sizeof(T) == 2) {
-      for (int e = tid; e < kMaxQ * D / 2; e += kThreads) {
-        const int r = e / (D / 2), col = (e % (D / 2)) * 2;
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(qs + r * RB + col * 2);
-        qf[r * RF + col] = bf16_lo(w);
-        qf[r * RF + col + 1] = bf16_hi(w);
-      }
-    }
+    unsigned char* as = smem + L.s_as;
+    float* zc = reinterpret_cast<float*>(smem + L.s_z);  // [chunk row][query], log2 domain
+    const float zscale = p.inv_sqrt_d * kLog2e;
     const float* asrc = p.al + (unit * p.P + static_cast<int64_t>(rank) * Pc) * D;
-    for (int c0 = 0; c0 < Pc; c0 += 32) {
+    const int nchunks = (Pc + kScoreChunk - 1) / kScoreChunk;
+    uint32_t bq[4][D / 16][2];
+    if constexpr (sizeof(T) == 2) load_q_frags<D>(qs, G, bq);
+    // z for chunk rows [c0, c0 + rows): stage A_L (bf16 inputs: exact
+    // hi + mid + lo bf16 planes), then one tensor-core / FMA tile.
+    auto chunk_logits = [&](int c0, int rows) {
       __syncthreads();
-      const int rows = min(32, Pc - c0);
       for (int e = tid; e < rows * (D / 4); e += kThreads) {
         const int r = e / (D / 4), col = (e % (D / 4)) * 4;
-        *reinterpret_cast<float4*>(as + r * RF + col) =
-            __ldg(reinterpret_cast<const float4*>(asrc + static_cast<int64_t>(c0 + r) * D + col));
+        const float4 a = __ldg(reinterpret_cast<const float4*>(asrc + static_cast<int64_t>(c0 + r) * D + col));
+        if constexpr (sizeof(T) == 2) {
+          const float av[4] = {a.x, a.y, a.z, a.w};
+          float pv[3][4];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {  // av = hi + mid + lo exactly (to 2^-25 relative)
+            const float hi = __bfloat162float(__float2bfloat16_rn(av[v]));
+            const float r1 = av[v] - hi;
+            const float mid = __bfloat162float(__float2bfloat16_rn(r1));
+            pv[0][v] = hi;
+            pv[1][v] = mid;
+            pv[2][v] = r1 - mid;
+          }
+#pragma unroll
+          for (int pl = 0; pl < 3; ++pl)
+            *reinterpret_cast<uint2*>(as + pl * kScoreChunk * RB + r * RB + col * 2) =
+                make_uint2(pack_bf16(pv[pl][0], pv[pl][1]), pack_bf16(pv[pl][2], pv[pl][3]));
+        } else {
+          *reinterpret_cast<float4*>(as + r * RB + col * 4) = a;
+        }
       }
       __syncthreads();
-      if (lane < rows && warp < G) {  // thread -> A_L row (lane), queries warp + 8i
-        float acc[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-        const float* arow = as + lane * RF;
-#pragma unroll 4
-        for (int col = 0; col < D; col += 4) {
-          const float4 a = *reinterpret_cast<const float4*>(arow + col);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 b = *reinterpret_cast<const float4*>(qf + (warp + 8 * i) * RF + col);
-            acc[i] = fmaf(a.x, b.x, acc[i]);
-            acc[i] = fmaf(a.y, b.y, acc[i]);
-            acc[i] = fmaf(a.z, b.z, acc[i]);
-            acc[i] = fmaf(a.w, b.w, acc[i]);
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int qi = warp + 8 * i;
-          if (qi < G) z[qi * Pc + c0 + lane] = acc[i] * p.inv_sqrt_d;
-        }
+      if constexpr (sizeof(T) == 2) {
+        logits_tile_bf16<D>(as, 3, kScoreChunk * RB, bq, zc, 0, rows, G, TS, zscale);
+      } else {
+        logits_tile_f32<D>(as, reinterpret_cast<const float*>(qs), zc, 0, rows, G, TS, zscale);
+      }
+      __syncthreads();
+    };
+    // Pass 1: per-query (max, sum) over this CTA's positions; thread ->
+    // queries lane / lane + 32, positions warp + 8i of every chunk.
+    float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+    for (int ch = 0; ch < nchunks; ++ch) {
+      const int c0 = ch * kScoreChunk, rows = min(kScoreChunk, Pc - c0);
+      chunk_logits(c0, rows);
+      for (int r = warp; r < rows; r += kWarps) {
+        if (lane < G) online_update(m0, l0, zc[r * TS + lane]);
+        if (lane + 32 < G) online_update(m1, l1, zc[r * TS + lane + 32]);
       }
     }
+    part_m[warp * kMaxQ + lane] = m0;
+    part_l[warp * kMaxQ + lane] = l0;
+    part_m[warp * kMaxQ + lane + 32] = m1;
+    part_l[warp * kMaxQ + lane + 32] = l1;
     __syncthreads();
-    for (int qi = warp; qi < G; qi += kWarps) {
-      float m = -INFINITY;
-      for (int j = lane; j < Pc; j += 32) m = fmaxf(m, z[qi * Pc + j]);
-      m = warp_max(m);
-      float l = 0.f;
-      for (int j = lane; j < Pc; j += 32) l += expf(z[qi * Pc + j] - m);
-      l = warp_sum(l);
-      if (lane == 0) {
-        part_m[qi] = m;
-        part_l[qi] = l;
+    {
+      float cm = -INFINITY, cl = 0.f;
+      if (tid < G)
+        for (int w = 0; w < kWarps; ++w) merge_ml(cm, cl, part_m[w * kMaxQ + tid], part_l[w * kMaxQ + tid]);
+      __syncthreads();
+      if (tid < G) {
+        part_m[tid] = cm;
+        part_l[tid] = cl;
       }
+      __syncthreads();
     }
-    __syncthreads();
     cluster_merge_stats(part_m, part_l, G, stat_in, gm, ginv);
-    for (int j = tid; j < Pc; j += kThreads) {
-      float s = 0.f;
-      for (int qi = 0; qi < G; ++qi) s += expf(z[qi * Pc + j] - gm[qi]) * ginv[qi];
-      keys[j] = __float_as_uint(s);
-      if (p.scores_out != nullptr) p.scores_out[unit * p.P + rank * Pc + j] = s;
+    // Pass 2: attention mass of every position (4 threads per position).
+    for (int ch = 0; ch < nchunks; ++ch) {
+      const int c0 = ch * kScoreChunk, rows = min(kScoreChunk, Pc - c0);
+      if (nchunks > 1) chunk_logits(c0, rows);  // one chunk: zc still holds it
+      const int r = tid >> 2, sub = tid & 3;
+      float sacc = 0.f;
+      if (r < rows)
+        for (int qi = sub; qi < G; qi += 4) sacc += exp2f(zc[r * TS + qi] - gm[qi]) * ginv[qi];
+      sacc += __shfl_xor_sync(0xffffffffu, sacc, 1);
+      sacc += __shfl_xor_sync(0xffffffffu, sacc, 2);
+      if (r < rows && sub == 0) {
+        keys[c0 + r] = __float_as_uint(sacc);
+        if (p.scores_out != nullptr) p.scores_out[unit * p.P + rank * Pc + c0 + r] = sacc;
+      }
     }
     __syncthreads();
     const TopkResult res = cluster_select(p, keys, Pc, p.kL, take, tk, keys_all);
@@ -450,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     unsigned char* kst = smem + L.f_kst;
     float* t = p.t_ws == nullptr
                    ? reinterpret_cast<float*>(smem + L.f_t)
-                   : p.t_ws + (static_cast<int64_t>(unit) * cs + rank) * p.rows_cap * G;
+                   : p.t_ws + (static_cast<int64_t>(unit) * cs + rank) * p.rows_cap * TS;
     const T* kp = static_cast<const T*>(p.kp);
     const int ntiles = (R + kTileRows - 1) / kTileRows;
     auto issue = [&](int tile, int stage) {  // warp 0 only
@@ -471,17 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       if (ntiles > 1) issue(1, 1);
     }
     uint32_t bq[4][D / 16][2];
-    if constexpr (sizeof(T) == 2) {
-      const int NB = (G + 7) >> 3, ng = warp >> 2;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int nb = min(ng + 2 * i, NB - 1);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          ldsm_x2(smem_u32(qs) + (nb * 8 + (lane & 7)) * RB + ks * 32 + ((lane >> 3) & 1) * 16,
-                  bq[i][ks]);
-      }
-    }
+    if constexpr (sizeof(T) == 2) load_q_frags<D>(qs, G, bq);
     for (int tile = 0; tile < ntiles; ++tile) {
       const int stage = tile & 1;
       int ok = 1;
@@ -491,10 +534,10 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       const unsigned char* buf = kst + stage * kTileRows * RB;
       const int rows_valid = min(kTileRows, R - tile * kTileRows);
       if constexpr (sizeof(T) == 2) {
-        token_logits_tile<D>(buf, bq, t, tile * kTileRows, rows_valid, G);
+        logits_tile_bf16<D>(buf, 1, 0, bq, t, tile * kTileRows, rows_valid, G, TS, 1.f);
       } else {
-        token_logits_tile_f32<D>(buf, reinterpret_cast<const float*>(qs), t, tile * kTileRows,
-                                 rows_valid, G);
+        logits_tile_f32<D>(buf, reinterpret_cast<const float*>(qs), t, tile * kTileRows,
+                           rows_valid, G, TS, 1.f);
       }
       __syncthreads();
       if (warp == 0 && tile + 2 < ntiles && misc[0] == 0) {
@@ -526,52 +569,67 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         n_surv = n_cand;
         continue;
       }
+      // Scores of this level's candidates (log2 domain, z = sc2 * Σ_leaves t):
+      //  pass 1  CTA max per query; pass 2  e = 2^(z - max), CTA sum (at level 0
+      //  e overwrites t, which is not needed afterwards); cluster merge;
+      //  pass 3  s_c = Σ_i e[c,i] * w_i with w_i = 2^(max_i - gmax_i) / gsum_i.
       const int leaves = 1 << j;
-      const float sc = p.scale[j];
-      float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+      const float sc2 = p.scale[j] * kLog2e;
+      auto node_logit = [&](int ci, int q) {
+        const float* tp = t + static_cast<int64_t>(cr[ci]) * TS + q;
+        float acc = 0.f;
+        for (int i = 0; i < leaves; ++i) acc += tp[i * TS];
+        return acc * sc2;
+      };
+      float m0 = -INFINITY, m1 = -INFINITY;
       for (int ci = warp; ci < n_cand; ci += kWarps) {
-        const float* tp = t + static_cast<int64_t>(cr[ci]) * G;
-        if (lane < G) {
-          float acc = 0.f;
-          for (int i = 0; i < leaves; ++i) acc += tp[i * G + lane];
-          online_update(m0, l0, acc * sc);
-        }
-        if (lane + 32 < G) {
-          float acc = 0.f;
-          for (int i = 0; i < leaves; ++i) acc += tp[i * G + lane + 32];
-          online_update(m1, l1, acc * sc);
-        }
+        if (lane < G) m0 = fmaxf(m0, node_logit(ci, lane));
+        if (lane + 32 < G) m1 = fmaxf(m1, node_logit(ci, lane + 32));
       }
       part_m[warp * kMaxQ + lane] = m0;
-      part_l[warp * kMaxQ + lane] = l0;
       part_m[warp * kMaxQ + lane + 32] = m1;
-      part_l[warp * kMaxQ + lane + 32] = l1;
-      __syncthreads();
-      float cta_m = -INFINITY, cta_l = 0.f;
-      if (tid < G)
-        for (int w = 0; w < kWarps; ++w) merge_ml(cta_m, cta_l, part_m[w * kMaxQ + tid], part_l[w * kMaxQ + tid]);
       __syncthreads();
       if (tid < G) {
-        part_m[tid] = cta_m;
-        part_l[tid] = cta_l;
+        float m = -INFINITY;
+        for (int w = 0; w < kWarps; ++w) m = fmaxf(m, part_m[w * kMaxQ + tid]);
+        loc_m[tid] = m;
       }
       __syncthreads();
-      cluster_merge_stats(part_m, part_l, G, stat_in, gm, ginv);
+      float e0 = 0.f, e1 = 0.f;
       for (int ci = warp; ci < n_cand; ci += kWarps) {
-        const float* tp = t + static_cast<int64_t>(cr[ci]) * G;
-        float s = 0.f;
         if (lane < G) {
-          float acc = 0.f;
-          for (int i = 0; i < leaves; ++i) acc += tp[i * G + lane];
-          s += expf(acc * sc - gm[lane]) * ginv[lane];
+          const float e = exp2f(node_logit(ci, lane) - loc_m[lane]);
+          e0 += e;
+          if (j == 0) t[static_cast<int64_t>(cr[ci]) * TS + lane] = e;
         }
         if (lane + 32 < G) {
-          float acc = 0.f;
-          for (int i = 0; i < leaves; ++i) acc += tp[i * G + lane + 32];
-          s += expf(acc * sc - gm[lane + 32]) * ginv[lane + 32];
+          const float e = exp2f(node_logit(ci, lane + 32) - loc_m[lane + 32]);
+          e1 += e;
+          if (j == 0) t[static_cast<int64_t>(cr[ci]) * TS + lane + 32] = e;
         }
-        s = warp_sum(s);
-        if (lane == 0) keys[ci] = __float_as_uint(s);
+      }
+      part_l[warp * kMaxQ + lane] = e0;
+      part_l[warp * kMaxQ + lane + 32] = e1;
+      __syncthreads();
+      if (tid < G) {
+        float l = 0.f;
+        for (int w = 0; w < kWarps; ++w) l += part_l[w * kMaxQ + tid];
+        loc_l[tid] = l;
+      }
+      __syncthreads();
+      cluster_merge_stats(loc_m, loc_l, G, stat_in, gm, ginv);
+      float* wq = part_m;  // per-query weights (part_m is free again)
+      if (tid < G) wq[tid] = loc_m[tid] == -INFINITY ? 0.f : exp2f(loc_m[tid] - gm[tid]) * ginv[tid];
+      __syncthreads();
+      for (int ci = tid; ci < n_cand; ci += kThreads) {
+        float s = 0.f;
+        if (j == 0) {
+          const float* ep = t + static_cast<int64_t>(cr[ci]) * TS;
+          for (int q = 0; q < G; ++q) s += ep[q] * wq[q];
+        } else {
+          for (int q = 0; q < G; ++q) s += exp2f(node_logit(ci, q) - loc_m[q]) * wq[q];
+        }
+        keys[ci] = __float_as_uint(s);
       }
       __syncthreads();
       (void)cluster_select(p, keys, n_cand, p.k[j], take, tk, keys_all);
@@ -983,49 +1041,55 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
   p.kL = k_l;
   p.budget = budget;
   p.n_keys = budget + ld.n_gen;
-  // One wave of clusters (one CTA per SM): the largest power-of-two cluster
-  // with units * cs <= SMs, capped by the work each phase can split.
-  int cs = pow2_floor(std::max(1, static_cast<int>(std::min<int64_t>(kMaxCluster, sm_count / std::max<int64_t>(1, ld.units)))));
-  if (mode & kModeScore) {
-    while (cs > 1 && (p.P % cs != 0 || p.P / cs < 8)) cs /= 2;
-  }
-  if (mode & kModeFilter) {
-    while (cs > 1 && k_l < cs) cs /= 2;
-  }
-  if (mode & kModeAttend) {
-    while (cs > 1 && p.n_keys < 16 * cs) cs /= 2;
-  }
-  p.cs = cs;
-  p.per_cta_p = (mode & kModeScore) ? p.P / cs : 0;
-  const int spans_cap = (mode & kModeFilter) ? (k_l + cs - 1) / cs : 0;
-  p.rows_cap = spans_cap << ld.levels;
-  int sc = 1;
-  while (sc < std::max(k_l, 1)) sc <<= 1;
-  p.sorted_cap = (mode & kModeFilter) ? sc : 0;
-  p.keys_cap = std::max(p.per_cta_p, p.rows_cap);
-  p.gather_all = static_cast<int64_t>(cs) * p.keys_cap <= 8192 ? 1 : 0;
-  p.klist_cap = (mode & kModeAttend) ? (p.n_keys + cs - 1) / cs + 1 : 0;
-  if (ld.dtype == WF_BF16) {
-    const int mb = ld.n_gen <= 16 ? 1 : (ld.n_gen <= 32 ? 2 : 4);
-    p.tile_keys = 16 * (kWarps / mb);
-  } else {
-    p.tile_keys = 32;
-  }
-  // Token logits in shared memory when they fit, else in the workspace.
-  p.t_ws = nullptr;
-  size_t smem = smem_bytes(ld, p);
+  // Preferred cluster: one wave of clusters at one CTA per SM (the largest
+  // power of two with units * cs <= SMs), capped by the work each phase can
+  // split.  If that does not fit in shared memory, larger clusters (smaller
+  // per-CTA slices) are tried before giving up.
+  int cs0 = pow2_floor(std::max(1, static_cast<int>(std::min<int64_t>(kMaxCluster, sm_count / std::max<int64_t>(1, ld.units)))));
+  auto cluster_ok = [&](int c) {
+    if ((mode & kModeScore) && (p.P % c != 0 || p.P / c < 8)) return false;
+    if ((mode & kModeFilter) && k_l < c) return false;
+    if ((mode & kModeAttend) && p.n_keys < 16 * c) return false;
+    return true;
+  };
+  while (cs0 > 1 && !cluster_ok(cs0)) cs0 /= 2;
+  int cs = cs0;
+  size_t smem = 0;
   bool t_in_smem = true;
-  if ((mode & kModeFilter) && smem > kMaxSmem) {
-    p.t_ws = reinterpret_cast<float*>(16);  // placeholder: only its nullness matters here
+  for (;; cs *= 2) {
+    p.cs = cs;
+    p.per_cta_p = (mode & kModeScore) ? p.P / cs : 0;
+    const int spans_cap = (mode & kModeFilter) ? (k_l + cs - 1) / cs : 0;
+    p.rows_cap = spans_cap << ld.levels;
+    int sc = 1;
+    while (sc < std::max(k_l, 1)) sc <<= 1;
+    p.sorted_cap = (mode & kModeFilter) ? sc : 0;
+    p.keys_cap = std::max(p.per_cta_p, p.rows_cap);
+    p.gather_all = static_cast<int64_t>(cs) * p.keys_cap <= 8192 ? 1 : 0;
+    p.klist_cap = (mode & kModeAttend) ? (p.n_keys + cs - 1) / cs + 1 : 0;
+    if (ld.dtype == WF_BF16) {
+      const int mb = ld.n_gen <= 16 ? 1 : (ld.n_gen <= 32 ? 2 : 4);
+      p.tile_keys = 16 * (kWarps / mb);
+    } else {
+      p.tile_keys = 32;
+    }
+    // Token logits in shared memory when they fit, else in the workspace.
+    p.t_ws = nullptr;
     smem = smem_bytes(ld, p);
-    t_in_smem = false;
+    t_in_smem = true;
+    if ((mode & kModeFilter) && smem > kMaxSmem) {
+      p.t_ws = reinterpret_cast<float*>(16);  // placeholder: only its nullness matters here
+      smem = smem_bytes(ld, p);
+      t_in_smem = false;
+    }
+    if (smem <= kMaxSmem || cs * 2 > kMaxCluster || !cluster_ok(cs * 2)) break;
   }
   plan->cluster = cs;
   plan->smem_bytes = smem;
   plan->t_in_smem = t_in_smem;
   plan->t_bytes = t_in_smem ? 0
                             : sizeof(float) * static_cast<size_t>(ld.units) * cs * p.rows_cap *
-                                  ld.n_gen;
+                                  (ld.n_gen | 1);
   plan->per_cta_p = p.per_cta_p;
   plan->rows_cap = p.rows_cap;
   plan->sorted_cap = p.sorted_cap;
