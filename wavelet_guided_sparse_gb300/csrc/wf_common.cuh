@@ -182,6 +182,23 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// ------------------------------------------------------------------ cp.async row gathers
+// 16-byte asynchronous global -> shared copies (L2 only), grouped and waited
+// on with commit/wait groups.  Used for gathers of many small rows, where
+// one instruction per thread per 16 bytes keeps the copies in flight without
+// per-copy descriptor overhead.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ------------------------------------------------------------------ cluster exchanges
 //
 // Every exchange between the CTAs of a cluster is push-based: a CTA stores

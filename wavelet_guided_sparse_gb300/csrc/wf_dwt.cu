@@ -112,7 +112,9 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
 #pragma unroll
         for (int v = 0; v < V; ++v) acc[v] = 0.f;
         const unsigned char* p = buf + (sl << levels) * RB + c * 16;
-        for (int r = 0; r < span_rows; ++r) add_chunk<T>(p + r * RB, acc);
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+          if (r < span_rows) add_chunk<T>(p + r * RB, acc);
         float4* o = reinterpret_cast<float4*>(dst + (span0 + sl) * D + c * V);
 #pragma unroll
         for (int v = 0; v < V; v += 4)

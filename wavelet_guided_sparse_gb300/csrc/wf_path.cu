@@ -24,10 +24,11 @@
 //  filter — by linearity Q·A_j[c] = 2^(-j/2) Σ_{n∈span(c)} Q·Kp[n]: token
 //           logits t = Kp[rows]·Q^T are computed once (bf16 tensor cores,
 //           exact products, fp32 sums) for the rows under this CTA's coarse
-//           survivors, staged by TMA-engine bulk copies in a two-stage
-//           mbarrier pipeline; every level sums t over the candidates' leaves.
+//           survivors, staged into padded shared-memory rows by 16-byte
+//           cp.async copies in a two-stage pipeline; every level sums t over
+//           the candidates' leaves.
 //  attend — split-KV: each CTA gathers the K/V rows of its key slot range by
-//           bulk copies, runs Q·K^T and P·V on tensor cores with an online
+//           cp.async, runs Q·K^T and P·V on tensor cores with an online
 //           softmax, and the partial (max, sum, O) rows are pushed to the CTA
 //           that finalises those query rows.
 #include <algorithm>
@@ -77,9 +78,9 @@ template <typename T, int D>
 struct PathSmem {
   static constexpr int kRowBytes = D * static_cast<int>(sizeof(T)) + 16;  // padded row pitch
   static constexpr int kRowF = D + 4;                                      // fp32 row pitch
-  size_t bars, qs, stat_in, gm, loc, part, cnt_a, cnt_b, misc, sl_all, sp, sr, cp, cr, keys, take,
+  size_t qs, stat_in, gm, loc, part, cnt_a, cnt_b, misc, sl_all, sp, sr, cp, cr, keys, take,
       topk, keys_all, klist;
-  size_t s_qf, s_as, s_z;          // score phase
+  size_t s_stage, s_as, s_z;       // score phase
   size_t f_kst, f_t;               // filter phase
   size_t a_kst, a_vst, a_work, a_recv, a_rml;  // attend phase
   size_t total;
@@ -90,7 +91,6 @@ struct PathSmem {
       o = (o + bytes + 15) & ~size_t(15);
       return at;
     };
-    bars = take_bytes(2 * sizeof(uint64_t));
     qs = take_bytes(static_cast<size_t>(kMaxQ) * kRowBytes);
     stat_in = take_bytes(sizeof(float) * kMaxCluster * 2 * kMaxQ);
     gm = take_bytes(sizeof(float) * 2 * kMaxQ);
@@ -113,10 +113,17 @@ struct PathSmem {
     size_t end = u;
     if (p.mode & kModeScore) {
       o = u;
-      s_qf = 0;
-      // A_L chunk: three bf16 planes (bf16 inputs) or one fp32 tile, 64 rows.
-      s_as = take_bytes(static_cast<size_t>(sizeof(T) == 2 ? 3 : 1) * kScoreChunk * kRowBytes);
-      s_z = take_bytes(sizeof(float) * static_cast<size_t>(kScoreChunk) * (p.G | 1));
+      // A_L chunk: fp32 rows staged by cp.async, then (bf16 inputs) split into
+      // three bf16 planes; fp32 inputs use the staged rows directly.
+      // bf16: the logits overwrite the staged fp32 rows once the planes exist.
+      s_stage = take_bytes(sizeof(float) * kScoreChunk * kRowF);
+      if (sizeof(T) == 2) {
+        s_as = take_bytes(3 * kScoreChunk * kRowBytes);
+        s_z = s_stage;
+      } else {
+        s_as = s_stage;
+        s_z = take_bytes(sizeof(float) * static_cast<size_t>(kScoreChunk) * (p.G | 1));
+      }
       end = end > o ? end : o;
     }
     if (p.mode & kModeFilter) {
@@ -307,7 +314,6 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   const PathSmem<T, D> L(p);
   constexpr int RB = PathSmem<T, D>::kRowBytes;
   constexpr int RF = PathSmem<T, D>::kRowF;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   unsigned char* qs = smem + L.qs;
   float* stat_in = reinterpret_cast<float*>(smem + L.stat_in);
   float* gm = reinterpret_cast<float*>(smem + L.gm);
@@ -331,12 +337,6 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   uint32_t* keys_all = reinterpret_cast<uint32_t*>(smem + L.keys_all);
   int32_t* klist = reinterpret_cast<int32_t*>(smem + L.klist);
 
-  if (tid == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
-    fence_mbar_init();
-    misc[0] = 0;  // 1 once a bounded wait gave up
-  }
   // Queries (input dtype, padded rows; rows >= G are zero).
   {
     const T* qsrc = static_cast<const T*>(p.q) + unit * G * D;
@@ -349,7 +349,6 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     }
   }
   __syncthreads();
-  uint32_t bar_phase[2] = {0u, 0u};  // completed uses of each mbarrier
 
   // ================================================================ score
   if (p.mode & kModeScore) {
@@ -363,12 +362,20 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     if constexpr (sizeof(T) == 2) load_q_frags<D>(qs, G, bq);
     // z for chunk rows [c0, c0 + rows): stage A_L (bf16 inputs: exact
     // hi + mid + lo bf16 planes), then one tensor-core / FMA tile.
+    float* stage_f = reinterpret_cast<float*>(smem + L.s_stage);  // [64][D + 4] fp32
     auto chunk_logits = [&](int c0, int rows) {
       __syncthreads();
       for (int e = tid; e < rows * (D / 4); e += kThreads) {
         const int r = e / (D / 4), col = (e % (D / 4)) * 4;
-        const float4 a = __ldg(reinterpret_cast<const float4*>(asrc + static_cast<int64_t>(c0 + r) * D + col));
-        if constexpr (sizeof(T) == 2) {
+        cp_async16(stage_f + r * RF + col, asrc + static_cast<int64_t>(c0 + r) * D + col);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      __syncthreads();
+      if constexpr (sizeof(T) == 2) {
+        for (int e = tid; e < rows * (D / 4); e += kThreads) {
+          const int r = e / (D / 4), col = (e % (D / 4)) * 4;
+          const float4 a = *reinterpret_cast<const float4*>(stage_f + r * RF + col);
           const float av[4] = {a.x, a.y, a.z, a.w};
           float pv[3][4];
 #pragma unroll
@@ -384,12 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           for (int pl = 0; pl < 3; ++pl)
             *reinterpret_cast<uint2*>(as + pl * kScoreChunk * RB + r * RB + col * 2) =
                 make_uint2(pack_bf16(pv[pl][0], pv[pl][1]), pack_bf16(pv[pl][2], pv[pl][3]));
-        } else {
-          *reinterpret_cast<float4*>(as + r * RB + col * 4) = a;
         }
-      }
-      __syncthreads();
-      if constexpr (sizeof(T) == 2) {
+        __syncthreads();
         logits_tile_bf16<D>(as, 3, kScoreChunk * RB, bq, zc, 0, rows, G, TS, zscale);
       } else {
         logits_tile_f32<D>(as, reinterpret_cast<const float*>(qs), zc, 0, rows, G, TS, zscale);
@@ -506,31 +509,29 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
                    : p.t_ws + (static_cast<int64_t>(unit) * cs + rank) * p.rows_cap * TS;
     const T* kp = static_cast<const T*>(p.kp);
     const int ntiles = (R + kTileRows - 1) / kTileRows;
-    auto issue = [&](int tile, int stage) {  // warp 0 only
+    constexpr int C16 = D * static_cast<int>(sizeof(T)) / 16;  // 16-byte chunks per row
+    auto issue = [&](int tile, int stage) {  // all threads; one cp.async group
       const int r0 = tile * kTileRows;
       const int nr = min(kTileRows, R - r0);
-      if (lane == 0) mbar_arrive_expect_tx(&bars[stage], nr * D * static_cast<int>(sizeof(T)));
-      __syncwarp();
-      for (int i = lane; i < nr; i += 32) {
+      for (int e = tid; e < nr * C16; e += kThreads) {
+        const int i = e / C16, ch = e % C16;
         const int lr = r0 + i;
         const int64_t grow = unit * p.n_prompt +
                              (static_cast<int64_t>(sl_all[s0 + (lr >> levels)]) << levels) +
                              (lr & ((1 << levels) - 1));
-        bulk_g2s(kst + (stage * kTileRows + i) * RB, kp + grow * D, D * sizeof(T), &bars[stage]);
+        cp_async16(kst + (stage * kTileRows + i) * RB + ch * 16,
+                   reinterpret_cast<const unsigned char*>(kp + grow * D) + ch * 16);
       }
+      cp_async_commit();
     };
-    if (warp == 0) {
-      if (ntiles > 0) issue(0, 0);
-      if (ntiles > 1) issue(1, 1);
-    }
+    if (ntiles > 0) issue(0, 0);
+    if (ntiles > 1) issue(1, 1);
     uint32_t bq[4][D / 16][2];
     if constexpr (sizeof(T) == 2) load_q_frags<D>(qs, G, bq);
     for (int tile = 0; tile < ntiles; ++tile) {
       const int stage = tile & 1;
-      int ok = 1;
-      if (misc[0] == 0) ok = mbar_wait_bounded(&bars[stage], bar_phase[stage] & 1, p.status) ? 1 : 0;
-      ++bar_phase[stage];
-      if (__syncthreads_or(!ok) && tid == 0) misc[0] = 1;
+      if (tile + 1 < ntiles) cp_async_wait<1>(); else cp_async_wait<0>();
+      __syncthreads();
       const unsigned char* buf = kst + stage * kTileRows * RB;
       const int rows_valid = min(kTileRows, R - tile * kTileRows);
       if constexpr (sizeof(T) == 2) {
@@ -540,10 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
                            rows_valid, G, TS, 1.f);
       }
       __syncthreads();
-      if (warp == 0 && tile + 2 < ntiles && misc[0] == 0) {
-        fence_proxy_async();
-        issue(tile + 2, stage);
-      }
+      if (tile + 2 < ntiles) issue(tile + 2, stage);
     }
     __syncthreads();
 
@@ -676,11 +674,11 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     }
     // Every slot of a tile is filled (invalid slots with a finite dummy row),
     // so masked probabilities multiply finite values.
-    auto issue = [&](int tile, int stage) {  // warp 0 only
+    constexpr int C16 = D * static_cast<int>(sizeof(T)) / 16;
+    auto issue = [&](int tile, int stage) {  // all threads; one cp.async group
       const int base = k0 + tile * TK;
-      if (lane == 0) mbar_arrive_expect_tx(&bars[stage], 2u * TK * D * sizeof(T));
-      __syncwarp();
-      for (int i = lane; i < TK; i += 32) {
+      for (int e = tid; e < TK * C16; e += kThreads) {
+        const int i = e / C16, ch = e % C16;
         const int g = base + i;
         const T* ks = kgp;
         const T* vs = vgp;
@@ -696,16 +694,16 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
             }
           }
         }
-        bulk_g2s(kst + (stage * TK + i) * RB, ks, D * sizeof(T), &bars[stage]);
-        bulk_g2s(vst + (stage * TK + i) * RB, vs, D * sizeof(T), &bars[stage]);
+        cp_async16(kst + (stage * TK + i) * RB + ch * 16,
+                   reinterpret_cast<const unsigned char*>(ks) + ch * 16);
+        cp_async16(vst + (stage * TK + i) * RB + ch * 16,
+                   reinterpret_cast<const unsigned char*>(vs) + ch * 16);
       }
+      cp_async_commit();
     };
     __syncthreads();  // filter-phase readers of the union are done
-    if (warp == 0 && misc[0] == 0) {
-      fence_proxy_async();
-      if (ntiles > 0) issue(0, 0);
-      if (ntiles > 1) issue(1, 1);
-    }
+    if (ntiles > 0) issue(0, 0);
+    if (ntiles > 1) issue(1, 1);
     auto valid = [&](int g) -> bool {
       if (g >= k1) return false;
       if (g >= B) return true;
@@ -729,10 +727,8 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
       for (int tile = 0; tile < ntiles; ++tile) {
         const int stage = tile & 1;
-        int ok = 1;
-        if (misc[0] == 0) ok = mbar_wait_bounded(&bars[stage], bar_phase[stage] & 1, p.status) ? 1 : 0;
-        ++bar_phase[stage];
-        if (__syncthreads_or(!ok) && tid == 0) misc[0] = 1;
+        if (tile + 1 < ntiles) cp_async_wait<1>(); else cp_async_wait<0>();
+        __syncthreads();
         const uint32_t kb = smem_u32(kst + (stage * TK + kgrp * 16) * RB);
         const uint32_t vb = smem_u32(vst + (stage * TK + kgrp * 16) * RB);
         float s[2][4];
@@ -804,10 +800,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           mma_bf16(oacc[dn + 1], pa, b + 2);
         }
         __syncthreads();
-        if (warp == 0 && tile + 2 < ntiles && misc[0] == 0) {
-          fence_proxy_async();
-          issue(tile + 2, stage);
-        }
+        if (tile + 2 < ntiles) issue(tile + 2, stage);
       }
       // Warp partials -> shared memory (overwrites the stages).
       float* opart = work;                    // [kWarps][16][D]
@@ -876,10 +869,8 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       __syncthreads();
       for (int tile = 0; tile < ntiles; ++tile) {
         const int stage = tile & 1;
-        int ok = 1;
-        if (misc[0] == 0) ok = mbar_wait_bounded(&bars[stage], bar_phase[stage] & 1, p.status) ? 1 : 0;
-        ++bar_phase[stage];
-        if (__syncthreads_or(!ok) && tid == 0) misc[0] = 1;
+        if (tile + 1 < ntiles) cp_async_wait<1>(); else cp_async_wait<0>();
+        __syncthreads();
         const float* kb = reinterpret_cast<const float*>(kst + stage * TK * RB);
         const float* vb = reinterpret_cast<const float*>(vst + stage * TK * RB);
         {
@@ -936,10 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           }
         }
         __syncthreads();
-        if (warp == 0 && tile + 2 < ntiles && misc[0] == 0) {
-          fence_proxy_async();
-          issue(tile + 2, stage);
-        }
+        if (tile + 2 < ntiles) issue(tile + 2, stage);
       }
       const int c4 = tid % C4, qg = tid / C4;
 #pragma unroll
