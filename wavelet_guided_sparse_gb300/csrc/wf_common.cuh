@@ -465,6 +465,95 @@ __device__ inline TopkResult topk_distributed(const uint32_t* keys, int n, int k
   return TopkResult{tot_gt + quota_me, offset};
 }
 
+// ------------------------------------------------------------------ block Top-K
+//
+// Block-wide exact selection over keys held in this CTA's shared memory.
+// `key(i)` returns the i-th key of a virtual array of n keys (the order is
+// the tie order: lower i wins).  Three radix rounds of 11/11/10 bits, two
+// __syncthreads each: all warps build the histogram (and clear the other
+// buffer for the next round), warp 0 finds the digit.  Returns the k-th
+// largest key T; `*need` gets the number of keys equal to T to take.
+template <typename KeyAt>
+__device__ inline uint32_t block_radix_select(KeyAt key, int n, int k, TopkSmem& sm, int* need_out) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t* buf[2] = {sm.hist, sm.total};
+  for (int b = tid; b < 2048; b += kThreads) buf[0][b] = 0;
+  __syncthreads();
+  uint32_t prefix = 0, pmask = 0;
+  int need = k;
+#pragma unroll 1
+  for (int round = 0; round < 3; ++round) {
+    const int shift = round_shift(round), nb = round_bins(round);
+    uint32_t* h = buf[round & 1];
+    for (int i = tid; i < n; i += kThreads) {
+      const uint32_t kv = key(i);
+      if ((kv & pmask) == prefix) atomicAdd(&h[(kv >> shift) & (nb - 1)], 1u);
+    }
+    if (round < 2)
+      for (int b = tid; b < 2048; b += kThreads) buf[(round + 1) & 1][b] = 0;
+    __syncthreads();
+    if (tid < 32) {
+      // Lane l owns bins [(31 - l) * per, (32 - l) * per): lane 0 the highest.
+      const int per = nb / 32;
+      const int b0 = (31 - lane) * per;
+      int mine = 0;
+      for (int b = 0; b < per; ++b) mine += static_cast<int>(h[b0 + b]);
+      const int incl = warp_incl_scan(mine);
+      const int above = incl - mine;
+      if (above < need && incl >= need) {
+        int acc = above;
+        for (int b = per - 1; b >= 0; --b) {
+          const int cnt = static_cast<int>(h[b0 + b]);
+          if (acc + cnt >= need) {
+            sm.bcast[0] = b0 + b;
+            sm.bcast[1] = acc;
+            break;
+          }
+          acc += cnt;
+        }
+      }
+    }
+    __syncthreads();
+    need -= sm.bcast[1];
+    prefix |= static_cast<uint32_t>(sm.bcast[0]) << shift;
+    pmask |= static_cast<uint32_t>(nb - 1) << shift;
+  }
+  *need_out = need;
+  return prefix;
+}
+
+// Stable compaction of the selected entries of a virtual array of n
+// candidates: sel(i) says whether candidate i is taken, emit(i, slot) receives
+// each taken candidate with its rank among the taken ones.  Each warp owns a
+// contiguous chunk; warp totals are scanned once.  Two __syncthreads.
+template <typename Sel, typename Emit>
+__device__ inline int block_compact(int n, Sel sel, Emit emit, int32_t* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int chunk = (n + kWarps - 1) / kWarps;
+  const int lo = min(n, warp * chunk), hi = min(n, lo + chunk);
+  int cnt = 0;
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    cnt += __popc(__ballot_sync(0xffffffffu, i < hi && sel(i)));
+  }
+  if (lane == 0) scratch[warp] = cnt;
+  __syncthreads();
+  int before = 0, total = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < warp) before += scratch[w];
+    total += scratch[w];
+  }
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    const bool t = i < hi && sel(i);
+    const unsigned m = __ballot_sync(0xffffffffu, t);
+    if (t) emit(i, before + __popc(m & ((1u << lane) - 1u)));
+    before += __popc(m);
+  }
+  __syncthreads();
+  return total;
+}
+
 // Exclusive prefix over the cluster of one int per CTA (pushed to every
 // peer).  Returns the sum over lower ranks; *total gets the cluster sum.
 // cnt_in: [kMaxCluster] ints.  Contains one cluster barrier.

@@ -79,7 +79,7 @@ struct PathSmem {
   static constexpr int kRowBytes = D * static_cast<int>(sizeof(T)) + 16;  // padded row pitch
   static constexpr int kRowF = D + 4;                                      // fp32 row pitch
   size_t qs, stat_in, gm, loc, part, cnt_a, cnt_b, misc, sl_all, sp, sr, cp, cr, keys, take,
-      topk, keys_all, klist;
+      topk, keys_all, pos_all, take_all, klist;
   size_t s_stage, s_as, s_z;       // score phase
   size_t f_kst, f_t;               // filter phase
   size_t a_kst, a_vst, a_work, a_recv, a_rml;  // attend phase
@@ -108,6 +108,8 @@ struct PathSmem {
     take = take_bytes(p.keys_cap);
     topk = take_bytes(sizeof(TopkSmem));
     keys_all = take_bytes(p.gather_all ? sizeof(uint32_t) * p.cs * p.keys_cap : 0);
+    pos_all = take_bytes(p.gather_all ? sizeof(int32_t) * p.cs * p.keys_cap : 0);
+    take_all = take_bytes(p.gather_all ? static_cast<size_t>(p.cs) * p.keys_cap : 0);
     klist = take_bytes(sizeof(int32_t) * p.klist_cap);
     const size_t u = o;
     size_t end = u;
@@ -335,6 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   uint8_t* take = smem + L.take;
   TopkSmem& tk = *reinterpret_cast<TopkSmem*>(smem + L.topk);
   uint32_t* keys_all = reinterpret_cast<uint32_t*>(smem + L.keys_all);
+  int32_t* pos_all = reinterpret_cast<int32_t*>(smem + L.pos_all);
+  uint8_t* take_all = smem + L.take_all;
   int32_t* klist = reinterpret_cast<int32_t*>(smem + L.klist);
 
   // Queries (input dtype, padded rows; rows >= G are zero).
@@ -352,11 +356,13 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
 
   // ================================================================ score
   if (p.mode & kModeScore) {
-    const int Pc = p.per_cta_p;
+    // Every CTA of the cluster scores all P coarse positions (redundant work
+    // that saves every cluster exchange of this phase) and selects locally.
+    const int Pc = p.P;
     unsigned char* as = smem + L.s_as;
     float* zc = reinterpret_cast<float*>(smem + L.s_z);  // [chunk row][query], log2 domain
     const float zscale = p.inv_sqrt_d * kLog2e;
-    const float* asrc = p.al + (unit * p.P + static_cast<int64_t>(rank) * Pc) * D;
+    const float* asrc = p.al + unit * p.P * D;
     const int nchunks = (Pc + kScoreChunk - 1) / kScoreChunk;
     uint32_t bq[4][D / 16][2];
     if constexpr (sizeof(T) == 2) load_q_frags<D>(qs, G, bq);
@@ -415,18 +421,13 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     part_m[warp * kMaxQ + lane + 32] = m1;
     part_l[warp * kMaxQ + lane + 32] = l1;
     __syncthreads();
-    {
+    if (tid < G) {
       float cm = -INFINITY, cl = 0.f;
-      if (tid < G)
-        for (int w = 0; w < kWarps; ++w) merge_ml(cm, cl, part_m[w * kMaxQ + tid], part_l[w * kMaxQ + tid]);
-      __syncthreads();
-      if (tid < G) {
-        part_m[tid] = cm;
-        part_l[tid] = cl;
-      }
-      __syncthreads();
+      for (int w = 0; w < kWarps; ++w) merge_ml(cm, cl, part_m[w * kMaxQ + tid], part_l[w * kMaxQ + tid]);
+      gm[tid] = cm;
+      ginv[tid] = 1.f / cl;
     }
-    cluster_merge_stats(part_m, part_l, G, stat_in, gm, ginv);
+    __syncthreads();
     // Pass 2: attention mass of every position (4 threads per position).
     for (int ch = 0; ch < nchunks; ++ch) {
       const int c0 = ch * kScoreChunk, rows = min(kScoreChunk, Pc - c0);
@@ -439,30 +440,25 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       sacc += __shfl_xor_sync(0xffffffffu, sacc, 2);
       if (r < rows && sub == 0) {
         keys[c0 + r] = __float_as_uint(sacc);
-        if (p.scores_out != nullptr) p.scores_out[unit * p.P + rank * Pc + c0 + r] = sacc;
+        if (p.scores_out != nullptr && rank == 0) p.scores_out[unit * p.P + c0 + r] = sacc;
       }
     }
     __syncthreads();
-    const TopkResult res = cluster_select(p, keys, Pc, p.kL, take, tk, keys_all);
-    const bool to_peers = (p.mode & kModeFilter) != 0;
-    int carry = 0;
-    for (int base = 0; base < Pc; base += kThreads) {
-      const int j = base + tid;
-      const int tkn = j < Pc ? take[j] : 0;
-      int tot;
-      const int pos = block_excl_scan(tkn, tk.scan, &tot);
-      const int slot = res.offset + carry + pos;
-      if (tkn && slot < p.kL) {
-        const int coarse = rank * Pc + j;
-        if (to_peers) {
-          for (int r = 0; r < cs; ++r) peer(sl_all, r)[slot] = coarse;
-        } else {
-          p.idx_l_out[unit * p.kL + slot] = coarse;
-        }
-      }
-      carry += tot;
-    }
-    if (to_peers) cluster.sync();  // every CTA now holds the sorted coarse survivors
+    // Local exact Top-k_L: threshold, ties in position order, compaction.
+    int need;
+    const uint32_t thr = block_radix_select([&](int i) { return keys[i]; }, Pc, p.kL, tk, &need);
+    for (int i = tid; i < Pc; i += kThreads) take[i] = keys[i] > thr;
+    __syncthreads();
+    block_compact(Pc, [&](int i) { return keys[i] == thr; },
+                  [&](int i, int slot) { take[i] = slot < need; }, tk.scan);
+    const bool to_filter = (p.mode & kModeFilter) != 0;
+    block_compact(Pc, [&](int i) { return take[i] != 0; },
+                  [&](int i, int slot) {
+                    if (slot >= p.kL) return;
+                    if (to_filter) sl_all[slot] = i;
+                    else if (rank == 0) p.idx_l_out[unit * p.kL + slot] = i;
+                  },
+                  tk.scan);
   } else if (p.mode & kModeFilter) {
     // Coarse survivors from the caller: load, sort ascending, validate.
     const int kL = p.kL, P = p.P;
@@ -546,6 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     __syncthreads();
 
     int n_surv = ns;
+    bool global_done = false;  // final token list already distributed
     for (int i = tid; i < ns; i += kThreads) {
       sp[i] = sl_all[s0 + i];
       sr[i] = i << levels;
@@ -630,10 +627,60 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         keys[ci] = __float_as_uint(s);
       }
       __syncthreads();
+      if (j == 0 && p.gather_all) {
+        // Final level: every CTA receives every candidate (score, position),
+        // selects the budget locally and keeps the token list it needs: its
+        // slot range of the key list (attend) and of the output (idx).
+        const int cap = p.keys_cap;
+        for (int e = tid; e < n_cand * cs; e += kThreads) {
+          const int i = e % n_cand, r = e / n_cand;
+          peer(keys_all, r)[rank * cap + i] = keys[i];
+          peer(pos_all, r)[rank * cap + i] = cp[i];
+        }
+        if (tid < cs) peer(tk.nloc_in, tid)[rank] = n_cand;
+        cluster.sync();
+        if (tid == 0) {
+          int o = 0;
+          for (int r = 0; r < cs; ++r) {
+            tk.red[r] = o;
+            o += tk.nloc_in[r];
+          }
+          tk.red[cs] = o;
+        }
+        __syncthreads();
+        const int n_all = tk.red[cs];
+        auto vslot = [&](int v) {  // dense candidate v -> (rank, local index) storage slot
+          int r = 0;
+          while (r + 1 < cs && tk.red[r + 1] <= v) ++r;
+          return r * cap + (v - tk.red[r]);
+        };
+        int need;
+        const uint32_t thr = block_radix_select([&](int v) { return keys_all[vslot(v)]; }, n_all,
+                                                p.k[0], tk, &need);
+        for (int v = tid; v < n_all; v += kThreads) take_all[v] = keys_all[vslot(v)] > thr;
+        __syncthreads();
+        block_compact(n_all, [&](int v) { return keys_all[vslot(v)] == thr; },
+                      [&](int v, int slot) { take_all[v] = slot < need; }, tk.scan);
+        const int B = p.budget;
+        const int a0 = key_slot_start(rank, cs, p.n_keys), a1 = key_slot_start(rank + 1, cs, p.n_keys);
+        const int w0 = key_slot_start(rank, cs, B), w1 = key_slot_start(rank + 1, cs, B);
+        const bool attend = (p.mode & kModeAttend) != 0;
+        block_compact(n_all, [&](int v) { return take_all[v] != 0; },
+                      [&](int v, int slot) {
+                        if (slot >= B) return;
+                        const int pos = pos_all[vslot(v)];
+                        if (attend && slot >= a0 && slot < a1) klist[slot - a0] = pos;
+                        if (p.idx_out != nullptr && slot >= w0 && slot < w1) p.idx_out[unit * B + slot] = pos;
+                      },
+                      tk.scan);
+        global_done = true;
+        break;
+      }
       (void)cluster_select(p, keys, n_cand, p.k[j], take, tk, keys_all);
       n_surv = compact2(cp, cr, take, n_cand, sp, sr, tk.scan);
     }
     // Tokens of this CTA: sp[0, n_surv), ascending.
+    if (!global_done) {
     int all;
     const int offset = cluster_excl_count(n_surv, cnt_a, &all);
     const int B = p.budget;
@@ -649,6 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     } else {
       for (int i = tid; i < n_surv; i += kThreads)
         if (offset + i < B) p.idx_out[unit * B + offset + i] = sp[i];
+    }
     }
   }
 
@@ -822,7 +870,9 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         mpart[warp * 16 + r_lo + 8] = m_hi;
         lpart[warp * 16 + r_lo + 8] = l_hi;
       }
-      __syncthreads();
+      // Every CTA must be past its filter phase (whose buffers share bytes
+      // with the receive area) before partials are pushed.
+      cluster.sync();
       // CTA partial of row qi, pushed straight to the CTA that finalises it.
       const int KGW = kWarps / MB;
       for (int e = tid; e < G * (D / 4); e += kThreads) {
@@ -929,6 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         __syncthreads();
         if (tile + 2 < ntiles) issue(tile + 2, stage);
       }
+      cluster.sync();  // peers are past their filter phase (shared receive area)
       const int c4 = tid % C4, qg = tid / C4;
 #pragma unroll
       for (int i = 0; i < QPT; ++i) {
@@ -1035,7 +1086,7 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
   // per-CTA slices) are tried before giving up.
   int cs0 = pow2_floor(std::max(1, static_cast<int>(std::min<int64_t>(kMaxCluster, sm_count / std::max<int64_t>(1, ld.units)))));
   auto cluster_ok = [&](int c) {
-    if ((mode & kModeScore) && (p.P % c != 0 || p.P / c < 8)) return false;
+    if (mode == kModeScore && c > 1) return false;  // scoring alone needs no cluster
     if ((mode & kModeFilter) && k_l < c) return false;
     if ((mode & kModeAttend) && p.n_keys < 16 * c) return false;
     return true;
@@ -1044,16 +1095,16 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
   int cs = cs0;
   size_t smem = 0;
   bool t_in_smem = true;
+  bool found = false;
   for (;; cs *= 2) {
     p.cs = cs;
-    p.per_cta_p = (mode & kModeScore) ? p.P / cs : 0;
+    p.per_cta_p = (mode & kModeScore) ? p.P : 0;  // every CTA scores all positions
     const int spans_cap = (mode & kModeFilter) ? (k_l + cs - 1) / cs : 0;
     p.rows_cap = spans_cap << ld.levels;
     int sc = 1;
     while (sc < std::max(k_l, 1)) sc <<= 1;
     p.sorted_cap = (mode & kModeFilter) ? sc : 0;
     p.keys_cap = std::max(p.per_cta_p, p.rows_cap);
-    p.gather_all = static_cast<int64_t>(cs) * p.keys_cap <= 8192 ? 1 : 0;
     p.klist_cap = (mode & kModeAttend) ? (p.n_keys + cs - 1) / cs + 1 : 0;
     if (ld.dtype == WF_BF16) {
       const int mb = ld.n_gen <= 16 ? 1 : (ld.n_gen <= 32 ? 2 : 4);
@@ -1061,16 +1112,21 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
     } else {
       p.tile_keys = 32;
     }
-    // Token logits in shared memory when they fit, else in the workspace.
-    p.t_ws = nullptr;
-    smem = smem_bytes(ld, p);
-    t_in_smem = true;
-    if ((mode & kModeFilter) && smem > kMaxSmem) {
-      p.t_ws = reinterpret_cast<float*>(16);  // placeholder: only its nullness matters here
+    // Prefer the gather-all selection and token logits in shared memory.
+    for (int ga = 1; ga >= 0 && !found; --ga) {
+      if (ga && static_cast<int64_t>(cs) * p.keys_cap > 8192) continue;
+      p.gather_all = ga;
+      p.t_ws = nullptr;
       smem = smem_bytes(ld, p);
-      t_in_smem = false;
+      t_in_smem = true;
+      if ((mode & kModeFilter) && smem > kMaxSmem) {
+        p.t_ws = reinterpret_cast<float*>(16);  // placeholder: only its nullness matters here
+        smem = smem_bytes(ld, p);
+        t_in_smem = false;
+      }
+      found = smem <= kMaxSmem;
     }
-    if (smem <= kMaxSmem || cs * 2 > kMaxCluster || !cluster_ok(cs * 2)) break;
+    if (found || cs * 2 > kMaxCluster || !cluster_ok(cs * 2)) break;
   }
   plan->cluster = cs;
   plan->smem_bytes = smem;
