@@ -231,9 +231,12 @@ constexpr int kMaxQ = 64;  // maximum queries per unit
 
 // All-reduce of per-query softmax statistics (log2 domain) over the cluster.
 // loc_m/loc_l hold this CTA's (max, Σ 2^(z - max)) per query; on return
-// gm/ginv hold the cluster-wide max and 1 / sum.  stat_in: [kMaxCluster][2][kMaxQ] floats.
+// gm/ginv hold the cluster-wide max and 1 / sum.  stat_in: [kMaxCluster][2]
+// [kMaxQ] floats.  If counts_in is not null, `my_count` is all-gathered into
+// counts_in[rank] in the same exchange.  One cluster barrier.
 __device__ inline void cluster_merge_stats(const float* loc_m, const float* loc_l, int G,
-                                           float* stat_in, float* gm, float* ginv) {
+                                           float* stat_in, float* gm, float* ginv,
+                                           int my_count = 0, int32_t* counts_in = nullptr) {
   cg::cluster_group cluster = cg::this_cluster();
   const int cs = static_cast<int>(cluster.num_blocks());
   const int me = static_cast<int>(cluster.block_rank());
@@ -243,6 +246,7 @@ __device__ inline void cluster_merge_stats(const float* loc_m, const float* loc_
     dst[q] = loc_m[q];
     dst[kMaxQ + q] = loc_l[q];
   }
+  if (counts_in != nullptr && threadIdx.x < cs) peer(counts_in, threadIdx.x)[me] = my_count;
   cluster.sync();
   for (int q = threadIdx.x; q < G; q += kThreads) {
     float m = -INFINITY, l = 0.f;
@@ -269,12 +273,9 @@ __device__ inline void cluster_merge_stats(const float* loc_m, const float* loc_
 // candidate sets, and distributed (histograms reduce-scattered and
 // all-gathered through DSMEM; two barriers per round) for large ones.
 struct TopkSmem {
-  uint32_t hist[2048];     // local digit histogram
-  uint32_t total[2048];    // cluster-wide histogram of the current round
-  uint32_t part_in[2048];  // distributed: histogram slices pushed by the peers
+  uint32_t hist[3][2048];          // digit histograms (one per radix round)
   int32_t cnt_in[kMaxCluster][2];  // distributed: (#> T, #== T) pushed by each rank
-  int32_t nloc_in[kMaxCluster];    // gather-all: candidate count of each rank
-  int32_t red[2 * kMaxCluster];    // gather-all: per-rank (#> T, #== T)
+  int32_t wcnt[2][kWarps];         // block select: per-warp (#> T, #== T)
   int32_t scan[kWarps + 1];
   int32_t bcast[4];
 };
@@ -334,74 +335,6 @@ __device__ inline void mark_taken(const uint32_t* keys, int n, uint32_t thr, int
   __syncthreads();
 }
 
-// Gather-all variant.  keys_all: [cs][cap] u32 in every CTA; n <= cap.
-__device__ inline TopkResult topk_gather_all(const uint32_t* keys, int n, int k, uint8_t* take,
-                                             TopkSmem& sm, uint32_t* keys_all, int cap) {
-  cg::cluster_group cluster = cg::this_cluster();
-  const int cs = static_cast<int>(cluster.num_blocks());
-  const int me = static_cast<int>(cluster.block_rank());
-  const int tid = threadIdx.x;
-  for (int e = tid; e < n * cs; e += kThreads) {
-    const int i = e % n, r = e / n;
-    peer(keys_all, r)[me * cap + i] = keys[i];
-  }
-  if (tid < cs) peer(sm.nloc_in, tid)[me] = n;
-  cluster.sync();
-  uint32_t prefix = 0, pmask = 0;
-  int need = k;
-#pragma unroll 1
-  for (int round = 0; round < 3; ++round) {
-    const int shift = round_shift(round), nb = round_bins(round);
-    for (int b = tid; b < nb; b += kThreads) sm.hist[b] = 0;
-    __syncthreads();
-    for (int r = 0; r < cs; ++r) {
-      const int nr = sm.nloc_in[r];
-      const uint32_t* kr = keys_all + r * cap;
-      for (int i = tid; i < nr; i += kThreads) {
-        const uint32_t key = kr[i];
-        if ((key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & (nb - 1)], 1u);
-      }
-    }
-    __syncthreads();
-    int above;
-    const uint32_t digit = find_digit(sm.hist, nb, need, sm, &above);
-    need -= above;
-    prefix |= digit << shift;
-    pmask |= static_cast<uint32_t>(nb - 1) << shift;
-  }
-  const uint32_t thr = prefix;
-  if (tid < 2 * kMaxCluster) sm.red[tid] = 0;
-  __syncthreads();
-  for (int r = 0; r < cs; ++r) {
-    const int nr = sm.nloc_in[r];
-    const uint32_t* kr = keys_all + r * cap;
-    int gt = 0, eq = 0;
-    for (int i = tid; i < nr; i += kThreads) {
-      gt += kr[i] > thr;
-      eq += kr[i] == thr;
-    }
-    gt = __reduce_add_sync(0xffffffffu, gt);
-    eq = __reduce_add_sync(0xffffffffu, eq);
-    if ((tid & 31) == 0) {
-      atomicAdd(&sm.red[2 * r], gt);
-      atomicAdd(&sm.red[2 * r + 1], eq);
-    }
-  }
-  __syncthreads();
-  int quota_me = 0, offset = 0, ties_before = 0;
-  for (int r = 0; r < cs; ++r) {
-    const int g = sm.red[2 * r], e = sm.red[2 * r + 1];
-    int q = need - ties_before;
-    q = q < 0 ? 0 : (q > e ? e : q);
-    if (r < me) offset += g + q;
-    if (r == me) quota_me = q;
-    ties_before += e;
-  }
-  const int gt_me = sm.red[2 * me];
-  mark_taken(keys, n, thr, quota_me, take, sm);
-  return TopkResult{gt_me + quota_me, offset};
-}
-
 // Distributed variant (any candidate count).
 __device__ inline TopkResult topk_distributed(const uint32_t* keys, int n, int k, uint8_t* take,
                                               TopkSmem& sm) {
@@ -409,30 +342,33 @@ __device__ inline TopkResult topk_distributed(const uint32_t* keys, int n, int k
   const int cs = static_cast<int>(cluster.num_blocks());
   const int me = static_cast<int>(cluster.block_rank());
   const int tid = threadIdx.x;
+  uint32_t* hist = sm.hist[0];     // local histogram
+  uint32_t* total = sm.hist[1];    // cluster-wide histogram
+  uint32_t* part_in = sm.hist[2];  // slices pushed by the peers
   uint32_t prefix = 0, pmask = 0;
   int need = k;
 #pragma unroll 1
   for (int round = 0; round < 3; ++round) {
     const int shift = round_shift(round), nb = round_bins(round);
     const int sl = nb / cs;  // bins owned by each rank
-    for (int b = tid; b < nb; b += kThreads) sm.hist[b] = 0;
+    for (int b = tid; b < nb; b += kThreads) hist[b] = 0;
     __syncthreads();
     for (int i = tid; i < n; i += kThreads) {
       const uint32_t key = keys[i];
-      if ((key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & (nb - 1)], 1u);
+      if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
     }
     __syncthreads();
-    for (int b = tid; b < nb; b += kThreads) peer(sm.part_in, b / sl)[me * sl + (b % sl)] = sm.hist[b];
+    for (int b = tid; b < nb; b += kThreads) peer(part_in, b / sl)[me * sl + (b % sl)] = hist[b];
     cluster.sync();
     for (int e = tid; e < sl * cs; e += kThreads) {
       const int bl = e % sl, r = e / sl;
       uint32_t t = 0;
-      for (int src = 0; src < cs; ++src) t += sm.part_in[src * sl + bl];
-      peer(sm.total, r)[me * sl + bl] = t;
+      for (int src = 0; src < cs; ++src) t += part_in[src * sl + bl];
+      peer(total, r)[me * sl + bl] = t;
     }
     cluster.sync();
     int above;
-    const uint32_t digit = find_digit(sm.total, nb, need, sm, &above);
+    const uint32_t digit = find_digit(total, nb, need, sm, &above);
     need -= above;
     prefix |= digit << shift;
     pmask |= static_cast<uint32_t>(nb - 1) << shift;
@@ -467,91 +403,113 @@ __device__ inline TopkResult topk_distributed(const uint32_t* keys, int n, int k
 
 // ------------------------------------------------------------------ block Top-K
 //
-// Block-wide exact selection over keys held in this CTA's shared memory.
-// `key(i)` returns the i-th key of a virtual array of n keys (the order is
-// the tie order: lower i wins).  Three radix rounds of 11/11/10 bits, two
-// __syncthreads each: all warps build the histogram (and clear the other
-// buffer for the next round), warp 0 finds the digit.  Returns the k-th
-// largest key T; `*need` gets the number of keys equal to T to take.
-template <typename KeyAt>
-__device__ inline uint32_t block_radix_select(KeyAt key, int n, int k, TopkSmem& sm, int* need_out) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  uint32_t* buf[2] = {sm.hist, sm.total};
-  for (int b = tid; b < 2048; b += kThreads) buf[0][b] = 0;
+// Block-wide exact Top-k over keys[0, n) in this CTA's shared memory (index
+// order is the tie order: lower index wins).  Radix rounds of 11/11/10 bits,
+// each histogram in its own pre-zeroed buffer, so a round costs one barrier:
+// every warp then finds the round's digit redundantly (vectorised bin sums,
+// a warp scan over lanes and a second warp scan inside the boundary lane's
+// bins).  A fused pass counts, per warp chunk, the keys above the threshold
+// and the ties, and emit(i, slot) receives every selected key with its rank
+// among the selected (ascending index).  Six __syncthreads in total.
+__device__ __forceinline__ void warp_find_digit(const uint32_t* h, int nb, int need,
+                                                uint32_t* digit, int* above) {
+  const int lane = threadIdx.x & 31;
+  const int per = nb / 32;             // 64 or 32 bins per lane
+  const int b0 = (31 - lane) * per;    // lane 0 owns the highest bins
+  int sum = 0;
+  for (int v = 0; v < per; v += 4) {
+    const uint4 q = *reinterpret_cast<const uint4*>(h + b0 + v);
+    sum += static_cast<int>(q.x + q.y + q.z + q.w);
+  }
+  const int incl = warp_incl_scan(sum);
+  const int before = incl - sum;
+  const unsigned owner_mask = __ballot_sync(0xffffffffu, before < need && incl >= need);
+  const int owner = __ffs(owner_mask) - 1;
+  const int base = __shfl_sync(0xffffffffu, before, owner);
+  const int ob0 = (31 - owner) * per;
+  // Inside the owner's bins, descending: lane l takes per/32 consecutive bins.
+  const int w = per / 32;  // 2 or 1
+  const int hi_bin = ob0 + per - 1 - lane * w;
+  const int c0 = static_cast<int>(h[hi_bin]);
+  const int c1 = w > 1 ? static_cast<int>(h[hi_bin - 1]) : 0;
+  const int incl2 = warp_incl_scan(c0 + c1);
+  const int pre = base + incl2 - (c0 + c1);
+  int my_digit = -1, my_above = 0;
+  if (pre < need && pre + c0 >= need) {
+    my_digit = hi_bin;
+    my_above = pre;
+  } else if (w > 1 && pre + c0 < need && pre + c0 + c1 >= need) {
+    my_digit = hi_bin - 1;
+    my_above = pre + c0;
+  }
+  const unsigned m2 = __ballot_sync(0xffffffffu, my_digit >= 0);
+  const int src = __ffs(m2) - 1;
+  *digit = static_cast<uint32_t>(__shfl_sync(0xffffffffu, my_digit, src));
+  *above = __shfl_sync(0xffffffffu, my_above, src);
+}
+
+template <typename Emit>
+__device__ inline void block_select_topk(const uint32_t* keys, int n, int k, TopkSmem& sm,
+                                         Emit emit) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int b = tid; b < 3 * 2048; b += kThreads) (&sm.hist[0][0])[b] = 0;
   __syncthreads();
   uint32_t prefix = 0, pmask = 0;
   int need = k;
-#pragma unroll 1
+#pragma unroll
   for (int round = 0; round < 3; ++round) {
-    const int shift = round_shift(round), nb = round_bins(round);
-    uint32_t* h = buf[round & 1];
+    const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
+    const int nb = round == 2 ? 1024 : 2048;
+    uint32_t* h = sm.hist[round];
     for (int i = tid; i < n; i += kThreads) {
-      const uint32_t kv = key(i);
+      const uint32_t kv = keys[i];
       if ((kv & pmask) == prefix) atomicAdd(&h[(kv >> shift) & (nb - 1)], 1u);
     }
-    if (round < 2)
-      for (int b = tid; b < 2048; b += kThreads) buf[(round + 1) & 1][b] = 0;
     __syncthreads();
-    if (tid < 32) {
-      // Lane l owns bins [(31 - l) * per, (32 - l) * per): lane 0 the highest.
-      const int per = nb / 32;
-      const int b0 = (31 - lane) * per;
-      int mine = 0;
-      for (int b = 0; b < per; ++b) mine += static_cast<int>(h[b0 + b]);
-      const int incl = warp_incl_scan(mine);
-      const int above = incl - mine;
-      if (above < need && incl >= need) {
-        int acc = above;
-        for (int b = per - 1; b >= 0; --b) {
-          const int cnt = static_cast<int>(h[b0 + b]);
-          if (acc + cnt >= need) {
-            sm.bcast[0] = b0 + b;
-            sm.bcast[1] = acc;
-            break;
-          }
-          acc += cnt;
-        }
-      }
-    }
-    __syncthreads();
-    need -= sm.bcast[1];
-    prefix |= static_cast<uint32_t>(sm.bcast[0]) << shift;
+    uint32_t digit;
+    int above;
+    warp_find_digit(h, nb, need, &digit, &above);
+    need -= above;
+    prefix |= digit << shift;
     pmask |= static_cast<uint32_t>(nb - 1) << shift;
   }
-  *need_out = need;
-  return prefix;
-}
-
-// Stable compaction of the selected entries of a virtual array of n
-// candidates: sel(i) says whether candidate i is taken, emit(i, slot) receives
-// each taken candidate with its rank among the taken ones.  Each warp owns a
-// contiguous chunk; warp totals are scanned once.  Two __syncthreads.
-template <typename Sel, typename Emit>
-__device__ inline int block_compact(int n, Sel sel, Emit emit, int32_t* scratch) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int chunk = (n + kWarps - 1) / kWarps;
+  const uint32_t thr = prefix;
+  // Fused compaction: warp w owns keys [lo, hi).
+  const int chunk = (((n + kWarps - 1) / kWarps) + 31) & ~31;
   const int lo = min(n, warp * chunk), hi = min(n, lo + chunk);
-  int cnt = 0;
+  int gt = 0, eq = 0;
   for (int base = lo; base < hi; base += 32) {
     const int i = base + lane;
-    cnt += __popc(__ballot_sync(0xffffffffu, i < hi && sel(i)));
+    const uint32_t kv = i < hi ? keys[i] : 0u;
+    gt += __popc(__ballot_sync(0xffffffffu, i < hi && kv > thr));
+    eq += __popc(__ballot_sync(0xffffffffu, i < hi && kv == thr));
   }
-  if (lane == 0) scratch[warp] = cnt;
+  if (lane == 0) {
+    sm.wcnt[0][warp] = gt;
+    sm.wcnt[1][warp] = eq;
+  }
   __syncthreads();
-  int before = 0, total = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    if (w < warp) before += scratch[w];
-    total += scratch[w];
+  int slot = 0, ties = 0;  // selected keys and ties before this warp's chunk
+  for (int w = 0; w < warp; ++w) {
+    const int e = sm.wcnt[1][w];
+    int q = need - ties;
+    q = q < 0 ? 0 : (q > e ? e : q);
+    slot += sm.wcnt[0][w] + q;
+    ties += e;
   }
   for (int base = lo; base < hi; base += 32) {
     const int i = base + lane;
-    const bool t = i < hi && sel(i);
-    const unsigned m = __ballot_sync(0xffffffffu, t);
-    if (t) emit(i, before + __popc(m & ((1u << lane) - 1u)));
-    before += __popc(m);
+    const uint32_t kv = i < hi ? keys[i] : 0u;
+    const unsigned below = (1u << lane) - 1u;
+    const unsigned eqm = __ballot_sync(0xffffffffu, i < hi && kv == thr);
+    const bool tie_taken = (eqm >> lane & 1u) && ties + __popc(eqm & below) < need;
+    const bool taken = (i < hi && kv > thr) || tie_taken;
+    const unsigned tm = __ballot_sync(0xffffffffu, taken);
+    if (taken) emit(i, slot + __popc(tm & below));
+    slot += __popc(tm);
+    ties += __popc(eqm);
   }
   __syncthreads();
-  return total;
 }
 
 // Exclusive prefix over the cluster of one int per CTA (pushed to every

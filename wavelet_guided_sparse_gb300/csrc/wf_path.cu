@@ -79,7 +79,7 @@ struct PathSmem {
   static constexpr int kRowBytes = D * static_cast<int>(sizeof(T)) + 16;  // padded row pitch
   static constexpr int kRowF = D + 4;                                      // fp32 row pitch
   size_t qs, stat_in, gm, loc, part, cnt_a, cnt_b, misc, sl_all, sp, sr, cp, cr, keys, take,
-      topk, keys_all, pos_all, take_all, klist;
+      topk, keys_all, pos_all, klist;
   size_t s_stage, s_as, s_z;       // score phase
   size_t f_kst, f_t;               // filter phase
   size_t a_kst, a_vst, a_work, a_recv, a_rml;  // attend phase
@@ -91,6 +91,7 @@ struct PathSmem {
       o = (o + bytes + 15) & ~size_t(15);
       return at;
     };
+    sp = sr = cp = cr = keys = take = 0;
     qs = take_bytes(static_cast<size_t>(kMaxQ) * kRowBytes);
     stat_in = take_bytes(sizeof(float) * kMaxCluster * 2 * kMaxQ);
     gm = take_bytes(sizeof(float) * 2 * kMaxQ);
@@ -100,16 +101,13 @@ struct PathSmem {
     cnt_b = take_bytes(sizeof(int32_t) * kMaxCluster);
     misc = take_bytes(sizeof(int32_t) * 8);
     sl_all = take_bytes(sizeof(int32_t) * p.sorted_cap);
-    sp = take_bytes(sizeof(int32_t) * p.rows_cap);
-    sr = take_bytes(sizeof(int32_t) * p.rows_cap);
-    cp = take_bytes(sizeof(int32_t) * p.rows_cap);
-    cr = take_bytes(sizeof(int32_t) * p.rows_cap);
-    keys = take_bytes(sizeof(uint32_t) * p.keys_cap);
-    take = take_bytes(p.keys_cap);
     topk = take_bytes(sizeof(TopkSmem));
-    keys_all = take_bytes(p.gather_all ? sizeof(uint32_t) * p.cs * p.keys_cap : 0);
-    pos_all = take_bytes(p.gather_all ? sizeof(int32_t) * p.cs * p.keys_cap : 0);
-    take_all = take_bytes(p.gather_all ? static_cast<size_t>(p.cs) * p.keys_cap : 0);
+    // All-gathered keys: the P coarse scores, and (final level, gather mode)
+    // every CTA's candidates with their positions.
+    const size_t gather_n = p.gather_all ? static_cast<size_t>(p.cs) * p.rows_cap : 0;
+    const size_t score_n = (p.mode & kModeScore) ? static_cast<size_t>(p.P) : 0;
+    keys_all = take_bytes(sizeof(uint32_t) * (gather_n > score_n ? gather_n : score_n));
+    pos_all = take_bytes(sizeof(int32_t) * gather_n);
     klist = take_bytes(sizeof(int32_t) * p.klist_cap);
     const size_t u = o;
     size_t end = u;
@@ -131,6 +129,12 @@ struct PathSmem {
     if (p.mode & kModeFilter) {
       o = u;
       f_kst = take_bytes(static_cast<size_t>(2) * kTileRows * kRowBytes);
+      sp = take_bytes(sizeof(int32_t) * p.rows_cap);  // survivor / candidate lists
+      sr = take_bytes(sizeof(int32_t) * p.rows_cap);
+      cp = take_bytes(sizeof(int32_t) * p.rows_cap);
+      cr = take_bytes(sizeof(int32_t) * p.rows_cap);
+      keys = take_bytes(sizeof(uint32_t) * p.keys_cap);
+      take = take_bytes(p.keys_cap);
       f_t = p.t_ws == nullptr ? take_bytes(sizeof(float) * static_cast<size_t>(p.rows_cap) * (p.G | 1)) : 0;
       end = end > o ? end : o;
     }
@@ -173,10 +177,8 @@ __device__ __forceinline__ int key_slot_owner(int g, int cs, int n_keys) {
 }
 
 // Selection among this CTA's candidates (keys[0..n)), exact over the cluster.
-__device__ __forceinline__ TopkResult cluster_select(const PathParams& p, const uint32_t* keys,
-                                                     int n, int k, uint8_t* take, TopkSmem& tk,
-                                                     uint32_t* keys_all) {
-  if (p.gather_all) return topk_gather_all(keys, n, k, take, tk, keys_all, p.keys_cap);
+__device__ __forceinline__ TopkResult cluster_select(const uint32_t* keys, int n, int k,
+                                                     uint8_t* take, TopkSmem& tk) {
   return topk_distributed(keys, n, k, take, tk);
 }
 
@@ -338,7 +340,6 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   TopkSmem& tk = *reinterpret_cast<TopkSmem*>(smem + L.topk);
   uint32_t* keys_all = reinterpret_cast<uint32_t*>(smem + L.keys_all);
   int32_t* pos_all = reinterpret_cast<int32_t*>(smem + L.pos_all);
-  uint8_t* take_all = smem + L.take_all;
   int32_t* klist = reinterpret_cast<int32_t*>(smem + L.klist);
 
   // Queries (input dtype, padded rows; rows >= G are zero).
@@ -356,13 +357,14 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
 
   // ================================================================ score
   if (p.mode & kModeScore) {
-    // Every CTA of the cluster scores all P coarse positions (redundant work
-    // that saves every cluster exchange of this phase) and selects locally.
-    const int Pc = p.P;
+    // Each CTA scores P/cs coarse positions; the per-query statistics are
+    // merged over the cluster, then every CTA receives all P scores and
+    // selects locally (so every CTA knows the sorted coarse survivors).
+    const int Pc = p.per_cta_p;
     unsigned char* as = smem + L.s_as;
     float* zc = reinterpret_cast<float*>(smem + L.s_z);  // [chunk row][query], log2 domain
     const float zscale = p.inv_sqrt_d * kLog2e;
-    const float* asrc = p.al + unit * p.P * D;
+    const float* asrc = p.al + (unit * p.P + static_cast<int64_t>(rank) * Pc) * D;
     const int nchunks = (Pc + kScoreChunk - 1) / kScoreChunk;
     uint32_t bq[4][D / 16][2];
     if constexpr (sizeof(T) == 2) load_q_frags<D>(qs, G, bq);
@@ -424,10 +426,11 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     if (tid < G) {
       float cm = -INFINITY, cl = 0.f;
       for (int w = 0; w < kWarps; ++w) merge_ml(cm, cl, part_m[w * kMaxQ + tid], part_l[w * kMaxQ + tid]);
-      gm[tid] = cm;
-      ginv[tid] = 1.f / cl;
+      loc_m[tid] = cm;
+      loc_l[tid] = cl;
     }
     __syncthreads();
+    cluster_merge_stats(loc_m, loc_l, G, stat_in, gm, ginv);
     // Pass 2: attention mass of every position (4 threads per position).
     for (int ch = 0; ch < nchunks; ++ch) {
       const int c0 = ch * kScoreChunk, rows = min(kScoreChunk, Pc - c0);
@@ -439,26 +442,17 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       sacc += __shfl_xor_sync(0xffffffffu, sacc, 1);
       sacc += __shfl_xor_sync(0xffffffffu, sacc, 2);
       if (r < rows && sub == 0) {
-        keys[c0 + r] = __float_as_uint(sacc);
-        if (p.scores_out != nullptr && rank == 0) p.scores_out[unit * p.P + c0 + r] = sacc;
+        for (int rr = 0; rr < cs; ++rr) peer(keys_all, rr)[rank * Pc + c0 + r] = __float_as_uint(sacc);
+        if (p.scores_out != nullptr) p.scores_out[unit * p.P + rank * Pc + c0 + r] = sacc;
       }
     }
-    __syncthreads();
-    // Local exact Top-k_L: threshold, ties in position order, compaction.
-    int need;
-    const uint32_t thr = block_radix_select([&](int i) { return keys[i]; }, Pc, p.kL, tk, &need);
-    for (int i = tid; i < Pc; i += kThreads) take[i] = keys[i] > thr;
-    __syncthreads();
-    block_compact(Pc, [&](int i) { return keys[i] == thr; },
-                  [&](int i, int slot) { take[i] = slot < need; }, tk.scan);
+    cluster.sync();  // every CTA holds all P scores
+    // Exact Top-k_L over all coarse positions (ties: lower position first).
     const bool to_filter = (p.mode & kModeFilter) != 0;
-    block_compact(Pc, [&](int i) { return take[i] != 0; },
-                  [&](int i, int slot) {
-                    if (slot >= p.kL) return;
-                    if (to_filter) sl_all[slot] = i;
-                    else if (rank == 0) p.idx_l_out[unit * p.kL + slot] = i;
-                  },
-                  tk.scan);
+    block_select_topk(keys_all, p.P, p.kL, tk, [&](int i, int slot) {
+      if (to_filter) sl_all[slot] = i;
+      else if (rank == 0) p.idx_l_out[unit * p.kL + slot] = i;
+    });
   } else if (p.mode & kModeFilter) {
     // Coarse survivors from the caller: load, sort ascending, validate.
     const int kL = p.kL, P = p.P;
@@ -568,8 +562,10 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       //  pass 1  CTA max per query; pass 2  e = 2^(z - max), CTA sum (at level 0
       //  e overwrites t, which is not needed afterwards); cluster merge;
       //  pass 3  s_c = Σ_i e[c,i] * w_i with w_i = 2^(max_i - gmax_i) / gsum_i.
+      // Passes 1-2: lanes = queries, each warp takes 4 candidates at a time.
       const int leaves = 1 << j;
       const float sc2 = p.scale[j] * kLog2e;
+      const bool final_gather = j == 0 && p.gather_all;
       auto node_logit = [&](int ci, int q) {
         const float* tp = t + static_cast<int64_t>(cr[ci]) * TS + q;
         float acc = 0.f;
@@ -577,9 +573,19 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         return acc * sc2;
       };
       float m0 = -INFINITY, m1 = -INFINITY;
-      for (int ci = warp; ci < n_cand; ci += kWarps) {
-        if (lane < G) m0 = fmaxf(m0, node_logit(ci, lane));
-        if (lane + 32 < G) m1 = fmaxf(m1, node_logit(ci, lane + 32));
+      for (int ci0 = warp * 4; ci0 < n_cand; ci0 += kWarps * 4) {
+        float za[4], zb[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const bool ok = ci0 + u < n_cand;
+          za[u] = ok && lane < G ? node_logit(ci0 + u, lane) : -INFINITY;
+          zb[u] = ok && lane + 32 < G ? node_logit(ci0 + u, lane + 32) : -INFINITY;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          m0 = fmaxf(m0, za[u]);
+          m1 = fmaxf(m1, zb[u]);
+        }
       }
       part_m[warp * kMaxQ + lane] = m0;
       part_m[warp * kMaxQ + lane + 32] = m1;
@@ -591,16 +597,27 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       }
       __syncthreads();
       float e0 = 0.f, e1 = 0.f;
-      for (int ci = warp; ci < n_cand; ci += kWarps) {
-        if (lane < G) {
-          const float e = exp2f(node_logit(ci, lane) - loc_m[lane]);
-          e0 += e;
-          if (j == 0) t[static_cast<int64_t>(cr[ci]) * TS + lane] = e;
-        }
-        if (lane + 32 < G) {
-          const float e = exp2f(node_logit(ci, lane + 32) - loc_m[lane + 32]);
-          e1 += e;
-          if (j == 0) t[static_cast<int64_t>(cr[ci]) * TS + lane + 32] = e;
+      {
+        const float lma = lane < G ? loc_m[lane] : 0.f;
+        const float lmb = lane + 32 < G ? loc_m[lane + 32] : 0.f;
+        for (int ci0 = warp * 4; ci0 < n_cand; ci0 += kWarps * 4) {
+          float ea[4], eb[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const bool ok = ci0 + u < n_cand;
+            ea[u] = ok && lane < G ? exp2f(node_logit(ci0 + u, lane) - lma) : 0.f;
+            eb[u] = ok && lane + 32 < G ? exp2f(node_logit(ci0 + u, lane + 32) - lmb) : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            e0 += ea[u];
+            e1 += eb[u];
+            if (j == 0 && ci0 + u < n_cand) {
+              float* tp = t + static_cast<int64_t>(cr[ci0 + u]) * TS;
+              if (lane < G) tp[lane] = ea[u];
+              if (lane + 32 < G) tp[lane + 32] = eb[u];
+            }
+          }
         }
       }
       part_l[warp * kMaxQ + lane] = e0;
@@ -612,71 +629,57 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         loc_l[tid] = l;
       }
       __syncthreads();
-      cluster_merge_stats(loc_m, loc_l, G, stat_in, gm, ginv);
+      cluster_merge_stats(loc_m, loc_l, G, stat_in, gm, ginv, n_cand, final_gather ? cnt_b : nullptr);
       float* wq = part_m;  // per-query weights (part_m is free again)
       if (tid < G) wq[tid] = loc_m[tid] == -INFINITY ? 0.f : exp2f(loc_m[tid] - gm[tid]) * ginv[tid];
       __syncthreads();
+      // Pass 3: one thread per candidate (odd row pitch: conflict-free).
       for (int ci = tid; ci < n_cand; ci += kThreads) {
-        float s = 0.f;
+        float sa = 0.f, sb = 0.f, sc = 0.f, sd = 0.f;
         if (j == 0) {
           const float* ep = t + static_cast<int64_t>(cr[ci]) * TS;
-          for (int q = 0; q < G; ++q) s += ep[q] * wq[q];
+          int q = 0;
+          for (; q + 4 <= G; q += 4) {
+            sa += ep[q] * wq[q];
+            sb += ep[q + 1] * wq[q + 1];
+            sc += ep[q + 2] * wq[q + 2];
+            sd += ep[q + 3] * wq[q + 3];
+          }
+          for (; q < G; ++q) sa += ep[q] * wq[q];
         } else {
-          for (int q = 0; q < G; ++q) s += exp2f(node_logit(ci, q) - loc_m[q]) * wq[q];
+          for (int q = 0; q < G; ++q) sa += exp2f(node_logit(ci, q) - loc_m[q]) * wq[q];
         }
-        keys[ci] = __float_as_uint(s);
+        keys[ci] = __float_as_uint((sa + sb) + (sc + sd));
       }
       __syncthreads();
-      if (j == 0 && p.gather_all) {
-        // Final level: every CTA receives every candidate (score, position),
-        // selects the budget locally and keeps the token list it needs: its
+      if (final_gather) {
+        // Every CTA receives every candidate (score, position) at its dense
+        // offset, selects the budget locally and keeps what it needs: its
         // slot range of the key list (attend) and of the output (idx).
-        const int cap = p.keys_cap;
+        int off = 0, n_all = 0;
+        for (int r = 0; r < cs; ++r) {
+          if (r < rank) off += cnt_b[r];
+          n_all += cnt_b[r];
+        }
         for (int e = tid; e < n_cand * cs; e += kThreads) {
           const int i = e % n_cand, r = e / n_cand;
-          peer(keys_all, r)[rank * cap + i] = keys[i];
-          peer(pos_all, r)[rank * cap + i] = cp[i];
+          peer(keys_all, r)[off + i] = keys[i];
+          peer(pos_all, r)[off + i] = cp[i];
         }
-        if (tid < cs) peer(tk.nloc_in, tid)[rank] = n_cand;
         cluster.sync();
-        if (tid == 0) {
-          int o = 0;
-          for (int r = 0; r < cs; ++r) {
-            tk.red[r] = o;
-            o += tk.nloc_in[r];
-          }
-          tk.red[cs] = o;
-        }
-        __syncthreads();
-        const int n_all = tk.red[cs];
-        auto vslot = [&](int v) {  // dense candidate v -> (rank, local index) storage slot
-          int r = 0;
-          while (r + 1 < cs && tk.red[r + 1] <= v) ++r;
-          return r * cap + (v - tk.red[r]);
-        };
-        int need;
-        const uint32_t thr = block_radix_select([&](int v) { return keys_all[vslot(v)]; }, n_all,
-                                                p.k[0], tk, &need);
-        for (int v = tid; v < n_all; v += kThreads) take_all[v] = keys_all[vslot(v)] > thr;
-        __syncthreads();
-        block_compact(n_all, [&](int v) { return keys_all[vslot(v)] == thr; },
-                      [&](int v, int slot) { take_all[v] = slot < need; }, tk.scan);
         const int B = p.budget;
         const int a0 = key_slot_start(rank, cs, p.n_keys), a1 = key_slot_start(rank + 1, cs, p.n_keys);
         const int w0 = key_slot_start(rank, cs, B), w1 = key_slot_start(rank + 1, cs, B);
         const bool attend = (p.mode & kModeAttend) != 0;
-        block_compact(n_all, [&](int v) { return take_all[v] != 0; },
-                      [&](int v, int slot) {
-                        if (slot >= B) return;
-                        const int pos = pos_all[vslot(v)];
-                        if (attend && slot >= a0 && slot < a1) klist[slot - a0] = pos;
-                        if (p.idx_out != nullptr && slot >= w0 && slot < w1) p.idx_out[unit * B + slot] = pos;
-                      },
-                      tk.scan);
+        block_select_topk(keys_all, n_all, B, tk, [&](int v, int slot) {
+          const int pos = pos_all[v];
+          if (attend && slot >= a0 && slot < a1) klist[slot - a0] = pos;
+          if (p.idx_out != nullptr && slot >= w0 && slot < w1) p.idx_out[unit * B + slot] = pos;
+        });
         global_done = true;
         break;
       }
-      (void)cluster_select(p, keys, n_cand, p.k[j], take, tk, keys_all);
+      (void)cluster_select(keys, n_cand, p.k[j], take, tk);
       n_surv = compact2(cp, cr, take, n_cand, sp, sr, tk.scan);
     }
     // Tokens of this CTA: sp[0, n_surv), ascending.
@@ -1086,6 +1089,7 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
   // per-CTA slices) are tried before giving up.
   int cs0 = pow2_floor(std::max(1, static_cast<int>(std::min<int64_t>(kMaxCluster, sm_count / std::max<int64_t>(1, ld.units)))));
   auto cluster_ok = [&](int c) {
+    if ((mode & kModeScore) && (p.P % c != 0 || p.P / c < 8)) return false;
     if (mode == kModeScore && c > 1) return false;  // scoring alone needs no cluster
     if ((mode & kModeFilter) && k_l < c) return false;
     if ((mode & kModeAttend) && p.n_keys < 16 * c) return false;
@@ -1098,7 +1102,7 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
   bool found = false;
   for (;; cs *= 2) {
     p.cs = cs;
-    p.per_cta_p = (mode & kModeScore) ? p.P : 0;  // every CTA scores all positions
+    p.per_cta_p = (mode & kModeScore) ? p.P / cs : 0;
     const int spans_cap = (mode & kModeFilter) ? (k_l + cs - 1) / cs : 0;
     p.rows_cap = spans_cap << ld.levels;
     int sc = 1;
@@ -1114,7 +1118,7 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
     }
     // Prefer the gather-all selection and token logits in shared memory.
     for (int ga = 1; ga >= 0 && !found; --ga) {
-      if (ga && static_cast<int64_t>(cs) * p.keys_cap > 8192) continue;
+      if (ga && (!(mode & kModeFilter) || static_cast<int64_t>(cs) * p.rows_cap > 8192)) continue;
       p.gather_all = ga;
       p.t_ws = nullptr;
       smem = smem_bytes(ld, p);
