@@ -411,35 +411,49 @@ __device__ inline TopkResult topk_distributed(const uint32_t* keys, int n, int k
 // bins).  A fused pass counts, per warp chunk, the keys above the threshold
 // and the ties, and emit(i, slot) receives every selected key with its rank
 // among the selected (ascending index).  Six __syncthreads in total.
+// Histogram bins are stored transposed — bin b of a round with `per` bins per
+// lane lives at (b % per) * 32 + b / per — so that every lane of a warp reads
+// a different bank while summing its own contiguous bin range.
+__device__ __forceinline__ int hist_index(uint32_t bin, int per) {
+  return static_cast<int>((bin & (per - 1)) * 32 + bin / per);
+}
+
+// Shared-memory histogram increment aggregated over the lanes of a warp that
+// hit the same bin (scores cluster in a few bins in the first round).
+__device__ __forceinline__ void hist_add(uint32_t* h, bool active, uint32_t bin, int per) {
+  const unsigned act = __ballot_sync(0xffffffffu, active);
+  if (!active) return;
+  const unsigned peers = __match_any_sync(act, bin);
+  if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[hist_index(bin, per)], __popc(peers));
+}
+
 __device__ __forceinline__ void warp_find_digit(const uint32_t* h, int nb, int need,
                                                 uint32_t* digit, int* above) {
   const int lane = threadIdx.x & 31;
-  const int per = nb / 32;             // 64 or 32 bins per lane
-  const int b0 = (31 - lane) * per;    // lane 0 owns the highest bins
+  const int per = nb / 32;       // 64 or 32 bins per lane
+  const int region = 31 - lane;  // lane 0 owns the highest bins
   int sum = 0;
-  for (int v = 0; v < per; v += 4) {
-    const uint4 q = *reinterpret_cast<const uint4*>(h + b0 + v);
-    sum += static_cast<int>(q.x + q.y + q.z + q.w);
-  }
+#pragma unroll 8
+  for (int v = 0; v < per; ++v) sum += static_cast<int>(h[v * 32 + region]);
   const int incl = warp_incl_scan(sum);
   const int before = incl - sum;
   const unsigned owner_mask = __ballot_sync(0xffffffffu, before < need && incl >= need);
   const int owner = __ffs(owner_mask) - 1;
   const int base = __shfl_sync(0xffffffffu, before, owner);
-  const int ob0 = (31 - owner) * per;
+  const int oreg = 31 - owner;
   // Inside the owner's bins, descending: lane l takes per/32 consecutive bins.
   const int w = per / 32;  // 2 or 1
-  const int hi_bin = ob0 + per - 1 - lane * w;
-  const int c0 = static_cast<int>(h[hi_bin]);
-  const int c1 = w > 1 ? static_cast<int>(h[hi_bin - 1]) : 0;
+  const int hi_off = per - 1 - lane * w;  // offset within the owner's region
+  const int c0 = static_cast<int>(h[hi_off * 32 + oreg]);
+  const int c1 = w > 1 ? static_cast<int>(h[(hi_off - 1) * 32 + oreg]) : 0;
   const int incl2 = warp_incl_scan(c0 + c1);
   const int pre = base + incl2 - (c0 + c1);
   int my_digit = -1, my_above = 0;
   if (pre < need && pre + c0 >= need) {
-    my_digit = hi_bin;
+    my_digit = oreg * per + hi_off;
     my_above = pre;
   } else if (w > 1 && pre + c0 < need && pre + c0 + c1 >= need) {
-    my_digit = hi_bin - 1;
+    my_digit = oreg * per + hi_off - 1;
     my_above = pre + c0;
   }
   const unsigned m2 = __ballot_sync(0xffffffffu, my_digit >= 0);
@@ -461,9 +475,11 @@ __device__ inline void block_select_topk(const uint32_t* keys, int n, int k, Top
     const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
     const int nb = round == 2 ? 1024 : 2048;
     uint32_t* h = sm.hist[round];
-    for (int i = tid; i < n; i += kThreads) {
-      const uint32_t kv = keys[i];
-      if ((kv & pmask) == prefix) atomicAdd(&h[(kv >> shift) & (nb - 1)], 1u);
+    const int per = nb / 32;
+    for (int base = 0; base < n; base += kThreads) {  // whole warps iterate together
+      const int i = base + tid;
+      const uint32_t kv = i < n ? keys[i] : 0u;
+      hist_add(h, i < n && (kv & pmask) == prefix, (kv >> shift) & (nb - 1), per);
     }
     __syncthreads();
     uint32_t digit;

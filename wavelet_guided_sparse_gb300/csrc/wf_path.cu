@@ -566,20 +566,25 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       const int leaves = 1 << j;
       const float sc2 = p.scale[j] * kLog2e;
       const bool final_gather = j == 0 && p.gather_all;
-      auto node_logit = [&](int ci, int q) {
-        const float* tp = t + static_cast<int64_t>(cr[ci]) * TS + q;
-        float acc = 0.f;
-        for (int i = 0; i < leaves; ++i) acc += tp[i * TS];
-        return acc * sc2;
-      };
+      // z of candidate ci for query q (leaf sums of t; one leaf at level 0).
+      const float* tq0 = t + (lane < G ? lane : 0);
+      const float* tq1 = t + (lane + 32 < G ? lane + 32 : 0);
+      const bool qa = lane < G, qb = lane + 32 < G;
       float m0 = -INFINITY, m1 = -INFINITY;
       for (int ci0 = warp * 4; ci0 < n_cand; ci0 += kWarps * 4) {
         float za[4], zb[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
+          const int ci = min(ci0 + u, n_cand - 1);
+          const int64_t row = static_cast<int64_t>(cr[ci]) * TS;
+          float a = tq0[row], b = tq1[row];
+          for (int i = 1; i < leaves; ++i) {
+            a += tq0[row + i * TS];
+            b += tq1[row + i * TS];
+          }
           const bool ok = ci0 + u < n_cand;
-          za[u] = ok && lane < G ? node_logit(ci0 + u, lane) : -INFINITY;
-          zb[u] = ok && lane + 32 < G ? node_logit(ci0 + u, lane + 32) : -INFINITY;
+          za[u] = ok && qa ? a * sc2 : -INFINITY;
+          zb[u] = ok && qb ? b * sc2 : -INFINITY;
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -598,24 +603,31 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       __syncthreads();
       float e0 = 0.f, e1 = 0.f;
       {
-        const float lma = lane < G ? loc_m[lane] : 0.f;
-        const float lmb = lane + 32 < G ? loc_m[lane + 32] : 0.f;
+        const float lma = qa ? loc_m[lane] : 0.f;
+        const float lmb = qb ? loc_m[lane + 32] : 0.f;
         for (int ci0 = warp * 4; ci0 < n_cand; ci0 += kWarps * 4) {
           float ea[4], eb[4];
+          int64_t rows[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
+            const int ci = min(ci0 + u, n_cand - 1);
+            rows[u] = static_cast<int64_t>(cr[ci]) * TS;
+            float a = tq0[rows[u]], b = tq1[rows[u]];
+            for (int i = 1; i < leaves; ++i) {
+              a += tq0[rows[u] + i * TS];
+              b += tq1[rows[u] + i * TS];
+            }
             const bool ok = ci0 + u < n_cand;
-            ea[u] = ok && lane < G ? exp2f(node_logit(ci0 + u, lane) - lma) : 0.f;
-            eb[u] = ok && lane + 32 < G ? exp2f(node_logit(ci0 + u, lane + 32) - lmb) : 0.f;
+            ea[u] = ok && qa ? exp2f(a * sc2 - lma) : 0.f;
+            eb[u] = ok && qb ? exp2f(b * sc2 - lmb) : 0.f;
           }
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             e0 += ea[u];
             e1 += eb[u];
-            if (j == 0 && ci0 + u < n_cand) {
-              float* tp = t + static_cast<int64_t>(cr[ci0 + u]) * TS;
-              if (lane < G) tp[lane] = ea[u];
-              if (lane + 32 < G) tp[lane + 32] = eb[u];
+            if (j == 0 && ci0 + u < n_cand) {  // level 0: e replaces t
+              if (qa) t[rows[u] + lane] = ea[u];
+              if (qb) t[rows[u] + lane + 32] = eb[u];
             }
           }
         }
@@ -647,7 +659,12 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           }
           for (; q < G; ++q) sa += ep[q] * wq[q];
         } else {
-          for (int q = 0; q < G; ++q) sa += exp2f(node_logit(ci, q) - loc_m[q]) * wq[q];
+          const float* tp = t + static_cast<int64_t>(cr[ci]) * TS;
+          for (int q = 0; q < G; ++q) {
+            float z = 0.f;
+            for (int i = 0; i < leaves; ++i) z += tp[i * TS + q];
+            sa += exp2f(z * sc2 - loc_m[q]) * wq[q];
+          }
         }
         keys[ci] = __float_as_uint((sa + sb) + (sc + sd));
       }
