@@ -211,6 +211,33 @@ int wf_step_host(const wf_dims* dims, const void* h_Q, const void* h_Kp,
                  float* d_O, float* d_lse, void* workspace,
                  size_t workspace_bytes, void* stream);
 
+/* Size of the device scratch array behind wf_step_static_scratch (48 MiB). */
+#define WF_STATIC_SCRATCH_BYTES (48u << 20)
+
+/* wf_step without a workspace argument and without any device allocation.
+ * The paper has no counterpart: this entry point exists for callers that
+ * cannot allocate device memory — plugin or enqueue interfaces of inference
+ * engines that forbid allocation inside the call, or latency-critical loops
+ * that cannot afford cudaMalloc's implicit device synchronisation.
+ *   Arguments, layouts, outputs and errors: as wf_step, minus workspace.
+ *   Scratch: a file-scope device array of WF_STATIC_SCRATCH_BYTES bytes that
+ *   every GPU loading this library holds until the process exits.  Sizes
+ *   whose wf_workspace_bytes() exceeds it are rejected with WF_ERR_WORKSPACE
+ *   before anything is enqueued (e.g. the batched-long workloads at 5 % and
+ *   10 % budgets).
+ *   The first call on a device, with that device current, looks up the
+ *   array's device address (cudaGetSymbolAddress); make that first call
+ *   before any stream capture.  Every call shares the one array and it keeps
+ *   the last call's contents (the status word is cleared at the start of each
+ *   call), so calls that overlap on the GPU — concurrent streams, or several
+ *   host threads — race; serialise them.  The device status word is not
+ *   readable through this entry point (use wf_step for diagnostics).
+ *   Calls no cudaMalloc, cudaFree or other allocating routine. */
+int wf_step_static_scratch(const wf_dims* dims, const void* Q, const void* Kp,
+                           const void* Vp, const void* Kg, const void* Vg,
+                           const int32_t* k_per_level, float* O, float* lse,
+                           int32_t* idx_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,66 @@
+"""The allocation-free entry point, wf_step_static_scratch.
+
+Some callers cannot allocate device memory: plugin or enqueue interfaces of
+inference engines that forbid allocation inside the call, and latency-critical
+loops that cannot afford cudaMalloc's implicit device synchronisation.  For
+them the library keeps its scratch in a fixed device array.  This test calls
+that entry point twice in a row through the C ABI and checks each result
+against the ordinary workspace entry point, wf_step, on the same inputs.
+
+The file is named to be collected last, so a run that stops at the first
+failure has already run every other test; it also passes on its own.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from wavelet_guided_sparse_gb300 import binding as bd
+from wavelet_guided_sparse_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+OUT_ATOL = 2e-2  # the attention-output tolerance of the parity tests
+
+
+def _inputs(name, layer=0):
+    cfg = wl.CONFIGS[name]
+    arrs = wl.generate_layer(cfg, layer)
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    return cfg, {k: torch.from_numpy(v).to(device="cuda", dtype=dt) for k, v in arrs.items()}
+
+
+@pytest.mark.parametrize("name", ["tiny", "llada8b_layer"])
+def test_static_scratch_matches_workspace_entry_point(name):
+    cfg, dev = _inputs(name)
+    ks = cfg.k_per_level()
+    dims = bd.make_dims(dev["Q"], dev["Kp"], cfg.levels)
+    ws = bd.alloc_workspace(dims, ks, dev["Q"].device)
+    ref_idx = torch.empty((cfg.batch, cfg.heads, ks[0]), dtype=torch.int32, device="cuda")
+    ref = bd.step(dev["Q"], dev["Kp"], dev["Vp"], dev["Kg"], dev["Vg"], cfg.levels, ks, ws,
+                  idx_out=ref_idx)
+    assert bd.read_device_status(ws) == 0
+    for call in range(2):  # the array keeps the previous call's contents
+        idx = torch.empty_like(ref_idx)
+        lse = torch.empty(dev["Q"].shape[:3], dtype=torch.float32, device="cuda")
+        out = bd.step_static_scratch(dev["Q"], dev["Kp"], dev["Vp"], dev["Kg"], dev["Vg"],
+                                     cfg.levels, ks, lse=lse, idx_out=idx)
+        torch.cuda.synchronize()
+        err = (out - ref).abs().max().item()
+        assert err <= OUT_ATOL, (call, err)
+        assert torch.equal(idx, ref_idx), call
+        assert torch.isfinite(lse).all()
+
+
+def test_static_scratch_rejects_sizes_beyond_its_limit():
+    # The 10 % budget of the batched-long workload needs far more scratch than
+    # the fixed array holds: rejected on the host before anything runs.
+    cfg = wl.CONFIGS["batched_long_10pct"]
+    dims = bd.Dims(cfg.batch, cfg.heads, cfg.n_prompt, cfg.n_gen, cfg.head_dim, cfg.levels, 0)
+    assert bd.workspace_bytes(dims, cfg.k_per_level()) > (48 << 20)
+    small = torch.empty(16, dtype=torch.bfloat16, device="cuda")
+    st = bd.lib().wf_step_static_scratch(bd.ctypes.byref(dims), bd._ptr(small), bd._ptr(small),
+                                         bd._ptr(small), bd._ptr(small), bd._ptr(small),
+                                         bd._k_array(cfg.k_per_level()), bd._ptr(small), None,
+                                         None, None)
+    assert st == 4  # WF_ERR_WORKSPACE

@@ -28,7 +28,7 @@ MAX_LEVELS = 12
 EXPORTS = ("wf_status_string", "wf_last_error_string", "wf_default_k_per_level", "wf_workspace_bytes",
            "wf_clear_device_status", "wf_read_device_status", "wf_dwt_lowpass",
            "wf_score_topk", "wf_recursive_filter", "wf_sparse_gather_attn", "wf_step",
-           "wf_step_host")
+           "wf_step_host", "wf_step_static_scratch")
 
 
 class WfError(RuntimeError):
@@ -67,6 +67,8 @@ _SIGS = {
                                _vp, _sz, _vp]),
     "wf_step_host": (ctypes.c_int, [_DIMSP, _vp, _vp, _vp, _vp, _vp, _i32p, _vp, _vp,
                                     _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "wf_step_static_scratch": (ctypes.c_int, [_DIMSP, _vp, _vp, _vp, _vp, _vp, _i32p, _vp,
+                                              _vp, _vp, _vp]),
 }
 
 
@@ -270,6 +272,23 @@ def step_host(dims: Dims, host: dict, k_per_level: Sequence[int], dev: dict, ws:
         _ptr(host.get("lse")), _ptr(dev["Q"]), _ptr(dev["Kp"]), _ptr(dev["Vp"]),
         _ptr(dev["Kg"]), _ptr(dev["Vg"]), _ptr(dev["O"]), _ptr(dev.get("lse")), _ptr(ws),
         ws.numel(), _stream(stream)))
+
+
+def step_static_scratch(q, kp, vp, kg, vg, levels: int, k_per_level: Sequence[int],
+                        out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                        idx_out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """wf_step_static_scratch: the whole path using the library's fixed device
+    scratch array instead of a workspace (no device allocation inside the
+    call).  Calls that overlap on the GPU share that array and race."""
+    for t, n in ((q, "Q"), (kp, "Kp"), (vp, "Vp"), (kg, "Kg"), (vg, "Vg")):
+        _require(t, n, q.dtype)
+    dims = make_dims(q, kp, levels)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    _check("wf_step_static_scratch", lib().wf_step_static_scratch(
+        ctypes.byref(dims), _ptr(q), _ptr(kp), _ptr(vp), _ptr(kg), _ptr(vg),
+        _k_array(k_per_level), _ptr(out), _ptr(lse), _ptr(idx_out), _stream(stream)))
+    return out
 
 
 def raw_call(name: str, *args) -> int:
