@@ -234,7 +234,7 @@ constexpr int kMaxQ = 64;  // maximum queries per unit
 // gm/ginv hold the cluster-wide max and 1 / sum.  stat_in: [kMaxCluster][2]
 // [kMaxQ] floats.  If counts_in is not null, `my_count` is all-gathered into
 // counts_in[rank] in the same exchange.  One cluster barrier.
-__device__ inline void cluster_merge_stats(const float* loc_m, const float* loc_l, int G,
+static __device__ __noinline__ void cluster_merge_stats(const float* loc_m, const float* loc_l, int G,
                                            float* stat_in, float* gm, float* ginv,
                                            int my_count = 0, int32_t* counts_in = nullptr) {
   cg::cluster_group cluster = cg::this_cluster();
@@ -274,6 +274,7 @@ __device__ inline void cluster_merge_stats(const float* loc_m, const float* loc_
 // all-gathered through DSMEM; two barriers per round) for large ones.
 struct TopkSmem {
   uint32_t hist[3][2048];          // digit histograms (one per radix round)
+  uint32_t region[3][32];          // per-round counts of 32 equal bin ranges
   int32_t cnt_in[kMaxCluster][2];  // distributed: (#> T, #== T) pushed by each rank
   int32_t wcnt[2][kWarps];         // block select: per-warp (#> T, #== T)
   int32_t scan[kWarps + 1];
@@ -336,7 +337,7 @@ __device__ inline void mark_taken(const uint32_t* keys, int n, uint32_t thr, int
 }
 
 // Distributed variant (any candidate count).
-__device__ inline TopkResult topk_distributed(const uint32_t* keys, int n, int k, uint8_t* take,
+static __device__ __noinline__ TopkResult topk_distributed(const uint32_t* keys, int n, int k, uint8_t* take,
                                               TopkSmem& sm) {
   cg::cluster_group cluster = cg::this_cluster();
   const int cs = static_cast<int>(cluster.num_blocks());
@@ -411,49 +412,47 @@ __device__ inline TopkResult topk_distributed(const uint32_t* keys, int n, int k
 // bins).  A fused pass counts, per warp chunk, the keys above the threshold
 // and the ties, and emit(i, slot) receives every selected key with its rank
 // among the selected (ascending index).  Six __syncthreads in total.
-// Histogram bins are stored transposed — bin b of a round with `per` bins per
-// lane lives at (b % per) * 32 + b / per — so that every lane of a warp reads
-// a different bank while summing its own contiguous bin range.
-__device__ __forceinline__ int hist_index(uint32_t bin, int per) {
-  return static_cast<int>((bin & (per - 1)) * 32 + bin / per);
-}
-
 // Shared-memory histogram increment aggregated over the lanes of a warp that
-// hit the same bin (scores cluster in a few bins in the first round).
-__device__ __forceinline__ void hist_add(uint32_t* h, bool active, uint32_t bin, int per) {
+// hit the same bin (scores cluster in a few bins in the first round); the
+// count of the bin's range of nb/32 bins is kept alongside.
+__device__ __forceinline__ void hist_add(uint32_t* h, uint32_t* region, bool active, uint32_t bin,
+                                         int per) {
   const unsigned act = __ballot_sync(0xffffffffu, active);
   if (!active) return;
   const unsigned peers = __match_any_sync(act, bin);
-  if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[hist_index(bin, per)], __popc(peers));
+  if ((threadIdx.x & 31) == __ffs(peers) - 1) {
+    atomicAdd(&h[bin], __popc(peers));
+    atomicAdd(&region[bin / per], __popc(peers));
+  }
 }
 
-__device__ __forceinline__ void warp_find_digit(const uint32_t* h, int nb, int need,
-                                                uint32_t* digit, int* above) {
+// Digit d of the round with #{digit > d} < need <= #{digit >= d}, found by one
+// warp from the 32 range counts (lane 0 = highest range) and then the bins of
+// the boundary range (descending, per/32 bins per lane).  Every lane returns
+// the digit and #{digit > d}.
+__device__ __forceinline__ void warp_find_digit(const uint32_t* h, const uint32_t* region, int nb,
+                                                int need, uint32_t* digit, int* above) {
   const int lane = threadIdx.x & 31;
-  const int per = nb / 32;       // 64 or 32 bins per lane
-  const int region = 31 - lane;  // lane 0 owns the highest bins
-  int sum = 0;
-#pragma unroll 8
-  for (int v = 0; v < per; ++v) sum += static_cast<int>(h[v * 32 + region]);
-  const int incl = warp_incl_scan(sum);
-  const int before = incl - sum;
+  const int per = nb / 32;  // 64 or 32 bins per range
+  const int rc = static_cast<int>(region[31 - lane]);
+  const int incl = warp_incl_scan(rc);
+  const int before = incl - rc;
   const unsigned owner_mask = __ballot_sync(0xffffffffu, before < need && incl >= need);
   const int owner = __ffs(owner_mask) - 1;
   const int base = __shfl_sync(0xffffffffu, before, owner);
-  const int oreg = 31 - owner;
-  // Inside the owner's bins, descending: lane l takes per/32 consecutive bins.
-  const int w = per / 32;  // 2 or 1
-  const int hi_off = per - 1 - lane * w;  // offset within the owner's region
-  const int c0 = static_cast<int>(h[hi_off * 32 + oreg]);
-  const int c1 = w > 1 ? static_cast<int>(h[(hi_off - 1) * 32 + oreg]) : 0;
+  const int obin0 = (31 - owner) * per;  // lowest bin of the boundary range
+  const int w = per / 32;                // 2 or 1
+  const int hi_bin = obin0 + per - 1 - lane * w;
+  const int c0 = static_cast<int>(h[hi_bin]);
+  const int c1 = w > 1 ? static_cast<int>(h[hi_bin - 1]) : 0;
   const int incl2 = warp_incl_scan(c0 + c1);
   const int pre = base + incl2 - (c0 + c1);
   int my_digit = -1, my_above = 0;
   if (pre < need && pre + c0 >= need) {
-    my_digit = oreg * per + hi_off;
+    my_digit = hi_bin;
     my_above = pre;
   } else if (w > 1 && pre + c0 < need && pre + c0 + c1 >= need) {
-    my_digit = oreg * per + hi_off - 1;
+    my_digit = hi_bin - 1;
     my_above = pre + c0;
   }
   const unsigned m2 = __ballot_sync(0xffffffffu, my_digit >= 0);
@@ -462,15 +461,17 @@ __device__ __forceinline__ void warp_find_digit(const uint32_t* h, int nb, int n
   *above = __shfl_sync(0xffffffffu, my_above, src);
 }
 
-template <typename Emit>
-__device__ inline void block_select_topk(const uint32_t* keys, int n, int k, TopkSmem& sm,
-                                         Emit emit) {
+// Writes out[slot - lo] = i for every selected key i whose rank among the
+// selected (ascending index) falls in [lo, hi).
+static __device__ __noinline__ void block_select_topk(const uint32_t* keys, int n, int k, int lo_slot,
+                                               int hi_slot, int32_t* out, TopkSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int b = tid; b < 3 * 2048; b += kThreads) (&sm.hist[0][0])[b] = 0;
+  if (tid < 3 * 32) (&sm.region[0][0])[tid] = 0;
   __syncthreads();
   uint32_t prefix = 0, pmask = 0;
   int need = k;
-#pragma unroll
+#pragma unroll 1
   for (int round = 0; round < 3; ++round) {
     const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
     const int nb = round == 2 ? 1024 : 2048;
@@ -479,12 +480,12 @@ __device__ inline void block_select_topk(const uint32_t* keys, int n, int k, Top
     for (int base = 0; base < n; base += kThreads) {  // whole warps iterate together
       const int i = base + tid;
       const uint32_t kv = i < n ? keys[i] : 0u;
-      hist_add(h, i < n && (kv & pmask) == prefix, (kv >> shift) & (nb - 1), per);
+      hist_add(h, sm.region[round], i < n && (kv & pmask) == prefix, (kv >> shift) & (nb - 1), per);
     }
     __syncthreads();
     uint32_t digit;
     int above;
-    warp_find_digit(h, nb, need, &digit, &above);
+    warp_find_digit(h, sm.region[round], nb, need, &digit, &above);
     need -= above;
     prefix |= digit << shift;
     pmask |= static_cast<uint32_t>(nb - 1) << shift;
@@ -521,7 +522,8 @@ __device__ inline void block_select_topk(const uint32_t* keys, int n, int k, Top
     const bool tie_taken = (eqm >> lane & 1u) && ties + __popc(eqm & below) < need;
     const bool taken = (i < hi && kv > thr) || tie_taken;
     const unsigned tm = __ballot_sync(0xffffffffu, taken);
-    if (taken) emit(i, slot + __popc(tm & below));
+    const int my_slot = slot + __popc(tm & below);
+    if (taken && my_slot >= lo_slot && my_slot < hi_slot) out[my_slot - lo_slot] = i;
     slot += __popc(tm);
     ties += __popc(eqm);
   }
@@ -548,7 +550,7 @@ __device__ inline int cluster_excl_count(int mine, int32_t* cnt_in, int* total) 
 
 // Stable compaction of the taken entries of two parallel int arrays.
 // Returns the new count.  Block-wide (contains __syncthreads()).
-__device__ inline int compact2(const int32_t* a_in, const int32_t* b_in, const uint8_t* take,
+static __device__ __noinline__ int compact2(const int32_t* a_in, const int32_t* b_in, const uint8_t* take,
                                int n, int32_t* a_out, int32_t* b_out, int32_t* scan) {
   int carry = 0;
   for (int base = 0; base < n; base += kThreads) {

@@ -189,11 +189,10 @@ __device__ __forceinline__ TopkResult cluster_select(const uint32_t* keys, int n
 // hi + mid + lo reproduce an fp32 row exactly).  Warp w: 16-row block (w & 3),
 // n-blocks (w >> 2) + 2i of 8 queries each.
 template <int D>
-__device__ __forceinline__ void logits_tile_bf16(const unsigned char* rows, int nplanes,
-                                                 int plane_bytes,
-                                                 const uint32_t (&bq)[4][D / 16][2], float* out,
-                                                 int row0, int rows_valid, int G, int pitch,
-                                                 float scale) {
+__device__ __noinline__ void logits_tile_bf16(const unsigned char* rows, int nplanes,
+                                              int plane_bytes, const unsigned char* qs,
+                                              float* out, int row0, int rows_valid, int G,
+                                              int pitch, float scale) {
   constexpr int RB = D * 2 + 16;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int mb = warp & 3, ng = warp >> 2;
@@ -203,16 +202,23 @@ __device__ __forceinline__ void logits_tile_bf16(const unsigned char* rows, int 
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
+  const uint32_t qbase = smem_u32(qs) + (lane & 7) * RB + ((lane >> 3) & 1) * 16;
   for (int pl = 0; pl < nplanes; ++pl) {
     const uint32_t abase =
         smem_u32(rows + pl * plane_bytes) + (mb * 16 + (lane & 15)) * RB + (lane >> 4) * 16;
-#pragma unroll
+#pragma unroll 2
     for (int ks = 0; ks < D / 16; ++ks) {
       uint32_t a[4];
       ldsm_x4(abase + ks * 32, a);
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (ng + 2 * i < NB) mma_bf16(acc[i], a, bq[i][ks]);
+      for (int i = 0; i < 4; ++i) {
+        const int nb = ng + 2 * i;
+        if (nb < NB) {  // Q B-fragment: 8 queries x 16 dims
+          uint32_t b[2];
+          ldsm_x2(qbase + nb * 8 * RB + ks * 32, b);
+          mma_bf16(acc[i], a, b);
+        }
+      }
     }
   }
   const int r_lo = mb * 16 + (lane >> 2);
@@ -366,8 +372,6 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     const float zscale = p.inv_sqrt_d * kLog2e;
     const float* asrc = p.al + (unit * p.P + static_cast<int64_t>(rank) * Pc) * D;
     const int nchunks = (Pc + kScoreChunk - 1) / kScoreChunk;
-    uint32_t bq[4][D / 16][2];
-    if constexpr (sizeof(T) == 2) load_q_frags<D>(qs, G, bq);
     // z for chunk rows [c0, c0 + rows): stage A_L (bf16 inputs: exact
     // hi + mid + lo bf16 planes), then one tensor-core / FMA tile.
     float* stage_f = reinterpret_cast<float*>(smem + L.s_stage);  // [64][D + 4] fp32
@@ -401,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
                 make_uint2(pack_bf16(pv[pl][0], pv[pl][1]), pack_bf16(pv[pl][2], pv[pl][3]));
         }
         __syncthreads();
-        logits_tile_bf16<D>(as, 3, kScoreChunk * RB, bq, zc, 0, rows, G, TS, zscale);
+        logits_tile_bf16<D>(as, 3, kScoreChunk * RB, qs, zc, 0, rows, G, TS, zscale);
       } else {
         logits_tile_f32<D>(as, reinterpret_cast<const float*>(qs), zc, 0, rows, G, TS, zscale);
       }
@@ -449,10 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     cluster.sync();  // every CTA holds all P scores
     // Exact Top-k_L over all coarse positions (ties: lower position first).
     const bool to_filter = (p.mode & kModeFilter) != 0;
-    block_select_topk(keys_all, p.P, p.kL, tk, [&](int i, int slot) {
-      if (to_filter) sl_all[slot] = i;
-      else if (rank == 0) p.idx_l_out[unit * p.kL + slot] = i;
-    });
+    block_select_topk(keys_all, p.P, p.kL, 0, p.kL, sl_all, tk);
+    if (!to_filter && rank == 0)
+      for (int i = tid; i < p.kL; i += kThreads) p.idx_l_out[unit * p.kL + i] = sl_all[i];
   } else if (p.mode & kModeFilter) {
     // Coarse survivors from the caller: load, sort ascending, validate.
     const int kL = p.kL, P = p.P;
@@ -516,8 +519,6 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     };
     if (ntiles > 0) issue(0, 0);
     if (ntiles > 1) issue(1, 1);
-    uint32_t bq[4][D / 16][2];
-    if constexpr (sizeof(T) == 2) load_q_frags<D>(qs, G, bq);
     for (int tile = 0; tile < ntiles; ++tile) {
       const int stage = tile & 1;
       if (tile + 1 < ntiles) cp_async_wait<1>(); else cp_async_wait<0>();
@@ -525,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       const unsigned char* buf = kst + stage * kTileRows * RB;
       const int rows_valid = min(kTileRows, R - tile * kTileRows);
       if constexpr (sizeof(T) == 2) {
-        logits_tile_bf16<D>(buf, 1, 0, bq, t, tile * kTileRows, rows_valid, G, TS, 1.f);
+        logits_tile_bf16<D>(buf, 1, 0, qs, t, tile * kTileRows, rows_valid, G, TS, 1.f);
       } else {
         logits_tile_f32<D>(buf, reinterpret_cast<const float*>(qs), t, tile * kTileRows,
                            rows_valid, G, TS, 1.f);
@@ -566,30 +567,36 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       const int leaves = 1 << j;
       const float sc2 = p.scale[j] * kLog2e;
       const bool final_gather = j == 0 && p.gather_all;
-      // z of candidate ci for query q (leaf sums of t; one leaf at level 0).
-      const float* tq0 = t + (lane < G ? lane : 0);
-      const float* tq1 = t + (lane + 32 < G ? lane + 32 : 0);
+      // z of candidate ci for query q: leaf sums of t (one leaf at level 0).
+      // Lanes = queries q and q + 32.  Single-leaf levels take 4 candidates
+      // per warp at a time; multi-leaf levels (rare) one candidate at a time.
       const bool qa = lane < G, qb = lane + 32 < G;
+      const int la = qa ? lane : 0, lb = qb ? lane + 32 : 0;
+      auto leaf_sum = [&](int64_t row, int q) {
+        float a = 0.f;
+#pragma unroll 1
+        for (int i = 0; i < leaves; ++i) a += t[row + i * TS + q];
+        return a;
+      };
       float m0 = -INFINITY, m1 = -INFINITY;
-      for (int ci0 = warp * 4; ci0 < n_cand; ci0 += kWarps * 4) {
-        float za[4], zb[4];
+      if (leaves == 1) {
+        for (int ci0 = warp * 4; ci0 < n_cand; ci0 += kWarps * 4) {
+          int64_t rows[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int ci = min(ci0 + u, n_cand - 1);
-          const int64_t row = static_cast<int64_t>(cr[ci]) * TS;
-          float a = tq0[row], b = tq1[row];
-          for (int i = 1; i < leaves; ++i) {
-            a += tq0[row + i * TS];
-            b += tq1[row + i * TS];
+          for (int u = 0; u < 4; ++u) rows[u] = static_cast<int64_t>(cr[min(ci0 + u, n_cand - 1)]) * TS;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const bool ok = ci0 + u < n_cand;
+            m0 = fmaxf(m0, ok && qa ? t[rows[u] + la] * sc2 : -INFINITY);
+            m1 = fmaxf(m1, ok && qb ? t[rows[u] + lb] * sc2 : -INFINITY);
           }
-          const bool ok = ci0 + u < n_cand;
-          za[u] = ok && qa ? a * sc2 : -INFINITY;
-          zb[u] = ok && qb ? b * sc2 : -INFINITY;
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          m0 = fmaxf(m0, za[u]);
-          m1 = fmaxf(m1, zb[u]);
+      } else {
+#pragma unroll 1
+        for (int ci = warp; ci < n_cand; ci += kWarps) {
+          const int64_t row = static_cast<int64_t>(cr[ci]) * TS;
+          if (qa) m0 = fmaxf(m0, leaf_sum(row, la) * sc2);
+          if (qb) m1 = fmaxf(m1, leaf_sum(row, lb) * sc2);
         }
       }
       part_m[warp * kMaxQ + lane] = m0;
@@ -605,30 +612,32 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       {
         const float lma = qa ? loc_m[lane] : 0.f;
         const float lmb = qb ? loc_m[lane + 32] : 0.f;
-        for (int ci0 = warp * 4; ci0 < n_cand; ci0 += kWarps * 4) {
-          float ea[4], eb[4];
-          int64_t rows[4];
+        if (leaves == 1) {  // level 0: e replaces t
+          for (int ci0 = warp * 4; ci0 < n_cand; ci0 += kWarps * 4) {
+            int64_t rows[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int ci = min(ci0 + u, n_cand - 1);
-            rows[u] = static_cast<int64_t>(cr[ci]) * TS;
-            float a = tq0[rows[u]], b = tq1[rows[u]];
-            for (int i = 1; i < leaves; ++i) {
-              a += tq0[rows[u] + i * TS];
-              b += tq1[rows[u] + i * TS];
+            for (int u = 0; u < 4; ++u) rows[u] = static_cast<int64_t>(cr[min(ci0 + u, n_cand - 1)]) * TS;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if (ci0 + u >= n_cand) continue;
+              if (qa) {
+                const float e = exp2f(t[rows[u] + la] * sc2 - lma);
+                e0 += e;
+                if (j == 0) t[rows[u] + la] = e;
+              }
+              if (qb) {
+                const float e = exp2f(t[rows[u] + lb] * sc2 - lmb);
+                e1 += e;
+                if (j == 0) t[rows[u] + lb] = e;
+              }
             }
-            const bool ok = ci0 + u < n_cand;
-            ea[u] = ok && qa ? exp2f(a * sc2 - lma) : 0.f;
-            eb[u] = ok && qb ? exp2f(b * sc2 - lmb) : 0.f;
           }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            e0 += ea[u];
-            e1 += eb[u];
-            if (j == 0 && ci0 + u < n_cand) {  // level 0: e replaces t
-              if (qa) t[rows[u] + lane] = ea[u];
-              if (qb) t[rows[u] + lane + 32] = eb[u];
-            }
+        } else {
+#pragma unroll 1
+          for (int ci = warp; ci < n_cand; ci += kWarps) {
+            const int64_t row = static_cast<int64_t>(cr[ci]) * TS;
+            if (qa) e0 += exp2f(leaf_sum(row, la) * sc2 - lma);
+            if (qb) e1 += exp2f(leaf_sum(row, lb) * sc2 - lmb);
           }
         }
       }
@@ -647,26 +656,20 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       __syncthreads();
       // Pass 3: one thread per candidate (odd row pitch: conflict-free).
       for (int ci = tid; ci < n_cand; ci += kThreads) {
-        float sa = 0.f, sb = 0.f, sc = 0.f, sd = 0.f;
-        if (j == 0) {
-          const float* ep = t + static_cast<int64_t>(cr[ci]) * TS;
-          int q = 0;
-          for (; q + 4 <= G; q += 4) {
-            sa += ep[q] * wq[q];
-            sb += ep[q + 1] * wq[q + 1];
-            sc += ep[q + 2] * wq[q + 2];
-            sd += ep[q + 3] * wq[q + 3];
+        const int64_t row = static_cast<int64_t>(cr[ci]) * TS;
+        float sa = 0.f, sb = 0.f;
+        if (j == 0) {  // t holds e
+#pragma unroll 4
+          for (int q = 0; q + 1 < G; q += 2) {
+            sa += t[row + q] * wq[q];
+            sb += t[row + q + 1] * wq[q + 1];
           }
-          for (; q < G; ++q) sa += ep[q] * wq[q];
+          if (G & 1) sa += t[row + G - 1] * wq[G - 1];
         } else {
-          const float* tp = t + static_cast<int64_t>(cr[ci]) * TS;
-          for (int q = 0; q < G; ++q) {
-            float z = 0.f;
-            for (int i = 0; i < leaves; ++i) z += tp[i * TS + q];
-            sa += exp2f(z * sc2 - loc_m[q]) * wq[q];
-          }
+#pragma unroll 1
+          for (int q = 0; q < G; ++q) sa += exp2f(leaf_sum(row, q) * sc2 - loc_m[q]) * wq[q];
         }
-        keys[ci] = __float_as_uint((sa + sb) + (sc + sd));
+        keys[ci] = __float_as_uint(sa + sb);
       }
       __syncthreads();
       if (final_gather) {
@@ -688,11 +691,19 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         const int a0 = key_slot_start(rank, cs, p.n_keys), a1 = key_slot_start(rank + 1, cs, p.n_keys);
         const int w0 = key_slot_start(rank, cs, B), w1 = key_slot_start(rank + 1, cs, B);
         const bool attend = (p.mode & kModeAttend) != 0;
-        block_select_topk(keys_all, n_all, B, tk, [&](int v, int slot) {
-          const int pos = pos_all[v];
-          if (attend && slot >= a0 && slot < a1) klist[slot - a0] = pos;
-          if (p.idx_out != nullptr && slot >= w0 && slot < w1) p.idx_out[unit * B + slot] = pos;
-        });
+        // This CTA's slots of the key list: [a0, min(a1, B)).  klist first
+        // receives candidate indices, then their token positions.
+        const int b1 = min(a1, B);
+        block_select_topk(keys_all, n_all, B, a0, b1, klist, tk);
+        for (int sl = a0 + tid; sl < b1; sl += kThreads) {
+          const int pos = pos_all[klist[sl - a0]];
+          klist[sl - a0] = pos;
+          if (p.idx_out != nullptr) p.idx_out[unit * B + sl] = pos;
+        }
+        __syncthreads();
+        (void)attend;
+        (void)w0;
+        (void)w1;
         global_done = true;
         break;
       }
