@@ -37,6 +37,8 @@ struct PathPlan {
   int gather_all;    // Top-K variant
   int klist_cap;     // attend: key slots per CTA (capacity)
   int tile_keys;     // attend: keys per staged tile
+  int f_stages;      // filter: cp.async ring depth
+  int a_stages;      // attend: cp.async ring depth
   bool t_in_smem;    // token logits in shared memory (else workspace)
   size_t smem_bytes; // dynamic shared memory per CTA
   size_t t_bytes;    // workspace bytes for token logits (0 if in shared memory)

@@ -69,6 +69,7 @@ struct PathParams {
   int mode;
   int n_prompt, G, levels, P, kL, budget, n_keys;
   int cs, per_cta_p, rows_cap, sorted_cap, keys_cap, gather_all, klist_cap, tile_keys;
+  int f_stages, a_stages;  // cp.async ring depths (filter tiles, attention tiles)
   int k[WF_MAX_LEVELS + 1];
   float scale[WF_MAX_LEVELS + 1];  // 2^(-j/2)/sqrt(d)
   float inv_sqrt_d, scale_log2;
@@ -128,7 +129,7 @@ struct PathSmem {
     }
     if (p.mode & kModeFilter) {
       o = u;
-      f_kst = take_bytes(static_cast<size_t>(2) * kTileRows * kRowBytes);
+      f_kst = take_bytes(static_cast<size_t>(p.f_stages) * kTileRows * kRowBytes);
       sp = take_bytes(sizeof(int32_t) * p.rows_cap);  // survivor / candidate lists
       sr = take_bytes(sizeof(int32_t) * p.rows_cap);
       cp = take_bytes(sizeof(int32_t) * p.rows_cap);
@@ -140,7 +141,7 @@ struct PathSmem {
     }
     if (p.mode & kModeAttend) {
       o = u;
-      const size_t stage = static_cast<size_t>(2) * p.tile_keys * kRowBytes;
+      const size_t stage = static_cast<size_t>(p.a_stages) * p.tile_keys * kRowBytes;
       if (sizeof(T) == 2) {  // warp partials overwrite the stages after the last tile
         const size_t work = sizeof(float) * (kWarps * 16 * D + 2 * kWarps * 16);
         a_kst = o;
@@ -182,58 +183,59 @@ __device__ __forceinline__ TopkResult cluster_select(const uint32_t* keys, int n
   return topk_distributed(keys, n, k, take, tk);
 }
 
-// ------------------------------------------------------------------ logits tiles
-// bf16: out[r][i] = scale * Σ_planes rows[r]·Q[i] for the 64 staged rows
-// (out row pitch `pitch` floats).  `nplanes` bf16 row tiles of 64 rows each,
-// `plane_bytes` apart, are accumulated (one plane for key rows; three planes
-// hi + mid + lo reproduce an fp32 row exactly).  Warp w: 16-row block (w & 3),
-// n-blocks (w >> 2) + 2i of 8 queries each.
+// ------------------------------------------------------------------ logits GEMM
+// bf16: out[r][i] = scale * Σ_planes rows[r]·Q[i] for r < n_rows (out row
+// pitch `pitch` floats).  `nplanes` bf16 row blocks `plane_bytes` apart are
+// accumulated (one plane for key rows; three planes hi + mid + lo reproduce an
+// fp32 row exactly).  Each warp owns whole 16-row m-blocks and keeps one
+// accumulator per 8-query n-block, so the MMA chains of a warp are independent.
 template <int D>
 __device__ __noinline__ void logits_tile_bf16(const unsigned char* rows, int nplanes,
                                               int plane_bytes, const unsigned char* qs,
-                                              float* out, int row0, int rows_valid, int G,
+                                              float* out, int row0, int n_rows, int G,
                                               int pitch, float scale) {
   constexpr int RB = D * 2 + 16;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int mb = warp & 3, ng = warp >> 2;
   const int NB = (G + 7) >> 3;
-  float acc[4][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
   const uint32_t qbase = smem_u32(qs) + (lane & 7) * RB + ((lane >> 3) & 1) * 16;
-  for (int pl = 0; pl < nplanes; ++pl) {
-    const uint32_t abase =
-        smem_u32(rows + pl * plane_bytes) + (mb * 16 + (lane & 15)) * RB + (lane >> 4) * 16;
-#pragma unroll 2
-    for (int ks = 0; ks < D / 16; ++ks) {
-      uint32_t a[4];
-      ldsm_x4(abase + ks * 32, a);
+  const int nmb = (n_rows + 15) >> 4;
+  for (int mb = warp; mb < nmb; mb += kWarps) {
+    float acc[8][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int nb = ng + 2 * i;
-        if (nb < NB) {  // Q B-fragment: 8 queries x 16 dims
-          uint32_t b[2];
-          ldsm_x2(qbase + nb * 8 * RB + ks * 32, b);
-          mma_bf16(acc[i], a, b);
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
+#pragma unroll 1
+    for (int pl = 0; pl < nplanes; ++pl) {
+      const uint32_t abase =
+          smem_u32(rows + pl * plane_bytes) + (mb * 16 + (lane & 15)) * RB + (lane >> 4) * 16;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(abase + ks * 32, a);
+#pragma unroll
+        for (int nb = 0; nb < 8; ++nb) {
+          if (nb < NB) {
+            uint32_t b[2];
+            ldsm_x2(qbase + nb * 8 * RB + ks * 32, b);
+            mma_bf16(acc[nb], a, b);
+          }
         }
       }
     }
-  }
-  const int r_lo = mb * 16 + (lane >> 2);
+    const int r_lo = mb * 16 + (lane >> 2);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int nb = ng + 2 * i;
-    if (nb >= NB) continue;
-    const int q0 = nb * 8 + (lane & 3) * 2;
+    for (int nb = 0; nb < 8; ++nb) {
+      if (nb >= NB) continue;
+      const int q0 = nb * 8 + (lane & 3) * 2;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = r_lo + 8 * h;
-      if (r >= rows_valid) continue;
-      float* dst = out + static_cast<int64_t>(row0 + r) * pitch;
-      if (q0 < G) dst[q0] = acc[i][2 * h] * scale;
-      if (q0 + 1 < G) dst[q0 + 1] = acc[i][2 * h + 1] * scale;
+      for (int h = 0; h < 2; ++h) {
+        const int r = r_lo + 8 * h;
+        if (r >= n_rows) continue;
+        float* dst = out + static_cast<int64_t>(row0 + r) * pitch;
+        if (q0 < G) dst[q0] = acc[nb][2 * h] * scale;
+        if (q0 + 1 < G) dst[q0 + 1] = acc[nb][2 * h + 1] * scale;
+      }
     }
   }
 }
@@ -292,6 +294,21 @@ __device__ __forceinline__ void online_update(float& m, float& l, float z) {
     m = z;
   } else {
     l += exp2f(z - m);
+  }
+}
+
+// Waits until at most `pending` of this thread's most recent cp.async groups
+// are still in flight (0 <= pending < 8).
+__device__ __forceinline__ void cp_async_wait_pending(int pending) {
+  switch (pending) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    default: cp_async_wait<7>(); break;
   }
 }
 
@@ -517,11 +534,19 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       }
       cp_async_commit();
     };
-    if (ntiles > 0) issue(0, 0);
-    if (ntiles > 1) issue(1, 1);
+    const int FS = p.f_stages;
+    for (int tl = 0; tl < FS && tl < ntiles; ++tl) issue(tl, tl);
+    if (ntiles <= FS && sizeof(T) == 2) {
+      // Every tile is in flight: one wait, then one GEMM over all R rows
+      // (tiles sit back to back in the ring).
+      cp_async_wait<0>();
+      __syncthreads();
+      logits_tile_bf16<D>(kst, 1, 0, qs, t, 0, R, G, TS, 1.f);
+      __syncthreads();
+    } else
     for (int tile = 0; tile < ntiles; ++tile) {
-      const int stage = tile & 1;
-      if (tile + 1 < ntiles) cp_async_wait<1>(); else cp_async_wait<0>();
+      const int stage = tile % FS;
+      cp_async_wait_pending(min(ntiles, tile + FS) - 1 - tile);
       __syncthreads();
       const unsigned char* buf = kst + stage * kTileRows * RB;
       const int rows_valid = min(kTileRows, R - tile * kTileRows);
@@ -532,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
                            rows_valid, G, TS, 1.f);
       }
       __syncthreads();
-      if (tile + 2 < ntiles) issue(tile + 2, stage);
+      if (tile + FS < ntiles) issue(tile + FS, stage);
     }
     __syncthreads();
 
@@ -781,8 +806,8 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       cp_async_commit();
     };
     __syncthreads();  // filter-phase readers of the union are done
-    if (ntiles > 0) issue(0, 0);
-    if (ntiles > 1) issue(1, 1);
+    const int AS = p.a_stages;
+    for (int tl = 0; tl < AS && tl < ntiles; ++tl) issue(tl, tl);
     auto valid = [&](int g) -> bool {
       if (g >= k1) return false;
       if (g >= B) return true;
@@ -805,8 +830,8 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         for (int e = 0; e < 4; ++e) oacc[i][e] = 0.f;
       float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
       for (int tile = 0; tile < ntiles; ++tile) {
-        const int stage = tile & 1;
-        if (tile + 1 < ntiles) cp_async_wait<1>(); else cp_async_wait<0>();
+        const int stage = tile % AS;
+        cp_async_wait_pending(min(ntiles, tile + AS) - 1 - tile);
         __syncthreads();
         const uint32_t kb = smem_u32(kst + (stage * TK + kgrp * 16) * RB);
         const uint32_t vb = smem_u32(vst + (stage * TK + kgrp * 16) * RB);
@@ -879,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           mma_bf16(oacc[dn + 1], pa, b + 2);
         }
         __syncthreads();
-        if (tile + 2 < ntiles) issue(tile + 2, stage);
+        if (tile + AS < ntiles) issue(tile + AS, stage);
       }
       // Warp partials -> shared memory (overwrites the stages).
       float* opart = work;                    // [kWarps][16][D]
@@ -949,8 +974,8 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       }
       __syncthreads();
       for (int tile = 0; tile < ntiles; ++tile) {
-        const int stage = tile & 1;
-        if (tile + 1 < ntiles) cp_async_wait<1>(); else cp_async_wait<0>();
+        const int stage = tile % AS;
+        cp_async_wait_pending(min(ntiles, tile + AS) - 1 - tile);
         __syncthreads();
         const float* kb = reinterpret_cast<const float*>(kst + stage * TK * RB);
         const float* vb = reinterpret_cast<const float*>(vst + stage * TK * RB);
@@ -1008,7 +1033,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           }
         }
         __syncthreads();
-        if (tile + 2 < ntiles) issue(tile + 2, stage);
+        if (tile + AS < ntiles) issue(tile + AS, stage);
       }
       cluster.sync();  // peers are past their filter phase (shared receive area)
       const int c4 = tid % C4, qg = tid / C4;
@@ -1144,8 +1169,16 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
     } else {
       p.tile_keys = 32;
     }
+    // cp.async ring depths: every tile in flight when it fits (at most 6).
+    const int f_tiles = (p.rows_cap + kTileRows - 1) / kTileRows;
+    const int a_tiles = ((p.n_keys + cs - 1) / cs + p.tile_keys - 1) / p.tile_keys;
+    const int f_want = std::max(2, std::min(6, f_tiles));
+    const int a_want = std::max(2, std::min(6, a_tiles));
     // Prefer the gather-all selection and token logits in shared memory.
+    for (int depth = 0; depth < 5 && !found; ++depth)
     for (int ga = 1; ga >= 0 && !found; --ga) {
+      p.f_stages = std::max(2, f_want - depth);
+      p.a_stages = std::max(2, a_want - depth);
       if (ga && (!(mode & kModeFilter) || static_cast<int64_t>(cs) * p.rows_cap > 8192)) continue;
       p.gather_all = ga;
       p.t_ws = nullptr;
@@ -1173,6 +1206,8 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
   plan->gather_all = p.gather_all;
   plan->klist_cap = p.klist_cap;
   plan->tile_keys = p.tile_keys;
+  plan->f_stages = p.f_stages;
+  plan->a_stages = p.a_stages;
   plan->mode = mode;
   return smem <= kMaxSmem;
 }
@@ -1211,6 +1246,8 @@ cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathAr
   p.gather_all = plan.gather_all;
   p.klist_cap = plan.klist_cap;
   p.tile_keys = plan.tile_keys;
+  p.f_stages = plan.f_stages;
+  p.a_stages = plan.a_stages;
   for (int j = 0; j <= ld.levels; ++j) {
     p.k[j] = a.k != nullptr ? a.k[j] : 0;
     p.scale[j] = static_cast<float>(std::pow(2.0, -0.5 * j) / std::sqrt(static_cast<double>(ld.head_dim)));
