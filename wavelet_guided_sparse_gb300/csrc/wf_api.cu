@@ -14,6 +14,8 @@
 #include "wavefilter.h"
 #include "wf_internal.h"
 
+#include <cuda_bf16.h>
+
 namespace {
 
 using wf::LaunchDims;
@@ -65,8 +67,9 @@ struct Layout {
 Layout layout(const LaunchDims& ld, const int32_t* k, const wf::PathPlan* fp) {
   Layout L;
   size_t o = kHeaderBytes;
-  L.al = o;
-  o = align_up(o + sizeof(float) * ld.units * (ld.n_prompt >> ld.levels) * ld.head_dim);
+  L.al = o;  // fp32 A_L, or for bf16 inputs three bf16 planes (6 bytes per element)
+  o = align_up(o + (ld.dtype == WF_BF16 ? 6 : 4) * static_cast<size_t>(ld.units) *
+                       (ld.n_prompt >> ld.levels) * ld.head_dim);
   L.idx_l = o;
   o = align_up(o + sizeof(int32_t) * ld.units * (k ? k[ld.levels] : 0));
   L.idx = o;
@@ -141,8 +144,8 @@ int wf_workspace_bytes(const wf_dims* dims, const int32_t* k_per_level, size_t* 
   if (st != WF_OK) return st;
   const int sms = wf::device_sm_count();
   wf::PathPlan all, filt;
-  if (!wf::plan_path(ld, wf::kPhaseAll, k_per_level, k_per_level[ld.levels], k_per_level[0], sms,
-                     &all) ||
+  if (!wf::plan_path(ld, wf::kPhaseAll | wf::kPhaseFuseDwt, k_per_level, k_per_level[ld.levels],
+                     k_per_level[0], sms, &all) ||
       !wf::plan_path(ld, wf::kPhaseFilter, k_per_level, k_per_level[ld.levels], k_per_level[0],
                      sms, &filt))
     return WF_ERR_UNSUPPORTED;
@@ -178,12 +181,12 @@ int wf_dwt_lowpass(const wf_dims* dims, const void* Kp, float* AL, float* A_all,
   if (Kp == nullptr || AL == nullptr) return WF_ERR_NULL;
   if (!aligned16(Kp) || !aligned16(AL) || (A_all && !aligned16(A_all))) return WF_ERR_ALIGNMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = wf::launch_dwt_lowpass(ld, Kp, AL, ld.levels, nullptr, s);
+  cudaError_t e = wf::launch_dwt_lowpass(ld, Kp, AL, nullptr, ld.levels, nullptr, s);
   if (e == cudaSuccess && A_all != nullptr) {
     // Test aid: every level j = 1..L, each from its own pass over Kp.
     size_t off = 0;
     for (int j = 1; j <= ld.levels && e == cudaSuccess; ++j) {
-      e = wf::launch_dwt_lowpass(ld, Kp, A_all + off, j, nullptr, s);
+      e = wf::launch_dwt_lowpass(ld, Kp, A_all + off, nullptr, j, nullptr, s);
       off += static_cast<size_t>(ld.units) * (ld.n_prompt >> j) * ld.head_dim;
     }
   }
@@ -299,23 +302,31 @@ int wf_step(const wf_dims* dims, const void* Q, const void* Kp, const void* Vp, 
   if (st != WF_OK) return st;
   const int budget = k_per_level[0];
   wf::PathPlan plan;
-  if (!wf::plan_path(ld, wf::kPhaseAll, k_per_level, k_per_level[ld.levels], budget,
-                     wf::device_sm_count(), &plan))
+  if (!wf::plan_path(ld, wf::kPhaseAll | wf::kPhaseFuseDwt, k_per_level, k_per_level[ld.levels],
+                     budget, wf::device_sm_count(), &plan))
     return WF_ERR_UNSUPPORTED;
   const Layout L = layout(ld, k_per_level, &plan);
   if (workspace_bytes < L.total) return WF_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   float* al = reinterpret_cast<float*>(ws + L.al);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = wf::launch_dwt_lowpass(ld, Kp, al, ld.levels, status_word(workspace), s);
-  if (e != cudaSuccess) return cuda_status(e);
+  // Step 1 runs inside the path kernel when the plan fuses it; otherwise a
+  // separate streaming launch writes A_L (bf16 inputs: straight to the three
+  // bf16 planes the score phase multiplies on tensor cores).
+  __nv_bfloat16* planes = ld.dtype == WF_BF16 ? reinterpret_cast<__nv_bfloat16*>(al) : nullptr;
+  if (!plan.fuse_dwt) {
+    const cudaError_t e =
+        wf::launch_dwt_lowpass(ld, Kp, al, planes, ld.levels, status_word(workspace), s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
   wf::PathArgs a = {};
   a.q = Q;
   a.kp = Kp;
   a.vp = Vp;
   a.kg = Kg;
   a.vg = Vg;
-  a.al = al;
+  a.al = planes != nullptr ? nullptr : al;
+  a.al_planes = planes;
   a.idx_out = idx_out;
   a.o = O;
   a.lse = lse;

@@ -11,7 +11,8 @@
 // contiguous byte range through a ring of three 64 KB shared-memory stages
 // filled by single bulk copies (TMA engine, mbarrier completion), so 128-192
 // KB per SM are in flight independent of register pressure.  Threads reduce
-// the staged rows in fp32: for spans of up to 16 rows one thread owns one
+// the staged rows in fp32 (and, for the fused step, emit A_L as the three
+// bf16 planes its tensor-core scoring consumes): for spans of up to 16 rows one thread owns one
 // (span, 16-byte column chunk) pair; longer spans are summed in 16-row blocks
 // whose partials are combined in a fixed order, with a running sum carried
 // across stages for spans longer than a stage.
@@ -50,13 +51,60 @@ __device__ __forceinline__ void add_chunk(const unsigned char* p, float* acc) {
   for (int i = 0; i < Elem<T>::kPer16B; ++i) acc[i] += f[i];
 }
 
+// Output of V channels of one A_L row: fp32 (`out`), or — when `planes` is
+// set — three bf16 planes hi + mid + lo whose sum reproduces the fp32 value
+// to 2^-25 relative, laid out [unit][plane][P][D] for tensor-core scoring.
+template <int V>
+__device__ __forceinline__ void store_al(const float* acc, float scale, float* out,
+                                         __nv_bfloat16* planes, int64_t span, int64_t P,
+                                         int D, int col) {
+  if (planes == nullptr) {
+    float4* o = reinterpret_cast<float4*>(out + span * D + col);
+#pragma unroll
+    for (int v = 0; v < V; v += 4)
+      o[v / 4] = make_float4(acc[v] * scale, acc[v + 1] * scale, acc[v + 2] * scale,
+                             acc[v + 3] * scale);
+    return;
+  }
+  const int64_t unit = span / P, row = span % P;
+  uint32_t w[3][V / 2];
+#pragma unroll
+  for (int v = 0; v < V; v += 2) {
+    float hv[2], mv[2], lv[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float a = acc[v + e] * scale;
+      hv[e] = __bfloat162float(__float2bfloat16_rn(a));
+      const float r1 = a - hv[e];
+      mv[e] = __bfloat162float(__float2bfloat16_rn(r1));
+      lv[e] = r1 - mv[e];
+    }
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(hv[0], hv[1]);
+    const __nv_bfloat162 m2 = __floats2bfloat162_rn(mv[0], mv[1]);
+    const __nv_bfloat162 l2 = __floats2bfloat162_rn(lv[0], lv[1]);
+    w[0][v / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+    w[1][v / 2] = *reinterpret_cast<const uint32_t*>(&m2);
+    w[2][v / 2] = *reinterpret_cast<const uint32_t*>(&l2);
+  }
+#pragma unroll
+  for (int pl = 0; pl < 3; ++pl) {
+    __nv_bfloat16* dst = planes + ((unit * 3 + pl) * P + row) * D + col;
+    if constexpr (V == 8) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(w[pl][0], w[pl][1], w[pl][2], w[pl][3]);
+    } else {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(w[pl][0], w[pl][1]);
+    }
+  }
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __restrict__ kp,
                                                                  float* __restrict__ out,
+                                                                 __nv_bfloat16* __restrict__ planes,
                                                                  int64_t n_spans,
                                                                  int64_t spans_per_cta,
-                                                                 int levels, float scale,
-                                                                 int32_t* status) {
+                                                                 int levels, int64_t P,
+                                                                 float scale, int32_t* status) {
   extern __shared__ __align__(128) unsigned char smem[];
   using S = DwtSmem<T, D>;
   constexpr int RB = S::kRowBytes, SR = S::kRows, V = S::V, C = S::C;
@@ -73,7 +121,6 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
   const int64_t rows_total = (s_end - s_begin) << levels;
   const int64_t n_stages = (rows_total + SR - 1) / SR;
   const unsigned char* src = reinterpret_cast<const unsigned char*>(kp + (s_begin << levels) * D);
-  float* dst = out + s_begin * D;
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) mbar_init(&bars[i], 1);
@@ -115,11 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
 #pragma unroll
         for (int r = 0; r < 16; ++r)
           if (r < span_rows) add_chunk<T>(p + r * RB, acc);
-        float4* o = reinterpret_cast<float4*>(dst + (span0 + sl) * D + c * V);
-#pragma unroll
-        for (int v = 0; v < V; v += 4)
-          o[v / 4] = make_float4(acc[v] * scale, acc[v + 1] * scale, acc[v + 2] * scale,
-                                 acc[v + 3] * scale);
+        store_al<V>(acc, scale, out, planes, s_begin + span0 + sl, P, D, c * V);
       }
     } else {
       // 16-row block partials, then per-span combination in block order.
@@ -152,11 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
 #pragma unroll
           for (int v = 0; v < V; ++v) acc[v] += part[(b * C + c) * V + v];
         if (((span + 1) << levels) <= first_row + rows_in) {
-          float4* o = reinterpret_cast<float4*>(dst + span * D + c * V);
-#pragma unroll
-          for (int v = 0; v < V; v += 4)
-            o[v / 4] = make_float4(acc[v] * scale, acc[v + 1] * scale, acc[v + 2] * scale,
-                                   acc[v + 3] * scale);
+          store_al<V>(acc, scale, out, planes, s_begin + span, P, D, c * V);
         } else {
 #pragma unroll
           for (int v = 0; v < V; ++v) carry[c * V + v] = acc[v];
@@ -172,8 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
 }
 
 template <typename T, int D>
-cudaError_t launch_typed(const void* kp, float* out, int64_t units, int n_prompt, int levels,
-                         int32_t* status, cudaStream_t stream) {
+cudaError_t launch_typed(const void* kp, float* out, __nv_bfloat16* planes, int64_t units,
+                         int n_prompt, int levels, int32_t* status, cudaStream_t stream) {
   const cudaError_t e = ensure_max_smem<dwt_stream_kernel<T, D>>();
   if (e != cudaSuccess) return e;
   const int64_t n_spans = units * (n_prompt >> levels);
@@ -182,24 +221,28 @@ cudaError_t launch_typed(const void* kp, float* out, int64_t units, int n_prompt
   const int64_t blocks = (n_spans + per - 1) / per;
   const float scale = static_cast<float>(std::pow(2.0, -0.5 * levels));  // 2^(-L/2)
   dwt_stream_kernel<T, D><<<static_cast<unsigned>(blocks), kThreads, DwtSmem<T, D>::kTotal,
-                            stream>>>(static_cast<const T*>(kp), out, n_spans, per, levels, scale,
+                            stream>>>(static_cast<const T*>(kp), out, planes, n_spans, per,
+                                      levels, static_cast<int64_t>(n_prompt >> levels), scale,
                                       status);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_dwt_lowpass(const LaunchDims& ld, const void* kp, float* out, int levels,
-                               int32_t* status, cudaStream_t stream) {
+cudaError_t launch_dwt_lowpass(const LaunchDims& ld, const void* kp, float* out,
+                               __nv_bfloat16* planes, int levels, int32_t* status,
+                               cudaStream_t stream) {
   if (ld.dtype == WF_BF16) {
     if (ld.head_dim == 128)
-      return launch_typed<__nv_bfloat16, 128>(kp, out, ld.units, ld.n_prompt, levels, status,
-                                              stream);
-    return launch_typed<__nv_bfloat16, 64>(kp, out, ld.units, ld.n_prompt, levels, status, stream);
+      return launch_typed<__nv_bfloat16, 128>(kp, out, planes, ld.units, ld.n_prompt, levels,
+                                              status, stream);
+    return launch_typed<__nv_bfloat16, 64>(kp, out, planes, ld.units, ld.n_prompt, levels,
+                                           status, stream);
   }
   if (ld.head_dim == 128)
-    return launch_typed<float, 128>(kp, out, ld.units, ld.n_prompt, levels, status, stream);
-  return launch_typed<float, 64>(kp, out, ld.units, ld.n_prompt, levels, status, stream);
+    return launch_typed<float, 128>(kp, out, planes, ld.units, ld.n_prompt, levels, status,
+                                    stream);
+  return launch_typed<float, 64>(kp, out, planes, ld.units, ld.n_prompt, levels, status, stream);
 }
 
 }  // namespace wf

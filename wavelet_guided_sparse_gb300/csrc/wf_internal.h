@@ -2,6 +2,7 @@
 // launchers (wf_dwt.cu: step 1; wf_path.cu: steps 2-5).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -24,11 +25,15 @@ struct LaunchDims {
 
 // Phases of the fused path kernel (wf_path.cu).
 enum : int { kPhaseScore = 1, kPhaseFilter = 2, kPhaseAttend = 4, kPhaseAll = 7 };
+// Request bit for plan_path with kPhaseAll: compute A_L inside the path
+// kernel (step 1 fused into the scoring) where the plan allows it.
+enum : int { kPhaseFuseDwt = 8 };
 
 // Launch plan of the path kernel; a pure function of the sizes and the
 // device's SM count.
 struct PathPlan {
-  int mode;          // kPhase* bit set
+  int mode;          // kPhase* bit set (without kPhaseFuseDwt)
+  int fuse_dwt;      // 1: the path kernel computes A_L itself (no separate DWT launch)
   int cluster;       // CTAs per unit
   int per_cta_p;     // score: coarse positions per CTA
   int rows_cap;      // filter: token rows per CTA (capacity)
@@ -48,6 +53,7 @@ struct PathPlan {
 struct PathArgs {
   const void *q, *kp, *vp, *kg, *vg;
   const float* al;
+  const __nv_bfloat16* al_planes;  // A_L as three bf16 planes (bf16 step), else null
   const int32_t* idx_l_in;
   const int32_t* idx_in;
   int32_t* idx_l_out;
@@ -66,8 +72,11 @@ int device_sm_count();
 bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int budget,
                int sm_count, PathPlan* plan);
 
-cudaError_t launch_dwt_lowpass(const LaunchDims& ld, const void* kp, float* out, int levels,
-                               int32_t* status, cudaStream_t stream);
+// Writes A_L as fp32 to `out`, or (planes != nullptr) as three bf16 planes
+// [unit][3][P][D] whose sum reproduces the fp32 values.
+cudaError_t launch_dwt_lowpass(const LaunchDims& ld, const void* kp, float* out,
+                               __nv_bfloat16* planes, int levels, int32_t* status,
+                               cudaStream_t stream);
 cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathArgs& args,
                         cudaStream_t stream);
 

@@ -45,6 +45,8 @@ namespace {
 
 constexpr int kTileRows = 64;    // filter: token rows per staged tile
 constexpr int kScoreChunk = 64;  // score: coarse positions per staged chunk
+constexpr int kFuseStages = 3;               // fused step 1: bulk-copy ring depth
+constexpr int kFuseStageBytes = 32 * 1024;   // fused step 1: bytes per ring stage
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -56,7 +58,8 @@ struct PathParams {
   const void* vp;
   const void* kg;
   const void* vg;
-  const float* al;           // score: A_L [U, P, d] fp32
+  const float* al;           // score: A_L [U, P, d] fp32 (null when al_planes is set)
+  const __nv_bfloat16* al_planes;  // score, bf16: A_L as hi/mid/lo planes [U, 3, P, d]
   const int32_t* idx_l_in;   // filter without score: S_L [U, k_L]
   const int32_t* idx_in;     // attend without filter: S [U, B]
   int32_t* idx_l_out;        // score without filter: S_L out [U, k_L]
@@ -70,6 +73,8 @@ struct PathParams {
   int n_prompt, G, levels, P, kL, budget, n_keys;
   int cs, per_cta_p, rows_cap, sorted_cap, keys_cap, gather_all, klist_cap, tile_keys;
   int f_stages, a_stages;  // cp.async ring depths (filter tiles, attention tiles)
+  int fuse_dwt;            // score: A_L from K_p inside this kernel
+  float al_scale;          // 2^(-L/2), the orthonormal Haar low-pass gain
   int k[WF_MAX_LEVELS + 1];
   float scale[WF_MAX_LEVELS + 1];  // 2^(-j/2)/sqrt(d)
   float inv_sqrt_d, scale_log2;
@@ -79,9 +84,9 @@ template <typename T, int D>
 struct PathSmem {
   static constexpr int kRowBytes = D * static_cast<int>(sizeof(T)) + 16;  // padded row pitch
   static constexpr int kRowF = D + 4;                                      // fp32 row pitch
-  size_t qs, stat_in, gm, loc, part, cnt_a, cnt_b, misc, sl_all, sp, sr, cp, cr, keys, take,
-      topk, keys_all, pos_all, klist;
-  size_t s_stage, s_as, s_z;       // score phase
+  size_t qs, stat_in, gm, loc, part, cnt_a, cnt_b, misc, bars, sl_all, sp, sr, cp, cr, keys,
+      take, topk, keys_all, pos_all, klist;
+  size_t s_stage, s_as, s_z, s_ring;  // score phase
   size_t f_kst, f_t;               // filter phase
   size_t a_kst, a_vst, a_work, a_recv, a_rml;  // attend phase
   size_t total;
@@ -101,6 +106,7 @@ struct PathSmem {
     cnt_a = take_bytes(sizeof(int32_t) * kMaxCluster);
     cnt_b = take_bytes(sizeof(int32_t) * kMaxCluster);
     misc = take_bytes(sizeof(int32_t) * 8);
+    bars = take_bytes(sizeof(uint64_t) * kFuseStages);
     sl_all = take_bytes(sizeof(int32_t) * p.sorted_cap);
     topk = take_bytes(sizeof(TopkSmem));
     // All-gathered keys: the P coarse scores, and (final level, gather mode)
@@ -112,7 +118,17 @@ struct PathSmem {
     klist = take_bytes(sizeof(int32_t) * p.klist_cap);
     const size_t u = o;
     size_t end = u;
-    if (p.mode & kModeScore) {
+    s_ring = 0;
+    if ((p.mode & kModeScore) && p.fuse_dwt) {
+      // Fused step 1: the bulk-copy ring of K_p rows, then A_L in the tile
+      // operand layout (bf16: hi / mid / lo planes; fp32: rows).  The logits
+      // overwrite the ring once every stage has been consumed.
+      o = u;
+      s_ring = take_bytes(static_cast<size_t>(kFuseStages) * kFuseStageBytes);
+      s_as = take_bytes((sizeof(T) == 2 ? 3 : 1) * kScoreChunk * kRowBytes);
+      s_stage = s_z = s_ring;
+      end = end > o ? end : o;
+    } else if (p.mode & kModeScore) {
       o = u;
       // A_L chunk: fp32 rows staged by cp.async, then (bf16 inputs) split into
       // three bf16 planes; fp32 inputs use the staged rows directly.
@@ -365,6 +381,32 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   int32_t* pos_all = reinterpret_cast<int32_t*>(smem + L.pos_all);
   int32_t* klist = reinterpret_cast<int32_t*>(smem + L.klist);
 
+  // Fused step 1: this CTA's K_p rows (the spans of its per_cta_p coarse
+  // positions, one contiguous byte range) stream through a ring of bulk
+  // copies; the first stages are in flight before anything else happens.
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  const int fuse_sr = kFuseStageBytes / (D * static_cast<int>(sizeof(T)));  // rows per stage
+  const int fuse_rows = p.fuse_dwt ? (p.per_cta_p << levels) : 0;
+  const int fuse_nst = (fuse_rows + fuse_sr - 1) / fuse_sr;
+  const unsigned char* fuse_src =
+      reinterpret_cast<const unsigned char*>(static_cast<const T*>(p.kp)) +
+      (unit * p.n_prompt + (static_cast<int64_t>(rank) * p.per_cta_p << levels)) * D *
+          static_cast<int64_t>(sizeof(T));
+  auto fuse_issue = [&](int st) {  // thread 0 only
+    const int rows = min(fuse_sr, fuse_rows - st * fuse_sr);
+    const uint32_t bytes = static_cast<uint32_t>(rows) * D * static_cast<uint32_t>(sizeof(T));
+    uint64_t* bar = &bars[st % kFuseStages];
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(smem + L.s_ring + (st % kFuseStages) * kFuseStageBytes,
+             fuse_src + static_cast<int64_t>(st) * kFuseStageBytes, bytes, bar);
+  };
+  int fuse_issued = min(kFuseStages, fuse_nst);
+  if (p.fuse_dwt && tid == 0) {
+    for (int i = 0; i < kFuseStages; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+    for (int st = 0; st < fuse_issued; ++st) fuse_issue(st);
+  }
+
   // Queries (input dtype, padded rows; rows >= G are zero).
   {
     const T* qsrc = static_cast<const T*>(p.q) + unit * G * D;
@@ -387,13 +429,111 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     unsigned char* as = smem + L.s_as;
     float* zc = reinterpret_cast<float*>(smem + L.s_z);  // [chunk row][query], log2 domain
     const float zscale = p.inv_sqrt_d * kLog2e;
-    const float* asrc = p.al + (unit * p.P + static_cast<int64_t>(rank) * Pc) * D;
+    const float* asrc =
+        p.al == nullptr ? nullptr : p.al + (unit * p.P + static_cast<int64_t>(rank) * Pc) * D;
     const int nchunks = (Pc + kScoreChunk - 1) / kScoreChunk;
     // z for chunk rows [c0, c0 + rows): stage A_L (bf16 inputs: exact
     // hi + mid + lo bf16 planes), then one tensor-core / FMA tile.
     float* stage_f = reinterpret_cast<float*>(smem + L.s_stage);  // [64][D + 4] fp32
-    auto chunk_logits = [&](int c0, int rows) {
+    const __nv_bfloat16* psrc =
+        p.al_planes == nullptr
+            ? nullptr
+            : p.al_planes + (static_cast<int64_t>(unit) * 3 * p.P + static_cast<int64_t>(rank) * Pc) * D;
+    bool z_ready = false;  // fused step 1 leaves the single chunk's logits in zc
+    if (p.fuse_dwt) {
+      // Step 1: A_L[c] = 2^(-L/2) * (sum of the 2^L rows of span c), fp32,
+      // one thread per (span, 16-byte column chunk) of a stage (a stage holds
+      // whole spans), written straight into the tile operand layout.
+      constexpr int V = Elem<T>::kPer16B, C = D / V;
+      const int span_rows = 1 << levels;
+      bool aborted = false;
+      for (int st = 0; st < fuse_issued; ++st) {
+        // Every issued stage is waited for (bounded), even after a timeout,
+        // so no copy is still landing when the ring is reused; a timeout
+        // only stops further issues (the status word reports it).
+        const bool ok = mbar_wait_bounded(&bars[st % kFuseStages],
+                                          static_cast<uint32_t>((st / kFuseStages) & 1), p.status);
+        if (__syncthreads_or(!ok)) aborted = true;
+        const unsigned char* buf = smem + L.s_ring + (st % kFuseStages) * kFuseStageBytes;
+        const int rows_in = min(fuse_sr, fuse_rows - st * fuse_sr);
+        const int span0 = (st * fuse_sr) >> levels;
+        for (int item = tid; item < (rows_in >> levels) * C; item += kThreads) {
+          const int sl = item / C, ch = item % C;
+          float acc[V];
+#pragma unroll
+          for (int v = 0; v < V; ++v) acc[v] = 0.f;
+          const unsigned char* src = buf + static_cast<size_t>(sl << levels) * D * sizeof(T) + ch * 16;
+#pragma unroll 8
+          for (int r = 0; r < span_rows; ++r) {
+            float f[V];
+            widen16(*reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * D * sizeof(T)),
+                    static_cast<const T*>(nullptr), f);
+#pragma unroll
+            for (int v = 0; v < V; ++v) acc[v] += f[v];
+          }
+          const int row = span0 + sl;
+          if constexpr (sizeof(T) == 2) {
+            uint32_t w[3][V / 2];
+#pragma unroll
+            for (int v = 0; v < V; v += 2) {
+              float hv[2], mv[2], lv[2];
+#pragma unroll
+              for (int e2 = 0; e2 < 2; ++e2) {  // a = hi + mid + lo exactly (to 2^-25 relative)
+                const float a = acc[v + e2] * p.al_scale;
+                hv[e2] = __bfloat162float(__float2bfloat16_rn(a));
+                const float r1 = a - hv[e2];
+                mv[e2] = __bfloat162float(__float2bfloat16_rn(r1));
+                lv[e2] = r1 - mv[e2];
+              }
+              w[0][v / 2] = pack_bf16(hv[0], hv[1]);
+              w[1][v / 2] = pack_bf16(mv[0], mv[1]);
+              w[2][v / 2] = pack_bf16(lv[0], lv[1]);
+            }
+#pragma unroll
+            for (int pl = 0; pl < 3; ++pl)
+              *reinterpret_cast<uint4*>(as + pl * kScoreChunk * RB + row * RB + ch * 16) =
+                  make_uint4(w[pl][0], w[pl][1], w[pl][2], w[pl][3]);
+          } else {
+            *reinterpret_cast<float4*>(as + row * RB + ch * 16) =
+                make_float4(acc[0] * p.al_scale, acc[1] * p.al_scale, acc[2] * p.al_scale,
+                            acc[3] * p.al_scale);
+          }
+        }
+        __syncthreads();  // stage consumed
+        if (!aborted && st + kFuseStages < fuse_nst) {
+          if (tid == 0) {
+            fence_proxy_async();
+            fuse_issue(st + kFuseStages);
+          }
+          ++fuse_issued;
+        }
+      }
+      if (sizeof(T) == 2)
+        logits_tile_bf16<D>(as, 3, kScoreChunk * RB, qs, zc, 0, Pc, G, TS, zscale);
+      else
+        logits_tile_f32<D>(as, reinterpret_cast<const float*>(qs), zc, 0, Pc, G, TS, zscale);
       __syncthreads();
+      z_ready = true;
+    }
+    auto chunk_logits = [&](int c0, int rows) {
+      if (z_ready) return;
+      __syncthreads();
+      if (sizeof(T) == 2 && psrc != nullptr) {
+        // A_L already split into hi / mid / lo bf16 planes: stage them directly.
+        constexpr int C8 = D / 8;
+        for (int e = tid; e < 3 * rows * C8; e += kThreads) {
+          const int pl = e / (rows * C8), rem = e - pl * rows * C8;
+          const int r = rem / C8, col = (rem % C8) * 8;
+          cp_async16(as + pl * kScoreChunk * RB + r * RB + col * 2,
+                     psrc + (static_cast<int64_t>(pl) * p.P + c0 + r) * D + col);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
+        logits_tile_bf16<D>(as, 3, kScoreChunk * RB, qs, zc, 0, rows, G, TS, zscale);
+        __syncthreads();
+        return;
+      }
       for (int e = tid; e < rows * (D / 4); e += kThreads) {
         const int r = e / (D / 4), col = (e % (D / 4)) * 4;
         cp_async16(stage_f + r * RF + col, asrc + static_cast<int64_t>(c0 + r) * D + col);
@@ -434,9 +574,25 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     for (int ch = 0; ch < nchunks; ++ch) {
       const int c0 = ch * kScoreChunk, rows = min(kScoreChunk, Pc - c0);
       chunk_logits(c0, rows);
+      // This chunk's maximum first, then one exp2 per logit.
+      const int q0 = lane < G ? lane : 0, q1 = lane + 32 < G ? lane + 32 : 0;
+      float c_m0 = m0, c_m1 = m1;
       for (int r = warp; r < rows; r += kWarps) {
-        if (lane < G) online_update(m0, l0, zc[r * TS + lane]);
-        if (lane + 32 < G) online_update(m1, l1, zc[r * TS + lane + 32]);
+        c_m0 = fmaxf(c_m0, zc[r * TS + q0]);
+        c_m1 = fmaxf(c_m1, zc[r * TS + q1]);
+      }
+      float s0 = 0.f, s1 = 0.f;
+      for (int r = warp; r < rows; r += kWarps) {
+        s0 += exp2f(zc[r * TS + q0] - c_m0);
+        s1 += exp2f(zc[r * TS + q1] - c_m1);
+      }
+      if (lane < G && c_m0 != -INFINITY) {
+        l0 = l0 * exp2f(m0 - c_m0) + s0;
+        m0 = c_m0;
+      }
+      if (lane + 32 < G && c_m1 != -INFINITY) {
+        l1 = l1 * exp2f(m1 - c_m1) + s1;
+        m1 = c_m1;
       }
     }
     part_m[warp * kMaxQ + lane] = m0;
@@ -1128,6 +1284,8 @@ int device_sm_count() {
 bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int budget,
                int sm_count, PathPlan* plan) {
   PathParams p = {};
+  const bool want_fuse = mode == (kPhaseAll | kPhaseFuseDwt);
+  mode &= kPhaseAll;
   p.mode = mode;
   p.G = ld.n_gen;
   p.levels = ld.levels;
@@ -1174,13 +1332,20 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
     const int a_tiles = ((p.n_keys + cs - 1) / cs + p.tile_keys - 1) / p.tile_keys;
     const int f_want = std::max(2, std::min(6, f_tiles));
     const int a_want = std::max(2, std::min(6, a_tiles));
-    // Prefer the gather-all selection and token logits in shared memory.
+    // Fused step 1 needs one score chunk per CTA and whole spans per stage.
+    const int elem = ld.dtype == WF_BF16 ? 2 : 4;
+    const bool fuse_try = want_fuse && p.per_cta_p <= kScoreChunk &&
+                          (static_cast<int64_t>(elem) * ld.head_dim << ld.levels) <= kFuseStageBytes;
+    // Prefer the fused step 1, the gather-all selection and token logits in
+    // shared memory, in that order.
+    for (int fz = fuse_try ? 1 : 0; fz >= 0 && !found; --fz)
     for (int depth = 0; depth < 5 && !found; ++depth)
     for (int ga = 1; ga >= 0 && !found; --ga) {
       p.f_stages = std::max(2, f_want - depth);
       p.a_stages = std::max(2, a_want - depth);
       if (ga && (!(mode & kModeFilter) || static_cast<int64_t>(cs) * p.rows_cap > 8192)) continue;
       p.gather_all = ga;
+      p.fuse_dwt = fz;
       p.t_ws = nullptr;
       smem = smem_bytes(ld, p);
       t_in_smem = true;
@@ -1189,7 +1354,7 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
         smem = smem_bytes(ld, p);
         t_in_smem = false;
       }
-      found = smem <= kMaxSmem;
+      found = smem <= kMaxSmem && (t_in_smem || !fz);  // never fuse at the cost of spilling
     }
     if (found || cs * 2 > kMaxCluster || !cluster_ok(cs * 2)) break;
   }
@@ -1208,6 +1373,7 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
   plan->tile_keys = p.tile_keys;
   plan->f_stages = p.f_stages;
   plan->a_stages = p.a_stages;
+  plan->fuse_dwt = p.fuse_dwt;
   plan->mode = mode;
   return smem <= kMaxSmem;
 }
@@ -1221,6 +1387,7 @@ cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathAr
   p.kg = a.kg;
   p.vg = a.vg;
   p.al = a.al;
+  p.al_planes = a.al_planes;
   p.idx_l_in = a.idx_l_in;
   p.idx_in = a.idx_in;
   p.idx_l_out = a.idx_l_out;
@@ -1248,6 +1415,8 @@ cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathAr
   p.tile_keys = plan.tile_keys;
   p.f_stages = plan.f_stages;
   p.a_stages = plan.a_stages;
+  p.fuse_dwt = plan.fuse_dwt;
+  p.al_scale = static_cast<float>(std::pow(2.0, -0.5 * ld.levels));  // 2^(-L/2)
   for (int j = 0; j <= ld.levels; ++j) {
     p.k[j] = a.k != nullptr ? a.k[j] : 0;
     p.scale[j] = static_cast<float>(std::pow(2.0, -0.5 * j) / std::sqrt(static_cast<double>(ld.head_dim)));
