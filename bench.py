@@ -41,7 +41,13 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one dwt_lowpass launch on the default workload,
 # from an ncu capture of the kernel source with this SHA-256 prefix; null
 # once the kernel has changed since the counters were taken.
-DWT_TRAFFIC = {"source_sha": "24a89596d1f42558", "bytes_per_launch": 33571840}  # 33.57 MB read + 0 B written
+# dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture
+# of the 4096-token layer (profiles/), valid while the kernel sources hash to
+# source_sha.
+DWT_TRAFFIC = {"sources": ("wf_dwt.cu",), "source_sha": "24a89596d1f42558",
+               "bytes_per_launch": 33571840}  # 33.57 MB read + 0 B written
+PATH_TRAFFIC = {"sources": ("wf_path.cu", "wf_common.cuh", "wf_mma.cuh"), "source_sha": None,
+                "bytes_per_launch": None}
 
 
 def _rank_env():
@@ -96,15 +102,30 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def _dwt_traffic():
-    src = os.path.join(ROOT, "wavelet_guided_sparse_gb300", "csrc", "wf_dwt.cu")
+def step_bytes(cfg, fused: bool) -> int:
+    """Algorithmic HBM bytes of one wf_step; the fused step never writes or
+    reads A_L in global memory."""
+    total = sum(path_bytes(cfg).values())
+    if fused:
+        total -= 2 * cfg.units_per_layer * (cfg.n_prompt >> cfg.levels) * cfg.head_dim * 4
+    return total
+
+
+def _source_sha(names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "wavelet_guided_sparse_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(table):
+    """ncu DRAM bytes per launch, if the kernel sources are the profiled ones."""
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        sha = _source_sha(table["sources"])
     except OSError:
         return None
-    if DWT_TRAFFIC["source_sha"] == sha:
-        return DWT_TRAFFIC["bytes_per_launch"]
-    return None
+    return table["bytes_per_launch"] if table["source_sha"] == sha else None
 
 
 class ClockSampler:
@@ -271,6 +292,7 @@ def run_ours(args, cfg):
     copies = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(n_copies - 1)]
     dims = bd.make_dims(base["Q"], base["Kp"], cfg.levels)
     ws = bd.alloc_workspace(dims, ks, dev)
+    launches = bd.step_launch_count(dims, ks)
     out = torch.empty(base["Q"].shape, dtype=torch.float32, device=dev)
     lse = torch.empty(base["Q"].shape[:3], dtype=torch.float32, device=dev)
     idx = torch.empty((cfg.batch, cfg.heads, ks[0]), dtype=torch.int32, device=dev)
@@ -282,6 +304,10 @@ def run_ours(args, cfg):
     for c in copies:  # eager pass (sets kernel attributes before capture)
         step(c)
     torch.cuda.synchronize()
+    # One graph per input copy (one step each) and one graph that runs a step
+    # on every copy in turn: the timed loop replays the latter, so that graph
+    # launch latency is paid once per n_copies steps, as it would be for a
+    # model's layers captured together.
     graphs = []
     cap_stream = torch.cuda.Stream(device=dev)
     for c in copies:
@@ -289,6 +315,10 @@ def run_ours(args, cfg):
         with torch.cuda.graph(g, stream=cap_stream):
             step(c)
         graphs.append(g)
+    cycle = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(cycle, stream=cap_stream):
+        for c in copies:
+            step(c)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)
 
@@ -306,8 +336,10 @@ def run_ours(args, cfg):
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for i in range(args.steps):
-        graphs[i % n_copies].replay()
+    for _ in range(args.steps // n_copies):
+        cycle.replay()
+    for i in range(args.steps % n_copies):
+        graphs[i].replay()
     ev1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -352,7 +384,7 @@ def run_ours(args, cfg):
         for j, name in enumerate(("dwt", "score", "filter", "attn")):
             stage_ms[name].append(e[j].elapsed_time(e[j + 1]))
     stage_us = {k: 1e3 * statistics.mean(v) for k, v in stage_ms.items()}
-    # The dominant kernel's average duration: back-to-back launches (rotating
+    # The standalone DWT entry point: average duration over back-to-back launches (rotating
     # input copies, as in the timed region) between one event pair.
     d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n_dwt = max(args.steps, 20)
@@ -396,9 +428,29 @@ def run_ours(args, cfg):
         dist.barrier()
         return 0
     peak, peak_kind = _peaks()
+    peak_source = (f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                   else "fallback 6.8 TB/s")
     dwt_bytes = touched["dwt"]
-    achieved = dwt_bytes / (dwt_us * 1e-6) / 1e9
-    total_bytes = sum(touched.values())
+    dwt_achieved = dwt_bytes / (dwt_us * 1e-6) / 1e9
+    fused = launches == 1
+    total_bytes = step_bytes(cfg, fused)
+    dwt_roofline = {"kernel": "dwt_stream_kernel (wf_dwt_lowpass, fp32 A_L)", "bound": "hbm",
+                    "achieved": dwt_achieved, "peak": peak, "unit": "GB/s",
+                    "frac": dwt_achieved / peak, "peak_source": peak_source,
+                    "traffic": _traffic(DWT_TRAFFIC), "algorithmic_bytes_per_launch": dwt_bytes,
+                    "launch_us": dwt_us,
+                    "timing": f"{n_dwt} back-to-back launches, rotating input copies"}
+    if fused:
+        # One kernel per step: its average duration is the timed region / K.
+        step_ach = total_bytes / (ms_per_step * 1e-3) / 1e9
+        roofline = {"kernel": "path_kernel (whole step: Haar low-pass, scoring, filter, gather,"
+                              " attention)", "bound": "hbm", "achieved": step_ach, "peak": peak,
+                    "unit": "GB/s", "frac": step_ach / peak, "peak_source": peak_source,
+                    "traffic": _traffic(PATH_TRAFFIC), "algorithmic_bytes_per_launch": total_bytes,
+                    "launch_us": ms_per_step * 1e3,
+                    "timing": "CUDA events over the timed region / K (one launch per step)"}
+    else:
+        roofline = dwt_roofline
     cpu_rate, cpu_units, cpu_s = (None, 0, 0.0)
     workers = os.cpu_count() or 1
     if world == 1 and not args.no_cpu_baseline:
@@ -412,20 +464,14 @@ def run_ours(args, cfg):
             "l2": f"rotating {n_copies} device input copies ({n_copies * per_copy / 2**20:.0f} MiB,"
                   f" {n_copies} x {touched_bytes / 2**20:.1f} MiB touched per step > "
                   f"{l2 / 2**20:.0f} MiB L2)",
-            "timing": "CUDA events around K replays of one CUDA graph (wf_step) per copy"}),
-        "roofline": {"kernel": "dwt_stream_kernel", "bound": "hbm",
-                     "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                     if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "traffic": _dwt_traffic(),
-                     "algorithmic_bytes_per_launch": dwt_bytes,
-                     "launch_us": dwt_us,
-                     "timing": f"{n_dwt} back-to-back launches, rotating input copies"},
+            "timing": f"CUDA events around K steps: replays of one CUDA graph holding one wf_step"
+                      f" per input copy ({n_copies} steps per replay), remainder from per-copy graphs"}),
+        "roofline": roofline,
         "path_roofline": {"bytes_per_step": total_bytes,
                           "achieved": total_bytes / (ms_per_step * 1e-3) / 1e9,
                           "peak": peak, "unit": "GB/s",
                           "frac": total_bytes / (ms_per_step * 1e-3) / 1e9 / peak},
+        "dwt_roofline": dwt_roofline,
         "stages_us": stage_us,
         "cpu_baseline": None if cpu_rate is None else {
             "value": cpu_rate, "unit": "tokens/s", "cores": workers, "kind": "oracle",
@@ -434,7 +480,7 @@ def run_ours(args, cfg):
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "entry_point": "wf_step_host (pinned host Q/Kp/Vp/Kg/Vg in, O out)"},
-        "gpu_launches": 2 * args.steps,  # dwt_stream_kernel + path_kernel per wf_step
+        "gpu_launches": launches * args.steps,  # path_kernel (+ dwt_stream_kernel unless fused)
         "clocks": clocks,
         "device_status": status,
     }

@@ -110,6 +110,15 @@ int wf_default_k_per_level(int32_t n_prompt, int32_t levels, int32_t budget,
 int wf_workspace_bytes(const wf_dims* dims, const int32_t* k_per_level,
                        size_t* bytes);
 
+/* Number of kernel launches one wf_step call makes for these sizes on the
+ * current device: 1 where the level-L approximation is computed inside the
+ * path kernel (per-CTA slice of at most 64 coarse positions whose spans fit
+ * the streaming ring), else 2 (a separate streaming DWT launch first).
+ * Stores it in *launches.  Host only; launches nothing.
+ * Errors: WF_ERR_NULL/SHAPE/UNSUPPORTED, as wf_workspace_bytes. */
+int wf_step_launch_count(const wf_dims* dims, const int32_t* k_per_level,
+                         int32_t* launches);
+
 /* Clears the device status word at the start of `workspace` (async). */
 int wf_clear_device_status(void* workspace, size_t workspace_bytes, void* stream);
 

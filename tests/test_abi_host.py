@@ -145,3 +145,21 @@ def test_every_workload_is_planned(lib, name):
     st, n = _ws(dims, cfg.k_per_level())
     assert st == 0, name
     assert n >= cfg.units_per_layer * (cfg.n_prompt >> cfg.levels) * cfg.head_dim * 4
+    # The fused single-launch step is planned where each CTA's coarse slice is
+    # small (the 4096-token layer and the tiny case); the long prompts keep a
+    # separate streaming DWT launch.
+    assert bd.step_launch_count(dims, cfg.k_per_level()) == (
+        1 if name in ("tiny", "llada8b_layer") else 2), name
+
+
+def test_step_launch_count_validates(lib):
+    dims = bd.Dims(1, 2, 1024, 32, 64, 3, 1)
+    k = (ctypes.c_int32 * 4)(64, 64, 32, 16)
+    out = ctypes.c_int32(-1)
+    assert lib.wf_step_launch_count(ctypes.byref(dims), k, None) == 1  # WF_ERR_NULL
+    assert lib.wf_step_launch_count(ctypes.byref(dims), None, ctypes.byref(out)) == 1
+    bad = bd.Dims(1, 2, 1004, 32, 64, 3, 1)  # N_p not a multiple of 2^L: WF_ERR_SHAPE
+    assert lib.wf_step_launch_count(ctypes.byref(bad), k, ctypes.byref(out)) == 2
+    assert out.value == -1
+    assert lib.wf_step_launch_count(ctypes.byref(dims), k, ctypes.byref(out)) == 0
+    assert out.value in (1, 2)

@@ -26,6 +26,7 @@ MAX_LEVELS = 12
 
 # Every symbol the header declares (checked by the host tests).
 EXPORTS = ("wf_status_string", "wf_last_error_string", "wf_default_k_per_level", "wf_workspace_bytes",
+           "wf_step_launch_count",
            "wf_clear_device_status", "wf_read_device_status", "wf_dwt_lowpass",
            "wf_score_topk", "wf_recursive_filter", "wf_sparse_gather_attn", "wf_step",
            "wf_step_host", "wf_step_static_scratch")
@@ -56,6 +57,7 @@ _SIGS = {
     "wf_last_error_string": (ctypes.c_char_p, []),
     "wf_default_k_per_level": (ctypes.c_int, [_i32, _i32, _i32, _i32p]),
     "wf_workspace_bytes": (ctypes.c_int, [_DIMSP, _i32p, ctypes.POINTER(_sz)]),
+    "wf_step_launch_count": (ctypes.c_int, [_DIMSP, _i32p, _i32p]),
     "wf_clear_device_status": (ctypes.c_int, [_vp, _sz, _vp]),
     "wf_read_device_status": (ctypes.c_int, [_vp, _sz, _vp, _i32p]),
     "wf_dwt_lowpass": (ctypes.c_int, [_DIMSP, _vp, _vp, _vp, _vp]),
@@ -147,6 +149,14 @@ def workspace_bytes(dims: Dims, k: Sequence[int]) -> int:
     n = ctypes.c_size_t(0)
     _check("wf_workspace_bytes", lib().wf_workspace_bytes(ctypes.byref(dims), _k_array(k),
                                                           ctypes.byref(n)))
+    return n.value
+
+
+def step_launch_count(dims: Dims, k: Sequence[int]) -> int:
+    """Kernel launches one wf_step makes for these sizes (1 fused, else 2)."""
+    n = ctypes.c_int32(0)
+    _check("wf_step_launch_count", lib().wf_step_launch_count(ctypes.byref(dims), _k_array(k),
+                                                              ctypes.byref(n)))
     return n.value
 
 

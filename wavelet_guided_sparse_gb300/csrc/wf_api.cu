@@ -154,6 +154,21 @@ int wf_workspace_bytes(const wf_dims* dims, const int32_t* k_per_level, size_t* 
   return WF_OK;
 }
 
+int wf_step_launch_count(const wf_dims* dims, const int32_t* k_per_level, int32_t* launches) {
+  LaunchDims ld;
+  int st = check_dims(dims, &ld);
+  if (st != WF_OK) return st;
+  if (launches == nullptr) return WF_ERR_NULL;
+  st = check_k(ld, k_per_level);
+  if (st != WF_OK) return st;
+  wf::PathPlan plan;
+  if (!wf::plan_path(ld, wf::kPhaseAll | wf::kPhaseFuseDwt, k_per_level, k_per_level[ld.levels],
+                     k_per_level[0], wf::device_sm_count(), &plan))
+    return WF_ERR_UNSUPPORTED;
+  *launches = plan.fuse_dwt ? 1 : 2;
+  return WF_OK;
+}
+
 int wf_clear_device_status(void* workspace, size_t workspace_bytes, void* stream) {
   if (workspace == nullptr) return WF_ERR_NULL;
   if (workspace_bytes < kHeaderBytes) return WF_ERR_WORKSPACE;

@@ -201,56 +201,68 @@ __device__ __forceinline__ TopkResult cluster_select(const uint32_t* keys, int n
 
 // ------------------------------------------------------------------ logits GEMM
 // bf16: out[r][i] = scale * Σ_planes rows[r]·Q[i] for r < n_rows (out row
-// pitch `pitch` floats).  `nplanes` bf16 row blocks `plane_bytes` apart are
+// pitch `pitch` floats).  NP bf16 row blocks `plane_bytes` apart are
 // accumulated (one plane for key rows; three planes hi + mid + lo reproduce an
-// fp32 row exactly).  Each warp owns whole 16-row m-blocks and keeps one
-// accumulator per 8-query n-block, so the MMA chains of a warp are independent.
-template <int D>
-__device__ __noinline__ void logits_tile_bf16(const unsigned char* rows, int nplanes,
-                                              int plane_bytes, const unsigned char* qs,
-                                              float* out, int row0, int n_rows, int G,
-                                              int pitch, float scale) {
+// fp32 row exactly).  Work items are (16-row m-block, group of at most NBG
+// 8-query n-blocks), spread over the warps so that short tiles still occupy
+// every warp; each (plane, n-block) has its own accumulator, so the MMA
+// chains of a warp are independent, and the planes are summed at the end.
+template <int D, int NP, int NBG>
+__device__ __noinline__ void logits_tile_bf16(const unsigned char* rows, int plane_bytes,
+                                              const unsigned char* qs, float* out, int row0,
+                                              int n_rows, int G, int pitch, float scale) {
+  static_assert(NP == 1 || NP == 3, "one key plane or three A_L planes");
   constexpr int RB = D * 2 + 16;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int NB = (G + 7) >> 3;
-  const uint32_t qbase = smem_u32(qs) + (lane & 7) * RB + ((lane >> 3) & 1) * 16;
   const int nmb = (n_rows + 15) >> 4;
-  for (int mb = warp; mb < nmb; mb += kWarps) {
-    float acc[8][4];
+  int ngrp = (NB + NBG - 1) / NBG;
+  while (ngrp < NB && nmb * ngrp < kWarps) ngrp *= 2;
+  if (ngrp > NB) ngrp = NB;
+  const uint32_t qbase = smem_u32(qs) + (lane & 7) * RB + ((lane >> 3) & 1) * 16;
+  for (int item = warp; item < nmb * ngrp; item += kWarps) {
+    const int mb = item / ngrp, g = item - mb * ngrp;
+    const int nb0 = g * NB / ngrp, nbn = (g + 1) * NB / ngrp - nb0;  // nbn <= NBG
+    float acc[NP][NBG][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int pl = 0; pl < NP; ++pl)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
-#pragma unroll 1
-    for (int pl = 0; pl < nplanes; ++pl) {
-      const uint32_t abase =
-          smem_u32(rows + pl * plane_bytes) + (mb * 16 + (lane & 15)) * RB + (lane >> 4) * 16;
+      for (int i = 0; i < NBG; ++i)
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        uint32_t a[4];
-        ldsm_x4(abase + ks * 32, a);
+        for (int e = 0; e < 4; ++e) acc[pl][i][e] = 0.f;
+    const uint32_t abase = smem_u32(rows) + (mb * 16 + (lane & 15)) * RB + (lane >> 4) * 16;
 #pragma unroll
-        for (int nb = 0; nb < 8; ++nb) {
-          if (nb < NB) {
-            uint32_t b[2];
-            ldsm_x2(qbase + nb * 8 * RB + ks * 32, b);
-            mma_bf16(acc[nb], a, b);
-          }
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t a[NP][4];
+#pragma unroll
+      for (int pl = 0; pl < NP; ++pl) ldsm_x4(abase + pl * plane_bytes + ks * 32, a[pl]);
+#pragma unroll
+      for (int i = 0; i < NBG; ++i) {
+        if (i < nbn) {
+          uint32_t b[2];
+          ldsm_x2(qbase + (nb0 + i) * 8 * RB + ks * 32, b);
+#pragma unroll
+          for (int pl = 0; pl < NP; ++pl) mma_bf16(acc[pl][i], a[pl], b);
         }
       }
     }
     const int r_lo = mb * 16 + (lane >> 2);
 #pragma unroll
-    for (int nb = 0; nb < 8; ++nb) {
-      if (nb >= NB) continue;
-      const int q0 = nb * 8 + (lane & 3) * 2;
+    for (int i = 0; i < NBG; ++i) {
+      if (i >= nbn) continue;
+      const int q0 = (nb0 + i) * 8 + (lane & 3) * 2;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int r = r_lo + 8 * h;
         if (r >= n_rows) continue;
+        float v0 = acc[0][i][2 * h], v1 = acc[0][i][2 * h + 1];
+        if constexpr (NP == 3) {  // hi + (mid + lo): the small planes first
+          v0 += acc[1][i][2 * h] + acc[2][i][2 * h];
+          v1 += acc[1][i][2 * h + 1] + acc[2][i][2 * h + 1];
+        }
         float* dst = out + static_cast<int64_t>(row0 + r) * pitch;
-        if (q0 < G) dst[q0] = acc[nb][2 * h] * scale;
-        if (q0 + 1 < G) dst[q0 + 1] = acc[nb][2 * h + 1] * scale;
+        if (q0 < G) dst[q0] = v0 * scale;
+        if (q0 + 1 < G) dst[q0 + 1] = v1 * scale;
       }
     }
   }
@@ -407,16 +419,21 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     for (int st = 0; st < fuse_issued; ++st) fuse_issue(st);
   }
 
-  // Queries (input dtype, padded rows; rows >= G are zero).
+  // Queries (input dtype, padded rows; rows >= G are zero), by cp.async: with
+  // fused step 1 they land while the ring streams and are waited for just
+  // before the first logits tile.
   {
     const T* qsrc = static_cast<const T*>(p.q) + unit * G * D;
     constexpr int V = Elem<T>::kPer16B;
     for (int e = tid; e < kMaxQ * (D / V); e += kThreads) {
       const int r = e / (D / V), col = (e % (D / V)) * V;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < G) v = ldg16(qsrc + r * D + col);
-      *reinterpret_cast<uint4*>(qs + r * RB + col * sizeof(T)) = v;
+      if (r < G)
+        cp_async16(qs + r * RB + col * sizeof(T), qsrc + r * D + col);
+      else
+        *reinterpret_cast<uint4*>(qs + r * RB + col * sizeof(T)) = make_uint4(0, 0, 0, 0);
     }
+    cp_async_commit();
+    if (!p.fuse_dwt) cp_async_wait<0>();
   }
   __syncthreads();
 
@@ -508,8 +525,10 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           ++fuse_issued;
         }
       }
+      cp_async_wait<0>();  // the queries
+      __syncthreads();
       if (sizeof(T) == 2)
-        logits_tile_bf16<D>(as, 3, kScoreChunk * RB, qs, zc, 0, Pc, G, TS, zscale);
+        logits_tile_bf16<D, 3, 4>(as, kScoreChunk * RB, qs, zc, 0, Pc, G, TS, zscale);
       else
         logits_tile_f32<D>(as, reinterpret_cast<const float*>(qs), zc, 0, Pc, G, TS, zscale);
       __syncthreads();
@@ -530,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         cp_async_commit();
         cp_async_wait<0>();
         __syncthreads();
-        logits_tile_bf16<D>(as, 3, kScoreChunk * RB, qs, zc, 0, rows, G, TS, zscale);
+        logits_tile_bf16<D, 3, 4>(as, kScoreChunk * RB, qs, zc, 0, rows, G, TS, zscale);
         __syncthreads();
         return;
       }
@@ -562,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
                 make_uint2(pack_bf16(pv[pl][0], pv[pl][1]), pack_bf16(pv[pl][2], pv[pl][3]));
         }
         __syncthreads();
-        logits_tile_bf16<D>(as, 3, kScoreChunk * RB, qs, zc, 0, rows, G, TS, zscale);
+        logits_tile_bf16<D, 3, 4>(as, kScoreChunk * RB, qs, zc, 0, rows, G, TS, zscale);
       } else {
         logits_tile_f32<D>(as, reinterpret_cast<const float*>(qs), zc, 0, rows, G, TS, zscale);
       }
@@ -697,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       // (tiles sit back to back in the ring).
       cp_async_wait<0>();
       __syncthreads();
-      logits_tile_bf16<D>(kst, 1, 0, qs, t, 0, R, G, TS, 1.f);
+      logits_tile_bf16<D, 1, 8>(kst, 0, qs, t, 0, R, G, TS, 1.f);
       __syncthreads();
     } else
     for (int tile = 0; tile < ntiles; ++tile) {
@@ -707,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       const unsigned char* buf = kst + stage * kTileRows * RB;
       const int rows_valid = min(kTileRows, R - tile * kTileRows);
       if constexpr (sizeof(T) == 2) {
-        logits_tile_bf16<D>(buf, 1, 0, qs, t, tile * kTileRows, rows_valid, G, TS, 1.f);
+        logits_tile_bf16<D, 1, 8>(buf, 0, qs, t, tile * kTileRows, rows_valid, G, TS, 1.f);
       } else {
         logits_tile_f32<D>(buf, reinterpret_cast<const float*>(qs), t, tile * kTileRows,
                            rows_valid, G, TS, 1.f);
