@@ -268,7 +268,9 @@ static __device__ __noinline__ void cluster_merge_stats(const float* loc_m, cons
 //
 // Three radix rounds (11, 11, 10 bits, most significant first) find the k-th
 // largest key T; every key > T is taken, plus the first (k - #{key > T}) keys
-// equal to T in (rank, index) order.  Two variants: gather-all (every CTA
+// equal to T in (rank, index) order.  When a round's boundary bin is taken
+// whole, T becomes the bin's lowest value minus one with no ties, and the
+// remaining rounds are skipped.  Two variants: gather-all (every CTA
 // receives every key and selects locally; one cluster barrier) for small
 // candidate sets, and distributed (histograms reduce-scattered and
 // all-gathered through DSMEM; two barriers per round) for large ones.
@@ -373,6 +375,12 @@ static __device__ __noinline__ TopkResult topk_distributed(const uint32_t* keys,
     need -= above;
     prefix |= digit << shift;
     pmask |= static_cast<uint32_t>(nb - 1) << shift;
+    // Early exit as in block_select_topk (total is the same on every rank).
+    if (round < 2 && static_cast<int>(total[digit]) == need && prefix != 0u) {
+      prefix -= 1u;
+      need = 0;
+      break;
+    }
   }
   const uint32_t thr = prefix;
   int gt = 0, eq = 0;
@@ -411,7 +419,8 @@ static __device__ __noinline__ TopkResult topk_distributed(const uint32_t* keys,
 // a warp scan over lanes and a second warp scan inside the boundary lane's
 // bins).  A fused pass counts, per warp chunk, the keys above the threshold
 // and the ties, and emit(i, slot) receives every selected key with its rank
-// among the selected (ascending index).  Six __syncthreads in total.
+// among the selected (ascending index).  A round whose boundary bin is taken
+// whole ends the search early (usually after the second round).
 // Shared-memory histogram increment aggregated over the lanes of a warp that
 // hit the same bin (scores cluster in a few bins in the first round); the
 // count of the bin's range of nb/32 bins is kept alongside.
@@ -489,6 +498,14 @@ static __device__ __noinline__ void block_select_topk(const uint32_t* keys, int 
     need -= above;
     prefix |= digit << shift;
     pmask |= static_cast<uint32_t>(nb - 1) << shift;
+    // Early exit: every key of the boundary bin is taken, so the threshold is
+    // the bin's lowest value (every key > prefix - 1) and no tie remains.
+    // (Same decision in every warp: all read the same histogram.)
+    if (round < 2 && static_cast<int>(h[digit]) == need && prefix != 0u) {
+      prefix -= 1u;
+      need = 0;
+      break;
+    }
   }
   const uint32_t thr = prefix;
   // Fused compaction: warp w owns keys [lo, hi).

@@ -760,114 +760,94 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         continue;
       }
       // Scores of this level's candidates (log2 domain, z = sc2 * Σ_leaves t):
-      //  pass 1  CTA max per query; pass 2  e = 2^(z - max), CTA sum (at level 0
-      //  e overwrites t, which is not needed afterwards); cluster merge;
-      //  pass 3  s_c = Σ_i e[c,i] * w_i with w_i = 2^(max_i - gmax_i) / gsum_i.
-      // Passes 1-2: lanes = queries, each warp takes 4 candidates at a time.
+      //  pass A  per query, online (max, Σ 2^(z - max)) over this CTA's
+      //          candidates (lanes = queries q and q + 32; a warp takes 4
+      //          candidates at a time, their loads issued together);
+      //  CTA and cluster merges give the global max gm and 1 / sum ginv;
+      //  pass B  s_c = Σ_q 2^(z[c,q] - gm_q) * ginv_q, one thread per candidate.
       const int leaves = 1 << j;
       const float sc2 = p.scale[j] * kLog2e;
       const bool final_gather = j == 0 && p.gather_all;
-      // z of candidate ci for query q: leaf sums of t (one leaf at level 0).
-      // Lanes = queries q and q + 32.  Single-leaf levels take 4 candidates
-      // per warp at a time; multi-leaf levels (rare) one candidate at a time.
       const bool qa = lane < G, qb = lane + 32 < G;
       const int la = qa ? lane : 0, lb = qb ? lane + 32 : 0;
+      // Leaf sum of t for candidate row `row` (times TS), query q.
       auto leaf_sum = [&](int64_t row, int q) {
         float a = 0.f;
 #pragma unroll 1
         for (int i = 0; i < leaves; ++i) a += t[row + i * TS + q];
         return a;
       };
-      float m0 = -INFINITY, m1 = -INFINITY;
-      if (leaves == 1) {
-        for (int ci0 = warp * 4; ci0 < n_cand; ci0 += kWarps * 4) {
+      float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+      for (int ci0 = warp * 4; ci0 < n_cand; ci0 += kWarps * 4) {
+        float za[4], zb[4];
+        if (leaves == 1) {
           int64_t rows[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) rows[u] = static_cast<int64_t>(cr[min(ci0 + u, n_cand - 1)]) * TS;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const bool ok = ci0 + u < n_cand;
-            m0 = fmaxf(m0, ok && qa ? t[rows[u] + la] * sc2 : -INFINITY);
-            m1 = fmaxf(m1, ok && qb ? t[rows[u] + lb] * sc2 : -INFINITY);
+            za[u] = t[rows[u] + la];
+            zb[u] = t[rows[u] + lb];
+          }
+        } else {
+#pragma unroll 1
+          for (int u = 0; u < 4; ++u) {
+            const int64_t row = static_cast<int64_t>(cr[min(ci0 + u, n_cand - 1)]) * TS;
+            za[u] = leaf_sum(row, la);
+            zb[u] = leaf_sum(row, lb);
           }
         }
-      } else {
-#pragma unroll 1
-        for (int ci = warp; ci < n_cand; ci += kWarps) {
-          const int64_t row = static_cast<int64_t>(cr[ci]) * TS;
-          if (qa) m0 = fmaxf(m0, leaf_sum(row, la) * sc2);
-          if (qb) m1 = fmaxf(m1, leaf_sum(row, lb) * sc2);
+        float cm0 = m0, cm1 = m1;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const bool ok = ci0 + u < n_cand;
+          za[u] = ok && qa ? za[u] * sc2 : -INFINITY;
+          zb[u] = ok && qb ? zb[u] * sc2 : -INFINITY;
+          cm0 = fmaxf(cm0, za[u]);
+          cm1 = fmaxf(cm1, zb[u]);
+        }
+        if (cm0 != -INFINITY) {
+          float acc = l0 * safe_exp2_diff(m0, cm0);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) acc += safe_exp2_diff(za[u], cm0);
+          l0 = acc;
+          m0 = cm0;
+        }
+        if (cm1 != -INFINITY) {
+          float acc = l1 * safe_exp2_diff(m1, cm1);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) acc += safe_exp2_diff(zb[u], cm1);
+          l1 = acc;
+          m1 = cm1;
         }
       }
       part_m[warp * kMaxQ + lane] = m0;
       part_m[warp * kMaxQ + lane + 32] = m1;
+      part_l[warp * kMaxQ + lane] = l0;
+      part_l[warp * kMaxQ + lane + 32] = l1;
       __syncthreads();
       if (tid < G) {
-        float m = -INFINITY;
-        for (int w = 0; w < kWarps; ++w) m = fmaxf(m, part_m[w * kMaxQ + tid]);
+        float m = -INFINITY, l = 0.f;
+        for (int w = 0; w < kWarps; ++w) merge_ml(m, l, part_m[w * kMaxQ + tid], part_l[w * kMaxQ + tid]);
         loc_m[tid] = m;
-      }
-      __syncthreads();
-      float e0 = 0.f, e1 = 0.f;
-      {
-        const float lma = qa ? loc_m[lane] : 0.f;
-        const float lmb = qb ? loc_m[lane + 32] : 0.f;
-        if (leaves == 1) {  // level 0: e replaces t
-          for (int ci0 = warp * 4; ci0 < n_cand; ci0 += kWarps * 4) {
-            int64_t rows[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) rows[u] = static_cast<int64_t>(cr[min(ci0 + u, n_cand - 1)]) * TS;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              if (ci0 + u >= n_cand) continue;
-              if (qa) {
-                const float e = exp2f(t[rows[u] + la] * sc2 - lma);
-                e0 += e;
-                if (j == 0) t[rows[u] + la] = e;
-              }
-              if (qb) {
-                const float e = exp2f(t[rows[u] + lb] * sc2 - lmb);
-                e1 += e;
-                if (j == 0) t[rows[u] + lb] = e;
-              }
-            }
-          }
-        } else {
-#pragma unroll 1
-          for (int ci = warp; ci < n_cand; ci += kWarps) {
-            const int64_t row = static_cast<int64_t>(cr[ci]) * TS;
-            if (qa) e0 += exp2f(leaf_sum(row, la) * sc2 - lma);
-            if (qb) e1 += exp2f(leaf_sum(row, lb) * sc2 - lmb);
-          }
-        }
-      }
-      part_l[warp * kMaxQ + lane] = e0;
-      part_l[warp * kMaxQ + lane + 32] = e1;
-      __syncthreads();
-      if (tid < G) {
-        float l = 0.f;
-        for (int w = 0; w < kWarps; ++w) l += part_l[w * kMaxQ + tid];
         loc_l[tid] = l;
       }
       __syncthreads();
       cluster_merge_stats(loc_m, loc_l, G, stat_in, gm, ginv, n_cand, final_gather ? cnt_b : nullptr);
-      float* wq = part_m;  // per-query weights (part_m is free again)
-      if (tid < G) wq[tid] = loc_m[tid] == -INFINITY ? 0.f : exp2f(loc_m[tid] - gm[tid]) * ginv[tid];
-      __syncthreads();
-      // Pass 3: one thread per candidate (odd row pitch: conflict-free).
+      // Pass B: one thread per candidate (odd row pitch: conflict-free).
       for (int ci = tid; ci < n_cand; ci += kThreads) {
         const int64_t row = static_cast<int64_t>(cr[ci]) * TS;
         float sa = 0.f, sb = 0.f;
-        if (j == 0) {  // t holds e
+        if (leaves == 1) {
 #pragma unroll 4
           for (int q = 0; q + 1 < G; q += 2) {
-            sa += t[row + q] * wq[q];
-            sb += t[row + q + 1] * wq[q + 1];
+            sa += exp2f(t[row + q] * sc2 - gm[q]) * ginv[q];
+            sb += exp2f(t[row + q + 1] * sc2 - gm[q + 1]) * ginv[q + 1];
           }
-          if (G & 1) sa += t[row + G - 1] * wq[G - 1];
+          if (G & 1) sa += exp2f(t[row + G - 1] * sc2 - gm[G - 1]) * ginv[G - 1];
         } else {
 #pragma unroll 1
-          for (int q = 0; q < G; ++q) sa += exp2f(leaf_sum(row, q) * sc2 - loc_m[q]) * wq[q];
+          for (int q = 0; q < G; ++q) sa += exp2f(leaf_sum(row, q) * sc2 - gm[q]) * ginv[q];
         }
         keys[ci] = __float_as_uint(sa + sb);
       }
