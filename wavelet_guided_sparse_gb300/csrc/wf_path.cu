@@ -38,6 +38,7 @@
 #include "wf_common.cuh"
 #include "wf_internal.h"
 #include "wf_mma.cuh"
+#include "wf_umma.cuh"
 
 namespace wf {
 
@@ -106,7 +107,7 @@ struct PathSmem {
     cnt_a = take_bytes(sizeof(int32_t) * kMaxCluster);
     cnt_b = take_bytes(sizeof(int32_t) * kMaxCluster);
     misc = take_bytes(sizeof(int32_t) * 8);
-    bars = take_bytes(sizeof(uint64_t) * kFuseStages);
+    bars = take_bytes(sizeof(uint64_t) * (kFuseStages + 1));  // ring stages + tensor-core commits
     sl_all = take_bytes(sizeof(int32_t) * p.sorted_cap);
     topk = take_bytes(sizeof(TopkSmem));
     // All-gathered keys: the P coarse scores, and (final level, gather mode)
@@ -200,89 +201,67 @@ __device__ __forceinline__ TopkResult cluster_select(const uint32_t* keys, int n
 }
 
 // ------------------------------------------------------------------ logits GEMM
-// bf16: out[r][i] = scale * Σ_planes rows[r]·Q[i] for r < n_rows (out row
-// pitch `pitch` floats).  NP bf16 row blocks `plane_bytes` apart are
-// accumulated (one plane for key rows; three planes hi + mid + lo reproduce an
-// fp32 row exactly).  Work items are (16-row m-block, group of at most NBG
-// 8-query n-blocks), spread over the warps so that short tiles still occupy
-// every warp; each (plane, n-block) has its own accumulator, so the MMA
-// chains of a warp are independent, and the planes are summed at the end.
-template <int D, int NP, int NBG>
-__device__ __noinline__ void logits_tile_bf16(const unsigned char* rows, int plane_bytes,
-                                              const unsigned char* qs, float* out, int row0,
-                                              int n_rows, int G, int pitch, float scale) {
-  static_assert(NP == 1 || NP == 3, "one key plane or three A_L planes");
-  constexpr int RB = D * 2 + 16;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int NB = (G + 7) >> 3;
-  const int nmb = (n_rows + 15) >> 4;
-  int ngrp = (NB + NBG - 1) / NBG;
-  while (ngrp < NB && nmb * ngrp < kWarps) ngrp *= 2;
-  if (ngrp > NB) ngrp = NB;
-  const uint32_t qbase = smem_u32(qs) + (lane & 7) * RB + ((lane >> 3) & 1) * 16;
-  for (int item = warp; item < nmb * ngrp; item += kWarps) {
-    const int mb = item / ngrp, g = item - mb * ngrp;
-    const int nb0 = g * NB / ngrp, nbn = (g + 1) * NB / ngrp - nb0;  // nbn <= NBG
-    float acc[NP][NBG][4];
-#pragma unroll
-    for (int pl = 0; pl < NP; ++pl)
-#pragma unroll
-      for (int i = 0; i < NBG; ++i)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[pl][i][e] = 0.f;
-    const uint32_t abase = smem_u32(rows) + (mb * 16 + (lane & 15)) * RB + (lane >> 4) * 16;
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      uint32_t a[NP][4];
-#pragma unroll
-      for (int pl = 0; pl < NP; ++pl) ldsm_x4(abase + pl * plane_bytes + ks * 32, a[pl]);
-#pragma unroll
-      for (int i = 0; i < NBG; ++i) {
-        if (i < nbn) {
-          uint32_t b[2];
-          ldsm_x2(qbase + (nb0 + i) * 8 * RB + ks * 32, b);
-#pragma unroll
-          for (int pl = 0; pl < NP; ++pl) mma_bf16(acc[pl][i], a[pl], b);
-        }
-      }
-    }
-    const int r_lo = mb * 16 + (lane >> 2);
-#pragma unroll
-    for (int i = 0; i < NBG; ++i) {
-      if (i >= nbn) continue;
-      const int q0 = (nb0 + i) * 8 + (lane & 3) * 2;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = r_lo + 8 * h;
-        if (r >= n_rows) continue;
-        float v0 = acc[0][i][2 * h], v1 = acc[0][i][2 * h + 1];
-        if constexpr (NP == 3) {  // hi + (mid + lo): the small planes first
-          v0 += acc[1][i][2 * h] + acc[2][i][2 * h];
-          v1 += acc[1][i][2 * h + 1] + acc[2][i][2 * h + 1];
-        }
-        float* dst = out + static_cast<int64_t>(row0 + r) * pitch;
-        if (q0 < G) dst[q0] = v0 * scale;
-        if (q0 + 1 < G) dst[q0 + 1] = v1 * scale;
-      }
-    }
-  }
-}
-
-// Q B-fragments (8 queries x 16 dims per n-block) of this warp's n-blocks.
+// bf16 logits tile on the fifth-generation tensor cores:
+//   out[(row0 + r) * pitch + q] = scale * Σ_planes Σ_k A_p[r][k] * Q[q][k]
+// for r < rows and q < G.  A (nplanes planes plane_bytes apart, summed: one
+// plane for key rows; hi + mid + lo planes reproduce an fp32 row exactly) and
+// Q are bf16 in the core-matrix layout (8-row groups 16 * D bytes apart).
+// The rows go in 128-row (M = 128) pieces, then 64-row (M = 64) pieces, each
+// into its own tensor-memory accumulator of N = G rounded up to 16 columns;
+// one thread issues every MMA, one commit signals `bar`, and the warps read
+// the accumulators back (M = 128: row = lane of the warp's lane quarter;
+// M = 64: rows 16q + l in lanes 32q + l, l < 16).  Rows up to the next
+// multiple of 64 are read from shared memory.  Block-wide; every thread keeps
+// the same `phase` count of completed commits on `bar`.
 template <int D>
-__device__ __forceinline__ void load_q_frags(const unsigned char* qs, int G,
-                                             uint32_t (&bq)[4][D / 16][2]) {
-  constexpr int RB = D * 2 + 16;
+__device__ __noinline__ void umma_logits(const unsigned char* a, int nplanes, int plane_bytes,
+                                         int rows, const unsigned char* qs, int G, float* out,
+                                         int row0, int pitch, float scale, uint32_t tmem,
+                                         uint64_t* bar, uint32_t& phase, int32_t* status) {
+  constexpr int SBO = D * 16;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int NB = (G + 7) >> 3, ng = warp >> 2;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int nb = min(ng + 2 * i, NB - 1);
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks)
-      ldsm_x2(smem_u32(qs) + (nb * 8 + (lane & 7)) * RB + ks * 32 + ((lane >> 3) & 1) * 16,
-              bq[i][ks]);
+  const int N = (G + 15) & ~15;
+  fence_proxy_async();  // operands written through the generic proxy
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0) {
+    const uint32_t a0 = smem_u32(a), q0 = smem_u32(qs);
+    int piece = 0;
+    for (int r0 = 0; r0 < rows; r0 += rows - r0 >= 128 ? 128 : 64, ++piece) {
+      const int m = rows - r0 >= 128 ? 128 : 64;
+      const uint32_t idesc = umma_idesc_bf16(m, N);
+      for (int pl = 0; pl < nplanes; ++pl)
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_bf16(tmem + piece * N,
+                    umma_desc(a0 + pl * plane_bytes + (r0 >> 3) * SBO + ks * 256, 128, SBO),
+                    umma_desc(q0 + ks * 256, 128, SBO), idesc, (pl | ks) != 0);
+    }
+    umma_commit(bar);
   }
+  const bool ok = mbar_wait_bounded(bar, phase & 1u, status);
+  ++phase;
+  tc_fence_after();
+  if (ok) {
+    const int q4 = warp & 3;
+    int piece = 0;
+    for (int r0 = 0; r0 < rows; r0 += rows - r0 >= 128 ? 128 : 64, ++piece) {
+      const int m = rows - r0 >= 128 ? 128 : 64;
+      const int r = m == 128 ? q4 * 32 + lane : q4 * 16 + (lane & 15);
+      const bool has = (m == 128 || lane < 16) && r0 + r < rows;
+      float* dst = out + static_cast<int64_t>(row0 + r0 + r) * pitch;
+      for (int c = (warp >> 2) * 16; c < N; c += 32) {
+        float v[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(q4 * 32) << 16) + piece * N + c, v);
+        if (has) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (c + i < G) dst[c + i] = v[i] * scale;
+        }
+      }
+    }
+  }
+  tc_fence_before();  // later MMAs into these columns follow these reads
 }
 
 // fp32: plain FMAs.  Thread -> row (tid & 63), queries (tid >> 6) + 4i.
@@ -369,6 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   const PathSmem<T, D> L(p);
   constexpr int RB = PathSmem<T, D>::kRowBytes;
   constexpr int RF = PathSmem<T, D>::kRowF;
+  // bf16 A_L planes (hi / mid / lo) of one score chunk, core-matrix layout.
+  constexpr int kPlaneBytes = kScoreChunk * D * 2;
   unsigned char* qs = smem + L.qs;
   float* stat_in = reinterpret_cast<float*>(smem + L.stat_in);
   float* gm = reinterpret_cast<float*>(smem + L.gm);
@@ -397,6 +378,12 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   // positions, one contiguous byte range) stream through a ring of bulk
   // copies; the first stages are in flight before anything else happens.
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* mma_bar = bars + kFuseStages;  // tensor-core commits (phase count in mma_phase)
+  uint32_t mma_phase = 0;
+  // bf16 logits tiles run on the tensor cores with accumulators in tensor
+  // memory: 256 columns (at most four pieces of N <= 64 queries).
+  constexpr uint32_t kTmemCols = 256;
+  const bool use_tmem = sizeof(T) == 2 && (p.mode & (kModeScore | kModeFilter)) != 0;
   const int fuse_sr = kFuseStageBytes / (D * static_cast<int>(sizeof(T)));  // rows per stage
   const int fuse_rows = p.fuse_dwt ? (p.per_cta_p << levels) : 0;
   const int fuse_nst = (fuse_rows + fuse_sr - 1) / fuse_sr;
@@ -413,29 +400,40 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
              fuse_src + static_cast<int64_t>(st) * kFuseStageBytes, bytes, bar);
   };
   int fuse_issued = min(kFuseStages, fuse_nst);
-  if (p.fuse_dwt && tid == 0) {
-    for (int i = 0; i < kFuseStages; ++i) mbar_init(&bars[i], 1);
+  if (tid == 0) {
+    if (p.fuse_dwt)
+      for (int i = 0; i < kFuseStages; ++i) mbar_init(&bars[i], 1);
+    mbar_init(mma_bar, 1);
     fence_mbar_init();
-    for (int st = 0; st < fuse_issued; ++st) fuse_issue(st);
+    if (p.fuse_dwt)
+      for (int st = 0; st < fuse_issued; ++st) fuse_issue(st);
   }
+  __syncwarp();
+  if (use_tmem && warp == 0) tmem_alloc(reinterpret_cast<uint32_t*>(misc + 7), kTmemCols);
 
   // Queries (input dtype, padded rows; rows >= G are zero), by cp.async: with
   // fused step 1 they land while the ring streams and are waited for just
   // before the first logits tile.
   {
+    // bf16: core-matrix layout (tensor-core operand); fp32: padded rows.
     const T* qsrc = static_cast<const T*>(p.q) + unit * G * D;
     constexpr int V = Elem<T>::kPer16B;
     for (int e = tid; e < kMaxQ * (D / V); e += kThreads) {
       const int r = e / (D / V), col = (e % (D / V)) * V;
+      unsigned char* dst = sizeof(T) == 2 ? qs + cm_offset(r, col / 8, D * 16)
+                                          : qs + r * RB + col * sizeof(T);
       if (r < G)
-        cp_async16(qs + r * RB + col * sizeof(T), qsrc + r * D + col);
+        cp_async16(dst, qsrc + r * D + col);
       else
-        *reinterpret_cast<uint4*>(qs + r * RB + col * sizeof(T)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
     }
     cp_async_commit();
     if (!p.fuse_dwt) cp_async_wait<0>();
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = use_tmem ? static_cast<uint32_t>(misc[7]) : 0u;  // accumulator base
 
   // ================================================================ score
   if (p.mode & kModeScore) {
@@ -508,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
             }
 #pragma unroll
             for (int pl = 0; pl < 3; ++pl)
-              *reinterpret_cast<uint4*>(as + pl * kScoreChunk * RB + row * RB + ch * 16) =
+              *reinterpret_cast<uint4*>(as + pl * kPlaneBytes + cm_offset(row, ch, D * 16)) =
                   make_uint4(w[pl][0], w[pl][1], w[pl][2], w[pl][3]);
           } else {
             *reinterpret_cast<float4*>(as + row * RB + ch * 16) =
@@ -526,11 +524,13 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         }
       }
       cp_async_wait<0>();  // the queries
-      __syncthreads();
-      if (sizeof(T) == 2)
-        logits_tile_bf16<D, 3, 4>(as, kScoreChunk * RB, qs, zc, 0, Pc, G, TS, zscale);
-      else
+      if (sizeof(T) == 2) {
+        umma_logits<D>(as, 3, kPlaneBytes, Pc, qs, G, zc, 0, TS, zscale, tmem, mma_bar, mma_phase,
+                       p.status);
+      } else {
+        __syncthreads();
         logits_tile_f32<D>(as, reinterpret_cast<const float*>(qs), zc, 0, Pc, G, TS, zscale);
+      }
       __syncthreads();
       z_ready = true;
     }
@@ -542,14 +542,14 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         constexpr int C8 = D / 8;
         for (int e = tid; e < 3 * rows * C8; e += kThreads) {
           const int pl = e / (rows * C8), rem = e - pl * rows * C8;
-          const int r = rem / C8, col = (rem % C8) * 8;
-          cp_async16(as + pl * kScoreChunk * RB + r * RB + col * 2,
-                     psrc + (static_cast<int64_t>(pl) * p.P + c0 + r) * D + col);
+          const int r = rem / C8, ch = rem % C8;
+          cp_async16(as + pl * kPlaneBytes + cm_offset(r, ch, D * 16),
+                     psrc + (static_cast<int64_t>(pl) * p.P + c0 + r) * D + ch * 8);
         }
         cp_async_commit();
         cp_async_wait<0>();
-        __syncthreads();
-        logits_tile_bf16<D, 3, 4>(as, kScoreChunk * RB, qs, zc, 0, rows, G, TS, zscale);
+        umma_logits<D>(as, 3, kPlaneBytes, rows, qs, G, zc, 0, TS, zscale, tmem, mma_bar, mma_phase,
+                       p.status);
         __syncthreads();
         return;
       }
@@ -577,11 +577,12 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           }
 #pragma unroll
           for (int pl = 0; pl < 3; ++pl)
-            *reinterpret_cast<uint2*>(as + pl * kScoreChunk * RB + r * RB + col * 2) =
+            *reinterpret_cast<uint2*>(as + pl * kPlaneBytes + cm_offset(r, col / 8, D * 16) +
+                                      (col % 8) * 2) =
                 make_uint2(pack_bf16(pv[pl][0], pv[pl][1]), pack_bf16(pv[pl][2], pv[pl][3]));
         }
-        __syncthreads();
-        logits_tile_bf16<D, 3, 4>(as, kScoreChunk * RB, qs, zc, 0, rows, G, TS, zscale);
+        umma_logits<D>(as, 3, kPlaneBytes, rows, qs, G, zc, 0, TS, zscale, tmem, mma_bar, mma_phase,
+                       p.status);
       } else {
         logits_tile_f32<D>(as, reinterpret_cast<const float*>(qs), zc, 0, rows, G, TS, zscale);
       }
@@ -695,6 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     const T* kp = static_cast<const T*>(p.kp);
     const int ntiles = (R + kTileRows - 1) / kTileRows;
     constexpr int C16 = D * static_cast<int>(sizeof(T)) / 16;  // 16-byte chunks per row
+    constexpr int kStageB = sizeof(T) == 2 ? kTileRows * D * 2 : kTileRows * RB;  // ring stage
     auto issue = [&](int tile, int stage) {  // all threads; one cp.async group
       const int r0 = tile * kTileRows;
       const int nr = min(kTileRows, R - r0);
@@ -704,32 +706,35 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         const int64_t grow = unit * p.n_prompt +
                              (static_cast<int64_t>(sl_all[s0 + (lr >> levels)]) << levels) +
                              (lr & ((1 << levels) - 1));
-        cp_async16(kst + (stage * kTileRows + i) * RB + ch * 16,
-                   reinterpret_cast<const unsigned char*>(kp + grow * D) + ch * 16);
+        // bf16: core-matrix layout, stages back to back (a tensor-core
+        // operand may span stages); fp32: padded rows.
+        unsigned char* dst = sizeof(T) == 2
+                                 ? kst + stage * kStageB + cm_offset(i, ch, D * 16)
+                                 : kst + (stage * kTileRows + i) * RB + ch * 16;
+        cp_async16(dst, reinterpret_cast<const unsigned char*>(kp + grow * D) + ch * 16);
       }
       cp_async_commit();
     };
     const int FS = p.f_stages;
     for (int tl = 0; tl < FS && tl < ntiles; ++tl) issue(tl, tl);
     if (ntiles <= FS && sizeof(T) == 2) {
-      // Every tile is in flight: one wait, then one GEMM over all R rows
-      // (tiles sit back to back in the ring).
+      // Every tile is in flight: one wait, then one tensor-core pass over
+      // all R rows (tiles sit back to back in the ring).
       cp_async_wait<0>();
-      __syncthreads();
-      logits_tile_bf16<D, 1, 8>(kst, 0, qs, t, 0, R, G, TS, 1.f);
+      umma_logits<D>(kst, 1, 0, R, qs, G, t, 0, TS, 1.f, tmem, mma_bar, mma_phase, p.status);
       __syncthreads();
     } else
     for (int tile = 0; tile < ntiles; ++tile) {
       const int stage = tile % FS;
       cp_async_wait_pending(min(ntiles, tile + FS) - 1 - tile);
-      __syncthreads();
-      const unsigned char* buf = kst + stage * kTileRows * RB;
       const int rows_valid = min(kTileRows, R - tile * kTileRows);
       if constexpr (sizeof(T) == 2) {
-        logits_tile_bf16<D, 1, 8>(buf, 0, qs, t, tile * kTileRows, rows_valid, G, TS, 1.f);
+        umma_logits<D>(kst + stage * kStageB, 1, 0, rows_valid, qs, G, t, tile * kTileRows, TS,
+                       1.f, tmem, mma_bar, mma_phase, p.status);
       } else {
-        logits_tile_f32<D>(buf, reinterpret_cast<const float*>(qs), t, tile * kTileRows,
-                           rows_valid, G, TS, 1.f);
+        __syncthreads();
+        logits_tile_f32<D>(kst + stage * kStageB, reinterpret_cast<const float*>(qs), t,
+                           tile * kTileRows, rows_valid, G, TS, 1.f);
       }
       __syncthreads();
       if (tile + FS < ntiles) issue(tile + FS, stage);
@@ -974,9 +979,10 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       const int mb = warp % MB, kgrp = warp / MB;  // 16 keys per warp per tile
       uint32_t qa[D / 16][4];
       {
-        const uint32_t qbase = smem_u32(qs) + (mb * 16 + (lane & 15)) * RB + (lane >> 4) * 16;
+        // Q rows mb * 16 + (lane & 15), chunk 2 ks + (lane >> 4), core-matrix layout.
+        const uint32_t qbase = smem_u32(qs) + cm_offset(mb * 16 + (lane & 15), lane >> 4, D * 16);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) ldsm_x4(qbase + ks * 32, qa[ks]);
+        for (int ks = 0; ks < D / 16; ++ks) ldsm_x4(qbase + ks * 256, qa[ks]);
       }
       float oacc[D / 8][4];
 #pragma unroll
@@ -1224,7 +1230,12 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       if (col == 0 && p.lse != nullptr) p.lse[unit * G + qi] = (mx + log2f(l)) * kLn2;
     }
   }
+  tc_fence_before();
   cluster.sync();  // peers may still read or write this CTA's shared memory
+  if (use_tmem && warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
 template <typename T, int D>

@@ -1,0 +1,106 @@
+// Fifth-generation tensor-core helpers (tcgen05, sm_100 family): tensor-
+// memory allocation, shared-memory matrix descriptors, the single-thread
+// bf16 MMA with an fp32 accumulator in tensor memory, its completion signal
+// and the accumulator read-back.
+//
+// Operand layout used throughout ("core-matrix" K-major layout, no swizzle):
+// a matrix of R rows x K bf16 values is stored as 8-row x 16-byte core
+// matrices; element (r, k) sits at byte
+//     (r / 8) * sbo + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2,
+// i.e. the core matrices of one 8-row group are contiguous along K
+// (leading byte offset 128) and consecutive 8-row groups are sbo = K * 16
+// bytes apart (stride byte offset).  Every 16-byte row chunk is contiguous,
+// so ldmatrix can read the same layout (one chunk address per lane).
+#pragma once
+
+#include <stdint.h>
+
+#include "wf_common.cuh"
+
+namespace wf {
+
+// Byte offset of row r, 16-byte chunk ch in the core-matrix layout.
+__device__ __forceinline__ uint32_t cm_offset(int r, int ch, int sbo) {
+  return static_cast<uint32_t>((r >> 3) * sbo + ch * 128 + (r & 7) * 16);
+}
+
+// ---------------------------------------------------------------- tensor memory
+// Allocates ncols (power of two, 32..512) columns of tensor memory for this
+// CTA; one whole warp executes it and the base address lands in *slot.
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// Ordering of tcgen05 operations across a thread barrier.
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- descriptors
+// Shared-memory matrix descriptor: K-major, no swizzle, base offset 0.
+//   bits 0-13  start address >> 4     bits 16-29 leading byte offset >> 4
+//   bits 32-45 stride byte offset >> 4  bits 46-47 descriptor version (1)
+//   bits 61-63 swizzle mode (0: none)
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+// Instruction descriptor of kind::f16: bf16 A and B (both K-major), fp32
+// accumulator, M x N tile (M = 64 or 128; N a multiple of 8 (M = 64) or 16).
+//   bits 4-5 accumulator format (1: f32)  bits 7-9 / 10-12 A / B format (1: bf16)
+//   bit 15 / 16 A / B major (0: K)  bits 17-22 N >> 3  bits 24-28 M >> 4
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- MMA
+// D[tmem] (+)= A * B^T over one K = 16 step; issued by a single thread.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrives once on `bar` when every tcgen05 operation this thread issued so
+// far has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------- read-back
+// Lane l of the calling warp receives columns [col, col + 16) of tensor-
+// memory lane (warp % 4) * 32 + l; taddr carries that lane base and column.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+}  // namespace wf
