@@ -46,6 +46,7 @@ namespace {
 
 constexpr int kTileRows = 64;    // filter: token rows per staged tile
 constexpr int kScoreChunk = 64;  // score: coarse positions per staged chunk
+static_assert(kScoreChunk == 8 * kWarps, "score pass 1 takes eight rows per warp per chunk");
 constexpr int kFuseStages = 3;               // fused step 1: bulk-copy ring depth
 constexpr int kFuseStageBytes = 32 * 1024;   // fused step 1: bytes per ring stage
 constexpr float kLog2e = 1.4426950408889634f;
@@ -294,14 +295,19 @@ __device__ __forceinline__ void logits_tile_f32(const unsigned char* kst, const 
     if (g + 4 * i < G) dst[g + 4 * i] = acc[i] * scale;
 }
 
-// Running (max, Σ 2^(z - max)) update (log2 domain).
-__device__ __forceinline__ void online_update(float& m, float& l, float z) {
-  if (z > m) {
-    l = l * exp2f(m - z) + 1.f;
-    m = z;
-  } else {
-    l += exp2f(z - m);
-  }
+// Running (max, Σ 2^(z - max)) update (log2 domain) with 8 logits at once
+// (entries that do not exist are -inf); the 8 loads and exponentials are
+// independent, so one warp keeps them in flight together.
+__device__ __forceinline__ void online8(float& m, float& l, const float (&z)[8]) {
+  float cm = m;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) cm = fmaxf(cm, z[u]);
+  if (cm == -INFINITY) return;
+  float acc = l * exp2f(m - cm);
+#pragma unroll
+  for (int u = 0; u < 8; ++u) acc += exp2f(z[u] - cm);
+  l = acc;
+  m = cm;
 }
 
 // Waits until at most `pending` of this thread's most recent cp.async groups
@@ -594,25 +600,22 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     for (int ch = 0; ch < nchunks; ++ch) {
       const int c0 = ch * kScoreChunk, rows = min(kScoreChunk, Pc - c0);
       chunk_logits(c0, rows);
-      // This chunk's maximum first, then one exp2 per logit.
+      // Rows warp + 8u of the chunk, eight at a time (kScoreChunk = 64).
       const int q0 = lane < G ? lane : 0, q1 = lane + 32 < G ? lane + 32 : 0;
-      float c_m0 = m0, c_m1 = m1;
-      for (int r = warp; r < rows; r += kWarps) {
-        c_m0 = fmaxf(c_m0, zc[r * TS + q0]);
-        c_m1 = fmaxf(c_m1, zc[r * TS + q1]);
+      float z[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int r = warp + kWarps * u;
+        z[u] = r < rows && lane < G ? zc[r * TS + q0] : -INFINITY;
       }
-      float s0 = 0.f, s1 = 0.f;
-      for (int r = warp; r < rows; r += kWarps) {
-        s0 += exp2f(zc[r * TS + q0] - c_m0);
-        s1 += exp2f(zc[r * TS + q1] - c_m1);
-      }
-      if (lane < G && c_m0 != -INFINITY) {
-        l0 = l0 * exp2f(m0 - c_m0) + s0;
-        m0 = c_m0;
-      }
-      if (lane + 32 < G && c_m1 != -INFINITY) {
-        l1 = l1 * exp2f(m1 - c_m1) + s1;
-        m1 = c_m1;
+      online8(m0, l0, z);
+      if (G > 32) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int r = warp + kWarps * u;
+          z[u] = r < rows && lane + 32 < G ? zc[r * TS + q1] : -INFINITY;
+        }
+        online8(m1, l1, z);
       }
     }
     part_m[warp * kMaxQ + lane] = m0;
@@ -633,9 +636,16 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       const int c0 = ch * kScoreChunk, rows = min(kScoreChunk, Pc - c0);
       if (nchunks > 1) chunk_logits(c0, rows);  // one chunk: zc still holds it
       const int r = tid >> 2, sub = tid & 3;
-      float sacc = 0.f;
-      if (r < rows)
-        for (int qi = sub; qi < G; qi += 4) sacc += exp2f(zc[r * TS + qi] - gm[qi]) * ginv[qi];
+      float sa = 0.f, sb = 0.f;
+      if (r < rows) {
+        int qi = sub;
+        for (; qi + 4 < G; qi += 8) {
+          sa += exp2f(zc[r * TS + qi] - gm[qi]) * ginv[qi];
+          sb += exp2f(zc[r * TS + qi + 4] - gm[qi + 4]) * ginv[qi + 4];
+        }
+        if (qi < G) sa += exp2f(zc[r * TS + qi] - gm[qi]) * ginv[qi];
+      }
+      float sacc = sa + sb;
       sacc += __shfl_xor_sync(0xffffffffu, sacc, 1);
       sacc += __shfl_xor_sync(0xffffffffu, sacc, 2);
       if (r < rows && sub == 0) {
@@ -775,55 +785,40 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       const bool final_gather = j == 0 && p.gather_all;
       const bool qa = lane < G, qb = lane + 32 < G;
       const int la = qa ? lane : 0, lb = qb ? lane + 32 : 0;
-      // Leaf sum of t for candidate row `row` (times TS), query q.
-      auto leaf_sum = [&](int64_t row, int q) {
+      // Leaf sum of t for candidate row offset `row` (row index * TS), query q.
+      auto leaf_sum = [&](int row, int q) {
         float a = 0.f;
 #pragma unroll 1
         for (int i = 0; i < leaves; ++i) a += t[row + i * TS + q];
         return a;
       };
       float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
-      for (int ci0 = warp * 4; ci0 < n_cand; ci0 += kWarps * 4) {
-        float za[4], zb[4];
+      for (int ci0 = warp * 8; ci0 < n_cand; ci0 += kWarps * 8) {
+        int rows[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) rows[u] = cr[min(ci0 + u, n_cand - 1)] * TS;
+        float z[8];
         if (leaves == 1) {
-          int64_t rows[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) rows[u] = static_cast<int64_t>(cr[min(ci0 + u, n_cand - 1)]) * TS;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            za[u] = t[rows[u] + la];
-            zb[u] = t[rows[u] + lb];
-          }
+          for (int u = 0; u < 8; ++u) z[u] = t[rows[u] + la];
         } else {
 #pragma unroll 1
-          for (int u = 0; u < 4; ++u) {
-            const int64_t row = static_cast<int64_t>(cr[min(ci0 + u, n_cand - 1)]) * TS;
-            za[u] = leaf_sum(row, la);
-            zb[u] = leaf_sum(row, lb);
+          for (int u = 0; u < 8; ++u) z[u] = leaf_sum(rows[u], la);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) z[u] = ci0 + u < n_cand && qa ? z[u] * sc2 : -INFINITY;
+        online8(m0, l0, z);
+        if (G > 32) {  // queries 32..63
+          if (leaves == 1) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) z[u] = t[rows[u] + lb];
+          } else {
+#pragma unroll 1
+            for (int u = 0; u < 8; ++u) z[u] = leaf_sum(rows[u], lb);
           }
-        }
-        float cm0 = m0, cm1 = m1;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const bool ok = ci0 + u < n_cand;
-          za[u] = ok && qa ? za[u] * sc2 : -INFINITY;
-          zb[u] = ok && qb ? zb[u] * sc2 : -INFINITY;
-          cm0 = fmaxf(cm0, za[u]);
-          cm1 = fmaxf(cm1, zb[u]);
-        }
-        if (cm0 != -INFINITY) {
-          float acc = l0 * safe_exp2_diff(m0, cm0);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) acc += safe_exp2_diff(za[u], cm0);
-          l0 = acc;
-          m0 = cm0;
-        }
-        if (cm1 != -INFINITY) {
-          float acc = l1 * safe_exp2_diff(m1, cm1);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) acc += safe_exp2_diff(zb[u], cm1);
-          l1 = acc;
-          m1 = cm1;
+          for (int u = 0; u < 8; ++u) z[u] = ci0 + u < n_cand && qb ? z[u] * sc2 : -INFINITY;
+          online8(m1, l1, z);
         }
       }
       part_m[warp * kMaxQ + lane] = m0;
@@ -839,22 +834,24 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       }
       __syncthreads();
       cluster_merge_stats(loc_m, loc_l, G, stat_in, gm, ginv, n_cand, final_gather ? cnt_b : nullptr);
-      // Pass B: one thread per candidate (odd row pitch: conflict-free).
+      // Pass B: one thread per candidate (odd row pitch: conflict-free);
+      // four independent partial sums over the queries.
       for (int ci = tid; ci < n_cand; ci += kThreads) {
-        const int64_t row = static_cast<int64_t>(cr[ci]) * TS;
-        float sa = 0.f, sb = 0.f;
+        const int row = cr[ci] * TS;
+        float sq[4] = {0.f, 0.f, 0.f, 0.f};
         if (leaves == 1) {
-#pragma unroll 4
-          for (int q = 0; q + 1 < G; q += 2) {
-            sa += exp2f(t[row + q] * sc2 - gm[q]) * ginv[q];
-            sb += exp2f(t[row + q + 1] * sc2 - gm[q + 1]) * ginv[q + 1];
+          int q = 0;
+#pragma unroll 2
+          for (; q + 4 <= G; q += 4) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) sq[k] += exp2f(t[row + q + k] * sc2 - gm[q + k]) * ginv[q + k];
           }
-          if (G & 1) sa += exp2f(t[row + G - 1] * sc2 - gm[G - 1]) * ginv[G - 1];
+          for (; q < G; ++q) sq[0] += exp2f(t[row + q] * sc2 - gm[q]) * ginv[q];
         } else {
 #pragma unroll 1
-          for (int q = 0; q < G; ++q) sa += exp2f(leaf_sum(row, q) * sc2 - gm[q]) * ginv[q];
+          for (int q = 0; q < G; ++q) sq[q & 3] += exp2f(leaf_sum(row, q) * sc2 - gm[q]) * ginv[q];
         }
-        keys[ci] = __float_as_uint(sa + sb);
+        keys[ci] = __float_as_uint((sq[0] + sq[1]) + (sq[2] + sq[3]));
       }
       __syncthreads();
       if (final_gather) {
