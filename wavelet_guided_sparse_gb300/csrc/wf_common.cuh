@@ -472,12 +472,23 @@ __device__ __forceinline__ void warp_find_digit(const uint32_t* h, const uint32_
 
 // Writes out[slot - lo] = i for every selected key i whose rank among the
 // selected (ascending index) falls in [lo, hi).
+// Zeroes the histograms of block_select_topk (block-wide, no barrier); a
+// caller may do this ahead of time, off its critical path.
+__device__ __forceinline__ void topk_zero(TopkSmem& sm) {
+  for (int b = threadIdx.x; b < 3 * 2048; b += kThreads) (&sm.hist[0][0])[b] = 0;
+  if (threadIdx.x < 3 * 32) (&sm.region[0][0])[threadIdx.x] = 0;
+}
+
+// `prezeroed`: the histograms were zeroed (topk_zero, followed by a barrier)
+// since their last use.
 static __device__ __noinline__ void block_select_topk(const uint32_t* keys, int n, int k, int lo_slot,
-                                               int hi_slot, int32_t* out, TopkSmem& sm) {
+                                               int hi_slot, int32_t* out, TopkSmem& sm,
+                                               bool prezeroed = false) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int b = tid; b < 3 * 2048; b += kThreads) (&sm.hist[0][0])[b] = 0;
-  if (tid < 3 * 32) (&sm.region[0][0])[tid] = 0;
-  __syncthreads();
+  if (!prezeroed) {
+    topk_zero(sm);
+    __syncthreads();
+  }
   uint32_t prefix = 0, pmask = 0;
   int need = k;
 #pragma unroll 1

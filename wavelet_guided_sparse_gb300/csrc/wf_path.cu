@@ -330,14 +330,14 @@ __device__ __forceinline__ float safe_exp2_diff(float m, float mx) {
 }
 
 // Prompt row of key slot g (g < B) of this unit, or -1 if out of range.
-__device__ __forceinline__ int prompt_row(const PathParams& p, const Ctx& c, const int32_t* klist,
-                                          int k0, int g) {
-  const int row = (p.mode & kModeFilter) ? klist[g - k0] : __ldg(p.idx_in + c.unit * p.budget + g);
+__device__ __forceinline__ int prompt_row(const PathParams& p, int mode, const Ctx& c,
+                                          const int32_t* klist, int k0, int g) {
+  const int row = (mode & kModeFilter) ? klist[g - k0] : __ldg(p.idx_in + c.unit * p.budget + g);
   return (row >= 0 && row < p.n_prompt) ? row : -1;
 }
 
 // ============================================================== the kernel
-template <typename T, int D>
+template <typename T, int D, bool kFast>
 __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant__ PathParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   cg::cluster_group cluster = cg::this_cluster();
@@ -351,6 +351,13 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   const int tid = c.tid, lane = c.lane, warp = c.warp, cs = c.cs, rank = c.rank;
   const int64_t unit = c.unit;
   const int G = p.G, levels = p.levels;
+  // The single-launch step of the common case (fused step 1, every phase,
+  // gather-all final selection, token logits in shared memory) is its own
+  // instantiation with these decisions constant.
+  const int mode = kFast ? (kModeScore | kModeFilter | kModeAttend) : p.mode;
+  const bool fuse_dwt = kFast || p.fuse_dwt;
+  const bool gather_all = kFast || p.gather_all;
+  float* const t_ws = kFast ? nullptr : p.t_ws;
   const PathSmem<T, D> L(p);
   constexpr int RB = PathSmem<T, D>::kRowBytes;
   constexpr int RF = PathSmem<T, D>::kRowF;
@@ -389,9 +396,9 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   // bf16 logits tiles run on the tensor cores with accumulators in tensor
   // memory: 256 columns (at most four pieces of N <= 64 queries).
   constexpr uint32_t kTmemCols = 256;
-  const bool use_tmem = sizeof(T) == 2 && (p.mode & (kModeScore | kModeFilter)) != 0;
+  const bool use_tmem = sizeof(T) == 2 && (mode & (kModeScore | kModeFilter)) != 0;
   const int fuse_sr = kFuseStageBytes / (D * static_cast<int>(sizeof(T)));  // rows per stage
-  const int fuse_rows = p.fuse_dwt ? (p.per_cta_p << levels) : 0;
+  const int fuse_rows = fuse_dwt ? (p.per_cta_p << levels) : 0;
   const int fuse_nst = (fuse_rows + fuse_sr - 1) / fuse_sr;
   const unsigned char* fuse_src =
       reinterpret_cast<const unsigned char*>(static_cast<const T*>(p.kp)) +
@@ -407,15 +414,19 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   };
   int fuse_issued = min(kFuseStages, fuse_nst);
   if (tid == 0) {
-    if (p.fuse_dwt)
+    if (fuse_dwt)
       for (int i = 0; i < kFuseStages; ++i) mbar_init(&bars[i], 1);
     mbar_init(mma_bar, 1);
     fence_mbar_init();
-    if (p.fuse_dwt)
+    if (fuse_dwt)
       for (int st = 0; st < fuse_issued; ++st) fuse_issue(st);
   }
   __syncwarp();
   if (use_tmem && warp == 0) tmem_alloc(reinterpret_cast<uint32_t*>(misc + 7), kTmemCols);
+
+  // The Top-K histograms start zeroed (the first selection skips that step).
+  topk_zero(tk);
+  bool tk_clean = true;
 
   // Queries (input dtype, padded rows; rows >= G are zero), by cp.async: with
   // fused step 1 they land while the ring streams and are waited for just
@@ -434,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
     }
     cp_async_commit();
-    if (!p.fuse_dwt) cp_async_wait<0>();
+    if (!fuse_dwt) cp_async_wait<0>();
   }
   tc_fence_before();
   __syncthreads();
@@ -442,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   const uint32_t tmem = use_tmem ? static_cast<uint32_t>(misc[7]) : 0u;  // accumulator base
 
   // ================================================================ score
-  if (p.mode & kModeScore) {
+  if (mode & kModeScore) {
     // Each CTA scores P/cs coarse positions; the per-query statistics are
     // merged over the cluster, then every CTA receives all P scores and
     // selects locally (so every CTA knows the sorted coarse survivors).
@@ -461,12 +472,14 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
             ? nullptr
             : p.al_planes + (static_cast<int64_t>(unit) * 3 * p.P + static_cast<int64_t>(rank) * Pc) * D;
     bool z_ready = false;  // fused step 1 leaves the single chunk's logits in zc
-    if (p.fuse_dwt) {
+    if (fuse_dwt) {
       // Step 1: A_L[c] = 2^(-L/2) * (sum of the 2^L rows of span c), fp32,
-      // one thread per (span, 16-byte column chunk) of a stage (a stage holds
-      // whole spans), written straight into the tile operand layout.
-      constexpr int V = Elem<T>::kPer16B, C = D / V;
-      const int span_rows = 1 << levels;
+      // written straight into the tile operand layout.  Two threads per
+      // (span, 16-byte column chunk) of a stage (a stage holds whole spans):
+      // each sums half of the span's rows, one shuffle per value combines
+      // the halves, and each thread stores half of the chunk's values.
+      constexpr int V = Elem<T>::kPer16B, C = D / V, VH = V / 2;
+      const int half_rows = 1 << (levels - 1);
       bool aborted = false;
       for (int st = 0; st < fuse_issued; ++st) {
         // Every issued stage is waited for (bounded), even after a timeout,
@@ -478,29 +491,42 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         const unsigned char* buf = smem + L.s_ring + (st % kFuseStages) * kFuseStageBytes;
         const int rows_in = min(fuse_sr, fuse_rows - st * fuse_sr);
         const int span0 = (st * fuse_sr) >> levels;
-        for (int item = tid; item < (rows_in >> levels) * C; item += kThreads) {
+        const int n_half = 2 * (rows_in >> levels) * C;  // (span, chunk, half) items, even
+        for (int base = 0; base < n_half; base += kThreads) {  // whole warps iterate together
+          const int it = base + tid, item = it >> 1, h = it & 1;
+          const bool active = it < n_half;
           const int sl = item / C, ch = item % C;
           float acc[V];
 #pragma unroll
           for (int v = 0; v < V; ++v) acc[v] = 0.f;
-          const unsigned char* src = buf + static_cast<size_t>(sl << levels) * D * sizeof(T) + ch * 16;
+          if (active) {
+            const unsigned char* src =
+                buf + static_cast<size_t>((sl << levels) + h * half_rows) * D * sizeof(T) + ch * 16;
 #pragma unroll 8
-          for (int r = 0; r < span_rows; ++r) {
-            float f[V];
-            widen16(*reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * D * sizeof(T)),
-                    static_cast<const T*>(nullptr), f);
+            for (int r = 0; r < half_rows; ++r) {
+              float f[V];
+              widen16(*reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * D * sizeof(T)),
+                      static_cast<const T*>(nullptr), f);
 #pragma unroll
-            for (int v = 0; v < V; ++v) acc[v] += f[v];
+              for (int v = 0; v < V; ++v) acc[v] += f[v];
+            }
           }
+          float mine[VH];  // this thread's half of the chunk: values h * VH ..
+#pragma unroll
+          for (int v = 0; v < V; ++v) {
+            const float tot = acc[v] + __shfl_xor_sync(0xffffffffu, acc[v], 1);
+            if ((v >= VH) == (h == 1)) mine[v % VH] = tot * p.al_scale;
+          }
+          if (!active) continue;
           const int row = span0 + sl;
           if constexpr (sizeof(T) == 2) {
-            uint32_t w[3][V / 2];
+            uint32_t w[3][VH / 2];
 #pragma unroll
-            for (int v = 0; v < V; v += 2) {
+            for (int v = 0; v < VH; v += 2) {
               float hv[2], mv[2], lv[2];
 #pragma unroll
               for (int e2 = 0; e2 < 2; ++e2) {  // a = hi + mid + lo exactly (to 2^-25 relative)
-                const float a = acc[v + e2] * p.al_scale;
+                const float a = mine[v + e2];
                 hv[e2] = __bfloat162float(__float2bfloat16_rn(a));
                 const float r1 = a - hv[e2];
                 mv[e2] = __bfloat162float(__float2bfloat16_rn(r1));
@@ -512,12 +538,10 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
             }
 #pragma unroll
             for (int pl = 0; pl < 3; ++pl)
-              *reinterpret_cast<uint4*>(as + pl * kPlaneBytes + cm_offset(row, ch, D * 16)) =
-                  make_uint4(w[pl][0], w[pl][1], w[pl][2], w[pl][3]);
+              *reinterpret_cast<uint2*>(as + pl * kPlaneBytes + cm_offset(row, ch, D * 16) + h * 8) =
+                  make_uint2(w[pl][0], w[pl][1]);
           } else {
-            *reinterpret_cast<float4*>(as + row * RB + ch * 16) =
-                make_float4(acc[0] * p.al_scale, acc[1] * p.al_scale, acc[2] * p.al_scale,
-                            acc[3] * p.al_scale);
+            *reinterpret_cast<float2*>(as + row * RB + ch * 16 + h * 8) = make_float2(mine[0], mine[1]);
           }
         }
         __syncthreads();  // stage consumed
@@ -655,11 +679,12 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     }
     cluster.sync();  // every CTA holds all P scores
     // Exact Top-k_L over all coarse positions (ties: lower position first).
-    const bool to_filter = (p.mode & kModeFilter) != 0;
-    block_select_topk(keys_all, p.P, p.kL, 0, p.kL, sl_all, tk);
+    const bool to_filter = (mode & kModeFilter) != 0;
+    block_select_topk(keys_all, p.P, p.kL, 0, p.kL, sl_all, tk, tk_clean);
+    tk_clean = false;
     if (!to_filter && rank == 0)
       for (int i = tid; i < p.kL; i += kThreads) p.idx_l_out[unit * p.kL + i] = sl_all[i];
-  } else if (p.mode & kModeFilter) {
+  } else if (mode & kModeFilter) {
     // Coarse survivors from the caller: load, sort ascending, validate.
     const int kL = p.kL, P = p.P;
     for (int i = tid; i < p.sorted_cap; i += kThreads)
@@ -693,16 +718,16 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   }
 
   // ================================================================ filter
-  if (p.mode & kModeFilter) {
+  if (mode & kModeFilter) {
     const int kL = p.kL;
     const int s0 = static_cast<int>((static_cast<int64_t>(rank) * kL) / cs);
     const int s1 = static_cast<int>((static_cast<int64_t>(rank + 1) * kL) / cs);
     const int ns = s1 - s0;
     const int R = ns << levels;
     unsigned char* kst = smem + L.f_kst;
-    float* t = p.t_ws == nullptr
+    float* t = t_ws == nullptr
                    ? reinterpret_cast<float*>(smem + L.f_t)
-                   : p.t_ws + (static_cast<int64_t>(unit) * cs + rank) * p.rows_cap * TS;
+                   : t_ws + (static_cast<int64_t>(unit) * cs + rank) * p.rows_cap * TS;
     const T* kp = static_cast<const T*>(p.kp);
     const int ntiles = (R + kTileRows - 1) / kTileRows;
     constexpr int C16 = D * static_cast<int>(sizeof(T)) / 16;  // 16-byte chunks per row
@@ -727,6 +752,10 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     };
     const int FS = p.f_stages;
     for (int tl = 0; tl < FS && tl < ntiles; ++tl) issue(tl, tl);
+    if (!tk_clean) {  // while the key rows are in flight (the tile barriers order it)
+      topk_zero(tk);
+      tk_clean = true;
+    }
     if (ntiles <= FS && sizeof(T) == 2) {
       // Every tile is in flight: one wait, then one tensor-core pass over
       // all R rows (tiles sit back to back in the ring).
@@ -782,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       //  pass B  s_c = Σ_q 2^(z[c,q] - gm_q) * ginv_q, one thread per candidate.
       const int leaves = 1 << j;
       const float sc2 = p.scale[j] * kLog2e;
-      const bool final_gather = j == 0 && p.gather_all;
+      const bool final_gather = j == 0 && gather_all;
       const bool qa = lane < G, qb = lane + 32 < G;
       const int la = qa ? lane : 0, lb = qb ? lane + 32 : 0;
       // Leaf sum of t for candidate row offset `row` (row index * TS), query q.
@@ -872,11 +901,12 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         const int B = p.budget;
         const int a0 = key_slot_start(rank, cs, p.n_keys), a1 = key_slot_start(rank + 1, cs, p.n_keys);
         const int w0 = key_slot_start(rank, cs, B), w1 = key_slot_start(rank + 1, cs, B);
-        const bool attend = (p.mode & kModeAttend) != 0;
+        const bool attend = (mode & kModeAttend) != 0;
         // This CTA's slots of the key list: [a0, min(a1, B)).  klist first
         // receives candidate indices, then their token positions.
         const int b1 = min(a1, B);
-        block_select_topk(keys_all, n_all, B, a0, b1, klist, tk);
+        block_select_topk(keys_all, n_all, B, a0, b1, klist, tk, tk_clean);
+        tk_clean = false;
         for (int sl = a0 + tid; sl < b1; sl += kThreads) {
           const int pos = pos_all[klist[sl - a0]];
           klist[sl - a0] = pos;
@@ -890,6 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         break;
       }
       (void)cluster_select(keys, n_cand, p.k[j], take, tk);
+      tk_clean = false;
       n_surv = compact2(cp, cr, take, n_cand, sp, sr, tk.scan);
     }
     // Tokens of this CTA: sp[0, n_surv), ascending.
@@ -897,7 +928,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     int all;
     const int offset = cluster_excl_count(n_surv, cnt_a, &all);
     const int B = p.budget;
-    if (p.mode & kModeAttend) {
+    if (mode & kModeAttend) {
       for (int i = tid; i < n_surv; i += kThreads) {
         const int g = offset + i;
         if (g >= B) continue;
@@ -914,7 +945,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   }
 
   // ================================================================ attend
-  if (p.mode & kModeAttend) {
+  if (mode & kModeAttend) {
     const int B = p.budget, TK = p.tile_keys;
     const int k0 = key_slot_start(rank, cs, p.n_keys);
     const int k1 = key_slot_start(rank + 1, cs, p.n_keys);
@@ -929,9 +960,9 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     const T* vgp = static_cast<const T*>(p.vg) + unit * G * D;
     const T* kpp = static_cast<const T*>(p.kp) + unit * p.n_prompt * D;
     const T* vpp = static_cast<const T*>(p.vp) + unit * p.n_prompt * D;
-    if (!(p.mode & kModeFilter)) {  // report bad caller indices of this slot range
+    if (!(mode & kModeFilter)) {  // report bad caller indices of this slot range
       for (int g = k0 + tid; g < min(k1, B); g += kThreads)
-        if (prompt_row(p, c, klist, k0, g) < 0) raise_flag(p.status, WF_DEV_BAD_INDEX);
+        if (prompt_row(p, mode, c, klist, k0, g) < 0) raise_flag(p.status, WF_DEV_BAD_INDEX);
     }
     // Every slot of a tile is filled (invalid slots with a finite dummy row),
     // so masked probabilities multiply finite values.
@@ -948,7 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
             ks = kgp + static_cast<int64_t>(g - B) * D;
             vs = vgp + static_cast<int64_t>(g - B) * D;
           } else {
-            const int row = prompt_row(p, c, klist, k0, g);
+            const int row = prompt_row(p, mode, c, klist, k0, g);
             if (row >= 0) {
               ks = kpp + static_cast<int64_t>(row) * D;
               vs = vpp + static_cast<int64_t>(row) * D;
@@ -968,7 +999,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     auto valid = [&](int g) -> bool {
       if (g >= k1) return false;
       if (g >= B) return true;
-      return prompt_row(p, c, klist, k0, g) >= 0;
+      return prompt_row(p, mode, c, klist, k0, g) >= 0;
     };
 
     if constexpr (sizeof(T) == 2) {
@@ -1237,7 +1268,10 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
 
 template <typename T, int D>
 cudaError_t launch_typed(int64_t units, const PathParams& prm, size_t smem, cudaStream_t stream) {
-  const cudaError_t e = ensure_max_smem<path_kernel<T, D>>();
+  const bool fast = prm.mode == (kModeScore | kModeFilter | kModeAttend) && prm.fuse_dwt &&
+                    prm.gather_all && prm.t_ws == nullptr;
+  const cudaError_t e = fast ? ensure_max_smem<path_kernel<T, D, true>>()
+                             : ensure_max_smem<path_kernel<T, D, false>>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(prm.cs, static_cast<unsigned>(units), 1);
@@ -1251,7 +1285,8 @@ cudaError_t launch_typed(int64_t units, const PathParams& prm, size_t smem, cuda
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, path_kernel<T, D>, prm);
+  return fast ? cudaLaunchKernelEx(&cfg, path_kernel<T, D, true>, prm)
+              : cudaLaunchKernelEx(&cfg, path_kernel<T, D, false>, prm);
 }
 
 size_t smem_bytes(const LaunchDims& ld, const PathParams& p) {
