@@ -94,7 +94,8 @@ struct PathSmem {
   size_t total;
   __host__ __device__ explicit PathSmem(const PathParams& p) {
     size_t o = 0;
-    auto take_bytes = [&](size_t bytes) {
+    auto take_bytes = [&](size_t bytes, size_t align = 16) {
+      o = (o + align - 1) & ~(align - 1);
       const size_t at = o;
       o = (o + bytes + 15) & ~size_t(15);
       return at;
@@ -127,7 +128,7 @@ struct PathSmem {
       // overwrite the ring once every stage has been consumed.
       o = u;
       s_ring = take_bytes(static_cast<size_t>(kFuseStages) * kFuseStageBytes);
-      s_as = take_bytes((sizeof(T) == 2 ? 3 : 1) * kScoreChunk * kRowBytes);
+      s_as = take_bytes((sizeof(T) == 2 ? 3 : 1) * kScoreChunk * kRowBytes, 1024);
       s_stage = s_z = s_ring;
       end = end > o ? end : o;
     } else if (p.mode & kModeScore) {
@@ -137,7 +138,7 @@ struct PathSmem {
       // bf16: the logits overwrite the staged fp32 rows once the planes exist.
       s_stage = take_bytes(sizeof(float) * kScoreChunk * kRowF);
       if (sizeof(T) == 2) {
-        s_as = take_bytes(3 * kScoreChunk * kRowBytes);
+        s_as = take_bytes(3 * kScoreChunk * kRowBytes, 1024);
         s_z = s_stage;
       } else {
         s_as = s_stage;
@@ -147,7 +148,7 @@ struct PathSmem {
     }
     if (p.mode & kModeFilter) {
       o = u;
-      f_kst = take_bytes(static_cast<size_t>(p.f_stages) * kTileRows * kRowBytes);
+      f_kst = take_bytes(static_cast<size_t>(p.f_stages) * kTileRows * kRowBytes, 1024);
       sp = take_bytes(sizeof(int32_t) * p.rows_cap);  // survivor / candidate lists
       sr = take_bytes(sizeof(int32_t) * p.rows_cap);
       cp = take_bytes(sizeof(int32_t) * p.rows_cap);
@@ -205,8 +206,9 @@ __device__ __forceinline__ TopkResult cluster_select(const uint32_t* keys, int n
 // bf16 logits tile on the fifth-generation tensor cores:
 //   out[(row0 + r) * pitch + q] = scale * Σ_planes Σ_k A_p[r][k] * Q[q][k]
 // for r < rows and q < G.  A (nplanes planes plane_bytes apart, summed: one
-// plane for key rows; hi + mid + lo planes reproduce an fp32 row exactly) and
-// Q are bf16 in the core-matrix layout (8-row groups 16 * D bytes apart).
+// plane for key rows; hi + mid + lo planes reproduce an fp32 row exactly) is
+// bf16 in the 128-byte-swizzled layout with m_alloc rows per column block;
+// Q is bf16 in the core-matrix layout (8-row groups 16 * D bytes apart).
 // The rows go in 128-row (M = 128) pieces, then 64-row (M = 64) pieces, each
 // into its own tensor-memory accumulator of N = G rounded up to 16 columns;
 // one thread issues every MMA, one commit signals `bar`, and the warps read
@@ -216,9 +218,10 @@ __device__ __forceinline__ TopkResult cluster_select(const uint32_t* keys, int n
 // the same `phase` count of completed commits on `bar`.
 template <int D>
 __device__ __noinline__ void umma_logits(const unsigned char* a, int nplanes, int plane_bytes,
-                                         int rows, const unsigned char* qs, int G, float* out,
-                                         int row0, int pitch, float scale, uint32_t tmem,
-                                         uint64_t* bar, uint32_t& phase, int32_t* status) {
+                                         int m_alloc, int rows, const unsigned char* qs, int G,
+                                         float* out, int row0, int pitch, float scale,
+                                         uint32_t tmem, uint64_t* bar, uint32_t& phase,
+                                         int32_t* status) {
   constexpr int SBO = D * 16;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int N = (G + 15) & ~15;
@@ -235,7 +238,8 @@ __device__ __noinline__ void umma_logits(const unsigned char* a, int nplanes, in
       for (int pl = 0; pl < nplanes; ++pl)
         for (int ks = 0; ks < D / 16; ++ks)
           umma_bf16(tmem + piece * N,
-                    umma_desc(a0 + pl * plane_bytes + (r0 >> 3) * SBO + ks * 256, 128, SBO),
+                    umma_desc_sw128(a0 + pl * plane_bytes + ((ks * 16) >> 6) * (m_alloc * 128) +
+                                    (r0 >> 3) * 1024 + ((ks * 16) & 63) * 2),
                     umma_desc(q0 + ks * 256, 128, SBO), idesc, (pl | ks) != 0);
     }
     umma_commit(bar);
@@ -339,7 +343,7 @@ __device__ __forceinline__ int prompt_row(const PathParams& p, int mode, const C
 // ============================================================== the kernel
 template <typename T, int D, bool kFast>
 __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant__ PathParams p) {
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem[];  // swizzled operands need 1024
   cg::cluster_group cluster = cg::this_cluster();
   Ctx c;
   c.cs = static_cast<int>(cluster.num_blocks());
@@ -538,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
             }
 #pragma unroll
             for (int pl = 0; pl < 3; ++pl)
-              *reinterpret_cast<uint2*>(as + pl * kPlaneBytes + cm_offset(row, ch, D * 16) + h * 8) =
+              *reinterpret_cast<uint2*>(as + pl * kPlaneBytes + sw_offset(row, ch, kScoreChunk) + h * 8) =
                   make_uint2(w[pl][0], w[pl][1]);
           } else {
             *reinterpret_cast<float2*>(as + row * RB + ch * 16 + h * 8) = make_float2(mine[0], mine[1]);
@@ -555,8 +559,8 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       }
       cp_async_wait<0>();  // the queries
       if (sizeof(T) == 2) {
-        umma_logits<D>(as, 3, kPlaneBytes, Pc, qs, G, zc, 0, TS, zscale, tmem, mma_bar, mma_phase,
-                       p.status);
+        umma_logits<D>(as, 3, kPlaneBytes, kScoreChunk, Pc, qs, G, zc, 0, TS, zscale, tmem, mma_bar,
+                       mma_phase, p.status);
       } else {
         __syncthreads();
         logits_tile_f32<D>(as, reinterpret_cast<const float*>(qs), zc, 0, Pc, G, TS, zscale);
@@ -573,13 +577,13 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         for (int e = tid; e < 3 * rows * C8; e += kThreads) {
           const int pl = e / (rows * C8), rem = e - pl * rows * C8;
           const int r = rem / C8, ch = rem % C8;
-          cp_async16(as + pl * kPlaneBytes + cm_offset(r, ch, D * 16),
+          cp_async16(as + pl * kPlaneBytes + sw_offset(r, ch, kScoreChunk),
                      psrc + (static_cast<int64_t>(pl) * p.P + c0 + r) * D + ch * 8);
         }
         cp_async_commit();
         cp_async_wait<0>();
-        umma_logits<D>(as, 3, kPlaneBytes, rows, qs, G, zc, 0, TS, zscale, tmem, mma_bar, mma_phase,
-                       p.status);
+        umma_logits<D>(as, 3, kPlaneBytes, kScoreChunk, rows, qs, G, zc, 0, TS, zscale, tmem, mma_bar,
+                       mma_phase, p.status);
         __syncthreads();
         return;
       }
@@ -607,12 +611,12 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           }
 #pragma unroll
           for (int pl = 0; pl < 3; ++pl)
-            *reinterpret_cast<uint2*>(as + pl * kPlaneBytes + cm_offset(r, col / 8, D * 16) +
+            *reinterpret_cast<uint2*>(as + pl * kPlaneBytes + sw_offset(r, col / 8, kScoreChunk) +
                                       (col % 8) * 2) =
                 make_uint2(pack_bf16(pv[pl][0], pv[pl][1]), pack_bf16(pv[pl][2], pv[pl][3]));
         }
-        umma_logits<D>(as, 3, kPlaneBytes, rows, qs, G, zc, 0, TS, zscale, tmem, mma_bar, mma_phase,
-                       p.status);
+        umma_logits<D>(as, 3, kPlaneBytes, kScoreChunk, rows, qs, G, zc, 0, TS, zscale, tmem, mma_bar,
+                       mma_phase, p.status);
       } else {
         logits_tile_f32<D>(as, reinterpret_cast<const float*>(qs), zc, 0, rows, G, TS, zscale);
       }
@@ -731,7 +735,10 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     const T* kp = static_cast<const T*>(p.kp);
     const int ntiles = (R + kTileRows - 1) / kTileRows;
     constexpr int C16 = D * static_cast<int>(sizeof(T)) / 16;  // 16-byte chunks per row
-    constexpr int kStageB = sizeof(T) == 2 ? kTileRows * D * 2 : kTileRows * RB;  // ring stage
+    // Offset of a ring stage: bf16, rows of the 128-byte-swizzled layout
+    // (column blocks of FS * kTileRows rows); fp32, padded rows.
+    constexpr int kStageB = sizeof(T) == 2 ? kTileRows * 128 : kTileRows * RB;
+    const int FS = p.f_stages;
     auto issue = [&](int tile, int stage) {  // all threads; one cp.async group
       const int r0 = tile * kTileRows;
       const int nr = min(kTileRows, R - r0);
@@ -744,13 +751,12 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         // bf16: core-matrix layout, stages back to back (a tensor-core
         // operand may span stages); fp32: padded rows.
         unsigned char* dst = sizeof(T) == 2
-                                 ? kst + stage * kStageB + cm_offset(i, ch, D * 16)
+                                 ? kst + sw_offset(stage * kTileRows + i, ch, FS * kTileRows)
                                  : kst + (stage * kTileRows + i) * RB + ch * 16;
         cp_async16(dst, reinterpret_cast<const unsigned char*>(kp + grow * D) + ch * 16);
       }
       cp_async_commit();
     };
-    const int FS = p.f_stages;
     for (int tl = 0; tl < FS && tl < ntiles; ++tl) issue(tl, tl);
     if (!tk_clean) {  // while the key rows are in flight (the tile barriers order it)
       topk_zero(tk);
@@ -760,7 +766,8 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       // Every tile is in flight: one wait, then one tensor-core pass over
       // all R rows (tiles sit back to back in the ring).
       cp_async_wait<0>();
-      umma_logits<D>(kst, 1, 0, R, qs, G, t, 0, TS, 1.f, tmem, mma_bar, mma_phase, p.status);
+      umma_logits<D>(kst, 1, 0, FS * kTileRows, R, qs, G, t, 0, TS, 1.f, tmem, mma_bar, mma_phase,
+                     p.status);
       __syncthreads();
     } else
     for (int tile = 0; tile < ntiles; ++tile) {
@@ -768,8 +775,8 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       cp_async_wait_pending(min(ntiles, tile + FS) - 1 - tile);
       const int rows_valid = min(kTileRows, R - tile * kTileRows);
       if constexpr (sizeof(T) == 2) {
-        umma_logits<D>(kst + stage * kStageB, 1, 0, rows_valid, qs, G, t, tile * kTileRows, TS,
-                       1.f, tmem, mma_bar, mma_phase, p.status);
+        umma_logits<D>(kst + stage * kStageB, 1, 0, FS * kTileRows, rows_valid, qs, G, t,
+                       tile * kTileRows, TS, 1.f, tmem, mma_bar, mma_phase, p.status);
       } else {
         __syncthreads();
         logits_tile_f32<D>(kst + stage * kStageB, reinterpret_cast<const float*>(qs), t,

@@ -3,7 +3,9 @@
 // bf16 MMA with an fp32 accumulator in tensor memory, its completion signal
 // and the accumulator read-back.
 //
-// Operand layout used throughout ("core-matrix" K-major layout, no swizzle):
+// Operand layouts: the queries use the "core-matrix" K-major layout without
+// swizzle; the A operands use its 128-byte-swizzled form (sw_offset below).
+// Core-matrix layout:
 // a matrix of R rows x K bf16 values is stored as 8-row x 16-byte core
 // matrices; element (r, k) sits at byte
 //     (r / 8) * sbo + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2,
@@ -22,6 +24,17 @@ namespace wf {
 // Byte offset of row r, 16-byte chunk ch in the core-matrix layout.
 __device__ __forceinline__ uint32_t cm_offset(int r, int ch, int sbo) {
   return static_cast<uint32_t>((r >> 3) * sbo + ch * 128 + (r & 7) * 16);
+}
+
+// 128-byte-swizzled K-major layout (the MMA A operands written row by row):
+// K is cut into 64-element (128-byte) column blocks of m_alloc rows each,
+// 128 bytes per row, 8-row groups 1024 bytes apart, and the 16-byte chunk c
+// of row r sits at chunk position c ^ (r % 8) of its 128-byte line.  The
+// eight chunks of a row half therefore fill one line: row-wise stores are
+// free of bank conflicts.  The region must start on a 1024-byte boundary.
+__device__ __forceinline__ uint32_t sw_offset(int r, int ch, int m_alloc) {
+  return static_cast<uint32_t>((ch >> 3) * (m_alloc * 128) + (r >> 3) * 1024 + (r & 7) * 128 +
+                               (((ch & 7) ^ (r & 7)) << 4));
 }
 
 // ---------------------------------------------------------------- tensor memory
@@ -55,6 +68,13 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint
   return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
          (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+// Descriptor of the 128-byte-swizzled K-major layout (swizzle mode 2,
+// stride byte offset 1024, leading byte offset unused); a K step inside a
+// 128-byte line advances the start address by 2 bytes per element.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (1ull << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 // Instruction descriptor of kind::f16: bf16 A and B (both K-major), fp32
 // accumulator, M x N tile (M = 64 or 128; N a multiple of 8 (M = 64) or 16).
