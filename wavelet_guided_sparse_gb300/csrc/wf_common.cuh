@@ -257,6 +257,16 @@ static __device__ __noinline__ void cluster_merge_stats(const float* loc_m, cons
   __syncthreads();
 }
 
+// Split cluster barrier: every thread arrives once early (relaxed, no
+// ordering) and waits later, e.g. so that no CTA touches a peer's shared
+// memory before every CTA of the cluster has started.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ cluster Top-K
 //
 // Exact selection of the k largest 32-bit keys spread over the CTAs of a

@@ -162,7 +162,7 @@ struct PathSmem {
       o = u;
       const size_t stage = static_cast<size_t>(p.a_stages) * p.tile_keys * kRowBytes;
       if (sizeof(T) == 2) {  // warp partials overwrite the stages after the last tile
-        const size_t work = sizeof(float) * (kWarps * 16 * D + 2 * kWarps * 16);
+        const size_t work = sizeof(float) * (kWarps * 16 * D + 2 * kWarps * 16 + kMaxQ * kWarps);
         a_kst = o;
         a_vst = o + stage;
         a_work = o;
@@ -391,6 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   int32_t* pos_all = reinterpret_cast<int32_t*>(smem + L.pos_all);
   int32_t* klist = reinterpret_cast<int32_t*>(smem + L.klist);
 
+  cluster_arrive_relaxed();  // waited for after the prologue, before any peer access
+
   // Fused step 1: this CTA's K_p rows (the spans of its per_cta_p coarse
   // positions, one contiguous byte range) stream through a ring of bulk
   // copies; the first stages are in flight before anything else happens.
@@ -455,6 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = use_tmem ? static_cast<uint32_t>(misc[7]) : 0u;  // accumulator base
+  cluster_wait();  // every CTA of the cluster has started: shared memory may be shared
 
   // ================================================================ score
   if (mode & kModeScore) {
@@ -1122,32 +1125,43 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         mpart[warp * 16 + r_lo + 8] = m_hi;
         lpart[warp * 16 + r_lo + 8] = l_hi;
       }
-      // Every CTA must be past its filter phase (whose buffers share bytes
-      // with the receive area) before partials are pushed.
-      cluster.sync();
-      // CTA partial of row qi, pushed straight to the CTA that finalises it.
+      // The receive area shares no bytes with what peers still use (their
+      // selection is complete and their own stages lie below it), so only
+      // this CTA's partials need a barrier.
+      __syncthreads();
+      // Per query row: the CTA max, the weights 2^(m_w - max) of the key-group
+      // warps and the weighted sum; (max, sum) go straight to the row's owner.
       const int KGW = kWarps / MB;
-      for (int e = tid; e < G * (D / 4); e += kThreads) {
-        const int qi = e / (D / 4), col = (e % (D / 4)) * 4;
-        const int qmb = qi >> 4, r = qi & 15;
+      float* wts = lpart + kWarps * 16;  // [G][KGW]
+      if (tid < G) {
+        const int qi = tid, qmb = qi >> 4, r = qi & 15;
         float mx = -INFINITY;
         for (int g = 0; g < KGW; ++g) mx = fmaxf(mx, mpart[(qmb + MB * g) * 16 + r]);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         float l = 0.f;
         for (int g = 0; g < KGW; ++g) {
           const int w = qmb + MB * g;
           const float f = safe_exp2_diff(mpart[w * 16 + r], mx);
-          const float4 v = *reinterpret_cast<const float4*>(opart + (w * 16 + r) * D + col);
-          acc.x += f * v.x; acc.y += f * v.y; acc.z += f * v.z; acc.w += f * v.w;
+          wts[qi * KGW + g] = f;
           l += f * lpart[w * 16 + r];
         }
         const int owner = qi / rpo, ro = qi - owner * rpo;
-        *reinterpret_cast<float4*>(peer(recv_o, owner) + (rank * rpo + ro) * D + col) = acc;
-        if (col == 0) {
-          float* dst = peer(recv_ml, owner) + (rank * rpo + ro) * 2;
-          dst[0] = mx;
-          dst[1] = l;
+        float* dst = peer(recv_ml, owner) + (rank * rpo + ro) * 2;
+        dst[0] = mx;
+        dst[1] = l;
+      }
+      __syncthreads();
+      // CTA partial of row qi, pushed straight to the CTA that finalises it.
+      for (int e = tid; e < G * (D / 4); e += kThreads) {
+        const int qi = e / (D / 4), col = (e % (D / 4)) * 4;
+        const int qmb = qi >> 4, r = qi & 15;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int g = 0; g < KGW; ++g) {
+          const float f = wts[qi * KGW + g];
+          const float4 v = *reinterpret_cast<const float4*>(opart + ((qmb + MB * g) * 16 + r) * D + col);
+          acc.x += f * v.x; acc.y += f * v.y; acc.z += f * v.z; acc.w += f * v.w;
         }
+        const int owner = qi / rpo, ro = qi - owner * rpo;
+        *reinterpret_cast<float4*>(peer(recv_o, owner) + (rank * rpo + ro) * D + col) = acc;
       }
     } else {
       // ------------------------------------------------ fp32 FMA path
@@ -1231,7 +1245,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         __syncthreads();
         if (tile + AS < ntiles) issue(tile + AS, stage);
       }
-      cluster.sync();  // peers are past their filter phase (shared receive area)
+      __syncthreads();  // the receive area shares no bytes with what peers still use
       const int c4 = tid % C4, qg = tid / C4;
 #pragma unroll
       for (int i = 0; i < QPT; ++i) {
@@ -1248,20 +1262,25 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       }
     }
     cluster.sync();
-    // Finalise this CTA's query rows [rank * rpo, ...): merge the cs partials.
+    // Finalise this CTA's query rows [rank * rpo, ...): merge the cs partials,
+    // four output columns per thread.
     const int q0 = rank * rpo, q1 = min(G, q0 + rpo);
-    for (int e = tid; e < (q1 - q0) * D; e += kThreads) {
-      const int ro = e / D, col = e % D;
+    for (int e = tid; e < (q1 - q0) * (D / 4); e += kThreads) {
+      const int ro = e / (D / 4), col = (e % (D / 4)) * 4;
       float mx = -INFINITY;
       for (int r = 0; r < cs; ++r) mx = fmaxf(mx, recv_ml[(r * rpo + ro) * 2]);
-      float acc = 0.f, l = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float l = 0.f;
       for (int r = 0; r < cs; ++r) {
         const float f = safe_exp2_diff(recv_ml[(r * rpo + ro) * 2], mx);
-        acc += f * recv_o[(r * rpo + ro) * D + col];
+        const float4 v = *reinterpret_cast<const float4*>(recv_o + (r * rpo + ro) * D + col);
+        acc.x += f * v.x; acc.y += f * v.y; acc.z += f * v.z; acc.w += f * v.w;
         l += f * recv_ml[(r * rpo + ro) * 2 + 1];
       }
+      const float inv = 1.f / l;
       const int qi = q0 + ro;
-      p.o[(unit * G + qi) * D + col] = acc / l;
+      *reinterpret_cast<float4*>(p.o + (unit * G + qi) * D + col) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
       if (col == 0 && p.lse != nullptr) p.lse[unit * G + qi] = (mx + log2f(l)) * kLn2;
     }
   }
