@@ -44,10 +44,11 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture
 # of the 4096-token layer (profiles/), valid while the kernel sources hash to
 # source_sha.
-DWT_TRAFFIC = {"sources": ("wf_dwt.cu",), "source_sha": "24a89596d1f42558",
-               "bytes_per_launch": 33571840}  # 33.57 MB read + 0 B written
-PATH_TRAFFIC = {"sources": ("wf_path.cu", "wf_common.cuh", "wf_mma.cuh"), "source_sha": None,
-                "bytes_per_launch": None}
+DWT_TRAFFIC = {"sources": ("wf_dwt.cu",), "source_sha": "2ddcb5bc05b588dc",
+               "bytes_per_launch": 33577984}  # 33.58 MB read + 0 B written (A_L stays in L2)
+PATH_TRAFFIC = {"sources": ("wf_path.cu", "wf_common.cuh", "wf_mma.cuh", "wf_umma.cuh"),
+                "source_sha": "1cc49183e15607ec",
+                "bytes_per_launch": 38677248}  # 38.67 MB read + 5.4 KB written
 
 
 def _rank_env():
