@@ -35,6 +35,8 @@
 #include <climits>
 #include <cmath>
 
+#include <cuda.h>
+
 #include "wf_common.cuh"
 #include "wf_internal.h"
 #include "wf_mma.cuh"
@@ -55,6 +57,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 enum : int { kModeScore = 1, kModeFilter = 2, kModeAttend = 4 };
 
 struct PathParams {
+  // K_p as a 2-D tensor [units * N_p rows, d columns] for tensor copies of whole
+  // spans (box: 64 columns x 2^L rows, 128-byte swizzle); valid if use_tma_spans.
+  alignas(64) CUtensorMap tmap_spans;
+  int use_tma_spans;
   const void* q;
   const void* kp;
   const void* vp;
@@ -109,7 +115,7 @@ struct PathSmem {
     cnt_a = take_bytes(sizeof(int32_t) * kMaxCluster);
     cnt_b = take_bytes(sizeof(int32_t) * kMaxCluster);
     misc = take_bytes(sizeof(int32_t) * 8);
-    bars = take_bytes(sizeof(uint64_t) * (kFuseStages + 1));  // ring stages + tensor-core commits
+    bars = take_bytes(sizeof(uint64_t) * (kFuseStages + 2));  // ring, tensor-core commits, span copies
     sl_all = take_bytes(sizeof(int32_t) * p.sorted_cap);
     topk = take_bytes(sizeof(TopkSmem));
     // All-gathered keys: the P coarse scores, and (final level, gather mode)
@@ -162,7 +168,7 @@ struct PathSmem {
       o = u;
       const size_t stage = static_cast<size_t>(p.a_stages) * p.tile_keys * kRowBytes;
       if (sizeof(T) == 2) {  // warp partials overwrite the stages after the last tile
-        const size_t work = sizeof(float) * (kWarps * 16 * D + 2 * kWarps * 16 + kMaxQ * kWarps);
+        const size_t work = sizeof(float) * (kWarps * 16 * (D + 8) + 2 * kWarps * 16 + kMaxQ * kWarps);
         a_kst = o;
         a_vst = o + stage;
         a_work = o;
@@ -398,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   // copies; the first stages are in flight before anything else happens.
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* mma_bar = bars + kFuseStages;  // tensor-core commits (phase count in mma_phase)
+  uint64_t* span_bar = bars + kFuseStages + 1;  // tensor copies of the filter's span rows (one use)
   uint32_t mma_phase = 0;
   // bf16 logits tiles run on the tensor cores with accumulators in tensor
   // memory: 256 columns (at most four pieces of N <= 64 queries).
@@ -423,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     if (fuse_dwt)
       for (int i = 0; i < kFuseStages; ++i) mbar_init(&bars[i], 1);
     mbar_init(mma_bar, 1);
+    mbar_init(span_bar, 1);
     fence_mbar_init();
     if (fuse_dwt)
       for (int st = 0; st < fuse_issued; ++st) fuse_issue(st);
@@ -760,15 +768,33 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       }
       cp_async_commit();
     };
-    for (int tl = 0; tl < FS && tl < ntiles; ++tl) issue(tl, tl);
+    // bf16 with every row in the ring at once: one tensor copy per (span,
+    // 64-column block) lands the span's 2^L rows straight in the swizzled
+    // operand layout (8-row groups, so 2^L >= 8); otherwise 16-byte cp.async.
+    const bool tma_spans = sizeof(T) == 2 && p.use_tma_spans && ntiles <= FS;
+    if (tma_spans) {
+      constexpr int KB = D / 64;  // 64-column blocks per row
+      if (tid == 0) mbar_arrive_expect_tx(span_bar, static_cast<uint32_t>(R) * D * sizeof(T));
+      for (int i = tid; i < ns * KB; i += kThreads) {
+        const int sp_i = i / KB, kb = i - sp_i * KB;
+        tma_load_2d(kst + kb * (FS * kTileRows * 128) + ((sp_i << levels) >> 3) * 1024,
+                    &p.tmap_spans, kb * 64,
+                    static_cast<int>(unit * p.n_prompt + (sl_all[s0 + sp_i] << levels)), span_bar);
+      }
+    } else {
+      for (int tl = 0; tl < FS && tl < ntiles; ++tl) issue(tl, tl);
+    }
     if (!tk_clean) {  // while the key rows are in flight (the tile barriers order it)
       topk_zero(tk);
       tk_clean = true;
     }
     if (ntiles <= FS && sizeof(T) == 2) {
-      // Every tile is in flight: one wait, then one tensor-core pass over
-      // all R rows (tiles sit back to back in the ring).
-      cp_async_wait<0>();
+      // Every row is in flight: one wait, then one tensor-core pass over all
+      // R rows (tiles sit back to back in the ring).
+      if (tma_spans)
+        (void)mbar_wait_bounded(span_bar, 0, p.status);
+      else
+        cp_async_wait<0>();
       umma_logits<D>(kst, 1, 0, FS * kTileRows, R, qs, G, t, 0, TS, 1.f, tmem, mma_bar, mma_phase,
                      p.status);
       __syncthreads();
@@ -1106,17 +1132,20 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         if (tile + AS < ntiles) issue(tile + AS, stage);
       }
       // Warp partials -> shared memory (overwrites the stages).
-      float* opart = work;                    // [kWarps][16][D]
-      float* mpart = work + kWarps * 16 * D;  // [kWarps][16]
+      // Row pitch D + 8 floats: a warp's fragment stores (8 rows x 4 column
+      // pairs) hit distinct banks.
+      constexpr int OP = D + 8;
+      float* opart = work;                     // [kWarps][16][OP]
+      float* mpart = work + kWarps * 16 * OP;  // [kWarps][16]
       float* lpart = mpart + kWarps * 16;
       __syncthreads();
       const int r_lo = lane >> 2;
 #pragma unroll
       for (int dn = 0; dn < D / 8; ++dn) {
         const int col = dn * 8 + (lane & 3) * 2;
-        *reinterpret_cast<float2*>(opart + (warp * 16 + r_lo) * D + col) =
+        *reinterpret_cast<float2*>(opart + (warp * 16 + r_lo) * OP + col) =
             make_float2(oacc[dn][0], oacc[dn][1]);
-        *reinterpret_cast<float2*>(opart + (warp * 16 + r_lo + 8) * D + col) =
+        *reinterpret_cast<float2*>(opart + (warp * 16 + r_lo + 8) * OP + col) =
             make_float2(oacc[dn][2], oacc[dn][3]);
       }
       if ((lane & 3) == 0) {
@@ -1157,7 +1186,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int g = 0; g < KGW; ++g) {
           const float f = wts[qi * KGW + g];
-          const float4 v = *reinterpret_cast<const float4*>(opart + ((qmb + MB * g) * 16 + r) * D + col);
+          const float4 v = *reinterpret_cast<const float4*>(opart + ((qmb + MB * g) * 16 + r) * OP + col);
           acc.x += f * v.x; acc.y += f * v.y; acc.z += f * v.z; acc.w += f * v.w;
         }
         const int owner = qi / rpo, ro = qi - owner * rpo;
@@ -1313,6 +1342,45 @@ cudaError_t launch_typed(int64_t units, const PathParams& prm, size_t smem, cuda
   cfg.numAttrs = 1;
   return fast ? cudaLaunchKernelEx(&cfg, path_kernel<T, D, true>, prm)
               : cudaLaunchKernelEx(&cfg, path_kernel<T, D, false>, prm);
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once (no link-time
+// dependency on the driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static std::atomic<void*> cached{nullptr};
+  void* f = cached.load(std::memory_order_acquire);
+  if (f == nullptr) {
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || f == nullptr) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+    cached.store(f, std::memory_order_release);
+  }
+  return reinterpret_cast<EncodeTiledFn>(f);
+}
+
+// Tensor map of K_p [units * N_p rows, d columns] (bf16) with a box of 64
+// columns x 2^L rows and the 128-byte swizzle of the tensor-core operand
+// layout.  Returns false (and the kernel uses cp.async) if unavailable.
+bool encode_span_map(const LaunchDims& ld, const void* kp, CUtensorMap* map) {
+  if (ld.dtype != WF_BF16 || kp == nullptr || ld.levels < 3 || ld.levels > 8) return false;
+  const EncodeTiledFn enc = encode_tiled();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(ld.head_dim),
+                              static_cast<cuuint64_t>(ld.units) * ld.n_prompt};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld.head_dim) * 2};
+  const cuuint32_t box[2] = {64, 1u << ld.levels};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kp), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 size_t smem_bytes(const LaunchDims& ld, const PathParams& p) {
@@ -1484,6 +1552,8 @@ cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathAr
   p.f_stages = plan.f_stages;
   p.a_stages = plan.a_stages;
   p.fuse_dwt = plan.fuse_dwt;
+  p.use_tma_spans =
+      (plan.mode & kModeFilter) != 0 && encode_span_map(ld, a.kp, &p.tmap_spans) ? 1 : 0;
   p.al_scale = static_cast<float>(std::pow(2.0, -0.5 * ld.levels));  // 2^(-L/2)
   for (int j = 0; j <= ld.levels; ++j) {
     p.k[j] = a.k != nullptr ? a.k[j] : 0;

@@ -37,6 +37,19 @@ __device__ __forceinline__ uint32_t sw_offset(int r, int ch, int m_alloc) {
                                (((ch & 7) ^ (r & 7)) << 4));
 }
 
+// ---------------------------------------------------------------- tensor copies
+// 2-D tiled tensor copy global -> shared (TMA engine) of the box at column x,
+// row y of the tensor map (a __grid_constant__ kernel parameter), completion
+// counted in bytes on `bar`.  x * element size must be a multiple of 16.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ---------------------------------------------------------------- tensor memory
 // Allocates ncols (power of two, 32..512) columns of tensor memory for this
 // CTA; one whole warp executes it and the base address lands in *slot.
