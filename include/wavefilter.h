@@ -207,6 +207,24 @@ int wf_step(const wf_dims* dims, const void* Q, const void* Kp, const void* Vp,
             float* O, float* lse, int32_t* idx_out, void* workspace,
             size_t workspace_bytes, void* stream);
 
+/* wf_step reusing a level-L approximation computed at an earlier step: steps
+ * 2-5 only, without the stream over K_p.  Under a prefix cache the prompt
+ * keys K~[I_p] do not change between denoising steps (WaveFilter §3.1 reads
+ * them at step t-1; §1 describes extracting the frequency structure with the
+ * DWT at the initial step), so one wf_dwt_lowpass result serves every later
+ * step of the same cache.
+ *   AL : device, [U, N_p/2^L, d] fp32 — the AL output of wf_dwt_lowpass for
+ *        these Kp and levels (kept by the caller; not checked).
+ *   Everything else as wf_step; Kp is still read for the span rows of the
+ *   coarse survivors and the selected keys.
+ * Errors: as wf_step (WF_ERR_NULL if AL is NULL, WF_ERR_ALIGNMENT if it is
+ * not 16-byte aligned). */
+int wf_step_cached_al(const wf_dims* dims, const void* Q, const void* Kp,
+                      const void* Vp, const void* Kg, const void* Vg,
+                      const float* AL, const int32_t* k_per_level, float* O,
+                      float* lse, int32_t* idx_out, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
 /* wf_step with host-resident inputs and outputs: copies Q/Kp/Vp/Kg/Vg from
  * HOST memory into the caller's device staging buffers (one
  * cudaMemcpyAsync each), runs wf_step, and copies O (and lse if both

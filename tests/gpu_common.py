@@ -71,7 +71,8 @@ def compare_step_unit(arrs, b, h, levels, ks, gpu_idx, gpu_out, gpu_lse=None, re
     return kind
 
 
-def run_step(dev: dict, levels: int, ks, with_idx=True):
+def run_step(dev: dict, levels: int, ks, with_idx=True, al=None):
+    """wf_step, or (al given: A_L from an earlier wf_dwt_lowpass) wf_step_cached_al."""
     q = dev["Q"]
     dims = bd.make_dims(q, dev["Kp"], levels)
     ws = bd.alloc_workspace(dims, ks, q.device)
@@ -79,7 +80,11 @@ def run_step(dev: dict, levels: int, ks, with_idx=True):
     out = torch.empty((b, h, g, d), dtype=torch.float32, device=q.device)
     lse = torch.empty((b, h, g), dtype=torch.float32, device=q.device)
     idx = torch.empty((b, h, ks[0]), dtype=torch.int32, device=q.device) if with_idx else None
-    bd.step(dev["Q"], dev["Kp"], dev["Vp"], dev["Kg"], dev["Vg"], levels, ks, ws,
-            out=out, lse=lse, idx_out=idx)
+    if al is None:
+        bd.step(dev["Q"], dev["Kp"], dev["Vp"], dev["Kg"], dev["Vg"], levels, ks, ws,
+                out=out, lse=lse, idx_out=idx)
+    else:
+        bd.step_cached_al(dev["Q"], dev["Kp"], dev["Vp"], dev["Kg"], dev["Vg"], al, levels, ks,
+                          ws, out=out, lse=lse, idx_out=idx)
     status = bd.read_device_status(ws)
     return out, lse, idx, status

@@ -124,6 +124,13 @@ def test_entry_points_reject_before_launch(lib):
                                      None, p16, 1 << 20, None) == 1
     assert lib.wf_clear_device_status(None, 256, None) == 1
     assert lib.wf_clear_device_status(p16, 8, None) == 4
+    # Cached A_L: the extra pointer is validated like the others.
+    assert lib.wf_step_cached_al(ctypes.byref(dims), p16, p16, p16, p16, p16, None, k, p16, None,
+                                 None, p16, 1 << 40, None) == 1
+    assert lib.wf_step_cached_al(ctypes.byref(dims), p16, p16, p16, p16, p16, p17, k, p16, None,
+                                 None, p16, 1 << 40, None) == 7
+    assert lib.wf_step_cached_al(ctypes.byref(dims), p16, p16, p16, p16, p16, p16, k, p16, None,
+                                 None, p16, 16, None) == 4
 
 
 def test_product_path_has_no_oracle_dependency():

@@ -263,12 +263,13 @@ def test_full_budget_is_full_attention():
 
 # ---------------------------------------------------------- whole step, configs
 
-def _step_config(name, units=None, layer=0):
+def _step_config(name, units=None, layer=0, cached_al=False):
     cfg = wl.CONFIGS[name]
     ks = cfg.k_per_level()
     arrs = layer_inputs(name, layer)
     dev = to_device(arrs, cfg.dtype)
-    out, lse, idx, status = run_step(dev, cfg.levels, ks)
+    al = bd.dwt_lowpass(dev["Kp"], cfg.levels) if cached_al else None
+    out, lse, idx, status = run_step(dev, cfg.levels, ks, al=al)
     assert status == 0
     out, lse, idx = out.cpu().numpy(), lse.cpu().numpy(), idx.cpu().numpy()
     del dev
@@ -288,6 +289,19 @@ def _step_config(name, units=None, layer=0):
 def test_step_matches_oracle_all_units(name):
     kinds = _step_config(name)
     assert kinds.count("exact") >= len(kinds) // 2
+
+
+@pytest.mark.parametrize("name", ["tiny", "llada8b_layer"])
+def test_step_cached_al_matches_oracle_all_units(name):
+    # Steps 2-5 from an A_L computed by an earlier wf_dwt_lowpass (unchanged
+    # prompt keys): the same contract as the whole step.
+    kinds = _step_config(name, cached_al=True)
+    assert kinds.count("exact") >= len(kinds) // 2
+
+
+def test_step_cached_al_long_prompt_sampled():
+    kinds = _step_config("long_prompt", units=[(0, 0), (0, 31)], cached_al=True)
+    assert len(kinds) == 2
 
 
 def test_step_long_prompt_sampled():

@@ -29,7 +29,7 @@ EXPORTS = ("wf_status_string", "wf_last_error_string", "wf_default_k_per_level",
            "wf_step_launch_count",
            "wf_clear_device_status", "wf_read_device_status", "wf_dwt_lowpass",
            "wf_score_topk", "wf_recursive_filter", "wf_sparse_gather_attn", "wf_step",
-           "wf_step_host", "wf_step_static_scratch")
+           "wf_step_host", "wf_step_static_scratch", "wf_step_cached_al")
 
 
 class WfError(RuntimeError):
@@ -71,6 +71,8 @@ _SIGS = {
                                     _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "wf_step_static_scratch": (ctypes.c_int, [_DIMSP, _vp, _vp, _vp, _vp, _vp, _i32p, _vp,
                                               _vp, _vp, _vp]),
+    "wf_step_cached_al": (ctypes.c_int, [_DIMSP, _vp, _vp, _vp, _vp, _vp, _vp, _i32p, _vp, _vp,
+                                         _vp, _vp, _sz, _vp]),
 }
 
 
@@ -267,6 +269,25 @@ def step(q, kp, vp, kg, vg, levels: int, k_per_level: Sequence[int], ws: torch.T
         out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
     _check("wf_step", lib().wf_step(
         ctypes.byref(dims), _ptr(q), _ptr(kp), _ptr(vp), _ptr(kg), _ptr(vg),
+        _k_array(k_per_level), _ptr(out), _ptr(lse), _ptr(idx_out), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return out
+
+
+def step_cached_al(q, kp, vp, kg, vg, al, levels: int, k_per_level: Sequence[int],
+                   ws: torch.Tensor, out: Optional[torch.Tensor] = None,
+                   lse: Optional[torch.Tensor] = None, idx_out: Optional[torch.Tensor] = None,
+                   stream=None) -> torch.Tensor:
+    """Steps 2-5 with A_L [b, H, N_p/2^L, d] fp32 from an earlier dwt_lowpass
+    (prompt keys unchanged); returns O [b, H, G, d] fp32."""
+    for t, n in ((q, "Q"), (kp, "Kp"), (vp, "Vp"), (kg, "Kg"), (vg, "Vg")):
+        _require(t, n, q.dtype)
+    _require(al, "AL", torch.float32)
+    dims = make_dims(q, kp, levels)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    _check("wf_step_cached_al", lib().wf_step_cached_al(
+        ctypes.byref(dims), _ptr(q), _ptr(kp), _ptr(vp), _ptr(kg), _ptr(vg), _ptr(al),
         _k_array(k_per_level), _ptr(out), _ptr(lse), _ptr(idx_out), _ptr(ws), ws.numel(),
         _stream(stream)))
     return out

@@ -353,6 +353,48 @@ int wf_step(const wf_dims* dims, const void* Q, const void* Kp, const void* Vp, 
   return cuda_status(wf::launch_path(ld, plan, a, s));
 }
 
+int wf_step_cached_al(const wf_dims* dims, const void* Q, const void* Kp, const void* Vp,
+                      const void* Kg, const void* Vg, const float* AL,
+                      const int32_t* k_per_level, float* O, float* lse, int32_t* idx_out,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  LaunchDims ld;
+  int st = check_dims(dims, &ld);
+  if (st != WF_OK) return st;
+  if (Q == nullptr || Kp == nullptr || Vp == nullptr || Kg == nullptr || Vg == nullptr ||
+      AL == nullptr || O == nullptr || workspace == nullptr)
+    return WF_ERR_NULL;
+  if (!aligned16(Q) || !aligned16(Kp) || !aligned16(Vp) || !aligned16(Kg) || !aligned16(Vg) ||
+      !aligned16(AL) || !aligned16(O) || !aligned16(workspace) || (lse && !aligned16(lse)) ||
+      (idx_out && !aligned16(idx_out)))
+    return WF_ERR_ALIGNMENT;
+  st = check_k(ld, k_per_level);
+  if (st != WF_OK) return st;
+  const int budget = k_per_level[0];
+  wf::PathPlan plan;
+  if (!wf::plan_path(ld, wf::kPhaseAll, k_per_level, k_per_level[ld.levels], budget,
+                     wf::device_sm_count(), &plan))
+    return WF_ERR_UNSUPPORTED;
+  const Layout L = layout(ld, k_per_level, &plan);
+  if (workspace_bytes < L.total) return WF_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  wf::PathArgs a = {};
+  a.q = Q;
+  a.kp = Kp;
+  a.vp = Vp;
+  a.kg = Kg;
+  a.vg = Vg;
+  a.al = AL;  // the score phase stages the cached fp32 rows (bf16: split on chip)
+  a.idx_out = idx_out;
+  a.o = O;
+  a.lse = lse;
+  a.status = status_word(workspace);
+  a.t_ws = reinterpret_cast<float*>(ws + L.t);
+  a.k = k_per_level;
+  a.k_l = k_per_level[ld.levels];
+  a.budget = budget;
+  return cuda_status(wf::launch_path(ld, plan, a, static_cast<cudaStream_t>(stream)));
+}
+
 int wf_step_host(const wf_dims* dims, const void* h_Q, const void* h_Kp, const void* h_Vp,
                  const void* h_Kg, const void* h_Vg, const int32_t* k_per_level, float* h_O,
                  float* h_lse, void* d_Q, void* d_Kp, void* d_Vp, void* d_Kg, void* d_Vg,
