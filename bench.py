@@ -103,6 +103,22 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def allreduce_max(value: float, world: int, device) -> float:
+    """The largest of every rank's value (the slowest rank's time); one rank: itself."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, tokens: int, steps: int, t_ms: float) -> float:
+    """Whole-job throughput: every replica processes `tokens` per step."""
+    return world * tokens * steps / (t_ms / 1e3)
+
+
 def step_bytes(cfg, fused: bool) -> int:
     """Algorithmic HBM bytes of one wf_step; the fused step never writes or
     reads A_L in global memory."""
@@ -345,13 +361,9 @@ def run_ours(args, cfg):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    t_ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        tt = torch.tensor([t_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_ms = float(tt.item())
+    t_ms = allreduce_max(ev0.elapsed_time(ev1), world, dev)
     ms_per_step = t_ms / args.steps
-    value = world * tokens_per_step(cfg) * args.steps / (t_ms / 1e3)
+    value = job_value(world, tokens_per_step(cfg), args.steps, t_ms)
 
     # ---- steps 2-5 with A_L cached from an earlier step (unchanged prompt keys)
     als = [bd.dwt_lowpass(c["Kp"], cfg.levels) for c in copies]
@@ -444,12 +456,8 @@ def run_ours(args, cfg):
         bd.step_host(dims, host, ks, stage, ws, stream=stream)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = world * tokens_per_step(cfg) * e2e_steps / (e2e_ms / 1e3)
+    e2e_ms = allreduce_max(e0.elapsed_time(e1), world, dev)
+    e2e_value = job_value(world, tokens_per_step(cfg), e2e_steps, e2e_ms)
     clocks = sampler.stop() if sampler else None
     status = bd.read_device_status(ws)
 
