@@ -322,6 +322,26 @@ def test_step_batched_long_sampled(tag):
     assert len(kinds) == 2
 
 
+@pytest.mark.parametrize("n,levels,g,d,h,budget", [
+    (2048, 4, 20, 64, 3, 96),     # bf16, d = 64, ragged G: one column block per row
+    (1024, 3, 64, 128, 2, 128),   # G = 64: two query halves, N = 64 tensor-core tiles
+    (4096, 5, 9, 128, 4, 200),    # 32-row spans, odd G
+])
+def test_step_single_launch_shapes(n, levels, g, d, h, budget):
+    # Shapes planned as one launch (Haar low-pass inside the path kernel, every
+    # key of a CTA resident), checked unit by unit against the oracle.
+    arrs = _rand_inputs(n + g + budget, 1, h, n, g, d, "bf16")
+    ks = bd.default_k_per_level(n, levels, budget)
+    dev = to_device(arrs, "bf16")
+    dims = bd.make_dims(dev["Q"], dev["Kp"], levels)
+    assert bd.step_launch_count(dims, ks) == 1
+    out, lse, idx, status = run_step(dev, levels, ks)
+    assert status == 0
+    out, lse, idx = out.cpu().numpy(), lse.cpu().numpy(), idx.cpu().numpy()
+    for j in range(h):
+        compare_step_unit(arrs, 0, j, levels, ks, idx[0, j], out[0, j], lse[0, j])
+
+
 def test_step_is_deterministic():
     cfg = wl.CONFIGS["llada8b_layer"]
     dev = to_device(layer_inputs("llada8b_layer"), cfg.dtype)
