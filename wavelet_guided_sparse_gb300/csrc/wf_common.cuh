@@ -490,10 +490,11 @@ __device__ __forceinline__ void topk_zero(TopkSmem& sm) {
 }
 
 // `prezeroed`: the histograms were zeroed (topk_zero, followed by a barrier)
-// since their last use.
+// since their last use.  `map` (nullable): out receives map[i] instead of i.
 static __device__ __noinline__ void block_select_topk(const uint32_t* keys, int n, int k, int lo_slot,
                                                int hi_slot, int32_t* out, TopkSmem& sm,
-                                               bool prezeroed = false) {
+                                               bool prezeroed = false,
+                                               const int32_t* map = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (!prezeroed) {
     topk_zero(sm);
@@ -544,14 +545,26 @@ static __device__ __noinline__ void block_select_topk(const uint32_t* keys, int 
     sm.wcnt[1][warp] = eq;
   }
   __syncthreads();
-  int slot = 0, ties = 0;  // selected keys and ties before this warp's chunk
-  for (int w = 0; w < warp; ++w) {
-    const int e = sm.wcnt[1][w];
-    int q = need - ties;
-    q = q < 0 ? 0 : (q > e ? e : q);
-    slot += sm.wcnt[0][w] + q;
-    ties += e;
+  // Selected keys and ties before this warp's chunk: exclusive scans of the
+  // per-warp counts (lane w holds warp w's); the ties taken before a chunk
+  // are min(need, ties seen before it).
+  int gi = 0, ei = 0;
+  if (lane < kWarps) {
+    gi = sm.wcnt[0][lane];
+    ei = sm.wcnt[1][lane];
   }
+  const int gw = gi, ew = ei;
+#pragma unroll
+  for (int off = 1; off < kWarps; off <<= 1) {
+    const int g2 = __shfl_up_sync(0xffffffffu, gi, off), e2 = __shfl_up_sync(0xffffffffu, ei, off);
+    if (lane >= off) {
+      gi += g2;
+      ei += e2;
+    }
+  }
+  const int e_ex = ei - ew;
+  int slot = __shfl_sync(0xffffffffu, gi - gw + min(need, e_ex), warp);
+  int ties = __shfl_sync(0xffffffffu, e_ex, warp);
   for (int base = lo; base < hi; base += 32) {
     const int i = base + lane;
     const uint32_t kv = i < hi ? keys[i] : 0u;
@@ -561,7 +574,7 @@ static __device__ __noinline__ void block_select_topk(const uint32_t* keys, int 
     const bool taken = (i < hi && kv > thr) || tie_taken;
     const unsigned tm = __ballot_sync(0xffffffffu, taken);
     const int my_slot = slot + __popc(tm & below);
-    if (taken && my_slot >= lo_slot && my_slot < hi_slot) out[my_slot - lo_slot] = i;
+    if (taken && my_slot >= lo_slot && my_slot < hi_slot) out[my_slot - lo_slot] = map ? map[i] : i;
     slot += __popc(tm);
     ties += __popc(eqm);
   }

@@ -434,6 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     fence_mbar_init();
     if (fuse_dwt)
       for (int st = 0; st < fuse_issued; ++st) fuse_issue(st);
+    if (p.use_tma_spans) prefetch_tensormap(&p.tmap_spans);  // used by the filter phase
   }
   __syncwarp();
   if (use_tmem && warp == 0) tmem_alloc(reinterpret_cast<uint32_t*>(misc + 7), kTmemCols);
@@ -938,17 +939,13 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         const int a0 = key_slot_start(rank, cs, p.n_keys), a1 = key_slot_start(rank + 1, cs, p.n_keys);
         const int w0 = key_slot_start(rank, cs, B), w1 = key_slot_start(rank + 1, cs, B);
         const bool attend = (mode & kModeAttend) != 0;
-        // This CTA's slots of the key list: [a0, min(a1, B)).  klist first
-        // receives candidate indices, then their token positions.
+        // This CTA's slots of the key list: [a0, min(a1, B)); klist receives
+        // the selected candidates' token positions.
         const int b1 = min(a1, B);
-        block_select_topk(keys_all, n_all, B, a0, b1, klist, tk, tk_clean);
+        block_select_topk(keys_all, n_all, B, a0, b1, klist, tk, tk_clean, pos_all);  // positions
         tk_clean = false;
-        for (int sl = a0 + tid; sl < b1; sl += kThreads) {
-          const int pos = pos_all[klist[sl - a0]];
-          klist[sl - a0] = pos;
-          if (p.idx_out != nullptr) p.idx_out[unit * B + sl] = pos;
-        }
-        __syncthreads();
+        if (p.idx_out != nullptr)
+          for (int sl = a0 + tid; sl < b1; sl += kThreads) p.idx_out[unit * B + sl] = klist[sl - a0];
         (void)attend;
         (void)w0;
         (void)w1;

@@ -50,6 +50,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
       : "memory");
 }
 
+// Brings a tensor map (kernel parameter) into the descriptor cache ahead of
+// its first tensor copy.
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
 // ---------------------------------------------------------------- tensor memory
 // Allocates ncols (power of two, 32..512) columns of tensor memory for this
 // CTA; one whole warp executes it and the base address lands in *slot.
