@@ -511,7 +511,14 @@ static __device__ __noinline__ void block_select_topk(const uint32_t* keys, int 
     for (int base = 0; base < n; base += kThreads) {  // whole warps iterate together
       const int i = base + tid;
       const uint32_t kv = i < n ? keys[i] : 0u;
-      hist_add(h, sm.region[round], i < n && (kv & pmask) == prefix, (kv >> shift) & (nb - 1), per);
+      const bool active = i < n && (kv & pmask) == prefix;
+      const uint32_t bin = (kv >> shift) & (nb - 1);
+      if (round == 0) {
+        hist_add(h, sm.region[round], active, bin, per);  // scores share a few leading bins
+      } else if (active) {  // later rounds: the boundary bin's keys spread out
+        atomicAdd(&h[bin], 1u);
+        atomicAdd(&sm.region[round][bin / per], 1u);
+      }
     }
     __syncthreads();
     uint32_t digit;
