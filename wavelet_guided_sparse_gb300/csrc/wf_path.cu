@@ -817,14 +817,21 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     }
     __syncthreads();
 
-    int n_surv = ns;
+    // Levels that keep every child need no scoring: start from the survivors
+    // of the lowest of them (all descendants of the coarse survivors, in
+    // position order) and walk down from the first level that selects.
+    int j_top = levels - 1;
+    while (j_top >= 0 && p.k[j_top] >= 2 * p.k[j_top + 1]) --j_top;
+    const int jj = j_top + 1, dsh = levels - jj;  // survivors at level jj: 2^dsh per span
+    int n_surv = ns << dsh;
     bool global_done = false;  // final token list already distributed
-    for (int i = tid; i < ns; i += kThreads) {
-      sp[i] = sl_all[s0 + i];
-      sr[i] = i << levels;
+    for (int e = tid; e < n_surv; e += kThreads) {
+      const int i = e >> dsh, m = e & ((1 << dsh) - 1);
+      sp[e] = (sl_all[s0 + i] << dsh) + m;
+      sr[e] = (i << levels) + (m << jj);
     }
     __syncthreads();
-    for (int j = levels - 1; j >= 0; --j) {
+    for (int j = j_top; j >= 0; --j) {
       for (int i = tid; i < n_surv; i += kThreads) {
         const int pos = sp[i], row = sr[i];
         cp[2 * i] = 2 * pos;
@@ -842,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       }
       // Scores of this level's candidates (log2 domain, z = sc2 * Σ_leaves t):
       //  pass A  per query, online (max, Σ 2^(z - max)) over this CTA's
-      //          candidates (lanes = queries q and q + 32; a warp takes 4
+      //          candidates (lanes = queries q and q + 32; a warp takes 8
       //          candidates at a time, their loads issued together);
       //  CTA and cluster merges give the global max gm and 1 / sum ginv;
       //  pass B  s_c = Σ_q 2^(z[c,q] - gm_q) * ginv_q, one thread per candidate.
