@@ -47,8 +47,8 @@ FALLBACK_HBM_GBS = 6800.0
 DWT_TRAFFIC = {"sources": ("wf_dwt.cu",), "source_sha": "2ddcb5bc05b588dc",
                "bytes_per_launch": 33577984}  # 33.58 MB read + 0 B written (A_L stays in L2)
 PATH_TRAFFIC = {"sources": ("wf_path.cu", "wf_common.cuh", "wf_mma.cuh", "wf_umma.cuh"),
-                "source_sha": "0b04d882ea6816d0",
-                "bytes_per_launch": 38693120}  # 38.68 MB read + 9.7 KB written
+                "source_sha": "1a06ef9c1ca3749f",
+                "bytes_per_launch": 38705152}  # 38.69 MB read + 16.6 KB written
 
 
 def _rank_env():
