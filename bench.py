@@ -42,12 +42,12 @@ FALLBACK_HBM_GBS = 6800.0
 # from an ncu capture of the kernel source with this SHA-256 prefix; null
 # once the kernel has changed since the counters were taken.
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture
-# of the 4096-token layer (profiles/), valid while the kernel sources hash to
-# source_sha.
-DWT_TRAFFIC = {"sources": ("wf_dwt.cu",), "source_sha": "2ddcb5bc05b588dc",
+# of the 4096-token layer (profiles/), valid while the kernel sources (without
+# comments and blank space) hash to source_sha.
+DWT_TRAFFIC = {"sources": ("wf_dwt.cu",), "source_sha": "65d64d392b075f89",
                "bytes_per_launch": 33577984}  # 33.58 MB read + 0 B written (A_L stays in L2)
 PATH_TRAFFIC = {"sources": ("wf_path.cu", "wf_common.cuh", "wf_mma.cuh", "wf_umma.cuh"),
-                "source_sha": "1a06ef9c1ca3749f",
+                "source_sha": "ede6ccfabcf718ba",
                 "bytes_per_launch": 38705152}  # 38.69 MB read + 16.6 KB written
 
 
@@ -128,11 +128,34 @@ def step_bytes(cfg, fused: bool) -> int:
     return total
 
 
+def _strip_comments(text: str) -> str:
+    """C++ source without comments and blank space (comment edits leave the
+    kernel, and so its measured traffic, unchanged)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        if text.startswith("//", i):
+            i = text.find("\n", i)
+            i = n if i < 0 else i
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif text[i] == '"':
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(text[i])
+            i += 1
+    return "".join("".join(out).split())
+
+
 def _source_sha(names) -> str:
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "wavelet_guided_sparse_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "wavelet_guided_sparse_gb300", "csrc", n)) as f:
+            h.update(_strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -11,9 +11,10 @@
 // contiguous byte range through a ring of three 64 KB shared-memory stages
 // filled by single bulk copies (TMA engine, mbarrier completion), so 128-192
 // KB per SM are in flight independent of register pressure.  Threads reduce
-// the staged rows in fp32 (and, for the fused step, emit A_L as the three
-// bf16 planes its tensor-core scoring consumes): for spans of up to 16 rows one thread owns one
-// (span, 16-byte column chunk) pair; longer spans are summed in 16-row blocks
+// the staged rows in fp32 (and, for a two-launch wf_step with bf16 inputs,
+// emit A_L as the three bf16 planes its tensor-core scoring consumes): for
+// spans of up to 16 rows one thread owns one (span, 16-byte column chunk)
+// pair; longer spans are summed in 16-row blocks
 // whose partials are combined in a fixed order, with a running sum carried
 // across stages for spans longer than a stage.
 #include <algorithm>

@@ -1,6 +1,8 @@
-// Steps 2-5 of the WaveFilter path in one thread-block-cluster kernel.
+// The WaveFilter path in one thread-block-cluster kernel (steps 2-5, and
+// step 1 too where a CTA's coarse slice is small enough).
 //
 // WaveFilter (arXiv 2606.00724):
+//  * step 1, §2.2 eq. (5) + pyramid, §3.1: A_L = 2^(-L/2) x span sums of K_p;
 //  * step 2, Fig. 2(c) / §1: score the low-frequency keys A_L against the
 //    generation-block queries with the eq. (3) logits and keep a coarse Top-K;
 //  * step 3, Fig. 2(d) / §1: multi-scale recursive filtering — children of
@@ -12,25 +14,30 @@
 //
 // One cluster of `cs` CTAs handles one (sequence, head) unit; the kernel runs
 // any contiguous subset of the phases (score / filter / attend), which is how
-// wf_score_topk, wf_recursive_filter, wf_sparse_gather_attn and wf_step share
-// it.  Between phases the work is rebalanced across the cluster through
-// DSMEM: the coarse survivors are all-gathered (every CTA then takes an equal
-// slice) and the final tokens are pushed to the CTA that attends over their
-// slot of the key list.
+// wf_score_topk, wf_recursive_filter, wf_sparse_gather_attn, wf_step and
+// wf_step_cached_al share it.  Between phases the work is rebalanced across
+// the cluster through DSMEM: the coarse survivors are all-gathered (every CTA
+// then takes an equal slice) and the final tokens are pushed to the CTA that
+// attends over their slot of the key list.
 //
 // Phase details:
-//  score  — each CTA owns P/cs coarse positions; z by fp32 FMAs (A_L is fp32),
-//           per-query (max, sum) merged over the cluster, exact Top-K.
+//  step 1 — (fused plans) each CTA streams the spans of its P/cs coarse
+//           positions through a ring of bulk copies and writes A_L straight
+//           into shared memory as hi/mid/lo bf16 planes.
+//  score  — z = Q·A_L^T per CTA slice: bf16 on the fifth-generation tensor
+//           cores (tcgen05.mma, accumulators in tensor memory, the three
+//           planes reproduce fp32 A_L), fp32 by FMAs; per-query (max, sum)
+//           merged over the cluster; every CTA selects the coarse Top-K.
 //  filter — by linearity Q·A_j[c] = 2^(-j/2) Σ_{n∈span(c)} Q·Kp[n]: token
-//           logits t = Kp[rows]·Q^T are computed once (bf16 tensor cores,
-//           exact products, fp32 sums) for the rows under this CTA's coarse
-//           survivors, staged into padded shared-memory rows by 16-byte
-//           cp.async copies in a two-stage pipeline; every level sums t over
-//           the candidates' leaves.
+//           logits t = Kp[rows]·Q^T are computed once (tcgen05, exact bf16
+//           products, fp32 sums) for the rows under this CTA's coarse
+//           survivors, fetched by 2-D tensor copies of whole spans (or 16-byte
+//           cp.async) into the 128-byte-swizzled operand layout; levels that
+//           keep every child are skipped, the others sum t over leaves.
 //  attend — split-KV: each CTA gathers the K/V rows of its key slot range by
-//           cp.async, runs Q·K^T and P·V on tensor cores with an online
-//           softmax, and the partial (max, sum, O) rows are pushed to the CTA
-//           that finalises those query rows.
+//           cp.async, runs Q·K^T and P·V on tensor cores (mma.sync) with an
+//           online softmax, and the partial (max, sum, O) rows are pushed to
+//           the CTA that finalises those query rows.
 #include <algorithm>
 #include <climits>
 #include <cmath>
