@@ -748,9 +748,12 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     const int ns = s1 - s0;
     const int R = ns << levels;
     unsigned char* kst = smem + L.f_kst;
+    // Row pitch of t: odd in shared memory (conflict-free row-wise passes),
+    // a multiple of 4 floats when spilled to the workspace (16-byte loads).
+    const int TT = t_ws == nullptr ? TS : ((G + 3) & ~3);
     float* t = t_ws == nullptr
                    ? reinterpret_cast<float*>(smem + L.f_t)
-                   : t_ws + (static_cast<int64_t>(unit) * cs + rank) * p.rows_cap * TS;
+                   : t_ws + (static_cast<int64_t>(unit) * cs + rank) * p.rows_cap * TT;
     const T* kp = static_cast<const T*>(p.kp);
     const int ntiles = (R + kTileRows - 1) / kTileRows;
     constexpr int C16 = D * static_cast<int>(sizeof(T)) / 16;  // 16-byte chunks per row
@@ -803,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         (void)mbar_wait_bounded(span_bar, 0, p.status);
       else
         cp_async_wait<0>();
-      umma_logits<D>(kst, 1, 0, FS * kTileRows, R, qs, G, t, 0, TS, 1.f, tmem, mma_bar, mma_phase,
+      umma_logits<D>(kst, 1, 0, FS * kTileRows, R, qs, G, t, 0, TT, 1.f, tmem, mma_bar, mma_phase,
                      p.status);
       __syncthreads();
     } else
@@ -813,11 +816,11 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       const int rows_valid = min(kTileRows, R - tile * kTileRows);
       if constexpr (sizeof(T) == 2) {
         umma_logits<D>(kst + stage * kStageB, 1, 0, FS * kTileRows, rows_valid, qs, G, t,
-                       tile * kTileRows, TS, 1.f, tmem, mma_bar, mma_phase, p.status);
+                       tile * kTileRows, TT, 1.f, tmem, mma_bar, mma_phase, p.status);
       } else {
         __syncthreads();
         logits_tile_f32<D>(kst + stage * kStageB, reinterpret_cast<const float*>(qs), t,
-                           tile * kTileRows, rows_valid, G, TS, 1.f);
+                           tile * kTileRows, rows_valid, G, TT, 1.f);
       }
       __syncthreads();
       if (tile + FS < ntiles) issue(tile + FS, stage);
@@ -865,40 +868,58 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       const bool final_gather = j == 0 && gather_all;
       const bool qa = lane < G, qb = lane + 32 < G;
       const int la = qa ? lane : 0, lb = qb ? lane + 32 : 0;
-      // Leaf sum of t for candidate row offset `row` (row index * TS), query q.
+      // Leaf sum of t for candidate row offset `row` (row index * TT), query q.
       auto leaf_sum = [&](int row, int q) {
         float a = 0.f;
 #pragma unroll 1
-        for (int i = 0; i < leaves; ++i) a += t[row + i * TS + q];
+        for (int i = 0; i < leaves; ++i) a += t[row + i * TT + q];
         return a;
       };
       float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
-      for (int ci0 = warp * 8; ci0 < n_cand; ci0 += kWarps * 8) {
-        int rows[8];
+      if (leaves == 1) {
+        // Sixteen candidates per warp step, every load of a step (both query
+        // halves) issued before the first exponential.
+        for (int ci0 = warp * 16; ci0 < n_cand; ci0 += kWarps * 16) {
+          int rows[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) rows[u] = cr[min(ci0 + u, n_cand - 1)] * TS;
-        float z[8];
-        if (leaves == 1) {
+          for (int u = 0; u < 16; ++u) rows[u] = cr[min(ci0 + u, n_cand - 1)] * TT;
+          float za[2][8], zb[2][8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) z[u] = t[rows[u] + la];
-        } else {
-#pragma unroll 1
-          for (int u = 0; u < 8; ++u) z[u] = leaf_sum(rows[u], la);
-        }
+          for (int u = 0; u < 16; ++u) za[u >> 3][u & 7] = t[rows[u] + la];
+          if (G > 32) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) z[u] = ci0 + u < n_cand && qa ? z[u] * sc2 : -INFINITY;
-        online8(m0, l0, z);
-        if (G > 32) {  // queries 32..63
-          if (leaves == 1) {
-#pragma unroll
-            for (int u = 0; u < 8; ++u) z[u] = t[rows[u] + lb];
-          } else {
-#pragma unroll 1
-            for (int u = 0; u < 8; ++u) z[u] = leaf_sum(rows[u], lb);
+            for (int u = 0; u < 16; ++u) zb[u >> 3][u & 7] = t[rows[u] + lb];
           }
 #pragma unroll
-          for (int u = 0; u < 8; ++u) z[u] = ci0 + u < n_cand && qb ? z[u] * sc2 : -INFINITY;
-          online8(m1, l1, z);
+          for (int u = 0; u < 16; ++u) {
+            const bool ok = ci0 + u < n_cand;
+            za[u >> 3][u & 7] = ok && qa ? za[u >> 3][u & 7] * sc2 : -INFINITY;
+            zb[u >> 3][u & 7] = ok && qb ? zb[u >> 3][u & 7] * sc2 : -INFINITY;
+          }
+          online8(m0, l0, za[0]);
+          online8(m0, l0, za[1]);
+          if (G > 32) {
+            online8(m1, l1, zb[0]);
+            online8(m1, l1, zb[1]);
+          }
+        }
+      } else {
+        for (int ci0 = warp * 8; ci0 < n_cand; ci0 += kWarps * 8) {
+          float z[8];
+#pragma unroll 1
+          for (int u = 0; u < 8; ++u) {
+            const int row = cr[min(ci0 + u, n_cand - 1)] * TT;
+            z[u] = ci0 + u < n_cand && qa ? leaf_sum(row, la) * sc2 : -INFINITY;
+          }
+          online8(m0, l0, z);
+          if (G > 32) {  // queries 32..63
+#pragma unroll 1
+            for (int u = 0; u < 8; ++u) {
+              const int row = cr[min(ci0 + u, n_cand - 1)] * TT;
+              z[u] = ci0 + u < n_cand && qb ? leaf_sum(row, lb) * sc2 : -INFINITY;
+            }
+            online8(m1, l1, z);
+          }
         }
       }
       part_m[warp * kMaxQ + lane] = m0;
@@ -914,12 +935,25 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       }
       __syncthreads();
       cluster_merge_stats(loc_m, loc_l, G, stat_in, gm, ginv, n_cand, final_gather ? cnt_b : nullptr);
-      // Pass B: one thread per candidate (odd row pitch: conflict-free);
-      // four independent partial sums over the queries.
+      // Pass B: one thread per candidate (odd row pitch in shared memory:
+      // conflict-free); four independent partial sums over the queries.
       for (int ci = tid; ci < n_cand; ci += kThreads) {
-        const int row = cr[ci] * TS;
+        const int row = cr[ci] * TT;
         float sq[4] = {0.f, 0.f, 0.f, 0.f};
-        if (leaves == 1) {
+        if (leaves == 1 && t_ws != nullptr) {
+          // Spilled rows (L2): 16-byte loads, four in flight; columns >= G are padding.
+          const float4* r4 = reinterpret_cast<const float4*>(t + row);
+#pragma unroll 4
+          for (int q4 = 0; q4 < TT / 4; ++q4) {
+            const float4 v = r4[q4];
+            const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int q = 4 * q4 + k;
+              if (q < G) sq[k] += exp2f(vv[k] * sc2 - gm[q]) * ginv[q];
+            }
+          }
+        } else if (leaves == 1) {
           int q = 0;
 #pragma unroll 2
           for (; q + 4 <= G; q += 4) {
@@ -1510,7 +1544,7 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
   plan->t_in_smem = t_in_smem;
   plan->t_bytes = t_in_smem ? 0
                             : sizeof(float) * static_cast<size_t>(ld.units) * cs * p.rows_cap *
-                                  (ld.n_gen | 1);
+                                  ((ld.n_gen + 3) & ~3);  // spilled row pitch
   plan->per_cta_p = p.per_cta_p;
   plan->rows_cap = p.rows_cap;
   plan->sorted_cap = p.sorted_cap;
