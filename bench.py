@@ -47,8 +47,8 @@ FALLBACK_HBM_GBS = 6800.0
 DWT_TRAFFIC = {"sources": ("wf_dwt.cu",), "source_sha": "65d64d392b075f89",
                "bytes_per_launch": 33577984}  # 33.58 MB read + 0 B written (A_L stays in L2)
 PATH_TRAFFIC = {"sources": ("wf_path.cu", "wf_common.cuh", "wf_mma.cuh", "wf_umma.cuh"),
-                "source_sha": "ede6ccfabcf718ba",
-                "bytes_per_launch": 38705152}  # 38.69 MB read + 16.6 KB written
+                "source_sha": "4e8b7fafc8ea55e4",
+                "bytes_per_launch": 38690048}  # 38.69 MB read + 3.3 KB written
 
 
 def _rank_env():
