@@ -54,6 +54,8 @@ __all__ = [
     "sparse_attention",
     "wavefilter_step",
     "wavefilter_step_batched",
+    "cache_init",
+    "cache_update",
 ]
 
 
@@ -224,3 +226,50 @@ def wavefilter_step_batched(inputs: Dict[str, np.ndarray], levels: int,
                                        inputs["Vp"][bi, hi], inputs["Kg"][bi, hi],
                                        inputs["Vg"][bi, hi], levels, k_per_level))
     return res
+
+
+def cache_init(k_all, v_all, n_prompt: int, levels: int) -> Dict:
+    """KV-cache initialisation at the first denoising step t = 1 (WaveFilter
+    §2.1 eq. (2)) plus the low-frequency component of the cached prompt keys
+    (§3.1), which §1 extracts at that initial step.
+
+    ``k_all``, ``v_all``: [N, H, d], one sequence in token-major order (the
+    keys and values eq. (1) computes for every position I, heads side by
+    side per token).  Positions [0, n_prompt) form the prompt I_p, the rest
+    [n_prompt, N) the generation block I_g.  Eq. (2) stores them unchanged:
+    the cache keeps each head's rows in position order.
+
+    Returns {"Kp": [H, N_p, d], "Vp", "Kg": [H, N - N_p, d], "Vg",
+    "a_l": [H, N_p / 2^L, d]} with a_l = A_L of Kp per head (haar_pyramid).
+    """
+    k = np.asarray(k_all, dtype=np.float64)
+    v = np.asarray(v_all, dtype=np.float64)
+    if k.ndim != 3 or k.shape != v.shape:
+        raise ValueError("K and V must both be [N, H, d]")
+    if not 0 < n_prompt <= k.shape[0]:
+        raise ValueError("n_prompt out of range")
+    # Per head h, cache row n is position n of that head: a swap of the
+    # token and head axes.
+    kp = np.swapaxes(k[:n_prompt], 0, 1)
+    vp = np.swapaxes(v[:n_prompt], 0, 1)
+    kg = np.swapaxes(k[n_prompt:], 0, 1)
+    vg = np.swapaxes(v[n_prompt:], 0, 1)
+    a_l = np.stack([haar_pyramid(kp[h], levels)[levels] for h in range(kp.shape[0])])
+    return {"Kp": kp, "Vp": vp, "Kg": kg, "Vg": vg, "a_l": a_l}
+
+
+def cache_update(k_gen, v_gen) -> Dict:
+    """Cache update at a later step t > 1 (WaveFilter §2.1 eq. (4)): the keys
+    and values just computed for the generation positions replace the cached
+    ones, K~^t[I~] = K^t[I~], V~^t[I~] = V^t[I~].
+
+    ``k_gen``, ``v_gen``: [G, H, d] token-major.  Returns {"Kg": [H, G, d],
+    "Vg"}: the new generation-block cache, rows in position order per head.
+    The prompt part of the cache is untouched, so an A_L computed from it
+    stays valid.
+    """
+    k = np.asarray(k_gen, dtype=np.float64)
+    v = np.asarray(v_gen, dtype=np.float64)
+    if k.ndim != 3 or k.shape != v.shape:
+        raise ValueError("K and V must both be [G, H, d]")
+    return {"Kg": np.swapaxes(k, 0, 1), "Vg": np.swapaxes(v, 0, 1)}

@@ -308,3 +308,73 @@ def test_planted_span_recall_sanity(name):
         assert len(idx) == cfg.budget and (np.diff(idx) > 0).all()
         recalls.append(np.isin(planted, idx).mean())
     assert min(recalls) > 0.5, recalls
+
+
+# ------------------------------------------------- cache write (eqs. (2), (4))
+
+def _coded_kv(n, h, d):
+    """K[n, h, c] = n + 1000 h + 10^6 c and V = -(K + 1/2): every entry names
+    its own (position, head, channel), exactly in float64."""
+    nn, hh, cc = np.meshgrid(np.arange(n), np.arange(h), np.arange(d), indexing="ij")
+    k = (nn + 1000.0 * hh + 1e6 * cc).astype(np.float64)
+    return k, -(k + 0.5)
+
+
+@pytest.mark.parametrize("n_prompt,n_gen,heads,d,levels", [(16, 3, 2, 3, 2), (32, 5, 3, 4, 3),
+                                                           (8, 1, 1, 2, 1)])
+def test_cache_init_places_every_row(n_prompt, n_gen, heads, d, levels):
+    # Eq. (2): cache row n of head h holds position n of head h, prompt and
+    # generation block split at n_prompt, values beside their keys.
+    k, v = _coded_kv(n_prompt + n_gen, heads, d)
+    c = wo.cache_init(k, v, n_prompt, levels)
+    assert c["Kp"].shape == (heads, n_prompt, d) and c["Kg"].shape == (heads, n_gen, d)
+    for h in range(heads):
+        for n in range(n_prompt + n_gen):
+            for ch in range(d):
+                want = n + 1000 * h + 1e6 * ch
+                if n < n_prompt:
+                    assert c["Kp"][h, n, ch] == want and c["Vp"][h, n, ch] == -(want + 0.5)
+                else:
+                    g = n - n_prompt
+                    assert c["Kg"][h, g, ch] == want and c["Vg"][h, g, ch] == -(want + 0.5)
+
+
+@pytest.mark.parametrize("levels", [1, 2, 3])
+def test_cache_init_lowpass_closed_form(levels):
+    # A_L of the coded keys in closed form: the span of coarse position p
+    # holds positions p 2^L .. p 2^L + 2^L - 1, so
+    #   sum = 2^L (1000 h + 10^6 c) + 2^(2L) p + 2^(L-1) (2^L - 1)
+    # and A_L = 2^(-L/2) * sum (orthonormal Haar, scaled span sum).
+    n_prompt, n_gen, heads, d = 32, 4, 2, 3
+    k, v = _coded_kv(n_prompt + n_gen, heads, d)
+    a = wo.cache_init(k, v, n_prompt, levels)["a_l"]
+    span = 1 << levels
+    assert a.shape == (heads, n_prompt >> levels, d)
+    for h in range(heads):
+        for p in range(n_prompt >> levels):
+            for ch in range(d):
+                s = span * (1000 * h + 1e6 * ch) + span * span * p + (span // 2) * (span - 1)
+                assert a[h, p, ch] == pytest.approx(s * 2.0 ** (-levels / 2), rel=1e-14)
+
+
+def test_cache_init_round_trip_and_rejects():
+    rng = np.random.default_rng(11)
+    k, v = rng.standard_normal((2, 40, 3, 5))
+    c = wo.cache_init(k, v, 32, 2)
+    back = np.concatenate([c["Kp"], c["Kg"]], axis=1)
+    np.testing.assert_array_equal(np.swapaxes(back, 0, 1), k)
+    with pytest.raises(ValueError):
+        wo.cache_init(k, v[:, :2], 32, 2)
+    with pytest.raises(ValueError):
+        wo.cache_init(k, v, 0, 2)
+
+
+def test_cache_update_places_every_row():
+    # Eq. (4): generation row g of head h takes the new key of position g.
+    k, v = _coded_kv(5, 3, 2)
+    c = wo.cache_update(k, v)
+    for h in range(3):
+        for g in range(5):
+            for ch in range(2):
+                want = g + 1000 * h + 1e6 * ch
+                assert c["Kg"][h, g, ch] == want and c["Vg"][h, g, ch] == -(want + 0.5)

@@ -67,6 +67,47 @@ def _attn_no_scale(q, kp, vp, kg, vg, idx):
 
 
 _ORIG_ATTN = wo.sparse_attention
+_ORIG_INIT = wo.cache_init
+
+
+def _init_gen_block_first(k_all, v_all, n_prompt, levels):
+    # The generation block taken from the front of the sequence.
+    n_gen = np.shape(k_all)[0] - n_prompt
+    roll = lambda a: np.roll(np.asarray(a, np.float64), -n_gen, axis=0)
+    return _ORIG_INIT(roll(k_all), roll(v_all), n_prompt, levels)
+
+
+def _init_reshape_not_swap(k_all, v_all, n_prompt, levels):
+    # [N, H, d] reinterpreted as [H, N, d] instead of swapping the axes.
+    k = np.asarray(k_all, np.float64)
+    v = np.asarray(v_all, np.float64)
+    n, h, d = k.shape
+    flip = lambda a: np.swapaxes(a.reshape(h, n, d), 0, 1)
+    return _ORIG_INIT(flip(k), flip(v), n_prompt, levels)
+
+
+def _init_lowpass_of_values(k_all, v_all, n_prompt, levels):
+    c = _ORIG_INIT(k_all, v_all, n_prompt, levels)
+    c["a_l"] = _ORIG_INIT(v_all, k_all, n_prompt, levels)["a_l"]
+    return c
+
+
+def _init_keys_values_swapped(k_all, v_all, n_prompt, levels):
+    c = _ORIG_INIT(k_all, v_all, n_prompt, levels)
+    c["Vp"], c["Vg"] = _ORIG_INIT(v_all, v_all, n_prompt, levels)["Kp"], c["Kg"]
+    return c
+
+
+def _init_lowpass_unscaled(k_all, v_all, n_prompt, levels):
+    c = _ORIG_INIT(k_all, v_all, n_prompt, levels)
+    c["a_l"] = c["a_l"] * 2.0 ** (levels / 2)
+    return c
+
+
+def _update_heads_reshaped(k_gen, v_gen):
+    k = np.asarray(k_gen, np.float64)
+    g, h, d = k.shape
+    return {"Kg": k.reshape(h, g, d), "Vg": np.asarray(v_gen, np.float64).reshape(h, g, d)}
 
 PIN_TESTS = [
     lambda: pins.test_haar_worked_example(),
@@ -84,6 +125,10 @@ PIN_TESTS = [
     lambda: pins.test_full_budget_is_full_attention(),
     lambda: pins.test_sparse_attention_uses_only_selected_rows(),
     lambda: pins.test_lse_closed_forms(),
+    lambda: pins.test_cache_init_places_every_row(16, 3, 2, 3, 2),
+    lambda: pins.test_cache_init_lowpass_closed_form(2),
+    lambda: pins.test_cache_init_round_trip_and_rejects(),
+    lambda: pins.test_cache_update_places_every_row(),
 ]
 
 MUTANTS = [
@@ -96,6 +141,12 @@ MUTANTS = [
     ("top_k", _topk_smallest),
     ("sparse_attention", _attn_drop_generation_rows),
     ("sparse_attention", _attn_no_scale),
+    ("cache_init", _init_gen_block_first),
+    ("cache_init", _init_reshape_not_swap),
+    ("cache_init", _init_lowpass_of_values),
+    ("cache_init", _init_keys_values_swapped),
+    ("cache_init", _init_lowpass_unscaled),
+    ("cache_update", _update_heads_reshaped),
 ]
 
 
