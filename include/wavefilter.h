@@ -12,6 +12,11 @@
  *   wf_sparse_gather_attn §2.1 eq. (3) over the sparse cache S ∪ I_g
  *   wf_step               all four, in order, on one stream
  *
+ * and the cache writes around it:
+ *
+ *   wf_cache_init         §2.1 eq. (2) at t = 1, plus A_L of the prompt keys
+ *   wf_cache_update       §2.1 eq. (4) at t > 1 (generation rows)
+ *
  * Readings fixed where the pages are silent: orthonormal Haar filters
  * g = [1/√2, 1/√2] on 0-based pairs (2n, 2n+1), so coarse position p at
  * level j covers tokens [p·2^j, (p+1)·2^j); the score of a candidate is its
@@ -224,6 +229,40 @@ int wf_step_cached_al(const wf_dims* dims, const void* Q, const void* Kp,
                       const float* AL, const int32_t* k_per_level, float* O,
                       float* lse, int32_t* idx_out, void* workspace,
                       size_t workspace_bytes, void* stream);
+
+/* KV-cache initialisation at the first denoising step t = 1 (WaveFilter
+ * §2.1 eq. (2): the keys and values computed for every position enter the
+ * cache unchanged), with the level-L approximation of the prompt keys
+ * (§3.1; §1 extracts it at this initial step) written in the same pass, so
+ * that later steps can call wf_step_cached_al without reading Kp for it.
+ *   K, V   : device, [batch, n_prompt + n_gen, heads, head_dim] of
+ *            dims.dtype, token-major (each position's heads side by side,
+ *            the layout of the key/value projections' output); positions
+ *            0 .. N_p-1 are the prompt I_p, N_p .. N_p+G-1 the generation
+ *            block I_g
+ *   Kp, Vp : device, out, [batch, heads, n_prompt, head_dim] (dims.dtype)
+ *   Kg, Vg : device, out, [batch, heads, n_gen, head_dim] (dims.dtype)
+ *   AL     : device, out, nullable, [U, N_p/2^L, d] fp32: A_L of Kp, the
+ *            same values wf_dwt_lowpass computes (bit for bit)
+ * dims: the dims of the wf_step calls that will read this cache.  Outputs
+ * must not overlap the inputs.  One kernel launch.
+ * Errors: WF_ERR_NULL, WF_ERR_SHAPE, WF_ERR_UNSUPPORTED, WF_ERR_ALIGNMENT,
+ * WF_ERR_CUDA. */
+int wf_cache_init(const wf_dims* dims, const void* K, const void* V, void* Kp,
+                  void* Vp, void* Kg, void* Vg, float* AL, void* stream);
+
+/* Cache update at a denoising step t > 1 (WaveFilter §2.1 eq. (4)): the keys
+ * and values just computed for the generation positions replace the cached
+ * generation rows.  The prompt rows, and an A_L computed from them, stay
+ * valid.
+ *   K, V   : device, [batch, n_gen, heads, head_dim] of dims.dtype,
+ *            token-major
+ *   Kg, Vg : device, out, [batch, heads, n_gen, head_dim]
+ * dims: as for wf_step (n_prompt and levels are validated, not used).
+ * Outputs must not overlap the inputs.  One kernel launch.
+ * Errors: as wf_cache_init. */
+int wf_cache_update(const wf_dims* dims, const void* K, const void* V, void* Kg,
+                    void* Vg, void* stream);
 
 /* wf_step with host-resident inputs and outputs: copies Q/Kp/Vp/Kg/Vg from
  * HOST memory into the caller's device staging buffers (one

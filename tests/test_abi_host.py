@@ -170,3 +170,26 @@ def test_step_launch_count_validates(lib):
     assert out.value == -1
     assert lib.wf_step_launch_count(ctypes.byref(dims), k, ctypes.byref(out)) == 0
     assert out.value in (1, 2)
+
+
+def test_cache_writes_reject_before_launch(lib):
+    # wf_cache_init / wf_cache_update validate like the step entry points;
+    # every case below fails on the host, so nothing is enqueued.
+    dims = _dims()
+    p16 = ctypes.c_void_p(1 << 20)
+    p17 = ctypes.c_void_p((1 << 20) + 4)
+    init = lib.wf_cache_init
+    assert init(None, p16, p16, p16, p16, p16, p16, p16, None) == 1
+    assert init(ctypes.byref(dims), None, p16, p16, p16, p16, p16, None, None) == 1
+    assert init(ctypes.byref(dims), p16, p16, p16, p16, p16, None, None, None) == 1
+    assert init(ctypes.byref(dims), p17, p16, p16, p16, p16, p16, None, None) == 7
+    assert init(ctypes.byref(dims), p16, p16, p16, p16, p16, p16, p17, None) == 7  # AL
+    assert init(ctypes.byref(_dims(n_prompt=4100)), p16, p16, p16, p16, p16, p16, p16,
+                None) == 2
+    assert init(ctypes.byref(_dims(head_dim=96)), p16, p16, p16, p16, p16, p16, p16, None) == 3
+    assert init(ctypes.byref(_dims(dtype=3)), p16, p16, p16, p16, p16, p16, p16, None) == 3
+    upd = lib.wf_cache_update
+    assert upd(ctypes.byref(dims), p16, p16, None, p16, None) == 1
+    assert upd(ctypes.byref(dims), p16, p17, p16, p16, None) == 7
+    assert upd(ctypes.byref(_dims(n_gen=0)), p16, p16, p16, p16, None) == 2
+    assert upd(ctypes.byref(_dims(n_gen=65)), p16, p16, p16, p16, None) == 3

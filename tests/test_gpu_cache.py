@@ -1,0 +1,142 @@
+"""GPU parity of the KV-cache writes around the filtering path, through the C
+ABI: the first-step initialisation of WaveFilter §2.1 eq. (2) with A_L of the
+prompt keys (§3.1), and the generation-row update of eq. (4).
+
+Bars: every cache row bit-exact (the operation is a copy); A_L within 1e-3
+relative of the float64 oracle and bit-identical to wf_dwt_lowpass of the
+written prompt keys (the same summation order); the step that then reads the
+cache (wf_step_cached_al with this A_L) meets the whole-step contract.
+Inputs are rounded to the device type on the host, so the oracle sees the
+values the GPU sees.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.wavefilter_oracle as wo
+from gpu_common import AL_RTOL, compare_step_unit, run_step, to_device, torch_dtype
+from wavelet_guided_sparse_gb300 import binding as bd
+from wavelet_guided_sparse_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def _rounder(dtype):
+    return wl.round_to_bf16 if dtype == "bf16" else (lambda x: x.astype(np.float32))
+
+
+def _token_major(arrs):
+    """[b, H, rows, d] prompt and generation arrays -> token-major K, V
+    [b, N_p + G, H, d] (the projections' output layout)."""
+    k = np.concatenate([arrs["Kp"], arrs["Kg"]], axis=2).transpose(0, 2, 1, 3)
+    v = np.concatenate([arrs["Vp"], arrs["Vg"]], axis=2).transpose(0, 2, 1, 3)
+    return np.ascontiguousarray(k), np.ascontiguousarray(v)
+
+
+def _al_close(got, ref):
+    tol = AL_RTOL * np.abs(ref) + 1e-6 * np.sqrt((ref ** 2).mean())
+    return (np.abs(got - ref) <= tol).all()
+
+
+def _check_init(k, v, n_prompt, levels, dtype):
+    """Runs wf_cache_init on host-rounded K, V and compares every output."""
+    dt = torch_dtype(dtype)
+    kd = torch.from_numpy(k).to("cuda", dt)
+    vd = torch.from_numpy(v).to("cuda", dt)
+    out = bd.cache_init(kd, vd, n_prompt, levels)
+    al_dwt = bd.dwt_lowpass(out["Kp"], levels)
+    torch.cuda.synchronize()
+    assert torch.equal(out["AL"], al_dwt), "A_L differs from wf_dwt_lowpass"
+    got = {n: out[n].cpu().double().numpy() for n in ("Kp", "Vp", "Kg", "Vg", "AL")}
+    b, _, h, _ = k.shape
+    for bi in range(b):
+        ref = wo.cache_init(k[bi], v[bi], n_prompt, levels)
+        for n in ("Kp", "Vp", "Kg", "Vg"):
+            np.testing.assert_array_equal(got[n][bi], ref[n], err_msg=f"{n} sequence {bi}")
+        for hi in range(h):
+            assert _al_close(got["AL"][bi, hi], ref["a_l"][hi]), (bi, hi)
+    return out
+
+
+@pytest.mark.parametrize("b,h,n_prompt,g,d,levels,dtype", [
+    (2, 3, 128, 7, 128, 4, "bf16"),    # ragged G, two sequences
+    (1, 2, 256, 33, 64, 5, "f32"),     # d = 64 fp32, 32-row spans
+    (2, 2, 64, 1, 64, 1, "bf16"),      # one generation row, pairs
+    (1, 2, 3 * 128, 5, 64, 7, "bf16"), # 128-row spans (eight 16-row blocks)
+    (1, 1, 4096, 64, 128, 12, "f32"),  # one span of 4096 rows, G at its maximum
+])
+def test_cache_init_shapes(b, h, n_prompt, g, d, levels, dtype):
+    rng = np.random.default_rng(n_prompt * 7 + g)
+    rnd = _rounder(dtype)
+    k = rnd(rng.standard_normal((b, n_prompt + g, h, d)) * 1.5)
+    v = rnd(rng.standard_normal((b, n_prompt + g, h, d)))
+    _check_init(k, v, n_prompt, levels, dtype)
+
+
+@pytest.mark.parametrize("name", ["tiny", "llada8b_layer"])
+def test_cache_init_workload_then_step(name):
+    # The full layer of the workload: initialise the cache from token-major
+    # K/V, then run steps 2-5 on it with the A_L the initialisation wrote;
+    # every unit is held to the whole-step contract against the oracle.
+    cfg = wl.CONFIGS[name]
+    ks = cfg.k_per_level()
+    arrs = wl.generate_layer(cfg, 0)
+    arrs = {n: _rounder(cfg.dtype)(a) for n, a in arrs.items()}
+    k, v = _token_major(arrs)
+    out = _check_init(k, v, cfg.n_prompt, cfg.levels, cfg.dtype)
+    q = to_device({"Q": arrs["Q"]}, cfg.dtype)["Q"]
+    dev = {"Q": q, "Kp": out["Kp"], "Vp": out["Vp"], "Kg": out["Kg"], "Vg": out["Vg"]}
+    o, lse, idx, status = run_step(dev, cfg.levels, ks, al=out["AL"])
+    assert status == 0
+    o, lse, idx = o.cpu().numpy(), lse.cpu().numpy(), idx.cpu().numpy()
+    kinds = [compare_step_unit(arrs, 0, hi, cfg.levels, ks, idx[0, hi], o[0, hi], lse[0, hi])
+             for hi in range(cfg.heads)]
+    assert kinds.count("exact") >= len(kinds) // 2
+
+
+def test_cache_init_without_al_writes_the_same_cache():
+    rng = np.random.default_rng(5)
+    k = wl.round_to_bf16(rng.standard_normal((1, 136, 4, 128)))
+    v = wl.round_to_bf16(rng.standard_normal((1, 136, 4, 128)))
+    kd, vd = (torch.from_numpy(x).to("cuda", torch.bfloat16) for x in (k, v))
+    a = bd.cache_init(kd, vd, 128, 3)
+    b = bd.cache_init(kd, vd, 128, 3, with_al=False)
+    torch.cuda.synchronize()
+    assert "AL" not in b
+    for n in ("Kp", "Vp", "Kg", "Vg"):
+        assert torch.equal(a[n], b[n]), n
+
+
+@pytest.mark.parametrize("g,d,dtype", [(32, 128, "bf16"), (5, 64, "f32"), (64, 64, "bf16")])
+def test_cache_update_then_step(g, d, dtype):
+    # Eq. (4): new generation keys/values replace the cached ones; the prompt
+    # rows and A_L are untouched, and the next step attends over the new rows.
+    b, h, n_prompt, levels = 1, 3, 512, 3
+    rng = np.random.default_rng(g * 31 + d)
+    rnd = _rounder(dtype)
+    arrs = {"Q": rnd(rng.standard_normal((b, h, g, d)) * 1.5),
+            "Kp": rnd(rng.standard_normal((b, h, n_prompt, d)) * 1.5),
+            "Vp": rnd(rng.standard_normal((b, h, n_prompt, d))),
+            "Kg": rnd(rng.standard_normal((b, h, g, d)) * 1.5),
+            "Vg": rnd(rng.standard_normal((b, h, g, d)))}
+    k_new = rnd(rng.standard_normal((b, g, h, d)) * 1.5)
+    v_new = rnd(rng.standard_normal((b, g, h, d)))
+    dev = to_device(arrs, dtype)
+    al = bd.dwt_lowpass(dev["Kp"], levels)
+    kp_before = dev["Kp"].clone()
+    dt = torch_dtype(dtype)
+    bd.cache_update(torch.from_numpy(k_new).to("cuda", dt), torch.from_numpy(v_new).to("cuda", dt),
+                    dev["Kg"], dev["Vg"], n_prompt, levels)
+    torch.cuda.synchronize()
+    ref = wo.cache_update(k_new[0], v_new[0])
+    np.testing.assert_array_equal(dev["Kg"][0].cpu().double().numpy(), ref["Kg"])
+    np.testing.assert_array_equal(dev["Vg"][0].cpu().double().numpy(), ref["Vg"])
+    assert torch.equal(dev["Kp"], kp_before)
+    ks = bd.default_k_per_level(n_prompt, levels, 64)
+    o, lse, idx, status = run_step(dev, levels, ks, al=al)
+    assert status == 0
+    updated = dict(arrs, Kg=ref["Kg"][None], Vg=ref["Vg"][None])
+    o, lse, idx = o.cpu().numpy(), lse.cpu().numpy(), idx.cpu().numpy()
+    for hi in range(h):
+        compare_step_unit(updated, 0, hi, levels, ks, idx[0, hi], o[0, hi], lse[0, hi])

@@ -29,7 +29,8 @@ EXPORTS = ("wf_status_string", "wf_last_error_string", "wf_default_k_per_level",
            "wf_step_launch_count",
            "wf_clear_device_status", "wf_read_device_status", "wf_dwt_lowpass",
            "wf_score_topk", "wf_recursive_filter", "wf_sparse_gather_attn", "wf_step",
-           "wf_step_host", "wf_step_static_scratch", "wf_step_cached_al")
+           "wf_step_host", "wf_step_static_scratch", "wf_step_cached_al",
+           "wf_cache_init", "wf_cache_update")
 
 
 class WfError(RuntimeError):
@@ -73,6 +74,8 @@ _SIGS = {
                                               _vp, _vp, _vp]),
     "wf_step_cached_al": (ctypes.c_int, [_DIMSP, _vp, _vp, _vp, _vp, _vp, _vp, _i32p, _vp, _vp,
                                          _vp, _vp, _sz, _vp]),
+    "wf_cache_init": (ctypes.c_int, [_DIMSP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "wf_cache_update": (ctypes.c_int, [_DIMSP, _vp, _vp, _vp, _vp, _vp]),
 }
 
 
@@ -320,6 +323,44 @@ def step_static_scratch(q, kp, vp, kg, vg, levels: int, k_per_level: Sequence[in
         ctypes.byref(dims), _ptr(q), _ptr(kp), _ptr(vp), _ptr(kg), _ptr(vg),
         _k_array(k_per_level), _ptr(out), _ptr(lse), _ptr(idx_out), _stream(stream)))
     return out
+
+
+def cache_init(k: torch.Tensor, v: torch.Tensor, n_prompt: int, levels: int,
+               with_al: bool = True, out: Optional[dict] = None, stream=None) -> dict:
+    """Eq. (2) cache initialisation from token-major K, V [b, N_p + G, H, d]:
+    returns {"Kp", "Vp": [b, H, N_p, d], "Kg", "Vg": [b, H, G, d]} and, if
+    ``with_al``, "AL" [b, H, N_p/2^L, d] fp32.  ``out`` may supply the
+    destination tensors (same keys)."""
+    _require(k, "K")
+    _require(v, "V", k.dtype)
+    if k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("K and V must both be [batch, n_prompt + n_gen, heads, head_dim]")
+    b, n, h, d = k.shape
+    g = n - n_prompt
+    dims = Dims(b, h, n_prompt, g, d, levels, dtype_code(k.dtype))
+    o = dict(out or {})
+    for name, rows in (("Kp", n_prompt), ("Vp", n_prompt), ("Kg", g), ("Vg", g)):
+        if name not in o:
+            o[name] = torch.empty((b, h, rows, d), dtype=k.dtype, device=k.device)
+        _require(o[name], name, k.dtype)
+    if with_al and "AL" not in o:
+        o["AL"] = torch.empty((b, h, n_prompt >> levels, d), dtype=torch.float32,
+                              device=k.device)
+    _check("wf_cache_init", lib().wf_cache_init(
+        ctypes.byref(dims), _ptr(k), _ptr(v), _ptr(o["Kp"]), _ptr(o["Vp"]), _ptr(o["Kg"]),
+        _ptr(o["Vg"]), _ptr(o.get("AL")) if with_al else None, _stream(stream)))
+    return o
+
+
+def cache_update(k: torch.Tensor, v: torch.Tensor, kg: torch.Tensor, vg: torch.Tensor,
+                 n_prompt: int, levels: int, stream=None) -> None:
+    """Eq. (4) cache update: token-major K, V [b, G, H, d] into Kg, Vg [b, H, G, d]."""
+    for t, name in ((k, "K"), (v, "V"), (kg, "Kg"), (vg, "Vg")):
+        _require(t, name, k.dtype)
+    b, g, h, d = k.shape
+    dims = Dims(b, h, n_prompt, g, d, levels, dtype_code(k.dtype))
+    _check("wf_cache_update", lib().wf_cache_update(ctypes.byref(dims), _ptr(k), _ptr(v),
+                                                    _ptr(kg), _ptr(vg), _stream(stream)))
 
 
 def raw_call(name: str, *args) -> int:

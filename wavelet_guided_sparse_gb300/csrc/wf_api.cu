@@ -1,6 +1,7 @@
 // C ABI of the WaveFilter KV-filtering path: argument validation, workspace
-// layout and the step driver.  Kernels live in wf_dwt.cu (step 1) and
-// wf_path.cu (steps 2-5, one cluster kernel whose phases the entry points select).
+// layout and the step driver.  Kernels live in wf_dwt.cu (step 1),
+// wf_path.cu (steps 2-5, one cluster kernel whose phases the entry points
+// select) and wf_cache.cu (the cache writes of eqs. (2) and (4)).
 //
 // Every entry point validates on the host first and enqueues nothing on a
 // validation error.  Nothing here allocates device memory or synchronises,
@@ -40,6 +41,7 @@ int check_dims(const wf_dims* d, LaunchDims* ld) {
   const int64_t units = static_cast<int64_t>(d->batch) * d->heads;
   if (units > 65535) return WF_ERR_UNSUPPORTED;  // one grid row per unit
   ld->units = units;
+  ld->batch = d->batch;
   ld->n_prompt = d->n_prompt;
   ld->n_gen = d->n_gen;
   ld->head_dim = d->head_dim;
@@ -206,6 +208,32 @@ int wf_dwt_lowpass(const wf_dims* dims, const void* Kp, float* AL, float* A_all,
     }
   }
   return cuda_status(e);
+}
+
+int wf_cache_init(const wf_dims* dims, const void* K, const void* V, void* Kp, void* Vp,
+                  void* Kg, void* Vg, float* AL, void* stream) {
+  LaunchDims ld;
+  int st = check_dims(dims, &ld);
+  if (st != WF_OK) return st;
+  if (K == nullptr || V == nullptr || Kp == nullptr || Vp == nullptr || Kg == nullptr ||
+      Vg == nullptr)
+    return WF_ERR_NULL;
+  if (!aligned16(K) || !aligned16(V) || !aligned16(Kp) || !aligned16(Vp) || !aligned16(Kg) ||
+      !aligned16(Vg) || (AL && !aligned16(AL)))
+    return WF_ERR_ALIGNMENT;
+  return cuda_status(wf::launch_cache_init(ld, K, V, Kp, Vp, Kg, Vg, AL,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+int wf_cache_update(const wf_dims* dims, const void* K, const void* V, void* Kg, void* Vg,
+                    void* stream) {
+  LaunchDims ld;
+  int st = check_dims(dims, &ld);
+  if (st != WF_OK) return st;
+  if (K == nullptr || V == nullptr || Kg == nullptr || Vg == nullptr) return WF_ERR_NULL;
+  if (!aligned16(K) || !aligned16(V) || !aligned16(Kg) || !aligned16(Vg)) return WF_ERR_ALIGNMENT;
+  return cuda_status(
+      wf::launch_cache_update(ld, K, V, Kg, Vg, static_cast<cudaStream_t>(stream)));
 }
 
 int wf_score_topk(const wf_dims* dims, const void* Q, const float* AL, int32_t k_L,

@@ -1,5 +1,6 @@
 // Host-side interface between the C-ABI layer (wf_api.cu) and the kernel
-// launchers (wf_dwt.cu: step 1; wf_path.cu: steps 2-5).
+// launchers (wf_dwt.cu: step 1; wf_path.cu: steps 2-5; wf_cache.cu: the
+// cache writes of eqs. (2) and (4)).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -16,6 +17,7 @@ namespace wf {
 // Validated sizes handed to the launchers.
 struct LaunchDims {
   int64_t units;  // batch * heads
+  int batch;
   int n_prompt;
   int n_gen;
   int head_dim;
@@ -79,6 +81,14 @@ cudaError_t launch_dwt_lowpass(const LaunchDims& ld, const void* kp, float* out,
                                cudaStream_t stream);
 cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathArgs& args,
                         cudaStream_t stream);
+
+// Cache initialisation (eq. (2)) from token-major K/V [batch, N_p + G,
+// heads, d] into Kp/Vp/Kg/Vg, with fp32 A_L of the prompt keys if `al` is
+// set; and the generation-row update (eq. (4)) from [batch, G, heads, d].
+cudaError_t launch_cache_init(const LaunchDims& ld, const void* k, const void* v, void* kp,
+                              void* vp, void* kg, void* vg, float* al, cudaStream_t stream);
+cudaError_t launch_cache_update(const LaunchDims& ld, const void* k, const void* v, void* kg,
+                                void* vg, cudaStream_t stream);
 
 // Dynamic shared memory the planners allow per CTA (the sm_103a opt-in limit
 // is 227 KB; a little is left for static shared memory).
