@@ -56,7 +56,7 @@ __device__ __forceinline__ void st_row(unsigned char* p, const uint4& x) {
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) cache_write_kernel(CacheParams p) {
+__global__ void __launch_bounds__(kThreads, 3) cache_write_kernel(CacheParams p) {
   constexpr int E = static_cast<int>(sizeof(T));
   constexpr int V = Elem<T>::kPer16B;  // elements per 16-byte chunk
   constexpr int C = D / V;             // chunks per row
@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kThreads) cache_write_kernel(CacheParams p) {
     const unsigned char* src =
         (is_v ? p.v : p.k) + (b * p.n_tok + tok0) * src_row + h * RB + c * 16;
     unsigned char* dst = (is_v ? p.vp : p.kp) + (u * p.n_prompt + tok0) * RB + c * 16;
-    const bool sum = !is_v && p.al != nullptr;
+    float* al = (!is_v && p.al != nullptr) ? p.al + (u * P + pos) * D + c * V : nullptr;
     float acc[V], blk[V];
 #pragma unroll
     for (int e = 0; e < V; ++e) acc[e] = blk[e] = 0.f;
@@ -89,11 +89,13 @@ __global__ void __launch_bounds__(kThreads) cache_write_kernel(CacheParams p) {
       uint4 x[kBatchRows];
 #pragma unroll
       for (int i = 0; i < kBatchRows; ++i)
-        if (i < nb) x[i] = ld_stream(src + (r0 + i) * src_row);
+        if (i < nb) x[i] = ld_stream(src + i * src_row);
 #pragma unroll
       for (int i = 0; i < kBatchRows; ++i)
-        if (i < nb) st_row(dst + static_cast<int64_t>(r0 + i) * RB, x[i]);
-      if (sum) {
+        if (i < nb) st_row(dst + i * RB, x[i]);
+      src += kBatchRows * src_row;
+      dst += kBatchRows * RB;
+      if (al != nullptr) {
 #pragma unroll
         for (int i = 0; i < kBatchRows; ++i) {
           if (i < nb) {
@@ -113,8 +115,8 @@ __global__ void __launch_bounds__(kThreads) cache_write_kernel(CacheParams p) {
         }
       }
     }
-    if (sum) {
-      float4* o = reinterpret_cast<float4*>(p.al + (u * P + pos) * D + c * V);
+    if (al != nullptr) {
+      float4* o = reinterpret_cast<float4*>(al);
 #pragma unroll
       for (int e = 0; e < V; e += 4)
         o[e / 4] = make_float4(acc[e] * p.scale, acc[e + 1] * p.scale, acc[e + 2] * p.scale,
