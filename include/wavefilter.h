@@ -277,6 +277,30 @@ int wf_step_host(const wf_dims* dims, const void* h_Q, const void* h_Kp,
                  float* d_O, float* d_lse, void* workspace,
                  size_t workspace_bytes, void* stream);
 
+/* One denoising step t > 1 with a device-resident cache and host-resident
+ * per-step data: the serving loop that wf_cache_init (at t = 1),
+ * wf_cache_update and wf_step_cached_al make possible.  On `stream`, in order:
+ * copies Q and the generation block's new keys/values from HOST memory into
+ * the device staging buffers (one cudaMemcpyAsync each), writes the new rows
+ * into Kg/Vg (eq. (4), as wf_cache_update), runs wf_step_cached_al on the
+ * cache, and copies O back to HOST memory.  Pinned host memory gives
+ * asynchronous copies.  Does not synchronise.
+ *   h_Q        : HOST, [batch, heads, n_gen, head_dim] (dims.dtype)
+ *   h_K, h_V   : HOST, [batch, n_gen, heads, head_dim] token-major new rows
+ *   h_O        : HOST, out, [batch, heads, n_gen, head_dim] fp32
+ *   d_Q, d_K, d_V, d_O : device staging buffers of the same sizes
+ *   Kp, Vp, AL : device, the resident prompt cache and its A_L (wf_cache_init)
+ *   Kg, Vg     : device, in/out, the generation rows of the cache
+ *   k_per_level, workspace : as wf_step
+ * Every argument is validated before anything is enqueued.
+ * Errors: as wf_step_cached_al. */
+int wf_decode_step_host(const wf_dims* dims, const void* h_Q, const void* h_K,
+                        const void* h_V, const int32_t* k_per_level, float* h_O,
+                        void* d_Q, void* d_K, void* d_V, const void* Kp,
+                        const void* Vp, void* Kg, void* Vg, const float* AL,
+                        float* d_O, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
 /* Size of the device scratch array behind wf_step_static_scratch (48 MiB). */
 #define WF_STATIC_SCRATCH_BYTES (48u << 20)
 

@@ -193,3 +193,27 @@ def test_cache_writes_reject_before_launch(lib):
     assert upd(ctypes.byref(dims), p16, p17, p16, p16, None) == 7
     assert upd(ctypes.byref(_dims(n_gen=0)), p16, p16, p16, p16, None) == 2
     assert upd(ctypes.byref(_dims(n_gen=65)), p16, p16, p16, p16, None) == 3
+
+
+def test_decode_step_host_rejects_before_copies(lib):
+    # Every argument of the host-buffer decode step is validated before its
+    # first copy is enqueued.
+    dims = _dims()
+    k = bd._k_array([512, 512, 256, 128, 64])
+    p16 = ctypes.c_void_p(1 << 20)
+    p17 = ctypes.c_void_p((1 << 20) + 4)
+    f = lib.wf_decode_step_host
+
+    def call(dims=dims, k=k, h=p16, dq=p16, al=p16, ws=p16, wsb=1 << 40):
+        return f(ctypes.byref(dims), h, h, h, k, h, dq, p16, p16, p16, p16, p16, p16, al, p16,
+                 ws, wsb, None)
+
+    assert call(h=None) == 1
+    assert call(al=None) == 1
+    assert call(ws=None) == 1
+    assert call(dq=p17) == 7
+    assert call(al=p17) == 7
+    assert call(wsb=16) == 4
+    assert call(k=bd._k_array([512, 512, 256, 128, 300])) == 2
+    assert call(dims=_dims(n_prompt=4100)) == 2
+    assert call(dims=_dims(head_dim=96)) == 3

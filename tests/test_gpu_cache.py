@@ -140,3 +140,50 @@ def test_cache_update_then_step(g, d, dtype):
     o, lse, idx = o.cpu().numpy(), lse.cpu().numpy(), idx.cpu().numpy()
     for hi in range(h):
         compare_step_unit(updated, 0, hi, levels, ks, idx[0, hi], o[0, hi], lse[0, hi])
+
+
+def test_decode_step_host_matches_device_path():
+    # The host-buffer serving step (copies, eq. (4) update, cached step, copy
+    # back) on the 4096-token layer: the same O as the device-only calls, bit
+    # for bit, and every unit within the step contract for the updated cache.
+    cfg = wl.CONFIGS["llada8b_layer"]
+    ks = cfg.k_per_level()
+    arrs = {n: wl.round_to_bf16(a) for n, a in wl.generate_layer(cfg, 0).items()}
+    rng = np.random.default_rng(77)
+    b, h, g, d = arrs["Q"].shape
+    k_new = wl.round_to_bf16(rng.standard_normal((b, g, h, d)) * 1.5)
+    v_new = wl.round_to_bf16(rng.standard_normal((b, g, h, d)))
+    k, v = _token_major(arrs)
+    kd, vd = (torch.from_numpy(x).to("cuda", torch.bfloat16) for x in (k, v))
+    caches = [bd.cache_init(kd, vd, cfg.n_prompt, cfg.levels) for _ in range(2)]
+    dims = bd.Dims(b, h, cfg.n_prompt, g, d, cfg.levels, bd.WF_BF16)
+    ws = bd.alloc_workspace(dims, ks, kd.device)
+    # Device-only path on cache 0.
+    q_dev = torch.from_numpy(arrs["Q"]).to("cuda", torch.bfloat16)
+    kn_dev = torch.from_numpy(k_new).to("cuda", torch.bfloat16)
+    vn_dev = torch.from_numpy(v_new).to("cuda", torch.bfloat16)
+    c0 = caches[0]
+    bd.cache_update(kn_dev, vn_dev, c0["Kg"], c0["Vg"], cfg.n_prompt, cfg.levels)
+    ref = bd.step_cached_al(q_dev, c0["Kp"], c0["Vp"], c0["Kg"], c0["Vg"], c0["AL"], cfg.levels,
+                            ks, ws)
+    # Host-buffer path on cache 1.
+    host = {"Q": q_dev.cpu().pin_memory(), "K": kn_dev.cpu().pin_memory(),
+            "V": vn_dev.cpu().pin_memory(),
+            "O": torch.empty((b, h, g, d), dtype=torch.float32).pin_memory()}
+    stage = {"Q": torch.empty_like(q_dev), "K": torch.empty_like(kn_dev),
+             "V": torch.empty_like(vn_dev), "O": torch.empty_like(ref)}
+    bd.decode_step_host(dims, host, ks, stage, caches[1], ws)
+    torch.cuda.synchronize()
+    assert bd.read_device_status(ws) == 0
+    assert torch.equal(host["O"], ref.cpu())
+    assert torch.equal(caches[1]["Kg"], c0["Kg"]) and torch.equal(caches[1]["Vg"], c0["Vg"])
+    upd = wo.cache_update(k_new[0], v_new[0])
+    updated = dict(arrs, Kg=upd["Kg"][None], Vg=upd["Vg"][None])
+    o = host["O"].numpy()
+    idx = torch.empty((b, h, ks[0]), dtype=torch.int32, device="cuda")
+    bd.step_cached_al(q_dev, c0["Kp"], c0["Vp"], c0["Kg"], c0["Vg"], c0["AL"], cfg.levels, ks,
+                      ws, idx_out=idx)
+    idx = idx.cpu().numpy()
+    kinds = [compare_step_unit(updated, 0, hi, cfg.levels, ks, idx[0, hi], o[0, hi])
+             for hi in range(h)]
+    assert kinds.count("exact") >= len(kinds) // 2

@@ -30,7 +30,7 @@ EXPORTS = ("wf_status_string", "wf_last_error_string", "wf_default_k_per_level",
            "wf_clear_device_status", "wf_read_device_status", "wf_dwt_lowpass",
            "wf_score_topk", "wf_recursive_filter", "wf_sparse_gather_attn", "wf_step",
            "wf_step_host", "wf_step_static_scratch", "wf_step_cached_al",
-           "wf_cache_init", "wf_cache_update")
+           "wf_cache_init", "wf_cache_update", "wf_decode_step_host")
 
 
 class WfError(RuntimeError):
@@ -76,6 +76,8 @@ _SIGS = {
                                          _vp, _vp, _sz, _vp]),
     "wf_cache_init": (ctypes.c_int, [_DIMSP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "wf_cache_update": (ctypes.c_int, [_DIMSP, _vp, _vp, _vp, _vp, _vp]),
+    "wf_decode_step_host": (ctypes.c_int, [_DIMSP, _vp, _vp, _vp, _i32p, _vp, _vp, _vp, _vp,
+                                           _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
 }
 
 
@@ -361,6 +363,20 @@ def cache_update(k: torch.Tensor, v: torch.Tensor, kg: torch.Tensor, vg: torch.T
     dims = Dims(b, h, n_prompt, g, d, levels, dtype_code(k.dtype))
     _check("wf_cache_update", lib().wf_cache_update(ctypes.byref(dims), _ptr(k), _ptr(v),
                                                     _ptr(kg), _ptr(vg), _stream(stream)))
+
+
+def decode_step_host(dims: Dims, host: dict, k_per_level: Sequence[int], stage: dict,
+                     cache: dict, ws: torch.Tensor, stream=None) -> None:
+    """wf_decode_step_host: pinned host Q [b, H, G, d], new token-major K, V
+    [b, G, H, d] and O out (keys Q, K, V, O of ``host``); device staging
+    buffers of the same names in ``stage``; the resident cache (Kp, Vp, Kg, Vg,
+    AL) in ``cache``, whose Kg/Vg receive the new rows."""
+    _check("wf_decode_step_host", lib().wf_decode_step_host(
+        ctypes.byref(dims), _ptr(host["Q"]), _ptr(host["K"]), _ptr(host["V"]),
+        _k_array(k_per_level), _ptr(host["O"]), _ptr(stage["Q"]), _ptr(stage["K"]),
+        _ptr(stage["V"]), _ptr(cache["Kp"]), _ptr(cache["Vp"]), _ptr(cache["Kg"]),
+        _ptr(cache["Vg"]), _ptr(cache["AL"]), _ptr(stage["O"]), _ptr(ws), ws.numel(),
+        _stream(stream)))
 
 
 def raw_call(name: str, *args) -> int:

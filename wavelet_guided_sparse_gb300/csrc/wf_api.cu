@@ -423,6 +423,45 @@ int wf_step_cached_al(const wf_dims* dims, const void* Q, const void* Kp, const 
   return cuda_status(wf::launch_path(ld, plan, a, static_cast<cudaStream_t>(stream)));
 }
 
+int wf_decode_step_host(const wf_dims* dims, const void* h_Q, const void* h_K, const void* h_V,
+                        const int32_t* k_per_level, float* h_O, void* d_Q, void* d_K,
+                        void* d_V, const void* Kp, const void* Vp, void* Kg, void* Vg,
+                        const float* AL, float* d_O, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  LaunchDims ld;
+  int st = check_dims(dims, &ld);
+  if (st != WF_OK) return st;
+  if (h_Q == nullptr || h_K == nullptr || h_V == nullptr || h_O == nullptr ||
+      d_Q == nullptr || d_K == nullptr || d_V == nullptr || Kp == nullptr || Vp == nullptr ||
+      Kg == nullptr || Vg == nullptr || AL == nullptr || d_O == nullptr || workspace == nullptr)
+    return WF_ERR_NULL;
+  if (!aligned16(d_Q) || !aligned16(d_K) || !aligned16(d_V) || !aligned16(Kp) ||
+      !aligned16(Vp) || !aligned16(Kg) || !aligned16(Vg) || !aligned16(AL) || !aligned16(d_O) ||
+      !aligned16(workspace))
+    return WF_ERR_ALIGNMENT;
+  st = check_k(ld, k_per_level);
+  if (st != WF_OK) return st;
+  // Everything the cached step checks, before any copy is enqueued.
+  wf::PathPlan plan;
+  if (!wf::plan_path(ld, wf::kPhaseAll, k_per_level, k_per_level[ld.levels], k_per_level[0],
+                     wf::device_sm_count(), &plan))
+    return WF_ERR_UNSUPPORTED;
+  if (workspace_bytes < layout(ld, k_per_level, &plan).total) return WF_ERR_WORKSPACE;
+  const size_t gen_bytes =
+      static_cast<size_t>(ld.units) * ld.n_gen * ld.head_dim * elem_bytes(ld.dtype);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t ce = cudaMemcpyAsync(d_Q, h_Q, gen_bytes, cudaMemcpyHostToDevice, s);
+  if (ce == cudaSuccess) ce = cudaMemcpyAsync(d_K, h_K, gen_bytes, cudaMemcpyHostToDevice, s);
+  if (ce == cudaSuccess) ce = cudaMemcpyAsync(d_V, h_V, gen_bytes, cudaMemcpyHostToDevice, s);
+  if (ce == cudaSuccess) ce = wf::launch_cache_update(ld, d_K, d_V, Kg, Vg, s);
+  if (ce != cudaSuccess) return cuda_status(ce);
+  st = wf_step_cached_al(dims, d_Q, Kp, Vp, Kg, Vg, AL, k_per_level, d_O, nullptr, nullptr,
+                         workspace, workspace_bytes, stream);
+  if (st != WF_OK) return st;
+  return cuda_status(cudaMemcpyAsync(h_O, d_O, sizeof(float) * ld.units * ld.n_gen * ld.head_dim,
+                                     cudaMemcpyDeviceToHost, s));
+}
+
 int wf_step_host(const wf_dims* dims, const void* h_Q, const void* h_Kp, const void* h_Vp,
                  const void* h_Kg, const void* h_Vg, const int32_t* k_per_level, float* h_O,
                  float* h_lse, void* d_Q, void* d_Kp, void* d_Vp, void* d_Kg, void* d_Vg,
