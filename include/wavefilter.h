@@ -281,7 +281,8 @@ int wf_step_host(const wf_dims* dims, const void* h_Q, const void* h_Kp,
  * per-step data: the serving loop that wf_cache_init (at t = 1),
  * wf_cache_update and wf_step_cached_al make possible.  On `stream`, in order:
  * copies Q and the generation block's new keys/values from HOST memory into
- * the device staging buffers (one cudaMemcpyAsync each), writes the new rows
+ * the device staging buffers (one cudaMemcpyAsync each, or a single one when
+ * h_Q, h_K, h_V and d_Q, d_K, d_V each lie back to back), writes the new rows
  * into Kg/Vg (eq. (4), as wf_cache_update), runs wf_step_cached_al on the
  * cache, and copies O back to HOST memory.  Pinned host memory gives
  * asynchronous copies.  Does not synchronise.

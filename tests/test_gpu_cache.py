@@ -142,7 +142,8 @@ def test_cache_update_then_step(g, d, dtype):
         compare_step_unit(updated, 0, hi, levels, ks, idx[0, hi], o[0, hi], lse[0, hi])
 
 
-def test_decode_step_host_matches_device_path():
+@pytest.mark.parametrize("packed", [False, True])
+def test_decode_step_host_matches_device_path(packed):
     # The host-buffer serving step (copies, eq. (4) update, cached step, copy
     # back) on the 4096-token layer: the same O as the device-only calls, bit
     # for bit, and every unit within the step contract for the updated cache.
@@ -167,11 +168,22 @@ def test_decode_step_host_matches_device_path():
     ref = bd.step_cached_al(q_dev, c0["Kp"], c0["Vp"], c0["Kg"], c0["Vg"], c0["AL"], cfg.levels,
                             ks, ws)
     # Host-buffer path on cache 1.
-    host = {"Q": q_dev.cpu().pin_memory(), "K": kn_dev.cpu().pin_memory(),
-            "V": vn_dev.cpu().pin_memory(),
-            "O": torch.empty((b, h, g, d), dtype=torch.float32).pin_memory()}
-    stage = {"Q": torch.empty_like(q_dev), "K": torch.empty_like(kn_dev),
-             "V": torch.empty_like(vn_dev), "O": torch.empty_like(ref)}
+    if packed:  # Q, K, V back to back on both sides: one host-to-device copy
+        n_el = q_dev.numel()
+        h_pack = torch.empty(3 * n_el, dtype=torch.bfloat16).pin_memory()
+        d_pack = torch.empty(3 * n_el, dtype=torch.bfloat16, device="cuda")
+        host, stage = {}, {}
+        for i, (name, t) in enumerate((("Q", q_dev), ("K", kn_dev), ("V", vn_dev))):
+            host[name] = h_pack[i * n_el:(i + 1) * n_el].view(t.shape)
+            host[name].copy_(t.cpu())
+            stage[name] = d_pack[i * n_el:(i + 1) * n_el].view(t.shape)
+    else:
+        host = {"Q": q_dev.cpu().pin_memory(), "K": kn_dev.cpu().pin_memory(),
+                "V": vn_dev.cpu().pin_memory()}
+        stage = {"Q": torch.empty_like(q_dev), "K": torch.empty_like(kn_dev),
+                 "V": torch.empty_like(vn_dev)}
+    host["O"] = torch.empty((b, h, g, d), dtype=torch.float32).pin_memory()
+    stage["O"] = torch.empty_like(ref)
     bd.decode_step_host(dims, host, ks, stage, caches[1], ws)
     torch.cuda.synchronize()
     assert bd.read_device_status(ws) == 0

@@ -450,9 +450,20 @@ int wf_decode_step_host(const wf_dims* dims, const void* h_Q, const void* h_K, c
   const size_t gen_bytes =
       static_cast<size_t>(ld.units) * ld.n_gen * ld.head_dim * elem_bytes(ld.dtype);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t ce = cudaMemcpyAsync(d_Q, h_Q, gen_bytes, cudaMemcpyHostToDevice, s);
-  if (ce == cudaSuccess) ce = cudaMemcpyAsync(d_K, h_K, gen_bytes, cudaMemcpyHostToDevice, s);
-  if (ce == cudaSuccess) ce = cudaMemcpyAsync(d_V, h_V, gen_bytes, cudaMemcpyHostToDevice, s);
+  // Q, K and V laid out back to back on both sides travel as one copy.
+  const auto at = [gen_bytes](const void* p, int i) {
+    return static_cast<const char*>(p) + i * gen_bytes;
+  };
+  const bool packed = h_K == at(h_Q, 1) && h_V == at(h_Q, 2) && d_K == at(d_Q, 1) &&
+                      d_V == at(d_Q, 2);
+  cudaError_t ce;
+  if (packed) {
+    ce = cudaMemcpyAsync(d_Q, h_Q, 3 * gen_bytes, cudaMemcpyHostToDevice, s);
+  } else {
+    ce = cudaMemcpyAsync(d_Q, h_Q, gen_bytes, cudaMemcpyHostToDevice, s);
+    if (ce == cudaSuccess) ce = cudaMemcpyAsync(d_K, h_K, gen_bytes, cudaMemcpyHostToDevice, s);
+    if (ce == cudaSuccess) ce = cudaMemcpyAsync(d_V, h_V, gen_bytes, cudaMemcpyHostToDevice, s);
+  }
   if (ce == cudaSuccess) ce = wf::launch_cache_update(ld, d_K, d_V, Kg, Vg, s);
   if (ce != cudaSuccess) return cuda_status(ce);
   st = wf_step_cached_al(dims, d_Q, Kp, Vp, Kg, Vg, AL, k_per_level, d_O, nullptr, nullptr,
