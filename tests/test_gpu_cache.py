@@ -199,3 +199,37 @@ def test_decode_step_host_matches_device_path(packed):
     kinds = [compare_step_unit(updated, 0, hi, cfg.levels, ks, idx[0, hi], o[0, hi])
              for hi in range(h)]
     assert kinds.count("exact") >= len(kinds) // 2
+
+
+def test_cache_init_batched_long_sampled():
+    # The largest workload's full launch shape (2 sequences x 32 heads x
+    # 131072 + 64 positions, L = 7): token-major K/V of 2.15 GB each, so source
+    # and cache byte offsets pass 2^31.  The first and last head of the last
+    # sequence carry the workload's generated units and are checked against
+    # the oracle; every other head is zero and must stay zero.
+    cfg = wl.CONFIGS["batched_long_1pct"]
+    b, h, n_p, g, d = cfg.batch, cfg.heads, cfg.n_prompt, cfg.n_gen, cfg.head_dim
+    k = torch.zeros((b, n_p + g, h, d), dtype=torch.bfloat16)
+    v = torch.zeros((b, n_p + g, h, d), dtype=torch.bfloat16)
+    seq, heads = b - 1, (0, h - 1)
+    units = {}
+    for hi in heads:
+        u = wl.generate_unit(cfg, seq, 0, hi)
+        units[hi] = (np.concatenate([u["Kp"], u["Kg"]]), np.concatenate([u["Vp"], u["Vg"]]))
+        k[seq, :, hi] = torch.from_numpy(units[hi][0]).to(torch.bfloat16)
+        v[seq, :, hi] = torch.from_numpy(units[hi][1]).to(torch.bfloat16)
+    out = bd.cache_init(k.cuda(), v.cuda(), n_p, cfg.levels)
+    del k, v
+    torch.cuda.synchronize()
+    for hi in heads:
+        ku, vu = units[hi]
+        ref = wo.cache_init(ku[:, None], vu[:, None], n_p, cfg.levels)
+        for n in ("Kp", "Vp", "Kg", "Vg"):
+            np.testing.assert_array_equal(out[n][seq, hi].cpu().double().numpy(), ref[n][0],
+                                          err_msg=f"{n} head {hi}")
+        assert _al_close(out["AL"][seq, hi].cpu().double().numpy(), ref["a_l"][0]), hi
+    mask = torch.ones((b, h), dtype=torch.bool)
+    for hi in heads:
+        mask[seq, hi] = False
+    for n in ("Kp", "Vp", "Kg", "Vg", "AL"):
+        assert int(torch.count_nonzero(out[n][mask.cuda()])) == 0, n
