@@ -28,6 +28,13 @@ one plainest consistent with the rest):
   * Top-K order: larger score first, equal scores -> lower position first.
   * The sparse cache is the selected prompt tokens (ascending) followed by
     all generation positions; eq. (3) attention over it, no mask.
+  * Longer bases (psi is open): the extremal-phase Daubechies filters with N
+    vanishing moments (N = 1 is Haar), each level extended periodically; the
+    recursive filter then keeps the pyramid's index tree (children 2p, 2p+1)
+    and scores A_j of that basis.
+  * Cache writes: eq. (2) stores the keys/values of every position at t = 1
+    (token-major input, head-major cache, prompt positions first), eq. (4)
+    replaces the generation rows at t > 1.
 
 Everything is float64 numpy, one unit (sequence, layer, head) at a time,
 with no blocking or fusion beyond the definitions above.
@@ -56,6 +63,10 @@ __all__ = [
     "wavefilter_step_batched",
     "cache_init",
     "cache_update",
+    "daubechies_lowpass",
+    "dwt_analysis_step",
+    "dwt_synthesis_step",
+    "wavelet_pyramid",
 ]
 
 
@@ -153,7 +164,7 @@ def top_k(scores: np.ndarray, positions: np.ndarray, k: int):
 
 
 def recursive_filter(q: np.ndarray, kp: np.ndarray, levels: int,
-                     k_per_level: Sequence[int]) -> Dict:
+                     k_per_level: Sequence[int], lowpass=None) -> Dict:
     """Coarse Top-K plus multi-scale recursive filtering (WaveFilter §3.1-§3.2,
     Fig. 2(b)-(d)).
 
@@ -162,10 +173,14 @@ def recursive_filter(q: np.ndarray, kp: np.ndarray, levels: int,
     j+1 survivors, scored against A_j; keep k_j.  Level 0 yields the final
     token set S (k_0 = B tokens, ascending).
 
+    ``lowpass``: None for the Haar pyramid, else the low-pass filter of
+    another orthonormal basis (``daubechies_lowpass``); the candidates still
+    follow the pyramid's index tree, A_j comes from :func:`wavelet_pyramid`.
+
     Returns {"idx": S, "levels": {j: {"cand", "scores", "sel", "gap"}}}.
     """
     q = np.asarray(q, dtype=np.float64)
-    pyr = haar_pyramid(kp, levels)
+    pyr = haar_pyramid(kp, levels) if lowpass is None else wavelet_pyramid(kp, levels, lowpass)
     if len(k_per_level) != levels + 1:
         raise ValueError("k_per_level needs levels + 1 entries")
     per_level = {}
@@ -202,15 +217,18 @@ def sparse_attention(q, kp, vp, kg, vg, idx):
     return out, lse
 
 
-def wavefilter_step(q, kp, vp, kg, vg, levels: int, k_per_level: Sequence[int]) -> Dict:
+def wavefilter_step(q, kp, vp, kg, vg, levels: int, k_per_level: Sequence[int],
+                    lowpass=None) -> Dict:
     """Whole path for one unit: DWT -> coarse Top-K -> recursive filtering ->
     sparse cache -> eq. (3) attention.  Returns the selection record plus
-    "out" [G, d], "lse" [G] and "a_l" (the level-L approximation)."""
-    sel = recursive_filter(q, kp, levels, k_per_level)
+    "out" [G, d], "lse" [G] and "a_l" (the level-L approximation).
+    ``lowpass`` as in :func:`recursive_filter` (None: Haar)."""
+    sel = recursive_filter(q, kp, levels, k_per_level, lowpass)
     out, lse = sparse_attention(q, kp, vp, kg, vg, sel["idx"])
     sel["out"] = out
     sel["lse"] = lse
-    sel["a_l"] = haar_pyramid(kp, levels)[levels]
+    sel["a_l"] = (haar_pyramid(kp, levels) if lowpass is None
+                  else wavelet_pyramid(kp, levels, lowpass))[levels]
     return sel
 
 
@@ -273,3 +291,94 @@ def cache_update(k_gen, v_gen) -> Dict:
     if k.ndim != 3 or k.shape != v.shape:
         raise ValueError("K and V must both be [G, H, d]")
     return {"Kg": np.swapaxes(k, 0, 1), "Vg": np.swapaxes(v, 0, 1)}
+
+
+# ------------------------------------------------------------------------
+# Longer orthonormal bases.  §3.1 leaves the basis psi open; the Haar pair is
+# the shortest member of the Daubechies family, whose longer members trade
+# span locality for smoother low-pass responses.  Readings: the filters are
+# the extremal-phase Daubechies filters with N vanishing moments, and each
+# level extends its input periodically, which keeps every level an
+# orthonormal transform for any even length.
+
+
+def daubechies_lowpass(n_moments: int) -> np.ndarray:
+    """Low-pass filter g (length 2N) of the orthonormal Daubechies wavelet
+    with N = ``n_moments`` vanishing moments, from its defining polynomial.
+
+    The filter's frequency response satisfies
+        |m0(w)|^2 = cos(w/2)^(2N) * P(sin(w/2)^2),
+        P(y) = sum_{k=0}^{N-1} binom(N-1+k, k) y^k,
+    so m0 has N zeros at z = -1 and, for every root y_k of P, one zero of
+    z^2 - (2 - 4 y_k) z + 1 (the substitution y = (2 - z - 1/z) / 4); of each
+    such reciprocal pair the zero inside the unit circle is taken (extremal
+    phase, energy front-loaded).  g holds the coefficients of the polynomial
+    with those zeros, highest power first, scaled so that sum(g) = sqrt2.
+    N = 1 gives the Haar filter [1/sqrt2, 1/sqrt2].
+    """
+    n = int(n_moments)
+    if n < 1:
+        raise ValueError("need at least one vanishing moment")
+    zeros = [-1.0] * n
+    if n > 1:
+        p_desc = [math.comb(n - 1 + k, k) for k in range(n - 1, -1, -1)]
+        for y in np.roots(p_desc):
+            b = 1.0 - 2.0 * y
+            r = np.sqrt(b * b - 1.0 + 0j)
+            z1, z2 = b + r, b - r
+            zeros.append(z1 if abs(z1) < 1.0 else z2)
+    g = np.real(np.poly(np.array(zeros, dtype=complex)))
+    return g * (SQRT2 / g.sum())
+
+
+def _highpass(g: np.ndarray) -> np.ndarray:
+    """Quadrature-mirror partner h[k] = (-1)^k g[F-1-k] of a low-pass g."""
+    g = np.asarray(g, dtype=np.float64)
+    return np.array([(-1.0) ** k * g[len(g) - 1 - k] for k in range(len(g))])
+
+
+def dwt_analysis_step(x: np.ndarray, g: np.ndarray):
+    """One level of eq. (5) (WaveFilter §2.2) along axis 0 for a general
+    orthonormal low-pass g, input extended periodically:
+        A[n] = sum_k g[k] x[(2n + k) mod M],  D[n] = sum_k h[k] x[(2n + k) mod M]
+    with h the quadrature mirror of g.  With the Haar g this is
+    :func:`haar_analysis_step`.  Axis 0 must have even length M.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    g = np.asarray(g, dtype=np.float64)
+    h = _highpass(g)
+    m = x.shape[0]
+    if m % 2:
+        raise ValueError("length must be even")
+    base = 2 * np.arange(m // 2)
+    a = np.zeros((m // 2,) + x.shape[1:])
+    d = np.zeros_like(a)
+    for k in range(len(g)):
+        rows = x[(base + k) % m]
+        a += g[k] * rows
+        d += h[k] * rows
+    return a, d
+
+
+def dwt_synthesis_step(a: np.ndarray, d: np.ndarray, g: np.ndarray) -> np.ndarray:
+    """Inverse of :func:`dwt_analysis_step`: the transpose of the orthonormal
+    analysis map, x[(2n + k) mod M] += g[k] A[n] + h[k] D[n]."""
+    a = np.asarray(a, dtype=np.float64)
+    d = np.asarray(d, dtype=np.float64)
+    g = np.asarray(g, dtype=np.float64)
+    h = _highpass(g)
+    m = 2 * a.shape[0]
+    x = np.zeros((m,) + a.shape[1:])
+    base = 2 * np.arange(m // 2)
+    for k in range(len(g)):
+        np.add.at(x, (base + k) % m, g[k] * a + h[k] * d)
+    return x
+
+
+def wavelet_pyramid(x: np.ndarray, levels: int, g: np.ndarray) -> List[np.ndarray]:
+    """Approximations [A_0 = x, A_1, ..., A_L] of the pyramid of WaveFilter
+    §2.2 for the low-pass g (each A_j fed back into eq. (5))."""
+    out = [np.asarray(x, dtype=np.float64)]
+    for _ in range(levels):
+        out.append(dwt_analysis_step(out[-1], g)[0])
+    return out

@@ -183,14 +183,39 @@ def test_top_k_gap_definition():
 
 # ----------------------------------------------------------- recursive filter
 
-def _dense_reference_levels(q, kp, levels, ks):
-    """Same selection written densely: every level's A_j from span sums, a
-    candidate mask from the parents, SDPA probabilities, brute-force Top-K."""
+def _equivalent_filter(g, j):
+    """Level-j equivalent low-pass: w_1 = g, w_j = (g upsampled by 2^(j-1)) * w_(j-1)."""
+    w = np.array([1.0])
+    for i in range(1, j + 1):
+        up = np.zeros((len(g) - 1) * 2 ** (i - 1) + 1)
+        up[:: 2 ** (i - 1)] = g
+        w = np.convolve(up, w)
+    return w
+
+
+def _direct_level(x, g, j):
+    """A_j[p] = sum_m w_j[m] x[(2^j p + m) mod N], summed directly."""
+    n = x.shape[0]
+    w = _equivalent_filter(g, j)
+    out = np.zeros((n >> j,) + x.shape[1:])
+    for p in range(n >> j):
+        for m, wm in enumerate(w):
+            out[p] += wm * x[((p << j) + m) % n]
+    return out
+
+
+def _dense_reference_levels(q, kp, levels, ks, lowpass=None):
+    """Same selection written densely: every level's A_j from span sums (or,
+    for another basis, its equivalent filter summed directly), a candidate
+    mask from the parents, SDPA probabilities, brute-force Top-K."""
     n = kp.shape[0]
     out = {}
     parents = None
     for j in range(levels, -1, -1):
-        a_j = kp.reshape(n >> j, 1 << j, -1).sum(axis=1) * 2.0 ** (-j / 2)
+        if lowpass is None:
+            a_j = kp.reshape(n >> j, 1 << j, -1).sum(axis=1) * 2.0 ** (-j / 2)
+        else:
+            a_j = _direct_level(kp, lowpass, j)
         pos = np.arange(n >> j)
         mask = np.ones(n >> j, bool) if parents is None else np.isin(pos >> 1, parents)
         cand = pos[mask]
@@ -378,3 +403,130 @@ def test_cache_update_places_every_row():
             for ch in range(2):
                 want = g + 1000 * h + 1e6 * ch
                 assert c["Kg"][h, g, ch] == want and c["Vg"][h, g, ch] == -(want + 0.5)
+
+
+# ----------------------------------------------------- Daubechies bases (psi)
+
+def test_daubechies_db1_is_haar():
+    g = wo.daubechies_lowpass(1)
+    np.testing.assert_allclose(g, [1 / math.sqrt(2)] * 2, rtol=1e-15)
+    x = np.random.default_rng(3).standard_normal((32, 5))
+    a, d = wo.dwt_analysis_step(x, g)
+    ha, hd = wo.haar_analysis_step(x)
+    np.testing.assert_allclose(a, ha, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(d, hd, rtol=1e-14, atol=1e-15)
+
+
+def test_daubechies_db2_closed_form():
+    # The four-tap Daubechies filter in closed form: (1+√3, 3+√3, 3−√3, 1−√3) / (4√2).
+    s3 = math.sqrt(3.0)
+    want = np.array([1 + s3, 3 + s3, 3 - s3, 1 - s3]) / (4 * math.sqrt(2.0))
+    np.testing.assert_allclose(wo.daubechies_lowpass(2), want, rtol=1e-13)
+
+
+@pytest.mark.parametrize("n", [2, 3, 4, 6])
+def test_daubechies_filter_conditions(n):
+    g = wo.daubechies_lowpass(n)
+    f = len(g)
+    assert f == 2 * n
+    assert math.isclose(g.sum(), math.sqrt(2.0), rel_tol=1e-13)
+    # Orthonormal to its own even shifts.
+    for m in range(n):
+        dot = float(np.dot(g[:f - 2 * m], g[2 * m:]))
+        assert abs(dot - (1.0 if m == 0 else 0.0)) < 1e-12, m
+    # N vanishing moments: the mirror high-pass kills polynomials of degree < N.
+    k = np.arange(f, dtype=np.float64)
+    for p in range(n):
+        assert abs(np.sum((-1.0) ** k * k ** p * g)) < 1e-9 * max(1.0, (f - 1) ** p), p
+    # Extremal phase: apart from the N zeros at -1, every zero inside the unit
+    # circle (a root of multiplicity N comes back from np.roots split by about
+    # eps^(1/N), hence the loose test for "at -1"; the others lie > 1 away).
+    zeros = np.roots(g)
+    inner = zeros[np.abs(zeros + 1) > 0.05]
+    assert len(inner) == n - 1 and (np.abs(inner) < 1).all()
+
+
+@pytest.mark.parametrize("n,levels", [(2, 3), (4, 2), (3, 4)])
+def test_wavelet_perfect_reconstruction_and_parseval(n, levels):
+    g = wo.daubechies_lowpass(n)
+    x = np.random.default_rng(n * 10 + levels).standard_normal((64, 3))
+    a, details = x, []
+    for _ in range(levels):
+        a, d = wo.dwt_analysis_step(a, g)
+        details.append(d)
+    energy = (a ** 2).sum() + sum((d ** 2).sum() for d in details)
+    assert math.isclose(energy, (x ** 2).sum(), rel_tol=1e-12)
+    for d in reversed(details):
+        a = wo.dwt_synthesis_step(a, d, g)
+    np.testing.assert_allclose(a, x, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("n", [2, 3, 4])
+def test_wavelet_polynomial_details_vanish(n):
+    # Away from the periodic wrap, the details of a degree < N polynomial are 0.
+    g = wo.daubechies_lowpass(n)
+    t = np.arange(64, dtype=np.float64) / 64
+    x = sum((j + 1) * t ** j for j in range(n))[:, None]
+    _, d = wo.dwt_analysis_step(x, g)
+    interior = d[: (64 - len(g)) // 2 + 1]
+    assert np.abs(interior).max() < 1e-10
+
+
+@pytest.mark.parametrize("n,levels", [(1, 3), (2, 3), (4, 2), (3, 3)])
+def test_wavelet_pyramid_equals_equivalent_filter(n, levels):
+    # Cascade identity: A_L[p] = sum_m w_L[m] x[(2^L p + m) mod N] with
+    # w_1 = g and w_j = (g upsampled by 2^(j-1)) convolved with w_(j-1).
+    g = wo.daubechies_lowpass(n)
+    w = g.copy()
+    for j in range(2, levels + 1):
+        up = np.zeros((len(g) - 1) * 2 ** (j - 1) + 1)
+        up[:: 2 ** (j - 1)] = g
+        w = np.convolve(up, w)
+    size = 128
+    x = np.random.default_rng(n + levels).standard_normal((size, 4))
+    want = np.zeros((size >> levels, 4))
+    for p in range(size >> levels):
+        for m, wm in enumerate(w):
+            want[p] += wm * x[((p << levels) + m) % size]
+    np.testing.assert_allclose(wo.wavelet_pyramid(x, levels, g)[levels], want, rtol=1e-12,
+                               atol=1e-12)
+
+
+
+@pytest.mark.parametrize("n_mom,n,levels,ks,g", [
+    (2, 64, 3, [5, 7, 6, 4], 3),
+    (4, 128, 3, [20, 18, 10, 6], 4),
+    (3, 256, 4, [30, 16, 9, 6, 4], 2),
+])
+def test_recursive_filter_basis_matches_dense_bruteforce(n_mom, n, levels, ks, g):
+    rng = np.random.default_rng(n + levels * 17 + g + 100 * n_mom)
+    d = 8
+    q = rng.standard_normal((g, d)) * 1.5
+    kp = rng.standard_normal((n, d)) * 1.5
+    low = wo.daubechies_lowpass(n_mom)
+    got = wo.recursive_filter(q, kp, levels, ks, lowpass=low)
+    want = _dense_reference_levels(q, kp, levels, ks, lowpass=low)
+    for j in range(levels + 1):
+        np.testing.assert_array_equal(got["levels"][j]["sel"], want[j], err_msg=f"level {j}")
+
+
+@pytest.mark.parametrize("n_mom", [2, 4])
+def test_recursive_filter_basis_keep_all_is_token_topk(n_mom):
+    rng = np.random.default_rng(50 + n_mom)
+    n, levels, b, d = 128, 3, 19, 16
+    q = rng.standard_normal((4, d))
+    kp = rng.standard_normal((n, d)) * 2
+    ks = [b] + [n >> j for j in range(1, levels + 1)]
+    got = wo.recursive_filter(q, kp, levels, ks, lowpass=wo.daubechies_lowpass(n_mom))["idx"]
+    np.testing.assert_array_equal(got, _brute_topk(_mass_by_sdpa(q, kp), np.arange(n), b))
+
+
+def test_recursive_filter_db1_equals_haar():
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((5, 8))
+    kp = rng.standard_normal((256, 8))
+    ks = [40, 30, 20, 12, 8]
+    a = wo.recursive_filter(q, kp, 4, ks)
+    b = wo.recursive_filter(q, kp, 4, ks, lowpass=wo.daubechies_lowpass(1))
+    for j in range(5):
+        np.testing.assert_array_equal(a["levels"][j]["sel"], b["levels"][j]["sel"])

@@ -104,6 +104,44 @@ def _init_lowpass_unscaled(k_all, v_all, n_prompt, levels):
     return c
 
 
+_ORIG_DB = wo.daubechies_lowpass
+_ORIG_DWT = wo.dwt_analysis_step
+_ORIG_RF = wo.recursive_filter
+
+
+def _db_reversed(n):
+    return _ORIG_DB(n)[::-1].copy()
+
+
+def _db_unit_sum(n):
+    g = _ORIG_DB(n)
+    return g / g.sum()
+
+
+def _dwt_zero_padded(x, g):
+    x = np.asarray(x, np.float64)
+    padded = np.concatenate([x, np.zeros((len(g),) + x.shape[1:])])
+    a, d = _ORIG_DWT(padded, g)
+    return a[: x.shape[0] // 2], d[: x.shape[0] // 2]
+
+
+def _dwt_shifted(x, g):
+    return _ORIG_DWT(np.roll(np.asarray(x, np.float64), -1, axis=0), g)
+
+
+def _dwt_mirror_without_signs(x, g):
+    x = np.asarray(x, np.float64)
+    m = x.shape[0]
+    base = 2 * np.arange(m // 2)
+    a = sum(g[k] * x[(base + k) % m] for k in range(len(g)))
+    d = sum(g[len(g) - 1 - k] * x[(base + k) % m] for k in range(len(g)))
+    return a, d
+
+
+def _rf_ignores_basis(q, kp, levels, k_per_level, lowpass=None):
+    return _ORIG_RF(q, kp, levels, k_per_level)
+
+
 def _update_heads_reshaped(k_gen, v_gen):
     k = np.asarray(k_gen, np.float64)
     g, h, d = k.shape
@@ -129,6 +167,12 @@ PIN_TESTS = [
     lambda: pins.test_cache_init_lowpass_closed_form(2),
     lambda: pins.test_cache_init_round_trip_and_rejects(),
     lambda: pins.test_cache_update_places_every_row(),
+    lambda: pins.test_daubechies_db1_is_haar(),
+    lambda: pins.test_daubechies_db2_closed_form(),
+    lambda: pins.test_daubechies_filter_conditions(4),
+    lambda: pins.test_wavelet_perfect_reconstruction_and_parseval(2, 3),
+    lambda: pins.test_wavelet_pyramid_equals_equivalent_filter(2, 3),
+    lambda: pins.test_recursive_filter_basis_matches_dense_bruteforce(2, 64, 3, [5, 7, 6, 4], 3),
 ]
 
 MUTANTS = [
@@ -147,6 +191,12 @@ MUTANTS = [
     ("cache_init", _init_keys_values_swapped),
     ("cache_init", _init_lowpass_unscaled),
     ("cache_update", _update_heads_reshaped),
+    ("daubechies_lowpass", _db_reversed),
+    ("daubechies_lowpass", _db_unit_sum),
+    ("dwt_analysis_step", _dwt_zero_padded),
+    ("dwt_analysis_step", _dwt_shifted),
+    ("dwt_analysis_step", _dwt_mirror_without_signs),
+    ("recursive_filter", _rf_ignores_basis),
 ]
 
 
