@@ -502,6 +502,37 @@ def run_ours(args, cfg):
     cache_us = 1e3 * k0.elapsed_time(k1) / (cache_reps * n_cache)
     del cache_graph, cache_sets
 
+    # ---- the step with a longer basis (eight-tap Daubechies filter): the
+    # general path (pyramid launches, level-by-level filter CTA per unit,
+    # gather + attention), from a CUDA graph over the rotating input copies.
+    db4 = bd.daubechies_lowpass(4)
+    basis_ws = torch.zeros(bd.basis_workspace_bytes(dims, db4, ks), dtype=torch.uint8,
+                           device=dev)
+
+    def step_basis(c):
+        bd.step_basis(c["Q"], c["Kp"], c["Vp"], c["Kg"], c["Vg"], cfg.levels, ks, db4,
+                      ws=basis_ws, out=out, lse=lse, idx_out=idx)
+
+    for c in copies:
+        step_basis(c)
+    torch.cuda.synchronize()
+    basis_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(basis_graph, stream=cap_stream):
+        for c in copies:
+            step_basis(c)
+    for _ in range(2):
+        basis_graph.replay()
+    torch.cuda.synchronize()
+    basis_reps = max(1, min(20, args.steps // n_copies))
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    for _ in range(basis_reps):
+        basis_graph.replay()
+    b1.record(stream)
+    torch.cuda.synchronize()
+    basis_ms = b0.elapsed_time(b1) / (basis_reps * n_copies)
+    del basis_graph, basis_ws
+
     # ---- end to end through the host-buffer entry point (pinned host memory)
     host = {k: v.cpu().pin_memory() for k, v in base.items()}
     host["O"] = torch.empty(out.shape, dtype=torch.float32).pin_memory()
@@ -645,6 +676,13 @@ def run_ours(args, cfg):
             "algorithmic_bytes_per_launch": cache_bytes, "launch_us": cache_us,
             "timing": "CUDA graph of 20 launches over two alternating input/output sets, "
                       "events around its replays"},
+        "basis_step": {
+            "what": "wf_step_basis with the eight-tap Daubechies low-pass (periodic pyramid, "
+                    "level-by-level filter, gather + attention): the general path for a "
+                    "longer basis",
+            "value": tokens_per_step(cfg) / (basis_ms * 1e-3), "unit": "tokens/s",
+            "ms_per_step": basis_ms,
+            "launches_per_step": cfg.levels + 2},
         "stages_us": stage_us,
         "cpu_baseline": None if cpu_rate is None else {
             "value": cpu_rate, "unit": "tokens/s", "cores": workers, "kind": "oracle",

@@ -17,6 +17,12 @@
  *   wf_cache_init         §2.1 eq. (2) at t = 1, plus A_L of the prompt keys
  *   wf_cache_update       §2.1 eq. (4) at t > 1 (generation rows)
  *
+ * and, for wavelet bases longer than the Haar pair (§3.1 leaves psi open):
+ *
+ *   wf_daubechies_lowpass  the extremal-phase Daubechies low-pass filters
+ *   wf_dwt_lowpass_basis   the pyramid A_1..A_L of such a basis
+ *   wf_step_basis          the whole step with such a basis
+ *
  * Readings fixed where the pages are silent: orthonormal Haar filters
  * g = [1/√2, 1/√2] on 0-based pairs (2n, 2n+1), so coarse position p at
  * level j covers tokens [p·2^j, (p+1)·2^j); the score of a candidate is its
@@ -301,6 +307,49 @@ int wf_decode_step_host(const wf_dims* dims, const void* h_Q, const void* h_K,
                         const void* Vp, void* Kg, void* Vg, const float* AL,
                         float* d_O, void* workspace, size_t workspace_bytes,
                         void* stream);
+
+/* ---- Longer orthonormal bases (WaveFilter §3.1: the basis psi is open).
+ * Readings: the basis is given by its low-pass filter g (an even number of
+ * taps, 2..16, orthonormal to its even shifts); every pyramid level extends
+ * its input periodically,
+ *   A_j[n] = Σ_k g[k] · A_{j-1}[(2n + k) mod M],  M = N_p / 2^(j-1),
+ * which keeps each level orthonormal; recursive filtering keeps the
+ * pyramid's index tree (candidates at level j < L are the children 2p, 2p+1
+ * of the level-(j+1) survivors) and scores them against this basis's A_j
+ * exactly as the Haar path does.  With g = [1/√2, 1/√2] every result equals
+ * the Haar entry points' (up to fp32 rounding order). */
+
+/* Low-pass filter of the orthonormal Daubechies wavelet with n_moments
+ * vanishing moments (1..8; 1 = Haar), extremal phase: taps_out receives
+ * 2·n_moments doubles, g[0] first, summing to √2.  Host only.
+ * Errors: WF_ERR_NULL, WF_ERR_UNSUPPORTED (n_moments outside 1..8). */
+int wf_daubechies_lowpass(int32_t n_moments, double* taps_out);
+
+/* Bytes of workspace wf_step_basis needs (it holds A_1..A_L in fp32, the
+ * candidate lists, scores and logits).  Errors: as wf_workspace_bytes, plus
+ * WF_ERR_UNSUPPORTED for a tap count outside 2..16 or odd. */
+int wf_basis_workspace_bytes(const wf_dims* dims, int32_t taps,
+                             const int32_t* k_per_level, size_t* bytes);
+
+/* Pyramid of a longer basis: every level j = 1..L of Kp into A_all,
+ * level-major ([U, N_p/2^j, d] fp32 blocks for j = 1, 2, ..., L), one launch
+ * per level.  lowpass: HOST, `taps` doubles.
+ * Errors: WF_ERR_NULL, WF_ERR_SHAPE, WF_ERR_UNSUPPORTED, WF_ERR_ALIGNMENT,
+ * WF_ERR_CUDA. */
+int wf_dwt_lowpass_basis(const wf_dims* dims, const double* lowpass,
+                         int32_t taps, const void* Kp, float* A_all,
+                         void* stream);
+
+/* The whole step with a longer basis: the pyramid (L launches), the
+ * recursive filter (one CTA per unit), then steps 4-5 as in
+ * wf_sparse_gather_attn.  Arguments as wf_step, plus the HOST filter
+ * `lowpass` of `taps` doubles; workspace ≥ wf_basis_workspace_bytes().
+ * Errors: as wf_step, plus WF_ERR_UNSUPPORTED for a bad tap count. */
+int wf_step_basis(const wf_dims* dims, const double* lowpass, int32_t taps,
+                  const void* Q, const void* Kp, const void* Vp,
+                  const void* Kg, const void* Vg, const int32_t* k_per_level,
+                  float* O, float* lse, int32_t* idx_out, void* workspace,
+                  size_t workspace_bytes, void* stream);
 
 /* Size of the device scratch array behind wf_step_static_scratch (48 MiB). */
 #define WF_STATIC_SCRATCH_BYTES (48u << 20)

@@ -217,3 +217,46 @@ def test_decode_step_host_rejects_before_copies(lib):
     assert call(k=bd._k_array([512, 512, 256, 128, 300])) == 2
     assert call(dims=_dims(n_prompt=4100)) == 2
     assert call(dims=_dims(head_dim=96)) == 3
+
+
+def test_daubechies_lowpass_host_helper(lib):
+    # The library's own filter generator (root finding in C++) against the
+    # oracle's numpy spectral factorisation: independent code, same filters.
+    import numpy as np
+
+    import oracle.wavefilter_oracle as wo
+    for n in range(1, 9):
+        np.testing.assert_allclose(bd.daubechies_lowpass(n), wo.daubechies_lowpass(n), rtol=0,
+                                   atol=1e-12)
+    out = (ctypes.c_double * 32)()
+    assert lib.wf_daubechies_lowpass(0, out) == 3
+    assert lib.wf_daubechies_lowpass(9, out) == 3
+    assert lib.wf_daubechies_lowpass(2, None) == 1
+
+
+def test_basis_entry_points_reject_before_launch(lib):
+    dims = _dims()
+    k = bd._k_array([512, 512, 256, 128, 64])
+    p16 = ctypes.c_void_p(1 << 20)
+    p17 = ctypes.c_void_p((1 << 20) + 4)
+    taps = (ctypes.c_double * 8)(*bd.daubechies_lowpass(4))
+    n = ctypes.c_size_t(0)
+    assert lib.wf_basis_workspace_bytes(ctypes.byref(dims), 8, k, ctypes.byref(n)) == 0
+    assert n.value > 32 * 4096 * 128 * 4 // 2  # holds A_1..A_L in fp32
+    assert lib.wf_basis_workspace_bytes(ctypes.byref(dims), 7, k, ctypes.byref(n)) == 3
+    assert lib.wf_basis_workspace_bytes(ctypes.byref(dims), 18, k, ctypes.byref(n)) == 3
+    assert lib.wf_dwt_lowpass_basis(ctypes.byref(dims), None, 8, p16, p16, None) == 1
+    assert lib.wf_dwt_lowpass_basis(ctypes.byref(dims), taps, 0, p16, p16, None) == 3
+    assert lib.wf_dwt_lowpass_basis(ctypes.byref(dims), taps, 8, p17, p16, None) == 7
+
+    def step(dims=dims, taps=taps, nt=8, q=p16, ws=p16, wsb=1 << 40, k=k):
+        return lib.wf_step_basis(ctypes.byref(dims), taps, nt, q, p16, p16, p16, p16, k, p16,
+                                 None, None, ws, wsb, None)
+
+    assert step(taps=None) == 1
+    assert step(nt=3) == 3
+    assert step(q=None) == 1
+    assert step(q=p17) == 7
+    assert step(wsb=n.value - 1) == 4
+    assert step(k=bd._k_array([512, 512, 256, 128, 300])) == 2
+    assert step(dims=_dims(n_prompt=4100)) == 2

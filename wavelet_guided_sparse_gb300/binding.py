@@ -30,7 +30,9 @@ EXPORTS = ("wf_status_string", "wf_last_error_string", "wf_default_k_per_level",
            "wf_clear_device_status", "wf_read_device_status", "wf_dwt_lowpass",
            "wf_score_topk", "wf_recursive_filter", "wf_sparse_gather_attn", "wf_step",
            "wf_step_host", "wf_step_static_scratch", "wf_step_cached_al",
-           "wf_cache_init", "wf_cache_update", "wf_decode_step_host")
+           "wf_cache_init", "wf_cache_update", "wf_decode_step_host",
+           "wf_daubechies_lowpass", "wf_basis_workspace_bytes", "wf_dwt_lowpass_basis",
+           "wf_step_basis")
 
 
 class WfError(RuntimeError):
@@ -52,6 +54,7 @@ _i32 = ctypes.c_int32
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _sz = ctypes.c_size_t
 _DIMSP = ctypes.POINTER(Dims)
+_f64p = ctypes.POINTER(ctypes.c_double)
 
 _SIGS = {
     "wf_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -78,6 +81,11 @@ _SIGS = {
     "wf_cache_update": (ctypes.c_int, [_DIMSP, _vp, _vp, _vp, _vp, _vp]),
     "wf_decode_step_host": (ctypes.c_int, [_DIMSP, _vp, _vp, _vp, _i32p, _vp, _vp, _vp, _vp,
                                            _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "wf_daubechies_lowpass": (ctypes.c_int, [_i32, _f64p]),
+    "wf_basis_workspace_bytes": (ctypes.c_int, [_DIMSP, _i32, _i32p, ctypes.POINTER(_sz)]),
+    "wf_dwt_lowpass_basis": (ctypes.c_int, [_DIMSP, _f64p, _i32, _vp, _vp, _vp]),
+    "wf_step_basis": (ctypes.c_int, [_DIMSP, _f64p, _i32, _vp, _vp, _vp, _vp, _vp, _i32p, _vp,
+                                     _vp, _vp, _vp, _sz, _vp]),
 }
 
 
@@ -377,6 +385,64 @@ def decode_step_host(dims: Dims, host: dict, k_per_level: Sequence[int], stage: 
         _ptr(stage["V"]), _ptr(cache["Kp"]), _ptr(cache["Vp"]), _ptr(cache["Kg"]),
         _ptr(cache["Vg"]), _ptr(cache["AL"]), _ptr(stage["O"]), _ptr(ws), ws.numel(),
         _stream(stream)))
+
+
+def daubechies_lowpass(n_moments: int) -> list:
+    """Extremal-phase Daubechies low-pass filter (2 n_moments taps) from the library."""
+    out = (ctypes.c_double * (2 * n_moments))()
+    _check("wf_daubechies_lowpass", lib().wf_daubechies_lowpass(n_moments, out))
+    return list(out)
+
+
+def _taps(lowpass: Sequence[float]):
+    return (ctypes.c_double * len(lowpass))(*[float(x) for x in lowpass]), len(lowpass)
+
+
+def basis_workspace_bytes(dims: Dims, lowpass: Sequence[float], k: Sequence[int]) -> int:
+    n = ctypes.c_size_t(0)
+    _check("wf_basis_workspace_bytes", lib().wf_basis_workspace_bytes(
+        ctypes.byref(dims), len(lowpass), _k_array(k), ctypes.byref(n)))
+    return n.value
+
+
+def dwt_lowpass_basis(kp: torch.Tensor, levels: int, lowpass: Sequence[float], stream=None):
+    """Levels A_1..A_L [b, H, N_p/2^j, d] fp32 of the basis with low-pass ``lowpass``."""
+    _require(kp, "Kp")
+    b, h, n, d = kp.shape
+    dims = Dims(b, h, n, 1, d, levels, dtype_code(kp.dtype))
+    total = sum(b * h * (n >> j) * d for j in range(1, levels + 1))
+    a_all = torch.empty(total, dtype=torch.float32, device=kp.device)
+    taps, nt = _taps(lowpass)
+    _check("wf_dwt_lowpass_basis", lib().wf_dwt_lowpass_basis(
+        ctypes.byref(dims), taps, nt, _ptr(kp), _ptr(a_all), _stream(stream)))
+    out, off = [], 0
+    for j in range(1, levels + 1):
+        size = b * h * (n >> j) * d
+        out.append(a_all[off:off + size].view(b, h, n >> j, d))
+        off += size
+    return out
+
+
+def step_basis(q, kp, vp, kg, vg, levels: int, k_per_level: Sequence[int],
+               lowpass: Sequence[float], ws: Optional[torch.Tensor] = None,
+               out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+               idx_out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The whole step with the orthonormal basis of low-pass ``lowpass``;
+    returns O [b, H, G, d] fp32.  ``ws`` defaults to a fresh workspace."""
+    for t, n in ((q, "Q"), (kp, "Kp"), (vp, "Vp"), (kg, "Kg"), (vg, "Vg")):
+        _require(t, n, q.dtype)
+    dims = make_dims(q, kp, levels)
+    if ws is None:
+        ws = torch.zeros(basis_workspace_bytes(dims, lowpass, k_per_level), dtype=torch.uint8,
+                         device=q.device)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    taps, nt = _taps(lowpass)
+    _check("wf_step_basis", lib().wf_step_basis(
+        ctypes.byref(dims), taps, nt, _ptr(q), _ptr(kp), _ptr(vp), _ptr(kg), _ptr(vg),
+        _k_array(k_per_level), _ptr(out), _ptr(lse), _ptr(idx_out), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return out
 
 
 def raw_call(name: str, *args) -> int:

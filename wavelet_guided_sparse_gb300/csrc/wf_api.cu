@@ -10,6 +10,8 @@
 
 #include <cstdint>
 #include <cstdio>
+#include <algorithm>
+#include <cmath>
 #include <cstring>
 
 #include "wavefilter.h"
@@ -83,6 +85,45 @@ Layout layout(const LaunchDims& ld, const int32_t* k, const wf::PathPlan* fp) {
 }
 
 int32_t* status_word(void* ws) { return static_cast<int32_t*>(ws); }
+
+// Filter taps of a longer basis: 2..16 taps, an even count.
+int check_taps(const double* g, int32_t taps, wf::BasisTaps* t) {
+  if (g == nullptr) return WF_ERR_NULL;
+  if (taps < 2 || taps > 16 || taps % 2 != 0) return WF_ERR_UNSUPPORTED;
+  t->n = taps;
+  for (int i = 0; i < 16; ++i) t->g[i] = i < taps ? static_cast<float>(g[i]) : 0.f;
+  return WF_OK;
+}
+
+// Workspace of the longer-basis step: [status header | A_1..A_L | candidates
+// and survivors | keys | logits | selected tokens].
+struct BasisLayout {
+  size_t a_all, cand, keys, z, idx, total;
+  int64_t cap;
+};
+
+BasisLayout basis_layout(const LaunchDims& ld, const int32_t* k) {
+  BasisLayout L;
+  int64_t cap = ld.n_prompt >> ld.levels;
+  for (int j = 0; j < ld.levels; ++j) cap = std::max<int64_t>(cap, 2 * int64_t{k[j + 1]});
+  L.cap = cap;
+  size_t levels_el = 0;
+  for (int j = 1; j <= ld.levels; ++j)
+    levels_el += static_cast<size_t>(ld.units) * (ld.n_prompt >> j) * ld.head_dim;
+  size_t o = kHeaderBytes;
+  L.a_all = o;
+  o = align_up(o + sizeof(float) * levels_el);
+  L.cand = o;
+  o = align_up(o + sizeof(int32_t) * 2 * ld.units * cap);
+  L.keys = o;
+  o = align_up(o + sizeof(uint32_t) * ld.units * cap);
+  L.z = o;
+  o = align_up(o + sizeof(float) * ld.units * cap * ld.n_gen);
+  L.idx = o;
+  o = align_up(o + sizeof(int32_t) * ld.units * k[0]);
+  L.total = o;
+  return L;
+}
 
 thread_local char g_last_error[256] = "no error";
 
@@ -471,6 +512,97 @@ int wf_decode_step_host(const wf_dims* dims, const void* h_Q, const void* h_K, c
   if (st != WF_OK) return st;
   return cuda_status(cudaMemcpyAsync(h_O, d_O, sizeof(float) * ld.units * ld.n_gen * ld.head_dim,
                                      cudaMemcpyDeviceToHost, s));
+}
+
+int wf_daubechies_lowpass(int32_t n_moments, double* taps_out) {
+  if (taps_out == nullptr) return WF_ERR_NULL;
+  if (n_moments < 1 || n_moments > 8) return WF_ERR_UNSUPPORTED;
+  wf::daubechies_lowpass(n_moments, taps_out);
+  return WF_OK;
+}
+
+int wf_basis_workspace_bytes(const wf_dims* dims, int32_t taps, const int32_t* k_per_level,
+                             size_t* bytes) {
+  LaunchDims ld;
+  int st = check_dims(dims, &ld);
+  if (st != WF_OK) return st;
+  if (bytes == nullptr) return WF_ERR_NULL;
+  if (taps < 2 || taps > 16 || taps % 2 != 0) return WF_ERR_UNSUPPORTED;
+  st = check_k(ld, k_per_level);
+  if (st != WF_OK) return st;
+  *bytes = basis_layout(ld, k_per_level).total;
+  return WF_OK;
+}
+
+int wf_dwt_lowpass_basis(const wf_dims* dims, const double* lowpass, int32_t taps,
+                         const void* Kp, float* A_all, void* stream) {
+  LaunchDims ld;
+  int st = check_dims(dims, &ld);
+  if (st != WF_OK) return st;
+  wf::BasisTaps t;
+  st = check_taps(lowpass, taps, &t);
+  if (st != WF_OK) return st;
+  if (Kp == nullptr || A_all == nullptr) return WF_ERR_NULL;
+  if (!aligned16(Kp) || !aligned16(A_all)) return WF_ERR_ALIGNMENT;
+  return cuda_status(
+      wf::launch_basis_pyramid(ld, Kp, A_all, t, static_cast<cudaStream_t>(stream)));
+}
+
+int wf_step_basis(const wf_dims* dims, const double* lowpass, int32_t taps, const void* Q,
+                  const void* Kp, const void* Vp, const void* Kg, const void* Vg,
+                  const int32_t* k_per_level, float* O, float* lse, int32_t* idx_out,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+  LaunchDims ld;
+  int st = check_dims(dims, &ld);
+  if (st != WF_OK) return st;
+  wf::BasisTaps t;
+  st = check_taps(lowpass, taps, &t);
+  if (st != WF_OK) return st;
+  if (Q == nullptr || Kp == nullptr || Vp == nullptr || Kg == nullptr || Vg == nullptr ||
+      O == nullptr || workspace == nullptr)
+    return WF_ERR_NULL;
+  if (!aligned16(Q) || !aligned16(Kp) || !aligned16(Vp) || !aligned16(Kg) || !aligned16(Vg) ||
+      !aligned16(O) || !aligned16(workspace) || (lse && !aligned16(lse)) ||
+      (idx_out && !aligned16(idx_out)))
+    return WF_ERR_ALIGNMENT;
+  st = check_k(ld, k_per_level);
+  if (st != WF_OK) return st;
+  const BasisLayout L = basis_layout(ld, k_per_level);
+  if (workspace_bytes < L.total) return WF_ERR_WORKSPACE;
+  wf::PathPlan plan;  // steps 4-5 must be plannable before anything is enqueued
+  if (!wf::plan_path(ld, wf::kPhaseAttend, nullptr, 0, k_per_level[0], wf::device_sm_count(),
+                     &plan))
+    return WF_ERR_UNSUPPORTED;
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* a_all = reinterpret_cast<float*>(ws + L.a_all);
+  cudaError_t ce = wf::launch_basis_pyramid(ld, Kp, a_all, t, s);
+  if (ce != cudaSuccess) return cuda_status(ce);
+  wf::BasisFilterParams p = {};
+  p.q = Q;
+  p.kp = Kp;
+  p.a_all = a_all;
+  int64_t off = 0;
+  for (int j = 1; j <= ld.levels; ++j) {
+    p.level_off[j] = off;
+    off += ld.units * static_cast<int64_t>(ld.n_prompt >> j) * ld.head_dim;
+  }
+  p.cand = reinterpret_cast<int32_t*>(ws + L.cand);
+  p.keys = reinterpret_cast<uint32_t*>(ws + L.keys);
+  p.z = reinterpret_cast<float*>(ws + L.z);
+  int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(ws + L.idx);
+  p.idx = idx;
+  p.units = ld.units;
+  p.cap = L.cap;
+  p.n_prompt = ld.n_prompt;
+  p.n_gen = ld.n_gen;
+  p.levels = ld.levels;
+  for (int j = 0; j <= ld.levels; ++j) p.k[j] = k_per_level[j];
+  p.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(ld.head_dim)));
+  ce = wf::launch_basis_filter(ld, p, s);
+  if (ce != cudaSuccess) return cuda_status(ce);
+  return wf_sparse_gather_attn(dims, Q, Kp, Vp, Kg, Vg, idx, k_per_level[0], O, lse, workspace,
+                               workspace_bytes, stream);
 }
 
 int wf_step_host(const wf_dims* dims, const void* h_Q, const void* h_Kp, const void* h_Vp,

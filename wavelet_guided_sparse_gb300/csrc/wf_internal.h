@@ -90,6 +90,34 @@ cudaError_t launch_cache_init(const LaunchDims& ld, const void* k, const void* v
 cudaError_t launch_cache_update(const LaunchDims& ld, const void* k, const void* v, void* kg,
                                 void* vg, cudaStream_t stream);
 
+// Longer orthonormal bases (wf_basis.cu).  Filter taps (fp32 copy of the
+// caller's low-pass) and the launch arguments of the level-by-level filter.
+struct BasisTaps {
+  float g[16];
+  int n;
+};
+struct BasisFilterParams {
+  const void* q;
+  const void* kp;
+  const float* a_all;                      // levels 1..L, level-major fp32 blocks
+  int64_t level_off[WF_MAX_LEVELS + 1];    // element offset of level j's block
+  int32_t* cand;                           // [2][units][cap]: candidates, survivors
+  uint32_t* keys;                          // [units][cap] scores as ordered bits
+  float* z;                                // [units][cap][G] logits (log2 domain)
+  int32_t* idx;                            // out: [units][k_0] selected tokens
+  int64_t units, cap;
+  int n_prompt, n_gen, levels;
+  int32_t k[WF_MAX_LEVELS + 1];
+  float qscale;                            // log2(e) / sqrt(d)
+};
+// Extremal-phase Daubechies low-pass with n_moments vanishing moments (host;
+// 2 n_moments doubles, highest power of the filter polynomial first).
+int daubechies_lowpass(int n_moments, double* out);
+cudaError_t launch_basis_pyramid(const LaunchDims& ld, const void* kp, float* a_all,
+                                 const BasisTaps& taps, cudaStream_t stream);
+cudaError_t launch_basis_filter(const LaunchDims& ld, const BasisFilterParams& p,
+                                cudaStream_t stream);
+
 // Dynamic shared memory the planners allow per CTA (the sm_103a opt-in limit
 // is 227 KB; a little is left for static shared memory).
 constexpr size_t kMaxSmem = 225 * 1024;
