@@ -15,9 +15,10 @@
 //    A_1..A_L in fp32 (level-major blocks), so level j of a candidate is one
 //    row read.
 //  * basis_filter_kernel: one 8-warp CTA per unit walks the levels L..0.
-//    A warp stages one candidate row (A_j in fp32, or the K_p row at level
-//    0) in shared memory and its lanes compute the logits of queries lane
-//    and lane + 32 against it (queries transposed in shared memory, so the
+//    A warp stages eight candidate rows at once (A_j in fp32, or the K_p
+//    rows at level 0; eight 16-byte loads in flight per lane) in shared
+//    memory and its lanes compute the logits of queries lane and lane + 32
+//    against each (queries transposed in shared memory, so the
 //    reads are conflict-free), keeping per-query online (max, sum) in the
 //    log2 domain; per-warp statistics are merged, each candidate's mass is
 //    summed over the queries and the block radix select keeps k_j (larger
@@ -38,6 +39,7 @@ namespace wf {
 namespace {
 
 constexpr int kMaxG = 64;  // queries per unit (lanes lane and lane + 32)
+constexpr int kRowsPerWarp = 8;  // candidate rows a warp stages at once (loads in flight)
 
 __device__ __forceinline__ void load4_f32(const float* p, float* f) {
   const float4 v = *reinterpret_cast<const float4*>(p);
@@ -95,31 +97,47 @@ template <typename T, int D>
 struct FilterLayout {
   static constexpr size_t kQt = (sizeof(FilterSmem) + 15) & ~size_t{15};
   static constexpr size_t kRow = kQt + sizeof(float) * D * kMaxG;
-  static constexpr size_t kTotal = kRow + sizeof(float) * kWarps * D;
+  static constexpr size_t kTotal = kRow + sizeof(float) * kWarps * kRowsPerWarp * D;
 };
 
-// Stages row `pos` of level j (fp32 A_j, or the K_p row of type T at j = 0)
-// into `buf` as D floats; one warp.
+// Stages rows pos[0..nr) of level j (fp32 A_j, or the K_p rows of type T at
+// j = 0) into buf[r][D] as floats; one warp.  Every lane issues its 16-byte
+// chunk of all nr rows before widening any, so nr loads are in flight.
 template <typename T, int D>
-__device__ __forceinline__ void stage_row(const BasisFilterParams& p, int64_t u, int j, int pos,
-                                          float* buf) {
+__device__ __forceinline__ void stage_rows(const BasisFilterParams& p, int64_t u, int j,
+                                           const int* pos, int nr, float* buf) {
   const int lane = threadIdx.x & 31;
   if (j == 0) {
-    constexpr int V = Elem<T>::kPer16B;
-    const T* row = static_cast<const T*>(p.kp) + (u * p.n_prompt + pos) * D;
-    for (int c = lane; c < D / V; c += 32) {
-      float f[V];
-      load16_f32(row + c * V, f);
+    constexpr int V = Elem<T>::kPer16B, C = D / V;  // C <= 32 chunks per row
+    const T* base = static_cast<const T*>(p.kp) + u * p.n_prompt * D + lane * V;
+    uint4 raw[kRowsPerWarp];
 #pragma unroll
-      for (int e = 0; e < V; ++e) buf[c * V + e] = f[e];
+    for (int r = 0; r < kRowsPerWarp; ++r)
+      if (r < nr && lane < C) raw[r] = ldg16(base + static_cast<int64_t>(pos[r]) * D);
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      if (r < nr && lane < C) {
+        float f[V];
+        widen16(raw[r], static_cast<const T*>(nullptr), f);
+#pragma unroll
+        for (int e = 0; e < V; ++e) buf[r * D + lane * V + e] = f[e];
+      }
     }
   } else {
-    const float* row = p.a_all + p.level_off[j] + (u * (p.n_prompt >> j) + pos) * D;
-    for (int c = lane; c < D / 4; c += 32) {
-      float f[4];
-      load16_f32(row + c * 4, f);
+    constexpr int C = D / 4;
+    const float* base = p.a_all + p.level_off[j] + u * (p.n_prompt >> j) * D + lane * 4;
+    uint4 raw[kRowsPerWarp];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) buf[c * 4 + e] = f[e];
+    for (int r = 0; r < kRowsPerWarp; ++r)
+      if (r < nr && lane < C) raw[r] = ldg16(base + static_cast<int64_t>(pos[r]) * D);
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      if (r < nr && lane < C) {
+        float f[4];
+        widen16(raw[r], static_cast<const float*>(nullptr), f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) buf[r * D + lane * 4 + e] = f[e];
+      }
     }
   }
 }
@@ -139,7 +157,7 @@ __global__ void __launch_bounds__(kThreads) basis_filter_kernel(BasisFilterParam
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t u = blockIdx.x;
   const int G = p.n_gen;
-  float* rowbuf = reinterpret_cast<float*>(smem + L::kRow) + warp * D;
+  float* rowbuf = reinterpret_cast<float*>(smem + L::kRow) + warp * kRowsPerWarp * D;
   const T* q = static_cast<const T*>(p.q) + u * G * D;
   for (int e = tid; e < kMaxG * D; e += kThreads) {
     const int i = e % kMaxG, c = e / kMaxG;
@@ -155,24 +173,31 @@ __global__ void __launch_bounds__(kThreads) basis_filter_kernel(BasisFilterParam
   for (int j = p.levels; j >= 0; --j) {
     // Logits and per-warp online statistics (queries lane and lane + 32).
     float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
-    for (int c = warp; c < ncand; c += kWarps) {
-      const int pos = map ? map[c] : c;
-      stage_row<T, D>(p, u, j, pos, rowbuf);
+    for (int c0 = warp * kRowsPerWarp; c0 < ncand; c0 += kWarps * kRowsPerWarp) {
+      const int nr = min(kRowsPerWarp, ncand - c0);
+      int pos[kRowsPerWarp];
+#pragma unroll
+      for (int r = 0; r < kRowsPerWarp; ++r) pos[r] = r < nr ? (map ? map[c0 + r] : c0 + r) : 0;
+      stage_rows<T, D>(p, u, j, pos, nr, rowbuf);
       __syncwarp();
-      float z0 = 0.f, z1 = 0.f;
+      for (int r = 0; r < nr; ++r) {
+        const float* row = rowbuf + r * D;
+        float z0 = 0.f, z1 = 0.f;
 #pragma unroll 8
-      for (int k = 0; k < D; ++k) {
-        const float r = rowbuf[k];
-        z0 = fmaf(r, qt[k * kMaxG + lane], z0);
-        z1 = fmaf(r, qt[k * kMaxG + lane + 32], z1);
-      }
-      if (lane < G) {
-        z[static_cast<int64_t>(c) * G + lane] = z0;
-        online_add(m0, l0, z0);
-      }
-      if (lane + 32 < G) {
-        z[static_cast<int64_t>(c) * G + lane + 32] = z1;
-        online_add(m1, l1, z1);
+        for (int k = 0; k < D; ++k) {
+          const float x = row[k];
+          z0 = fmaf(x, qt[k * kMaxG + lane], z0);
+          z1 = fmaf(x, qt[k * kMaxG + lane + 32], z1);
+        }
+        const int64_t c = c0 + r;
+        if (lane < G) {
+          z[c * G + lane] = z0;
+          online_add(m0, l0, z0);
+        }
+        if (lane + 32 < G) {
+          z[c * G + lane + 32] = z1;
+          online_add(m1, l1, z1);
+        }
       }
       __syncwarp();
     }
