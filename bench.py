@@ -2,8 +2,9 @@
 """Throughput of the WaveFilter per-layer, per-step KV-filtering path.
 
 One step = one pass of the whole path (Haar low-pass, coarse scoring + Top-K,
-recursive filtering, sparse gather + eq. (3) attention) over one layer of the
-workload, through the C ABI.  Metric: cached prompt tokens filtered+attended
+recursive filtering, sparse gather + eq. (3) attention) over every layer of
+the workload, through the C ABI; the default workload is the full denoising
+step (32 layers of 32 heads over a 65536-token prompt).  Metric: cached prompt tokens filtered+attended
 per second per layer-step (batch * layers * N_p per step), plus the achieved
 HBM bandwidth of the dominant kernel against the measured peak.
 
@@ -35,7 +36,7 @@ sys.path.insert(0, ROOT)
 from wavelet_guided_sparse_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "cached prompt tokens filtered+attended/sec per layer-step; HBM GB/s vs peak"
-DEFAULT_CONFIG = "llada8b_layer"
+DEFAULT_CONFIG = "full_step"
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) of one dwt_lowpass launch on the default workload,
@@ -62,14 +63,14 @@ def _rank_env():
 
 def _workload_desc(cfg: wl.WorkloadConfig) -> str:
     ks = cfg.k_per_level()
-    return (f"{cfg.name}: batch={cfg.batch}, layers=1 of {cfg.layers}, H={cfg.heads}, "
+    return (f"{cfg.name}: batch={cfg.batch}, layers={cfg.layers}, H={cfg.heads}, "
             f"d={cfg.head_dim}, N_p={cfg.n_prompt}, G={cfg.n_gen}, {cfg.dtype}, "
             f"Haar L={cfg.levels}, k_L={ks[-1]}, budget B={cfg.budget}")
 
 
 def _config_obj(cfg, extra=None):
     ks = cfg.k_per_level()
-    obj = {"workload": _workload_desc(cfg), "batch": cfg.batch, "layers_per_step": 1,
+    obj = {"workload": _workload_desc(cfg), "batch": cfg.batch, "layers_per_step": cfg.layers,
            "heads": cfg.heads, "head_dim": cfg.head_dim, "n_prompt": cfg.n_prompt,
            "n_gen": cfg.n_gen, "levels": cfg.levels, "k_per_level": ks,
            "budget": cfg.budget, "parallelism": "replicas"}
@@ -79,11 +80,18 @@ def _config_obj(cfg, extra=None):
 
 
 def tokens_per_step(cfg) -> int:
-    return cfg.batch * 1 * cfg.n_prompt
+    """Cached prompt tokens filtered+attended per step: batch * layers * N_p."""
+    return cfg.batch * cfg.layers * cfg.n_prompt
+
+
+def tokens_per_unit(cfg) -> float:
+    """Share of one (sequence, layer, head) unit in tokens_per_step."""
+    return cfg.n_prompt / cfg.heads
 
 
 def path_bytes(cfg) -> dict:
-    """Algorithmic HBM bytes of one step (one layer), by stage."""
+    """Algorithmic HBM bytes of one layer of the step, by stage (the staged
+    entry points; each stage reads its own inputs)."""
     e = 2 if cfg.dtype == "bf16" else 4
     U, d, n, g, L = cfg.units_per_layer, cfg.head_dim, cfg.n_prompt, cfg.n_gen, cfg.levels
     ks = cfg.k_per_level()
@@ -95,6 +103,27 @@ def path_bytes(cfg) -> dict:
         "filter": U * (rows * d * e + g * d * e + ks[L] * 4 + B * 4),
         "attn": U * (2 * B * d * e + 2 * g * d * e + g * d * e + B * 4 + g * d * 4),
     }
+
+
+def layer_bytes(cfg) -> int:
+    """Algorithmic HBM bytes of one layer of the step, term by term as the
+    measurement plan defines them: the K_p stream, the A_L write and read, the
+    span rows of the coarse survivors, the gathered K/V rows, K_g/V_g, Q, O
+    and the selected indices."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    U, d, n, g, L = cfg.units_per_layer, cfg.head_dim, cfg.n_prompt, cfg.n_gen, cfg.levels
+    ks = cfg.k_per_level()
+    P, B = n >> L, ks[0]
+    return U * (n * d * e + 2 * P * d * 4 + (ks[L] << L) * d * e + 2 * B * d * e +
+                2 * g * d * e + g * d * e + g * d * 4 + 4 * B)
+
+
+def stream_bytes(cfg) -> int:
+    """The share of layer_bytes that the K_p stream moves: K_p read once and
+    the A_L write."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    return cfg.units_per_layer * (cfg.n_prompt * cfg.head_dim * e +
+                                  (cfg.n_prompt >> cfg.levels) * cfg.head_dim * 4)
 
 
 def _peaks():
@@ -130,15 +159,6 @@ def cache_init_bytes(cfg) -> int:
     rows = cfg.n_prompt + cfg.n_gen
     return (4 * cfg.units_per_layer * rows * cfg.head_dim * e +
             cfg.units_per_layer * (cfg.n_prompt >> cfg.levels) * cfg.head_dim * 4)
-
-
-def step_bytes(cfg, fused: bool) -> int:
-    """Algorithmic HBM bytes of one wf_step; the fused step never writes or
-    reads A_L in global memory."""
-    total = sum(path_bytes(cfg).values())
-    if fused:
-        total -= 2 * cfg.units_per_layer * (cfg.n_prompt >> cfg.levels) * cfg.head_dim * 4
-    return total
 
 
 def _strip_comments(text: str) -> str:
@@ -252,28 +272,37 @@ def _oracle_pool(workers):
 
 def _unit_jobs(arrs, cfg, units):
     ks = cfg.k_per_level()
+    n_b, n_h = arrs["Q"].shape[:2]
     jobs = []
     for u in units:
-        b, h = divmod(u, cfg.heads)
+        b, h = divmod(u % (n_b * n_h), n_h)
         jobs.append((arrs["Q"][b, h], arrs["Kp"][b, h], arrs["Vp"][b, h], arrs["Kg"][b, h],
                      arrs["Vg"][b, h], cfg.levels, ks))
     return jobs
 
 
+def _oracle_sample(cfg, workers):
+    """Seeded units of layer 0 for the CPU legs (numpy generator): every unit of
+    the layer when that is cheap, else as many as there are workers."""
+    heads = list(range(cfg.heads)) if cfg.units_per_layer * cfg.n_prompt <= (1 << 22) else \
+        list(range(min(cfg.heads, max(workers, 1))))
+    return wl.generate_layer(cfg, 0, seqs=[0], heads=heads, workers=min(16, max(workers, 1)))
+
+
 def cpu_oracle_rate(arrs, cfg, budget_s: float, workers: int):
-    """Oracle tokens/s on a bounded sample: whole units, all host cores."""
-    U = cfg.units_per_layer
+    """Oracle tokens/s on a bounded sample: whole (sequence, layer, head) units
+    of the workload, all host cores."""
+    n_units = arrs["Q"].shape[0] * arrs["Q"].shape[1]
     with _oracle_pool(workers) as pool:
         list(pool.map(_oracle_unit, _unit_jobs(arrs, cfg, [0] * workers)))  # start workers
         done, t0 = 0, time.perf_counter()
         while time.perf_counter() - t0 < budget_s:
-            n = min(U, max(workers, 1))
-            units = [(done + i) % U for i in range(n)]
+            n = max(workers, 1)
+            units = [(done + i) % n_units for i in range(n)]
             list(pool.map(_oracle_unit, _unit_jobs(arrs, cfg, units)))
             done += n
         elapsed = time.perf_counter() - t0
-    tokens = done / U * tokens_per_step(cfg)
-    return tokens / elapsed, done, elapsed
+    return done * tokens_per_unit(cfg) / elapsed, done, elapsed
 
 
 # ------------------------------------------------------------------ arms
@@ -282,28 +311,30 @@ def run_reference(args, cfg):
     rank, world, _ = _rank_env()
     if rank != 0:
         return 0
-    arrs = wl.generate_layer(cfg, 0, workers=min(16, os.cpu_count() or 1))
     workers = os.cpu_count() or 1
-    U = cfg.units_per_layer
-    # Size each step's sample so the whole run takes about two minutes.
+    arrs = _oracle_sample(cfg, workers)
+    n_units = arrs["Q"].shape[0] * arrs["Q"].shape[1]
+    units_per_step = cfg.units_per_layer * cfg.layers
+    # Size each step's sample so that the whole run takes about two minutes.
     with _oracle_pool(workers) as pool:
         list(pool.map(_oracle_unit, _unit_jobs(arrs, cfg, [0] * workers)))
         t0 = time.perf_counter()
-        list(pool.map(_oracle_unit, _unit_jobs(arrs, cfg, list(range(min(U, workers))))))
+        list(pool.map(_oracle_unit, _unit_jobs(arrs, cfg, list(range(workers)))))
         per_round = time.perf_counter() - t0
-        rounds = max(1, min(math.ceil(U / workers),
+        rounds = max(1, min(math.ceil(units_per_step / workers),
                             int(120.0 / max(per_round * (args.steps + args.warmup), 1e-9))))
-        sample_units = min(U, rounds * workers)
+        sample_units = min(units_per_step, rounds * workers)
         for i in range(args.warmup):
             list(pool.map(_oracle_unit, _unit_jobs(arrs, cfg, list(range(sample_units)))))
         t0 = time.perf_counter()
         for i in range(args.steps):
-            units = [(i * sample_units + j) % U for j in range(sample_units)]
+            units = [(i * sample_units + j) % n_units for j in range(sample_units)]
             list(pool.map(_oracle_unit, _unit_jobs(arrs, cfg, units)))
         elapsed = time.perf_counter() - t0
-    frac = sample_units / U
+    frac = sample_units / units_per_step
     value = args.steps * frac * tokens_per_step(cfg) / elapsed
-    sample = (f"{sample_units} of {U} (sequence, head) units per step, float64 numpy oracle, "
+    sample = (f"{sample_units} of the {units_per_step} (sequence, layer, head) units of a step, "
+              f"drawn from {n_units} seeded units of layer 0; float64 numpy oracle, "
               f"{workers} single-threaded worker processes")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -317,6 +348,48 @@ def run_reference(args, cfg):
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def _event():
+    import torch
+    return torch.cuda.Event(enable_timing=True)
+
+
+def _capture(fn, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def _input_sets(cfg, dev, l2_bytes):
+    """Device-resident inputs the timed steps cycle through.  A multi-layer
+    workload holds every layer (independent seeds; one step = one call per
+    layer).  A one-layer workload holds enough copies of its layer that the
+    bytes one step touches times the copies exceed 4x L2, so that no step
+    finds its inputs in L2."""
+    import torch
+    if cfg.layers > 1:
+        return [wl.generate_layer_torch(cfg, layer, dev) for layer in range(cfg.layers)], 1
+    base = wl.generate_layer_torch(cfg, 0, dev)
+    n = max(2, math.ceil(4 * l2_bytes / max(layer_bytes(cfg), 1)))
+    return [base] + [{k: v.clone() for k, v in base.items()} for _ in range(n - 1)], n
+
+
+def _time_cycles(cycle, graphs, steps, steps_per_cycle, stream):
+    """CUDA-event time of `steps` steps: replays of the cycle graph (one call
+    per input set) plus, for a remainder, per-set graphs."""
+    e0, e1 = _event(), _event()
+    e0.record(stream)
+    for _ in range(steps // steps_per_cycle):
+        cycle.replay()
+    for i in range(steps % steps_per_cycle):
+        graphs[i].replay()
+    e1.record(stream)
+    import torch
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
 
 
 def run_ours(args, cfg):
@@ -334,44 +407,33 @@ def run_ours(args, cfg):
     dev = torch.device("cuda", local)
     bd.lib()
     ks = cfg.k_per_level()
-    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
-    arrs = wl.generate_layer(cfg, 0, workers=min(16, os.cpu_count() or 1))
-    base = {k: torch.from_numpy(v).to(device=dev, dtype=dt) for k, v in arrs.items()}
-    per_copy = sum(t.numel() * t.element_size() for t in base.values())
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    touched = path_bytes(cfg)
-    touched_bytes = sum(touched.values())
-    n_copies = max(2, math.ceil(4 * l2 / max(touched_bytes, 1)))
-    copies = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(n_copies - 1)]
+    sets, n_copies = _input_sets(cfg, dev, l2)
+    steps_per_cycle = 1 if cfg.layers > 1 else n_copies
+    base = sets[0]
+    per_set = sum(t.numel() * t.element_size() for t in base.values())
     dims = bd.make_dims(base["Q"], base["Kp"], cfg.levels)
     ws = bd.alloc_workspace(dims, ks, dev)
-    launches = bd.step_launch_count(dims, ks)
+    plan = bd.step_plan(dims, ks)
+    launches = plan["launches"]
     out = torch.empty(base["Q"].shape, dtype=torch.float32, device=dev)
     lse = torch.empty(base["Q"].shape[:3], dtype=torch.float32, device=dev)
     idx = torch.empty((cfg.batch, cfg.heads, ks[0]), dtype=torch.int32, device=dev)
 
-    def step(c, stream=None):
+    def step(c):
         bd.step(c["Q"], c["Kp"], c["Vp"], c["Kg"], c["Vg"], cfg.levels, ks, ws, out=out,
-                lse=lse, idx_out=idx, stream=stream)
+                lse=lse, idx_out=idx)
 
-    for c in copies:  # eager pass (sets kernel attributes before capture)
+    for c in sets:  # eager pass (sets kernel attributes before capture)
         step(c)
     torch.cuda.synchronize()
-    # One graph per input copy (one step each) and one graph that runs a step
-    # on every copy in turn: the timed loop replays the latter, so that graph
-    # launch latency is paid once per n_copies steps, as it would be for a
-    # model's layers captured together.
-    graphs = []
+    # One graph per input set and one graph with a call on every set in turn:
+    # the timed loop replays the latter (for a multi-layer workload it is one
+    # whole step, the layers in order, as a model's layers would be captured).
     cap_stream = torch.cuda.Stream(device=dev)
-    for c in copies:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=cap_stream):
-            step(c)
-        graphs.append(g)
-    cycle = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(cycle, stream=cap_stream):
-        for c in copies:
-            step(c)
+    graphs = [_capture(lambda c=c: step(c), cap_stream) for c in sets] \
+        if steps_per_cycle > 1 else []
+    cycle = _capture(lambda: [step(c) for c in sets], cap_stream)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)
 
@@ -380,67 +442,66 @@ def run_ours(args, cfg):
     sampler = ClockSampler(smi_index) if rank == 0 else None
     time.sleep(0.3)
 
-    # ---- warm-up + timed region (CUDA graph of wf_step per input copy)
+    # ---- warm-up + timed region
     for i in range(args.warmup):
-        graphs[i % n_copies].replay()
+        (graphs[i % n_copies] if graphs else cycle).replay()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps // n_copies):
-        cycle.replay()
-    for i in range(args.steps % n_copies):
-        graphs[i].replay()
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    t_ms = allreduce_max(_time_cycles(cycle, graphs, args.steps, steps_per_cycle, stream),
+                         world, dev)
     if world > 1:
         dist.barrier()
-    t_ms = allreduce_max(ev0.elapsed_time(ev1), world, dev)
     ms_per_step = t_ms / args.steps
     value = job_value(world, tokens_per_step(cfg), args.steps, t_ms)
+    layer_us = ms_per_step * 1e3 / cfg.layers
 
-    # ---- steps 2-5 with A_L cached from an earlier step (unchanged prompt keys)
-    als = [bd.dwt_lowpass(c["Kp"], cfg.levels) for c in copies]
-    torch.cuda.synchronize()
-
-    def step_cached(c, al):
-        bd.step_cached_al(c["Q"], c["Kp"], c["Vp"], c["Kg"], c["Vg"], al, cfg.levels, ks, ws,
-                          out=out, lse=lse, idx_out=idx)
-
-    for c, al in zip(copies, als):
-        step_cached(c, al)
-    torch.cuda.synchronize()
-    cyc_cached = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(cyc_cached, stream=cap_stream):
-        for c, al in zip(copies, als):
-            step_cached(c, al)
-    for _ in range(max(1, args.warmup // n_copies)):
-        cyc_cached.replay()
-    torch.cuda.synchronize()
-    r_reps = max(1, args.steps // n_copies)
-    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    c0.record(stream)
-    for _ in range(r_reps):
-        cyc_cached.replay()
-    c1.record(stream)
-    torch.cuda.synchronize()
-    cached_ms = c0.elapsed_time(c1) / (r_reps * n_copies)
-    del cyc_cached, als
-
-    # ---- per-stage kernel durations (same launches, events on the launch stream)
-    stage_ms = {"dwt": [], "score": [], "filter": [], "attn": []}
-    al = torch.empty((cfg.batch, cfg.heads, cfg.n_prompt >> cfg.levels, cfg.head_dim),
-                     dtype=torch.float32, device=dev)
-    idx_l = torch.empty((cfg.batch, cfg.heads, ks[-1]), dtype=torch.int32, device=dev)
+    # ---- the first launch of a two-launch step, alone (the standalone DWT
+    # entry point over the same keys): back-to-back launches over the sets.
     lib = bd.lib()
     sp = bd._stream(stream)
+    al = torch.empty((cfg.batch, cfg.heads, cfg.n_prompt >> cfg.levels, cfg.head_dim),
+                     dtype=torch.float32, device=dev)
+    n_dwt = max(20, len(sets))
+    d0, d1 = _event(), _event()
+    d0.record(stream)
+    for i in range(n_dwt):
+        lib.wf_dwt_lowpass(bd.ctypes.byref(dims), bd._ptr(sets[i % len(sets)]["Kp"]), bd._ptr(al),
+                           None, sp)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    dwt_us = 1e3 * d0.elapsed_time(d1) / n_dwt
+
+    # ---- steps 2-5 with A_L cached from an earlier step (unchanged prompt keys)
+    als = [bd.dwt_lowpass(c["Kp"], cfg.levels) for c in sets]
+    torch.cuda.synchronize()
+
+    def step_cached(c, a):
+        bd.step_cached_al(c["Q"], c["Kp"], c["Vp"], c["Kg"], c["Vg"], a, cfg.levels, ks, ws,
+                          out=out, lse=lse, idx_out=idx)
+
+    for c, a in zip(sets, als):
+        step_cached(c, a)
+    torch.cuda.synchronize()
+    cyc_cached = _capture(lambda: [step_cached(c, a) for c, a in zip(sets, als)], cap_stream)
+    for _ in range(max(1, args.warmup // steps_per_cycle)):
+        cyc_cached.replay()
+    torch.cuda.synchronize()
+    r_reps = max(1, args.steps // steps_per_cycle)
+    cached_ms = _time_cycles(cyc_cached, [], r_reps * steps_per_cycle, steps_per_cycle,
+                             stream) / (r_reps * steps_per_cycle)
+    cached_layer_us = cached_ms * 1e3 / cfg.layers
+    del cyc_cached
+
+    # ---- per-stage kernel durations (staged entry points, events on the launch stream)
+    stage_ms = {"dwt": [], "score": [], "filter": [], "attn": []}
+    idx_l = torch.empty((cfg.batch, cfg.heads, ks[-1]), dtype=torch.int32, device=dev)
     karr = bd._k_array(ks)
-    n_stage_steps = max(args.steps, 20)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_stage_steps)]
-    for i in range(n_stage_steps):
-        c = copies[i % n_copies]
+    n_stage = 20
+    evs = [[_event() for _ in range(5)] for _ in range(n_stage)]
+    for i in range(n_stage):
+        c = sets[i % len(sets)]
         e = evs[i]
         e[0].record(stream)
         lib.wf_dwt_lowpass(bd.ctypes.byref(dims), bd._ptr(c["Kp"]), bd._ptr(al), None, sp)
@@ -461,111 +522,89 @@ def run_ours(args, cfg):
         for j, name in enumerate(("dwt", "score", "filter", "attn")):
             stage_ms[name].append(e[j].elapsed_time(e[j + 1]))
     stage_us = {k: 1e3 * statistics.mean(v) for k, v in stage_ms.items()}
-    # The standalone DWT entry point: average duration over back-to-back launches (rotating
-    # input copies, as in the timed region) between one event pair.
-    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n_dwt = max(args.steps, 20)
-    d0.record(stream)
-    for i in range(n_dwt):
-        lib.wf_dwt_lowpass(bd.ctypes.byref(dims), bd._ptr(copies[i % n_copies]["Kp"]), bd._ptr(al),
-                           None, sp)
-    d1.record(stream)
-    torch.cuda.synchronize()
-    dwt_us = 1e3 * d0.elapsed_time(d1) / n_dwt
 
     # ---- first-step cache write (eq. (2)) with A_L, from token-major K/V:
-    # two input/output sets alternate (each launch touches more than L2), and
-    # the launches are replayed from one CUDA graph so that host call
-    # overhead stays out of the kernel time.
+    # two input/output sets alternate (each launch touches more than L2),
+    # replayed from one CUDA graph so host call overhead stays out.
     cache_sets = []
-    for c in copies[:2]:
+    for c in sets[:2]:
         tk = torch.cat([c["Kp"], c["Kg"]], dim=2).transpose(1, 2).contiguous()
         tv = torch.cat([c["Vp"], c["Vg"]], dim=2).transpose(1, 2).contiguous()
         cache_sets.append((tk, tv, bd.cache_init(tk, tv, cfg.n_prompt, cfg.levels)))
     torch.cuda.synchronize()
     n_cache = 20
-    cache_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(cache_graph, stream=cap_stream):
-        for i in range(n_cache):
-            tk, tv, o = cache_sets[i % 2]
-            bd.cache_init(tk, tv, cfg.n_prompt, cfg.levels, out=o)
+    cache_graph = _capture(lambda: [bd.cache_init(cache_sets[i % 2][0], cache_sets[i % 2][1],
+                                                  cfg.n_prompt, cfg.levels,
+                                                  out=cache_sets[i % 2][2])
+                                    for i in range(n_cache)], cap_stream)
     for _ in range(3):
         cache_graph.replay()
     torch.cuda.synchronize()
     cache_reps = max(1, min(50, args.steps // n_cache))
-    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    k0.record(stream)
-    for _ in range(cache_reps):
-        cache_graph.replay()
-    k1.record(stream)
-    torch.cuda.synchronize()
-    cache_us = 1e3 * k0.elapsed_time(k1) / (cache_reps * n_cache)
+    cache_us = 1e3 * _time_cycles(cache_graph, [], cache_reps, 1, stream) / (cache_reps * n_cache)
     del cache_graph, cache_sets
+    torch.cuda.empty_cache()
 
     # ---- the step with a longer basis (eight-tap Daubechies filter): the
     # general path (pyramid launches, level-by-level filter CTA per unit,
-    # gather + attention), from a CUDA graph over the rotating input copies.
+    # gather + attention), from a CUDA graph over (up to four) input sets.
     db4 = bd.daubechies_lowpass(4)
     basis_ws = torch.zeros(bd.basis_workspace_bytes(dims, db4, ks), dtype=torch.uint8,
                            device=dev)
+    bsets = sets[:4]
 
     def step_basis(c):
         bd.step_basis(c["Q"], c["Kp"], c["Vp"], c["Kg"], c["Vg"], cfg.levels, ks, db4,
                       ws=basis_ws, out=out, lse=lse, idx_out=idx)
 
-    for c in copies:
+    for c in bsets:
         step_basis(c)
     torch.cuda.synchronize()
-    basis_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(basis_graph, stream=cap_stream):
-        for c in copies:
-            step_basis(c)
-    for _ in range(2):
-        basis_graph.replay()
+    basis_graph = _capture(lambda: [step_basis(c) for c in bsets], cap_stream)
+    basis_graph.replay()
     torch.cuda.synchronize()
-    basis_reps = max(1, min(20, args.steps // n_copies))
-    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    b0.record(stream)
-    for _ in range(basis_reps):
-        basis_graph.replay()
-    b1.record(stream)
-    torch.cuda.synchronize()
-    basis_ms = b0.elapsed_time(b1) / (basis_reps * n_copies)
+    basis_reps = max(1, min(10, args.steps // len(bsets)))
+    basis_ms = _time_cycles(basis_graph, [], basis_reps, 1, stream) / (basis_reps * len(bsets))
     del basis_graph, basis_ws
+    torch.cuda.empty_cache()
 
-    # ---- end to end through the host-buffer entry point (pinned host memory)
-    host = {k: v.cpu().pin_memory() for k, v in base.items()}
-    host["O"] = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    # ---- end to end through the host-buffer entry point: every layer-step
+    # sends its Q/K_p/V_p/K_g/V_g from pinned host memory and reads O back.
+    # The host side holds (up to) two layers' inputs, used alternately.
+    host_sets = []
+    for c in sets[:2]:
+        h = {k: v.cpu().pin_memory() for k, v in c.items()}
+        h["O"] = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+        host_sets.append(h)
     stage = {k: torch.empty_like(v) for k, v in base.items()}
     stage["O"] = torch.empty_like(out)
-    h2d = sum(host[k].numel() * host[k].element_size() for k in ("Q", "Kp", "Vp", "Kg", "Vg"))
-    d2h = host["O"].numel() * host["O"].element_size()
-    e2e_steps = max(10, min(args.steps, 200))
-    for _ in range(3):
-        bd.step_host(dims, host, ks, stage, ws, stream=stream)
+    h2d_layer = sum(host_sets[0][k].numel() * host_sets[0][k].element_size()
+                    for k in ("Q", "Kp", "Vp", "Kg", "Vg"))
+    d2h_layer = host_sets[0]["O"].numel() * host_sets[0]["O"].element_size()
+    e2e_steps = max(3, min(args.steps, 200 // cfg.layers))
+
+    def e2e_step():
+        for layer in range(cfg.layers):
+            bd.step_host(dims, host_sets[layer % len(host_sets)], ks, stage, ws, stream=stream)
+
+    e2e_step()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0, e1 = _event(), _event()
     e0.record(stream)
     for _ in range(e2e_steps):
-        bd.step_host(dims, host, ks, stage, ws, stream=stream)
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = allreduce_max(e0.elapsed_time(e1), world, dev)
     e2e_value = job_value(world, tokens_per_step(cfg), e2e_steps, e2e_ms)
-    # ---- end to end with a device-resident cache (the serving loop): per step
-    # the host sends Q and the generation block's new K/V rows (token-major),
-    # eq. (4) writes them into the cache, steps 2-5 run from the A_L that
-    # wf_cache_init wrote, and O comes back.  One resident cache per input copy,
-    # as each layer of a model keeps its own.
-    res_caches = []
-    for c in copies:
-        tk = torch.cat([c["Kp"], c["Kg"]], dim=2).transpose(1, 2).contiguous()
-        tv = torch.cat([c["Vp"], c["Vg"]], dim=2).transpose(1, 2).contiguous()
-        res_caches.append(bd.cache_init(tk, tv, cfg.n_prompt, cfg.levels))
-        del tk, tv
-    # Q and the new rows sit back to back on both sides (one H2D copy per step).
+    del host_sets, stage
+
+    # ---- end to end with device-resident caches (the serving loop): per
+    # layer-step the host sends Q and the generation block's new K/V rows
+    # (token-major, back to back: one copy), eq. (4) writes them into that
+    # layer's cache, steps 2-5 run from its cached A_L, and O comes back.
     new_k = base["Kg"].transpose(1, 2).contiguous()
     new_v = base["Vg"].transpose(1, 2).contiguous()
     n_gen_el = base["Q"].numel()
@@ -578,22 +617,31 @@ def run_ours(args, cfg):
         dstage[name] = d_pack[i * n_gen_el:(i + 1) * n_gen_el].view(src.shape)
     dhost["O"] = torch.empty(out.shape, dtype=torch.float32).pin_memory()
     dstage["O"] = torch.empty_like(out)
+    caches = [{"Kp": c["Kp"], "Vp": c["Vp"], "Kg": c["Kg"], "Vg": c["Vg"], "AL": a}
+              for c, a in zip(sets, als)]
     res_h2d = sum(dhost[k].numel() * dhost[k].element_size() for k in ("Q", "K", "V"))
     res_d2h = dhost["O"].numel() * dhost["O"].element_size()
-    for i in range(3):
-        bd.decode_step_host(dims, dhost, ks, dstage, res_caches[i % n_copies], ws, stream=stream)
+    res_steps = max(10, min(args.steps, 400 // cfg.layers))
+
+    def res_step(i):
+        for layer in range(cfg.layers):
+            cache = caches[(i * cfg.layers + layer) % len(caches)]
+            bd.decode_step_host(dims, dhost, ks, dstage, cache, ws, stream=stream)
+
+    for i in range(2):
+        res_step(i)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0, r1 = _event(), _event()
     r0.record(stream)
-    for i in range(e2e_steps):
-        bd.decode_step_host(dims, dhost, ks, dstage, res_caches[i % n_copies], ws, stream=stream)
+    for i in range(res_steps):
+        res_step(i)
     r1.record(stream)
     torch.cuda.synchronize()
     res_ms = allreduce_max(r0.elapsed_time(r1), world, dev)
-    res_value = job_value(world, tokens_per_step(cfg), e2e_steps, res_ms)
-    del res_caches
+    res_value = job_value(world, tokens_per_step(cfg), res_steps, res_ms)
+    del caches, als
     clocks = sampler.stop() if sampler else None
     status = bd.read_device_status(ws)
 
@@ -603,102 +651,106 @@ def run_ours(args, cfg):
     peak, peak_kind = _peaks()
     peak_source = (f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                    else "fallback 6.8 TB/s")
-    dwt_bytes = touched["dwt"]
-    cache_bytes = cache_init_bytes(cfg)
-    dwt_achieved = dwt_bytes / (dwt_us * 1e-6) / 1e9
-    fused = launches == 1
-    total_bytes = step_bytes(cfg, fused)
-    dwt_roofline = {"kernel": "dwt_stream_kernel (wf_dwt_lowpass, fp32 A_L)", "bound": "hbm",
-                    "achieved": dwt_achieved, "peak": peak, "unit": "GB/s",
-                    "frac": dwt_achieved / peak, "peak_source": peak_source,
-                    "traffic": _traffic(DWT_TRAFFIC), "algorithmic_bytes_per_launch": dwt_bytes,
-                    "launch_us": dwt_us,
-                    "timing": f"{n_dwt} back-to-back launches, rotating input copies"}
-    if fused:
-        # One kernel per step: its average duration is the timed region / K.
-        step_ach = total_bytes / (ms_per_step * 1e-3) / 1e9
-        roofline = {"kernel": "path_kernel (whole step: Haar low-pass, scoring, filter, gather,"
-                              " attention)", "bound": "hbm", "achieved": step_ach, "peak": peak,
-                    "unit": "GB/s", "frac": step_ach / peak, "peak_source": peak_source,
-                    "traffic": _traffic(PATH_TRAFFIC), "algorithmic_bytes_per_launch": total_bytes,
-                    "launch_us": ms_per_step * 1e3,
-                    "timing": "CUDA events over the timed region / K (one launch per step)"}
+    lbytes = layer_bytes(cfg)
+    sbytes = stream_bytes(cfg)
+    dwt_roofline = {"kernel": "dwt_stream_kernel (wf_dwt_lowpass: K_p stream, fp32 A_L)",
+                    "bound": "hbm", "achieved": sbytes / (dwt_us * 1e-6) / 1e9, "peak": peak,
+                    "unit": "GB/s", "frac": sbytes / (dwt_us * 1e-6) / 1e9 / peak,
+                    "peak_source": peak_source, "traffic": _traffic(DWT_TRAFFIC),
+                    "algorithmic_bytes_per_launch": sbytes, "launch_us": dwt_us,
+                    "timing": f"{n_dwt} back-to-back launches over the input sets"}
+    if launches == 1:
+        # One kernel per layer-step: its average duration is the timed region
+        # divided by the layer-steps in it.
+        roofline = {"kernel": "path_kernel (the whole layer-step: Haar low-pass, scoring, "
+                              "filter, gather, attention)", "bound": "hbm",
+                    "achieved": lbytes / (layer_us * 1e-6) / 1e9, "peak": peak, "unit": "GB/s",
+                    "frac": lbytes / (layer_us * 1e-6) / 1e9 / peak, "peak_source": peak_source,
+                    "traffic": _traffic(PATH_TRAFFIC), "algorithmic_bytes_per_launch": lbytes,
+                    "launch_us": layer_us,
+                    "timing": "CUDA events over the timed region / layer-steps (one launch each)"}
     else:
-        # Two launches per step: the roofline line is the longer of the two
-        # kernels; the path kernel alone is what wf_step_cached_al times.
-        rest_bytes = touched["score"] + touched["filter"] + touched["attn"]
-        if cached_ms * 1e3 > dwt_us:
-            rest_ach = rest_bytes / (cached_ms * 1e-3) / 1e9
-            roofline = {"kernel": "path_kernel (steps 2-5; the longer of the step's two launches)",
-                        "bound": "hbm", "achieved": rest_ach, "peak": peak, "unit": "GB/s",
-                        "frac": rest_ach / peak, "peak_source": peak_source, "traffic": None,
-                        "algorithmic_bytes_per_launch": rest_bytes,
-                        "launch_us": cached_ms * 1e3,
-                        "timing": "graph replays of wf_step_cached_al (the same kernel without "
-                                  "the DWT launch) / steps"}
-        else:
-            roofline = dwt_roofline
+        # Two launches per layer-step; the dominant one is the path kernel
+        # (steps 2-5): its bytes are the layer's minus the stream's, its
+        # duration the layer-step's minus the separately timed stream launch.
+        pk_us = layer_us - dwt_us
+        pk_bytes = lbytes - sbytes
+        big = pk_us >= dwt_us
+        roofline = {"kernel": "path_kernel (steps 2-5 of the layer-step)", "bound": "hbm",
+                    "achieved": pk_bytes / (pk_us * 1e-6) / 1e9, "peak": peak, "unit": "GB/s",
+                    "frac": pk_bytes / (pk_us * 1e-6) / 1e9 / peak, "peak_source": peak_source,
+                    "traffic": _traffic(PATH_TRAFFIC), "algorithmic_bytes_per_launch": pk_bytes,
+                    "launch_us": pk_us,
+                    "timing": "layer-step time from the timed region minus the separately timed "
+                              "stream launch"} if big else dwt_roofline
     cpu_rate, cpu_units, cpu_s = (None, 0, 0.0)
     workers = os.cpu_count() or 1
     if world == 1 and not args.no_cpu_baseline:
+        arrs = _oracle_sample(cfg, workers)
         cpu_rate, cpu_units, cpu_s = cpu_oracle_rate(arrs, cfg, args.cpu_seconds, workers)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": cfg.dtype, "data": "synthetic (seeded generator with planted needle spans)",
+        "dtype": cfg.dtype, "data": "synthetic (seeded generator with planted needle spans, "
+                                    "drawn on the device)",
         "config": _config_obj(cfg, {
-            "l2": f"rotating {n_copies} device input copies ({n_copies * per_copy / 2**20:.0f} MiB,"
-                  f" {n_copies} x {touched_bytes / 2**20:.1f} MiB touched per step > "
-                  f"{l2 / 2**20:.0f} MiB L2)",
-            "timing": f"CUDA events around K steps: replays of one CUDA graph holding one wf_step"
-                      f" per input copy ({n_copies} steps per replay), remainder from per-copy graphs"}),
+            "l2": (f"{len(sets)} distinct device-resident layers, "
+                   f"{len(sets) * per_set / 2**30:.1f} GiB, each step reads every one"
+                   if cfg.layers > 1 else
+                   f"rotating {n_copies} device input copies ({n_copies * per_set / 2**20:.0f} "
+                   f"MiB, {n_copies} x {layer_bytes(cfg) / 2**20:.1f} MiB touched per step > "
+                   f"{l2 / 2**20:.0f} MiB L2)"),
+            "timing": "CUDA events around K steps: replays of one CUDA graph holding one wf_step "
+                      "per input set in order"}),
         "roofline": roofline,
-        "path_roofline": {"bytes_per_step": total_bytes,
-                          "achieved": total_bytes / (ms_per_step * 1e-3) / 1e9,
-                          "peak": peak, "unit": "GB/s",
-                          "frac": total_bytes / (ms_per_step * 1e-3) / 1e9 / peak},
+        "path_roofline": {"what": "whole step, algorithmic bytes of every term",
+                          "bytes_per_step": lbytes * cfg.layers,
+                          "achieved": lbytes / (layer_us * 1e-6) / 1e9, "peak": peak,
+                          "unit": "GB/s", "frac": lbytes / (layer_us * 1e-6) / 1e9 / peak},
         "dwt_roofline": dwt_roofline,
+        "plan": plan,
+        "layer_step_us": layer_us,
         "cached_al_step": {
             "what": "wf_step_cached_al: steps 2-5 with A_L from an earlier wf_dwt_lowpass "
                     "(prompt keys unchanged between denoising steps)",
             "value": tokens_per_step(cfg) / (cached_ms * 1e-3), "unit": "tokens/s",
-            "ms_per_step": cached_ms,
-            "algorithmic_bytes_per_step": touched["score"] + touched["filter"] + touched["attn"],
-            "achieved_gbs": (touched["score"] + touched["filter"] + touched["attn"]) /
-                            (cached_ms * 1e-3) / 1e9},
+            "ms_per_step": cached_ms, "layer_step_us": cached_layer_us,
+            "algorithmic_bytes_per_layer": lbytes - sbytes,
+            "achieved_gbs": (lbytes - sbytes) / (cached_layer_us * 1e-6) / 1e9},
         "cache_init_roofline": {
             "kernel": "cache_write_kernel (wf_cache_init: eq. (2) cache write of K/V from "
-                      "token-major projections + fp32 A_L of the prompt keys)",
-            "bound": "hbm", "achieved": cache_bytes / (cache_us * 1e-6) / 1e9, "peak": peak,
-            "unit": "GB/s", "frac": cache_bytes / (cache_us * 1e-6) / 1e9 / peak,
+                      "token-major projections + fp32 A_L of the prompt keys), one layer",
+            "bound": "hbm", "achieved": cache_init_bytes(cfg) / (cache_us * 1e-6) / 1e9,
+            "peak": peak, "unit": "GB/s",
+            "frac": cache_init_bytes(cfg) / (cache_us * 1e-6) / 1e9 / peak,
             "peak_source": peak_source, "traffic": _traffic(CACHE_TRAFFIC),
-            "algorithmic_bytes_per_launch": cache_bytes, "launch_us": cache_us,
+            "algorithmic_bytes_per_launch": cache_init_bytes(cfg), "launch_us": cache_us,
             "timing": "CUDA graph of 20 launches over two alternating input/output sets, "
                       "events around its replays"},
         "basis_step": {
             "what": "wf_step_basis with the eight-tap Daubechies low-pass (periodic pyramid, "
-                    "level-by-level filter, gather + attention): the general path for a "
-                    "longer basis",
-            "value": tokens_per_step(cfg) / (basis_ms * 1e-3), "unit": "tokens/s",
-            "ms_per_step": basis_ms,
-            "launches_per_step": cfg.levels + 2},
+                    "level-by-level filter, gather + attention), one layer",
+            "value": tokens_per_step(cfg) / cfg.layers / (basis_ms * 1e-3), "unit": "tokens/s",
+            "layer_step_ms": basis_ms, "launches_per_layer_step": cfg.levels + 2},
         "stages_us": stage_us,
         "cpu_baseline": None if cpu_rate is None else {
             "value": cpu_rate, "unit": "tokens/s", "cores": workers, "kind": "oracle",
-            "sample": f"{cpu_units} (sequence, head) units of this workload in {cpu_s:.1f} s, "
-                      f"float64 numpy oracle, {workers} single-threaded worker processes"},
-        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "entry_point": "wf_step_host (pinned host Q/Kp/Vp/Kg/Vg in, O out)"},
+            "sample": f"{cpu_units} (sequence, layer, head) units of this workload in "
+                      f"{cpu_s:.1f} s, float64 numpy oracle, {workers} single-threaded "
+                      f"worker processes"},
+        "e2e": {"value": e2e_value, "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d_layer * cfg.layers,
+                "d2h_bytes_per_step": d2h_layer * cfg.layers, "steps": e2e_steps,
+                "entry_point": "wf_step_host per layer (pinned host Q/Kp/Vp/Kg/Vg in, O out)"},
         "e2e_resident_cache": {
-            "value": res_value, "unit": "tokens/s", "h2d_bytes_per_step": res_h2d,
-            "d2h_bytes_per_step": res_d2h, "steps": e2e_steps,
-            "ms_per_step": res_ms / e2e_steps,
-            "entry_point": "wf_decode_step_host (pinned host Q and new token-major K/V rows in, "
-                           "back to back: one H2D copy; eq. (4) update + steps 2-5 on a "
-                           "device-resident cache written by wf_cache_init; O out)"},
-        "gpu_launches": launches * args.steps,  # path_kernel (+ dwt_stream_kernel unless fused)
+            "value": res_value, "unit": "tokens/s", "h2d_bytes_per_step": res_h2d * cfg.layers,
+            "d2h_bytes_per_step": res_d2h * cfg.layers, "steps": res_steps,
+            "ms_per_step": res_ms / res_steps,
+            "entry_point": "wf_decode_step_host per layer (pinned host Q and new token-major "
+                           "K/V rows in, one H2D copy; eq. (4) update + steps 2-5 on the "
+                           "layer's device-resident cache and A_L; O out)"},
+        "gpu_launches": launches * cfg.layers * args.steps,
         "clocks": clocks,
         "device_status": status,
     }

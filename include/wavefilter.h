@@ -130,6 +130,43 @@ int wf_workspace_bytes(const wf_dims* dims, const int32_t* k_per_level,
 int wf_step_launch_count(const wf_dims* dims, const int32_t* k_per_level,
                          int32_t* launches);
 
+/* Where the token-level logits of the recursive filter are kept (wf_plan). */
+enum {
+  WF_LOGITS_SHARED = 0,          /* in shared memory                              */
+  WF_LOGITS_WORKSPACE = 1,       /* written to the workspace and read back        */
+  WF_LOGITS_TENSOR_MEMORY = 2,   /* in the accumulators' tensor memory            */
+  WF_LOGITS_RECOMPUTED = 3       /* recomputed from the key rows for each pass    */
+};
+
+/* Launch plan of one wf_step call (diagnostics). */
+typedef struct {
+  int32_t launches;      /* as wf_step_launch_count                                  */
+  int32_t cluster;       /* CTAs (one thread-block cluster) per (sequence, head) unit */
+  int32_t final_gather;  /* 1: every CTA of a unit selects the budget over all of the
+                            unit's token candidates; 0: the radix select runs
+                            distributed over the cluster                             */
+  int32_t token_logits;  /* WF_LOGITS_*                                              */
+  int32_t smem_bytes;    /* dynamic shared memory per CTA of the path kernel         */
+} wf_plan;
+
+/* Fills *plan with the launch plan wf_step uses for these sizes on the
+ * current device.  Host only; launches nothing.
+ * Errors: WF_ERR_NULL/SHAPE/UNSUPPORTED, as wf_workspace_bytes. */
+int wf_step_plan(const wf_dims* dims, const int32_t* k_per_level, wf_plan* plan);
+
+/* Fault injection for tests of the bounded device waits (no counterpart in
+ * the paper).  Arms a one-shot injection consumed by the next kernel launch
+ * that streams K_p through mbarrier-counted bulk copies (the separate DWT
+ * launch of wf_step / wf_dwt_lowpass, or the single-launch wf_step): in its
+ * first CTA the first copy of the ring is never issued and the wait for it
+ * gives up after `polls` polls (polls >= 1), which raises WF_DEV_WAIT_TIMEOUT
+ * in the workspace status word.  Every copy that was issued is still waited
+ * for, so none is in flight when the kernel ends; the launch returns WF_OK,
+ * its outputs are meaningless, and later calls behave normally.
+ * polls = 0 disarms.  Process-wide; not for concurrent use with other calls.
+ * Errors: WF_ERR_SHAPE if polls < 0. */
+int wf_debug_inject_wait_timeout(int32_t polls);
+
 /* Clears the device status word at the start of `workspace` (async). */
 int wf_clear_device_status(void* workspace, size_t workspace_bytes, void* stream);
 
@@ -367,7 +404,10 @@ int wf_step_basis(const wf_dims* dims, const double* lowpass, int32_t taps,
  *   10 % budgets).
  *   The first call on a device, with that device current, looks up the
  *   array's device address (cudaGetSymbolAddress); make that first call
- *   before any stream capture.  Every call shares the one array and it keeps
+ *   before any stream capture.  The address is kept for the life of the
+ *   process: after cudaDeviceReset (or any other teardown of the device's
+ *   primary context) this entry point must not be called again in that
+ *   process.  Every call shares the one array and it keeps
  *   the last call's contents (the status word is cleared at the start of each
  *   call), so calls that overlap on the GPU — concurrent streams, or several
  *   host threads — race; serialise them.  The device status word is not

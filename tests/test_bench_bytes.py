@@ -1,6 +1,7 @@
 """The bench's algorithmic byte counts (the numerators of every roofline
-fraction it prints), written out term by term for the 4096-token layer:
-32 units, N_p = 4096, d = 128, bf16, G = 32, L = 4, k_L = 64, B = 512."""
+fraction it prints), written out term by term: the 4096-token layer (32
+units, N_p = 4096, d = 128, bf16, G = 32, L = 4, k_L = 64, B = 512) and the
+32-layer full denoising step."""
 
 import bench
 from wavelet_guided_sparse_gb300 import workloads as wl
@@ -15,19 +16,26 @@ def test_workload_is_the_one_written_out():
     assert cfg.k_per_level()[L] == KL and cfg.budget == B and cfg.dtype == "bf16"
 
 
-def test_single_launch_step_bytes():
+def test_layer_bytes_term_by_term():
     kp_stream = U * N * D * E                 # every prompt key once
+    al = 2 * U * P * D * 4                    # A_L written and read back (fp32)
     span_rows = U * (KL << L) * D * E         # the coarse survivors' spans
     gathered = U * 2 * B * D * E              # selected keys and values
-    small = U * (3 * G * D * E                # Q, read by scoring, filtering, attention
-                 + 2 * G * D * E              # K_g, V_g
+    small = U * (2 * G * D * E                # K_g, V_g
+                 + G * D * E                  # Q
                  + G * D * 4                  # O written
-                 + (KL + KL + B + B) * 4)     # survivor and token index lists
-    assert bench.step_bytes(wl.CONFIGS["llada8b_layer"], fused=True) == (
-        kp_stream + span_rows + gathered + small)
-    # Two launches: A_L written by the stream and read back by the scoring.
-    assert bench.step_bytes(wl.CONFIGS["llada8b_layer"], fused=False) == (
-        kp_stream + span_rows + gathered + small + 2 * U * P * D * 4)
+                 + 4 * B)                     # selected token indices
+    cfg = wl.CONFIGS["llada8b_layer"]
+    assert bench.layer_bytes(cfg) == kp_stream + al + span_rows + gathered + small
+    assert round(bench.layer_bytes(cfg) / 1e6, 2) == 60.10
+    assert bench.stream_bytes(cfg) == kp_stream + al // 2
+
+
+def test_full_step_bytes():
+    cfg = wl.CONFIGS["full_step"]
+    assert cfg.layers == 32 and cfg.k_per_level()[cfg.levels] == 128
+    assert bench.tokens_per_step(cfg) == 32 * 65536
+    assert round(bench.layer_bytes(cfg) * cfg.layers / 1e9, 1) == 22.6
 
 
 def test_cache_init_bytes():

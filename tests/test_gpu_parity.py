@@ -16,7 +16,8 @@ import torch
 
 import oracle.wavefilter_oracle as wo
 from gpu_common import (AL_RTOL, GAP_TOL, OUT_ATOL, WORKERS, check_index_set,
-                        compare_step_unit, oracle_unit, run_step, to_device, unit_inputs)
+                        compare_step_unit, layer_with_gaps, oracle_unit, pick_units, run_step,
+                        to_device, unit_inputs)
 from wavelet_guided_sparse_gb300 import binding as bd
 from wavelet_guided_sparse_gb300 import workloads as wl
 
@@ -263,10 +264,23 @@ def test_full_budget_is_full_attention():
 
 # ---------------------------------------------------------- whole step, configs
 
-def _step_config(name, units=None, layer=0, cached_al=False):
+_GAPS = {}
+
+
+def layer_gaps(name, layer=0):
+    """Inputs of one layer and each unit's smallest oracle boundary gap."""
+    key = (name, layer)
+    if key not in _GAPS:
+        _GAPS.clear()
+        _CACHE.clear()
+        _GAPS[key] = layer_with_gaps(name, layer)
+    return _GAPS[key]
+
+
+def _step_config(name, units=None, layer=0, cached_al=False, arrs=None):
     cfg = wl.CONFIGS[name]
     ks = cfg.k_per_level()
-    arrs = layer_inputs(name, layer)
+    arrs = arrs if arrs is not None else layer_inputs(name, layer)
     dev = to_device(arrs, cfg.dtype)
     al = bd.dwt_lowpass(dev["Kp"], cfg.levels) if cached_al else None
     out, lse, idx, status = run_step(dev, cfg.levels, ks, al=al)
@@ -285,6 +299,21 @@ def _step_config(name, units=None, layer=0, cached_al=False):
     return kinds
 
 
+def _step_sampled(name, layer=0, cached_al=False):
+    """A large workload at full shape: every unit runs on the GPU; the units
+    compared with the oracle in full are picked from a pass over every
+    unit's oracle gaps, so that decisive units (index sets compared element by
+    element) are among them whenever the layer has any, next to near-tie
+    units (validated) and the layer's last unit."""
+    arrs, gaps = layer_gaps(name, layer)
+    units = pick_units(gaps)
+    kinds = _step_config(name, units=units, layer=layer, cached_al=cached_al, arrs=arrs)
+    assert len(kinds) == len(units)
+    if any(g > GAP_TOL for g in gaps.values()):
+        assert kinds.count("exact") >= 1, (name, units, kinds)
+    return kinds, gaps
+
+
 @pytest.mark.parametrize("name", ["tiny", "llada8b_layer"])
 def test_step_matches_oracle_all_units(name):
     kinds = _step_config(name)
@@ -300,26 +329,81 @@ def test_step_cached_al_matches_oracle_all_units(name):
 
 
 def test_step_cached_al_long_prompt_sampled():
-    kinds = _step_config("long_prompt", units=[(0, 0), (0, 31)], cached_al=True)
-    assert len(kinds) == 2
+    _step_sampled("long_prompt", cached_al=True)
 
 
 def test_step_long_prompt_sampled():
-    kinds = _step_config("long_prompt", units=[(0, 0), (0, 13), (0, 31)])
-    assert len(kinds) == 3
+    kinds, gaps = _step_sampled("long_prompt")
+    assert kinds.count("exact") >= 1
 
 
 def test_step_full_step_layer_sampled():
-    # The 32 layers of the full step share one launch shape; layer 0 and 31 are checked.
+    # The 32 layers of the full step share one launch shape; layers 0 and 31
+    # (independently seeded keys) are checked.
     for layer in (0, 31):
-        kinds = _step_config("full_step", units=[(0, 0), (0, 17)], layer=layer)
-        assert len(kinds) == 2
+        _step_sampled("full_step", layer=layer)
 
 
 @pytest.mark.parametrize("tag", ["1pct", "2p5pct", "5pct", "10pct"])
 def test_step_batched_long_sampled(tag):
-    kinds = _step_config(f"batched_long_{tag}", units=[(0, 5), (1, 30)])
-    assert len(kinds) == 2
+    _step_sampled(f"batched_long_{tag}")
+
+
+def _planted_inputs(seed, heads, n, g, d, levels, k_l, dtype="bf16"):
+    """Inputs whose every selection is decided by a wide margin: k_l coarse
+    spans (of the n / 2^levels) carry strong keys on half of their tokens
+    (K = 5u + noise at even offsets, u the queries' common direction), every
+    other key is small noise.  The coarse Top-k_l is then exactly the planted
+    spans and the token-level Top-B (B = k_l 2^levels / 2) exactly their
+    strong tokens, with boundary gaps far above 1e-4."""
+    rng = np.random.default_rng(seed)
+    span = 1 << levels
+    P = n // span
+    arrs = {k: np.empty((1, heads, r, d)) for k, r in
+            (("Q", g), ("Kp", n), ("Vp", n), ("Kg", g), ("Vg", g))}
+    for h in range(heads):
+        u = rng.standard_normal(d)
+        u /= np.linalg.norm(u)
+        kp = 0.2 * rng.standard_normal((n, d))
+        spans = np.sort(rng.choice(P, k_l, replace=False))
+        for p in spans:
+            kp[p * span:(p + 1) * span:2] += 5.0 * u
+        arrs["Kp"][0, h] = kp
+        arrs["Q"][0, h] = 3.0 * u + 0.3 * rng.standard_normal((g, d))
+        arrs["Vp"][0, h] = rng.standard_normal((n, d))
+        arrs["Kg"][0, h] = 0.2 * rng.standard_normal((g, d))
+        arrs["Vg"][0, h] = rng.standard_normal((g, d))
+    rnd = wl.round_to_bf16 if dtype == "bf16" else (lambda x: x.astype(np.float32))
+    return {k: rnd(v) for k, v in arrs.items()}
+
+
+@pytest.mark.parametrize("n,levels,g,k_l,gather,logits", [
+    (32768, 5, 32, 384, 0, "workspace"),   # 12288 token candidates: distributed select, spill
+    (32768, 5, 64, 128, 1, "workspace"),   # 4096 candidates gathered; 64 queries spill
+    (32768, 5, 8, 384, 0, "shared"),       # distributed select, logits on chip
+])
+def test_step_forced_plans_decisive(n, levels, g, k_l, gather, logits):
+    # The selection paths the batched-long budgets use (distributed radix
+    # select over more than 8192 token candidates, token logits spilled to
+    # the workspace), on inputs where every unit is decisive: index sets
+    # compared element by element.
+    d, heads = 128, 2
+    budget = k_l * (1 << levels) // 2
+    ks = bd.default_k_per_level(n, levels, budget)
+    assert ks[levels] == k_l
+    arrs = _planted_inputs(n + g + k_l, heads, n, g, d, levels, k_l)
+    dev = to_device(arrs, "bf16")
+    dims = bd.make_dims(dev["Q"], dev["Kp"], levels)
+    plan = bd.step_plan(dims, ks)
+    assert plan["final_gather"] == gather and plan["token_logits"] == logits, plan
+    out, lse, idx, status = run_step(dev, levels, ks)
+    assert status == 0
+    out, lse, idx = out.cpu().numpy(), lse.cpu().numpy(), idx.cpu().numpy()
+    for h in range(heads):
+        res = oracle_unit(arrs, 0, h, levels, ks)
+        assert all(lv["gap"] > 0.1 for lv in res["levels"].values()), "inputs not decisive"
+        kind = compare_step_unit(arrs, 0, h, levels, ks, idx[0, h], out[0, h], lse[0, h], res=res)
+        assert kind == "exact"
 
 
 @pytest.mark.parametrize("n,levels,g,d,h,budget", [
@@ -365,3 +449,32 @@ def test_step_host_matches_device_step():
     bd.step_host(dims, host, ks, stage, ws)
     torch.cuda.synchronize()
     assert torch.equal(host["O"], ref.cpu())
+
+
+# ----------------------------------------------- step 1 at the full shapes
+
+@pytest.mark.parametrize("name", ["long_prompt", "full_step", "batched_long_1pct"])
+def test_dwt_full_shape_sampled_units(name):
+    # wf_dwt_lowpass over a whole layer of the large workloads (the persistent
+    # stream splits gigabytes of keys over one CTA per SM, with byte offsets
+    # past 2^31 on the batched workload); the first, an interior and the last
+    # head of the last sequence carry the seeded keys and are checked against
+    # the oracle's Haar pyramid, every other unit holds device-drawn keys.
+    cfg = wl.CONFIGS[name]
+    b = cfg.batch - 1
+    heads = [0, cfg.heads // 2 + 1, cfg.heads - 1]
+    arrs = wl.generate_layer(cfg, 0, seqs=[b], heads=heads, workers=WORKERS)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(5)
+    kp = torch.randn((cfg.batch, cfg.heads, cfg.n_prompt, cfg.head_dim), generator=gen,
+                     device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    for i, h in enumerate(heads):
+        kp[b, h] = torch.from_numpy(arrs["Kp"][0, i]).to("cuda", torch.bfloat16)
+    al = bd.dwt_lowpass(kp, cfg.levels)
+    del kp
+    torch.cuda.synchronize()
+    for i, h in enumerate(heads):
+        ref = wo.haar_pyramid(arrs["Kp"][0, i], cfg.levels)[cfg.levels]
+        got = al[b, h].cpu().numpy()
+        tol = AL_RTOL * np.abs(ref) + 1e-6 * np.sqrt((ref ** 2).mean())
+        assert (np.abs(got - ref) <= tol).all(), (name, b, h)

@@ -26,7 +26,7 @@ MAX_LEVELS = 12
 
 # Every symbol the header declares (checked by the host tests).
 EXPORTS = ("wf_status_string", "wf_last_error_string", "wf_default_k_per_level", "wf_workspace_bytes",
-           "wf_step_launch_count",
+           "wf_step_launch_count", "wf_step_plan", "wf_debug_inject_wait_timeout",
            "wf_clear_device_status", "wf_read_device_status", "wf_dwt_lowpass",
            "wf_score_topk", "wf_recursive_filter", "wf_sparse_gather_attn", "wf_step",
            "wf_step_host", "wf_step_static_scratch", "wf_step_cached_al",
@@ -39,6 +39,15 @@ class WfError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
         super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}")
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("launches", ctypes.c_int32), ("cluster", ctypes.c_int32),
+                ("final_gather", ctypes.c_int32), ("token_logits", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int32)]
+
+
+LOGITS_NAMES = {0: "shared", 1: "workspace", 2: "tensor_memory", 3: "recomputed"}
 
 
 class Dims(ctypes.Structure):
@@ -62,6 +71,8 @@ _SIGS = {
     "wf_default_k_per_level": (ctypes.c_int, [_i32, _i32, _i32, _i32p]),
     "wf_workspace_bytes": (ctypes.c_int, [_DIMSP, _i32p, ctypes.POINTER(_sz)]),
     "wf_step_launch_count": (ctypes.c_int, [_DIMSP, _i32p, _i32p]),
+    "wf_step_plan": (ctypes.c_int, [_DIMSP, _i32p, ctypes.POINTER(Plan)]),
+    "wf_debug_inject_wait_timeout": (ctypes.c_int, [_i32]),
     "wf_clear_device_status": (ctypes.c_int, [_vp, _sz, _vp]),
     "wf_read_device_status": (ctypes.c_int, [_vp, _sz, _vp, _i32p]),
     "wf_dwt_lowpass": (ctypes.c_int, [_DIMSP, _vp, _vp, _vp, _vp]),
@@ -173,6 +184,21 @@ def step_launch_count(dims: Dims, k: Sequence[int]) -> int:
     _check("wf_step_launch_count", lib().wf_step_launch_count(ctypes.byref(dims), _k_array(k),
                                                               ctypes.byref(n)))
     return n.value
+
+
+def step_plan(dims: Dims, k: Sequence[int]) -> dict:
+    """wf_step's launch plan for these sizes (host only)."""
+    p = Plan()
+    _check("wf_step_plan", lib().wf_step_plan(ctypes.byref(dims), _k_array(k), ctypes.byref(p)))
+    return {"launches": p.launches, "cluster": p.cluster, "final_gather": p.final_gather,
+            "token_logits": LOGITS_NAMES.get(p.token_logits, p.token_logits),
+            "smem_bytes": p.smem_bytes}
+
+
+def inject_wait_timeout(polls: int) -> None:
+    """Arms the one-shot wait-timeout injection of the next streaming launch
+    (tests of the bounded device waits); 0 disarms."""
+    _check("wf_debug_inject_wait_timeout", lib().wf_debug_inject_wait_timeout(int(polls)))
 
 
 def alloc_workspace(dims: Dims, k: Sequence[int], device) -> torch.Tensor:

@@ -13,6 +13,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <atomic>
 
 #include "wavefilter.h"
 #include "wf_internal.h"
@@ -127,6 +128,9 @@ BasisLayout basis_layout(const LaunchDims& ld, const int32_t* k) {
 
 thread_local char g_last_error[256] = "no error";
 
+// Poll limit of the next injected wait timeout (wf_debug_inject_wait_timeout).
+std::atomic<uint32_t> g_wait_injection{0};
+
 int cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return WF_OK;
   wf::note_cuda_error(e);
@@ -136,6 +140,8 @@ int cuda_status(cudaError_t e) {
 }  // namespace
 
 namespace wf {
+uint32_t consume_wait_injection() { return g_wait_injection.exchange(0u); }
+
 void note_cuda_error(cudaError_t e) {
   std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
                 cudaGetErrorString(e));
@@ -209,6 +215,31 @@ int wf_step_launch_count(const wf_dims* dims, const int32_t* k_per_level, int32_
                      k_per_level[0], wf::device_sm_count(), &plan))
     return WF_ERR_UNSUPPORTED;
   *launches = plan.fuse_dwt ? 1 : 2;
+  return WF_OK;
+}
+
+int wf_step_plan(const wf_dims* dims, const int32_t* k_per_level, wf_plan* out) {
+  LaunchDims ld;
+  int st = check_dims(dims, &ld);
+  if (st != WF_OK) return st;
+  if (out == nullptr) return WF_ERR_NULL;
+  st = check_k(ld, k_per_level);
+  if (st != WF_OK) return st;
+  wf::PathPlan plan;
+  if (!wf::plan_path(ld, wf::kPhaseAll | wf::kPhaseFuseDwt, k_per_level, k_per_level[ld.levels],
+                     k_per_level[0], wf::device_sm_count(), &plan))
+    return WF_ERR_UNSUPPORTED;
+  out->launches = plan.fuse_dwt ? 1 : 2;
+  out->cluster = plan.cluster;
+  out->final_gather = plan.gather_all;
+  out->token_logits = plan.t_in_smem ? WF_LOGITS_SHARED : WF_LOGITS_WORKSPACE;
+  out->smem_bytes = static_cast<int32_t>(plan.smem_bytes);
+  return WF_OK;
+}
+
+int wf_debug_inject_wait_timeout(int32_t polls) {
+  if (polls < 0) return WF_ERR_SHAPE;
+  g_wait_injection.store(static_cast<uint32_t>(polls));
   return WF_OK;
 }
 

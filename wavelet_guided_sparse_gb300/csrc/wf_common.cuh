@@ -161,10 +161,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait on an mbarrier phase.  Returns false (and raises
-// WF_DEV_WAIT_TIMEOUT) if the phase did not complete within kWaitPolls polls.
+// WF_DEV_WAIT_TIMEOUT) if the phase did not complete within `polls` polls
+// (kWaitPolls unless a test injects a shorter limit).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  int32_t* status) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+                                                  int32_t* status,
+                                                  uint32_t polls = kWaitPolls) {
+  for (uint32_t i = 0; i < polls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
   }
   raise_flag(status, WF_DEV_WAIT_TIMEOUT);

@@ -105,7 +105,8 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
                                                                  int64_t n_spans,
                                                                  int64_t spans_per_cta,
                                                                  int levels, int64_t P,
-                                                                 float scale, int32_t* status) {
+                                                                 float scale, int32_t* status,
+                                                                 uint32_t inject_polls) {
   extern __shared__ __align__(128) unsigned char smem[];
   using S = DwtSmem<T, D>;
   constexpr int RB = S::kRowBytes, SR = S::kRows, V = S::V, C = S::C;
@@ -113,7 +114,6 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
   unsigned char* ring = smem + S::kRing;
   float* part = reinterpret_cast<float*>(smem + S::kPart);
   float* carry = reinterpret_cast<float*>(smem + S::kCarry);
-  __shared__ int aborted;
   const int tid = threadIdx.x;
   const int64_t s_begin = static_cast<int64_t>(blockIdx.x) * spans_per_cta;
   const int64_t s_end = min(n_spans, s_begin + spans_per_cta);
@@ -122,11 +122,13 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
   const int64_t rows_total = (s_end - s_begin) << levels;
   const int64_t n_stages = (rows_total + SR - 1) / SR;
   const unsigned char* src = reinterpret_cast<const unsigned char*>(kp + (s_begin << levels) * D);
+  // Fault injection (tests of the bounded waits): stage 0 of CTA 0 is never
+  // issued and its wait gives up after inject_polls polls.
+  const bool inject = inject_polls != 0 && blockIdx.x == 0;
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
-    aborted = 0;
   }
   __syncthreads();
   auto issue = [&](int64_t st) {  // thread 0 only
@@ -137,16 +139,19 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
     bulk_g2s(ring + (st % kStages) * kStageBytes, src + st * static_cast<int64_t>(SR) * RB, bytes,
              bar);
   };
+  // Stages issued so far (every thread keeps the same count).  After a wait
+  // gives up no further stage is issued, but every stage already issued is
+  // still waited for (bounded), so no copy is in flight when the CTA exits.
+  int64_t issued = min(static_cast<int64_t>(kStages), n_stages);
   if (tid == 0)
-    for (int64_t st = 0; st < kStages && st < n_stages; ++st) issue(st);
+    for (int64_t st = 0; st < issued; ++st)
+      if (!(inject && st == 0)) issue(st);
+  bool aborted = false;
 
-  for (int64_t st = 0; st < n_stages; ++st) {
-    int ok = 1;
-    if (aborted == 0)
-      ok = mbar_wait_bounded(&bars[st % kStages], static_cast<uint32_t>((st / kStages) & 1), status)
-               ? 1
-               : 0;
-    if (__syncthreads_or(!ok) && tid == 0) aborted = 1;
+  for (int64_t st = 0; st < issued; ++st) {
+    const bool ok = mbar_wait_bounded(&bars[st % kStages], static_cast<uint32_t>((st / kStages) & 1),
+                                      status, inject && st == 0 ? inject_polls : kWaitPolls);
+    if (__syncthreads_or(!ok)) aborted = true;
     const unsigned char* buf = ring + (st % kStages) * kStageBytes;
     const int rows_in = static_cast<int>(min(static_cast<int64_t>(SR), rows_total - st * SR));
     const int64_t first_row = st * SR;
@@ -204,9 +209,12 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
       }
     }
     __syncthreads();  // stage consumed (and carry / partials settled)
-    if (tid == 0 && st + kStages < n_stages && aborted == 0) {
-      fence_proxy_async();
-      issue(st + kStages);
+    if (st + kStages < n_stages && !aborted) {
+      if (tid == 0) {
+        fence_proxy_async();
+        issue(st + kStages);
+      }
+      ++issued;
     }
   }
 }
@@ -224,7 +232,7 @@ cudaError_t launch_typed(const void* kp, float* out, __nv_bfloat16* planes, int6
   dwt_stream_kernel<T, D><<<static_cast<unsigned>(blocks), kThreads, DwtSmem<T, D>::kTotal,
                             stream>>>(static_cast<const T*>(kp), out, planes, n_spans, per,
                                       levels, static_cast<int64_t>(n_prompt >> levels), scale,
-                                      status);
+                                      status, consume_wait_injection());
   return cudaGetLastError();
 }
 

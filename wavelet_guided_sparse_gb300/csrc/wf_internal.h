@@ -122,6 +122,11 @@ cudaError_t launch_basis_filter(const LaunchDims& ld, const BasisFilterParams& p
 // is 227 KB; a little is left for static shared memory).
 constexpr size_t kMaxSmem = 225 * 1024;
 
+// Poll limit armed by wf_debug_inject_wait_timeout for the next kernel
+// launch that streams through mbarrier-counted copies (0: none); reading it
+// disarms it.
+uint32_t consume_wait_injection();
+
 // Records the last CUDA error of this thread for wf_last_error_string().
 void note_cuda_error(cudaError_t e);
 

@@ -89,6 +89,7 @@ struct PathParams {
   int cs, per_cta_p, rows_cap, sorted_cap, keys_cap, gather_all, klist_cap, tile_keys;
   int f_stages, a_stages;  // cp.async ring depths (filter tiles, attention tiles)
   int fuse_dwt;            // score: A_L from K_p inside this kernel
+  uint32_t inject_polls;   // fault injection (tests): see the fused step 1 below
   float al_scale;          // 2^(-L/2), the orthonormal Haar low-pass gain
   int k[WF_MAX_LEVELS + 1];
   float scale[WF_MAX_LEVELS + 1];  // 2^(-j/2)/sqrt(d)
@@ -433,6 +434,9 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
              fuse_src + static_cast<int64_t>(st) * kFuseStageBytes, bytes, bar);
   };
   int fuse_issued = min(kFuseStages, fuse_nst);
+  // Fault injection (tests of the bounded waits): in the first CTA, stage 0
+  // of the ring is never issued and its wait gives up after inject_polls polls.
+  const bool inject = fuse_dwt && p.inject_polls != 0 && blockIdx.x == 0 && blockIdx.y == 0;
   if (tid == 0) {
     if (fuse_dwt)
       for (int i = 0; i < kFuseStages; ++i) mbar_init(&bars[i], 1);
@@ -440,7 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     mbar_init(span_bar, 1);
     fence_mbar_init();
     if (fuse_dwt)
-      for (int st = 0; st < fuse_issued; ++st) fuse_issue(st);
+      for (int st = 0; st < fuse_issued; ++st)
+        if (!(inject && st == 0)) fuse_issue(st);
     if (p.use_tma_spans) prefetch_tensormap(&p.tmap_spans);  // used by the filter phase
   }
   __syncwarp();
@@ -509,7 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         // so no copy is still landing when the ring is reused; a timeout
         // only stops further issues (the status word reports it).
         const bool ok = mbar_wait_bounded(&bars[st % kFuseStages],
-                                          static_cast<uint32_t>((st / kFuseStages) & 1), p.status);
+                                          static_cast<uint32_t>((st / kFuseStages) & 1), p.status,
+                                          inject && st == 0 ? p.inject_polls : kWaitPolls);
         if (__syncthreads_or(!ok)) aborted = true;
         const unsigned char* buf = smem + L.s_ring + (st % kFuseStages) * kFuseStageBytes;
         const int rows_in = min(fuse_sr, fuse_rows - st * fuse_sr);
@@ -1597,6 +1603,7 @@ cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathAr
   p.f_stages = plan.f_stages;
   p.a_stages = plan.a_stages;
   p.fuse_dwt = plan.fuse_dwt;
+  p.inject_polls = plan.fuse_dwt ? consume_wait_injection() : 0u;
   p.use_tma_spans =
       (plan.mode & kModeFilter) != 0 && encode_span_map(ld, a.kp, &p.tmap_spans) ? 1 : 0;
   p.al_scale = static_cast<float>(std::pow(2.0, -0.5 * ld.levels));  // 2^(-L/2)

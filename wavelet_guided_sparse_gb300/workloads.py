@@ -46,6 +46,7 @@ __all__ = [
     "default_k_per_level",
     "generate_unit",
     "generate_layer",
+    "generate_layer_torch",
     "round_to_bf16",
 ]
 
@@ -244,4 +245,53 @@ def generate_layer(cfg: WorkloadConfig, layer: int = 0,
         bi, hi = divmod(i, len(heads))
         for name in shapes:
             out[name][bi, hi] = unit[name]
+    return out
+
+
+def generate_layer_torch(cfg: WorkloadConfig, layer: int = 0, device="cuda",
+                         seqs: Optional[Sequence[int]] = None):
+    """The recipe of :func:`generate_unit` for every head of one layer, drawn
+    with torch's generator on ``device`` (a 32-layer workload of 65536-token
+    prompts takes seconds this way instead of tens of minutes on the host).
+
+    Same distributions, planted-span layout rules and rounding as the numpy
+    generator, but a different random stream: the values differ from
+    :func:`generate_layer`'s, so parity tests use that one and this serves
+    throughput measurements.  Returns tensors of the workload dtype (bf16 by
+    round-to-nearest-even, or fp32): Q, Kp, Vp, Kg, Vg as [b, H, rows, d].
+    """
+    import torch
+
+    seqs = list(range(cfg.batch)) if seqs is None else list(seqs)
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    d, n_p, g, H = cfg.head_dim, cfg.n_prompt, cfg.n_gen, cfg.heads
+    n = n_p + g
+    out = {k: torch.empty((len(seqs), H, rows, d), dtype=dt, device=device)
+           for k, rows in (("Q", g), ("Kp", n_p), ("Vp", n_p), ("Kg", g), ("Vg", g))}
+    for bi, s in enumerate(seqs):
+        # Host-side draws of the small per-(sequence, layer) parameters, from
+        # the numpy generator (identical to generate_unit's).
+        scale = torch.from_numpy(_channel_scale(cfg, s, layer)).to(device, torch.float32)
+        starts = span_starts(cfg, s, layer)
+        gen = torch.Generator(device=device)
+        gen.manual_seed(int(np.random.SeedSequence([cfg.seed, s, layer, 7]).generate_state(1)[0]))
+        for h in range(H):
+            u = torch.randn(d, generator=gen, device=device, dtype=torch.float32)
+            u /= u.norm()
+            walk = torch.randn((n, d), generator=gen, device=device, dtype=torch.float32)
+            walk = walk.cumsum(0)
+            walk -= walk.mean(0, keepdim=True)
+            walk /= walk.std(0, unbiased=False, keepdim=True)
+            keys = torch.randn((n, d), generator=gen, device=device, dtype=torch.float32)
+            keys.mul_(0.6).add_(walk, alpha=0.8).mul_(scale[None, :])
+            del walk
+            for st in starts:
+                keys[int(st):int(st) + cfg.span_len] += 3.0 * u
+            q = torch.randn((g, d), generator=gen, device=device, dtype=torch.float32) + 3.0 * u
+            v = torch.randn((n, d), generator=gen, device=device, dtype=torch.float32)
+            out["Q"][bi, h] = q.to(dt)
+            out["Kp"][bi, h] = keys[:n_p].to(dt)
+            out["Kg"][bi, h] = keys[n_p:].to(dt)
+            out["Vp"][bi, h] = v[:n_p].to(dt)
+            out["Vg"][bi, h] = v[n_p:].to(dt)
     return out
