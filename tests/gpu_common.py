@@ -104,7 +104,7 @@ def _band(scores, cand, k, tol):
     return must, free
 
 
-def selection_is_valid(q, kp, levels, ks, gpu_idx, tol=GAP_TOL, budget=20000):
+def selection_is_valid(q, kp, levels, ks, gpu_idx, tol=GAP_TOL, budget=20000, lowpass=None):
     """True if the final token set `gpu_idx` is what the recursive filter
     (Fig. 2(c)-(d) of the WaveFilter page, as the oracle reads it) can return
     when scores are known only to `tol` relative: at every selecting level
@@ -116,8 +116,10 @@ def selection_is_valid(q, kp, levels, ks, gpu_idx, tol=GAP_TOL, budget=20000):
     are reconstructed: they contain the ancestors of the final tokens, and the
     near-tie band's remaining slots are enumerated (depth first; `budget`
     bounds the number of candidate sets scored).  Scores are the oracle's
-    float64 attention masses over each hypothesised candidate set."""
-    pyr = wo.haar_pyramid(kp, levels)
+    float64 attention masses over each hypothesised candidate set.  `lowpass`:
+    None for the Haar pyramid, else the low-pass of a longer basis."""
+    pyr = (wo.haar_pyramid(kp, levels) if lowpass is None
+           else wo.wavelet_pyramid(kp, levels, lowpass))
     gpu = np.asarray(gpu_idx, dtype=np.int64)
     gpu_set = set(gpu.tolist())
     if len(gpu_set) != len(gpu) or len(gpu) != ks[0]:
@@ -156,7 +158,8 @@ def selection_is_valid(q, kp, levels, ks, gpu_idx, tol=GAP_TOL, budget=20000):
     return rec(levels, np.arange(pyr[levels].shape[0], dtype=np.int64))
 
 
-def compare_step_unit(arrs, b, h, levels, ks, gpu_idx, gpu_out, gpu_lse=None, res=None):
+def compare_step_unit(arrs, b, h, levels, ks, gpu_idx, gpu_out, gpu_lse=None, res=None,
+                      lowpass=None):
     """Parity of one unit of a full step.  Returns "exact" (every selecting
     level decisive: the index set equals the oracle's) or "valid" (a near-tie
     at some level: the GPU's set passes :func:`selection_is_valid`, and the
@@ -170,7 +173,7 @@ def compare_step_unit(arrs, b, h, levels, ks, gpu_idx, gpu_out, gpu_lse=None, re
         kind = "exact"
     else:
         u = unit_inputs(arrs, b, h)
-        assert selection_is_valid(u["Q"], u["Kp"], levels, ks, gpu_idx), \
+        assert selection_is_valid(u["Q"], u["Kp"], levels, ks, gpu_idx, lowpass=lowpass), \
             f"unit ({b},{h}): selection is not a valid near-tie outcome"
         ref_out, ref_lse = wo.sparse_attention(u["Q"], u["Kp"], u["Vp"], u["Kg"], u["Vg"],
                                                gpu_idx)

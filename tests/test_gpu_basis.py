@@ -70,7 +70,7 @@ def _check_step(arrs, dtype, levels, ks, moments):
             res = wo.wavefilter_step(u["Q"], u["Kp"], u["Vp"], u["Kg"], u["Vg"], levels, ks,
                                      lowpass=low)
             kinds.append(compare_step_unit(arrs, bi, hi, levels, ks, idx[bi, hi], out[bi, hi],
-                                           lse[bi, hi], res=res))
+                                           lse[bi, hi], res=res, lowpass=low))
     return kinds
 
 

@@ -112,3 +112,17 @@ def test_exact_tie_resolved_either_way_is_valid():
         assert res2["levels"][0]["gap"] <= GAP_TOL
         return
     pytest.skip("no sibling pair at the boundary in the scanned seeds")
+
+
+def test_longer_basis_selection_is_validated_on_its_own_pyramid():
+    # With a Daubechies basis the scores come from that basis's pyramid: the
+    # oracle's selection passes when the validator is given the basis, and
+    # the same set need not pass under the Haar pyramid's scores.
+    q, kp = _inputs(9, 512, 8, 32)
+    ks, levels = [40, 30, 20, 12, 8], 4
+    low = wo.daubechies_lowpass(3)
+    idx = wo.recursive_filter(q, kp, levels, ks, lowpass=low)["idx"]
+    assert selection_is_valid(q, kp, levels, ks, idx, lowpass=low)
+    haar_idx = wo.recursive_filter(q, kp, levels, ks)["idx"]
+    if not np.array_equal(idx, haar_idx):
+        assert not selection_is_valid(q, kp, levels, ks, idx)
