@@ -200,7 +200,8 @@ int wf_dwt_lowpass(const wf_dims* dims, const void* Kp, float* AL, float* A_all,
  *   k_L      : 1 ≤ k_L ≤ N_p/2^L
  *   idx_L    : device, out, [U, k_L] int32, ascending
  *   scores_L : device, out, nullable, [U, N_p/2^L] fp32 (s)
- *   workspace: device, ≥ wf_workspace_bytes() (only its status word is used)
+ *   workspace: device, ≥ wf_workspace_bytes(); receives the coarse logits
+ *              Q·A_L/√d of every position on the way to the scores
  * Errors: as wf_dwt_lowpass plus WF_ERR_WORKSPACE. */
 int wf_score_topk(const wf_dims* dims, const void* Q, const float* AL,
                   int32_t k_L, int32_t* idx_L, float* scores_L,
@@ -245,9 +246,10 @@ int wf_sparse_gather_attn(const wf_dims* dims, const void* Q, const void* Kp,
  *                 wf_recursive_filter plus 1 ≤ k_L ≤ N_p/2^L
  *   O, lse      : outputs of step 5 (lse nullable)
  *   idx_out     : device, out, nullable, [U, B] int32 — the selected tokens
- *   workspace   : device scratch of ≥ wf_workspace_bytes() bytes; holds A_L,
- *                 S_L and (for large budgets) token logits; contents are
- *                 overwritten.  Concurrent calls need separate workspaces.
+ *   workspace   : device scratch of ≥ wf_workspace_bytes() bytes; holds the
+ *                 coarse logits Q·A_L/√d, S_L and (for large budgets) token
+ *                 logits; contents are overwritten.  Concurrent calls need
+ *                 separate workspaces.
  * Errors: WF_ERR_NULL, WF_ERR_SHAPE, WF_ERR_UNSUPPORTED, WF_ERR_ALIGNMENT,
  * WF_ERR_WORKSPACE, WF_ERR_CUDA. */
 int wf_step(const wf_dims* dims, const void* Q, const void* Kp, const void* Vp,

@@ -64,17 +64,18 @@ int check_k(const LaunchDims& ld, const int32_t* k) {
   return WF_OK;
 }
 
-// Workspace layout shared by every entry point: [status header | A_L | S_L | S | t].
+// Workspace layout shared by every entry point: [status header | coarse
+// logits | S_L | S | t].
 struct Layout {
-  size_t al, idx_l, idx, t, total;
+  size_t zl, idx_l, idx, t, total;
 };
 
 Layout layout(const LaunchDims& ld, const int32_t* k, const wf::PathPlan* fp) {
   Layout L;
   size_t o = kHeaderBytes;
-  L.al = o;  // fp32 A_L, or for bf16 inputs three bf16 planes (6 bytes per element)
-  o = align_up(o + (ld.dtype == WF_BF16 ? 6 : 4) * static_cast<size_t>(ld.units) *
-                       (ld.n_prompt >> ld.levels) * ld.head_dim);
+  L.zl = o;  // coarse logits [U, P, coarse_logit_pitch(G)] fp32
+  o = align_up(o + sizeof(float) * static_cast<size_t>(ld.units) * (ld.n_prompt >> ld.levels) *
+                       wf::coarse_logit_pitch(ld.n_gen));
   L.idx_l = o;
   o = align_up(o + sizeof(int32_t) * ld.units * (k ? k[ld.levels] : 0));
   L.idx = o;
@@ -270,12 +271,12 @@ int wf_dwt_lowpass(const wf_dims* dims, const void* Kp, float* AL, float* A_all,
   if (Kp == nullptr || AL == nullptr) return WF_ERR_NULL;
   if (!aligned16(Kp) || !aligned16(AL) || (A_all && !aligned16(A_all))) return WF_ERR_ALIGNMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = wf::launch_dwt_lowpass(ld, Kp, AL, nullptr, ld.levels, nullptr, s);
+  cudaError_t e = wf::launch_dwt_lowpass(ld, Kp, AL, nullptr, nullptr, ld.levels, nullptr, s);
   if (e == cudaSuccess && A_all != nullptr) {
     // Test aid: every level j = 1..L, each from its own pass over Kp.
     size_t off = 0;
     for (int j = 1; j <= ld.levels && e == cudaSuccess; ++j) {
-      e = wf::launch_dwt_lowpass(ld, Kp, A_all + off, nullptr, j, nullptr, s);
+      e = wf::launch_dwt_lowpass(ld, Kp, A_all + off, nullptr, nullptr, j, nullptr, s);
       off += static_cast<size_t>(ld.units) * (ld.n_prompt >> j) * ld.head_dim;
     }
   }
@@ -320,18 +321,23 @@ int wf_score_topk(const wf_dims* dims, const void* Q, const float* AL, int32_t k
       (scores_L && !aligned16(scores_L)))
     return WF_ERR_ALIGNMENT;
   if (k_L < 1 || k_L > (ld.n_prompt >> ld.levels)) return WF_ERR_SHAPE;
-  if (workspace_bytes < kHeaderBytes) return WF_ERR_WORKSPACE;
+  const Layout L = layout(ld, nullptr, nullptr);
+  if (workspace_bytes < L.total) return WF_ERR_WORKSPACE;
   wf::PathPlan plan;
   if (!wf::plan_path(ld, wf::kPhaseScore, nullptr, k_L, 0, wf::device_sm_count(), &plan))
     return WF_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* zl = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.zl);
+  const cudaError_t e = wf::launch_coarse_logits(ld, AL, Q, zl, s);
+  if (e != cudaSuccess) return cuda_status(e);
   wf::PathArgs a = {};
   a.q = Q;
-  a.al = AL;
+  a.zl = zl;
   a.idx_l_out = idx_L;
   a.scores_out = scores_L;
   a.status = status_word(workspace);
   a.k_l = k_L;
-  return cuda_status(wf::launch_path(ld, plan, a, static_cast<cudaStream_t>(stream)));
+  return cuda_status(wf::launch_path(ld, plan, a, s));
 }
 
 int wf_recursive_filter(const wf_dims* dims, const void* Q, const void* Kp, const int32_t* idx_L,
@@ -423,15 +429,14 @@ int wf_step(const wf_dims* dims, const void* Q, const void* Kp, const void* Vp, 
   const Layout L = layout(ld, k_per_level, &plan);
   if (workspace_bytes < L.total) return WF_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
-  float* al = reinterpret_cast<float*>(ws + L.al);
+  float* zl = reinterpret_cast<float*>(ws + L.zl);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // Step 1 runs inside the path kernel when the plan fuses it; otherwise a
-  // separate streaming launch writes A_L (bf16 inputs: straight to the three
-  // bf16 planes the score phase multiplies on tensor cores).
-  __nv_bfloat16* planes = ld.dtype == WF_BF16 ? reinterpret_cast<__nv_bfloat16*>(al) : nullptr;
+  // separate streaming launch sums the spans and writes each coarse
+  // position's logits against the queries (A_L itself stays on chip).
   if (!plan.fuse_dwt) {
     const cudaError_t e =
-        wf::launch_dwt_lowpass(ld, Kp, al, planes, ld.levels, status_word(workspace), s);
+        wf::launch_dwt_lowpass(ld, Kp, nullptr, Q, zl, ld.levels, status_word(workspace), s);
     if (e != cudaSuccess) return cuda_status(e);
   }
   wf::PathArgs a = {};
@@ -440,8 +445,7 @@ int wf_step(const wf_dims* dims, const void* Q, const void* Kp, const void* Vp, 
   a.vp = Vp;
   a.kg = Kg;
   a.vg = Vg;
-  a.al = planes != nullptr ? nullptr : al;
-  a.al_planes = planes;
+  a.zl = plan.fuse_dwt ? nullptr : zl;
   a.idx_out = idx_out;
   a.o = O;
   a.lse = lse;
@@ -477,13 +481,18 @@ int wf_step_cached_al(const wf_dims* dims, const void* Q, const void* Kp, const 
   const Layout L = layout(ld, k_per_level, &plan);
   if (workspace_bytes < L.total) return WF_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
+  float* zl = reinterpret_cast<float*>(ws + L.zl);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The cached A_L's coarse logits against this step's queries, then steps 2-5.
+  const cudaError_t e = wf::launch_coarse_logits(ld, AL, Q, zl, s);
+  if (e != cudaSuccess) return cuda_status(e);
   wf::PathArgs a = {};
   a.q = Q;
   a.kp = Kp;
   a.vp = Vp;
   a.kg = Kg;
   a.vg = Vg;
-  a.al = AL;  // the score phase stages the cached fp32 rows (bf16: split on chip)
+  a.zl = zl;
   a.idx_out = idx_out;
   a.o = O;
   a.lse = lse;
@@ -492,7 +501,7 @@ int wf_step_cached_al(const wf_dims* dims, const void* Q, const void* Kp, const 
   a.k = k_per_level;
   a.k_l = k_per_level[ld.levels];
   a.budget = budget;
-  return cuda_status(wf::launch_path(ld, plan, a, static_cast<cudaStream_t>(stream)));
+  return cuda_status(wf::launch_path(ld, plan, a, s));
 }
 
 int wf_decode_step_host(const wf_dims* dims, const void* h_Q, const void* h_K, const void* h_V,

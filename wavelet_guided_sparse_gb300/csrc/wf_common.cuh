@@ -590,6 +590,75 @@ static __device__ __noinline__ void block_select_topk(const uint32_t* keys, int 
   __syncthreads();
 }
 
+// ------------------------------------------------------------------ coarse logits
+//
+// z[q] = zscale * Σ_c a[c] * Q[q][c] for one row a of the level-L
+// approximation, computed by the C consecutive lanes that hold its channels
+// (lane l of the group: channels l*V .. l*V+V-1, fp32) against every query of
+// the row's unit.  Each lane forms its channels' partial dot product with all
+// queries, then a reduce-scatter over the group (log2 C shuffle rounds, each
+// halving the values a lane keeps) leaves lane l the totals of queries
+// l*GP/C .. (l+1)*GP/C - 1.  Warp-collective: every lane of the warp calls it
+// (groups are C-aligned within the warp); `active` lanes store their queries
+// (those below G) to out[q].  GP >= G is a multiple of C.
+
+template <int N, int O>
+struct ReduceScatter {
+  static __device__ __forceinline__ void run(float* v, int lane) {
+    const bool up = (lane & O) != 0;
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      const float send = up ? v[i] : v[i + N / 2];
+      const float keep = up ? v[i + N / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+    }
+    ReduceScatter<N / 2, O / 2>::run(v, lane);
+  }
+};
+template <int N>
+struct ReduceScatter<N, 0> {
+  static __device__ __forceinline__ void run(float*, int) {}
+};
+
+template <typename T, int V, int C, int GP>
+__device__ __forceinline__ void emit_coarse_logits(const float* a, bool active, const T* q_unit,
+                                                   int D, int G, float zscale, float* out) {
+  static_assert(GP % C == 0 && (C & (C - 1)) == 0 && C <= 32, "lane group layout");
+  static_assert(V == Elem<T>::kPer16B, "a lane holds one 16-byte chunk of each query row");
+  const int lane = threadIdx.x & 31, g = lane & (C - 1);
+  float v[GP];
+#pragma unroll
+  for (int q = 0; q < GP; ++q) {
+    float s = 0.f;
+    if (active && q < G) {
+      float f[V];
+      widen16(ldg16(q_unit + static_cast<int64_t>(q) * D + g * V), static_cast<const T*>(nullptr), f);
+#pragma unroll
+      for (int e = 0; e < V; ++e) s = fmaf(a[e], f[e], s);
+    }
+    v[q] = s;
+  }
+  ReduceScatter<GP, C / 2>::run(v, lane);
+  constexpr int W = GP / C;  // queries per lane after the reduce-scatter
+  if (!active) return;
+  const int q0 = g * W;
+  if (q0 + W <= G) {
+    if constexpr (W == 4) {
+      *reinterpret_cast<float4*>(out + q0) =
+          make_float4(v[0] * zscale, v[1] * zscale, v[2] * zscale, v[3] * zscale);
+    } else if constexpr (W == 2) {
+      *reinterpret_cast<float2*>(out + q0) = make_float2(v[0] * zscale, v[1] * zscale);
+    } else {
+#pragma unroll
+      for (int i = 0; i < W; ++i) out[q0 + i] = v[i] * zscale;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < W; ++i)
+      if (q0 + i < G) out[q0 + i] = v[i] * zscale;
+  }
+}
+
 // Exclusive prefix over the cluster of one int per CTA (pushed to every
 // peer).  Returns the sum over lower ranks; *total gets the cluster sum.
 // cnt_in: [kMaxCluster] ints.  Contains one cluster barrier.

@@ -11,12 +11,13 @@
 // contiguous byte range through a ring of three 64 KB shared-memory stages
 // filled by single bulk copies (TMA engine, mbarrier completion), so 128-192
 // KB per SM are in flight independent of register pressure.  Threads reduce
-// the staged rows in fp32 (and, for a two-launch wf_step with bf16 inputs,
-// emit A_L as the three bf16 planes its tensor-core scoring consumes): for
-// spans of up to 16 rows one thread owns one (span, 16-byte column chunk)
-// pair; longer spans are summed in 16-row blocks
+// the staged rows in fp32: for spans of up to 16 rows one thread owns one
+// (span, 16-byte column chunk) pair; longer spans are summed in 16-row blocks
 // whose partials are combined in a fixed order, with a running sum carried
-// across stages for spans longer than a stage.
+// across stages for spans longer than a stage.  Each finished row is either
+// stored (wf_dwt_lowpass: fp32 A_L) or — for the step — turned at once into
+// the row's coarse logits Q·A_L/√d against its unit's queries (the first
+// quantity step 2 scores), so A_L itself never reaches global memory there.
 #include <algorithm>
 #include <cmath>
 
@@ -52,56 +53,39 @@ __device__ __forceinline__ void add_chunk(const unsigned char* p, float* acc) {
   for (int i = 0; i < Elem<T>::kPer16B; ++i) acc[i] += f[i];
 }
 
-// Output of V channels of one A_L row: fp32 (`out`), or — when `planes` is
-// set — three bf16 planes hi + mid + lo whose sum reproduces the fp32 value
-// to 2^-25 relative, laid out [unit][plane][P][D] for tensor-core scoring.
-template <int V>
-__device__ __forceinline__ void store_al(const float* acc, float scale, float* out,
-                                         __nv_bfloat16* planes, int64_t span, int64_t P,
-                                         int D, int col) {
-  if (planes == nullptr) {
-    float4* o = reinterpret_cast<float4*>(out + span * D + col);
+// Output of one finished A_L row's V channels (lane layout: C consecutive
+// lanes per row): the fp32 values (`out`, [U, P, D]) or, when `zl` is set,
+// the row's coarse logits zl[(unit P + p) GZ + q] = zscale Q[unit][q]·A_L[p]
+// for the G queries of its unit (warp-collective: every lane calls it).
+template <typename T, int D, int V, int C>
+__device__ __forceinline__ void finish_row(const float* acc, bool active, float scale,
+                                           int64_t span, int c, float* out, const T* q,
+                                           float* zl, int G, int GZ, int64_t P, float zscale) {
+  float a[V];
 #pragma unroll
-    for (int v = 0; v < V; v += 4)
-      o[v / 4] = make_float4(acc[v] * scale, acc[v + 1] * scale, acc[v + 2] * scale,
-                             acc[v + 3] * scale);
+  for (int v = 0; v < V; ++v) a[v] = acc[v] * scale;
+  if (zl != nullptr) {
+    const int64_t unit = active ? span / P : 0;
+    const T* q_unit = q + unit * G * D;
+    float* dst = zl + (active ? span : 0) * GZ;
+    if (G <= 32)
+      emit_coarse_logits<T, V, C, (C > 32 ? C : 32)>(a, active, q_unit, D, G, zscale, dst);
+    else
+      emit_coarse_logits<T, V, C, 64>(a, active, q_unit, D, G, zscale, dst);
     return;
   }
-  const int64_t unit = span / P, row = span % P;
-  uint32_t w[3][V / 2];
+  if (!active) return;
+  float4* o = reinterpret_cast<float4*>(out + span * D + c * V);
 #pragma unroll
-  for (int v = 0; v < V; v += 2) {
-    float hv[2], mv[2], lv[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const float a = acc[v + e] * scale;
-      hv[e] = __bfloat162float(__float2bfloat16_rn(a));
-      const float r1 = a - hv[e];
-      mv[e] = __bfloat162float(__float2bfloat16_rn(r1));
-      lv[e] = r1 - mv[e];
-    }
-    const __nv_bfloat162 h2 = __floats2bfloat162_rn(hv[0], hv[1]);
-    const __nv_bfloat162 m2 = __floats2bfloat162_rn(mv[0], mv[1]);
-    const __nv_bfloat162 l2 = __floats2bfloat162_rn(lv[0], lv[1]);
-    w[0][v / 2] = *reinterpret_cast<const uint32_t*>(&h2);
-    w[1][v / 2] = *reinterpret_cast<const uint32_t*>(&m2);
-    w[2][v / 2] = *reinterpret_cast<const uint32_t*>(&l2);
-  }
-#pragma unroll
-  for (int pl = 0; pl < 3; ++pl) {
-    __nv_bfloat16* dst = planes + ((unit * 3 + pl) * P + row) * D + col;
-    if constexpr (V == 8) {
-      *reinterpret_cast<uint4*>(dst) = make_uint4(w[pl][0], w[pl][1], w[pl][2], w[pl][3]);
-    } else {
-      *reinterpret_cast<uint2*>(dst) = make_uint2(w[pl][0], w[pl][1]);
-    }
-  }
+  for (int v = 0; v < V; v += 4) o[v / 4] = make_float4(a[v], a[v + 1], a[v + 2], a[v + 3]);
 }
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __restrict__ kp,
                                                                  float* __restrict__ out,
-                                                                 __nv_bfloat16* __restrict__ planes,
+                                                                 const T* __restrict__ q,
+                                                                 float* __restrict__ zl, int G,
+                                                                 int GZ, float zscale,
                                                                  int64_t n_spans,
                                                                  int64_t spans_per_cta,
                                                                  int levels, int64_t P,
@@ -157,18 +141,24 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
     const int64_t first_row = st * SR;
     if (span_rows <= 16) {
       // One thread per (span, chunk) of this stage; a stage holds whole spans.
+      // Whole warps iterate together (the coarse logits are warp-collective).
       const int spans_in = rows_in >> levels;
       const int64_t span0 = first_row >> levels;
-      for (int item = tid; item < spans_in * C; item += kThreads) {
+      for (int base = 0; base < spans_in * C; base += kThreads) {
+        const int item = base + tid;
+        const bool act = item < spans_in * C;
         const int sl = item / C, c = item % C;
         float acc[V];
 #pragma unroll
         for (int v = 0; v < V; ++v) acc[v] = 0.f;
-        const unsigned char* p = buf + (sl << levels) * RB + c * 16;
+        if (act) {
+          const unsigned char* p = buf + (sl << levels) * RB + c * 16;
 #pragma unroll
-        for (int r = 0; r < 16; ++r)
-          if (r < span_rows) add_chunk<T>(p + r * RB, acc);
-        store_al<V>(acc, scale, out, planes, s_begin + span0 + sl, P, D, c * V);
+          for (int r = 0; r < 16; ++r)
+            if (r < span_rows) add_chunk<T>(p + r * RB, acc);
+        }
+        finish_row<T, D, V, C>(acc, act, scale, s_begin + span0 + sl, c, out, q, zl, G, GZ, P,
+                               zscale);
       }
     } else {
       // 16-row block partials, then per-span combination in block order.
@@ -188,24 +178,31 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
       const int64_t sp0 = first_row >> levels;
       const int64_t sp1 = (first_row + rows_in - 1) >> levels;
       const int nsp = static_cast<int>(sp1 - sp0 + 1);
-      for (int item = tid; item < nsp * C; item += kThreads) {
+      for (int base = 0; base < nsp * C; base += kThreads) {  // whole warps together
+        const int item = base + tid;
+        const bool in = item < nsp * C;
         const int sl = item / C, c = item % C;
         const int64_t span = sp0 + sl;
-        const int64_t r_lo = max(span << levels, first_row);
-        const int64_t r_hi = min((span + 1) << levels, first_row + rows_in);
-        const bool carried = (span << levels) < first_row;
         float acc[V];
 #pragma unroll
-        for (int v = 0; v < V; ++v) acc[v] = carried ? carry[c * V + v] : 0.f;
-        for (int b = static_cast<int>((r_lo - first_row) / 16); b < (r_hi - first_row) / 16; ++b)
+        for (int v = 0; v < V; ++v) acc[v] = 0.f;
+        bool done = false;
+        if (in) {
+          const int64_t r_lo = max(span << levels, first_row);
+          const int64_t r_hi = min((span + 1) << levels, first_row + rows_in);
+          const bool carried = (span << levels) < first_row;
 #pragma unroll
-          for (int v = 0; v < V; ++v) acc[v] += part[(b * C + c) * V + v];
-        if (((span + 1) << levels) <= first_row + rows_in) {
-          store_al<V>(acc, scale, out, planes, s_begin + span, P, D, c * V);
-        } else {
+          for (int v = 0; v < V; ++v) acc[v] = carried ? carry[c * V + v] : 0.f;
+          for (int b = static_cast<int>((r_lo - first_row) / 16); b < (r_hi - first_row) / 16; ++b)
 #pragma unroll
-          for (int v = 0; v < V; ++v) carry[c * V + v] = acc[v];
+            for (int v = 0; v < V; ++v) acc[v] += part[(b * C + c) * V + v];
+          done = ((span + 1) << levels) <= first_row + rows_in;
+          if (!done) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) carry[c * V + v] = acc[v];
+          }
         }
+        finish_row<T, D, V, C>(acc, done, scale, s_begin + span, c, out, q, zl, G, GZ, P, zscale);
       }
     }
     __syncthreads();  // stage consumed (and carry / partials settled)
@@ -220,38 +217,90 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
 }
 
 template <typename T, int D>
-cudaError_t launch_typed(const void* kp, float* out, __nv_bfloat16* planes, int64_t units,
-                         int n_prompt, int levels, int32_t* status, cudaStream_t stream) {
+cudaError_t launch_typed(const LaunchDims& ld, const void* kp, float* out, const void* q,
+                         float* zl, int levels, int32_t* status, cudaStream_t stream) {
   const cudaError_t e = ensure_max_smem<dwt_stream_kernel<T, D>>();
   if (e != cudaSuccess) return e;
-  const int64_t n_spans = units * (n_prompt >> levels);
+  const int64_t n_spans = ld.units * (ld.n_prompt >> levels);
   const int64_t grid = std::min<int64_t>(device_sm_count(), n_spans);
   const int64_t per = (n_spans + grid - 1) / grid;
   const int64_t blocks = (n_spans + per - 1) / per;
   const float scale = static_cast<float>(std::pow(2.0, -0.5 * levels));  // 2^(-L/2)
+  const float zscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
   dwt_stream_kernel<T, D><<<static_cast<unsigned>(blocks), kThreads, DwtSmem<T, D>::kTotal,
-                            stream>>>(static_cast<const T*>(kp), out, planes, n_spans, per,
-                                      levels, static_cast<int64_t>(n_prompt >> levels), scale,
+                            stream>>>(static_cast<const T*>(kp), out, static_cast<const T*>(q), zl,
+                                      ld.n_gen, coarse_logit_pitch(ld.n_gen), zscale, n_spans, per,
+                                      levels, static_cast<int64_t>(ld.n_prompt >> levels), scale,
                                       status, consume_wait_injection());
+  return cudaGetLastError();
+}
+
+// Coarse logits from an fp32 A_L [U, P, D] kept from an earlier step: the
+// rows' C-lane groups load their channels and form the logits exactly as the
+// stream does for the rows it sums.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) coarse_logits_kernel(const float* __restrict__ al,
+                                                                 const T* __restrict__ q,
+                                                                 float* __restrict__ zl,
+                                                                 int64_t rows_total, int64_t P,
+                                                                 int G, int GZ, float zscale) {
+  constexpr int V = Elem<T>::kPer16B, C = D / V, RPP = kThreads / C;  // rows per pass
+  const int tid = threadIdx.x, c = tid % C;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPP; base < rows_total;
+       base += static_cast<int64_t>(gridDim.x) * RPP) {  // uniform over the block
+    const int64_t row = base + tid / C;
+    const bool act = row < rows_total;
+    float a[V];
+#pragma unroll
+    for (int v = 0; v < V; v += 4) {
+      const float4 x = act ? __ldg(reinterpret_cast<const float4*>(al + row * D + c * V + v))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      a[v] = x.x; a[v + 1] = x.y; a[v + 2] = x.z; a[v + 3] = x.w;
+    }
+    const int64_t unit = act ? row / P : 0;
+    float* dst = zl + (act ? row : 0) * GZ;
+    if (G <= 32)
+      emit_coarse_logits<T, V, C, 32>(a, act, q + unit * G * D, D, G, zscale, dst);
+    else
+      emit_coarse_logits<T, V, C, 64>(a, act, q + unit * G * D, D, G, zscale, dst);
+  }
+}
+
+template <typename T, int D>
+cudaError_t launch_logits_typed(const LaunchDims& ld, const float* al, const void* q, float* zl,
+                                cudaStream_t stream) {
+  constexpr int RPP = kThreads / (D / Elem<T>::kPer16B);
+  const int64_t P = ld.n_prompt >> ld.levels;
+  const int64_t rows = ld.units * P;
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((rows + RPP - 1) / RPP,
+                                                              8 * static_cast<int64_t>(device_sm_count())));
+  const float zscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+  coarse_logits_kernel<T, D><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
+      al, static_cast<const T*>(q), zl, rows, P, ld.n_gen, coarse_logit_pitch(ld.n_gen), zscale);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_dwt_lowpass(const LaunchDims& ld, const void* kp, float* out,
-                               __nv_bfloat16* planes, int levels, int32_t* status,
-                               cudaStream_t stream) {
+cudaError_t launch_coarse_logits(const LaunchDims& ld, const float* al, const void* q, float* zl,
+                                 cudaStream_t stream) {
+  if (ld.dtype == WF_BF16) {
+    if (ld.head_dim == 128) return launch_logits_typed<__nv_bfloat16, 128>(ld, al, q, zl, stream);
+    return launch_logits_typed<__nv_bfloat16, 64>(ld, al, q, zl, stream);
+  }
+  if (ld.head_dim == 128) return launch_logits_typed<float, 128>(ld, al, q, zl, stream);
+  return launch_logits_typed<float, 64>(ld, al, q, zl, stream);
+}
+
+cudaError_t launch_dwt_lowpass(const LaunchDims& ld, const void* kp, float* out, const void* q,
+                               float* zl, int levels, int32_t* status, cudaStream_t stream) {
   if (ld.dtype == WF_BF16) {
     if (ld.head_dim == 128)
-      return launch_typed<__nv_bfloat16, 128>(kp, out, planes, ld.units, ld.n_prompt, levels,
-                                              status, stream);
-    return launch_typed<__nv_bfloat16, 64>(kp, out, planes, ld.units, ld.n_prompt, levels,
-                                           status, stream);
+      return launch_typed<__nv_bfloat16, 128>(ld, kp, out, q, zl, levels, status, stream);
+    return launch_typed<__nv_bfloat16, 64>(ld, kp, out, q, zl, levels, status, stream);
   }
-  if (ld.head_dim == 128)
-    return launch_typed<float, 128>(kp, out, planes, ld.units, ld.n_prompt, levels, status,
-                                    stream);
-  return launch_typed<float, 64>(kp, out, planes, ld.units, ld.n_prompt, levels, status, stream);
+  if (ld.head_dim == 128) return launch_typed<float, 128>(ld, kp, out, q, zl, levels, status, stream);
+  return launch_typed<float, 64>(ld, kp, out, q, zl, levels, status, stream);
 }
 
 }  // namespace wf

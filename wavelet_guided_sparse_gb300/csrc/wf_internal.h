@@ -51,11 +51,15 @@ struct PathPlan {
   size_t t_bytes;    // workspace bytes for token logits (0 if in shared memory)
 };
 
+// Row pitch (floats) of the coarse logits [U, P, pitch]: G rounded up to a
+// multiple of four, so that every row starts on a 16-byte boundary.
+inline int coarse_logit_pitch(int G) { return (G + 3) & ~3; }
+
 // Pointers of one path launch (device memory unless noted).
 struct PathArgs {
   const void *q, *kp, *vp, *kg, *vg;
-  const float* al;
-  const __nv_bfloat16* al_planes;  // A_L as three bf16 planes (bf16 step), else null
+  const float* zl;   // score phase without the fused stream: coarse logits
+                     // [U, P, coarse_logit_pitch(G)], log2 domain (Q·A_L·log2e/√d)
   const int32_t* idx_l_in;
   const int32_t* idx_in;
   int32_t* idx_l_out;
@@ -74,11 +78,15 @@ int device_sm_count();
 bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int budget,
                int sm_count, PathPlan* plan);
 
-// Writes A_L as fp32 to `out`, or (planes != nullptr) as three bf16 planes
-// [unit][3][P][D] whose sum reproduces the fp32 values.
-cudaError_t launch_dwt_lowpass(const LaunchDims& ld, const void* kp, float* out,
-                               __nv_bfloat16* planes, int levels, int32_t* status,
-                               cudaStream_t stream);
+// Streams Kp once and writes its level-`levels` Haar approximation as fp32
+// to `out` [U, N_p/2^levels, d], or (zl != nullptr; levels = ld.levels) the
+// coarse logits of every row against the unit's queries `q` to zl
+// [U, P, coarse_logit_pitch(G)] in the log2 domain.
+cudaError_t launch_dwt_lowpass(const LaunchDims& ld, const void* kp, float* out, const void* q,
+                               float* zl, int levels, int32_t* status, cudaStream_t stream);
+// Coarse logits from an fp32 A_L [U, P, d] (computed at an earlier step).
+cudaError_t launch_coarse_logits(const LaunchDims& ld, const float* al, const void* q, float* zl,
+                                 cudaStream_t stream);
 cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathArgs& args,
                         cudaStream_t stream);
 

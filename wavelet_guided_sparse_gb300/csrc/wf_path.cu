@@ -24,9 +24,11 @@
 //  step 1 — (fused plans) each CTA streams the spans of its P/cs coarse
 //           positions through a ring of bulk copies and writes A_L straight
 //           into shared memory as hi/mid/lo bf16 planes.
-//  score  — z = Q·A_L^T per CTA slice: bf16 on the fifth-generation tensor
-//           cores (tcgen05.mma, accumulators in tensor memory, the three
-//           planes reproduce fp32 A_L), fp32 by FMAs; per-query (max, sum)
+//  score  — z = Q·A_L^T per CTA slice: with the fused stream, bf16 on the
+//           fifth-generation tensor cores (tcgen05.mma, accumulators in
+//           tensor memory, three bf16 planes reproduce fp32 A_L), fp32 by
+//           FMAs; otherwise read from the coarse logits the streaming launch
+//           (or the cached-A_L logits kernel) wrote; per-query (max, sum)
 //           merged over the cluster; every CTA selects the coarse Top-K.
 //  filter — by linearity Q·A_j[c] = 2^(-j/2) Σ_{n∈span(c)} Q·Kp[n]: token
 //           logits t = Kp[rows]·Q^T are computed once (tcgen05, exact bf16
@@ -54,7 +56,8 @@ namespace wf {
 namespace {
 
 constexpr int kTileRows = 64;    // filter: token rows per staged tile
-constexpr int kScoreChunk = 64;  // score: coarse positions per staged chunk
+constexpr int kScoreChunk = 64;  // score: coarse positions per staged chunk (fused step 1)
+constexpr int kZRows = 256;      // score: coarse-logit rows per staged chunk (from global)
 static_assert(kScoreChunk == 8 * kWarps, "score pass 1 takes eight rows per warp per chunk");
 constexpr int kFuseStages = 3;               // fused step 1: bulk-copy ring depth
 constexpr int kFuseStageBytes = 32 * 1024;   // fused step 1: bytes per ring stage
@@ -73,8 +76,7 @@ struct PathParams {
   const void* vp;
   const void* kg;
   const void* vg;
-  const float* al;           // score: A_L [U, P, d] fp32 (null when al_planes is set)
-  const __nv_bfloat16* al_planes;  // score, bf16: A_L as hi/mid/lo planes [U, 3, P, d]
+  const float* zl;           // score without the fused stream: coarse logits [U, P, GZ]
   const int32_t* idx_l_in;   // filter without score: S_L [U, k_L]
   const int32_t* idx_in;     // attend without filter: S [U, B]
   int32_t* idx_l_out;        // score without filter: S_L out [U, k_L]
@@ -85,7 +87,7 @@ struct PathParams {
   int32_t* status;
   float* t_ws;               // token logits in global memory (nullptr: shared)
   int mode;
-  int n_prompt, G, levels, P, kL, budget, n_keys;
+  int n_prompt, G, GZ, levels, P, kL, budget, n_keys;
   int cs, per_cta_p, rows_cap, sorted_cap, keys_cap, gather_all, klist_cap, tile_keys;
   int f_stages, a_stages;  // cp.async ring depths (filter tiles, attention tiles)
   int fuse_dwt;            // score: A_L from K_p inside this kernel
@@ -146,18 +148,11 @@ struct PathSmem {
       s_stage = s_z = s_ring;
       end = end > o ? end : o;
     } else if (p.mode & kModeScore) {
+      // Coarse logits of up to kZRows positions, padded rows of GZ + 4 floats.
       o = u;
-      // A_L chunk: fp32 rows staged by cp.async, then (bf16 inputs) split into
-      // three bf16 planes; fp32 inputs use the staged rows directly.
-      // bf16: the logits overwrite the staged fp32 rows once the planes exist.
-      s_stage = take_bytes(sizeof(float) * kScoreChunk * kRowF);
-      if (sizeof(T) == 2) {
-        s_as = take_bytes(3 * kScoreChunk * kRowBytes, 1024);
-        s_z = s_stage;
-      } else {
-        s_as = s_stage;
-        s_z = take_bytes(sizeof(float) * static_cast<size_t>(kScoreChunk) * (p.G | 1));
-      }
+      s_z = take_bytes(sizeof(float) * static_cast<size_t>(p.per_cta_p < kZRows ? p.per_cta_p : kZRows) *
+                       (p.GZ + 4));
+      s_stage = s_as = s_z;
       end = end > o ? end : o;
     }
     if (p.mode & kModeFilter) {
@@ -487,19 +482,14 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     // selects locally (so every CTA knows the sorted coarse survivors).
     const int Pc = p.per_cta_p;
     unsigned char* as = smem + L.s_as;
-    float* zc = reinterpret_cast<float*>(smem + L.s_z);  // [chunk row][query], log2 domain
+    float* zc = reinterpret_cast<float*>(smem + L.s_z);  // [position][query], log2 domain
     const float zscale = p.inv_sqrt_d * kLog2e;
-    const float* asrc =
-        p.al == nullptr ? nullptr : p.al + (unit * p.P + static_cast<int64_t>(rank) * Pc) * D;
-    const int nchunks = (Pc + kScoreChunk - 1) / kScoreChunk;
-    // z for chunk rows [c0, c0 + rows): stage A_L (bf16 inputs: exact
-    // hi + mid + lo bf16 planes), then one tensor-core / FMA tile.
-    float* stage_f = reinterpret_cast<float*>(smem + L.s_stage);  // [64][D + 4] fp32
-    const __nv_bfloat16* psrc =
-        p.al_planes == nullptr
-            ? nullptr
-            : p.al_planes + (static_cast<int64_t>(unit) * 3 * p.P + static_cast<int64_t>(rank) * Pc) * D;
-    bool z_ready = false;  // fused step 1 leaves the single chunk's logits in zc
+    // Row pitch of zc: the fused stream's logits tile (odd pitch), or padded
+    // rows of the coarse logits read from global memory (16-byte aligned).
+    const int ZP = fuse_dwt ? TS : p.GZ + 4;
+    const int zrows = fuse_dwt ? Pc : min(Pc, kZRows);  // positions resident at a time
+    const int nz = (Pc + zrows - 1) / zrows;
+    const float* zsrc = fuse_dwt ? nullptr : p.zl + (unit * p.P + static_cast<int64_t>(rank) * Pc) * p.GZ;
     if (fuse_dwt) {
       // Step 1: A_L[c] = 2^(-L/2) * (sum of the 2^L rows of span c), fp32,
       // written straight into the tile operand layout.  Two threads per
@@ -591,84 +581,42 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         logits_tile_f32<D>(as, reinterpret_cast<const float*>(qs), zc, 0, Pc, G, TS, zscale);
       }
       __syncthreads();
-      z_ready = true;
     }
-    auto chunk_logits = [&](int c0, int rows) {
-      if (z_ready) return;
-      __syncthreads();
-      if (sizeof(T) == 2 && psrc != nullptr) {
-        // A_L already split into hi / mid / lo bf16 planes: stage them directly.
-        constexpr int C8 = D / 8;
-        for (int e = tid; e < 3 * rows * C8; e += kThreads) {
-          const int pl = e / (rows * C8), rem = e - pl * rows * C8;
-          const int r = rem / C8, ch = rem % C8;
-          cp_async16(as + pl * kPlaneBytes + sw_offset(r, ch, kScoreChunk),
-                     psrc + (static_cast<int64_t>(pl) * p.P + c0 + r) * D + ch * 8);
-        }
-        cp_async_commit();
-        cp_async_wait<0>();
-        umma_logits<D>(as, 3, kPlaneBytes, kScoreChunk, rows, qs, G, zc, 0, TS, zscale, tmem, mma_bar,
-                       mma_phase, p.status);
-        __syncthreads();
-        return;
-      }
-      for (int e = tid; e < rows * (D / 4); e += kThreads) {
-        const int r = e / (D / 4), col = (e % (D / 4)) * 4;
-        cp_async16(stage_f + r * RF + col, asrc + static_cast<int64_t>(c0 + r) * D + col);
+    // Coarse logits of positions [c0, c0 + rows) from global memory into zc.
+    auto load_z = [&](int c0, int rows) {
+      __syncthreads();  // earlier readers of zc are done
+      const int c4 = p.GZ >> 2;
+      for (int e = tid; e < rows * c4; e += kThreads) {
+        const int r = e / c4, k = e - r * c4;
+        cp_async16(zc + r * ZP + 4 * k, zsrc + static_cast<int64_t>(c0 + r) * p.GZ + 4 * k);
       }
       cp_async_commit();
       cp_async_wait<0>();
       __syncthreads();
-      if constexpr (sizeof(T) == 2) {
-        for (int e = tid; e < rows * (D / 4); e += kThreads) {
-          const int r = e / (D / 4), col = (e % (D / 4)) * 4;
-          const float4 a = *reinterpret_cast<const float4*>(stage_f + r * RF + col);
-          const float av[4] = {a.x, a.y, a.z, a.w};
-          float pv[3][4];
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {  // av = hi + mid + lo exactly (to 2^-25 relative)
-            const float hi = __bfloat162float(__float2bfloat16_rn(av[v]));
-            const float r1 = av[v] - hi;
-            const float mid = __bfloat162float(__float2bfloat16_rn(r1));
-            pv[0][v] = hi;
-            pv[1][v] = mid;
-            pv[2][v] = r1 - mid;
-          }
-#pragma unroll
-          for (int pl = 0; pl < 3; ++pl)
-            *reinterpret_cast<uint2*>(as + pl * kPlaneBytes + sw_offset(r, col / 8, kScoreChunk) +
-                                      (col % 8) * 2) =
-                make_uint2(pack_bf16(pv[pl][0], pv[pl][1]), pack_bf16(pv[pl][2], pv[pl][3]));
-        }
-        umma_logits<D>(as, 3, kPlaneBytes, kScoreChunk, rows, qs, G, zc, 0, TS, zscale, tmem, mma_bar,
-                       mma_phase, p.status);
-      } else {
-        logits_tile_f32<D>(as, reinterpret_cast<const float*>(qs), zc, 0, rows, G, TS, zscale);
-      }
-      __syncthreads();
     };
     // Pass 1: per-query (max, sum) over this CTA's positions; thread ->
-    // queries lane / lane + 32, positions warp + 8i of every chunk.
+    // queries lane / lane + 32, positions warp + 8u of every 64-row block.
     float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
-    for (int ch = 0; ch < nchunks; ++ch) {
-      const int c0 = ch * kScoreChunk, rows = min(kScoreChunk, Pc - c0);
-      chunk_logits(c0, rows);
-      // Rows warp + 8u of the chunk, eight at a time (kScoreChunk = 64).
+    for (int zc0 = 0; zc0 < Pc; zc0 += zrows) {
+      const int zr = min(zrows, Pc - zc0);
+      if (!fuse_dwt) load_z(zc0, zr);
       const int q0 = lane < G ? lane : 0, q1 = lane + 32 < G ? lane + 32 : 0;
-      float z[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int r = warp + kWarps * u;
-        z[u] = r < rows && lane < G ? zc[r * TS + q0] : -INFINITY;
-      }
-      online8(m0, l0, z);
-      if (G > 32) {
+      for (int c0 = 0; c0 < zr; c0 += kScoreChunk) {
+        float z[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const int r = warp + kWarps * u;
-          z[u] = r < rows && lane + 32 < G ? zc[r * TS + q1] : -INFINITY;
+          const int r = c0 + warp + kWarps * u;
+          z[u] = r < zr && lane < G ? zc[r * ZP + q0] : -INFINITY;
         }
-        online8(m1, l1, z);
+        online8(m0, l0, z);
+        if (G > 32) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int r = c0 + warp + kWarps * u;
+            z[u] = r < zr && lane + 32 < G ? zc[r * ZP + q1] : -INFINITY;
+          }
+          online8(m1, l1, z);
+        }
       }
     }
     part_m[warp * kMaxQ + lane] = m0;
@@ -685,25 +633,28 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     __syncthreads();
     cluster_merge_stats(loc_m, loc_l, G, stat_in, gm, ginv);
     // Pass 2: attention mass of every position (4 threads per position).
-    for (int ch = 0; ch < nchunks; ++ch) {
-      const int c0 = ch * kScoreChunk, rows = min(kScoreChunk, Pc - c0);
-      if (nchunks > 1) chunk_logits(c0, rows);  // one chunk: zc still holds it
-      const int r = tid >> 2, sub = tid & 3;
-      float sa = 0.f, sb = 0.f;
-      if (r < rows) {
-        int qi = sub;
-        for (; qi + 4 < G; qi += 8) {
-          sa += exp2f(zc[r * TS + qi] - gm[qi]) * ginv[qi];
-          sb += exp2f(zc[r * TS + qi + 4] - gm[qi + 4]) * ginv[qi + 4];
+    for (int zc0 = 0; zc0 < Pc; zc0 += zrows) {
+      const int zr = min(zrows, Pc - zc0);
+      if (nz > 1) load_z(zc0, zr);  // one chunk: zc still holds it
+      for (int c0 = 0; c0 < zr; c0 += kThreads / 4) {
+        const int r = c0 + (tid >> 2), sub = tid & 3;
+        float sa = 0.f, sb = 0.f;
+        if (r < zr) {
+          int qi = sub;
+          for (; qi + 4 < G; qi += 8) {
+            sa += exp2f(zc[r * ZP + qi] - gm[qi]) * ginv[qi];
+            sb += exp2f(zc[r * ZP + qi + 4] - gm[qi + 4]) * ginv[qi + 4];
+          }
+          if (qi < G) sa += exp2f(zc[r * ZP + qi] - gm[qi]) * ginv[qi];
         }
-        if (qi < G) sa += exp2f(zc[r * TS + qi] - gm[qi]) * ginv[qi];
-      }
-      float sacc = sa + sb;
-      sacc += __shfl_xor_sync(0xffffffffu, sacc, 1);
-      sacc += __shfl_xor_sync(0xffffffffu, sacc, 2);
-      if (r < rows && sub == 0) {
-        for (int rr = 0; rr < cs; ++rr) peer(keys_all, rr)[rank * Pc + c0 + r] = __float_as_uint(sacc);
-        if (p.scores_out != nullptr) p.scores_out[unit * p.P + rank * Pc + c0 + r] = sacc;
+        float sacc = sa + sb;
+        sacc += __shfl_xor_sync(0xffffffffu, sacc, 1);
+        sacc += __shfl_xor_sync(0xffffffffu, sacc, 2);
+        if (r < zr && sub == 0) {
+          const int pos = rank * Pc + zc0 + r;
+          for (int rr = 0; rr < cs; ++rr) peer(keys_all, rr)[pos] = __float_as_uint(sacc);
+          if (p.scores_out != nullptr) p.scores_out[unit * p.P + pos] = sacc;
+        }
       }
     }
     cluster.sync();  // every CTA holds all P scores
@@ -1475,6 +1426,7 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
   mode &= kPhaseAll;
   p.mode = mode;
   p.G = ld.n_gen;
+  p.GZ = coarse_logit_pitch(ld.n_gen);
   p.levels = ld.levels;
   p.n_prompt = ld.n_prompt;
   p.P = ld.n_prompt >> ld.levels;
@@ -1573,8 +1525,7 @@ cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathAr
   p.vp = a.vp;
   p.kg = a.kg;
   p.vg = a.vg;
-  p.al = a.al;
-  p.al_planes = a.al_planes;
+  p.zl = a.zl;
   p.idx_l_in = a.idx_l_in;
   p.idx_in = a.idx_in;
   p.idx_l_out = a.idx_l_out;
@@ -1587,6 +1538,7 @@ cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathAr
   p.mode = plan.mode;
   p.n_prompt = ld.n_prompt;
   p.G = ld.n_gen;
+  p.GZ = coarse_logit_pitch(ld.n_gen);
   p.levels = ld.levels;
   p.P = ld.n_prompt >> ld.levels;
   p.kL = a.k_l;
