@@ -233,7 +233,10 @@ int wf_step_plan(const wf_dims* dims, const int32_t* k_per_level, wf_plan* out) 
   out->launches = plan.fuse_dwt ? 1 : 2;
   out->cluster = plan.cluster;
   out->final_gather = plan.gather_all;
-  out->token_logits = plan.t_in_smem ? WF_LOGITS_SHARED : WF_LOGITS_WORKSPACE;
+  out->token_logits = plan.filter_fast == 1   ? WF_LOGITS_TENSOR_MEMORY
+                      : plan.filter_fast == 2 ? WF_LOGITS_RECOMPUTED
+                      : plan.t_in_smem        ? WF_LOGITS_SHARED
+                                              : WF_LOGITS_WORKSPACE;
   out->smem_bytes = static_cast<int32_t>(plan.smem_bytes);
   return WF_OK;
 }

@@ -172,6 +172,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   raise_flag(status, WF_DEV_WAIT_TIMEOUT);
   return false;
 }
+// Plain arrival (no transaction bytes) on an mbarrier.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Barrier among a subset of the CTA's warps (named barrier `id` >= 1, `count`
+// threads, a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 // One bulk global -> shared copy through the TMA engine; completion is
 // signalled on `bar` as transaction bytes.  dst, src and bytes must be
 // multiples of 16.

@@ -47,6 +47,9 @@ struct PathPlan {
   int f_stages;      // filter: cp.async ring depth
   int a_stages;      // attend: cp.async ring depth
   bool t_in_smem;    // token logits in shared memory (else workspace)
+  int filter_fast;   // 0: general filter; 1: token logits resident in tensor
+                     // memory; 2: token logits recomputed per pass (no spill)
+  int f_nb;          // fast filter: tensor-memory accumulator slots
   size_t smem_bytes; // dynamic shared memory per CTA
   size_t t_bytes;    // workspace bytes for token logits (0 if in shared memory)
 };

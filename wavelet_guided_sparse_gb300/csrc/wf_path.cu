@@ -89,7 +89,9 @@ struct PathParams {
   int mode;
   int n_prompt, G, GZ, levels, P, kL, budget, n_keys;
   int cs, per_cta_p, rows_cap, sorted_cap, keys_cap, gather_all, klist_cap, tile_keys;
-  int f_stages, a_stages;  // cp.async ring depths (filter tiles, attention tiles)
+  int f_stages, a_stages;  // ring depths (filter tiles, attention tiles)
+  int filter_fast;         // token logits: 0 general path; 1 tensor-memory resident; 2 streamed twice
+  int f_nb;                // fast filter: tensor-memory accumulator slots
   int fuse_dwt;            // score: A_L from K_p inside this kernel
   uint32_t inject_polls;   // fault injection (tests): see the fused step 1 below
   float al_scale;          // 2^(-L/2), the orthonormal Haar low-pass gain
@@ -105,7 +107,8 @@ struct PathSmem {
   size_t qs, stat_in, gm, loc, part, cnt_a, cnt_b, misc, bars, sl_all, sp, sr, cp, cr, keys,
       take, topk, keys_all, pos_all, klist;
   size_t s_stage, s_as, s_z, s_ring;  // score phase
-  size_t f_kst, f_t;               // filter phase
+  size_t f_kst, f_t;               // filter phase (general path)
+  size_t f_ring, f_stage, f_bars, f_gather;  // filter phase (fast path)
   size_t a_kst, a_vst, a_work, a_recv, a_rml;  // attend phase
   size_t total;
   __host__ __device__ explicit PathSmem(const PathParams& p) {
@@ -117,6 +120,7 @@ struct PathSmem {
       return at;
     };
     sp = sr = cp = cr = keys = take = 0;
+    f_kst = f_t = f_ring = f_stage = f_bars = f_gather = 0;
     qs = take_bytes(static_cast<size_t>(kMaxQ) * kRowBytes);
     stat_in = take_bytes(sizeof(float) * kMaxCluster * 2 * kMaxQ);
     gm = take_bytes(sizeof(float) * 2 * kMaxQ);
@@ -130,7 +134,9 @@ struct PathSmem {
     topk = take_bytes(sizeof(TopkSmem));
     // All-gathered keys: the P coarse scores, and (final level, gather mode)
     // every CTA's candidates with their positions.
-    const size_t gather_n = p.gather_all ? static_cast<size_t>(p.cs) * p.rows_cap : 0;
+    // (The fast filter keeps its all-gather buffers in its own region.)
+    const size_t gather_n =
+        p.gather_all && !p.filter_fast ? static_cast<size_t>(p.cs) * p.rows_cap : 0;
     const size_t score_n = (p.mode & kModeScore) ? static_cast<size_t>(p.P) : 0;
     keys_all = take_bytes(sizeof(uint32_t) * (gather_n > score_n ? gather_n : score_n));
     pos_all = take_bytes(sizeof(int32_t) * gather_n);
@@ -155,8 +161,28 @@ struct PathSmem {
       s_stage = s_as = s_z;
       end = end > o ? end : o;
     }
-    if (p.mode & kModeFilter) {
+    if ((p.mode & kModeFilter) && p.filter_fast) {
+      // Ring of 128-row key tiles in the swizzled operand layout, the staging
+      // tile of the statistics pass, row scores, selection flags, survivors.
+      // The all-gather of (score, position) pairs for the final selection
+      // starts after every CTA's statistics pass: with resident logits the
+      // ring is idle by then and holds it; otherwise it has its own bytes.
       o = u;
+      f_kst = f_t = 0;
+      const size_t ring_b = static_cast<size_t>(p.f_stages) * D * 256;
+      const size_t gath_b = p.gather_all ? sizeof(uint32_t) * 2 * static_cast<size_t>(p.cs) * p.rows_cap : 0;
+      const bool overlay = p.filter_fast == 1;
+      f_ring = take_bytes(overlay && gath_b > ring_b ? gath_b : ring_b, 1024);
+      f_gather = overlay ? f_ring : (gath_b ? take_bytes(gath_b) : 0);
+      f_stage = take_bytes(sizeof(float) * 128 * static_cast<size_t>(p.GZ + 4));
+      keys = take_bytes(sizeof(uint32_t) * p.rows_cap);
+      take = take_bytes(p.rows_cap);
+      sp = take_bytes(sizeof(int32_t) * p.rows_cap);
+      f_bars = take_bytes(sizeof(uint64_t) * (p.f_stages + 2 * p.f_nb), 8);
+      end = end > o ? end : o;
+    } else if (p.mode & kModeFilter) {
+      o = u;
+      f_ring = f_stage = f_bars = f_gather = 0;
       f_kst = take_bytes(static_cast<size_t>(p.f_stages) * kTileRows * kRowBytes, 1024);
       sp = take_bytes(sizeof(int32_t) * p.rows_cap);  // survivor / candidate lists
       sr = take_bytes(sizeof(int32_t) * p.rows_cap);
@@ -410,8 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   uint64_t* span_bar = bars + kFuseStages + 1;  // tensor copies of the filter's span rows (one use)
   uint32_t mma_phase = 0;
   // bf16 logits tiles run on the tensor cores with accumulators in tensor
-  // memory: 256 columns (at most four pieces of N <= 64 queries).
-  constexpr uint32_t kTmemCols = 256;
+  // memory: 256 columns (at most four pieces of N <= 64 queries), or 512.
+  // The fast filter keeps up to 512 columns of token logits.
+  const uint32_t kTmemCols = (kFast || p.filter_fast) ? 512u : 256u;
   const bool use_tmem = sizeof(T) == 2 && (mode & (kModeScore | kModeFilter)) != 0;
   const int fuse_sr = kFuseStageBytes / (D * static_cast<int>(sizeof(T)));  // rows per stage
   const int fuse_rows = fuse_dwt ? (p.per_cta_p << levels) : 0;
@@ -704,262 +731,546 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     const int s1 = static_cast<int>((static_cast<int64_t>(rank + 1) * kL) / cs);
     const int ns = s1 - s0;
     const int R = ns << levels;
-    unsigned char* kst = smem + L.f_kst;
-    // Row pitch of t: odd in shared memory (conflict-free row-wise passes),
-    // a multiple of 4 floats when spilled to the workspace (16-byte loads).
-    const int TT = t_ws == nullptr ? TS : ((G + 3) & ~3);
-    float* t = t_ws == nullptr
-                   ? reinterpret_cast<float*>(smem + L.f_t)
-                   : t_ws + (static_cast<int64_t>(unit) * cs + rank) * p.rows_cap * TT;
-    const T* kp = static_cast<const T*>(p.kp);
-    const int ntiles = (R + kTileRows - 1) / kTileRows;
-    constexpr int C16 = D * static_cast<int>(sizeof(T)) / 16;  // 16-byte chunks per row
-    // Offset of a ring stage: bf16, rows of the 128-byte-swizzled layout
-    // (column blocks of FS * kTileRows rows); fp32, padded rows.
-    constexpr int kStageB = sizeof(T) == 2 ? kTileRows * 128 : kTileRows * RB;
-    const int FS = p.f_stages;
-    auto issue = [&](int tile, int stage) {  // all threads; one cp.async group
-      const int r0 = tile * kTileRows;
-      const int nr = min(kTileRows, R - r0);
-      for (int e = tid; e < nr * C16; e += kThreads) {
-        const int i = e / C16, ch = e % C16;
-        const int lr = r0 + i;
-        const int64_t grow = unit * p.n_prompt +
-                             (static_cast<int64_t>(sl_all[s0 + (lr >> levels)]) << levels) +
-                             (lr & ((1 << levels) - 1));
-        // bf16: core-matrix layout, stages back to back (a tensor-core
-        // operand may span stages); fp32: padded rows.
-        unsigned char* dst = sizeof(T) == 2
-                                 ? kst + sw_offset(stage * kTileRows + i, ch, FS * kTileRows)
-                                 : kst + (stage * kTileRows + i) * RB + ch * 16;
-        cp_async16(dst, reinterpret_cast<const unsigned char*>(kp + grow * D) + ch * 16);
-      }
-      cp_async_commit();
-    };
-    // bf16 with every row in the ring at once: one tensor copy per (span,
-    // 64-column block) lands the span's 2^L rows straight in the swizzled
-    // operand layout (8-row groups, so 2^L >= 8); otherwise 16-byte cp.async.
-    const bool tma_spans = sizeof(T) == 2 && p.use_tma_spans && ntiles <= FS;
-    if (tma_spans) {
-      constexpr int KB = D / 64;  // 64-column blocks per row
-      if (tid == 0) mbar_arrive_expect_tx(span_bar, static_cast<uint32_t>(R) * D * sizeof(T));
-      for (int i = tid; i < ns * KB; i += kThreads) {
-        const int sp_i = i / KB, kb = i - sp_i * KB;
-        tma_load_2d(kst + kb * (FS * kTileRows * 128) + ((sp_i << levels) >> 3) * 1024,
-                    &p.tmap_spans, kb * 64,
-                    static_cast<int>(unit * p.n_prompt + (sl_all[s0 + sp_i] << levels)), span_bar);
-      }
-    } else {
-      for (int tl = 0; tl < FS && tl < ntiles; ++tl) issue(tl, tl);
-    }
-    if (!tk_clean) {  // while the key rows are in flight (the tile barriers order it)
-      topk_zero(tk);
-      tk_clean = true;
-    }
-    if (ntiles <= FS && sizeof(T) == 2) {
-      // Every row is in flight: one wait, then one tensor-core pass over all
-      // R rows (tiles sit back to back in the ring).
-      if (tma_spans)
-        (void)mbar_wait_bounded(span_bar, 0, p.status);
-      else
-        cp_async_wait<0>();
-      umma_logits<D>(kst, 1, 0, FS * kTileRows, R, qs, G, t, 0, TT, 1.f, tmem, mma_bar, mma_phase,
-                     p.status);
-      __syncthreads();
-    } else
-    for (int tile = 0; tile < ntiles; ++tile) {
-      const int stage = tile % FS;
-      cp_async_wait_pending(min(ntiles, tile + FS) - 1 - tile);
-      const int rows_valid = min(kTileRows, R - tile * kTileRows);
-      if constexpr (sizeof(T) == 2) {
-        umma_logits<D>(kst + stage * kStageB, 1, 0, FS * kTileRows, rows_valid, qs, G, t,
-                       tile * kTileRows, TT, 1.f, tmem, mma_bar, mma_phase, p.status);
-      } else {
-        __syncthreads();
-        logits_tile_f32<D>(kst + stage * kStageB, reinterpret_cast<const float*>(qs), t,
-                           tile * kTileRows, rows_valid, G, TT, 1.f);
-      }
-      __syncthreads();
-      if (tile + FS < ntiles) issue(tile + FS, stage);
-    }
-    __syncthreads();
-
-    // Levels that keep every child need no scoring: start from the survivors
-    // of the lowest of them (all descendants of the coarse survivors, in
-    // position order) and walk down from the first level that selects.
-    int j_top = levels - 1;
-    while (j_top >= 0 && p.k[j_top] >= 2 * p.k[j_top + 1]) --j_top;
-    const int jj = j_top + 1, dsh = levels - jj;  // survivors at level jj: 2^dsh per span
-    int n_surv = ns << dsh;
     bool global_done = false;  // final token list already distributed
-    for (int e = tid; e < n_surv; e += kThreads) {
-      const int i = e >> dsh, m = e & ((1 << dsh) - 1);
-      sp[e] = (sl_all[s0 + i] << dsh) + m;
-      sr[e] = (i << levels) + (m << jj);
-    }
-    __syncthreads();
-    for (int j = j_top; j >= 0; --j) {
-      for (int i = tid; i < n_surv; i += kThreads) {
-        const int pos = sp[i], row = sr[i];
-        cp[2 * i] = 2 * pos;
-        cp[2 * i + 1] = 2 * pos + 1;
-        cr[2 * i] = row;
-        cr[2 * i + 1] = row + (1 << j);
-      }
-      const int n_cand = 2 * n_surv;
-      __syncthreads();
-      if (p.k[j] >= 2 * p.k[j + 1]) {  // every candidate survives: no scoring
-        int32_t* x = sp; sp = cp; cp = x;
-        x = sr; sr = cr; cr = x;
-        n_surv = n_cand;
-        continue;
-      }
-      // Scores of this level's candidates (log2 domain, z = sc2 * Σ_leaves t):
-      //  pass A  per query, online (max, Σ 2^(z - max)) over this CTA's
-      //          candidates (lanes = queries q and q + 32; a warp takes 8
-      //          candidates at a time, their loads issued together);
-      //  CTA and cluster merges give the global max gm and 1 / sum ginv;
-      //  pass B  s_c = Σ_q 2^(z[c,q] - gm_q) * ginv_q, one thread per candidate.
-      const int leaves = 1 << j;
-      const float sc2 = p.scale[j] * kLog2e;
-      const bool final_gather = j == 0 && gather_all;
-      const bool qa = lane < G, qb = lane + 32 < G;
-      const int la = qa ? lane : 0, lb = qb ? lane + 32 : 0;
-      // Leaf sum of t for candidate row offset `row` (row index * TT), query q.
-      auto leaf_sum = [&](int row, int q) {
-        float a = 0.f;
-#pragma unroll 1
-        for (int i = 0; i < leaves; ++i) a += t[row + i * TT + q];
-        return a;
+    int n_surv = 0;
+    if (sizeof(T) == 2 && (kFast || p.filter_fast)) {
+      // -------- fast path (token-level selection only; every level between
+      // L and 0 keeps all children): the R = ns 2^L rows under this CTA's
+      // coarse survivors go through a ring of 128-row tiles filled by 2-D
+      // tensor copies (whole spans, 128-byte swizzle), one tcgen05.mma pass
+      // per tile into its own tensor-memory accumulator (N = G rounded up to
+      // 16 columns).  Thread 0 issues copies and MMAs; warps 4-7 (one per
+      // tensor-memory lane quarter) read each finished accumulator, stage it
+      // in shared memory and fold it into per-query (max, sum) statistics.
+      // After the cluster-wide merge the token scores are formed from the
+      // accumulators again: still resident (filter_fast == 1, ntiles * N <=
+      // 512 columns), or recomputed by a second pass over the tiles through
+      // a few rotating accumulators (filter_fast == 2, which never spills).
+      constexpr int TR = 128;
+      constexpr int kStageBytes = D * 256;  // D / 64 column blocks of 128 rows x 128 B
+      const int box_rows = min(1 << levels, TR);
+      const int ntiles = (R + TR - 1) / TR;
+      const int S = p.f_stages, NB = p.f_nb;
+      const bool resident = kFast || p.filter_fast == 1;
+      const int N = (G + 15) & ~15;
+      const int total = resident ? ntiles : 2 * ntiles;
+      const int ZT2 = p.GZ + 4;
+      unsigned char* ring = smem + L.f_ring;
+      float* fst = reinterpret_cast<float*>(smem + L.f_stage);
+      uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.f_bars);
+      uint64_t* done = full + S;
+      uint64_t* empty = done + NB;
+      volatile int32_t* fabort = misc + 6;
+      const float sc2 = p.scale[0] * kLog2e;
+      auto pos_of = [&](int row) {
+        return (sl_all[s0 + (row >> levels)] << levels) + (row & ((1 << levels) - 1));
       };
-      float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
-      if (leaves == 1) {
-        // Sixteen candidates per warp step, every load of a step (both query
-        // halves) issued before the first exponential.
-        for (int ci0 = warp * 16; ci0 < n_cand; ci0 += kWarps * 16) {
-          int rows[16];
-#pragma unroll
-          for (int u = 0; u < 16; ++u) rows[u] = cr[min(ci0 + u, n_cand - 1)] * TT;
-          float za[2][8], zb[2][8];
-#pragma unroll
-          for (int u = 0; u < 16; ++u) za[u >> 3][u & 7] = t[rows[u] + la];
-          if (G > 32) {
-#pragma unroll
-            for (int u = 0; u < 16; ++u) zb[u >> 3][u & 7] = t[rows[u] + lb];
-          }
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const bool ok = ci0 + u < n_cand;
-            za[u >> 3][u & 7] = ok && qa ? za[u >> 3][u & 7] * sc2 : -INFINITY;
-            zb[u >> 3][u & 7] = ok && qb ? zb[u >> 3][u & 7] * sc2 : -INFINITY;
-          }
-          online8(m0, l0, za[0]);
-          online8(m0, l0, za[1]);
-          if (G > 32) {
-            online8(m1, l1, zb[0]);
-            online8(m1, l1, zb[1]);
+      if (tid == 0) {
+        for (int i = 0; i < S; ++i) mbar_init(&full[i], 1);
+        for (int i = 0; i < NB; ++i) {
+          mbar_init(&done[i], 1);
+          mbar_init(&empty[i], 4);  // one arrival per consumer warp
+        }
+        fence_mbar_init();
+        *fabort = 0;
+      }
+      if (!tk_clean) {
+        topk_zero(tk);
+        tk_clean = true;
+      }
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+
+      // ---- producer state (thread 0): next tile to copy, next tile to multiply
+      int next_tma = 0, g_mma = 0, g_full = 0;
+      bool p_ok = true;
+      auto tile_tma = [&](int g) {
+        const int t = g % ntiles, st = g % S;
+        const int rows = min(TR, R - t * TR);
+        mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(rows) * D * 2);
+        for (int b = 0; b * box_rows < rows; ++b) {
+          const int lr = t * TR + b * box_rows;
+          const int y = static_cast<int>(unit * p.n_prompt) + (sl_all[s0 + (lr >> levels)] << levels) +
+                        (lr & ((1 << levels) - 1));
+          for (int kb = 0; kb < D / 64; ++kb)
+            tma_load_2d(ring + st * kStageBytes + kb * (TR * 128) + b * box_rows * 128, &p.tmap_spans,
+                        kb * 64, y, &full[st]);
+        }
+      };
+      auto produce = [&](int g_end) {  // thread 0
+        if (next_tma == 0) {
+          for (; next_tma < min(S, total); ++next_tma) tile_tma(next_tma);
+        }
+        const uint32_t q0 = smem_u32(qs);
+        const uint32_t idesc = umma_idesc_bf16(TR, N);
+        for (; p_ok && g_mma < g_end; ++g_mma) {
+          const int g = g_mma, st = g % S, slot = g % NB;
+          p_ok = mbar_wait_bounded(&full[st], static_cast<uint32_t>((g / S) & 1), p.status);
+          if (!p_ok) break;
+          g_full = g + 1;
+          if (g >= NB)
+            p_ok = mbar_wait_bounded(&empty[slot], static_cast<uint32_t>(((g / NB) - 1) & 1), p.status);
+          if (!p_ok) break;
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(ring + st * kStageBytes);
+          for (int ks = 0; ks < D / 16; ++ks)
+            umma_bf16(tmem + slot * N,
+                      umma_desc_sw128(a0 + ((ks * 16) >> 6) * (TR * 128) + ((ks * 16) & 63) * 2),
+                      umma_desc(q0 + ks * 256, 128, D * 16), idesc, ks != 0);
+          umma_commit(&done[slot]);
+          // Refill a stage once the multiply that read it has finished: that of
+          // tile g - 1 (so tile g's multiply is queued behind it meanwhile), or
+          // with a single stage that of tile g itself.
+          const int j = S > 1 ? g - 1 : g;
+          if (j >= 0 && j + S < total) {
+            p_ok = mbar_wait_bounded(&done[j % NB], static_cast<uint32_t>((j / NB) & 1), p.status);
+            if (!p_ok) {
+              ++g_mma;
+              break;
+            }
+            tile_tma(next_tma++);  // tile j + S into stage j % S
           }
         }
-      } else {
-        for (int ci0 = warp * 8; ci0 < n_cand; ci0 += kWarps * 8) {
-          float z[8];
-#pragma unroll 1
-          for (int u = 0; u < 8; ++u) {
-            const int row = cr[min(ci0 + u, n_cand - 1)] * TT;
-            z[u] = ci0 + u < n_cand && qa ? leaf_sum(row, la) * sc2 : -INFINITY;
-          }
-          online8(m0, l0, z);
-          if (G > 32) {  // queries 32..63
-#pragma unroll 1
-            for (int u = 0; u < 8; ++u) {
-              const int row = cr[min(ci0 + u, n_cand - 1)] * TT;
-              z[u] = ci0 + u < n_cand && qb ? leaf_sum(row, lb) * sc2 : -INFINITY;
+        if (!p_ok) {
+          // Give up cleanly: no new work; every copy issued lands and the
+          // last multiply issued finishes before the shared memory and the
+          // tensor memory are reused (bounded waits).
+          *fabort = 1;
+          for (int g = g_full; g < next_tma; ++g)
+            (void)mbar_wait_bounded(&full[g % S], static_cast<uint32_t>((g / S) & 1), p.status);
+          if (g_mma > 0)
+            (void)mbar_wait_bounded(&done[(g_mma - 1) % NB],
+                                    static_cast<uint32_t>(((g_mma - 1) / NB) & 1), p.status);
+          g_full = next_tma;
+        }
+      };
+      // Reads the N accumulator columns of this thread's row of slot `slot`.
+      auto read_acc = [&](int slot, float (&v)[kMaxQ]) {
+        uint32_t r[4][16];
+        const uint32_t ta = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + slot * N;
+        tmem_ld16_nowait(ta, r[0]);
+        if (N > 16) tmem_ld16_nowait(ta + 16, r[1]);
+        if (N > 32) {
+          tmem_ld16_nowait(ta + 32, r[2]);
+          tmem_ld16_nowait(ta + 48, r[3]);
+        }
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[c * 16 + i] = __uint_as_float(r[c][i]);
+      };
+      auto row_score = [&](const float (&v)[kMaxQ]) {
+        float sq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < kMaxQ; ++q)
+          if (q < G) sq[q & 3] += exp2f(v[q] * sc2 - gm[q]) * ginv[q];
+        return (sq[0] + sq[1]) + (sq[2] + sq[3]);
+      };
+      const int row_l = (warp & 3) * 32 + lane;
+
+      // ---- pass A: statistics
+      float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+      if (warp == 0) {
+        if (lane == 0) produce(resident ? total : min(total, ntiles + NB));
+        __syncwarp();
+      } else if (warp >= 4) {
+        const int qw = warp & 3;
+        for (int t = 0; t < ntiles; ++t) {
+          const int slot = t % NB;
+          bool okc = *fabort == 0 &&
+                     mbar_wait_bounded(&done[slot], static_cast<uint32_t>((t / NB) & 1), p.status);
+          okc = __all_sync(0xffffffffu, okc);
+          tc_fence_after();
+          const int rows_valid = min(TR, R - t * TR);
+          if (okc) {
+            float v[kMaxQ];
+            read_acc(slot, v);
+            if (row_l < rows_valid) {
+              float* dst = fst + row_l * ZT2;
+#pragma unroll
+              for (int q = 0; q < kMaxQ; q += 4)
+                if (q < p.GZ) *reinterpret_cast<float4*>(dst + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
             }
-            online8(m1, l1, z);
           }
+          if (!resident) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+          }
+          named_bar_sync(1, 128);
+          const int qa = lane < G ? lane : 0, qb = lane + 32 < G ? lane + 32 : 0;
+#pragma unroll
+          for (int u0 = 0; u0 < 32; u0 += 8) {
+            float z[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int r = qw * 32 + u0 + u;
+              z[u] = okc && r < rows_valid && lane < G ? fst[r * ZT2 + qa] * sc2 : -INFINITY;
+            }
+            online8(m0, l0, z);
+            if (G > 32) {
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int r = qw * 32 + u0 + u;
+                z[u] = okc && r < rows_valid && lane + 32 < G ? fst[r * ZT2 + qb] * sc2 : -INFINITY;
+              }
+              online8(m1, l1, z);
+            }
+          }
+          named_bar_sync(1, 128);
         }
       }
-      part_m[warp * kMaxQ + lane] = m0;
-      part_m[warp * kMaxQ + lane + 32] = m1;
-      part_l[warp * kMaxQ + lane] = l0;
-      part_l[warp * kMaxQ + lane + 32] = l1;
+      if (warp >= 4) {
+        const int w4 = warp - 4;
+        part_m[w4 * kMaxQ + lane] = m0;
+        part_l[w4 * kMaxQ + lane] = l0;
+        part_m[w4 * kMaxQ + lane + 32] = m1;
+        part_l[w4 * kMaxQ + lane + 32] = l1;
+      }
       __syncthreads();
       if (tid < G) {
         float m = -INFINITY, l = 0.f;
-        for (int w = 0; w < kWarps; ++w) merge_ml(m, l, part_m[w * kMaxQ + tid], part_l[w * kMaxQ + tid]);
+        for (int w = 0; w < 4; ++w) merge_ml(m, l, part_m[w * kMaxQ + tid], part_l[w * kMaxQ + tid]);
         loc_m[tid] = m;
         loc_l[tid] = l;
       }
       __syncthreads();
-      cluster_merge_stats(loc_m, loc_l, G, stat_in, gm, ginv, n_cand, final_gather ? cnt_b : nullptr);
-      // Pass B: one thread per candidate (odd row pitch in shared memory:
-      // conflict-free); four independent partial sums over the queries.
-      for (int ci = tid; ci < n_cand; ci += kThreads) {
-        const int row = cr[ci] * TT;
-        float sq[4] = {0.f, 0.f, 0.f, 0.f};
-        if (leaves == 1 && t_ws != nullptr) {
-          // Spilled rows (L2): 16-byte loads, four in flight; columns >= G are padding.
-          const float4* r4 = reinterpret_cast<const float4*>(t + row);
-#pragma unroll 4
-          for (int q4 = 0; q4 < TT / 4; ++q4) {
-            const float4 v = r4[q4];
-            const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int q = 4 * q4 + k;
-              if (q < G) sq[k] += exp2f(vv[k] * sc2 - gm[q]) * ginv[q];
-            }
+      cluster_merge_stats(loc_m, loc_l, G, stat_in, gm, ginv, R, gather_all ? cnt_b : nullptr);
+
+      // ---- pass B: token scores s = Σ_q 2^(z - gm_q) / sum_q
+      if (resident) {
+        if (warp >= 4 && *fabort == 0) {
+          for (int t = 0; t < ntiles; ++t) {
+            float v[kMaxQ];
+            read_acc(t, v);
+            const int row = t * TR + row_l;
+            if (row < R) keys[row] = __float_as_uint(row_score(v));
           }
-        } else if (leaves == 1) {
-          int q = 0;
-#pragma unroll 2
-          for (; q + 4 <= G; q += 4) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) sq[k] += exp2f(t[row + q + k] * sc2 - gm[q + k]) * ginv[q + k];
-          }
-          for (; q < G; ++q) sq[0] += exp2f(t[row + q] * sc2 - gm[q]) * ginv[q];
-        } else {
-#pragma unroll 1
-          for (int q = 0; q < G; ++q) sq[q & 3] += exp2f(leaf_sum(row, q) * sc2 - gm[q]) * ginv[q];
         }
-        keys[ci] = __float_as_uint((sq[0] + sq[1]) + (sq[2] + sq[3]));
+      } else if (warp == 0) {
+        if (lane == 0) produce(total);
+        __syncwarp();
+      } else if (warp >= 4) {
+        for (int t = 0; t < ntiles; ++t) {
+          const int g = ntiles + t, slot = g % NB;
+          bool okc = *fabort == 0 &&
+                     mbar_wait_bounded(&done[slot], static_cast<uint32_t>((g / NB) & 1), p.status);
+          okc = __all_sync(0xffffffffu, okc);
+          tc_fence_after();
+          if (okc) {
+            float v[kMaxQ];
+            read_acc(slot, v);
+            const int row = t * TR + row_l;
+            if (row < R) keys[row] = __float_as_uint(row_score(v));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[slot]);
+        }
       }
+      tc_fence_before();
       __syncthreads();
-      if (final_gather) {
-        // Every CTA receives every candidate (score, position) at its dense
-        // offset, selects the budget locally and keeps what it needs: its
-        // slot range of the key list (attend) and of the output (idx).
+      tc_fence_after();
+
+      // ---- selection of the budget among the unit's token candidates
+      const int B = p.budget;
+      if (gather_all) {
+        // Every CTA receives every candidate (score, position) and selects
+        // the budget locally, keeping its slot range of the key list.
         int off = 0, n_all = 0;
         for (int r = 0; r < cs; ++r) {
           if (r < rank) off += cnt_b[r];
           n_all += cnt_b[r];
         }
-        for (int e = tid; e < n_cand * cs; e += kThreads) {
-          const int i = e % n_cand, r = e / n_cand;
-          peer(keys_all, r)[off + i] = keys[i];
-          peer(pos_all, r)[off + i] = cp[i];
+        uint32_t* gkeys = reinterpret_cast<uint32_t*>(smem + L.f_gather);
+        int32_t* gpos = reinterpret_cast<int32_t*>(gkeys + cs * p.rows_cap);
+        for (int e = tid; e < R * cs; e += kThreads) {
+          const int i = e % R, r = e / R;
+          peer(gkeys, r)[off + i] = keys[i];
+          peer(gpos, r)[off + i] = pos_of(i);
         }
         cluster.sync();
-        const int B = p.budget;
         const int a0 = key_slot_start(rank, cs, p.n_keys), a1 = key_slot_start(rank + 1, cs, p.n_keys);
-        const int w0 = key_slot_start(rank, cs, B), w1 = key_slot_start(rank + 1, cs, B);
-        const bool attend = (mode & kModeAttend) != 0;
-        // This CTA's slots of the key list: [a0, min(a1, B)); klist receives
-        // the selected candidates' token positions.
         const int b1 = min(a1, B);
-        block_select_topk(keys_all, n_all, B, a0, b1, klist, tk, tk_clean, pos_all);  // positions
+        block_select_topk(gkeys, n_all, B, a0, b1, klist, tk, tk_clean, gpos);
         tk_clean = false;
         if (p.idx_out != nullptr)
           for (int sl = a0 + tid; sl < b1; sl += kThreads) p.idx_out[unit * B + sl] = klist[sl - a0];
-        (void)attend;
-        (void)w0;
-        (void)w1;
         global_done = true;
-        break;
+      } else {
+        (void)cluster_select(keys, R, B, take, tk);
+        tk_clean = false;
+        int carry = 0;
+        for (int base = 0; base < R; base += kThreads) {
+          const int i = base + tid;
+          const int tf = i < R ? take[i] : 0;
+          int tot;
+          const int at = block_excl_scan(tf, tk.scan, &tot);
+          if (tf) sp[carry + at] = pos_of(i);
+          carry += tot;
+        }
+        __syncthreads();
+        n_surv = carry;
       }
-      (void)cluster_select(keys, n_cand, p.k[j], take, tk);
-      tk_clean = false;
-      n_surv = compact2(cp, cr, take, n_cand, sp, sr, tk.scan);
+    } else {
+      unsigned char* kst = smem + L.f_kst;
+      // Row pitch of t: odd in shared memory (conflict-free row-wise passes),
+      // a multiple of 4 floats when spilled to the workspace (16-byte loads).
+      const int TT = t_ws == nullptr ? TS : ((G + 3) & ~3);
+      float* t = t_ws == nullptr
+                     ? reinterpret_cast<float*>(smem + L.f_t)
+                     : t_ws + (static_cast<int64_t>(unit) * cs + rank) * p.rows_cap * TT;
+      const T* kp = static_cast<const T*>(p.kp);
+      const int ntiles = (R + kTileRows - 1) / kTileRows;
+      constexpr int C16 = D * static_cast<int>(sizeof(T)) / 16;  // 16-byte chunks per row
+      // Offset of a ring stage: bf16, rows of the 128-byte-swizzled layout
+      // (column blocks of FS * kTileRows rows); fp32, padded rows.
+      constexpr int kStageB = sizeof(T) == 2 ? kTileRows * 128 : kTileRows * RB;
+      const int FS = p.f_stages;
+      auto issue = [&](int tile, int stage) {  // all threads; one cp.async group
+        const int r0 = tile * kTileRows;
+        const int nr = min(kTileRows, R - r0);
+        for (int e = tid; e < nr * C16; e += kThreads) {
+          const int i = e / C16, ch = e % C16;
+          const int lr = r0 + i;
+          const int64_t grow = unit * p.n_prompt +
+                               (static_cast<int64_t>(sl_all[s0 + (lr >> levels)]) << levels) +
+                               (lr & ((1 << levels) - 1));
+          // bf16: core-matrix layout, stages back to back (a tensor-core
+          // operand may span stages); fp32: padded rows.
+          unsigned char* dst = sizeof(T) == 2
+                                   ? kst + sw_offset(stage * kTileRows + i, ch, FS * kTileRows)
+                                   : kst + (stage * kTileRows + i) * RB + ch * 16;
+          cp_async16(dst, reinterpret_cast<const unsigned char*>(kp + grow * D) + ch * 16);
+        }
+        cp_async_commit();
+      };
+      // bf16 with every row in the ring at once: one tensor copy per (span,
+      // 64-column block) lands the span's 2^L rows straight in the swizzled
+      // operand layout (8-row groups, so 2^L >= 8); otherwise 16-byte cp.async.
+      const bool tma_spans = sizeof(T) == 2 && p.use_tma_spans && ntiles <= FS;
+      if (tma_spans) {
+        constexpr int KB = D / 64;  // 64-column blocks per row
+        if (tid == 0) mbar_arrive_expect_tx(span_bar, static_cast<uint32_t>(R) * D * sizeof(T));
+        for (int i = tid; i < ns * KB; i += kThreads) {
+          const int sp_i = i / KB, kb = i - sp_i * KB;
+          tma_load_2d(kst + kb * (FS * kTileRows * 128) + ((sp_i << levels) >> 3) * 1024,
+                      &p.tmap_spans, kb * 64,
+                      static_cast<int>(unit * p.n_prompt + (sl_all[s0 + sp_i] << levels)), span_bar);
+        }
+      } else {
+        for (int tl = 0; tl < FS && tl < ntiles; ++tl) issue(tl, tl);
+      }
+      if (!tk_clean) {  // while the key rows are in flight (the tile barriers order it)
+        topk_zero(tk);
+        tk_clean = true;
+      }
+      if (ntiles <= FS && sizeof(T) == 2) {
+        // Every row is in flight: one wait, then one tensor-core pass over all
+        // R rows (tiles sit back to back in the ring).
+        if (tma_spans)
+          (void)mbar_wait_bounded(span_bar, 0, p.status);
+        else
+          cp_async_wait<0>();
+        umma_logits<D>(kst, 1, 0, FS * kTileRows, R, qs, G, t, 0, TT, 1.f, tmem, mma_bar, mma_phase,
+                       p.status);
+        __syncthreads();
+      } else
+      for (int tile = 0; tile < ntiles; ++tile) {
+        const int stage = tile % FS;
+        cp_async_wait_pending(min(ntiles, tile + FS) - 1 - tile);
+        const int rows_valid = min(kTileRows, R - tile * kTileRows);
+        if constexpr (sizeof(T) == 2) {
+          umma_logits<D>(kst + stage * kStageB, 1, 0, FS * kTileRows, rows_valid, qs, G, t,
+                         tile * kTileRows, TT, 1.f, tmem, mma_bar, mma_phase, p.status);
+        } else {
+          __syncthreads();
+          logits_tile_f32<D>(kst + stage * kStageB, reinterpret_cast<const float*>(qs), t,
+                             tile * kTileRows, rows_valid, G, TT, 1.f);
+        }
+        __syncthreads();
+        if (tile + FS < ntiles) issue(tile + FS, stage);
+      }
+      __syncthreads();
+
+      // Levels that keep every child need no scoring: start from the survivors
+      // of the lowest of them (all descendants of the coarse survivors, in
+      // position order) and walk down from the first level that selects.
+      int j_top = levels - 1;
+      while (j_top >= 0 && p.k[j_top] >= 2 * p.k[j_top + 1]) --j_top;
+      const int jj = j_top + 1, dsh = levels - jj;  // survivors at level jj: 2^dsh per span
+      n_surv = ns << dsh;
+      for (int e = tid; e < n_surv; e += kThreads) {
+        const int i = e >> dsh, m = e & ((1 << dsh) - 1);
+        sp[e] = (sl_all[s0 + i] << dsh) + m;
+        sr[e] = (i << levels) + (m << jj);
+      }
+      __syncthreads();
+      for (int j = j_top; j >= 0; --j) {
+        for (int i = tid; i < n_surv; i += kThreads) {
+          const int pos = sp[i], row = sr[i];
+          cp[2 * i] = 2 * pos;
+          cp[2 * i + 1] = 2 * pos + 1;
+          cr[2 * i] = row;
+          cr[2 * i + 1] = row + (1 << j);
+        }
+        const int n_cand = 2 * n_surv;
+        __syncthreads();
+        if (p.k[j] >= 2 * p.k[j + 1]) {  // every candidate survives: no scoring
+          int32_t* x = sp; sp = cp; cp = x;
+          x = sr; sr = cr; cr = x;
+          n_surv = n_cand;
+          continue;
+        }
+        // Scores of this level's candidates (log2 domain, z = sc2 * Σ_leaves t):
+        //  pass A  per query, online (max, Σ 2^(z - max)) over this CTA's
+        //          candidates (lanes = queries q and q + 32; a warp takes 8
+        //          candidates at a time, their loads issued together);
+        //  CTA and cluster merges give the global max gm and 1 / sum ginv;
+        //  pass B  s_c = Σ_q 2^(z[c,q] - gm_q) * ginv_q, one thread per candidate.
+        const int leaves = 1 << j;
+        const float sc2 = p.scale[j] * kLog2e;
+        const bool final_gather = j == 0 && gather_all;
+        const bool qa = lane < G, qb = lane + 32 < G;
+        const int la = qa ? lane : 0, lb = qb ? lane + 32 : 0;
+        // Leaf sum of t for candidate row offset `row` (row index * TT), query q.
+        auto leaf_sum = [&](int row, int q) {
+          float a = 0.f;
+  #pragma unroll 1
+          for (int i = 0; i < leaves; ++i) a += t[row + i * TT + q];
+          return a;
+        };
+        float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+        if (leaves == 1) {
+          // Sixteen candidates per warp step, every load of a step (both query
+          // halves) issued before the first exponential.
+          for (int ci0 = warp * 16; ci0 < n_cand; ci0 += kWarps * 16) {
+            int rows[16];
+  #pragma unroll
+            for (int u = 0; u < 16; ++u) rows[u] = cr[min(ci0 + u, n_cand - 1)] * TT;
+            float za[2][8], zb[2][8];
+  #pragma unroll
+            for (int u = 0; u < 16; ++u) za[u >> 3][u & 7] = t[rows[u] + la];
+            if (G > 32) {
+  #pragma unroll
+              for (int u = 0; u < 16; ++u) zb[u >> 3][u & 7] = t[rows[u] + lb];
+            }
+  #pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const bool ok = ci0 + u < n_cand;
+              za[u >> 3][u & 7] = ok && qa ? za[u >> 3][u & 7] * sc2 : -INFINITY;
+              zb[u >> 3][u & 7] = ok && qb ? zb[u >> 3][u & 7] * sc2 : -INFINITY;
+            }
+            online8(m0, l0, za[0]);
+            online8(m0, l0, za[1]);
+            if (G > 32) {
+              online8(m1, l1, zb[0]);
+              online8(m1, l1, zb[1]);
+            }
+          }
+        } else {
+          for (int ci0 = warp * 8; ci0 < n_cand; ci0 += kWarps * 8) {
+            float z[8];
+  #pragma unroll 1
+            for (int u = 0; u < 8; ++u) {
+              const int row = cr[min(ci0 + u, n_cand - 1)] * TT;
+              z[u] = ci0 + u < n_cand && qa ? leaf_sum(row, la) * sc2 : -INFINITY;
+            }
+            online8(m0, l0, z);
+            if (G > 32) {  // queries 32..63
+  #pragma unroll 1
+              for (int u = 0; u < 8; ++u) {
+                const int row = cr[min(ci0 + u, n_cand - 1)] * TT;
+                z[u] = ci0 + u < n_cand && qb ? leaf_sum(row, lb) * sc2 : -INFINITY;
+              }
+              online8(m1, l1, z);
+            }
+          }
+        }
+        part_m[warp * kMaxQ + lane] = m0;
+        part_m[warp * kMaxQ + lane + 32] = m1;
+        part_l[warp * kMaxQ + lane] = l0;
+        part_l[warp * kMaxQ + lane + 32] = l1;
+        __syncthreads();
+        if (tid < G) {
+          float m = -INFINITY, l = 0.f;
+          for (int w = 0; w < kWarps; ++w) merge_ml(m, l, part_m[w * kMaxQ + tid], part_l[w * kMaxQ + tid]);
+          loc_m[tid] = m;
+          loc_l[tid] = l;
+        }
+        __syncthreads();
+        cluster_merge_stats(loc_m, loc_l, G, stat_in, gm, ginv, n_cand, final_gather ? cnt_b : nullptr);
+        // Pass B: one thread per candidate (odd row pitch in shared memory:
+        // conflict-free); four independent partial sums over the queries.
+        for (int ci = tid; ci < n_cand; ci += kThreads) {
+          const int row = cr[ci] * TT;
+          float sq[4] = {0.f, 0.f, 0.f, 0.f};
+          if (leaves == 1 && t_ws != nullptr) {
+            // Spilled rows (L2): 16-byte loads, four in flight; columns >= G are padding.
+            const float4* r4 = reinterpret_cast<const float4*>(t + row);
+  #pragma unroll 4
+            for (int q4 = 0; q4 < TT / 4; ++q4) {
+              const float4 v = r4[q4];
+              const float vv[4] = {v.x, v.y, v.z, v.w};
+  #pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int q = 4 * q4 + k;
+                if (q < G) sq[k] += exp2f(vv[k] * sc2 - gm[q]) * ginv[q];
+              }
+            }
+          } else if (leaves == 1) {
+            int q = 0;
+  #pragma unroll 2
+            for (; q + 4 <= G; q += 4) {
+  #pragma unroll
+              for (int k = 0; k < 4; ++k) sq[k] += exp2f(t[row + q + k] * sc2 - gm[q + k]) * ginv[q + k];
+            }
+            for (; q < G; ++q) sq[0] += exp2f(t[row + q] * sc2 - gm[q]) * ginv[q];
+          } else {
+  #pragma unroll 1
+            for (int q = 0; q < G; ++q) sq[q & 3] += exp2f(leaf_sum(row, q) * sc2 - gm[q]) * ginv[q];
+          }
+          keys[ci] = __float_as_uint((sq[0] + sq[1]) + (sq[2] + sq[3]));
+        }
+        __syncthreads();
+        if (final_gather) {
+          // Every CTA receives every candidate (score, position) at its dense
+          // offset, selects the budget locally and keeps what it needs: its
+          // slot range of the key list (attend) and of the output (idx).
+          int off = 0, n_all = 0;
+          for (int r = 0; r < cs; ++r) {
+            if (r < rank) off += cnt_b[r];
+            n_all += cnt_b[r];
+          }
+          for (int e = tid; e < n_cand * cs; e += kThreads) {
+            const int i = e % n_cand, r = e / n_cand;
+            peer(keys_all, r)[off + i] = keys[i];
+            peer(pos_all, r)[off + i] = cp[i];
+          }
+          cluster.sync();
+          const int B = p.budget;
+          const int a0 = key_slot_start(rank, cs, p.n_keys), a1 = key_slot_start(rank + 1, cs, p.n_keys);
+          const int w0 = key_slot_start(rank, cs, B), w1 = key_slot_start(rank + 1, cs, B);
+          const bool attend = (mode & kModeAttend) != 0;
+          // This CTA's slots of the key list: [a0, min(a1, B)); klist receives
+          // the selected candidates' token positions.
+          const int b1 = min(a1, B);
+          block_select_topk(keys_all, n_all, B, a0, b1, klist, tk, tk_clean, pos_all);  // positions
+          tk_clean = false;
+          if (p.idx_out != nullptr)
+            for (int sl = a0 + tid; sl < b1; sl += kThreads) p.idx_out[unit * B + sl] = klist[sl - a0];
+          (void)attend;
+          (void)w0;
+          (void)w1;
+          global_done = true;
+          break;
+        }
+        (void)cluster_select(keys, n_cand, p.k[j], take, tk);
+        tk_clean = false;
+        n_surv = compact2(cp, cr, take, n_cand, sp, sr, tk.scan);
+      }
     }
     // Tokens of this CTA: sp[0, n_surv), ascending.
     if (!global_done) {
@@ -1326,7 +1637,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
 template <typename T, int D>
 cudaError_t launch_typed(int64_t units, const PathParams& prm, size_t smem, cudaStream_t stream) {
   const bool fast = prm.mode == (kModeScore | kModeFilter | kModeAttend) && prm.fuse_dwt &&
-                    prm.gather_all && prm.t_ws == nullptr;
+                    prm.gather_all && prm.filter_fast == 1;
   const cudaError_t e = fast ? ensure_max_smem<path_kernel<T, D, true>>()
                              : ensure_max_smem<path_kernel<T, D, false>>();
   if (e != cudaSuccess) return e;
@@ -1369,16 +1680,16 @@ EncodeTiledFn encode_tiled() {
 }
 
 // Tensor map of K_p [units * N_p rows, d columns] (bf16) with a box of 64
-// columns x 2^L rows and the 128-byte swizzle of the tensor-core operand
-// layout.  Returns false (and the kernel uses cp.async) if unavailable.
-bool encode_span_map(const LaunchDims& ld, const void* kp, CUtensorMap* map) {
-  if (ld.dtype != WF_BF16 || kp == nullptr || ld.levels < 3 || ld.levels > 8) return false;
+// columns x box_rows rows and the 128-byte swizzle of the tensor-core operand
+// layout.  Returns false if unavailable.
+bool encode_span_map(const LaunchDims& ld, const void* kp, CUtensorMap* map, int box_rows) {
+  if (ld.dtype != WF_BF16 || kp == nullptr || box_rows < 8 || box_rows > 256) return false;
   const EncodeTiledFn enc = encode_tiled();
   if (enc == nullptr) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(ld.head_dim),
                               static_cast<cuuint64_t>(ld.units) * ld.n_prompt};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld.head_dim) * 2};
-  const cuuint32_t box[2] = {64, 1u << ld.levels};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kp), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1450,6 +1761,17 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
   size_t smem = 0;
   bool t_in_smem = true;
   bool found = false;
+  // The fast filter (token logits on tcgen05 through a tensor-copy ring) serves
+  // bf16 inputs whose schedule selects only at the token level below L (every
+  // level in between keeps all children; the default schedule) with spans of
+  // 8..256 rows.
+  bool fast_sched = (mode & kModeFilter) && ld.dtype == WF_BF16 && ld.levels >= 3 &&
+                    ld.levels <= 8 && k != nullptr;
+  if (fast_sched) {
+    for (int j = 1; j < ld.levels; ++j)
+      if (k[j] < 2 * k[j + 1]) fast_sched = false;
+    if (k[0] >= 2 * k[1]) fast_sched = false;
+  }
   for (;; cs *= 2) {
     p.cs = cs;
     p.per_cta_p = (mode & kModeScore) ? p.P / cs : 0;
@@ -1477,10 +1799,23 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
                           (static_cast<int64_t>(elem) * ld.head_dim << ld.levels) <= kFuseStageBytes;
     // Prefer the fused step 1, the gather-all selection and token logits in
     // shared memory, in that order.
+    // Fast filter: resident accumulators when every tile has its own columns
+    // (ntiles * N <= 512), else four rotating ones; ring of up to 4 tiles.
+    const int n_cols = (ld.n_gen + 15) & ~15;
+    const int f_ntl = (p.rows_cap + 127) / 128;
+    const bool f_res = f_ntl * n_cols <= 512;
+    const int f_nb = f_res ? f_ntl : std::min(4, 512 / n_cols);
+    const int s_want = std::min(std::min(4, f_ntl), f_nb);
+    // The fast filter keeps the all-gather selection while a ring of two
+    // tiles fits; the general path prefers deeper rings first.
+    for (int ff = fast_sched ? 1 : 0; ff >= 0 && !found; --ff)
     for (int fz = fuse_try ? 1 : 0; fz >= 0 && !found; --fz)
-    for (int depth = 0; depth < 5 && !found; ++depth)
-    for (int ga = 1; ga >= 0 && !found; --ga) {
-      p.f_stages = std::max(2, f_want - depth);
+    for (int it = 0; it < 10 && !found; ++it) {
+      const int depth = ff ? (it < 5 ? std::min(it, std::max(0, s_want - 2)) : it - 5) : it >> 1;
+      const int ga = ff ? (it < 5 ? 1 : 0) : 1 - (it & 1);
+      p.filter_fast = ff ? (f_res ? 1 : 2) : 0;
+      p.f_nb = ff ? f_nb : 0;
+      p.f_stages = ff ? std::max(1, s_want - depth) : std::max(2, f_want - depth);
       p.a_stages = std::max(2, a_want - depth);
       if (ga && (!(mode & kModeFilter) || static_cast<int64_t>(cs) * p.rows_cap > 8192)) continue;
       p.gather_all = ga;
@@ -1488,6 +1823,10 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
       p.t_ws = nullptr;
       smem = smem_bytes(ld, p);
       t_in_smem = true;
+      if (ff) {
+        found = smem <= kMaxSmem;
+        continue;
+      }
       if ((mode & kModeFilter) && smem > kMaxSmem) {
         p.t_ws = reinterpret_cast<float*>(16);  // placeholder: only its nullness matters here
         smem = smem_bytes(ld, p);
@@ -1513,6 +1852,8 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
   plan->f_stages = p.f_stages;
   plan->a_stages = p.a_stages;
   plan->fuse_dwt = p.fuse_dwt;
+  plan->filter_fast = p.filter_fast;
+  plan->f_nb = p.f_nb;
   plan->mode = mode;
   return smem <= kMaxSmem;
 }
@@ -1556,8 +1897,19 @@ cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathAr
   p.a_stages = plan.a_stages;
   p.fuse_dwt = plan.fuse_dwt;
   p.inject_polls = plan.fuse_dwt ? consume_wait_injection() : 0u;
-  p.use_tma_spans =
-      (plan.mode & kModeFilter) != 0 && encode_span_map(ld, a.kp, &p.tmap_spans) ? 1 : 0;
+  p.filter_fast = plan.filter_fast;
+  p.f_nb = plan.f_nb;
+  if (plan.filter_fast) {
+    // The fast filter's tiles come only through tensor copies.
+    if (!encode_span_map(ld, a.kp, &p.tmap_spans, std::min(1 << ld.levels, 128)))
+      return cudaErrorNotSupported;
+    p.use_tma_spans = 1;
+  } else {
+    p.use_tma_spans = (plan.mode & kModeFilter) != 0 && ld.levels >= 3 && ld.levels <= 8 &&
+                              encode_span_map(ld, a.kp, &p.tmap_spans, 1 << ld.levels)
+                          ? 1
+                          : 0;
+  }
   p.al_scale = static_cast<float>(std::pow(2.0, -0.5 * ld.levels));  // 2^(-L/2)
   for (int j = 0; j <= ld.levels; ++j) {
     p.k[j] = a.k != nullptr ? a.k[j] : 0;
