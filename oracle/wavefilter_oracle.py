@@ -63,6 +63,8 @@ __all__ = [
     "wavefilter_step_batched",
     "cache_init",
     "cache_update",
+    "cache_scatter",
+    "al_repair",
     "daubechies_lowpass",
     "dwt_analysis_step",
     "dwt_synthesis_step",
@@ -291,6 +293,62 @@ def cache_update(k_gen, v_gen) -> Dict:
     if k.ndim != 3 or k.shape != v.shape:
         raise ValueError("K and V must both be [G, H, d]")
     return {"Kg": np.swapaxes(k, 0, 1), "Vg": np.swapaxes(v, 0, 1)}
+
+
+def cache_scatter(kp, vp, kg, vg, k_new, v_new, positions) -> Dict:
+    """Cache update over an arbitrary inferred set (WaveFilter §2.1 eq. (4):
+    K~^t[I~] = K^t[I~], V~^t[I~] = V^t[I~]), where I~ may hold generation
+    positions and prompt positions alike (caching schemes that refresh part of
+    the prompt cache write those rows too).
+
+    ``kp``, ``vp``: [H, N_p, d] and ``kg``, ``vg``: [H, G, d], the cache of one
+    sequence (position n < N_p is prompt row n, position N_p + g is generation
+    row g).  ``k_new``, ``v_new``: [M, H, d] token-major rows for the M
+    distinct ``positions`` (0 <= position < N_p + G).  Returns new arrays
+    {"Kp", "Vp", "Kg", "Vg"}; every row not in ``positions`` is unchanged.
+    """
+    kp, vp = np.array(kp, np.float64), np.array(vp, np.float64)
+    kg, vg = np.array(kg, np.float64), np.array(vg, np.float64)
+    k_new = np.asarray(k_new, np.float64)
+    v_new = np.asarray(v_new, np.float64)
+    pos = np.asarray(positions, np.int64)
+    n_prompt, n_gen = kp.shape[1], kg.shape[1]
+    if k_new.shape != v_new.shape or k_new.ndim != 3 or k_new.shape[0] != len(pos):
+        raise ValueError("new rows must be [M, H, d] for M positions")
+    if k_new.shape[1:] != (kp.shape[0], kp.shape[2]):
+        raise ValueError("new rows disagree with the cache on heads / head_dim")
+    if len(set(pos.tolist())) != len(pos):
+        raise ValueError("positions must be distinct")
+    if ((pos < 0) | (pos >= n_prompt + n_gen)).any():
+        raise ValueError("position outside the cache")
+    for m, n in enumerate(pos):
+        if n < n_prompt:
+            kp[:, n], vp[:, n] = k_new[m], v_new[m]
+        else:
+            kg[:, n - n_prompt], vg[:, n - n_prompt] = k_new[m], v_new[m]
+    return {"Kp": kp, "Vp": vp, "Kg": kg, "Vg": vg}
+
+
+def al_repair(a_l, kp_new, positions, levels: int) -> np.ndarray:
+    """The level-L approximation (WaveFilter §2.2 pyramid, §3.1) of the
+    prompt keys after a scatter, without recomputing all of it: a coarse
+    position p covers tokens [p 2^L, (p+1) 2^L), so only the coarse positions
+    whose span holds a rewritten prompt position change; each of them is the
+    pyramid of its span's new keys, every other row of ``a_l`` is kept.
+
+    ``a_l``: [H, N_p / 2^L, d] of the cache before the scatter; ``kp_new``:
+    [H, N_p, d] after it; ``positions`` as for :func:`cache_scatter`
+    (generation positions do not touch A_L).
+    """
+    out = np.array(a_l, np.float64)
+    kp_new = np.asarray(kp_new, np.float64)
+    n_prompt = kp_new.shape[1]
+    touched = sorted({int(n) >> levels for n in np.asarray(positions) if n < n_prompt})
+    for c in touched:
+        for h in range(kp_new.shape[0]):
+            span = kp_new[h, c << levels:(c + 1) << levels]
+            out[h, c] = haar_pyramid(span, levels)[levels][0]
+    return out
 
 
 # ------------------------------------------------------------------------

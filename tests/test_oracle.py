@@ -405,6 +405,92 @@ def test_cache_update_places_every_row():
                 assert c["Kg"][h, g, ch] == want and c["Vg"][h, g, ch] == -(want + 0.5)
 
 
+def _scatter_case(n_prompt=16, n_gen=4, heads=2, d=3, seed=5):
+    """A cache holding coded rows and M new coded rows (offset by 0.25 so they
+    differ from every old entry) for a scattered position set that mixes
+    prompt and generation positions."""
+    k, v = _coded_kv(n_prompt + n_gen, heads, d)
+    c = wo.cache_init(k, v, n_prompt, 1)
+    rng = np.random.default_rng(seed)
+    pos = rng.choice(n_prompt + n_gen, size=7, replace=False)
+    nk = np.stack([k[n] + 0.25 for n in pos])
+    nv = np.stack([v[n] - 0.25 for n in pos])
+    return c, pos, nk, nv
+
+
+def test_cache_scatter_places_every_row():
+    # Eq. (4) over a scattered set: row n of head h holds the new coded row of
+    # position n if n was written, else its old coded row.
+    n_prompt, n_gen, heads, d = 16, 4, 2, 3
+    c, pos, nk, nv = _scatter_case(n_prompt, n_gen, heads, d)
+    out = wo.cache_scatter(c["Kp"], c["Vp"], c["Kg"], c["Vg"], nk, nv, pos)
+    written = set(pos.tolist())
+    for h in range(heads):
+        for n in range(n_prompt + n_gen):
+            for ch in range(d):
+                base = n + 1000 * h + 1e6 * ch
+                want_k = base + 0.25 if n in written else base
+                want_v = -(base + 0.5) - 0.25 if n in written else -(base + 0.5)
+                kk = out["Kp"][h, n, ch] if n < n_prompt else out["Kg"][h, n - n_prompt, ch]
+                vv = out["Vp"][h, n, ch] if n < n_prompt else out["Vg"][h, n - n_prompt, ch]
+                assert kk == want_k and vv == want_v, (h, n, ch)
+
+
+def test_cache_scatter_rejects():
+    c, pos, nk, nv = _scatter_case()
+    with pytest.raises(ValueError):
+        wo.cache_scatter(c["Kp"], c["Vp"], c["Kg"], c["Vg"], nk, nv, np.r_[pos[:-1], pos[0]])
+    with pytest.raises(ValueError):
+        wo.cache_scatter(c["Kp"], c["Vp"], c["Kg"], c["Vg"], nk, nv, np.r_[pos[:-1], 20])
+    with pytest.raises(ValueError):
+        wo.cache_scatter(c["Kp"], c["Vp"], c["Kg"], c["Vg"], nk[:, :1], nv[:, :1], pos)
+
+
+@pytest.mark.parametrize("levels", [1, 2, 3])
+def test_al_repair_equals_full_pyramid_and_keeps_untouched_rows(levels):
+    # The repaired A_L equals the pyramid of the whole updated prompt cache,
+    # and coarse positions whose span holds no rewritten row are the input's
+    # rows bit for bit.
+    n_prompt = 32
+    rng = np.random.default_rng(levels)
+    kp = rng.standard_normal((3, n_prompt, 4))
+    a_l = np.stack([wo.haar_pyramid(kp[h], levels)[levels] for h in range(3)])
+    pos = np.array([3, 17, 18, 33])  # 33: a generation position
+    nk = rng.standard_normal((4, 3, 4))
+    kp_new = kp.copy()
+    for m, n in enumerate(pos):
+        if n < n_prompt:
+            kp_new[:, n] = nk[m]
+    out = wo.al_repair(a_l, kp_new, pos, levels)
+    full = np.stack([wo.haar_pyramid(kp_new[h], levels)[levels] for h in range(3)])
+    np.testing.assert_allclose(out, full, rtol=1e-14, atol=1e-14)
+    touched = {int(n) >> levels for n in pos if n < n_prompt}
+    for c in range(n_prompt >> levels):
+        if c not in touched:
+            assert np.array_equal(out[:, c], a_l[:, c]), c
+        else:
+            assert not np.array_equal(out[:, c], a_l[:, c]), c
+
+
+def test_al_repair_closed_form():
+    # Coded keys, prompt position 5 rewritten to K + 0.25 at L = 2: the span
+    # of coarse position 1 (tokens 4..7) sums to its old closed form plus 0.25,
+    # scaled by 2^(-L/2); the other coarse positions keep theirs.
+    n_prompt, heads, d, L = 16, 2, 3, 2
+    k, v = _coded_kv(n_prompt + 2, heads, d)
+    c = wo.cache_init(k, v, n_prompt, L)
+    kp_new = c["Kp"].copy()
+    kp_new[:, 5] += 0.25
+    out = wo.al_repair(c["a_l"], kp_new, [5], L)
+    span = 1 << L
+    for h in range(heads):
+        for p in range(n_prompt >> L):
+            for ch in range(d):
+                s = span * (1000 * h + 1e6 * ch) + span * span * p + (span // 2) * (span - 1)
+                s += 0.25 if p == 1 else 0.0
+                assert out[h, p, ch] == pytest.approx(s * 2.0 ** (-L / 2), rel=1e-14)
+
+
 # ----------------------------------------------------- Daubechies bases (psi)
 
 def test_daubechies_db1_is_haar():

@@ -147,6 +147,43 @@ def _update_heads_reshaped(k_gen, v_gen):
     g, h, d = k.shape
     return {"Kg": k.reshape(h, g, d), "Vg": np.asarray(v_gen, np.float64).reshape(h, g, d)}
 
+def _scatter_off_by_one(kp, vp, kg, vg, k_new, v_new, positions):
+    return _real_scatter(kp, vp, kg, vg, k_new, v_new, np.minimum(np.asarray(positions) + 1,
+                                                                  kp.shape[1] + kg.shape[1] - 1))
+
+
+def _scatter_all_to_generation(kp, vp, kg, vg, k_new, v_new, positions):
+    kg2, vg2 = np.array(kg, np.float64), np.array(vg, np.float64)
+    for m, n in enumerate(np.asarray(positions)):
+        g = int(n) % kg2.shape[1]
+        kg2[:, g], vg2[:, g] = np.asarray(k_new)[m], np.asarray(v_new)[m]
+    return {"Kp": np.array(kp, np.float64), "Vp": np.array(vp, np.float64), "Kg": kg2, "Vg": vg2}
+
+
+def _scatter_keys_values_swapped(kp, vp, kg, vg, k_new, v_new, positions):
+    return _real_scatter(kp, vp, kg, vg, v_new, k_new, positions)
+
+
+def _repair_unscaled(a_l, kp_new, positions, levels):
+    out = _real_repair(a_l, kp_new, positions, levels)
+    touched = {int(n) >> levels for n in positions if n < kp_new.shape[1]}
+    for c in touched:
+        out[:, c] *= 2.0 ** (levels / 2)
+    return out
+
+
+def _repair_wrong_span(a_l, kp_new, positions, levels):
+    return _real_repair(a_l, kp_new, [int(n) + (1 << levels) for n in positions
+                                      if int(n) + (1 << levels) < kp_new.shape[1]], levels)
+
+
+def _repair_nothing(a_l, kp_new, positions, levels):
+    return np.array(a_l, np.float64)
+
+
+_real_scatter = wo.cache_scatter
+_real_repair = wo.al_repair
+
 PIN_TESTS = [
     lambda: pins.test_haar_worked_example(),
     lambda: pins.test_haar_parseval(3),
@@ -167,6 +204,9 @@ PIN_TESTS = [
     lambda: pins.test_cache_init_lowpass_closed_form(2),
     lambda: pins.test_cache_init_round_trip_and_rejects(),
     lambda: pins.test_cache_update_places_every_row(),
+    lambda: pins.test_cache_scatter_places_every_row(),
+    lambda: pins.test_al_repair_equals_full_pyramid_and_keeps_untouched_rows(2),
+    lambda: pins.test_al_repair_closed_form(),
     lambda: pins.test_daubechies_db1_is_haar(),
     lambda: pins.test_daubechies_db2_closed_form(),
     lambda: pins.test_daubechies_filter_conditions(4),
@@ -191,6 +231,12 @@ MUTANTS = [
     ("cache_init", _init_keys_values_swapped),
     ("cache_init", _init_lowpass_unscaled),
     ("cache_update", _update_heads_reshaped),
+    ("cache_scatter", _scatter_off_by_one),
+    ("cache_scatter", _scatter_all_to_generation),
+    ("cache_scatter", _scatter_keys_values_swapped),
+    ("al_repair", _repair_unscaled),
+    ("al_repair", _repair_wrong_span),
+    ("al_repair", _repair_nothing),
     ("daubechies_lowpass", _db_reversed),
     ("daubechies_lowpass", _db_unit_sum),
     ("dwt_analysis_step", _dwt_zero_padded),
