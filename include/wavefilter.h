@@ -16,6 +16,7 @@
  *
  *   wf_cache_init         §2.1 eq. (2) at t = 1, plus A_L of the prompt keys
  *   wf_cache_update       §2.1 eq. (4) at t > 1 (generation rows)
+ *   wf_cache_scatter      §2.1 eq. (4) over any position set, with A_L repair
  *
  * and, for wavelet bases longer than the Haar pair (§3.1 leaves psi open):
  *
@@ -308,6 +309,36 @@ int wf_cache_init(const wf_dims* dims, const void* K, const void* V, void* Kp,
  * Errors: as wf_cache_init. */
 int wf_cache_update(const wf_dims* dims, const void* K, const void* V, void* Kg,
                     void* Vg, void* stream);
+
+/* Cache update over an arbitrary inferred set (WaveFilter §2.1 eq. (4),
+ * K~^t[I~] = K^t[I~], V~^t[I~] = V^t[I~]): the rows of any positions — of
+ * the generation block or of the prompt, as caching schemes that refresh
+ * part of the prompt cache write — replace the cached ones, and the level-L
+ * approximation of the prompt keys (§3.1) is re-formed at exactly the coarse
+ * positions whose spans hold a rewritten prompt row (the others stay valid),
+ * so wf_step_cached_al can keep running from AL without a new stream over Kp.
+ *   K, V       : device, [batch, n_rows, heads, head_dim] of dims.dtype,
+ *                token-major new rows
+ *   positions  : device, [batch, n_rows] int32, cache positions in
+ *                [0, n_prompt + n_gen) (n < n_prompt: prompt row n; else
+ *                generation row n - n_prompt), distinct within a sequence
+ *                (with a repeated position the row that lands is unspecified,
+ *                and AL still matches the cache)
+ *   Kp, Vp, Kg, Vg : device, in/out, the cache
+ *   AL         : device, in/out, nullable, [U, N_p/2^L, d] fp32: A_L of Kp
+ *                before the call (wf_dwt_lowpass / wf_cache_init); afterwards
+ *                it equals wf_dwt_lowpass of the updated Kp bit for bit
+ *   workspace  : device, nullable; if given (>= 256 bytes) a position outside
+ *                the cache raises WF_DEV_BAD_INDEX in its status word (the row
+ *                is skipped either way)
+ * n_rows = 0 is a no-op.  Outputs must not overlap the inputs.  One or two
+ * kernel launches.
+ * Errors: WF_ERR_NULL, WF_ERR_SHAPE, WF_ERR_UNSUPPORTED, WF_ERR_ALIGNMENT,
+ * WF_ERR_WORKSPACE, WF_ERR_CUDA. */
+int wf_cache_scatter(const wf_dims* dims, const void* K, const void* V,
+                     const int32_t* positions, int32_t n_rows, void* Kp, void* Vp, void* Kg,
+                     void* Vg, float* AL, void* workspace, size_t workspace_bytes,
+                     void* stream);
 
 /* wf_step with host-resident inputs and outputs: copies Q/Kp/Vp/Kg/Vg from
  * HOST memory into the caller's device staging buffers (one

@@ -233,3 +233,83 @@ def test_cache_init_batched_long_sampled():
         mask[seq, hi] = False
     for n in ("Kp", "Vp", "Kg", "Vg", "AL"):
         assert int(torch.count_nonzero(out[n][mask.cuda()])) == 0, n
+
+
+# ------------------------------------------ eq. (4) over an arbitrary set
+
+def _scatter_positions(rng, b, n_prompt, n_gen, m, with_bad=False):
+    """Distinct positions per sequence mixing prompt and generation rows
+    (several in one coarse span); optionally one out-of-range entry."""
+    pool = np.setdiff1d(np.arange(n_prompt + n_gen), [5, 6])
+    # 5 and 6 share a coarse span for every L >= 2
+    pos = np.stack([np.r_[5, 6, rng.choice(pool, size=m - 2, replace=False)] for _ in range(b)])
+    if with_bad:
+        pos[0, -1] = n_prompt + n_gen + 3
+    return pos.astype(np.int32)
+
+
+@pytest.mark.parametrize("name,m", [("tiny", 24), ("llada8b_layer", 48)])
+def test_cache_scatter_matches_oracle_and_repairs_al(name, m):
+    # Rows bit-exact against the oracle's eq. (4); the repaired A_L equals a
+    # fresh wf_dwt_lowpass of the updated prompt keys bit for bit (and the
+    # oracle's repair within 1e-3); the cached-A_L step on the updated cache
+    # then meets the whole-step contract on every unit.
+    cfg = wl.CONFIGS[name]
+    ks = cfg.k_per_level()
+    rnd = _rounder(cfg.dtype)
+    arrs = {k: rnd(v) for k, v in wl.generate_layer(cfg).items()}
+    dev = to_device(arrs, cfg.dtype)
+    al = bd.dwt_lowpass(dev["Kp"], cfg.levels)
+    rng = np.random.default_rng(m)
+    b, h, d = cfg.batch, cfg.heads, cfg.head_dim
+    pos = _scatter_positions(rng, b, cfg.n_prompt, cfg.n_gen, m)
+    nk = rnd(rng.standard_normal((b, m, h, d)) * 1.5)
+    nv = rnd(rng.standard_normal((b, m, h, d)))
+    cache = {"Kp": dev["Kp"], "Vp": dev["Vp"], "Kg": dev["Kg"], "Vg": dev["Vg"], "AL": al}
+    dt = torch_dtype(cfg.dtype)
+    ws = bd.alloc_status_workspace("cuda")
+    bd.cache_scatter(torch.from_numpy(nk).to("cuda", dt), torch.from_numpy(nv).to("cuda", dt),
+                     torch.from_numpy(pos).cuda(), cache, cfg.levels, ws=ws)
+    assert bd.read_device_status(ws) == 0
+    assert torch.equal(al, bd.dwt_lowpass(dev["Kp"], cfg.levels)), "repair differs from a fresh DWT"
+    got = {n: cache[n].cpu().double().numpy() for n in ("Kp", "Vp", "Kg", "Vg", "AL")}
+    new = {}
+    for bi in range(b):
+        ref = wo.cache_scatter(arrs["Kp"][bi], arrs["Vp"][bi], arrs["Kg"][bi], arrs["Vg"][bi],
+                               nk[bi], nv[bi], pos[bi])
+        for n in ("Kp", "Vp", "Kg", "Vg"):
+            np.testing.assert_array_equal(got[n][bi], ref[n], err_msg=f"{n} sequence {bi}")
+            new.setdefault(n, []).append(ref[n])
+        a0 = np.stack([wo.haar_pyramid(arrs["Kp"][bi, hi], cfg.levels)[cfg.levels]
+                       for hi in range(h)])
+        rep = wo.al_repair(a0, ref["Kp"], pos[bi], cfg.levels)
+        for hi in range(h):
+            assert _al_close(got["AL"][bi, hi], rep[hi]), (bi, hi)
+    upd = {n: np.stack(v).astype(np.float32) for n, v in new.items()}
+    upd["Q"] = arrs["Q"]
+    out, lse, idx, status = run_step(dev, cfg.levels, ks, al=al)
+    assert status == 0
+    out, lse, idx = out.cpu().numpy(), lse.cpu().numpy(), idx.cpu().numpy()
+    for bi in range(b):
+        for hi in range(h):
+            compare_step_unit(upd, bi, hi, cfg.levels, ks, idx[bi, hi], out[bi, hi], lse[bi, hi])
+
+
+def test_cache_scatter_skips_and_flags_bad_positions():
+    cfg = wl.CONFIGS["tiny"]
+    arrs = {k: v.astype(np.float32) for k, v in wl.generate_layer(cfg).items()}
+    dev = to_device(arrs, cfg.dtype)
+    before = {n: dev[n].clone() for n in ("Kp", "Vp", "Kg", "Vg")}
+    rng = np.random.default_rng(3)
+    pos = _scatter_positions(rng, 1, cfg.n_prompt, cfg.n_gen, 4, with_bad=True)
+    nk = rng.standard_normal((1, 4, cfg.heads, cfg.head_dim)).astype(np.float32)
+    ws = bd.alloc_status_workspace("cuda")
+    cache = {n: dev[n] for n in ("Kp", "Vp", "Kg", "Vg")}
+    bd.cache_scatter(torch.from_numpy(nk).cuda(), torch.from_numpy(nk).cuda(),
+                     torch.from_numpy(pos).cuda(), cache, cfg.levels, ws=ws)
+    assert bd.read_device_status(ws) & bd.DEV_BAD_INDEX
+    ref = wo.cache_scatter(arrs["Kp"][0], arrs["Vp"][0], arrs["Kg"][0], arrs["Vg"][0],
+                           nk[0, :3], nk[0, :3], pos[0, :3])
+    for n in ("Kp", "Vp", "Kg", "Vg"):
+        np.testing.assert_array_equal(cache[n][0].cpu().double().numpy(), ref[n])
+    assert not torch.equal(cache["Kp"], before["Kp"])

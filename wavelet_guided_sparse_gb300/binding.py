@@ -30,7 +30,7 @@ EXPORTS = ("wf_status_string", "wf_last_error_string", "wf_default_k_per_level",
            "wf_clear_device_status", "wf_read_device_status", "wf_dwt_lowpass",
            "wf_score_topk", "wf_recursive_filter", "wf_sparse_gather_attn", "wf_step",
            "wf_step_host", "wf_step_static_scratch", "wf_step_cached_al",
-           "wf_cache_init", "wf_cache_update", "wf_decode_step_host",
+           "wf_cache_init", "wf_cache_update", "wf_cache_scatter", "wf_decode_step_host",
            "wf_daubechies_lowpass", "wf_basis_workspace_bytes", "wf_dwt_lowpass_basis",
            "wf_step_basis")
 
@@ -90,6 +90,8 @@ _SIGS = {
                                          _vp, _vp, _sz, _vp]),
     "wf_cache_init": (ctypes.c_int, [_DIMSP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "wf_cache_update": (ctypes.c_int, [_DIMSP, _vp, _vp, _vp, _vp, _vp]),
+    "wf_cache_scatter": (ctypes.c_int, [_DIMSP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp,
+                                        _vp, _sz, _vp]),
     "wf_decode_step_host": (ctypes.c_int, [_DIMSP, _vp, _vp, _vp, _i32p, _vp, _vp, _vp, _vp,
                                            _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "wf_daubechies_lowpass": (ctypes.c_int, [_i32, _f64p]),
@@ -397,6 +399,23 @@ def cache_update(k: torch.Tensor, v: torch.Tensor, kg: torch.Tensor, vg: torch.T
     dims = Dims(b, h, n_prompt, g, d, levels, dtype_code(k.dtype))
     _check("wf_cache_update", lib().wf_cache_update(ctypes.byref(dims), _ptr(k), _ptr(v),
                                                     _ptr(kg), _ptr(vg), _stream(stream)))
+
+
+def cache_scatter(k: torch.Tensor, v: torch.Tensor, positions: torch.Tensor, cache: dict,
+                  levels: int, ws: Optional[torch.Tensor] = None, stream=None) -> None:
+    """wf_cache_scatter: token-major new rows K, V [b, M, H, d] at cache
+    positions [b, M] (int32) into cache {"Kp", "Vp", "Kg", "Vg"[, "AL"]} in
+    place (AL, if present, repaired at the touched coarse positions)."""
+    for t, name in ((k, "K"), (v, "V")):
+        _require(t, name)
+    _require(positions, "positions", torch.int32)
+    b, m, h, d = k.shape
+    kp = cache["Kp"]
+    dims = Dims(b, h, kp.shape[2], cache["Kg"].shape[2], d, levels, dtype_code(k.dtype))
+    _check("wf_cache_scatter", lib().wf_cache_scatter(
+        ctypes.byref(dims), _ptr(k), _ptr(v), _ptr(positions), m, _ptr(cache["Kp"]),
+        _ptr(cache["Vp"]), _ptr(cache["Kg"]), _ptr(cache["Vg"]), _ptr(cache.get("AL")),
+        _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
 
 
 def decode_step_host(dims: Dims, host: dict, k_per_level: Sequence[int], stage: dict,

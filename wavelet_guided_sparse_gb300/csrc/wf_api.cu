@@ -312,6 +312,28 @@ int wf_cache_update(const wf_dims* dims, const void* K, const void* V, void* Kg,
       wf::launch_cache_update(ld, K, V, Kg, Vg, static_cast<cudaStream_t>(stream)));
 }
 
+int wf_cache_scatter(const wf_dims* dims, const void* K, const void* V,
+                     const int32_t* positions, int32_t n_rows, void* Kp, void* Vp, void* Kg,
+                     void* Vg, float* AL, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  LaunchDims ld;
+  int st = check_dims(dims, &ld);
+  if (st != WF_OK) return st;
+  if (n_rows < 0) return WF_ERR_SHAPE;
+  if (n_rows == 0) return WF_OK;
+  if (K == nullptr || V == nullptr || positions == nullptr || Kp == nullptr || Vp == nullptr ||
+      Kg == nullptr || Vg == nullptr)
+    return WF_ERR_NULL;
+  if (!aligned16(K) || !aligned16(V) || !aligned16(Kp) || !aligned16(Vp) || !aligned16(Kg) ||
+      !aligned16(Vg) || (AL && !aligned16(AL)) || (workspace && !aligned16(workspace)) ||
+      (reinterpret_cast<uintptr_t>(positions) & 3u) != 0)
+    return WF_ERR_ALIGNMENT;
+  if (workspace != nullptr && workspace_bytes < kHeaderBytes) return WF_ERR_WORKSPACE;
+  return cuda_status(wf::launch_cache_scatter(
+      ld, K, V, positions, n_rows, Kp, Vp, Kg, Vg, AL,
+      workspace ? status_word(workspace) : nullptr, static_cast<cudaStream_t>(stream)));
+}
+
 int wf_score_topk(const wf_dims* dims, const void* Q, const float* AL, int32_t k_L,
                   int32_t* idx_L, float* scores_L, void* workspace, size_t workspace_bytes,
                   void* stream) {

@@ -23,6 +23,7 @@
 
 #include "wf_common.cuh"
 #include "wf_internal.h"
+#include "wf_mma.cuh"
 
 namespace wf {
 
@@ -41,7 +42,10 @@ struct DwtSmem {
   static constexpr size_t kRing = 128;
   static constexpr size_t kPart = kRing + static_cast<size_t>(kStages) * kStageBytes;
   static constexpr size_t kCarry = kPart + sizeof(float) * (kRows / 16) * C * V;
-  static constexpr size_t kTotal = kCarry + sizeof(float) * C * V;
+  // Finished A_L rows (fp32, padded pitch) waiting for their coarse logits.
+  static constexpr int kZfPitch = D + 4;
+  static constexpr size_t kZf = kCarry + sizeof(float) * C * V;
+  static constexpr size_t kTotal = kZf + sizeof(float) * 16 * kZfPitch;
 };
 
 template <typename T>
@@ -98,6 +102,12 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
   unsigned char* ring = smem + S::kRing;
   float* part = reinterpret_cast<float*>(smem + S::kPart);
   float* carry = reinterpret_cast<float*>(smem + S::kCarry);
+  float* zf = reinterpret_cast<float*>(smem + S::kZf);
+  constexpr int ZFP = S::kZfPitch;
+  // bf16 inputs: finished rows are buffered (16 at a time) and their coarse
+  // logits formed on the tensor cores; fp32 inputs use lane-group FMAs.
+  constexpr bool kMmaLogits = sizeof(T) == 2;
+  const bool zmma = kMmaLogits && zl != nullptr;
   const int tid = threadIdx.x;
   const int64_t s_begin = static_cast<int64_t>(blockIdx.x) * spans_per_cta;
   const int64_t s_end = min(n_spans, s_begin + spans_per_cta);
@@ -131,6 +141,22 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
     for (int64_t st = 0; st < issued; ++st)
       if (!(inject && st == 0)) issue(st);
   bool aborted = false;
+  // Coarse logits of the n buffered rows zf[0, n) = spans span_base ..:
+  // warp w forms query tiles w, w + 8 (8 queries each), separately for each
+  // unit the rows belong to.  Block-wide (call between barriers).
+  auto flush = [&](int64_t span_base, int n) {
+    if constexpr (kMmaLogits) {
+      if (n <= 0) return;
+      const int w = tid >> 5;
+      for (int64_t u = span_base / P; u * P < span_base + n; ++u) {
+        const int ra = static_cast<int>(u * P > span_base ? u * P - span_base : 0);
+        const int rb = static_cast<int>((u + 1) * P - span_base < n ? (u + 1) * P - span_base : n);
+        coarse_logits_rows16<D>(zf, ZFP, n, ra, rb, span_base,
+                                reinterpret_cast<const __nv_bfloat16*>(q) + u * G * D, G, GZ,
+                                zscale, zl, w, kWarps);
+      }
+    }
+  };
 
   for (int64_t st = 0; st < issued; ++st) {
     const bool ok = mbar_wait_bounded(&bars[st % kStages], static_cast<uint32_t>((st / kStages) & 1),
@@ -139,7 +165,33 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
     const unsigned char* buf = ring + (st % kStages) * kStageBytes;
     const int rows_in = static_cast<int>(min(static_cast<int64_t>(SR), rows_total - st * SR));
     const int64_t first_row = st * SR;
-    if (span_rows <= 16) {
+    if (span_rows <= 16 && zmma) {
+      // One thread per (span, chunk) of up to 16 spans at a time; their rows
+      // go to the buffer, then to the tensor cores.
+      const int spans_in = rows_in >> levels;
+      const int64_t span0 = first_row >> levels;
+      for (int g0 = 0; g0 < spans_in; g0 += 16) {
+        const int gn = min(16, spans_in - g0);
+        for (int item = tid; item < gn * C; item += kThreads) {
+          const int sl = item / C, c = item % C;
+          float acc[V];
+#pragma unroll
+          for (int v = 0; v < V; ++v) acc[v] = 0.f;
+          const unsigned char* p = buf + ((g0 + sl) << levels) * RB + c * 16;
+#pragma unroll
+          for (int r = 0; r < 16; ++r)
+            if (r < span_rows) add_chunk<T>(p + r * RB, acc);
+          float4* dst = reinterpret_cast<float4*>(zf + sl * ZFP + c * V);
+#pragma unroll
+          for (int v = 0; v < V; v += 4)
+            dst[v / 4] = make_float4(acc[v] * scale, acc[v + 1] * scale, acc[v + 2] * scale,
+                                     acc[v + 3] * scale);
+        }
+        __syncthreads();
+        flush(s_begin + span0 + g0, gn);
+        __syncthreads();
+      }
+    } else if (span_rows <= 16) {
       // One thread per (span, chunk) of this stage; a stage holds whole spans.
       // Whole warps iterate together (the coarse logits are warp-collective).
       const int spans_in = rows_in >> levels;
@@ -178,6 +230,40 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
       const int64_t sp0 = first_row >> levels;
       const int64_t sp1 = (first_row + rows_in - 1) >> levels;
       const int nsp = static_cast<int>(sp1 - sp0 + 1);
+      if (zmma) {
+        // Spans finished in this stage (all but possibly the last), 16 at a
+        // time: rows to the buffer, then to the tensor cores.
+        const bool last_open = ((sp1 + 1) << levels) > first_row + rows_in;
+        for (int g0 = 0; g0 < nsp; g0 += 16) {
+          const int gn = min(16, nsp - g0);
+          for (int item = tid; item < gn * C; item += kThreads) {
+            const int sl = g0 + item / C, c = item % C;
+            const int64_t span = sp0 + sl;
+            const int64_t r_lo = max(span << levels, first_row);
+            const int64_t r_hi = min((span + 1) << levels, first_row + rows_in);
+            const bool carried = (span << levels) < first_row;
+            float acc[V];
+#pragma unroll
+            for (int v = 0; v < V; ++v) acc[v] = carried ? carry[c * V + v] : 0.f;
+            for (int b = static_cast<int>((r_lo - first_row) / 16); b < (r_hi - first_row) / 16; ++b)
+#pragma unroll
+              for (int v = 0; v < V; ++v) acc[v] += part[(b * C + c) * V + v];
+            if (((span + 1) << levels) <= first_row + rows_in) {
+              float4* dst = reinterpret_cast<float4*>(zf + (item / C) * ZFP + c * V);
+#pragma unroll
+              for (int v = 0; v < V; v += 4)
+                dst[v / 4] = make_float4(acc[v] * scale, acc[v + 1] * scale, acc[v + 2] * scale,
+                                         acc[v + 3] * scale);
+            } else {
+#pragma unroll
+              for (int v = 0; v < V; ++v) carry[c * V + v] = acc[v];
+            }
+          }
+          __syncthreads();
+          flush(s_begin + sp0 + g0, gn - (last_open && g0 + gn == nsp ? 1 : 0));
+          __syncthreads();
+        }
+      } else
       for (int base = 0; base < nsp * C; base += kThreads) {  // whole warps together
         const int item = base + tid;
         const bool in = item < nsp * C;
@@ -244,6 +330,21 @@ __global__ void __launch_bounds__(kThreads) coarse_logits_kernel(const float* __
                                                                  float* __restrict__ zl,
                                                                  int64_t rows_total, int64_t P,
                                                                  int G, int GZ, float zscale) {
+  if constexpr (sizeof(T) == 2) {
+    // One warp per 16-row block on the tensor cores.
+    const int64_t warp_g = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    for (int64_t r0 = warp_g * 16; r0 < rows_total; r0 += static_cast<int64_t>(gridDim.x) * kWarps * 16) {
+      const int n = static_cast<int>(rows_total - r0 < 16 ? rows_total - r0 : 16);
+      for (int64_t u = r0 / P; u * P < r0 + n; ++u) {
+        const int ra = static_cast<int>(u * P > r0 ? u * P - r0 : 0);
+        const int rb = static_cast<int>((u + 1) * P - r0 < n ? (u + 1) * P - r0 : n);
+        coarse_logits_rows16<D>(al + r0 * D, D, n, ra, rb, r0,
+                                reinterpret_cast<const __nv_bfloat16*>(q) + u * G * D, G, GZ,
+                                zscale, zl, 0, 1);
+      }
+    }
+    return;
+  }
   constexpr int V = Elem<T>::kPer16B, C = D / V, RPP = kThreads / C;  // rows per pass
   const int tid = threadIdx.x, c = tid % C;
   for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPP; base < rows_total;
@@ -269,7 +370,7 @@ __global__ void __launch_bounds__(kThreads) coarse_logits_kernel(const float* __
 template <typename T, int D>
 cudaError_t launch_logits_typed(const LaunchDims& ld, const float* al, const void* q, float* zl,
                                 cudaStream_t stream) {
-  constexpr int RPP = kThreads / (D / Elem<T>::kPer16B);
+  constexpr int RPP = sizeof(T) == 2 ? kWarps * 16 : kThreads / (D / Elem<T>::kPer16B);
   const int64_t P = ld.n_prompt >> ld.levels;
   const int64_t rows = ld.units * P;
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((rows + RPP - 1) / RPP,

@@ -100,6 +100,13 @@ cudaError_t launch_cache_init(const LaunchDims& ld, const void* k, const void* v
                               void* vp, void* kg, void* vg, float* al, cudaStream_t stream);
 cudaError_t launch_cache_update(const LaunchDims& ld, const void* k, const void* v, void* kg,
                                 void* vg, cudaStream_t stream);
+// Eq. (4) over `rows` positions per sequence (pos [batch, rows], prompt or
+// generation) from token-major K/V [batch, rows, heads, d]; A_L (nullable)
+// re-formed at the touched coarse positions; bad positions flagged in
+// *status (nullable).
+cudaError_t launch_cache_scatter(const LaunchDims& ld, const void* k, const void* v,
+                                 const int32_t* pos, int rows, void* kp, void* vp, void* kg,
+                                 void* vg, float* al, int32_t* status, cudaStream_t stream);
 
 // Longer orthonormal bases (wf_basis.cu).  Filter taps (fp32 copy of the
 // caller's low-pass) and the launch arguments of the level-by-level filter.

@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "wf_common.cuh"
+
 namespace wf {
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
@@ -33,6 +35,91 @@ __device__ __forceinline__ void mma_bf16(float* c, const uint32_t* a, const uint
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Exact split of an fp32 value into three bf16 parts, hi + mid + lo = x to
+// within 2^-24 relative (each part rounds the remainder of the previous).
+__device__ __forceinline__ void split3_bf16(float x, float& hi, float& mid, float& lo) {
+  hi = __bfloat162float(__float2bfloat16_rn(x));
+  const float r1 = x - hi;
+  mid = __bfloat162float(__float2bfloat16_rn(r1));
+  lo = r1 - mid;
+}
+
+// Coarse logits of 16 consecutive rows of the level-L approximation on the
+// warp's tensor cores:
+//   out[(span0 + r) * GZ + q] = zscale * Σ_k A[r][k] * Q[q][k]
+// for rows r in [ra, rb) and queries q < G (one unit's queries, bf16).  A
+// rows come as fp32 (rows r < nrows of `a`, `pitch` floats apart; shared or
+// global memory); each value is split into three bf16 parts whose products
+// with the bf16 queries are exact, accumulated in fp32 by m16n8k16 MMAs.
+// The warp covers the query tiles nt0, nt0 + nt_step, ... (8 queries each).
+// Warp-collective.
+template <int D>
+__device__ __forceinline__ void coarse_logits_rows16(const float* a, int pitch, int nrows, int ra,
+                                                     int rb, int64_t span0,
+                                                     const __nv_bfloat16* q, int G, int GZ,
+                                                     float zscale, float* out, int nt0,
+                                                     int nt_step) {
+  const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+  const int NT = (G + 7) >> 3;
+  constexpr int kMaxTiles = 8;  // G <= 64
+  float c[kMaxTiles][4];
+#pragma unroll
+  for (int t = 0; t < kMaxTiles; ++t)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) c[t][e] = 0.f;
+  const bool r0ok = gid < nrows, r1ok = gid + 8 < nrows;
+#pragma unroll 2
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const int k0 = ks * 16 + 2 * tig;
+    float2 v[4];  // (row gid, k0), (row gid + 8, k0), (row gid, k0 + 8), (row gid + 8, k0 + 8)
+    v[0] = r0ok ? *reinterpret_cast<const float2*>(a + gid * pitch + k0) : make_float2(0.f, 0.f);
+    v[1] = r1ok ? *reinterpret_cast<const float2*>(a + (gid + 8) * pitch + k0) : make_float2(0.f, 0.f);
+    v[2] = r0ok ? *reinterpret_cast<const float2*>(a + gid * pitch + k0 + 8) : make_float2(0.f, 0.f);
+    v[3] = r1ok ? *reinterpret_cast<const float2*>(a + (gid + 8) * pitch + k0 + 8) : make_float2(0.f, 0.f);
+    uint32_t af[3][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float h0, m0, l0, h1, m1, l1;
+      split3_bf16(v[i].x, h0, m0, l0);
+      split3_bf16(v[i].y, h1, m1, l1);
+      af[0][i] = pack_bf16(h0, h1);
+      af[1][i] = pack_bf16(m0, m1);
+      af[2][i] = pack_bf16(l0, l1);
+    }
+#pragma unroll
+    for (int t = 0; t < kMaxTiles; ++t) {
+      const int nt = nt0 + t * nt_step;
+      if (nt >= NT) break;
+      const int qn = nt * 8 + gid;
+      uint32_t b[2] = {0u, 0u};
+      if (qn < G) {
+        const __nv_bfloat16* qr = q + static_cast<int64_t>(qn) * D + k0;
+        b[0] = __ldg(reinterpret_cast<const unsigned int*>(qr));
+        b[1] = __ldg(reinterpret_cast<const unsigned int*>(qr + 8));
+      }
+#pragma unroll
+      for (int pl = 0; pl < 3; ++pl) mma_bf16(c[t], af[pl], b);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kMaxTiles; ++t) {
+    const int nt = nt0 + t * nt_step;
+    if (nt >= NT) break;
+    const int col = nt * 8 + 2 * tig;
+    if (col >= G) continue;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = gid + 8 * h;
+      if (r < ra || r >= rb) continue;
+      float* dst = out + (span0 + r) * GZ + col;
+      if (col + 1 < G)
+        *reinterpret_cast<float2*>(dst) = make_float2(c[t][2 * h] * zscale, c[t][2 * h + 1] * zscale);
+      else
+        dst[0] = c[t][2 * h] * zscale;
+    }
+  }
 }
 
 }  // namespace wf

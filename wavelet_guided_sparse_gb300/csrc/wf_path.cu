@@ -992,12 +992,19 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           peer(gpos, r)[off + i] = pos_of(i);
         }
         cluster.sync();
-        const int a0 = key_slot_start(rank, cs, p.n_keys), a1 = key_slot_start(rank + 1, cs, p.n_keys);
-        const int b1 = min(a1, B);
-        block_select_topk(gkeys, n_all, B, a0, b1, klist, tk, tk_clean, gpos);
+        if (mode & kModeAttend) {
+          // This CTA's slots of the key list, [a0, min(a1, B)).
+          const int a0 = key_slot_start(rank, cs, p.n_keys), a1 = key_slot_start(rank + 1, cs, p.n_keys);
+          const int b1 = min(a1, B);
+          block_select_topk(gkeys, n_all, B, a0, b1, klist, tk, tk_clean, gpos);
+          if (p.idx_out != nullptr)
+            for (int sl = a0 + tid; sl < b1; sl += kThreads) p.idx_out[unit * B + sl] = klist[sl - a0];
+        } else {
+          // No key list: this CTA's share of the output slots, straight to idx.
+          const int w0 = key_slot_start(rank, cs, B), w1 = key_slot_start(rank + 1, cs, B);
+          block_select_topk(gkeys, n_all, B, w0, w1, p.idx_out + unit * B + w0, tk, tk_clean, gpos);
+        }
         tk_clean = false;
-        if (p.idx_out != nullptr)
-          for (int sl = a0 + tid; sl < b1; sl += kThreads) p.idx_out[unit * B + sl] = klist[sl - a0];
         global_done = true;
       } else {
         (void)cluster_select(keys, R, B, take, tk);
@@ -1251,19 +1258,21 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           }
           cluster.sync();
           const int B = p.budget;
-          const int a0 = key_slot_start(rank, cs, p.n_keys), a1 = key_slot_start(rank + 1, cs, p.n_keys);
-          const int w0 = key_slot_start(rank, cs, B), w1 = key_slot_start(rank + 1, cs, B);
-          const bool attend = (mode & kModeAttend) != 0;
-          // This CTA's slots of the key list: [a0, min(a1, B)); klist receives
-          // the selected candidates' token positions.
-          const int b1 = min(a1, B);
-          block_select_topk(keys_all, n_all, B, a0, b1, klist, tk, tk_clean, pos_all);  // positions
+          if (mode & kModeAttend) {
+            // This CTA's slots of the key list: [a0, min(a1, B)); klist
+            // receives the selected candidates' token positions.
+            const int a0 = key_slot_start(rank, cs, p.n_keys), a1 = key_slot_start(rank + 1, cs, p.n_keys);
+            const int b1 = min(a1, B);
+            block_select_topk(keys_all, n_all, B, a0, b1, klist, tk, tk_clean, pos_all);  // positions
+            if (p.idx_out != nullptr)
+              for (int sl = a0 + tid; sl < b1; sl += kThreads) p.idx_out[unit * B + sl] = klist[sl - a0];
+          } else {
+            // No key list: this CTA's share of the output slots, straight to idx.
+            const int w0 = key_slot_start(rank, cs, B), w1 = key_slot_start(rank + 1, cs, B);
+            block_select_topk(keys_all, n_all, B, w0, w1, p.idx_out + unit * B + w0, tk, tk_clean,
+                              pos_all);
+          }
           tk_clean = false;
-          if (p.idx_out != nullptr)
-            for (int sl = a0 + tid; sl < b1; sl += kThreads) p.idx_out[unit * B + sl] = klist[sl - a0];
-          (void)attend;
-          (void)w0;
-          (void)w1;
           global_done = true;
           break;
         }
