@@ -60,14 +60,14 @@ def test_static_scratch_matches_workspace_entry_point(name):
 
 
 def test_static_scratch_rejects_sizes_beyond_its_limit():
-    # The 10 % budget of the batched-long workload needs far more scratch than
-    # the fixed array holds: rejected on the host before anything runs.
-    cfg = wl.CONFIGS["batched_long_10pct"]
-    dims = bd.Dims(cfg.batch, cfg.heads, cfg.n_prompt, cfg.n_gen, cfg.head_dim, cfg.levels, 0)
-    assert bd.workspace_bytes(dims, cfg.k_per_level()) > (48 << 20)
+    # Eight sequences of 32 heads over a 131072-token prompt at L = 5 need
+    # far more scratch than the fixed array holds: rejected on the host
+    # before anything runs.
+    dims = bd.Dims(8, 32, 131072, 64, 128, 5, 0)
+    ks = bd.default_k_per_level(131072, 5, 4096)
+    assert bd.workspace_bytes(dims, ks) > (48 << 20)
     small = torch.empty(16, dtype=torch.bfloat16, device="cuda")
     st = bd.lib().wf_step_static_scratch(bd.ctypes.byref(dims), bd._ptr(small), bd._ptr(small),
                                          bd._ptr(small), bd._ptr(small), bd._ptr(small),
-                                         bd._k_array(cfg.k_per_level()), bd._ptr(small), None,
-                                         None, None)
+                                         bd._k_array(ks), bd._ptr(small), None, None, None)
     assert st == 4  # WF_ERR_WORKSPACE

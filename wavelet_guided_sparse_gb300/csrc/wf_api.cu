@@ -65,17 +65,19 @@ int check_k(const LaunchDims& ld, const int32_t* k) {
 }
 
 // Workspace layout shared by every entry point: [status header | coarse
-// logits | S_L | S | t].
+// logits | A_L | S_L | S | t].
 struct Layout {
-  size_t zl, idx_l, idx, t, total;
+  size_t zl, al, idx_l, idx, t, total;
 };
 
 Layout layout(const LaunchDims& ld, const int32_t* k, const wf::PathPlan* fp) {
   Layout L;
   size_t o = kHeaderBytes;
+  const size_t rows = static_cast<size_t>(ld.units) * (ld.n_prompt >> ld.levels);
   L.zl = o;  // coarse logits [U, P, coarse_logit_pitch(G)] fp32
-  o = align_up(o + sizeof(float) * static_cast<size_t>(ld.units) * (ld.n_prompt >> ld.levels) *
-                       wf::coarse_logit_pitch(ld.n_gen));
+  o = align_up(o + sizeof(float) * rows * wf::coarse_logit_pitch(ld.n_gen));
+  L.al = o;  // fp32 A_L [U, P, d] of a separate streaming launch
+  o = align_up(o + sizeof(float) * rows * ld.head_dim);
   L.idx_l = o;
   o = align_up(o + sizeof(int32_t) * ld.units * (k ? k[ld.levels] : 0));
   L.idx = o;
@@ -457,11 +459,11 @@ int wf_step(const wf_dims* dims, const void* Q, const void* Kp, const void* Vp, 
   float* zl = reinterpret_cast<float*>(ws + L.zl);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // Step 1 runs inside the path kernel when the plan fuses it; otherwise a
-  // separate streaming launch sums the spans and writes each coarse
-  // position's logits against the queries (A_L itself stays on chip).
+  // separate streaming launch writes A_L and then each coarse position's
+  // logits against the queries.
   if (!plan.fuse_dwt) {
-    const cudaError_t e =
-        wf::launch_dwt_lowpass(ld, Kp, nullptr, Q, zl, ld.levels, status_word(workspace), s);
+    const cudaError_t e = wf::launch_dwt_lowpass(ld, Kp, reinterpret_cast<float*>(ws + L.al), Q,
+                                                 zl, ld.levels, status_word(workspace), s);
     if (e != cudaSuccess) return cuda_status(e);
   }
   wf::PathArgs a = {};

@@ -14,10 +14,10 @@
 // the staged rows in fp32: for spans of up to 16 rows one thread owns one
 // (span, 16-byte column chunk) pair; longer spans are summed in 16-row blocks
 // whose partials are combined in a fixed order, with a running sum carried
-// across stages for spans longer than a stage.  Each finished row is either
-// stored (wf_dwt_lowpass: fp32 A_L) or — for the step — turned at once into
-// the row's coarse logits Q·A_L/√d against its unit's queries (the first
-// quantity step 2 scores), so A_L itself never reaches global memory there.
+// across stages for spans longer than a stage; finished rows are stored as
+// fp32 A_L.  For the step, the CTA then turns its rows into coarse logits
+// Q·A_L/√d against their units' queries (the first quantity step 2 scores)
+// while they are still in L2.
 #include <algorithm>
 #include <cmath>
 
@@ -42,10 +42,7 @@ struct DwtSmem {
   static constexpr size_t kRing = 128;
   static constexpr size_t kPart = kRing + static_cast<size_t>(kStages) * kStageBytes;
   static constexpr size_t kCarry = kPart + sizeof(float) * (kRows / 16) * C * V;
-  // Finished A_L rows (fp32, padded pitch) waiting for their coarse logits.
-  static constexpr int kZfPitch = D + 4;
-  static constexpr size_t kZf = kCarry + sizeof(float) * C * V;
-  static constexpr size_t kTotal = kZf + sizeof(float) * 16 * kZfPitch;
+  static constexpr size_t kTotal = kCarry + sizeof(float) * C * V;
 };
 
 template <typename T>
@@ -57,31 +54,58 @@ __device__ __forceinline__ void add_chunk(const unsigned char* p, float* acc) {
   for (int i = 0; i < Elem<T>::kPer16B; ++i) acc[i] += f[i];
 }
 
-// Output of one finished A_L row's V channels (lane layout: C consecutive
-// lanes per row): the fp32 values (`out`, [U, P, D]) or, when `zl` is set,
-// the row's coarse logits zl[(unit P + p) GZ + q] = zscale Q[unit][q]·A_L[p]
-// for the G queries of its unit (warp-collective: every lane calls it).
-template <typename T, int D, int V, int C>
-__device__ __forceinline__ void finish_row(const float* acc, bool active, float scale,
-                                           int64_t span, int c, float* out, const T* q,
-                                           float* zl, int G, int GZ, int64_t P, float zscale) {
-  float a[V];
-#pragma unroll
-  for (int v = 0; v < V; ++v) a[v] = acc[v] * scale;
-  if (zl != nullptr) {
-    const int64_t unit = active ? span / P : 0;
-    const T* q_unit = q + unit * G * D;
-    float* dst = zl + (active ? span : 0) * GZ;
-    if (G <= 32)
-      emit_coarse_logits<T, V, C, (C > 32 ? C : 32)>(a, active, q_unit, D, G, zscale, dst);
-    else
-      emit_coarse_logits<T, V, C, 64>(a, active, q_unit, D, G, zscale, dst);
-    return;
-  }
-  if (!active) return;
+// Stores V channels of one finished A_L row (fp32, [U, P, D]).
+template <int D, int V>
+__device__ __forceinline__ void store_row(const float* acc, float scale, int64_t span, int c,
+                                          float* out) {
   float4* o = reinterpret_cast<float4*>(out + span * D + c * V);
 #pragma unroll
-  for (int v = 0; v < V; v += 4) o[v / 4] = make_float4(a[v], a[v + 1], a[v + 2], a[v + 3]);
+  for (int v = 0; v < V; v += 4)
+    o[v / 4] = make_float4(acc[v] * scale, acc[v + 1] * scale, acc[v + 2] * scale, acc[v + 3] * scale);
+}
+
+// Coarse logits zl[r, q] = zscale Q[unit(r)][q]·A_L[r] of the A_L rows
+// [r_begin, r_end) (global, fp32; unit(r) = r / P), by `workers` of the
+// block's warps (worker w = this warp's index among them).  bf16 queries: 16
+// rows per warp task on the tensor cores (exact three-way split of A_L);
+// fp32 queries: lane groups (C lanes per row) with FMAs.
+template <typename T, int D>
+__device__ __forceinline__ void coarse_logits_range(const float* al, const T* q, float* zl,
+                                                    int64_t r_begin, int64_t r_end, int64_t P,
+                                                    int G, int GZ, float zscale, int64_t worker,
+                                                    int64_t workers) {
+  if constexpr (sizeof(T) == 2) {
+    for (int64_t r0 = r_begin + worker * 16; r0 < r_end; r0 += workers * 16) {
+      const int n = static_cast<int>(r_end - r0 < 16 ? r_end - r0 : 16);
+      for (int64_t u = r0 / P; u * P < r0 + n; ++u) {
+        const int ra = static_cast<int>(u * P > r0 ? u * P - r0 : 0);
+        const int rb = static_cast<int>((u + 1) * P - r0 < n ? (u + 1) * P - r0 : n);
+        coarse_logits_rows16<D>(al + r0 * D, D, n, ra, rb, r0,
+                                reinterpret_cast<const __nv_bfloat16*>(q) + u * G * D, G, GZ,
+                                zscale, zl, 0, 1);
+      }
+    }
+  } else {
+    constexpr int V = Elem<T>::kPer16B, C = D / V, RPW = 32 / C;  // rows per warp pass
+    const int lane = threadIdx.x & 31, c = lane % C;
+    for (int64_t base = r_begin + worker * RPW; base < r_end; base += workers * RPW) {
+      const int64_t row = base + lane / C;
+      const bool act = row < r_end;
+      float a[V];
+#pragma unroll
+      for (int v = 0; v < V; v += 4) {
+        const float4 x = act ? *reinterpret_cast<const float4*>(al + row * D + c * V + v)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        a[v] = x.x; a[v + 1] = x.y; a[v + 2] = x.z; a[v + 3] = x.w;
+      }
+      const int64_t unit = act ? row / P : 0;
+      float* dst = zl + (act ? row : 0) * GZ;
+      if (G <= 32)
+        emit_coarse_logits<T, V, C, 32>(a, act, q + unit * G * D, D, G, zscale, dst);
+      else
+        emit_coarse_logits<T, V, C, 64>(a, act, q + unit * G * D, D, G, zscale, dst);
+    }
+  }
 }
 
 template <typename T, int D>
@@ -102,12 +126,6 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
   unsigned char* ring = smem + S::kRing;
   float* part = reinterpret_cast<float*>(smem + S::kPart);
   float* carry = reinterpret_cast<float*>(smem + S::kCarry);
-  float* zf = reinterpret_cast<float*>(smem + S::kZf);
-  constexpr int ZFP = S::kZfPitch;
-  // bf16 inputs: finished rows are buffered (16 at a time) and their coarse
-  // logits formed on the tensor cores; fp32 inputs use lane-group FMAs.
-  constexpr bool kMmaLogits = sizeof(T) == 2;
-  const bool zmma = kMmaLogits && zl != nullptr;
   const int tid = threadIdx.x;
   const int64_t s_begin = static_cast<int64_t>(blockIdx.x) * spans_per_cta;
   const int64_t s_end = min(n_spans, s_begin + spans_per_cta);
@@ -141,23 +159,6 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
     for (int64_t st = 0; st < issued; ++st)
       if (!(inject && st == 0)) issue(st);
   bool aborted = false;
-  // Coarse logits of the n buffered rows zf[0, n) = spans span_base ..:
-  // warp w forms query tiles w, w + 8 (8 queries each), separately for each
-  // unit the rows belong to.  Block-wide (call between barriers).
-  auto flush = [&](int64_t span_base, int n) {
-    if constexpr (kMmaLogits) {
-      if (n <= 0) return;
-      const int w = tid >> 5;
-      for (int64_t u = span_base / P; u * P < span_base + n; ++u) {
-        const int ra = static_cast<int>(u * P > span_base ? u * P - span_base : 0);
-        const int rb = static_cast<int>((u + 1) * P - span_base < n ? (u + 1) * P - span_base : n);
-        coarse_logits_rows16<D>(zf, ZFP, n, ra, rb, span_base,
-                                reinterpret_cast<const __nv_bfloat16*>(q) + u * G * D, G, GZ,
-                                zscale, zl, w, kWarps);
-      }
-    }
-  };
-
   for (int64_t st = 0; st < issued; ++st) {
     const bool ok = mbar_wait_bounded(&bars[st % kStages], static_cast<uint32_t>((st / kStages) & 1),
                                       status, inject && st == 0 ? inject_polls : kWaitPolls);
@@ -165,33 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
     const unsigned char* buf = ring + (st % kStages) * kStageBytes;
     const int rows_in = static_cast<int>(min(static_cast<int64_t>(SR), rows_total - st * SR));
     const int64_t first_row = st * SR;
-    if (span_rows <= 16 && zmma) {
-      // One thread per (span, chunk) of up to 16 spans at a time; their rows
-      // go to the buffer, then to the tensor cores.
-      const int spans_in = rows_in >> levels;
-      const int64_t span0 = first_row >> levels;
-      for (int g0 = 0; g0 < spans_in; g0 += 16) {
-        const int gn = min(16, spans_in - g0);
-        for (int item = tid; item < gn * C; item += kThreads) {
-          const int sl = item / C, c = item % C;
-          float acc[V];
-#pragma unroll
-          for (int v = 0; v < V; ++v) acc[v] = 0.f;
-          const unsigned char* p = buf + ((g0 + sl) << levels) * RB + c * 16;
-#pragma unroll
-          for (int r = 0; r < 16; ++r)
-            if (r < span_rows) add_chunk<T>(p + r * RB, acc);
-          float4* dst = reinterpret_cast<float4*>(zf + sl * ZFP + c * V);
-#pragma unroll
-          for (int v = 0; v < V; v += 4)
-            dst[v / 4] = make_float4(acc[v] * scale, acc[v + 1] * scale, acc[v + 2] * scale,
-                                     acc[v + 3] * scale);
-        }
-        __syncthreads();
-        flush(s_begin + span0 + g0, gn);
-        __syncthreads();
-      }
-    } else if (span_rows <= 16) {
+    if (span_rows <= 16) {
       // One thread per (span, chunk) of this stage; a stage holds whole spans.
       // Whole warps iterate together (the coarse logits are warp-collective).
       const int spans_in = rows_in >> levels;
@@ -209,8 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
           for (int r = 0; r < 16; ++r)
             if (r < span_rows) add_chunk<T>(p + r * RB, acc);
         }
-        finish_row<T, D, V, C>(acc, act, scale, s_begin + span0 + sl, c, out, q, zl, G, GZ, P,
-                               zscale);
+        if (act) store_row<D, V>(acc, scale, s_begin + span0 + sl, c, out);
       }
     } else {
       // 16-row block partials, then per-span combination in block order.
@@ -230,40 +204,6 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
       const int64_t sp0 = first_row >> levels;
       const int64_t sp1 = (first_row + rows_in - 1) >> levels;
       const int nsp = static_cast<int>(sp1 - sp0 + 1);
-      if (zmma) {
-        // Spans finished in this stage (all but possibly the last), 16 at a
-        // time: rows to the buffer, then to the tensor cores.
-        const bool last_open = ((sp1 + 1) << levels) > first_row + rows_in;
-        for (int g0 = 0; g0 < nsp; g0 += 16) {
-          const int gn = min(16, nsp - g0);
-          for (int item = tid; item < gn * C; item += kThreads) {
-            const int sl = g0 + item / C, c = item % C;
-            const int64_t span = sp0 + sl;
-            const int64_t r_lo = max(span << levels, first_row);
-            const int64_t r_hi = min((span + 1) << levels, first_row + rows_in);
-            const bool carried = (span << levels) < first_row;
-            float acc[V];
-#pragma unroll
-            for (int v = 0; v < V; ++v) acc[v] = carried ? carry[c * V + v] : 0.f;
-            for (int b = static_cast<int>((r_lo - first_row) / 16); b < (r_hi - first_row) / 16; ++b)
-#pragma unroll
-              for (int v = 0; v < V; ++v) acc[v] += part[(b * C + c) * V + v];
-            if (((span + 1) << levels) <= first_row + rows_in) {
-              float4* dst = reinterpret_cast<float4*>(zf + (item / C) * ZFP + c * V);
-#pragma unroll
-              for (int v = 0; v < V; v += 4)
-                dst[v / 4] = make_float4(acc[v] * scale, acc[v + 1] * scale, acc[v + 2] * scale,
-                                         acc[v + 3] * scale);
-            } else {
-#pragma unroll
-              for (int v = 0; v < V; ++v) carry[c * V + v] = acc[v];
-            }
-          }
-          __syncthreads();
-          flush(s_begin + sp0 + g0, gn - (last_open && g0 + gn == nsp ? 1 : 0));
-          __syncthreads();
-        }
-      } else
       for (int base = 0; base < nsp * C; base += kThreads) {  // whole warps together
         const int item = base + tid;
         const bool in = item < nsp * C;
@@ -288,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
             for (int v = 0; v < V; ++v) carry[c * V + v] = acc[v];
           }
         }
-        finish_row<T, D, V, C>(acc, done, scale, s_begin + span, c, out, q, zl, G, GZ, P, zscale);
+        if (done) store_row<D, V>(acc, scale, s_begin + span, c, out);
       }
     }
     __syncthreads();  // stage consumed (and carry / partials settled)
@@ -299,6 +239,12 @@ __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __rest
       }
       ++issued;
     }
+  }
+  // With queries: the coarse logits of this CTA's rows, from the A_L rows it
+  // has just written (L2), by all warps.
+  if (zl != nullptr) {
+    __syncthreads();
+    coarse_logits_range<T, D>(out, q, zl, s_begin, s_end, P, G, GZ, zscale, tid >> 5, kWarps);
   }
 }
 
@@ -330,47 +276,15 @@ __global__ void __launch_bounds__(kThreads) coarse_logits_kernel(const float* __
                                                                  float* __restrict__ zl,
                                                                  int64_t rows_total, int64_t P,
                                                                  int G, int GZ, float zscale) {
-  if constexpr (sizeof(T) == 2) {
-    // One warp per 16-row block on the tensor cores.
-    const int64_t warp_g = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-    for (int64_t r0 = warp_g * 16; r0 < rows_total; r0 += static_cast<int64_t>(gridDim.x) * kWarps * 16) {
-      const int n = static_cast<int>(rows_total - r0 < 16 ? rows_total - r0 : 16);
-      for (int64_t u = r0 / P; u * P < r0 + n; ++u) {
-        const int ra = static_cast<int>(u * P > r0 ? u * P - r0 : 0);
-        const int rb = static_cast<int>((u + 1) * P - r0 < n ? (u + 1) * P - r0 : n);
-        coarse_logits_rows16<D>(al + r0 * D, D, n, ra, rb, r0,
-                                reinterpret_cast<const __nv_bfloat16*>(q) + u * G * D, G, GZ,
-                                zscale, zl, 0, 1);
-      }
-    }
-    return;
-  }
-  constexpr int V = Elem<T>::kPer16B, C = D / V, RPP = kThreads / C;  // rows per pass
-  const int tid = threadIdx.x, c = tid % C;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPP; base < rows_total;
-       base += static_cast<int64_t>(gridDim.x) * RPP) {  // uniform over the block
-    const int64_t row = base + tid / C;
-    const bool act = row < rows_total;
-    float a[V];
-#pragma unroll
-    for (int v = 0; v < V; v += 4) {
-      const float4 x = act ? __ldg(reinterpret_cast<const float4*>(al + row * D + c * V + v))
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-      a[v] = x.x; a[v + 1] = x.y; a[v + 2] = x.z; a[v + 3] = x.w;
-    }
-    const int64_t unit = act ? row / P : 0;
-    float* dst = zl + (act ? row : 0) * GZ;
-    if (G <= 32)
-      emit_coarse_logits<T, V, C, 32>(a, act, q + unit * G * D, D, G, zscale, dst);
-    else
-      emit_coarse_logits<T, V, C, 64>(a, act, q + unit * G * D, D, G, zscale, dst);
-  }
+  coarse_logits_range<T, D>(al, q, zl, 0, rows_total, P, G, GZ, zscale,
+                            static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5),
+                            static_cast<int64_t>(gridDim.x) * kWarps);
 }
 
 template <typename T, int D>
 cudaError_t launch_logits_typed(const LaunchDims& ld, const float* al, const void* q, float* zl,
                                 cudaStream_t stream) {
-  constexpr int RPP = sizeof(T) == 2 ? kWarps * 16 : kThreads / (D / Elem<T>::kPer16B);
+  constexpr int RPP = kWarps * (sizeof(T) == 2 ? 16 : 32 / (D / Elem<T>::kPer16B));
   const int64_t P = ld.n_prompt >> ld.levels;
   const int64_t rows = ld.units * P;
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((rows + RPP - 1) / RPP,

@@ -82,8 +82,8 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
                int sm_count, PathPlan* plan);
 
 // Streams Kp once and writes its level-`levels` Haar approximation as fp32
-// to `out` [U, N_p/2^levels, d], or (zl != nullptr; levels = ld.levels) the
-// coarse logits of every row against the unit's queries `q` to zl
+// to `out` [U, N_p/2^levels, d]; if zl != nullptr (levels = ld.levels), then
+// also the coarse logits of every row against the unit's queries `q` to zl
 // [U, P, coarse_logit_pitch(G)] in the log2 domain.
 cudaError_t launch_dwt_lowpass(const LaunchDims& ld, const void* kp, float* out, const void* q,
                                float* zl, int levels, int32_t* status, cudaStream_t stream);

@@ -171,13 +171,18 @@ struct PathSmem {
       f_kst = f_t = 0;
       const size_t ring_b = static_cast<size_t>(p.f_stages) * D * 256;
       const size_t gath_b = p.gather_all ? sizeof(uint32_t) * 2 * static_cast<size_t>(p.cs) * p.rows_cap : 0;
+      // The distributed selection's flags and survivor list are formed after
+      // the last tile has been consumed, so they overlay the ring as well.
       const bool overlay = p.filter_fast == 1;
-      f_ring = take_bytes(overlay && gath_b > ring_b ? gath_b : ring_b, 1024);
+      const size_t sel_b = static_cast<size_t>(p.rows_cap) * (sizeof(int32_t) + 1);
+      size_t ring_sz = ring_b > sel_b ? ring_b : sel_b;
+      if (overlay && gath_b > ring_sz) ring_sz = gath_b;
+      f_ring = take_bytes(ring_sz, 1024);
       f_gather = overlay ? f_ring : (gath_b ? take_bytes(gath_b) : 0);
+      sp = f_ring;
+      take = f_ring + sizeof(int32_t) * static_cast<size_t>(p.rows_cap);
       f_stage = take_bytes(sizeof(float) * 128 * static_cast<size_t>(p.GZ + 4));
       keys = take_bytes(sizeof(uint32_t) * p.rows_cap);
-      take = take_bytes(p.rows_cap);
-      sp = take_bytes(sizeof(int32_t) * p.rows_cap);
       f_bars = take_bytes(sizeof(uint64_t) * (p.f_stages + 2 * p.f_nb), 8);
       end = end > o ? end : o;
     } else if (p.mode & kModeFilter) {
