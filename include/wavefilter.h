@@ -148,6 +148,8 @@ typedef struct {
                             distributed over the cluster                             */
   int32_t token_logits;  /* WF_LOGITS_*                                              */
   int32_t smem_bytes;    /* dynamic shared memory per CTA of the path kernel         */
+  int32_t filter_stages; /* key tiles in flight in the filter                        */
+  int32_t attend_stages; /* key/value tiles in flight in the attention               */
 } wf_plan;
 
 /* Fills *plan with the launch plan wf_step uses for these sizes on the

@@ -44,7 +44,8 @@ class WfError(RuntimeError):
 class Plan(ctypes.Structure):
     _fields_ = [("launches", ctypes.c_int32), ("cluster", ctypes.c_int32),
                 ("final_gather", ctypes.c_int32), ("token_logits", ctypes.c_int32),
-                ("smem_bytes", ctypes.c_int32)]
+                ("smem_bytes", ctypes.c_int32), ("filter_stages", ctypes.c_int32),
+                ("attend_stages", ctypes.c_int32)]
 
 
 LOGITS_NAMES = {0: "shared", 1: "workspace", 2: "tensor_memory", 3: "recomputed"}
@@ -194,7 +195,8 @@ def step_plan(dims: Dims, k: Sequence[int]) -> dict:
     _check("wf_step_plan", lib().wf_step_plan(ctypes.byref(dims), _k_array(k), ctypes.byref(p)))
     return {"launches": p.launches, "cluster": p.cluster, "final_gather": p.final_gather,
             "token_logits": LOGITS_NAMES.get(p.token_logits, p.token_logits),
-            "smem_bytes": p.smem_bytes}
+            "smem_bytes": p.smem_bytes, "filter_stages": p.filter_stages,
+            "attend_stages": p.attend_stages}
 
 
 def inject_wait_timeout(polls: int) -> None:

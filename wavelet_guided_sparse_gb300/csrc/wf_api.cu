@@ -240,6 +240,8 @@ int wf_step_plan(const wf_dims* dims, const int32_t* k_per_level, wf_plan* out) 
                       : plan.t_in_smem        ? WF_LOGITS_SHARED
                                               : WF_LOGITS_WORKSPACE;
   out->smem_bytes = static_cast<int32_t>(plan.smem_bytes);
+  out->filter_stages = plan.f_stages;
+  out->attend_stages = plan.a_stages;
   return WF_OK;
 }
 

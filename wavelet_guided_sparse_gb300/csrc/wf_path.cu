@@ -181,8 +181,12 @@ struct PathSmem {
       f_gather = overlay ? f_ring : (gath_b ? take_bytes(gath_b) : 0);
       sp = f_ring;
       take = f_ring + sizeof(int32_t) * static_cast<size_t>(p.rows_cap);
-      f_stage = take_bytes(sizeof(float) * 128 * static_cast<size_t>(p.GZ + 4));
-      keys = take_bytes(sizeof(uint32_t) * p.rows_cap);
+      // The statistics pass's staging tile is done before the scores are
+      // formed: the row scores share its bytes.
+      const size_t stage_b = sizeof(float) * 128 * static_cast<size_t>(p.GZ + 4);
+      const size_t keys_b = sizeof(uint32_t) * static_cast<size_t>(p.rows_cap);
+      f_stage = take_bytes(stage_b > keys_b ? stage_b : keys_b);
+      keys = f_stage;
       f_bars = take_bytes(sizeof(uint64_t) * (p.f_stages + 2 * p.f_nb), 8);
       end = end > o ? end : o;
     } else if (p.mode & kModeFilter) {
@@ -1820,17 +1824,28 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
     const bool f_res = f_ntl * n_cols <= 512;
     const int f_nb = f_res ? f_ntl : std::min(4, 512 / n_cols);
     const int s_want = std::min(std::min(4, f_ntl), f_nb);
-    // The fast filter keeps the all-gather selection while a ring of two
-    // tiles fits; the general path prefers deeper rings first.
+    // The fast filter prefers the all-gather selection, then the deepest
+    // tile ring, then the deepest attention ring (the phases share one
+    // region, so the two depths are independent); the general path trades
+    // ring depth against the all-gather.
     for (int ff = fast_sched ? 1 : 0; ff >= 0 && !found; --ff)
     for (int fz = fuse_try ? 1 : 0; fz >= 0 && !found; --fz)
-    for (int it = 0; it < 10 && !found; ++it) {
-      const int depth = ff ? (it < 5 ? std::min(it, std::max(0, s_want - 2)) : it - 5) : it >> 1;
-      const int ga = ff ? (it < 5 ? 1 : 0) : 1 - (it & 1);
+    for (int it = 0; it < (ff ? 2 * 4 * 5 : 10) && !found; ++it) {
+      int ga, fs, as;
+      if (ff) {
+        ga = 1 - it / 20;
+        fs = std::max(1, s_want - (it % 20) / 5);
+        as = std::max(2, a_want - it % 5);
+        if (ga && fs < std::min(2, s_want)) continue;  // no all-gather at the cost of a serial ring
+      } else {
+        ga = 1 - (it & 1);
+        fs = std::max(2, f_want - (it >> 1));
+        as = std::max(2, a_want - (it >> 1));
+      }
       p.filter_fast = ff ? (f_res ? 1 : 2) : 0;
       p.f_nb = ff ? f_nb : 0;
-      p.f_stages = ff ? std::max(1, s_want - depth) : std::max(2, f_want - depth);
-      p.a_stages = std::max(2, a_want - depth);
+      p.f_stages = fs;
+      p.a_stages = as;
       if (ga && (!(mode & kModeFilter) || static_cast<int64_t>(cs) * p.rows_cap > 8192)) continue;
       p.gather_all = ga;
       p.fuse_dwt = fz;
