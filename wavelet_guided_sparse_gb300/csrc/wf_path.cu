@@ -384,6 +384,174 @@ __device__ __forceinline__ int prompt_row(const PathParams& p, int mode, const C
   return (row >= 0 && row < p.n_prompt) ? row : -1;
 }
 
+// Key slots of one CTA's attention: slot g < B is prompt row idx[g] (the
+// filter's list or the caller's), B <= g < n_keys generation row g - B.
+template <typename T>
+struct AttnRows {
+  const T *kg, *vg, *kp, *vp;  // this unit's rows
+  const int32_t* klist;
+  int k0, k1, B;               // this CTA's slots [k0, k1)
+};
+
+template <typename T>
+__device__ __forceinline__ bool attn_key_valid(const PathParams& p, int mode, const Ctx& c,
+                                               const AttnRows<T>& ar, int g) {
+  if (g >= ar.k1) return false;
+  if (g >= ar.B) return true;
+  return prompt_row(p, mode, c, ar.klist, ar.k0, g) >= 0;
+}
+
+// Gathers the key and value rows of slots [k0 + tile TK, ...) into ring stage
+// `stage` by 16-byte cp.async (one commit group; all threads).
+template <typename T, int D>
+__device__ __forceinline__ void attn_issue(const PathParams& p, int mode, const Ctx& c,
+                                           const AttnRows<T>& ar, unsigned char* kst,
+                                           unsigned char* vst, int TK, int tile, int stage) {
+  constexpr int C16 = D * static_cast<int>(sizeof(T)) / 16;
+  constexpr int RB = PathSmem<T, D>::kRowBytes;
+  const int base = ar.k0 + tile * TK;
+  for (int e = threadIdx.x; e < TK * C16; e += kThreads) {
+    const int i = e / C16, ch = e % C16;
+    const int g = base + i;
+    const T* ks = ar.kg;
+    const T* vs = ar.vg;
+    if (g < ar.k1) {
+      if (g >= ar.B) {
+        ks = ar.kg + static_cast<int64_t>(g - ar.B) * D;
+        vs = ar.vg + static_cast<int64_t>(g - ar.B) * D;
+      } else {
+        const int row = prompt_row(p, mode, c, ar.klist, ar.k0, g);
+        if (row >= 0) {
+          ks = ar.kp + static_cast<int64_t>(row) * D;
+          vs = ar.vp + static_cast<int64_t>(row) * D;
+        }
+      }
+    }
+    cp_async16(kst + (stage * TK + i) * RB + ch * 16, reinterpret_cast<const unsigned char*>(ks) + ch * 16);
+    cp_async16(vst + (stage * TK + i) * RB + ch * 16, reinterpret_cast<const unsigned char*>(vs) + ch * 16);
+  }
+  cp_async_commit();
+}
+
+// Producer of the fast filter (one thread): fills a ring of S 128-row tiles
+// by 2-D tensor copies (whole spans of the coarse survivors, 128-byte
+// swizzle) and issues one tcgen05.mma pass per tile into tensor-memory slot
+// g % NB (N columns each), committing to done[slot]; a slot is reused once
+// the consumers released it (empty[slot]).  Tiles g >= ntiles are the second
+// pass over the same rows.  Every wait is bounded; on a timeout the producer
+// stops issuing, sets *abort, waits (bounded) for the copies it issued and
+// the last multiply, and returns.
+template <int D>
+struct FilterProducer {
+  static constexpr int TR = 128;
+  static constexpr int kStageBytes = D * 256;
+  unsigned char* ring;
+  uint64_t *full, *done;
+  const void* tmap;
+  const int32_t* sl;
+  const unsigned char* qs;
+  int32_t* status;
+  volatile int32_t* abort;
+  uint32_t tmem;
+  int s0, levels, row_base, R, ntiles, total, S, NB, N;
+  int next_tma = 0, g_mma = 0, g_full = 0;
+  bool ok = true;
+
+  __device__ __forceinline__ void copy_tile(int g) {
+    const int t = g % ntiles, st = g % S;
+    const int box_rows = min(1 << levels, TR);
+    const int rows = min(TR, R - t * TR);
+    mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(rows) * D * 2);
+    for (int b = 0; b * box_rows < rows; ++b) {
+      const int lr = t * TR + b * box_rows;
+      const int y = row_base + (sl[s0 + (lr >> levels)] << levels) + (lr & ((1 << levels) - 1));
+      for (int kb = 0; kb < D / 64; ++kb)
+        tma_load_2d(ring + st * kStageBytes + kb * (TR * 128) + b * box_rows * 128, tmap, kb * 64,
+                    y, &full[st]);
+    }
+  }
+
+  __device__ __forceinline__ void run(int g_end) {
+    if (next_tma == 0)
+      for (; next_tma < min(S, total); ++next_tma) copy_tile(next_tma);
+    const uint32_t q0 = smem_u32(qs);
+    const uint32_t idesc = umma_idesc_bf16(TR, N);
+    int g = g_mma;
+    for (; ok && g < g_end; ++g) {
+      const int st = g % S, slot = g % NB;
+      ok = mbar_wait_bounded(&full[st], static_cast<uint32_t>((g / S) & 1), status);
+      if (!ok) break;
+      g_full = g + 1;
+      if (g >= NB) ok = mbar_wait_bounded(&empty_bar(slot), static_cast<uint32_t>(((g / NB) - 1) & 1), status);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(ring + st * kStageBytes);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks)
+        umma_bf16(tmem + slot * N, umma_desc_sw128(a0 + ((ks * 16) >> 6) * (TR * 128) + ((ks * 16) & 63) * 2),
+                  umma_desc(q0 + ks * 256, 128, D * 16), idesc, ks != 0);
+      umma_commit(&done[slot]);
+      // Refill a stage once the multiply that read it has finished: that of
+      // tile g - 1 (so tile g's multiply is queued behind it meanwhile), or
+      // with a single stage that of tile g itself.
+      const int j = S > 1 ? g - 1 : g;
+      if (j >= 0 && j + S < total) {
+        ok = mbar_wait_bounded(&done[j % NB], static_cast<uint32_t>((j / NB) & 1), status);
+        if (!ok) {
+          ++g;
+          break;
+        }
+        copy_tile(next_tma++);  // tile j + S into stage j % S
+      }
+    }
+    g_mma = g;
+    if (!ok) {
+      *abort = 1;
+      for (int h = g_full; h < next_tma; ++h)
+        (void)mbar_wait_bounded(&full[h % S], static_cast<uint32_t>((h / S) & 1), status);
+      if (g_mma > 0)
+        (void)mbar_wait_bounded(&done[(g_mma - 1) % NB], static_cast<uint32_t>(((g_mma - 1) / NB) & 1),
+                                status);
+      g_full = next_tma;
+    }
+  }
+  __device__ __forceinline__ uint64_t& empty_bar(int slot) { return done[NB + slot]; }
+};
+
+// Token position of row `row` of a CTA's span rows (survivor spans
+// sl[s0 ..], 2^levels rows each).
+__device__ __forceinline__ int span_token(const int32_t* sl, int s0, int row, int levels) {
+  return (sl[s0 + (row >> levels)] << levels) + (row & ((1 << levels) - 1));
+}
+
+// The N (16..64) accumulator columns of this thread's tensor-memory lane at
+// taddr, into registers v[0, N).  Warp-collective.
+__device__ __forceinline__ void tmem_read_row(uint32_t taddr, int N, float (&v)[kMaxQ]) {
+  uint32_t r[4][16];
+  tmem_ld16_nowait(taddr, r[0]);
+  if (N > 16) tmem_ld16_nowait(taddr + 16, r[1]);
+  if (N > 32) {
+    tmem_ld16_nowait(taddr + 32, r[2]);
+    tmem_ld16_nowait(taddr + 48, r[3]);
+  }
+  tmem_wait_ld();
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[c * 16 + i] = c * 16 < N ? __uint_as_float(r[c][i]) : 0.f;
+}
+
+// Attention mass of one token: Σ_q 2^(v_q sc2 - gm_q) / sum_q over the G
+// queries (four partial sums, fixed order).
+__device__ __forceinline__ float token_score(const float (&v)[kMaxQ], int G, float sc2,
+                                             const float* gm, const float* ginv) {
+  float sq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int q = 0; q < kMaxQ; ++q)
+    if (q < G) sq[q & 3] += exp2f(v[q] * sc2 - gm[q]) * ginv[q];
+  return (sq[0] + sq[1]) + (sq[2] + sq[3]);
+}
+
 // ============================================================== the kernel
 template <typename T, int D, bool kFast>
 __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant__ PathParams p) {
@@ -771,9 +939,6 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       uint64_t* empty = done + NB;
       volatile int32_t* fabort = misc + 6;
       const float sc2 = p.scale[0] * kLog2e;
-      auto pos_of = [&](int row) {
-        return (sl_all[s0 + (row >> levels)] << levels) + (row & ((1 << levels) - 1));
-      };
       if (tid == 0) {
         for (int i = 0; i < S; ++i) mbar_init(&full[i], 1);
         for (int i = 0; i < NB; ++i) {
@@ -791,98 +956,17 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       __syncthreads();
       tc_fence_after();
 
-      // ---- producer state (thread 0): next tile to copy, next tile to multiply
-      int next_tma = 0, g_mma = 0, g_full = 0;
-      bool p_ok = true;
-      auto tile_tma = [&](int g) {
-        const int t = g % ntiles, st = g % S;
-        const int rows = min(TR, R - t * TR);
-        mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(rows) * D * 2);
-        for (int b = 0; b * box_rows < rows; ++b) {
-          const int lr = t * TR + b * box_rows;
-          const int y = static_cast<int>(unit * p.n_prompt) + (sl_all[s0 + (lr >> levels)] << levels) +
-                        (lr & ((1 << levels) - 1));
-          for (int kb = 0; kb < D / 64; ++kb)
-            tma_load_2d(ring + st * kStageBytes + kb * (TR * 128) + b * box_rows * 128, &p.tmap_spans,
-                        kb * 64, y, &full[st]);
-        }
-      };
-      auto produce = [&](int g_end) {  // thread 0
-        if (next_tma == 0) {
-          for (; next_tma < min(S, total); ++next_tma) tile_tma(next_tma);
-        }
-        const uint32_t q0 = smem_u32(qs);
-        const uint32_t idesc = umma_idesc_bf16(TR, N);
-        for (; p_ok && g_mma < g_end; ++g_mma) {
-          const int g = g_mma, st = g % S, slot = g % NB;
-          p_ok = mbar_wait_bounded(&full[st], static_cast<uint32_t>((g / S) & 1), p.status);
-          if (!p_ok) break;
-          g_full = g + 1;
-          if (g >= NB)
-            p_ok = mbar_wait_bounded(&empty[slot], static_cast<uint32_t>(((g / NB) - 1) & 1), p.status);
-          if (!p_ok) break;
-          tc_fence_after();
-          const uint32_t a0 = smem_u32(ring + st * kStageBytes);
-          for (int ks = 0; ks < D / 16; ++ks)
-            umma_bf16(tmem + slot * N,
-                      umma_desc_sw128(a0 + ((ks * 16) >> 6) * (TR * 128) + ((ks * 16) & 63) * 2),
-                      umma_desc(q0 + ks * 256, 128, D * 16), idesc, ks != 0);
-          umma_commit(&done[slot]);
-          // Refill a stage once the multiply that read it has finished: that of
-          // tile g - 1 (so tile g's multiply is queued behind it meanwhile), or
-          // with a single stage that of tile g itself.
-          const int j = S > 1 ? g - 1 : g;
-          if (j >= 0 && j + S < total) {
-            p_ok = mbar_wait_bounded(&done[j % NB], static_cast<uint32_t>((j / NB) & 1), p.status);
-            if (!p_ok) {
-              ++g_mma;
-              break;
-            }
-            tile_tma(next_tma++);  // tile j + S into stage j % S
-          }
-        }
-        if (!p_ok) {
-          // Give up cleanly: no new work; every copy issued lands and the
-          // last multiply issued finishes before the shared memory and the
-          // tensor memory are reused (bounded waits).
-          *fabort = 1;
-          for (int g = g_full; g < next_tma; ++g)
-            (void)mbar_wait_bounded(&full[g % S], static_cast<uint32_t>((g / S) & 1), p.status);
-          if (g_mma > 0)
-            (void)mbar_wait_bounded(&done[(g_mma - 1) % NB],
-                                    static_cast<uint32_t>(((g_mma - 1) / NB) & 1), p.status);
-          g_full = next_tma;
-        }
-      };
-      // Reads the N accumulator columns of this thread's row of slot `slot`.
-      auto read_acc = [&](int slot, float (&v)[kMaxQ]) {
-        uint32_t r[4][16];
-        const uint32_t ta = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + slot * N;
-        tmem_ld16_nowait(ta, r[0]);
-        if (N > 16) tmem_ld16_nowait(ta + 16, r[1]);
-        if (N > 32) {
-          tmem_ld16_nowait(ta + 32, r[2]);
-          tmem_ld16_nowait(ta + 48, r[3]);
-        }
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[c * 16 + i] = __uint_as_float(r[c][i]);
-      };
-      auto row_score = [&](const float (&v)[kMaxQ]) {
-        float sq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int q = 0; q < kMaxQ; ++q)
-          if (q < G) sq[q & 3] += exp2f(v[q] * sc2 - gm[q]) * ginv[q];
-        return (sq[0] + sq[1]) + (sq[2] + sq[3]);
-      };
+      // ---- producer (thread 0): next tile to copy, next tile to multiply
+      FilterProducer<D> prod{ring, full, done, &p.tmap_spans, sl_all, qs, p.status, fabort, tmem,
+                             s0, levels, static_cast<int>(unit * p.n_prompt), R, ntiles, total, S,
+                             NB, N};
+      const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
       const int row_l = (warp & 3) * 32 + lane;
 
       // ---- pass A: statistics
       float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
       if (warp == 0) {
-        if (lane == 0) produce(resident ? total : min(total, ntiles + NB));
+        if (lane == 0) prod.run(resident ? total : min(total, ntiles + NB));
         __syncwarp();
       } else if (warp >= 4) {
         const int qw = warp & 3;
@@ -895,7 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           const int rows_valid = min(TR, R - t * TR);
           if (okc) {
             float v[kMaxQ];
-            read_acc(slot, v);
+            tmem_read_row(t_lane + slot * N, N, v);
             if (row_l < rows_valid) {
               float* dst = fst + row_l * ZT2;
 #pragma unroll
@@ -953,13 +1037,13 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         if (warp >= 4 && *fabort == 0) {
           for (int t = 0; t < ntiles; ++t) {
             float v[kMaxQ];
-            read_acc(t, v);
+            tmem_read_row(t_lane + t * N, N, v);
             const int row = t * TR + row_l;
-            if (row < R) keys[row] = __float_as_uint(row_score(v));
+            if (row < R) keys[row] = __float_as_uint(token_score(v, G, sc2, gm, ginv));
           }
         }
       } else if (warp == 0) {
-        if (lane == 0) produce(total);
+        if (lane == 0) prod.run(total);
         __syncwarp();
       } else if (warp >= 4) {
         for (int t = 0; t < ntiles; ++t) {
@@ -970,9 +1054,9 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           tc_fence_after();
           if (okc) {
             float v[kMaxQ];
-            read_acc(slot, v);
+            tmem_read_row(t_lane + slot * N, N, v);
             const int row = t * TR + row_l;
-            if (row < R) keys[row] = __float_as_uint(row_score(v));
+            if (row < R) keys[row] = __float_as_uint(token_score(v, G, sc2, gm, ginv));
           }
           tc_fence_before();
           __syncwarp();
@@ -998,7 +1082,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         for (int e = tid; e < R * cs; e += kThreads) {
           const int i = e % R, r = e / R;
           peer(gkeys, r)[off + i] = keys[i];
-          peer(gpos, r)[off + i] = pos_of(i);
+          peer(gpos, r)[off + i] = span_token(sl_all, s0, i, levels);
         }
         cluster.sync();
         if (mode & kModeAttend) {
@@ -1024,7 +1108,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           const int tf = i < R ? take[i] : 0;
           int tot;
           const int at = block_excl_scan(tf, tk.scan, &tot);
-          if (tf) sp[carry + at] = pos_of(i);
+          if (tf) sp[carry + at] = span_token(sl_all, s0, i, levels);
           carry += tot;
         }
         __syncthreads();
@@ -1333,41 +1417,10 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     }
     // Every slot of a tile is filled (invalid slots with a finite dummy row),
     // so masked probabilities multiply finite values.
-    constexpr int C16 = D * static_cast<int>(sizeof(T)) / 16;
-    auto issue = [&](int tile, int stage) {  // all threads; one cp.async group
-      const int base = k0 + tile * TK;
-      for (int e = tid; e < TK * C16; e += kThreads) {
-        const int i = e / C16, ch = e % C16;
-        const int g = base + i;
-        const T* ks = kgp;
-        const T* vs = vgp;
-        if (g < k1) {
-          if (g >= B) {
-            ks = kgp + static_cast<int64_t>(g - B) * D;
-            vs = vgp + static_cast<int64_t>(g - B) * D;
-          } else {
-            const int row = prompt_row(p, mode, c, klist, k0, g);
-            if (row >= 0) {
-              ks = kpp + static_cast<int64_t>(row) * D;
-              vs = vpp + static_cast<int64_t>(row) * D;
-            }
-          }
-        }
-        cp_async16(kst + (stage * TK + i) * RB + ch * 16,
-                   reinterpret_cast<const unsigned char*>(ks) + ch * 16);
-        cp_async16(vst + (stage * TK + i) * RB + ch * 16,
-                   reinterpret_cast<const unsigned char*>(vs) + ch * 16);
-      }
-      cp_async_commit();
-    };
+    const AttnRows<T> ar{kgp, vgp, kpp, vpp, klist, k0, k1, B};
     __syncthreads();  // filter-phase readers of the union are done
     const int AS = p.a_stages;
-    for (int tl = 0; tl < AS && tl < ntiles; ++tl) issue(tl, tl);
-    auto valid = [&](int g) -> bool {
-      if (g >= k1) return false;
-      if (g >= B) return true;
-      return prompt_row(p, mode, c, klist, k0, g) >= 0;
-    };
+    for (int tl = 0; tl < AS && tl < ntiles; ++tl) attn_issue<T, D>(p, mode, c, ar, kst, vst, TK, tl, tl);
 
     if constexpr (sizeof(T) == 2) {
       const int MB = G <= 16 ? 1 : (G <= 32 ? 2 : 4);
@@ -1410,7 +1463,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const bool v = valid(jbase + nb * 8 + e);
+            const bool v = attn_key_valid(p, mode, c, ar, jbase + nb * 8 + e);
             s[nb][e] = v ? s[nb][e] * p.scale_log2 : -INFINITY;
             s[nb][e + 2] = v ? s[nb][e + 2] * p.scale_log2 : -INFINITY;
             mx_lo = fmaxf(mx_lo, s[nb][e]);
@@ -1460,7 +1513,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           mma_bf16(oacc[dn + 1], pa, b + 2);
         }
         __syncthreads();
-        if (tile + AS < ntiles) issue(tile + AS, stage);
+        if (tile + AS < ntiles) attn_issue<T, D>(p, mode, c, ar, kst, vst, TK, tile + AS, stage);
       }
       // Warp partials -> shared memory (overwrites the stages).
       // Row pitch D + 8 floats: a warp's fragment stores (8 rows x 4 column
@@ -1551,7 +1604,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         const float* vb = reinterpret_cast<const float*>(vst + stage * TK * RB);
         {
           const int kk = tid & 31, g = tid >> 5;
-          const bool v = valid(k0 + tile * TK + kk);
+          const bool v = attn_key_valid(p, mode, c, ar, k0 + tile * TK + kk);
           for (int qi = g; qi < G; qi += 8) {
             float acc = 0.f;
             for (int col = 0; col < D; col += 4) {
@@ -1603,7 +1656,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           }
         }
         __syncthreads();
-        if (tile + AS < ntiles) issue(tile + AS, stage);
+        if (tile + AS < ntiles) attn_issue<T, D>(p, mode, c, ar, kst, vst, TK, tile + AS, stage);
       }
       __syncthreads();  // the receive area shares no bytes with what peers still use
       const int c4 = tid % C4, qg = tid / C4;
