@@ -524,32 +524,41 @@ __device__ __forceinline__ int span_token(const int32_t* sl, int s0, int row, in
   return (sl[s0 + (row >> levels)] << levels) + (row & ((1 << levels) - 1));
 }
 
-// The N (16..64) accumulator columns of this thread's tensor-memory lane at
-// taddr, into registers v[0, N).  Warp-collective.
-__device__ __forceinline__ void tmem_read_row(uint32_t taddr, int N, float (&v)[kMaxQ]) {
-  uint32_t r[4][16];
-  tmem_ld16_nowait(taddr, r[0]);
-  if (N > 16) tmem_ld16_nowait(taddr + 16, r[1]);
-  if (N > 32) {
-    tmem_ld16_nowait(taddr + 32, r[2]);
-    tmem_ld16_nowait(taddr + 48, r[3]);
+// Attention mass of the token whose logits sit in this thread's tensor-memory
+// lane at taddr (N columns, the G queries first): Σ_q 2^(v_q sc2 - gm_q) /
+// sum_q, with four partial sums in a fixed order.  Sixteen columns per
+// iteration keep the loop body (and the code to fetch) small.
+// Warp-collective.
+__device__ __forceinline__ float token_score_tmem(uint32_t taddr, int N, int G, float sc2,
+                                                  const float* gm, const float* ginv) {
+  float sq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+  for (int c = 0; c < N; c += 16) {
+    float v[16];
+    tmem_ld16(taddr + c, v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int q = c + i;
+      if (q < G) sq[i & 3] += exp2f(v[i] * sc2 - gm[q]) * ginv[q];
+    }
   }
-  tmem_wait_ld();
-#pragma unroll
-  for (int c = 0; c < 4; ++c)
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[c * 16 + i] = c * 16 < N ? __uint_as_float(r[c][i]) : 0.f;
+  return (sq[0] + sq[1]) + (sq[2] + sq[3]);
 }
 
-// Attention mass of one token: Σ_q 2^(v_q sc2 - gm_q) / sum_q over the G
-// queries (four partial sums, fixed order).
-__device__ __forceinline__ float token_score(const float (&v)[kMaxQ], int G, float sc2,
-                                             const float* gm, const float* ginv) {
-  float sq[4] = {0.f, 0.f, 0.f, 0.f};
+// Copies the first `cols` (a multiple of 4) logits of this thread's lane at
+// taddr to dst (fp32, 16-byte aligned) if `store`.  Warp-collective.
+__device__ __forceinline__ void tmem_row_to_smem(uint32_t taddr, int N, int cols, bool store,
+                                                 float* dst) {
+#pragma unroll 1
+  for (int c = 0; c < N; c += 16) {
+    float v[16];
+    tmem_ld16(taddr + c, v);
+    if (store) {
 #pragma unroll
-  for (int q = 0; q < kMaxQ; ++q)
-    if (q < G) sq[q & 3] += exp2f(v[q] * sc2 - gm[q]) * ginv[q];
-  return (sq[0] + sq[1]) + (sq[2] + sq[3]);
+      for (int i = 0; i < 16; i += 4)
+        if (c + i < cols) *reinterpret_cast<float4*>(dst + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    }
+  }
 }
 
 // ============================================================== the kernel
@@ -977,16 +986,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           okc = __all_sync(0xffffffffu, okc);
           tc_fence_after();
           const int rows_valid = min(TR, R - t * TR);
-          if (okc) {
-            float v[kMaxQ];
-            tmem_read_row(t_lane + slot * N, N, v);
-            if (row_l < rows_valid) {
-              float* dst = fst + row_l * ZT2;
-#pragma unroll
-              for (int q = 0; q < kMaxQ; q += 4)
-                if (q < p.GZ) *reinterpret_cast<float4*>(dst + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
-            }
-          }
+          if (okc) tmem_row_to_smem(t_lane + slot * N, N, p.GZ, row_l < rows_valid, fst + row_l * ZT2);
           if (!resident) {
             tc_fence_before();
             __syncwarp();
@@ -1036,10 +1036,9 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       if (resident) {
         if (warp >= 4 && *fabort == 0) {
           for (int t = 0; t < ntiles; ++t) {
-            float v[kMaxQ];
-            tmem_read_row(t_lane + t * N, N, v);
+            const float sc = token_score_tmem(t_lane + t * N, N, G, sc2, gm, ginv);
             const int row = t * TR + row_l;
-            if (row < R) keys[row] = __float_as_uint(token_score(v, G, sc2, gm, ginv));
+            if (row < R) keys[row] = __float_as_uint(sc);
           }
         }
       } else if (warp == 0) {
@@ -1053,10 +1052,9 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           okc = __all_sync(0xffffffffu, okc);
           tc_fence_after();
           if (okc) {
-            float v[kMaxQ];
-            tmem_read_row(t_lane + slot * N, N, v);
+            const float sc = token_score_tmem(t_lane + slot * N, N, G, sc2, gm, ginv);
             const int row = t * TR + row_l;
-            if (row < R) keys[row] = __float_as_uint(token_score(v, G, sc2, gm, ginv));
+            if (row < R) keys[row] = __float_as_uint(sc);
           }
           tc_fence_before();
           __syncwarp();
