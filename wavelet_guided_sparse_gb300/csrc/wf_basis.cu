@@ -144,7 +144,7 @@ __device__ __forceinline__ void stage_rows(const BasisFilterParams& p, int64_t u
 
 __device__ __forceinline__ void online_add(float& m, float& l, float z) {
   const float mn = fmaxf(m, z);
-  l = l * exp2f(m - mn) + exp2f(z - mn);
+  l = l * fast_exp2(m - mn) + fast_exp2(z - mn);
   m = mn;
 }
 
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kThreads) basis_filter_kernel(BasisFilterParam
       for (int w = 0; w < kWarps; ++w) m = fmaxf(m, sm.stat_m[w][tid]);
       float l = 0.f;
       for (int w = 0; w < kWarps; ++w)
-        if (sm.stat_m[w][tid] != -INFINITY) l += sm.stat_l[w][tid] * exp2f(sm.stat_m[w][tid] - m);
+        if (sm.stat_m[w][tid] != -INFINITY) l += sm.stat_l[w][tid] * fast_exp2(sm.stat_m[w][tid] - m);
       sm.gm[tid] = m;
       sm.ginv[tid] = 1.f / l;
     }
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kThreads) basis_filter_kernel(BasisFilterParam
     for (int c = tid; c < ncand; c += kThreads) {
       const float* zc = z + static_cast<int64_t>(c) * G;
       float s = 0.f;
-      for (int i = 0; i < G; ++i) s += exp2f(zc[i] - sm.gm[i]) * sm.ginv[i];
+      for (int i = 0; i < G; ++i) s += fast_exp2(zc[i] - sm.gm[i]) * sm.ginv[i];
       keys[c] = __float_as_uint(s);  // s >= 0: the bit pattern orders like the value
     }
     __syncthreads();

@@ -83,6 +83,16 @@ __device__ __forceinline__ void widen16(const uint4& v, const float*, float* f) 
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ float to_f32(float x) { return x; }
 
+// 2^x by the hardware approximation (ex2.approx.ftz: relative error below
+// 2^-22; results below 2^-126 flush to zero, which only drops softmax terms
+// that vanish beside the maximum).  The softmax statistics, scores and
+// attention weights of the path all use it.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------------------------------ reductions
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -234,7 +244,7 @@ __device__ __forceinline__ void merge_ml(float& m, float& l, float m2, float l2)
     return;
   }
   const float mx = fmaxf(m, m2);
-  l = l * exp2f(m - mx) + l2 * exp2f(m2 - mx);
+  l = l * fast_exp2(m - mx) + l2 * fast_exp2(m2 - mx);
   m = mx;
 }
 

@@ -351,9 +351,9 @@ __device__ __forceinline__ void online8(float& m, float& l, const float (&z)[8])
 #pragma unroll
   for (int u = 0; u < 8; ++u) cm = fmaxf(cm, z[u]);
   if (cm == -INFINITY) return;
-  float acc = l * exp2f(m - cm);
+  float acc = l * fast_exp2(m - cm);
 #pragma unroll
-  for (int u = 0; u < 8; ++u) acc += exp2f(z[u] - cm);
+  for (int u = 0; u < 8; ++u) acc += fast_exp2(z[u] - cm);
   l = acc;
   m = cm;
 }
@@ -374,7 +374,7 @@ __device__ __forceinline__ void cp_async_wait_pending(int pending) {
 }
 
 __device__ __forceinline__ float safe_exp2_diff(float m, float mx) {
-  return m == -INFINITY ? 0.f : exp2f(m - mx);
+  return m == -INFINITY ? 0.f : fast_exp2(m - mx);
 }
 
 // Prompt row of key slot g (g < B) of this unit, or -1 if out of range.
@@ -539,7 +539,7 @@ __device__ __forceinline__ float token_score_tmem(uint32_t taddr, int N, int G, 
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int q = c + i;
-      if (q < G) sq[i & 3] += exp2f(v[i] * sc2 - gm[q]) * ginv[q];
+      if (q < G) sq[i & 3] += fast_exp2(v[i] * sc2 - gm[q]) * ginv[q];
     }
   }
   return (sq[0] + sq[1]) + (sq[2] + sq[3]);
@@ -855,10 +855,10 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         if (r < zr) {
           int qi = sub;
           for (; qi + 4 < G; qi += 8) {
-            sa += exp2f(zc[r * ZP + qi] - gm[qi]) * ginv[qi];
-            sb += exp2f(zc[r * ZP + qi + 4] - gm[qi + 4]) * ginv[qi + 4];
+            sa += fast_exp2(zc[r * ZP + qi] - gm[qi]) * ginv[qi];
+            sb += fast_exp2(zc[r * ZP + qi + 4] - gm[qi + 4]) * ginv[qi + 4];
           }
-          if (qi < G) sa += exp2f(zc[r * ZP + qi] - gm[qi]) * ginv[qi];
+          if (qi < G) sa += fast_exp2(zc[r * ZP + qi] - gm[qi]) * ginv[qi];
         }
         float sacc = sa + sb;
         sacc += __shfl_xor_sync(0xffffffffu, sacc, 1);
@@ -1315,7 +1315,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   #pragma unroll
               for (int k = 0; k < 4; ++k) {
                 const int q = 4 * q4 + k;
-                if (q < G) sq[k] += exp2f(vv[k] * sc2 - gm[q]) * ginv[q];
+                if (q < G) sq[k] += fast_exp2(vv[k] * sc2 - gm[q]) * ginv[q];
               }
             }
           } else if (leaves == 1) {
@@ -1323,12 +1323,12 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   #pragma unroll 2
             for (; q + 4 <= G; q += 4) {
   #pragma unroll
-              for (int k = 0; k < 4; ++k) sq[k] += exp2f(t[row + q + k] * sc2 - gm[q + k]) * ginv[q + k];
+              for (int k = 0; k < 4; ++k) sq[k] += fast_exp2(t[row + q + k] * sc2 - gm[q + k]) * ginv[q + k];
             }
-            for (; q < G; ++q) sq[0] += exp2f(t[row + q] * sc2 - gm[q]) * ginv[q];
+            for (; q < G; ++q) sq[0] += fast_exp2(t[row + q] * sc2 - gm[q]) * ginv[q];
           } else {
   #pragma unroll 1
-            for (int q = 0; q < G; ++q) sq[q & 3] += exp2f(leaf_sum(row, q) * sc2 - gm[q]) * ginv[q];
+            for (int q = 0; q < G; ++q) sq[q & 3] += fast_exp2(leaf_sum(row, q) * sc2 - gm[q]) * ginv[q];
           }
           keys[ci] = __float_as_uint((sq[0] + sq[1]) + (sq[2] + sq[3]));
         }
@@ -1474,14 +1474,14 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
         const float base_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
         const float base_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
-        const float corr_lo = exp2f(m_lo - base_lo), corr_hi = exp2f(m_hi - base_hi);
+        const float corr_lo = fast_exp2(m_lo - base_lo), corr_hi = fast_exp2(m_hi - base_hi);
         float sum_lo = 0.f, sum_hi = 0.f;
 #pragma unroll
         for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            s[nb][e] = exp2f(s[nb][e] - base_lo);
-            s[nb][e + 2] = exp2f(s[nb][e + 2] - base_hi);
+            s[nb][e] = fast_exp2(s[nb][e] - base_lo);
+            s[nb][e + 2] = fast_exp2(s[nb][e + 2] - base_hi);
             sum_lo += s[nb][e];
             sum_hi += s[nb][e + 2];
           }
@@ -1622,11 +1622,11 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           const float mo = m_run[qi];
           const float mn = fmaxf(mo, warp_max(sv));
           const float base = mn == -INFINITY ? 0.f : mn;
-          const float pv = exp2f(sv - base);
+          const float pv = fast_exp2(sv - base);
           const float sum = warp_sum(pv);
           sS[qi * 33 + lane] = pv;
           if (lane == 0) {
-            const float corr = exp2f(mo - base);
+            const float corr = fast_exp2(mo - base);
             corr_s[qi] = corr;
             l_run[qi] = l_run[qi] * corr + sum;
             m_run[qi] = mn;
