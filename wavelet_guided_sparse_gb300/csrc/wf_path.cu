@@ -992,7 +992,9 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
           }
-          named_bar_sync(1, 128);
+          // Each warp stages and then reads only its own 32 rows: a warp-level
+          // barrier orders the staging stores before the reads.
+          __syncwarp();
           const int qa = lane < G ? lane : 0, qb = lane + 32 < G ? lane + 32 : 0;
 #pragma unroll
           for (int u0 = 0; u0 < 32; u0 += 8) {
@@ -1012,7 +1014,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
               online8(m1, l1, z);
             }
           }
-          named_bar_sync(1, 128);
+          __syncwarp();  // the next tile's staging overwrites these rows
         }
       }
       if (warp >= 4) {
@@ -1077,10 +1079,14 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         }
         uint32_t* gkeys = reinterpret_cast<uint32_t*>(smem + L.f_gather);
         int32_t* gpos = reinterpret_cast<int32_t*>(gkeys + cs * p.rows_cap);
-        for (int e = tid; e < R * cs; e += kThreads) {
-          const int i = e % R, r = e / R;
-          peer(gkeys, r)[off + i] = keys[i];
-          peer(gpos, r)[off + i] = span_token(sl_all, s0, i, levels);
+        // Four candidates per 16-byte store (R and every offset are multiples of 8).
+        const int R4 = R >> 2;
+        for (int e = tid; e < R4 * cs; e += kThreads) {
+          const int i = (e % R4) * 4, r = e / R4;
+          *reinterpret_cast<uint4*>(peer(gkeys, r) + off + i) = *reinterpret_cast<const uint4*>(keys + i);
+          *reinterpret_cast<int4*>(peer(gpos, r) + off + i) =
+              make_int4(span_token(sl_all, s0, i, levels), span_token(sl_all, s0, i + 1, levels),
+                        span_token(sl_all, s0, i + 2, levels), span_token(sl_all, s0, i + 3, levels));
         }
         cluster.sync();
         if (mode & kModeAttend) {
@@ -1438,8 +1444,12 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
       for (int tile = 0; tile < ntiles; ++tile) {
         const int stage = tile % AS;
-        cp_async_wait_pending(min(ntiles, tile + AS) - 1 - tile);
-        __syncthreads();
+        // Tiles issued before this iteration's refill: 0 .. min(ntiles, AS + tile - 1) - 1.
+        cp_async_wait_pending(tile == 0 ? min(ntiles, AS) - 1 : min(ntiles - tile - 1, AS - 2));
+        __syncthreads();  // this tile's rows are visible; every warp is done with tile - 1
+        // Refill the stage tile - 1 used, while this tile is computed.
+        if (tile >= 1 && tile - 1 + AS < ntiles)
+          attn_issue<T, D>(p, mode, c, ar, kst, vst, TK, tile - 1 + AS, (tile - 1) % AS);
         const uint32_t kb = smem_u32(kst + (stage * TK + kgrp * 16) * RB);
         const uint32_t vb = smem_u32(vst + (stage * TK + kgrp * 16) * RB);
         float s[2][4];
@@ -1510,8 +1520,6 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           mma_bf16(oacc[dn], pa, b);
           mma_bf16(oacc[dn + 1], pa, b + 2);
         }
-        __syncthreads();
-        if (tile + AS < ntiles) attn_issue<T, D>(p, mode, c, ar, kst, vst, TK, tile + AS, stage);
       }
       // Warp partials -> shared memory (overwrites the stages).
       // Row pitch D + 8 floats: a warp's fragment stores (8 rows x 4 column
@@ -1596,8 +1604,12 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       __syncthreads();
       for (int tile = 0; tile < ntiles; ++tile) {
         const int stage = tile % AS;
-        cp_async_wait_pending(min(ntiles, tile + AS) - 1 - tile);
-        __syncthreads();
+        // Tiles issued before this iteration's refill: 0 .. min(ntiles, AS + tile - 1) - 1.
+        cp_async_wait_pending(tile == 0 ? min(ntiles, AS) - 1 : min(ntiles - tile - 1, AS - 2));
+        __syncthreads();  // this tile's rows are visible; every warp is done with tile - 1
+        // Refill the stage tile - 1 used, while this tile is computed.
+        if (tile >= 1 && tile - 1 + AS < ntiles)
+          attn_issue<T, D>(p, mode, c, ar, kst, vst, TK, tile - 1 + AS, (tile - 1) % AS);
         const float* kb = reinterpret_cast<const float*>(kst + stage * TK * RB);
         const float* vb = reinterpret_cast<const float*>(vst + stage * TK * RB);
         {
@@ -1653,8 +1665,6 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
             oacc[i][0] = a0; oacc[i][1] = a1; oacc[i][2] = a2; oacc[i][3] = a3;
           }
         }
-        __syncthreads();
-        if (tile + AS < ntiles) attn_issue<T, D>(p, mode, c, ar, kst, vst, TK, tile + AS, stage);
       }
       __syncthreads();  // the receive area shares no bytes with what peers still use
       const int c4 = tid % C4, qg = tid / C4;
