@@ -356,12 +356,9 @@ int wf_score_topk(const wf_dims* dims, const void* Q, const float* AL, int32_t k
   if (!wf::plan_path(ld, wf::kPhaseScore, nullptr, k_L, 0, wf::device_sm_count(), &plan))
     return WF_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float* zl = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.zl);
-  const cudaError_t e = wf::launch_coarse_logits(ld, AL, Q, zl, s);
-  if (e != cudaSuccess) return cuda_status(e);
   wf::PathArgs a = {};
   a.q = Q;
-  a.zl = zl;
+  a.al = AL;  // the score phase forms the coarse logits itself
   a.idx_l_out = idx_L;
   a.scores_out = scores_L;
   a.status = status_word(workspace);
@@ -510,18 +507,14 @@ int wf_step_cached_al(const wf_dims* dims, const void* Q, const void* Kp, const 
   const Layout L = layout(ld, k_per_level, &plan);
   if (workspace_bytes < L.total) return WF_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
-  float* zl = reinterpret_cast<float*>(ws + L.zl);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The cached A_L's coarse logits against this step's queries, then steps 2-5.
-  const cudaError_t e = wf::launch_coarse_logits(ld, AL, Q, zl, s);
-  if (e != cudaSuccess) return cuda_status(e);
   wf::PathArgs a = {};
   a.q = Q;
   a.kp = Kp;
   a.vp = Vp;
   a.kg = Kg;
   a.vg = Vg;
-  a.zl = zl;
+  a.al = AL;  // one launch: the score phase forms the coarse logits from the cached A_L
   a.idx_out = idx_out;
   a.o = O;
   a.lse = lse;

@@ -64,50 +64,6 @@ __device__ __forceinline__ void store_row(const float* acc, float scale, int64_t
     o[v / 4] = make_float4(acc[v] * scale, acc[v + 1] * scale, acc[v + 2] * scale, acc[v + 3] * scale);
 }
 
-// Coarse logits zl[r, q] = zscale Q[unit(r)][q]·A_L[r] of the A_L rows
-// [r_begin, r_end) (global, fp32; unit(r) = r / P), by `workers` of the
-// block's warps (worker w = this warp's index among them).  bf16 queries: 16
-// rows per warp task on the tensor cores (exact three-way split of A_L);
-// fp32 queries: lane groups (C lanes per row) with FMAs.
-template <typename T, int D>
-__device__ __forceinline__ void coarse_logits_range(const float* al, const T* q, float* zl,
-                                                    int64_t r_begin, int64_t r_end, int64_t P,
-                                                    int G, int GZ, float zscale, int64_t worker,
-                                                    int64_t workers) {
-  if constexpr (sizeof(T) == 2) {
-    for (int64_t r0 = r_begin + worker * 16; r0 < r_end; r0 += workers * 16) {
-      const int n = static_cast<int>(r_end - r0 < 16 ? r_end - r0 : 16);
-      for (int64_t u = r0 / P; u * P < r0 + n; ++u) {
-        const int ra = static_cast<int>(u * P > r0 ? u * P - r0 : 0);
-        const int rb = static_cast<int>((u + 1) * P - r0 < n ? (u + 1) * P - r0 : n);
-        coarse_logits_rows16<D>(al + r0 * D, D, n, ra, rb, r0,
-                                reinterpret_cast<const __nv_bfloat16*>(q) + u * G * D, G, GZ,
-                                zscale, zl, 0, 1);
-      }
-    }
-  } else {
-    constexpr int V = Elem<T>::kPer16B, C = D / V, RPW = 32 / C;  // rows per warp pass
-    const int lane = threadIdx.x & 31, c = lane % C;
-    for (int64_t base = r_begin + worker * RPW; base < r_end; base += workers * RPW) {
-      const int64_t row = base + lane / C;
-      const bool act = row < r_end;
-      float a[V];
-#pragma unroll
-      for (int v = 0; v < V; v += 4) {
-        const float4 x = act ? *reinterpret_cast<const float4*>(al + row * D + c * V + v)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-        a[v] = x.x; a[v + 1] = x.y; a[v + 2] = x.z; a[v + 3] = x.w;
-      }
-      const int64_t unit = act ? row / P : 0;
-      float* dst = zl + (act ? row : 0) * GZ;
-      if (G <= 32)
-        emit_coarse_logits<T, V, C, 32>(a, act, q + unit * G * D, D, G, zscale, dst);
-      else
-        emit_coarse_logits<T, V, C, 64>(a, act, q + unit * G * D, D, G, zscale, dst);
-    }
-  }
-}
-
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1) dwt_stream_kernel(const T* __restrict__ kp,
                                                                  float* __restrict__ out,
@@ -267,45 +223,7 @@ cudaError_t launch_typed(const LaunchDims& ld, const void* kp, float* out, const
   return cudaGetLastError();
 }
 
-// Coarse logits from an fp32 A_L [U, P, D] kept from an earlier step: the
-// rows' C-lane groups load their channels and form the logits exactly as the
-// stream does for the rows it sums.
-template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) coarse_logits_kernel(const float* __restrict__ al,
-                                                                 const T* __restrict__ q,
-                                                                 float* __restrict__ zl,
-                                                                 int64_t rows_total, int64_t P,
-                                                                 int G, int GZ, float zscale) {
-  coarse_logits_range<T, D>(al, q, zl, 0, rows_total, P, G, GZ, zscale,
-                            static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5),
-                            static_cast<int64_t>(gridDim.x) * kWarps);
-}
-
-template <typename T, int D>
-cudaError_t launch_logits_typed(const LaunchDims& ld, const float* al, const void* q, float* zl,
-                                cudaStream_t stream) {
-  constexpr int RPP = kWarps * (sizeof(T) == 2 ? 16 : 32 / (D / Elem<T>::kPer16B));
-  const int64_t P = ld.n_prompt >> ld.levels;
-  const int64_t rows = ld.units * P;
-  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((rows + RPP - 1) / RPP,
-                                                              8 * static_cast<int64_t>(device_sm_count())));
-  const float zscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
-  coarse_logits_kernel<T, D><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
-      al, static_cast<const T*>(q), zl, rows, P, ld.n_gen, coarse_logit_pitch(ld.n_gen), zscale);
-  return cudaGetLastError();
-}
-
 }  // namespace
-
-cudaError_t launch_coarse_logits(const LaunchDims& ld, const float* al, const void* q, float* zl,
-                                 cudaStream_t stream) {
-  if (ld.dtype == WF_BF16) {
-    if (ld.head_dim == 128) return launch_logits_typed<__nv_bfloat16, 128>(ld, al, q, zl, stream);
-    return launch_logits_typed<__nv_bfloat16, 64>(ld, al, q, zl, stream);
-  }
-  if (ld.head_dim == 128) return launch_logits_typed<float, 128>(ld, al, q, zl, stream);
-  return launch_logits_typed<float, 64>(ld, al, q, zl, stream);
-}
 
 cudaError_t launch_dwt_lowpass(const LaunchDims& ld, const void* kp, float* out, const void* q,
                                float* zl, int levels, int32_t* status, cudaStream_t stream) {

@@ -63,6 +63,8 @@ struct PathArgs {
   const void *q, *kp, *vp, *kg, *vg;
   const float* zl;   // score phase without the fused stream: coarse logits
                      // [U, P, coarse_logit_pitch(G)], log2 domain (Q·A_L·log2e/√d)
+  const float* al;   // or, instead: an fp32 A_L [U, P, d] whose logits the score
+                     // phase forms itself
   const int32_t* idx_l_in;
   const int32_t* idx_in;
   int32_t* idx_l_out;
@@ -87,9 +89,7 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
 // [U, P, coarse_logit_pitch(G)] in the log2 domain.
 cudaError_t launch_dwt_lowpass(const LaunchDims& ld, const void* kp, float* out, const void* q,
                                float* zl, int levels, int32_t* status, cudaStream_t stream);
-// Coarse logits from an fp32 A_L [U, P, d] (computed at an earlier step).
-cudaError_t launch_coarse_logits(const LaunchDims& ld, const float* al, const void* q, float* zl,
-                                 cudaStream_t stream);
+
 cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathArgs& args,
                         cudaStream_t stream);
 

@@ -122,4 +122,48 @@ __device__ __forceinline__ void coarse_logits_rows16(const float* a, int pitch, 
   }
 }
 
+// Coarse logits zl[r, q] = zscale Q[unit(r)][q]·A_L[r] of the A_L rows
+// [r_begin, r_end) (global, fp32; unit(r) = r / P), by `workers` of the
+// block's warps (worker w = this warp's index among them).  bf16 queries: 16
+// rows per warp task on the tensor cores (exact three-way split of A_L);
+// fp32 queries: lane groups (C lanes per row) with FMAs.
+template <typename T, int D>
+__device__ __forceinline__ void coarse_logits_range(const float* al, const T* q, float* zl,
+                                                    int64_t r_begin, int64_t r_end, int64_t P,
+                                                    int G, int GZ, float zscale, int64_t worker,
+                                                    int64_t workers) {
+  if constexpr (sizeof(T) == 2) {
+    for (int64_t r0 = r_begin + worker * 16; r0 < r_end; r0 += workers * 16) {
+      const int n = static_cast<int>(r_end - r0 < 16 ? r_end - r0 : 16);
+      for (int64_t u = r0 / P; u * P < r0 + n; ++u) {
+        const int ra = static_cast<int>(u * P > r0 ? u * P - r0 : 0);
+        const int rb = static_cast<int>((u + 1) * P - r0 < n ? (u + 1) * P - r0 : n);
+        coarse_logits_rows16<D>(al + r0 * D, D, n, ra, rb, r0,
+                                reinterpret_cast<const __nv_bfloat16*>(q) + u * G * D, G, GZ,
+                                zscale, zl, 0, 1);
+      }
+    }
+  } else {
+    constexpr int V = Elem<T>::kPer16B, C = D / V, RPW = 32 / C;  // rows per warp pass
+    const int lane = threadIdx.x & 31, c = lane % C;
+    for (int64_t base = r_begin + worker * RPW; base < r_end; base += workers * RPW) {
+      const int64_t row = base + lane / C;
+      const bool act = row < r_end;
+      float a[V];
+#pragma unroll
+      for (int v = 0; v < V; v += 4) {
+        const float4 x = act ? *reinterpret_cast<const float4*>(al + row * D + c * V + v)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        a[v] = x.x; a[v + 1] = x.y; a[v + 2] = x.z; a[v + 3] = x.w;
+      }
+      const int64_t unit = act ? row / P : 0;
+      float* dst = zl + (act ? row : 0) * GZ;
+      if (G <= 32)
+        emit_coarse_logits<T, V, C, 32>(a, act, q + unit * G * D, D, G, zscale, dst);
+      else
+        emit_coarse_logits<T, V, C, 64>(a, act, q + unit * G * D, D, G, zscale, dst);
+    }
+  }
+}
+
 }  // namespace wf

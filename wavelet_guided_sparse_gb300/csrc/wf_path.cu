@@ -77,6 +77,7 @@ struct PathParams {
   const void* kg;
   const void* vg;
   const float* zl;           // score without the fused stream: coarse logits [U, P, GZ]
+  const float* al;           // or an fp32 A_L [U, P, d] whose logits this kernel forms
   const int32_t* idx_l_in;   // filter without score: S_L [U, k_L]
   const int32_t* idx_in;     // attend without filter: S [U, B]
   int32_t* idx_l_out;        // score without filter: S_L out [U, k_L]
@@ -702,7 +703,8 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     const int ZP = fuse_dwt ? TS : p.GZ + 4;
     const int zrows = fuse_dwt ? Pc : min(Pc, kZRows);  // positions resident at a time
     const int nz = (Pc + zrows - 1) / zrows;
-    const float* zsrc = fuse_dwt ? nullptr : p.zl + (unit * p.P + static_cast<int64_t>(rank) * Pc) * p.GZ;
+    const int64_t row0 = unit * p.P + static_cast<int64_t>(rank) * Pc;  // this CTA's first position
+    const float* zsrc = fuse_dwt || p.zl == nullptr ? nullptr : p.zl + row0 * p.GZ;
     if (fuse_dwt) {
       // Step 1: A_L[c] = 2^(-L/2) * (sum of the 2^L rows of span c), fp32,
       // written straight into the tile operand layout.  Two threads per
@@ -795,16 +797,22 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       }
       __syncthreads();
     }
-    // Coarse logits of positions [c0, c0 + rows) from global memory into zc.
+    // Coarse logits of positions [c0, c0 + rows) into zc: read from global
+    // memory, or formed here from a cached fp32 A_L (16 rows per warp task).
     auto load_z = [&](int c0, int rows) {
       __syncthreads();  // earlier readers of zc are done
-      const int c4 = p.GZ >> 2;
-      for (int e = tid; e < rows * c4; e += kThreads) {
-        const int r = e / c4, k = e - r * c4;
-        cp_async16(zc + r * ZP + 4 * k, zsrc + static_cast<int64_t>(c0 + r) * p.GZ + 4 * k);
+      if (p.al != nullptr) {
+        coarse_logits_range<T, D>(p.al + (row0 + c0) * D, static_cast<const T*>(p.q) + unit * G * D,
+                                  zc, 0, rows, int64_t{1} << 40, G, ZP, zscale, warp, kWarps);
+      } else {
+        const int c4 = p.GZ >> 2;
+        for (int e = tid; e < rows * c4; e += kThreads) {
+          const int r = e / c4, k = e - r * c4;
+          cp_async16(zc + r * ZP + 4 * k, zsrc + static_cast<int64_t>(c0 + r) * p.GZ + 4 * k);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
       }
-      cp_async_commit();
-      cp_async_wait<0>();
       __syncthreads();
     };
     // Pass 1: per-query (max, sum) over this CTA's positions; thread ->
@@ -1957,6 +1965,7 @@ cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathAr
   p.kg = a.kg;
   p.vg = a.vg;
   p.zl = a.zl;
+  p.al = a.al;
   p.idx_l_in = a.idx_l_in;
   p.idx_in = a.idx_in;
   p.idx_l_out = a.idx_l_out;
