@@ -501,7 +501,7 @@ int wf_step_cached_al(const wf_dims* dims, const void* Q, const void* Kp, const 
   if (st != WF_OK) return st;
   const int budget = k_per_level[0];
   wf::PathPlan plan;
-  if (!wf::plan_path(ld, wf::kPhaseAll, k_per_level, k_per_level[ld.levels], budget,
+  if (!wf::plan_path(ld, wf::kPhaseAll | wf::kPhaseCachedAl, k_per_level, k_per_level[ld.levels], budget,
                      wf::device_sm_count(), &plan))
     return WF_ERR_UNSUPPORTED;
   const Layout L = layout(ld, k_per_level, &plan);

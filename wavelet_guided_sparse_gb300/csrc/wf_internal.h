@@ -30,12 +30,16 @@ enum : int { kPhaseScore = 1, kPhaseFilter = 2, kPhaseAttend = 4, kPhaseAll = 7 
 // Request bit for plan_path with kPhaseAll: compute A_L inside the path
 // kernel (step 1 fused into the scoring) where the plan allows it.
 enum : int { kPhaseFuseDwt = 8 };
+// Request bit for plan_path with kPhaseAll when the caller passes a cached
+// fp32 A_L: stage its rows by one bulk copy per CTA where the plan allows it.
+enum : int { kPhaseCachedAl = 16 };
 
 // Launch plan of the path kernel; a pure function of the sizes and the
 // device's SM count.
 struct PathPlan {
   int mode;          // kPhase* bit set (without kPhaseFuseDwt)
   int fuse_dwt;      // 1: the path kernel computes A_L itself (no separate DWT launch)
+  int al_stage;      // 1: cached A_L rows staged by one bulk copy per CTA (PathArgs::al)
   int cluster;       // CTAs per unit
   int per_cta_p;     // score: coarse positions per CTA
   int rows_cap;      // filter: token rows per CTA (capacity)

@@ -94,6 +94,8 @@ struct PathParams {
   int filter_fast;         // token logits: 0 general path; 1 tensor-memory resident; 2 streamed twice
   int f_nb;                // fast filter: tensor-memory accumulator slots
   int fuse_dwt;            // score: A_L from K_p inside this kernel
+  int al_stage;            // score: this CTA's rows of the cached fp32 A_L arrive by one
+                           // bulk copy and go to the tensor cores (per_cta_p <= kScoreChunk)
   uint32_t inject_polls;   // fault injection (tests): see the fused step 1 below
   float al_scale;          // 2^(-L/2), the orthonormal Haar low-pass gain
   int k[WF_MAX_LEVELS + 1];
@@ -145,12 +147,14 @@ struct PathSmem {
     const size_t u = o;
     size_t end = u;
     s_ring = 0;
-    if ((p.mode & kModeScore) && p.fuse_dwt) {
-      // Fused step 1: the bulk-copy ring of K_p rows, then A_L in the tile
-      // operand layout (bf16: hi / mid / lo planes; fp32: rows).  The logits
-      // overwrite the ring once every stage has been consumed.
+    if ((p.mode & kModeScore) && (p.fuse_dwt || p.al_stage)) {
+      // Fused step 1: the bulk-copy ring of K_p rows (or the one copy of the
+      // cached A_L rows), then A_L in the tile operand layout (bf16: hi / mid
+      // / lo planes; fp32: rows).  The logits overwrite the ring once every
+      // stage has been consumed.
       o = u;
-      s_ring = take_bytes(static_cast<size_t>(kFuseStages) * kFuseStageBytes);
+      const size_t al_b = sizeof(float) * kScoreChunk * (D > kMaxQ + 1 ? D : kMaxQ + 1);
+      s_ring = take_bytes(p.fuse_dwt ? static_cast<size_t>(kFuseStages) * kFuseStageBytes : al_b);
       s_as = take_bytes((sizeof(T) == 2 ? 3 : 1) * kScoreChunk * kRowBytes, 1024);
       s_stage = s_z = s_ring;
       end = end > o ? end : o;
@@ -563,8 +567,13 @@ __device__ __forceinline__ void tmem_row_to_smem(uint32_t taddr, int N, int cols
 }
 
 // ============================================================== the kernel
-template <typename T, int D, bool kFast>
+// kVar selects an instantiation with the common decisions constant:
+// 0: general (every decision read from the parameters); 1: the single-launch
+// step (fused step 1, every phase, all-gather final selection, resident token
+// logits); 2: the same step from a cached fp32 A_L (no stream).
+template <typename T, int D, int kVar>
 __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant__ PathParams p) {
+  constexpr bool kFast = kVar != 0;
   extern __shared__ __align__(1024) unsigned char smem[];  // swizzled operands need 1024
   cg::cluster_group cluster = cg::this_cluster();
   Ctx c;
@@ -577,11 +586,10 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   const int tid = c.tid, lane = c.lane, warp = c.warp, cs = c.cs, rank = c.rank;
   const int64_t unit = c.unit;
   const int G = p.G, levels = p.levels;
-  // The single-launch step of the common case (fused step 1, every phase,
-  // gather-all final selection, token logits in shared memory) is its own
-  // instantiation with these decisions constant.
   const int mode = kFast ? (kModeScore | kModeFilter | kModeAttend) : p.mode;
-  const bool fuse_dwt = kFast || p.fuse_dwt;
+  const bool fuse_dwt = kVar == 1 || (kVar == 0 && p.fuse_dwt);
+  const bool cached_al = kVar == 2 || (kVar == 0 && p.al != nullptr);
+  const bool al_stage = kVar != 1 && p.al_stage;
   const bool gather_all = kFast || p.gather_all;
   float* const t_ws = kFast ? nullptr : p.t_ws;
   const PathSmem<T, D> L(p);
@@ -649,12 +657,19 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   if (tid == 0) {
     if (fuse_dwt)
       for (int i = 0; i < kFuseStages; ++i) mbar_init(&bars[i], 1);
+    if (al_stage) mbar_init(&bars[0], 1);
     mbar_init(mma_bar, 1);
     mbar_init(span_bar, 1);
     fence_mbar_init();
     if (fuse_dwt)
       for (int st = 0; st < fuse_issued; ++st)
         if (!(inject && st == 0)) fuse_issue(st);
+    if (al_stage) {  // this CTA's per_cta_p rows of the cached A_L: one contiguous range
+      const uint32_t bytes = static_cast<uint32_t>(p.per_cta_p) * D * sizeof(float);
+      mbar_arrive_expect_tx(&bars[0], bytes);
+      bulk_g2s(smem + L.s_ring,
+               p.al + (unit * p.P + static_cast<int64_t>(rank) * p.per_cta_p) * D, bytes, &bars[0]);
+    }
     if (p.use_tma_spans) prefetch_tensormap(&p.tmap_spans);  // used by the filter phase
   }
   __syncwarp();
@@ -700,8 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     const float zscale = p.inv_sqrt_d * kLog2e;
     // Row pitch of zc: the fused stream's logits tile (odd pitch), or padded
     // rows of the coarse logits read from global memory (16-byte aligned).
-    const int ZP = fuse_dwt ? TS : p.GZ + 4;
-    const int zrows = fuse_dwt ? Pc : min(Pc, kZRows);  // positions resident at a time
+    const int ZP = fuse_dwt || al_stage ? TS : p.GZ + 4;
+    const int zrows = fuse_dwt || al_stage ? Pc : min(Pc, kZRows);  // positions resident at a time
     const int nz = (Pc + zrows - 1) / zrows;
     const int64_t row0 = unit * p.P + static_cast<int64_t>(rank) * Pc;  // this CTA's first position
     const float* zsrc = fuse_dwt || p.zl == nullptr ? nullptr : p.zl + row0 * p.GZ;
@@ -796,12 +811,42 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         logits_tile_f32<D>(as, reinterpret_cast<const float*>(qs), zc, 0, Pc, G, TS, zscale);
       }
       __syncthreads();
+    } else if (sizeof(T) == 2 && al_stage) {
+      // Cached A_L: the rows landed in the ring; each value is split exactly
+      // into three bf16 parts written to the tile operand planes (one thread
+      // per 4 values), then the logits are formed as in the fused case.  A
+      // timed-out copy is waited for once more (bounded) before the ring is
+      // reused; the status word reports it.
+      if (!mbar_wait_bounded(&bars[0], 0u, p.status)) (void)mbar_wait_bounded(&bars[0], 0u, p.status);
+      const float* ring = reinterpret_cast<const float*>(smem + L.s_ring);
+      for (int it = tid; it < Pc * (D / 4); it += kThreads) {
+        const int row = it / (D / 4), q4 = it % (D / 4), ch = q4 >> 1, h = q4 & 1;
+        const float4 v = *reinterpret_cast<const float4*>(ring + row * D + 4 * q4);
+        const float a[4] = {v.x, v.y, v.z, v.w};
+        uint32_t w[3][2];
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+          float h0, m0, l0, h1, m1, l1;
+          split3_bf16(a[e], h0, m0, l0);
+          split3_bf16(a[e + 1], h1, m1, l1);
+          w[0][e / 2] = pack_bf16(h0, h1);
+          w[1][e / 2] = pack_bf16(m0, m1);
+          w[2][e / 2] = pack_bf16(l0, l1);
+        }
+#pragma unroll
+        for (int pl = 0; pl < 3; ++pl)
+          *reinterpret_cast<uint2*>(as + pl * kPlaneBytes + sw_offset(row, ch, kScoreChunk) + h * 8) =
+              make_uint2(w[pl][0], w[pl][1]);
+      }
+      umma_logits<D>(as, 3, kPlaneBytes, kScoreChunk, Pc, qs, G, zc, 0, TS, zscale, tmem, mma_bar,
+                     mma_phase, p.status);
+      __syncthreads();
     }
     // Coarse logits of positions [c0, c0 + rows) into zc: read from global
     // memory, or formed here from a cached fp32 A_L (16 rows per warp task).
     auto load_z = [&](int c0, int rows) {
       __syncthreads();  // earlier readers of zc are done
-      if (p.al != nullptr) {
+      if (cached_al) {
         coarse_logits_range<T, D>(p.al + (row0 + c0) * D, static_cast<const T*>(p.q) + unit * G * D,
                                   zc, 0, rows, int64_t{1} << 40, G, ZP, zscale, warp, kWarps);
       } else {
@@ -820,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
     for (int zc0 = 0; zc0 < Pc; zc0 += zrows) {
       const int zr = min(zrows, Pc - zc0);
-      if (!fuse_dwt) load_z(zc0, zr);
+      if (!fuse_dwt && !al_stage) load_z(zc0, zr);
       const int q0 = lane < G ? lane : 0, q1 = lane + 32 < G ? lane + 32 : 0;
       for (int c0 = 0; c0 < zr; c0 += kScoreChunk) {
         float z[8];
@@ -1723,10 +1768,25 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
 
 template <typename T, int D>
 cudaError_t launch_typed(int64_t units, const PathParams& prm, size_t smem, cudaStream_t stream) {
-  const bool fast = prm.mode == (kModeScore | kModeFilter | kModeAttend) && prm.fuse_dwt &&
-                    prm.gather_all && prm.filter_fast == 1;
-  const cudaError_t e = fast ? ensure_max_smem<path_kernel<T, D, true>>()
-                             : ensure_max_smem<path_kernel<T, D, false>>();
+  // The constant-folded variants serve bf16 steps with every phase, the
+  // all-gather final selection and resident token logits.
+  int var = 0;
+  if (sizeof(T) == 2 && prm.mode == (kModeScore | kModeFilter | kModeAttend) && prm.gather_all &&
+      prm.filter_fast == 1)
+    var = prm.fuse_dwt ? 1 : (prm.al != nullptr ? 2 : 0);
+  void (*kern)(const PathParams) = path_kernel<T, D, 0>;
+  if constexpr (sizeof(T) == 2) {
+    if (var == 1) kern = path_kernel<T, D, 1>;
+    if (var == 2) kern = path_kernel<T, D, 2>;
+  }
+  cudaError_t e = cudaSuccess;
+  if (var == 1) {
+    if constexpr (sizeof(T) == 2) e = ensure_max_smem<path_kernel<T, D, 1>>();
+  } else if (var == 2) {
+    if constexpr (sizeof(T) == 2) e = ensure_max_smem<path_kernel<T, D, 2>>();
+  } else {
+    e = ensure_max_smem<path_kernel<T, D, 0>>();
+  }
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(prm.cs, static_cast<unsigned>(units), 1);
@@ -1740,8 +1800,7 @@ cudaError_t launch_typed(int64_t units, const PathParams& prm, size_t smem, cuda
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return fast ? cudaLaunchKernelEx(&cfg, path_kernel<T, D, true>, prm)
-              : cudaLaunchKernelEx(&cfg, path_kernel<T, D, false>, prm);
+  return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once (no link-time
@@ -1821,6 +1880,7 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
                int sm_count, PathPlan* plan) {
   PathParams p = {};
   const bool want_fuse = mode == (kPhaseAll | kPhaseFuseDwt);
+  const bool want_al = mode == (kPhaseAll | kPhaseCachedAl);
   mode &= kPhaseAll;
   p.mode = mode;
   p.G = ld.n_gen;
@@ -1884,6 +1944,8 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
     const int elem = ld.dtype == WF_BF16 ? 2 : 4;
     const bool fuse_try = want_fuse && p.per_cta_p <= kScoreChunk &&
                           (static_cast<int64_t>(elem) * ld.head_dim << ld.levels) <= kFuseStageBytes;
+    // Cached A_L staged by one bulk copy (bf16 queries; one score chunk per CTA).
+    const bool al_try = want_al && ld.dtype == WF_BF16 && p.per_cta_p <= kScoreChunk;
     // Prefer the fused step 1, the gather-all selection and token logits in
     // shared memory, in that order.
     // Fast filter: resident accumulators when every tile has its own columns
@@ -1898,7 +1960,7 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
     // region, so the two depths are independent); the general path trades
     // ring depth against the all-gather.
     for (int ff = fast_sched ? 1 : 0; ff >= 0 && !found; --ff)
-    for (int fz = fuse_try ? 1 : 0; fz >= 0 && !found; --fz)
+    for (int fz = fuse_try || al_try ? 1 : 0; fz >= 0 && !found; --fz)
     for (int it = 0; it < (ff ? 2 * 4 * 5 : 10) && !found; ++it) {
       int ga, fs, as;
       if (ff) {
@@ -1917,7 +1979,8 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
       p.a_stages = as;
       if (ga && (!(mode & kModeFilter) || static_cast<int64_t>(cs) * p.rows_cap > 8192)) continue;
       p.gather_all = ga;
-      p.fuse_dwt = fz;
+      p.fuse_dwt = fuse_try ? fz : 0;
+      p.al_stage = al_try ? fz : 0;
       p.t_ws = nullptr;
       smem = smem_bytes(ld, p);
       t_in_smem = true;
@@ -1950,6 +2013,7 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
   plan->f_stages = p.f_stages;
   plan->a_stages = p.a_stages;
   plan->fuse_dwt = p.fuse_dwt;
+  plan->al_stage = p.al_stage;
   plan->filter_fast = p.filter_fast;
   plan->f_nb = p.f_nb;
   plan->mode = mode;
@@ -1995,6 +2059,8 @@ cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathAr
   p.f_stages = plan.f_stages;
   p.a_stages = plan.a_stages;
   p.fuse_dwt = plan.fuse_dwt;
+  p.al_stage = plan.al_stage;
+  if (plan.al_stage && a.al == nullptr) return cudaErrorInvalidValue;
   p.inject_polls = plan.fuse_dwt ? consume_wait_injection() : 0u;
   p.filter_fast = plan.filter_fast;
   p.f_nb = plan.f_nb;
