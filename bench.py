@@ -545,10 +545,15 @@ def run_ours(args, cfg):
     del cache_graph, cache_sets
     torch.cuda.empty_cache()
 
-    # ---- the step with a longer basis (eight-tap Daubechies filter): the
-    # general path (pyramid launches, level-by-level filter CTA per unit,
-    # gather + attention), from a CUDA graph over (up to four) input sets.
+    # ---- the step with a longer basis (eight-tap Daubechies filter), from a
+    # CUDA graph over (up to four) input sets: with the default schedule
+    # (every level between L and 0 keeps all children) the composed level-L
+    # filter's logits and the path kernel; otherwise the general path
+    # (pyramid launches, level-by-level filter CTA per unit, gather +
+    # attention).
     db4 = bd.daubechies_lowpass(4)
+    keep_all = all(ks[j] == 2 * ks[j + 1] for j in range(1, cfg.levels))
+    basis_launches = 2 if keep_all and cfg.dtype == "bf16" else cfg.levels + 2
     basis_ws = torch.zeros(bd.basis_workspace_bytes(dims, db4, ks), dtype=torch.uint8,
                            device=dev)
     bsets = sets[:4]
@@ -729,10 +734,12 @@ def run_ours(args, cfg):
             "timing": "CUDA graph of 20 launches over two alternating input/output sets, "
                       "events around its replays"},
         "basis_step": {
-            "what": "wf_step_basis with the eight-tap Daubechies low-pass (periodic pyramid, "
-                    "level-by-level filter, gather + attention), one layer",
+            "what": "wf_step_basis with the eight-tap Daubechies low-pass, one layer: "
+                    + ("level-L logits of the composed periodic filter, then the path kernel"
+                       if basis_launches == 2 else
+                       "periodic pyramid, level-by-level filter, gather + attention"),
             "value": tokens_per_step(cfg) / cfg.layers / (basis_ms * 1e-3), "unit": "tokens/s",
-            "layer_step_ms": basis_ms, "launches_per_layer_step": cfg.levels + 2},
+            "layer_step_ms": basis_ms, "launches_per_layer_step": basis_launches},
         "stages_us": stage_us,
         "cpu_baseline": None if cpu_rate is None else {
             "value": cpu_rate, "unit": "tokens/s", "cores": workers, "kind": "oracle",

@@ -397,8 +397,10 @@ int wf_decode_step_host(const wf_dims* dims, const void* h_Q, const void* h_K,
  * Errors: WF_ERR_NULL, WF_ERR_UNSUPPORTED (n_moments outside 1..8). */
 int wf_daubechies_lowpass(int32_t n_moments, double* taps_out);
 
-/* Bytes of workspace wf_step_basis needs (it holds A_1..A_L in fp32, the
- * candidate lists, scores and logits).  Errors: as wf_workspace_bytes, plus
+/* Bytes of workspace wf_step_basis needs for these sizes, tap count and
+ * per-level k (the route of wf_step_basis below decides: the level-L logits
+ * and the path kernel's scratch, or A_1..A_L in fp32 with the candidate
+ * lists, scores and logits).  Errors: as wf_workspace_bytes, plus
  * WF_ERR_UNSUPPORTED for a tap count outside 2..16 or odd. */
 int wf_basis_workspace_bytes(const wf_dims* dims, int32_t taps,
                              const int32_t* k_per_level, size_t* bytes);
@@ -412,10 +414,18 @@ int wf_dwt_lowpass_basis(const wf_dims* dims, const double* lowpass,
                          int32_t taps, const void* Kp, float* A_all,
                          void* stream);
 
-/* The whole step with a longer basis: the pyramid (L launches), the
- * recursive filter (one CTA per unit), then steps 4-5 as in
- * wf_sparse_gather_attn.  Arguments as wf_step, plus the HOST filter
- * `lowpass` of `taps` doubles; workspace ≥ wf_basis_workspace_bytes().
+/* The whole step with a longer basis.  When every level between L and 0
+ * keeps all children (k_j = 2 k_{j+1} for 0 < j < L, the default schedule),
+ * the inputs are bf16, G <= 64 and the composed level-L filter has at most
+ * 4096 taps ((2^L - 1)(taps - 1) + 1), two launches: the level-L logits
+ * z_L[c] = Q·A_L[c]/√d with A_L[c] = Σ_m w[m] Kp[(2^L c + m) mod N_p] (the L
+ * periodic levels composed into one filter w, from the taps in double), then
+ * steps 2-5 of wf_step on them (the tokens under the coarse survivors are
+ * the same dyadic spans for any basis and are scored on their own keys).
+ * Otherwise the pyramid (L launches), the recursive filter (one CTA per
+ * unit), then steps 4-5 as in wf_sparse_gather_attn.  Arguments as wf_step,
+ * plus the HOST filter `lowpass` of `taps` doubles; workspace ≥
+ * wf_basis_workspace_bytes() for the same sizes, taps and k.
  * Errors: as wf_step, plus WF_ERR_UNSUPPORTED for a bad tap count. */
 int wf_step_basis(const wf_dims* dims, const double* lowpass, int32_t taps,
                   const void* Q, const void* Kp, const void* Vp,

@@ -241,8 +241,14 @@ def test_basis_entry_points_reject_before_launch(lib):
     p17 = ctypes.c_void_p((1 << 20) + 4)
     taps = (ctypes.c_double * 8)(*bd.daubechies_lowpass(4))
     n = ctypes.c_size_t(0)
+    # Every level between L and 0 keeps all children: the level-L logits and
+    # the path kernel's scratch; a level that discards: A_1..A_L in fp32.
     assert lib.wf_basis_workspace_bytes(ctypes.byref(dims), 8, k, ctypes.byref(n)) == 0
-    assert n.value > 32 * 4096 * 128 * 4 // 2  # holds A_1..A_L in fp32
+    assert 32 * 256 * 32 * 4 < n.value < 32 * 4096 * 128 * 4 // 2
+    k_sel = bd._k_array([400, 500, 256, 128, 64])
+    n_sel = ctypes.c_size_t(0)
+    assert lib.wf_basis_workspace_bytes(ctypes.byref(dims), 8, k_sel, ctypes.byref(n_sel)) == 0
+    assert n_sel.value > 32 * 4096 * 128 * 4 // 2
     assert lib.wf_basis_workspace_bytes(ctypes.byref(dims), 7, k, ctypes.byref(n)) == 3
     assert lib.wf_basis_workspace_bytes(ctypes.byref(dims), 18, k, ctypes.byref(n)) == 3
     assert lib.wf_dwt_lowpass_basis(ctypes.byref(dims), None, 8, p16, p16, None) == 1
@@ -258,5 +264,6 @@ def test_basis_entry_points_reject_before_launch(lib):
     assert step(q=None) == 1
     assert step(q=p17) == 7
     assert step(wsb=n.value - 1) == 4
+    assert step(k=k_sel, wsb=n_sel.value - 1) == 4
     assert step(k=bd._k_array([512, 512, 256, 128, 300])) == 2
     assert step(dims=_dims(n_prompt=4100)) == 2

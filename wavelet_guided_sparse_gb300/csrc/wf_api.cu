@@ -90,6 +90,18 @@ Layout layout(const LaunchDims& ld, const int32_t* k, const wf::PathPlan* fp) {
 
 int32_t* status_word(void* ws) { return static_cast<int32_t*>(ws); }
 
+// The longer-basis step takes the Haar path kernel with precomputed coarse
+// logits when every level between L and 0 keeps all children (then only the
+// level-L logits depend on the basis), the inputs are bf16, and the composed
+// level-L filter is short enough; returns the plan of that route.
+bool basis_coarse_route(const LaunchDims& ld, int32_t taps, const int32_t* k, wf::PathPlan* plan) {
+  if (ld.dtype != WF_BF16 || ld.n_gen > 64 || wf::basis_cascade_len(taps, ld.levels) < 0)
+    return false;
+  for (int j = 1; j < ld.levels; ++j)
+    if (k[j] != 2 * k[j + 1]) return false;
+  return wf::plan_path(ld, wf::kPhaseAll, k, k[ld.levels], k[0], wf::device_sm_count(), plan);
+}
+
 // Filter taps of a longer basis: 2..16 taps, an even count.
 int check_taps(const double* g, int32_t taps, wf::BasisTaps* t) {
   if (g == nullptr) return WF_ERR_NULL;
@@ -592,7 +604,9 @@ int wf_basis_workspace_bytes(const wf_dims* dims, int32_t taps, const int32_t* k
   if (taps < 2 || taps > 16 || taps % 2 != 0) return WF_ERR_UNSUPPORTED;
   st = check_k(ld, k_per_level);
   if (st != WF_OK) return st;
-  *bytes = basis_layout(ld, k_per_level).total;
+  wf::PathPlan plan;
+  *bytes = basis_coarse_route(ld, taps, k_per_level, &plan) ? layout(ld, k_per_level, &plan).total
+                                                            : basis_layout(ld, k_per_level).total;
   return WF_OK;
 }
 
@@ -629,6 +643,48 @@ int wf_step_basis(const wf_dims* dims, const double* lowpass, int32_t taps, cons
     return WF_ERR_ALIGNMENT;
   st = check_k(ld, k_per_level);
   if (st != WF_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  {
+    wf::PathPlan plan;
+    if (basis_coarse_route(ld, taps, k_per_level, &plan)) {
+      // Two launches: the basis's level-L logits, then steps 2-5 of the path
+      // kernel on them (the tokens under the coarse survivors are scored on
+      // their own keys, independent of the basis).
+      const Layout L = layout(ld, k_per_level, &plan);
+      if (workspace_bytes < L.total) return WF_ERR_WORKSPACE;
+      char* ws = static_cast<char*>(workspace);
+      float* zl = reinterpret_cast<float*>(ws + L.zl);
+      static thread_local wf::BasisCoarseParams cp;  // 16 KB of filter taps: off the stack
+      cp.q = Q;
+      cp.kp = Kp;
+      cp.zl = zl;
+      cp.n_prompt = ld.n_prompt;
+      cp.n_gen = ld.n_gen;
+      cp.levels = ld.levels;
+      cp.gz = wf::coarse_logit_pitch(ld.n_gen);
+      cp.zscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(ld.head_dim)));
+      cp.w_len = wf::basis_cascade(lowpass, taps, ld.levels, cp.w);
+      if (cp.w_len < 1) return WF_ERR_UNSUPPORTED;
+      cudaError_t ce = wf::launch_basis_coarse(ld, cp, s);
+      if (ce != cudaSuccess) return cuda_status(ce);
+      wf::PathArgs a = {};
+      a.q = Q;
+      a.kp = Kp;
+      a.vp = Vp;
+      a.kg = Kg;
+      a.vg = Vg;
+      a.zl = zl;
+      a.idx_out = idx_out;
+      a.o = O;
+      a.lse = lse;
+      a.status = status_word(workspace);
+      a.t_ws = reinterpret_cast<float*>(ws + L.t);
+      a.k = k_per_level;
+      a.k_l = k_per_level[ld.levels];
+      a.budget = k_per_level[0];
+      return cuda_status(wf::launch_path(ld, plan, a, s));
+    }
+  }
   const BasisLayout L = basis_layout(ld, k_per_level);
   if (workspace_bytes < L.total) return WF_ERR_WORKSPACE;
   wf::PathPlan plan;  // steps 4-5 must be plannable before anything is enqueued
@@ -636,7 +692,6 @@ int wf_step_basis(const wf_dims* dims, const double* lowpass, int32_t taps, cons
                      &plan))
     return WF_ERR_UNSUPPORTED;
   char* ws = static_cast<char*>(workspace);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* a_all = reinterpret_cast<float*>(ws + L.a_all);
   cudaError_t ce = wf::launch_basis_pyramid(ld, Kp, a_all, t, s);
   if (ce != cudaSuccess) return cuda_status(ce);

@@ -33,6 +33,7 @@
 
 #include "wf_common.cuh"
 #include "wf_internal.h"
+#include "wf_mma.cuh"
 
 namespace wf {
 
@@ -241,6 +242,154 @@ __global__ void __launch_bounds__(kThreads) basis_filter_kernel(BasisFilterParam
   }
 }
 
+// ------------------------------------------------- coarse logits of a basis
+//
+// With every level between L and 0 keeping all children (k_j = 2 k_{j+1}),
+// the step needs only the level-L logits of the basis pyramid: the tokens
+// under the coarse survivors are the same dyadic spans as in the Haar case
+// and are scored on their own keys.  The L periodic levels compose into one
+// periodic filter of the tokens,
+//   A_L[c] = Σ_m w[m] · Kp[(2^L c + m) mod N_p],   m < W = (2^L - 1)(F - 1) + 1,
+//   w = g for L = 1,   w_j[t] = Σ_k g[k] · w_{j-1}[t - 2^{j-1} k]
+// (periodic extension commutes with the composition because 2 (x mod M) mod
+// 2M = 2x mod 2M), so the logits are the same filter applied to the token
+// logits:  z_L[c][q] = Σ_m w[m] · (Q_q · Kp[(2^L c + m) mod N_p]).
+// basis_coarse_kernel: a CTA takes up to kCoarsePos consecutive coarse
+// positions, streams the token rows under their filter windows through a
+// two-stage cp.async ring of 64-row tiles, forms each tile's token logits on
+// the tensor cores (mma.sync, bf16 in, fp32 out) and adds them into its
+// (position, query) accumulators with the filter weights.
+constexpr int kCoarsePos = 32;   // coarse positions per CTA
+constexpr int kCoarseRows = 64;  // token rows per tile
+
+template <int D>
+struct CoarseSmem {
+  static constexpr int kPitch = D * 2 + 16;  // bf16 row pitch (conflict-free fragment loads)
+  static constexpr size_t kQ = 0;
+  static constexpr size_t kStage = kQ + static_cast<size_t>(64) * kPitch;
+  static constexpr size_t kZ = kStage + static_cast<size_t>(2) * kCoarseRows * kPitch;
+  static constexpr size_t kW = kZ + sizeof(float) * kCoarseRows * 65;
+  static constexpr size_t kTotal = kW + sizeof(float) * kMaxCascade;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 2) basis_coarse_kernel(const __grid_constant__ BasisCoarseParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  using S = CoarseSmem<D>;
+  constexpr int RB = S::kPitch, C16 = D / 8;  // 16-byte chunks per row
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t u = blockIdx.y;
+  const int G = p.n_gen, L = p.levels, N = p.n_prompt, P = N >> L, W = p.w_len;
+  const int c0 = blockIdx.x * kCoarsePos;
+  const int ncp = min(kCoarsePos, P - c0);
+  const int nrows = ((ncp - 1) << L) + W;
+  const int nch = (nrows + kCoarseRows - 1) / kCoarseRows;
+  const int64_t base = static_cast<int64_t>(c0) << L;
+  const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(p.kp) + u * N * D;
+  unsigned char* qs = smem + S::kQ;
+  float* zt = reinterpret_cast<float*>(smem + S::kZ);
+  float* ws = reinterpret_cast<float*>(smem + S::kW);
+  const int ZT = G | 1;
+
+  auto issue = [&](int ch, int stage) {
+    unsigned char* dst = smem + S::kStage + static_cast<size_t>(stage) * kCoarseRows * RB;
+    for (int e = tid; e < kCoarseRows * C16; e += kThreads) {
+      const int r = e / C16, c = e % C16;
+      const int64_t rel = static_cast<int64_t>(ch) * kCoarseRows + r;
+      const int64_t row = (base + (rel < nrows ? rel : 0)) % N;
+      cp_async16(dst + r * RB + c * 16, kp + row * D + c * 8);
+    }
+    cp_async_commit();
+  };
+  issue(0, 0);
+  if (nch > 1) issue(1, 1);
+  // Queries (rows >= G zero) and the filter weights.
+  {
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q) + u * G * D;
+    for (int e = tid; e < 64 * C16; e += kThreads) {
+      const int r = e / C16, c = e % C16;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (r < G) v = *reinterpret_cast<const uint4*>(q + r * D + c * 8);
+      *reinterpret_cast<uint4*>(qs + r * RB + c * 16) = v;
+    }
+    for (int m = tid; m < W; m += kThreads) ws[m] = p.w[m];
+  }
+  // Accumulators: item it = tid + kThreads i is (position it / G, query it % G).
+  constexpr int kItems = kCoarsePos * 64 / kThreads;
+  float acc[kItems];
+#pragma unroll
+  for (int i = 0; i < kItems; ++i) acc[i] = 0.f;
+  const int rb = 16 * (warp & 3);  // this warp's 16 rows of a tile
+  const int NT = (G + 7) >> 3;
+  const uint32_t qb = smem_u32(qs);
+  for (int ch = 0; ch < nch; ++ch) {
+    const int stage = ch & 1;
+    if (ch + 1 < nch) cp_async_wait<1>(); else cp_async_wait<0>();
+    __syncthreads();  // tile ch landed; every thread is done with the previous logits
+    // Token logits of the tile: rows rb..rb+15, query tiles warp / 4 + 2t.
+    {
+      const uint32_t kb = smem_u32(smem + S::kStage + static_cast<size_t>(stage) * kCoarseRows * RB);
+      const uint32_t arow = kb + (rb + (lane & 15)) * RB + (lane >> 4) * 16;
+      float c[4][4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c[t][e] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(arow + ks * 32, a);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int nt = (warp >> 2) + 2 * t;
+          if (nt < NT) {
+            const uint32_t ba = qb + (nt * 8 + (lane >> 2)) * RB + ks * 32 + (lane & 3) * 4;
+            uint32_t b[2];
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b[0]) : "r"(ba));
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b[1]) : "r"(ba + 16));
+            mma_bf16(c[t], a, b);
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int nt = (warp >> 2) + 2 * t;
+        if (nt >= NT) break;
+        const int col = nt * 8 + 2 * (lane & 3);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = rb + (lane >> 2) + 8 * h;
+          if (col < G) zt[r * ZT + col] = c[t][2 * h];
+          if (col + 1 < G) zt[r * ZT + col + 1] = c[t][2 * h + 1];
+        }
+      }
+    }
+    __syncthreads();  // the tile's logits are complete; its stage may be refilled
+    if (ch + 2 < nch) issue(ch + 2, stage);
+    // Filter the tile's logits into the accumulators.
+    const int r0 = ch * kCoarseRows;
+#pragma unroll
+    for (int i = 0; i < kItems; ++i) {
+      const int it = tid + kThreads * i;
+      const int cr = it / G, q = it - cr * G;
+      if (cr < ncp) {
+        const int w0 = cr << L;  // first row of the position's window
+        const int lo = max(r0, w0), hi = min(r0 + kCoarseRows, w0 + W);
+        float s = acc[i];
+        for (int r = lo; r < hi; ++r) s = fmaf(ws[r - w0], zt[(r - r0) * ZT + q], s);
+        acc[i] = s;
+      }
+    }
+  }
+  float* out = p.zl + (u * P + c0) * p.gz;
+#pragma unroll
+  for (int i = 0; i < kItems; ++i) {
+    const int it = tid + kThreads * i;
+    const int cr = it / G, q = it - cr * G;
+    if (cr < ncp) out[cr * p.gz + q] = acc[i] * p.zscale;
+  }
+}
+
 template <typename T, int D>
 cudaError_t launch_pyramid_typed(const LaunchDims& ld, const void* kp, float* a_all,
                                  const BasisTaps& taps, cudaStream_t stream) {
@@ -363,6 +512,45 @@ cudaError_t launch_basis_filter(const LaunchDims& ld, const BasisFilterParams& p
   }
   if (ld.head_dim == 128) return launch_filter_typed<float, 128>(ld, p, stream);
   return launch_filter_typed<float, 64>(ld, p, stream);
+}
+
+int basis_cascade_len(int taps, int levels) {
+  const int64_t len = ((int64_t{1} << levels) - 1) * (taps - 1) + 1;
+  return len > kMaxCascade ? -1 : static_cast<int>(len);
+}
+
+int basis_cascade(const double* g, int taps, int levels, float* w) {
+  const int W = basis_cascade_len(taps, levels);
+  if (W < 0) return -1;
+  std::vector<double> cur(g, g + taps), next;
+  for (int j = 2; j <= levels; ++j) {
+    const int len = ((1 << j) - 1) * (taps - 1) + 1, step = 1 << (j - 1);
+    next.assign(len, 0.0);
+    for (int k = 0; k < taps; ++k)
+      for (size_t m = 0; m < cur.size(); ++m) next[k * step + m] += g[k] * cur[m];
+    cur.swap(next);
+  }
+  for (int m = 0; m < W; ++m) w[m] = static_cast<float>(cur[m]);
+  return W;
+}
+
+cudaError_t launch_basis_coarse(const LaunchDims& ld, const BasisCoarseParams& p,
+                                cudaStream_t stream) {
+  if (ld.dtype != WF_BF16 || p.w_len < 1 || p.w_len > kMaxCascade || ld.n_gen > 64)
+    return cudaErrorInvalidValue;
+  const int P = ld.n_prompt >> ld.levels;
+  const dim3 grid(static_cast<unsigned>((P + kCoarsePos - 1) / kCoarsePos),
+                  static_cast<unsigned>(ld.units));
+  if (ld.head_dim == 128) {
+    const cudaError_t e = ensure_max_smem<basis_coarse_kernel<128>>();
+    if (e != cudaSuccess) return e;
+    basis_coarse_kernel<128><<<grid, kThreads, CoarseSmem<128>::kTotal, stream>>>(p);
+  } else {
+    const cudaError_t e = ensure_max_smem<basis_coarse_kernel<64>>();
+    if (e != cudaSuccess) return e;
+    basis_coarse_kernel<64><<<grid, kThreads, CoarseSmem<64>::kTotal, stream>>>(p);
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace wf

@@ -139,6 +139,26 @@ cudaError_t launch_basis_pyramid(const LaunchDims& ld, const void* kp, float* a_
                                  const BasisTaps& taps, cudaStream_t stream);
 cudaError_t launch_basis_filter(const LaunchDims& ld, const BasisFilterParams& p,
                                 cudaStream_t stream);
+// Level-L coarse logits of a longer basis in one pass over the tokens: the
+// L periodic levels composed into one filter w of w_len taps (see
+// basis_cascade), z_L[c][q] = zscale Σ_m w[m] Q_q·Kp[(2^L c + m) mod N_p],
+// written to zl [U, P, gz] (bf16 inputs).
+constexpr int kMaxCascade = 4096;
+struct BasisCoarseParams {
+  const void* q;
+  const void* kp;
+  float* zl;
+  int n_prompt, n_gen, levels, w_len, gz;
+  float zscale;
+  float w[kMaxCascade];
+};
+// The composed filter of `levels` periodic levels of the low-pass g (taps
+// doubles, computed in double, stored as fp32 in w); returns its length
+// (levels·... = (2^levels - 1)(taps - 1) + 1), or -1 if above kMaxCascade.
+int basis_cascade(const double* g, int taps, int levels, float* w);
+int basis_cascade_len(int taps, int levels);
+cudaError_t launch_basis_coarse(const LaunchDims& ld, const BasisCoarseParams& p,
+                                cudaStream_t stream);
 
 // Dynamic shared memory the planners allow per CTA (the sm_103a opt-in limit
 // is 227 KB; a little is left for static shared memory).

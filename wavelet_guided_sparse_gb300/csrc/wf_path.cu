@@ -566,6 +566,76 @@ __device__ __forceinline__ void tmem_row_to_smem(uint32_t taddr, int N, int cols
   }
 }
 
+// Coarse logits of `rows` (<= 64) rows of an fp32 A_L in shared memory (D
+// floats apart) against the unit's queries in the tensor-core operand layout
+// (qs, bf16, rows >= G zero), into z (row pitch `pitch`, scaled by zscale), on
+// the warps' mma.sync units: each A_L value is split exactly into three bf16
+// parts in registers, whose products with the bf16 queries are exact (fp32
+// accumulation).  Warp w takes rows 16 (w % 4) .. + 15 and the query tiles
+// w / 4, w / 4 + 2, ... (8 queries each).  Block-wide (every warp calls it).
+template <int D>
+__device__ __forceinline__ void coarse_logits_ring(const float* a, int rows, const unsigned char* qs,
+                                                   int G, float* z, int pitch, float zscale) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, gid = lane >> 2, tig = lane & 3;
+  const int rb = 16 * (warp & 3);
+  if (rb >= rows) return;
+  const int NT = (G + 7) >> 3;
+  constexpr int kMaxTiles = 4;  // G <= 64: at most 8 query tiles over two warps
+  float c[kMaxTiles][4];
+#pragma unroll
+  for (int t = 0; t < kMaxTiles; ++t)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) c[t][e] = 0.f;
+  const bool r0ok = rb + gid < rows, r1ok = rb + gid + 8 < rows;
+  const float* a0 = a + (rb + gid) * D;
+  const float* a1 = a0 + 8 * D;
+  const uint32_t q0 = smem_u32(qs);
+#pragma unroll 2
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const int k0 = ks * 16 + 2 * tig;
+    float2 v[4];  // (row gid, k0), (row gid + 8, k0), (row gid, k0 + 8), (row gid + 8, k0 + 8)
+    v[0] = r0ok ? *reinterpret_cast<const float2*>(a0 + k0) : make_float2(0.f, 0.f);
+    v[1] = r1ok ? *reinterpret_cast<const float2*>(a1 + k0) : make_float2(0.f, 0.f);
+    v[2] = r0ok ? *reinterpret_cast<const float2*>(a0 + k0 + 8) : make_float2(0.f, 0.f);
+    v[3] = r1ok ? *reinterpret_cast<const float2*>(a1 + k0 + 8) : make_float2(0.f, 0.f);
+    uint32_t af[3][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float h0, m0, l0, h1, m1, l1;
+      split3_bf16(v[i].x, h0, m0, l0);
+      split3_bf16(v[i].y, h1, m1, l1);
+      af[0][i] = pack_bf16(h0, h1);
+      af[1][i] = pack_bf16(m0, m1);
+      af[2][i] = pack_bf16(l0, l1);
+    }
+#pragma unroll
+    for (int t = 0; t < kMaxTiles; ++t) {
+      const int nt = (warp >> 2) + 2 * t;
+      if (nt >= NT) break;
+      // Queries nt * 8 + gid, k0 and k0 + 8: two bf16 each, from the core-matrix layout.
+      const uint32_t qa = q0 + cm_offset(nt * 8 + gid, k0 >> 3, D * 16) + (k0 & 7) * 2;
+      uint32_t b[2];
+      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b[0]) : "r"(qa));
+      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b[1]) : "r"(qa + 128));
+#pragma unroll
+      for (int pl = 0; pl < 3; ++pl) mma_bf16(c[t], af[pl], b);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kMaxTiles; ++t) {
+    const int nt = (warp >> 2) + 2 * t;
+    if (nt >= NT) break;
+    const int col = nt * 8 + 2 * tig;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = rb + gid + 8 * h;
+      if (r >= rows) continue;
+      if (col < G) z[r * pitch + col] = c[t][2 * h] * zscale;
+      if (col + 1 < G) z[r * pitch + col + 1] = c[t][2 * h + 1] * zscale;
+    }
+  }
+}
+
 // ============================================================== the kernel
 // kVar selects an instantiation with the common decisions constant:
 // 0: general (every decision read from the parameters); 1: the single-launch
@@ -696,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
     }
     cp_async_commit();
-    if (!fuse_dwt) cp_async_wait<0>();
+    if (!fuse_dwt && !al_stage) cp_async_wait<0>();
   }
   tc_fence_before();
   __syncthreads();
@@ -812,34 +882,14 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       }
       __syncthreads();
     } else if (sizeof(T) == 2 && al_stage) {
-      // Cached A_L: the rows landed in the ring; each value is split exactly
-      // into three bf16 parts written to the tile operand planes (one thread
-      // per 4 values), then the logits are formed as in the fused case.  A
+      // Cached A_L: the rows landed in the ring (fp32, D floats apart); the
+      // warps form their logits with the queries straight from there.  A
       // timed-out copy is waited for once more (bounded) before the ring is
       // reused; the status word reports it.
       if (!mbar_wait_bounded(&bars[0], 0u, p.status)) (void)mbar_wait_bounded(&bars[0], 0u, p.status);
-      const float* ring = reinterpret_cast<const float*>(smem + L.s_ring);
-      for (int it = tid; it < Pc * (D / 4); it += kThreads) {
-        const int row = it / (D / 4), q4 = it % (D / 4), ch = q4 >> 1, h = q4 & 1;
-        const float4 v = *reinterpret_cast<const float4*>(ring + row * D + 4 * q4);
-        const float a[4] = {v.x, v.y, v.z, v.w};
-        uint32_t w[3][2];
-#pragma unroll
-        for (int e = 0; e < 4; e += 2) {
-          float h0, m0, l0, h1, m1, l1;
-          split3_bf16(a[e], h0, m0, l0);
-          split3_bf16(a[e + 1], h1, m1, l1);
-          w[0][e / 2] = pack_bf16(h0, h1);
-          w[1][e / 2] = pack_bf16(m0, m1);
-          w[2][e / 2] = pack_bf16(l0, l1);
-        }
-#pragma unroll
-        for (int pl = 0; pl < 3; ++pl)
-          *reinterpret_cast<uint2*>(as + pl * kPlaneBytes + sw_offset(row, ch, kScoreChunk) + h * 8) =
-              make_uint2(w[pl][0], w[pl][1]);
-      }
-      umma_logits<D>(as, 3, kPlaneBytes, kScoreChunk, Pc, qs, G, zc, 0, TS, zscale, tmem, mma_bar,
-                     mma_phase, p.status);
+      cp_async_wait<0>();  // the queries
+      __syncthreads();
+      coarse_logits_ring<D>(reinterpret_cast<const float*>(smem + L.s_ring), Pc, qs, G, zc, TS, zscale);
       __syncthreads();
     }
     // Coarse logits of positions [c0, c0 + rows) into zc: read from global
@@ -1759,7 +1809,12 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     }
   }
   tc_fence_before();
-  cluster.sync();  // peers may still read or write this CTA's shared memory
+  // Peers may still read or write this CTA's shared memory, unless the attend
+  // phase ran: its cluster barrier followed the last such access.
+  if (mode & kModeAttend)
+    __syncthreads();
+  else
+    cluster.sync();
   if (use_tmem && warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
