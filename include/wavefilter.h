@@ -417,7 +417,7 @@ int wf_dwt_lowpass_basis(const wf_dims* dims, const double* lowpass,
 /* The whole step with a longer basis.  When every level between L and 0
  * keeps all children (k_j = 2 k_{j+1} for 0 < j < L, the default schedule),
  * the inputs are bf16, G <= 64 and the composed level-L filter has at most
- * 4096 taps ((2^L - 1)(taps - 1) + 1), two launches: the level-L logits
+ * 2048 taps ((2^L - 1)(taps - 1) + 1), two launches: the level-L logits
  * z_L[c] = Q·A_L[c]/√d with A_L[c] = Σ_m w[m] Kp[(2^L c + m) mod N_p] (the L
  * periodic levels composed into one filter w, from the taps in double), then
  * steps 2-5 of wf_step on them (the tokens under the coarse survivors are

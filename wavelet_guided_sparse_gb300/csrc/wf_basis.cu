@@ -256,18 +256,19 @@ __global__ void __launch_bounds__(kThreads) basis_filter_kernel(BasisFilterParam
 // logits:  z_L[c][q] = Σ_m w[m] · (Q_q · Kp[(2^L c + m) mod N_p]).
 // basis_coarse_kernel: a CTA takes up to kCoarsePos consecutive coarse
 // positions, streams the token rows under their filter windows through a
-// two-stage cp.async ring of 64-row tiles, forms each tile's token logits on
+// four-stage cp.async ring of 64-row tiles, forms each tile's token logits on
 // the tensor cores (mma.sync, bf16 in, fp32 out) and adds them into its
 // (position, query) accumulators with the filter weights.
 constexpr int kCoarsePos = 32;   // coarse positions per CTA
 constexpr int kCoarseRows = 64;  // token rows per tile
+constexpr int kCoarseStages = 4;  // tiles in flight (two CTAs per SM)
 
 template <int D>
 struct CoarseSmem {
   static constexpr int kPitch = D * 2 + 16;  // bf16 row pitch (conflict-free fragment loads)
   static constexpr size_t kQ = 0;
   static constexpr size_t kStage = kQ + static_cast<size_t>(64) * kPitch;
-  static constexpr size_t kZ = kStage + static_cast<size_t>(2) * kCoarseRows * kPitch;
+  static constexpr size_t kZ = kStage + static_cast<size_t>(kCoarseStages) * kCoarseRows * kPitch;
   static constexpr size_t kW = kZ + sizeof(float) * kCoarseRows * 65;
   static constexpr size_t kTotal = kW + sizeof(float) * kMaxCascade;
 };
@@ -301,8 +302,7 @@ __global__ void __launch_bounds__(kThreads, 2) basis_coarse_kernel(const __grid_
     }
     cp_async_commit();
   };
-  issue(0, 0);
-  if (nch > 1) issue(1, 1);
+  for (int ch = 0; ch < kCoarseStages && ch < nch; ++ch) issue(ch, ch);
   // Queries (rows >= G zero) and the filter weights.
   {
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q) + u * G * D;
@@ -323,8 +323,14 @@ __global__ void __launch_bounds__(kThreads, 2) basis_coarse_kernel(const __grid_
   const int NT = (G + 7) >> 3;
   const uint32_t qb = smem_u32(qs);
   for (int ch = 0; ch < nch; ++ch) {
-    const int stage = ch & 1;
-    if (ch + 1 < nch) cp_async_wait<1>(); else cp_async_wait<0>();
+    const int stage = ch % kCoarseStages;
+    // Tiles issued so far: 0 .. min(ch + kCoarseStages, nch) - 1; tile ch must have landed.
+    switch (min(kCoarseStages - 1, nch - 1 - ch)) {
+      case 0: cp_async_wait<0>(); break;
+      case 1: cp_async_wait<1>(); break;
+      case 2: cp_async_wait<2>(); break;
+      default: cp_async_wait<3>(); break;
+    }
     __syncthreads();  // tile ch landed; every thread is done with the previous logits
     // Token logits of the tile: rows rb..rb+15, query tiles warp / 4 + 2t.
     {
@@ -365,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 2) basis_coarse_kernel(const __grid_
       }
     }
     __syncthreads();  // the tile's logits are complete; its stage may be refilled
-    if (ch + 2 < nch) issue(ch + 2, stage);
+    if (ch + kCoarseStages < nch) issue(ch + kCoarseStages, stage);
     // Filter the tile's logits into the accumulators.
     const int r0 = ch * kCoarseRows;
 #pragma unroll

@@ -143,7 +143,7 @@ cudaError_t launch_basis_filter(const LaunchDims& ld, const BasisFilterParams& p
 // L periodic levels composed into one filter w of w_len taps (see
 // basis_cascade), z_L[c][q] = zscale Σ_m w[m] Q_q·Kp[(2^L c + m) mod N_p],
 // written to zl [U, P, gz] (bf16 inputs).
-constexpr int kMaxCascade = 4096;
+constexpr int kMaxCascade = 2048;
 struct BasisCoarseParams {
   const void* q;
   const void* kp;

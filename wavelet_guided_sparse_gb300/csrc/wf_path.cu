@@ -1134,6 +1134,16 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         loc_m[tid] = m;
         loc_l[tid] = l;
       }
+      if (warp == 2 && (mode & kModeAttend)) {  // (G <= 64: no thread of warp 2 merged above)
+        // Every span row has been read: the value rows of the same spans go to
+        // L2 now (whole spans, streamed), so the attention's row gather after
+        // the final selection finds them there instead of in HBM.
+        const unsigned char* vrows = reinterpret_cast<const unsigned char*>(
+            static_cast<const T*>(p.vp) + unit * p.n_prompt * D);
+        const uint32_t span_b = static_cast<uint32_t>(D * sizeof(T)) << levels;
+        for (int i = lane; i < ns; i += 32)
+          bulk_prefetch_l2(vrows + static_cast<int64_t>(sl_all[s0 + i]) * span_b, span_b);
+      }
       __syncthreads();
       cluster_merge_stats(loc_m, loc_l, G, stat_in, gm, ginv, R, gather_all ? cnt_b : nullptr);
 
