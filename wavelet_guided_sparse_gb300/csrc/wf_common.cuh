@@ -208,11 +208,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // on with commit/wait groups.  Used for gathers of many small rows, where
 // one instruction per thread per 16 bytes keeps the copies in flight without
 // per-copy descriptor overhead.
-// L2 prefetch of [src, src + bytes) by the bulk-copy engine (nothing to wait
-// for); src 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
                : "memory");

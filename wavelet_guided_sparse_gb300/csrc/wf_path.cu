@@ -572,13 +572,14 @@ __device__ __forceinline__ void tmem_row_to_smem(uint32_t taddr, int N, int cols
 // the warps' mma.sync units: each A_L value is split exactly into three bf16
 // parts in registers, whose products with the bf16 queries are exact (fp32
 // accumulation).  Warp w takes rows 16 (w % 4) .. + 15 and the query tiles
-// w / 4, w / 4 + 2, ... (8 queries each).  Block-wide (every warp calls it).
+// w / 4, w / 4 + 2, ... (8 queries each).  z may overlay the A_L rows: every
+// warp has read its rows (block barrier) before any result is stored.
+// Block-wide (every thread calls it).
 template <int D>
 __device__ __forceinline__ void coarse_logits_ring(const float* a, int rows, const unsigned char* qs,
                                                    int G, float* z, int pitch, float zscale) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, gid = lane >> 2, tig = lane & 3;
   const int rb = 16 * (warp & 3);
-  if (rb >= rows) return;
   const int NT = (G + 7) >> 3;
   constexpr int kMaxTiles = 4;  // G <= 64: at most 8 query tiles over two warps
   float c[kMaxTiles][4];
@@ -586,41 +587,45 @@ __device__ __forceinline__ void coarse_logits_ring(const float* a, int rows, con
   for (int t = 0; t < kMaxTiles; ++t)
 #pragma unroll
     for (int e = 0; e < 4; ++e) c[t][e] = 0.f;
-  const bool r0ok = rb + gid < rows, r1ok = rb + gid + 8 < rows;
-  const float* a0 = a + (rb + gid) * D;
-  const float* a1 = a0 + 8 * D;
-  const uint32_t q0 = smem_u32(qs);
+  if (rb < rows) {
+    const bool r0ok = rb + gid < rows, r1ok = rb + gid + 8 < rows;
+    const float* a0 = a + (rb + gid) * D;
+    const float* a1 = a0 + 8 * D;
+    const uint32_t q0 = smem_u32(qs);
 #pragma unroll 2
-  for (int ks = 0; ks < D / 16; ++ks) {
-    const int k0 = ks * 16 + 2 * tig;
-    float2 v[4];  // (row gid, k0), (row gid + 8, k0), (row gid, k0 + 8), (row gid + 8, k0 + 8)
-    v[0] = r0ok ? *reinterpret_cast<const float2*>(a0 + k0) : make_float2(0.f, 0.f);
-    v[1] = r1ok ? *reinterpret_cast<const float2*>(a1 + k0) : make_float2(0.f, 0.f);
-    v[2] = r0ok ? *reinterpret_cast<const float2*>(a0 + k0 + 8) : make_float2(0.f, 0.f);
-    v[3] = r1ok ? *reinterpret_cast<const float2*>(a1 + k0 + 8) : make_float2(0.f, 0.f);
-    uint32_t af[3][4];
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const int k0 = ks * 16 + 2 * tig;
+      float2 v[4];  // (row gid, k0), (row gid + 8, k0), (row gid, k0 + 8), (row gid + 8, k0 + 8)
+      v[0] = r0ok ? *reinterpret_cast<const float2*>(a0 + k0) : make_float2(0.f, 0.f);
+      v[1] = r1ok ? *reinterpret_cast<const float2*>(a1 + k0) : make_float2(0.f, 0.f);
+      v[2] = r0ok ? *reinterpret_cast<const float2*>(a0 + k0 + 8) : make_float2(0.f, 0.f);
+      v[3] = r1ok ? *reinterpret_cast<const float2*>(a1 + k0 + 8) : make_float2(0.f, 0.f);
+      uint32_t af[3][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float h0, m0, l0, h1, m1, l1;
-      split3_bf16(v[i].x, h0, m0, l0);
-      split3_bf16(v[i].y, h1, m1, l1);
-      af[0][i] = pack_bf16(h0, h1);
-      af[1][i] = pack_bf16(m0, m1);
-      af[2][i] = pack_bf16(l0, l1);
-    }
+      for (int i = 0; i < 4; ++i) {
+        float h0, m0, l0, h1, m1, l1;
+        split3_bf16(v[i].x, h0, m0, l0);
+        split3_bf16(v[i].y, h1, m1, l1);
+        af[0][i] = pack_bf16(h0, h1);
+        af[1][i] = pack_bf16(m0, m1);
+        af[2][i] = pack_bf16(l0, l1);
+      }
 #pragma unroll
-    for (int t = 0; t < kMaxTiles; ++t) {
-      const int nt = (warp >> 2) + 2 * t;
-      if (nt >= NT) break;
-      // Queries nt * 8 + gid, k0 and k0 + 8: two bf16 each, from the core-matrix layout.
-      const uint32_t qa = q0 + cm_offset(nt * 8 + gid, k0 >> 3, D * 16) + (k0 & 7) * 2;
-      uint32_t b[2];
-      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b[0]) : "r"(qa));
-      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b[1]) : "r"(qa + 128));
+      for (int t = 0; t < kMaxTiles; ++t) {
+        const int nt = (warp >> 2) + 2 * t;
+        if (nt >= NT) break;
+        // Queries nt * 8 + gid, k0 and k0 + 8: two bf16 each, from the core-matrix layout.
+        const uint32_t qa = q0 + cm_offset(nt * 8 + gid, k0 >> 3, D * 16) + (k0 & 7) * 2;
+        uint32_t b[2];
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b[0]) : "r"(qa));
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b[1]) : "r"(qa + 128));
 #pragma unroll
-      for (int pl = 0; pl < 3; ++pl) mma_bf16(c[t], af[pl], b);
+        for (int pl = 0; pl < 3; ++pl) mma_bf16(c[t], af[pl], b);
+      }
     }
   }
+  __syncthreads();  // every warp has read its A_L rows
+  if (rb >= rows) return;
 #pragma unroll
   for (int t = 0; t < kMaxTiles; ++t) {
     const int nt = (warp >> 2) + 2 * t;
@@ -1133,16 +1138,6 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         for (int w = 0; w < 4; ++w) merge_ml(m, l, part_m[w * kMaxQ + tid], part_l[w * kMaxQ + tid]);
         loc_m[tid] = m;
         loc_l[tid] = l;
-      }
-      if (warp == 2 && (mode & kModeAttend)) {  // (G <= 64: no thread of warp 2 merged above)
-        // Every span row has been read: the value rows of the same spans go to
-        // L2 now (whole spans, streamed), so the attention's row gather after
-        // the final selection finds them there instead of in HBM.
-        const unsigned char* vrows = reinterpret_cast<const unsigned char*>(
-            static_cast<const T*>(p.vp) + unit * p.n_prompt * D);
-        const uint32_t span_b = static_cast<uint32_t>(D * sizeof(T)) << levels;
-        for (int i = lane; i < ns; i += 32)
-          bulk_prefetch_l2(vrows + static_cast<int64_t>(sl_all[s0 + i]) * span_b, span_b);
       }
       __syncthreads();
       cluster_merge_stats(loc_m, loc_l, G, stat_in, gm, ginv, R, gather_all ? cnt_b : nullptr);
