@@ -94,8 +94,8 @@ struct PathParams {
   int filter_fast;         // token logits: 0 general path; 1 tensor-memory resident; 2 streamed twice
   int f_nb;                // fast filter: tensor-memory accumulator slots
   int fuse_dwt;            // score: A_L from K_p inside this kernel
-  int al_stage;            // score: this CTA's rows of the cached fp32 A_L arrive by one
-                           // bulk copy and go to the tensor cores (per_cta_p <= kScoreChunk)
+  int al_stage;            // score: this CTA's rows of the cached fp32 A_L arrive by bulk
+                           // copies, 64 rows a stage (per_cta_p <= kZRows)
   uint32_t inject_polls;   // fault injection (tests): see the fused step 1 below
   float al_scale;          // 2^(-L/2), the orthonormal Haar low-pass gain
   int k[WF_MAX_LEVELS + 1];
@@ -147,16 +147,30 @@ struct PathSmem {
     const size_t u = o;
     size_t end = u;
     s_ring = 0;
-    if ((p.mode & kModeScore) && (p.fuse_dwt || p.al_stage)) {
-      // Fused step 1: the bulk-copy ring of K_p rows (or the one copy of the
-      // cached A_L rows), then A_L in the tile operand layout (bf16: hi / mid
-      // / lo planes; fp32: rows).  The logits overwrite the ring once every
-      // stage has been consumed.
+    if ((p.mode & kModeScore) && p.fuse_dwt) {
+      // Fused step 1: the bulk-copy ring of K_p rows, then A_L in the tile
+      // operand layout (bf16: hi / mid / lo planes; fp32: rows).  The logits
+      // overwrite the ring once every stage has been consumed.
       o = u;
-      const size_t al_b = sizeof(float) * kScoreChunk * (D > kMaxQ + 1 ? D : kMaxQ + 1);
-      s_ring = take_bytes(p.fuse_dwt ? static_cast<size_t>(kFuseStages) * kFuseStageBytes : al_b);
+      s_ring = take_bytes(static_cast<size_t>(kFuseStages) * kFuseStageBytes);
       s_as = take_bytes((sizeof(T) == 2 ? 3 : 1) * kScoreChunk * kRowBytes, 1024);
       s_stage = s_z = s_ring;
+      end = end > o ? end : o;
+    } else if ((p.mode & kModeScore) && p.al_stage) {
+      // Cached A_L by bulk copies of 64 fp32 rows: one stage, which the
+      // logits then overwrite, when the CTA has at most 64 positions; else a
+      // ring of kFuseStages stages with the logits tile beside it.
+      o = u;
+      const size_t stage_b = sizeof(float) * kScoreChunk * D;
+      const size_t z_b = sizeof(float) * static_cast<size_t>(p.per_cta_p) * (p.G | 1);
+      if (p.per_cta_p <= kScoreChunk) {
+        s_ring = take_bytes(stage_b > z_b ? stage_b : z_b);
+        s_z = s_ring;
+      } else {
+        s_ring = take_bytes(static_cast<size_t>(kFuseStages) * stage_b);
+        s_z = take_bytes(z_b);
+      }
+      s_stage = s_as = s_ring;
       end = end > o ? end : o;
     } else if (p.mode & kModeScore) {
       // Coarse logits of up to kZRows positions, padded rows of GZ + 4 floats.
@@ -726,25 +740,34 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
              fuse_src + static_cast<int64_t>(st) * kFuseStageBytes, bytes, bar);
   };
   int fuse_issued = min(kFuseStages, fuse_nst);
+  // Cached A_L: stages of kScoreChunk fp32 rows of this CTA's contiguous range.
+  const int al_nst = al_stage ? (p.per_cta_p + kScoreChunk - 1) / kScoreChunk : 0;
+  const int al_nring = al_nst > 1 ? kFuseStages : 1;
+  auto al_issue = [&](int st) {  // thread 0 only
+    const int rows = min(kScoreChunk, p.per_cta_p - st * kScoreChunk);
+    const uint32_t bytes = static_cast<uint32_t>(rows) * D * static_cast<uint32_t>(sizeof(float));
+    uint64_t* bar = &bars[st % al_nring];
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(smem + L.s_ring + static_cast<size_t>(st % al_nring) * kScoreChunk * D * sizeof(float),
+             p.al + (unit * p.P + static_cast<int64_t>(rank) * p.per_cta_p + st * kScoreChunk) * D,
+             bytes, bar);
+  };
+  int al_issued = min(al_nring, al_nst);
   // Fault injection (tests of the bounded waits): in the first CTA, stage 0
   // of the ring is never issued and its wait gives up after inject_polls polls.
   const bool inject = fuse_dwt && p.inject_polls != 0 && blockIdx.x == 0 && blockIdx.y == 0;
   if (tid == 0) {
     if (fuse_dwt)
       for (int i = 0; i < kFuseStages; ++i) mbar_init(&bars[i], 1);
-    if (al_stage) mbar_init(&bars[0], 1);
+    if (al_stage)
+      for (int i = 0; i < al_nring; ++i) mbar_init(&bars[i], 1);
     mbar_init(mma_bar, 1);
     mbar_init(span_bar, 1);
     fence_mbar_init();
     if (fuse_dwt)
       for (int st = 0; st < fuse_issued; ++st)
         if (!(inject && st == 0)) fuse_issue(st);
-    if (al_stage) {  // this CTA's per_cta_p rows of the cached A_L: one contiguous range
-      const uint32_t bytes = static_cast<uint32_t>(p.per_cta_p) * D * sizeof(float);
-      mbar_arrive_expect_tx(&bars[0], bytes);
-      bulk_g2s(smem + L.s_ring,
-               p.al + (unit * p.P + static_cast<int64_t>(rank) * p.per_cta_p) * D, bytes, &bars[0]);
-    }
+    for (int st = 0; st < al_issued; ++st) al_issue(st);
     if (p.use_tma_spans) prefetch_tensormap(&p.tmap_spans);  // used by the filter phase
   }
   __syncwarp();
@@ -887,15 +910,30 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       }
       __syncthreads();
     } else if (sizeof(T) == 2 && al_stage) {
-      // Cached A_L: the rows landed in the ring (fp32, D floats apart); the
-      // warps form their logits with the queries straight from there.  A
-      // timed-out copy is waited for once more (bounded) before the ring is
-      // reused; the status word reports it.
-      if (!mbar_wait_bounded(&bars[0], 0u, p.status)) (void)mbar_wait_bounded(&bars[0], 0u, p.status);
-      cp_async_wait<0>();  // the queries
-      __syncthreads();
-      coarse_logits_ring<D>(reinterpret_cast<const float*>(smem + L.s_ring), Pc, qs, G, zc, TS, zscale);
-      __syncthreads();
+      // Cached A_L: stages of 64 rows (fp32, D floats apart) land in the
+      // ring; the warps form each stage's logits with the queries straight
+      // from there.  Every issued stage is waited for (bounded), even after a
+      // timeout, so no copy lands after the ring is reused; a timeout only
+      // stops further issues (the status word reports it).
+      const float* ring = reinterpret_cast<const float*>(smem + L.s_ring);
+      cp_async_wait<0>();  // the queries (visible after the loop's first barrier)
+      bool aborted = false;
+      for (int st = 0; st < al_issued; ++st) {
+        const bool ok = mbar_wait_bounded(&bars[st % al_nring],
+                                          static_cast<uint32_t>((st / al_nring) & 1), p.status);
+        if (__syncthreads_or(!ok)) aborted = true;
+        const int r0 = st * kScoreChunk;
+        coarse_logits_ring<D>(ring + static_cast<size_t>(st % al_nring) * kScoreChunk * D,
+                              min(kScoreChunk, Pc - r0), qs, G, zc + r0 * TS, TS, zscale);
+        __syncthreads();  // stage consumed
+        if (!aborted && st + al_nring < al_nst) {
+          if (tid == 0) {
+            fence_proxy_async();
+            al_issue(st + al_nring);
+          }
+          ++al_issued;
+        }
+      }
     }
     // Coarse logits of positions [c0, c0 + rows) into zc: read from global
     // memory, or formed here from a cached fp32 A_L (16 rows per warp task).
@@ -2004,8 +2042,9 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
     const int elem = ld.dtype == WF_BF16 ? 2 : 4;
     const bool fuse_try = want_fuse && p.per_cta_p <= kScoreChunk &&
                           (static_cast<int64_t>(elem) * ld.head_dim << ld.levels) <= kFuseStageBytes;
-    // Cached A_L staged by one bulk copy (bf16 queries; one score chunk per CTA).
-    const bool al_try = want_al && ld.dtype == WF_BF16 && p.per_cta_p <= kScoreChunk;
+    // Cached A_L staged by bulk copies (bf16 queries; the logits of every
+    // position of the CTA resident at once).
+    const bool al_try = want_al && ld.dtype == WF_BF16 && p.per_cta_p <= kZRows;
     // Prefer the fused step 1, the gather-all selection and token logits in
     // shared memory, in that order.
     // Fast filter: resident accumulators when every tile has its own columns
