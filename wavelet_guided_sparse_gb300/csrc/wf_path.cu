@@ -1182,8 +1182,12 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
 
       // ---- pass B: token scores s = Σ_q 2^(z - gm_q) / sum_q
       if (resident) {
-        if (warp >= 4 && *fabort == 0) {
-          for (int t = 0; t < ntiles; ++t) {
+        // Every multiply has completed (pass A waited for each): all eight
+        // warps read the accumulators, warps w and w + 4 sharing a lane
+        // quarter and taking alternate tiles.
+        tc_fence_after();
+        if (*fabort == 0) {
+          for (int t = warp >> 2; t < ntiles; t += 2) {
             const float sc = token_score_tmem(t_lane + t * N, N, G, sc2, gm, ginv);
             const int row = t * TR + row_l;
             if (row < R) keys[row] = __float_as_uint(sc);
