@@ -79,6 +79,7 @@ def _check_step(arrs, dtype, levels, ks, moments):
     (4, 1024, 4, 32, 128, 2, 128, "f32"),
     (3, 2048, 4, 64, 128, 2, 200, "bf16"),
     (1, 1024, 3, 7, 64, 2, 64, "bf16"),
+    (8, 64, 3, 5, 64, 2, 16, "bf16"),  # 106-tap composed filter over 64 tokens: windows wrap
 ])
 def test_step_basis_shapes(moments, n, levels, g, d, h, budget, dtype):
     arrs = _rand(n + g + moments, 1, h, n, g, d, dtype)

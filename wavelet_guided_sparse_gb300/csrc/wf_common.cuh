@@ -529,6 +529,7 @@ static __device__ __noinline__ void block_select_topk(const uint32_t* keys, int 
     const int nb = round == 2 ? 1024 : 2048;
     uint32_t* h = sm.hist[round];
     const int per = nb / 32;
+#pragma unroll 4
     for (int base = 0; base < n; base += kThreads) {  // whole warps iterate together
       const int i = base + tid;
       const uint32_t kv = i < n ? keys[i] : 0u;
@@ -562,6 +563,7 @@ static __device__ __noinline__ void block_select_topk(const uint32_t* keys, int 
   const int chunk = (((n + kWarps - 1) / kWarps) + 31) & ~31;
   const int lo = min(n, warp * chunk), hi = min(n, lo + chunk);
   int gt = 0, eq = 0;
+#pragma unroll 4
   for (int base = lo; base < hi; base += 32) {
     const int i = base + lane;
     const uint32_t kv = i < hi ? keys[i] : 0u;
@@ -593,6 +595,7 @@ static __device__ __noinline__ void block_select_topk(const uint32_t* keys, int 
   const int e_ex = ei - ew;
   int slot = __shfl_sync(0xffffffffu, gi - gw + min(need, e_ex), warp);
   int ties = __shfl_sync(0xffffffffu, e_ex, warp);
+#pragma unroll 4
   for (int base = lo; base < hi; base += 32) {
     const int i = base + lane;
     const uint32_t kv = i < hi ? keys[i] : 0u;

@@ -39,7 +39,8 @@ enum : int { kPhaseCachedAl = 16 };
 struct PathPlan {
   int mode;          // kPhase* bit set (without kPhaseFuseDwt)
   int fuse_dwt;      // 1: the path kernel computes A_L itself (no separate DWT launch)
-  int al_stage;      // 1: cached A_L rows staged by one bulk copy per CTA (PathArgs::al)
+  int al_stage;      // 1: cached A_L rows staged by bulk copies (PathArgs::al)
+  int al_ring;       // their ring depth (64-row stages)
   int cluster;       // CTAs per unit
   int per_cta_p;     // score: coarse positions per CTA
   int rows_cap;      // filter: token rows per CTA (capacity)

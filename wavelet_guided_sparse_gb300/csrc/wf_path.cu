@@ -95,7 +95,9 @@ struct PathParams {
   int f_nb;                // fast filter: tensor-memory accumulator slots
   int fuse_dwt;            // score: A_L from K_p inside this kernel
   int al_stage;            // score: this CTA's rows of the cached fp32 A_L arrive by bulk
-                           // copies, 64 rows a stage (per_cta_p <= kZRows)
+                           // copies, 64 rows a stage (per_cta_p <= kZRows), through a
+                           // ring of al_ring stages (every stage resident when it fits)
+  int al_ring;
   uint32_t inject_polls;   // fault injection (tests): see the fused step 1 below
   float al_scale;          // 2^(-L/2), the orthonormal Haar low-pass gain
   int k[WF_MAX_LEVELS + 1];
@@ -167,7 +169,7 @@ struct PathSmem {
         s_ring = take_bytes(stage_b > z_b ? stage_b : z_b);
         s_z = s_ring;
       } else {
-        s_ring = take_bytes(static_cast<size_t>(kFuseStages) * stage_b);
+        s_ring = take_bytes(static_cast<size_t>(p.al_ring) * stage_b);
         s_z = take_bytes(z_b);
       }
       s_stage = s_as = s_ring;
@@ -742,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   int fuse_issued = min(kFuseStages, fuse_nst);
   // Cached A_L: stages of kScoreChunk fp32 rows of this CTA's contiguous range.
   const int al_nst = al_stage ? (p.per_cta_p + kScoreChunk - 1) / kScoreChunk : 0;
-  const int al_nring = al_nst > 1 ? kFuseStages : 1;
+  const int al_nring = al_nst > 1 ? p.al_ring : 1;
   auto al_issue = [&](int st) {  // thread 0 only
     const int rows = min(kScoreChunk, p.per_cta_p - st * kScoreChunk);
     const uint32_t bytes = static_cast<uint32_t>(rows) * D * static_cast<uint32_t>(sizeof(float));
@@ -2085,6 +2087,9 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
       p.fuse_dwt = fuse_try ? fz : 0;
       p.al_stage = al_try ? fz : 0;
       p.t_ws = nullptr;
+      // Every A_L stage resident (no refill latency) if that fits, else a ring of three.
+      p.al_ring = (p.per_cta_p + kScoreChunk - 1) / kScoreChunk;
+      if (p.al_stage && p.al_ring > kFuseStages && smem_bytes(ld, p) > kMaxSmem) p.al_ring = kFuseStages;
       smem = smem_bytes(ld, p);
       t_in_smem = true;
       if (ff) {
@@ -2117,6 +2122,7 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
   plan->a_stages = p.a_stages;
   plan->fuse_dwt = p.fuse_dwt;
   plan->al_stage = p.al_stage;
+  plan->al_ring = p.al_ring;
   plan->filter_fast = p.filter_fast;
   plan->f_nb = p.f_nb;
   plan->mode = mode;
@@ -2163,6 +2169,7 @@ cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathAr
   p.a_stages = plan.a_stages;
   p.fuse_dwt = plan.fuse_dwt;
   p.al_stage = plan.al_stage;
+  p.al_ring = plan.al_ring;
   if (plan.al_stage && a.al == nullptr) return cudaErrorInvalidValue;
   p.inject_polls = plan.fuse_dwt ? consume_wait_injection() : 0u;
   p.filter_fast = plan.filter_fast;
