@@ -150,6 +150,10 @@ typedef struct {
   int32_t smem_bytes;    /* dynamic shared memory per CTA of the path kernel         */
   int32_t filter_stages; /* key tiles in flight in the filter                        */
   int32_t attend_stages; /* key/value tiles in flight in the attention               */
+  int32_t stream_is_dwt_lowpass; /* two launches: 1 when the first is exactly
+                            wf_dwt_lowpass (A_L only) and the second exactly the launch
+                            of wf_step_cached_al on that A_L; 0 when the first also
+                            forms the coarse logits the second reads (or one launch) */
 } wf_plan;
 
 /* Fills *plan with the launch plan wf_step uses for these sizes on the

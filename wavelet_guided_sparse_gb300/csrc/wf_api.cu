@@ -90,6 +90,26 @@ Layout layout(const LaunchDims& ld, const int32_t* k, const wf::PathPlan* fp) {
 
 int32_t* status_word(void* ws) { return static_cast<int32_t*>(ws); }
 
+// The plan of wf_step: one launch where the path kernel fuses step 1;
+// otherwise two.  The second launch then forms the coarse logits itself from
+// the A_L the stream wrote (*from_al: every CTA's A_L rows staged in shared
+// memory, the cached-A_L path), or, where that staging does not fit, reads
+// the logits the stream formed in its epilogue.
+bool step_plan(const LaunchDims& ld, const int32_t* k, wf::PathPlan* plan, bool* from_al) {
+  *from_al = false;
+  const int sms = wf::device_sm_count();
+  if (!wf::plan_path(ld, wf::kPhaseAll | wf::kPhaseFuseDwt, k, k[ld.levels], k[0], sms, plan))
+    return false;
+  if (plan->fuse_dwt) return true;
+  wf::PathPlan c;
+  if (wf::plan_path(ld, wf::kPhaseAll | wf::kPhaseCachedAl, k, k[ld.levels], k[0], sms, &c) &&
+      c.al_stage) {
+    *plan = c;
+    *from_al = true;
+  }
+  return true;
+}
+
 // The longer-basis step takes the Haar path kernel with precomputed coarse
 // logits when every level between L and 0 keeps all children (then only the
 // level-L logits depend on the basis), the inputs are bf16, and the composed
@@ -207,13 +227,16 @@ int wf_workspace_bytes(const wf_dims* dims, const int32_t* k_per_level, size_t* 
   st = check_k(ld, k_per_level);
   if (st != WF_OK) return st;
   const int sms = wf::device_sm_count();
-  wf::PathPlan all, filt;
+  wf::PathPlan all, step, filt;
+  bool from_al = false;
   if (!wf::plan_path(ld, wf::kPhaseAll | wf::kPhaseFuseDwt, k_per_level, k_per_level[ld.levels],
                      k_per_level[0], sms, &all) ||
+      !step_plan(ld, k_per_level, &step, &from_al) ||
       !wf::plan_path(ld, wf::kPhaseFilter, k_per_level, k_per_level[ld.levels], k_per_level[0],
                      sms, &filt))
     return WF_ERR_UNSUPPORTED;
-  const wf::PathPlan& big = all.t_bytes >= filt.t_bytes ? all : filt;
+  const size_t t = std::max(all.t_bytes, std::max(step.t_bytes, filt.t_bytes));
+  const wf::PathPlan& big = all.t_bytes == t ? all : (step.t_bytes == t ? step : filt);
   *bytes = layout(ld, k_per_level, &big).total;
   return WF_OK;
 }
@@ -241,9 +264,8 @@ int wf_step_plan(const wf_dims* dims, const int32_t* k_per_level, wf_plan* out) 
   st = check_k(ld, k_per_level);
   if (st != WF_OK) return st;
   wf::PathPlan plan;
-  if (!wf::plan_path(ld, wf::kPhaseAll | wf::kPhaseFuseDwt, k_per_level, k_per_level[ld.levels],
-                     k_per_level[0], wf::device_sm_count(), &plan))
-    return WF_ERR_UNSUPPORTED;
+  bool from_al = false;
+  if (!step_plan(ld, k_per_level, &plan, &from_al)) return WF_ERR_UNSUPPORTED;
   out->launches = plan.fuse_dwt ? 1 : 2;
   out->cluster = plan.cluster;
   out->final_gather = plan.gather_all;
@@ -254,6 +276,7 @@ int wf_step_plan(const wf_dims* dims, const int32_t* k_per_level, wf_plan* out) 
   out->smem_bytes = static_cast<int32_t>(plan.smem_bytes);
   out->filter_stages = plan.f_stages;
   out->attend_stages = plan.a_stages;
+  out->stream_is_dwt_lowpass = from_al ? 1 : 0;
   return WF_OK;
 }
 
@@ -461,20 +484,21 @@ int wf_step(const wf_dims* dims, const void* Q, const void* Kp, const void* Vp, 
   if (st != WF_OK) return st;
   const int budget = k_per_level[0];
   wf::PathPlan plan;
-  if (!wf::plan_path(ld, wf::kPhaseAll | wf::kPhaseFuseDwt, k_per_level, k_per_level[ld.levels],
-                     budget, wf::device_sm_count(), &plan))
-    return WF_ERR_UNSUPPORTED;
+  bool from_al = false;
+  if (!step_plan(ld, k_per_level, &plan, &from_al)) return WF_ERR_UNSUPPORTED;
   const Layout L = layout(ld, k_per_level, &plan);
   if (workspace_bytes < L.total) return WF_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   float* zl = reinterpret_cast<float*>(ws + L.zl);
+  float* al = reinterpret_cast<float*>(ws + L.al);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // Step 1 runs inside the path kernel when the plan fuses it; otherwise a
-  // separate streaming launch writes A_L and then each coarse position's
-  // logits against the queries.
+  // separate streaming launch writes A_L (and, when the path kernel does not
+  // form them itself, each coarse position's logits against the queries).
   if (!plan.fuse_dwt) {
-    const cudaError_t e = wf::launch_dwt_lowpass(ld, Kp, reinterpret_cast<float*>(ws + L.al), Q,
-                                                 zl, ld.levels, status_word(workspace), s);
+    const cudaError_t e = wf::launch_dwt_lowpass(ld, Kp, al, from_al ? nullptr : Q,
+                                                 from_al ? nullptr : zl, ld.levels,
+                                                 status_word(workspace), s);
     if (e != cudaSuccess) return cuda_status(e);
   }
   wf::PathArgs a = {};
@@ -483,7 +507,8 @@ int wf_step(const wf_dims* dims, const void* Q, const void* Kp, const void* Vp, 
   a.vp = Vp;
   a.kg = Kg;
   a.vg = Vg;
-  a.zl = plan.fuse_dwt ? nullptr : zl;
+  a.zl = plan.fuse_dwt || from_al ? nullptr : zl;
+  a.al = from_al ? al : nullptr;
   a.idx_out = idx_out;
   a.o = O;
   a.lse = lse;
