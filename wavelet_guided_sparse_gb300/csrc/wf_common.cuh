@@ -559,7 +559,56 @@ static __device__ __noinline__ void block_select_topk(const uint32_t* keys, int 
     }
   }
   const uint32_t thr = prefix;
-  // Fused compaction: warp w owns keys [lo, hi).
+  const int S = (n + 31) >> 5;  // 32-key sub-chunks
+  if (S <= kThreads) {
+    // Counts of keys above the threshold and of ties per sub-chunk (warp w
+    // takes sub-chunks w, w + kWarps, ...), in the spent first histogram;
+    // exclusive scans over the sub-chunks give each one its first slot, so
+    // only the sub-chunks holding slots of [lo_slot, hi_slot) are emitted,
+    // spread over the warps.
+    __syncthreads();  // every warp is done reading the histograms
+    int32_t* sgt = reinterpret_cast<int32_t*>(sm.hist[0]);
+    int32_t* seq = sgt + kThreads;
+    int32_t* sslot = seq + kThreads;      // S + 1 entries
+    int32_t* stie = sslot + kThreads + 1;
+    for (int sc = warp; sc < S; sc += kWarps) {
+      const int i = sc * 32 + lane;
+      const uint32_t kv = i < n ? keys[i] : 0u;
+      const int g = __popc(__ballot_sync(0xffffffffu, i < n && kv > thr));
+      const int e = __popc(__ballot_sync(0xffffffffu, i < n && kv == thr));
+      if (lane == 0) {
+        sgt[sc] = g;
+        seq[sc] = e;
+      }
+    }
+    __syncthreads();
+    const int g = tid < S ? sgt[tid] : 0, e = tid < S ? seq[tid] : 0;
+    int tot_g, tot_e;
+    const int gb = block_excl_scan(g, sm.scan, &tot_g);
+    const int eb = block_excl_scan(e, sm.scan, &tot_e);
+    if (tid < S) {
+      sslot[tid] = gb + min(need, eb);  // selected keys before the sub-chunk
+      stie[tid] = eb;                   // ties before it
+    }
+    if (tid == 0) sslot[S] = tot_g + min(need, tot_e);
+    __syncthreads();
+    for (int sc = warp; sc < S; sc += kWarps) {
+      const int s0 = sslot[sc], s1 = sslot[sc + 1];
+      if (s1 <= lo_slot || s0 >= hi_slot) continue;  // no slot of the range here
+      const int i = sc * 32 + lane;
+      const uint32_t kv = i < n ? keys[i] : 0u;
+      const unsigned below = (1u << lane) - 1u;
+      const unsigned eqm = __ballot_sync(0xffffffffu, i < n && kv == thr);
+      const bool tie_taken = (eqm >> lane & 1u) && stie[sc] + __popc(eqm & below) < need;
+      const bool taken = (i < n && kv > thr) || tie_taken;
+      const unsigned tm = __ballot_sync(0xffffffffu, taken);
+      const int my_slot = s0 + __popc(tm & below);
+      if (taken && my_slot >= lo_slot && my_slot < hi_slot) out[my_slot - lo_slot] = map ? map[i] : i;
+    }
+    __syncthreads();
+    return;
+  }
+  // Larger sets: fused compaction, warp w owns keys [lo, hi).
   const int chunk = (((n + kWarps - 1) / kWarps) + 31) & ~31;
   const int lo = min(n, warp * chunk), hi = min(n, lo + chunk);
   int gt = 0, eq = 0;
