@@ -70,6 +70,9 @@ struct PathParams {
   // K_p as a 2-D tensor [units * N_p rows, d columns] for tensor copies of whole
   // spans (box: 64 columns x 2^L rows, 128-byte swizzle); valid if use_tma_spans.
   alignas(64) CUtensorMap tmap_spans;
+  // A cached fp32 A_L as a 2-D tensor [units * P rows, d columns] (box: 32
+  // columns x 64 rows, 128-byte swizzle); valid if al_stage.
+  alignas(64) CUtensorMap tmap_al;
   int use_tma_spans;
   const void* q;
   const void* kp;
@@ -166,10 +169,10 @@ struct PathSmem {
       const size_t stage_b = sizeof(float) * kScoreChunk * D;
       const size_t z_b = sizeof(float) * static_cast<size_t>(p.per_cta_p) * (p.G | 1);
       if (p.per_cta_p <= kScoreChunk) {
-        s_ring = take_bytes(stage_b > z_b ? stage_b : z_b);
+        s_ring = take_bytes(stage_b > z_b ? stage_b : z_b, 1024);
         s_z = s_ring;
       } else {
-        s_ring = take_bytes(static_cast<size_t>(p.al_ring) * stage_b);
+        s_ring = take_bytes(static_cast<size_t>(p.al_ring) * stage_b, 1024);
         s_z = take_bytes(z_b);
       }
       s_stage = s_as = s_ring;
@@ -582,8 +585,8 @@ __device__ __forceinline__ void tmem_row_to_smem(uint32_t taddr, int N, int cols
   }
 }
 
-// Coarse logits of `rows` (<= 64) rows of an fp32 A_L in shared memory (D
-// floats apart) against the unit's queries in the tensor-core operand layout
+// Coarse logits of `rows` (<= 64) rows of an fp32 A_L in shared memory (the
+// 128-byte-swizzled layout of 64-row, 32-column blocks a tensor copy writes) against the unit's queries in the tensor-core operand layout
 // (qs, bf16, rows >= G zero), into z (row pitch `pitch`, scaled by zscale), on
 // the warps' mma.sync units: each A_L value is split exactly into three bf16
 // parts in registers, whose products with the bf16 queries are exact (fp32
@@ -605,17 +608,21 @@ __device__ __forceinline__ void coarse_logits_ring(const float* a, int rows, con
     for (int e = 0; e < 4; ++e) c[t][e] = 0.f;
   if (rb < rows) {
     const bool r0ok = rb + gid < rows, r1ok = rb + gid + 8 < rows;
-    const float* a0 = a + (rb + gid) * D;
-    const float* a1 = a0 + 8 * D;
+    const unsigned char* ab = reinterpret_cast<const unsigned char*>(a);
+    // Element (r, k): 16-byte chunk k / 4 of row r in the 128-byte-swizzled
+    // layout of 64-row, 32-column blocks.
+    auto at = [&](int r, int k) {
+      return *reinterpret_cast<const float2*>(ab + sw_offset(r, k >> 2, kScoreChunk) + (k & 3) * 4);
+    };
     const uint32_t q0 = smem_u32(qs);
 #pragma unroll 2
     for (int ks = 0; ks < D / 16; ++ks) {
       const int k0 = ks * 16 + 2 * tig;
       float2 v[4];  // (row gid, k0), (row gid + 8, k0), (row gid, k0 + 8), (row gid + 8, k0 + 8)
-      v[0] = r0ok ? *reinterpret_cast<const float2*>(a0 + k0) : make_float2(0.f, 0.f);
-      v[1] = r1ok ? *reinterpret_cast<const float2*>(a1 + k0) : make_float2(0.f, 0.f);
-      v[2] = r0ok ? *reinterpret_cast<const float2*>(a0 + k0 + 8) : make_float2(0.f, 0.f);
-      v[3] = r1ok ? *reinterpret_cast<const float2*>(a1 + k0 + 8) : make_float2(0.f, 0.f);
+      v[0] = r0ok ? at(rb + gid, k0) : make_float2(0.f, 0.f);
+      v[1] = r1ok ? at(rb + gid + 8, k0) : make_float2(0.f, 0.f);
+      v[2] = r0ok ? at(rb + gid, k0 + 8) : make_float2(0.f, 0.f);
+      v[3] = r1ok ? at(rb + gid + 8, k0 + 8) : make_float2(0.f, 0.f);
       uint32_t af[3][4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -745,14 +752,16 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
   // Cached A_L: stages of kScoreChunk fp32 rows of this CTA's contiguous range.
   const int al_nst = al_stage ? (p.per_cta_p + kScoreChunk - 1) / kScoreChunk : 0;
   const int al_nring = al_nst > 1 ? p.al_ring : 1;
+  // A stage is D / 32 tensor copies of 64 rows x 32 columns (128-byte
+  // swizzle; rows past the tensor's end arrive as zeros, rows of the next
+  // CTA's slice are ignored), so the fragment loads below hit distinct banks.
   auto al_issue = [&](int st) {  // thread 0 only
-    const int rows = min(kScoreChunk, p.per_cta_p - st * kScoreChunk);
-    const uint32_t bytes = static_cast<uint32_t>(rows) * D * static_cast<uint32_t>(sizeof(float));
     uint64_t* bar = &bars[st % al_nring];
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_g2s(smem + L.s_ring + static_cast<size_t>(st % al_nring) * kScoreChunk * D * sizeof(float),
-             p.al + (unit * p.P + static_cast<int64_t>(rank) * p.per_cta_p + st * kScoreChunk) * D,
-             bytes, bar);
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(kScoreChunk * D * sizeof(float)));
+    unsigned char* dst = smem + L.s_ring + static_cast<size_t>(st % al_nring) * kScoreChunk * D * sizeof(float);
+    const int y = static_cast<int>(unit * p.P) + rank * p.per_cta_p + st * kScoreChunk;
+    for (int kb = 0; kb < D / 32; ++kb)
+      tma_load_2d(dst + kb * (kScoreChunk * 128), &p.tmap_al, kb * 32, y, bar);
   };
   int al_issued = min(al_nring, al_nst);
   // Fault injection (tests of the bounded waits): in the first CTA, stage 0
@@ -769,6 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     if (fuse_dwt)
       for (int st = 0; st < fuse_issued; ++st)
         if (!(inject && st == 0)) fuse_issue(st);
+    if (al_stage) prefetch_tensormap(&p.tmap_al);
     for (int st = 0; st < al_issued; ++st) al_issue(st);
     if (p.use_tma_spans) prefetch_tensormap(&p.tmap_spans);  // used by the filter phase
   }
@@ -1946,6 +1956,21 @@ bool encode_span_map(const LaunchDims& ld, const void* kp, CUtensorMap* map, int
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A cached fp32 A_L [U, P, d] as a 2-D tensor for tensor copies of 64-row,
+// 32-column boxes with 128-byte swizzle.
+bool encode_al_map(const LaunchDims& ld, const float* al, CUtensorMap* map) {
+  const EncodeTiledFn enc = encode_tiled();
+  if (enc == nullptr || al == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(ld.head_dim),
+                              static_cast<cuuint64_t>(ld.units) * (ld.n_prompt >> ld.levels)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld.head_dim) * 4};
+  const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(kScoreChunk)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(al), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t smem_bytes(const LaunchDims& ld, const PathParams& p) {
   if (ld.dtype == WF_BF16)
     return ld.head_dim == 128 ? PathSmem<__nv_bfloat16, 128>(p).total
@@ -2170,7 +2195,7 @@ cudaError_t launch_path(const LaunchDims& ld, const PathPlan& plan, const PathAr
   p.fuse_dwt = plan.fuse_dwt;
   p.al_stage = plan.al_stage;
   p.al_ring = plan.al_ring;
-  if (plan.al_stage && a.al == nullptr) return cudaErrorInvalidValue;
+  if (plan.al_stage && !encode_al_map(ld, a.al, &p.tmap_al)) return cudaErrorInvalidValue;
   p.inject_polls = plan.fuse_dwt ? consume_wait_injection() : 0u;
   p.filter_fast = plan.filter_fast;
   p.f_nb = plan.f_nb;
