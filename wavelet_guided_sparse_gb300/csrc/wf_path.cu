@@ -585,22 +585,23 @@ __device__ __forceinline__ void tmem_row_to_smem(uint32_t taddr, int N, int cols
   }
 }
 
-// Coarse logits of `rows` (<= 64) rows of an fp32 A_L in shared memory (the
-// 128-byte-swizzled layout of 64-row, 32-column blocks a tensor copy writes) against the unit's queries in the tensor-core operand layout
-// (qs, bf16, rows >= G zero), into z (row pitch `pitch`, scaled by zscale), on
-// the warps' mma.sync units: each A_L value is split exactly into three bf16
-// parts in registers, whose products with the bf16 queries are exact (fp32
-// accumulation).  Warp w takes rows 16 (w % 4) .. + 15 and the query tiles
-// w / 4, w / 4 + 2, ... (8 queries each).  z may overlay the A_L rows: every
-// warp has read its rows (block barrier) before any result is stored.
-// Block-wide (every thread calls it).
+// Coarse logits of `rows` (<= 128) rows of an fp32 A_L in shared memory
+// (64-row stages one after another, each in the 128-byte-swizzled layout of
+// 32-column blocks a tensor copy writes) against the unit's queries in the
+// tensor-core operand layout (qs, bf16, rows >= G zero), into z (row pitch
+// `pitch`, scaled by zscale), on the warps' mma.sync units: each A_L value is
+// split exactly into three bf16 parts in registers, whose products with the
+// bf16 queries are exact (fp32 accumulation).  Warp w takes rows 16w .. 16w
+// + 15 against every query tile, so each value is split once.  z may overlay
+// the A_L rows: every warp has read its rows (block barrier) before any
+// result is stored.  Block-wide (every thread calls it).
 template <int D>
 __device__ __forceinline__ void coarse_logits_ring(const float* a, int rows, const unsigned char* qs,
                                                    int G, float* z, int pitch, float zscale) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, gid = lane >> 2, tig = lane & 3;
-  const int rb = 16 * (warp & 3);
+  const int rb = 16 * warp;
   const int NT = (G + 7) >> 3;
-  constexpr int kMaxTiles = 4;  // G <= 64: at most 8 query tiles over two warps
+  constexpr int kMaxTiles = 8;  // G <= 64
   float c[kMaxTiles][4];
 #pragma unroll
   for (int t = 0; t < kMaxTiles; ++t)
@@ -608,9 +609,10 @@ __device__ __forceinline__ void coarse_logits_ring(const float* a, int rows, con
     for (int e = 0; e < 4; ++e) c[t][e] = 0.f;
   if (rb < rows) {
     const bool r0ok = rb + gid < rows, r1ok = rb + gid + 8 < rows;
-    const unsigned char* ab = reinterpret_cast<const unsigned char*>(a);
-    // Element (r, k): 16-byte chunk k / 4 of row r in the 128-byte-swizzled
-    // layout of 64-row, 32-column blocks.
+    // Element (r, k): stage r / 64, then 16-byte chunk k / 4 of row r % 64.
+    const unsigned char* ab = reinterpret_cast<const unsigned char*>(a) +
+                              static_cast<size_t>(rb >> 6) * kScoreChunk * D * sizeof(float);
+    const int r0 = (rb & 63) + gid, r1 = r0 + 8;
     auto at = [&](int r, int k) {
       return *reinterpret_cast<const float2*>(ab + sw_offset(r, k >> 2, kScoreChunk) + (k & 3) * 4);
     };
@@ -619,10 +621,10 @@ __device__ __forceinline__ void coarse_logits_ring(const float* a, int rows, con
     for (int ks = 0; ks < D / 16; ++ks) {
       const int k0 = ks * 16 + 2 * tig;
       float2 v[4];  // (row gid, k0), (row gid + 8, k0), (row gid, k0 + 8), (row gid + 8, k0 + 8)
-      v[0] = r0ok ? at(rb + gid, k0) : make_float2(0.f, 0.f);
-      v[1] = r1ok ? at(rb + gid + 8, k0) : make_float2(0.f, 0.f);
-      v[2] = r0ok ? at(rb + gid, k0 + 8) : make_float2(0.f, 0.f);
-      v[3] = r1ok ? at(rb + gid + 8, k0 + 8) : make_float2(0.f, 0.f);
+      v[0] = r0ok ? at(r0, k0) : make_float2(0.f, 0.f);
+      v[1] = r1ok ? at(r1, k0) : make_float2(0.f, 0.f);
+      v[2] = r0ok ? at(r0, k0 + 8) : make_float2(0.f, 0.f);
+      v[3] = r1ok ? at(r1, k0 + 8) : make_float2(0.f, 0.f);
       uint32_t af[3][4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -635,10 +637,9 @@ __device__ __forceinline__ void coarse_logits_ring(const float* a, int rows, con
       }
 #pragma unroll
       for (int t = 0; t < kMaxTiles; ++t) {
-        const int nt = (warp >> 2) + 2 * t;
-        if (nt >= NT) break;
-        // Queries nt * 8 + gid, k0 and k0 + 8: two bf16 each, from the core-matrix layout.
-        const uint32_t qa = q0 + cm_offset(nt * 8 + gid, k0 >> 3, D * 16) + (k0 & 7) * 2;
+        if (t >= NT) break;
+        // Queries t * 8 + gid, k0 and k0 + 8: two bf16 each, from the core-matrix layout.
+        const uint32_t qa = q0 + cm_offset(t * 8 + gid, k0 >> 3, D * 16) + (k0 & 7) * 2;
         uint32_t b[2];
         asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b[0]) : "r"(qa));
         asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b[1]) : "r"(qa + 128));
@@ -651,9 +652,8 @@ __device__ __forceinline__ void coarse_logits_ring(const float* a, int rows, con
   if (rb >= rows) return;
 #pragma unroll
   for (int t = 0; t < kMaxTiles; ++t) {
-    const int nt = (warp >> 2) + 2 * t;
-    if (nt >= NT) break;
-    const int col = nt * 8 + 2 * tig;
+    if (t >= NT) break;
+    const int col = t * 8 + 2 * tig;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int r = rb + gid + 8 * h;
@@ -930,15 +930,21 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       const float* ring = reinterpret_cast<const float*>(smem + L.s_ring);
       cp_async_wait<0>();  // the queries (visible after the loop's first barrier)
       bool aborted = false;
-      for (int st = 0; st < al_issued; ++st) {
-        const bool ok = mbar_wait_bounded(&bars[st % al_nring],
-                                          static_cast<uint32_t>((st / al_nring) & 1), p.status);
+      // With every stage resident two stages (128 rows, one 16-row tile per
+      // warp) go through the tensor cores at a time; with a refilled ring one.
+      const int step = al_nring == al_nst ? 2 : 1;
+      for (int st = 0; st < al_issued; st += step) {
+        const int n_st = min(step, al_issued - st);
+        bool ok = true;
+        for (int j = 0; j < n_st; ++j)
+          ok = mbar_wait_bounded(&bars[(st + j) % al_nring],
+                                 static_cast<uint32_t>(((st + j) / al_nring) & 1), p.status) && ok;
         if (__syncthreads_or(!ok)) aborted = true;
         const int r0 = st * kScoreChunk;
         coarse_logits_ring<D>(ring + static_cast<size_t>(st % al_nring) * kScoreChunk * D,
-                              min(kScoreChunk, Pc - r0), qs, G, zc + r0 * TS, TS, zscale);
+                              min(n_st * kScoreChunk, Pc - r0), qs, G, zc + r0 * TS, TS, zscale);
         __syncthreads();  // stage consumed
-        if (!aborted && st + al_nring < al_nst) {
+        if (step == 1 && !aborted && st + al_nring < al_nst) {
           if (tid == 0) {
             fence_proxy_async();
             al_issue(st + al_nring);
