@@ -39,21 +39,19 @@ METRIC = "cached prompt tokens filtered+attended/sec per layer-step; HBM GB/s vs
 DEFAULT_CONFIG = "full_step"
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes (read + write) of one dwt_lowpass launch on the default workload,
-# from an ncu capture of the kernel source with this SHA-256 prefix; null
-# once the kernel has changed since the counters were taken.
-# dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture
-# of the 4096-token layer (profiles/), valid while the kernel sources (without
-# comments and blank space) hash to source_sha.
-DWT_TRAFFIC = {"sources": ("wf_dwt.cu",), "source_sha": "65d64d392b075f89",
-               "bytes_per_launch": 33577984}  # 33.58 MB read + 0 B written (A_L stays in L2)
-PATH_TRAFFIC = {"sources": ("wf_path.cu", "wf_common.cuh", "wf_mma.cuh", "wf_umma.cuh"),
-                "source_sha": "4e8b7fafc8ea55e4",
-                "bytes_per_launch": 38690048}  # 38.69 MB read + 3.3 KB written
-# One cold launch: the reads are the K/V bytes exactly; most of the 71.6 MB
-# of cache writes are still in L2 when the kernel ends (written back later).
-CACHE_TRAFFIC = {"sources": ("wf_cache.cu", "wf_common.cuh"), "source_sha": "d9a8f99a6f16b2e0",
-                 "bytes_per_launch": 81929216}  # 67.65 MB read + 14.28 MB written
+# DRAM bytes (read + write) per launch of each kernel on a workload:
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch from a one-pass
+# ncu capture of `bench.py` on that workload (profiles/), valid while the
+# kernel's sources (without comments and blank space) hash to source_sha.
+TRAFFIC = {
+    "dwt": {"sources": ("wf_dwt.cu", "wf_common.cuh", "wf_mma.cuh", "wf_internal.h"),
+            "source_sha": "", "bytes": {}},
+    "path": {"sources": ("wf_path.cu", "wf_common.cuh", "wf_mma.cuh", "wf_umma.cuh",
+                         "wf_internal.h"),
+             "source_sha": "", "bytes": {}},
+    "cache": {"sources": ("wf_cache.cu", "wf_common.cuh", "wf_internal.h"),
+              "source_sha": "", "bytes": {}},
+}
 
 
 def _rank_env():
@@ -192,13 +190,15 @@ def _source_sha(names) -> str:
     return h.hexdigest()[:16]
 
 
-def _traffic(table):
-    """ncu DRAM bytes per launch, if the kernel sources are the profiled ones."""
+def _traffic(kind, cfg):
+    """ncu DRAM bytes per launch of a kernel on this workload, if captured for
+    the current kernel sources; else None."""
+    table = TRAFFIC[kind]
     try:
         sha = _source_sha(table["sources"])
     except OSError:
         return None
-    return table["bytes_per_launch"] if table["source_sha"] == sha else None
+    return table["bytes"].get(cfg.name) if table["source_sha"] == sha else None
 
 
 class ClockSampler:
@@ -696,7 +696,7 @@ def run_ours(args, cfg):
     dwt_roofline = {"kernel": "dwt_stream_kernel (wf_dwt_lowpass: K_p stream, fp32 A_L)",
                     "bound": "hbm", "achieved": sbytes / (dwt_us * 1e-6) / 1e9, "peak": peak,
                     "unit": "GB/s", "frac": sbytes / (dwt_us * 1e-6) / 1e9 / peak,
-                    "peak_source": peak_source, "traffic": _traffic(DWT_TRAFFIC),
+                    "peak_source": peak_source, "traffic": _traffic("dwt", cfg),
                     "algorithmic_bytes_per_launch": sbytes, "launch_us": dwt_us,
                     "timing": f"{n_dwt} back-to-back launches over the input sets"}
     if launches == 1:
@@ -706,7 +706,7 @@ def run_ours(args, cfg):
                               "filter, gather, attention)", "bound": "hbm",
                     "achieved": lbytes / (layer_us * 1e-6) / 1e9, "peak": peak, "unit": "GB/s",
                     "frac": lbytes / (layer_us * 1e-6) / 1e9 / peak, "peak_source": peak_source,
-                    "traffic": _traffic(PATH_TRAFFIC), "algorithmic_bytes_per_launch": lbytes,
+                    "traffic": _traffic("path", cfg), "algorithmic_bytes_per_launch": lbytes,
                     "launch_us": layer_us,
                     "timing": "CUDA events over the timed region / layer-steps (one launch each)"}
     else:
@@ -729,7 +729,7 @@ def run_ours(args, cfg):
         roofline = {"kernel": "path_kernel (steps 2-5 of the layer-step)", "bound": "hbm",
                     "achieved": pk_bytes / (pk_us * 1e-6) / 1e9, "peak": peak, "unit": "GB/s",
                     "frac": pk_bytes / (pk_us * 1e-6) / 1e9 / peak, "peak_source": peak_source,
-                    "traffic": _traffic(PATH_TRAFFIC), "algorithmic_bytes_per_launch": pk_bytes,
+                    "traffic": _traffic("path", cfg), "algorithmic_bytes_per_launch": pk_bytes,
                     "launch_us": pk_us, "timing": timing} if big else dwt_roofline
     cpu_rate, cpu_units, cpu_s = (None, 0, 0.0)
     workers = os.cpu_count() or 1
@@ -772,7 +772,7 @@ def run_ours(args, cfg):
             "bound": "hbm", "achieved": cache_init_bytes(cfg) / (cache_us * 1e-6) / 1e9,
             "peak": peak, "unit": "GB/s",
             "frac": cache_init_bytes(cfg) / (cache_us * 1e-6) / 1e9 / peak,
-            "peak_source": peak_source, "traffic": _traffic(CACHE_TRAFFIC),
+            "peak_source": peak_source, "traffic": _traffic("cache", cfg),
             "algorithmic_bytes_per_launch": cache_init_bytes(cfg), "launch_us": cache_us,
             "timing": "CUDA graph of 20 launches over two alternating input/output sets, "
                       "events around its replays"},

@@ -592,14 +592,18 @@ __device__ __forceinline__ void tmem_row_to_smem(uint32_t taddr, int N, int cols
 // `pitch`, scaled by zscale), on the warps' mma.sync units: each A_L value is
 // split exactly into three bf16 parts in registers, whose products with the
 // bf16 queries are exact (fp32 accumulation).  Warp w takes rows 16w .. 16w
-// + 15 against every query tile, so each value is split once.  z may overlay
+// + 15 against every query tile, so each value is split once; for at most 64
+// rows warps w and w + 4 share a row tile and take alternate query tiles
+// instead (all eight warps busy).  z may overlay
 // the A_L rows: every warp has read its rows (block barrier) before any
 // result is stored.  Block-wide (every thread calls it).
 template <int D>
 __device__ __forceinline__ void coarse_logits_ring(const float* a, int rows, const unsigned char* qs,
                                                    int G, float* z, int pitch, float zscale) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, gid = lane >> 2, tig = lane & 3;
-  const int rb = 16 * warp;
+  const bool shared_rows = rows <= 64;
+  const int rb = 16 * (shared_rows ? (warp & 3) : warp);
+  const int t0 = shared_rows ? (warp >> 2) : 0, tstep = shared_rows ? 2 : 1;  // query tiles
   const int NT = (G + 7) >> 3;
   constexpr int kMaxTiles = 8;  // G <= 64
   float c[kMaxTiles][4];
@@ -637,9 +641,10 @@ __device__ __forceinline__ void coarse_logits_ring(const float* a, int rows, con
       }
 #pragma unroll
       for (int t = 0; t < kMaxTiles; ++t) {
-        if (t >= NT) break;
-        // Queries t * 8 + gid, k0 and k0 + 8: two bf16 each, from the core-matrix layout.
-        const uint32_t qa = q0 + cm_offset(t * 8 + gid, k0 >> 3, D * 16) + (k0 & 7) * 2;
+        const int nt = t0 + tstep * t;
+        if (nt >= NT) break;
+        // Queries nt * 8 + gid, k0 and k0 + 8: two bf16 each, from the core-matrix layout.
+        const uint32_t qa = q0 + cm_offset(nt * 8 + gid, k0 >> 3, D * 16) + (k0 & 7) * 2;
         uint32_t b[2];
         asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b[0]) : "r"(qa));
         asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b[1]) : "r"(qa + 128));
@@ -652,8 +657,9 @@ __device__ __forceinline__ void coarse_logits_ring(const float* a, int rows, con
   if (rb >= rows) return;
 #pragma unroll
   for (int t = 0; t < kMaxTiles; ++t) {
-    if (t >= NT) break;
-    const int col = t * 8 + 2 * tig;
+    const int nt = t0 + tstep * t;
+    if (nt >= NT) break;
+    const int col = nt * 8 + 2 * tig;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int r = rb + gid + 8 * h;
