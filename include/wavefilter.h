@@ -154,6 +154,9 @@ typedef struct {
                             wf_dwt_lowpass (A_L only) and the second exactly the launch
                             of wf_step_cached_al on that A_L; 0 when the first also
                             forms the coarse logits the second reads (or one launch) */
+  int32_t al_stages;     /* A_L stages (64 rows each) the path kernel keeps in flight
+                            when it stages A_L itself (two-launch plans with
+                            stream_is_dwt_lowpass = 1), else 0                       */
 } wf_plan;
 
 /* Fills *plan with the launch plan wf_step uses for these sizes on the

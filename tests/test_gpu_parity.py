@@ -421,6 +421,49 @@ def test_step_forced_plans_decisive(n, levels, g, k_l, heads, gather, logits):
         assert kind == "exact"
 
 
+@pytest.mark.parametrize("heads,n,levels,g,k_l,stages", [
+    # 38 units: four-CTA clusters of 256 coarse positions each; every A_L stage
+    # resident (two per tensor-core pass) with 32 queries, a refilled ring of
+    # three with 48 (shared memory)
+    (38, 16384, 4, 32, 128, 4),
+    (38, 16384, 4, 48, 128, 3),
+])
+def test_step_staged_al_decisive(heads, n, levels, g, k_l, stages):
+    # The two-launch step whose path kernel stages the stream's A_L itself
+    # (as wf_step_cached_al does), on inputs where every unit is decisive:
+    # wf_step and wf_step_cached_al index sets compared element by element.
+    d = 128
+    budget = k_l * (1 << levels) // 2
+    ks = bd.default_k_per_level(n, levels, budget)
+    assert ks[levels] == k_l
+    checked = sorted({0, heads // 2, heads - 1})
+    planted = _planted_inputs(n + g + stages, len(checked), n, g, d, levels, k_l)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(n + g + 1)
+    dev = {k: (0.2 * torch.randn((1, heads) + v.shape[2:], generator=gen, device="cuda"))
+           .to(torch.bfloat16) for k, v in planted.items()}
+    for i, h in enumerate(checked):
+        for k, v in planted.items():
+            dev[k][0, h] = torch.from_numpy(v[0, i]).to("cuda", torch.bfloat16)
+    dims = bd.make_dims(dev["Q"], dev["Kp"], levels)
+    plan = bd.step_plan(dims, ks)
+    assert plan["launches"] == 2 and plan["stream_is_dwt_lowpass"] == 1, plan
+    assert plan["al_stages"] == stages, plan
+    al = bd.dwt_lowpass(dev["Kp"], levels)
+    for cached in (False, True):
+        out, lse, idx, status = run_step(dev, levels, ks, al=al if cached else None)
+        assert status == 0
+        out, lse, idx = out.cpu().numpy(), lse.cpu().numpy(), idx.cpu().numpy()
+        for i, h in enumerate(checked):
+            res = oracle_unit(planted, 0, i, levels, ks)
+            assert all(lv["gap"] > 0.1 for lv in res["levels"].values()), "inputs not decisive"
+            kind = compare_step_unit(planted, 0, i, levels, ks, idx[0, h], out[0, h], lse[0, h],
+                                     res=res)
+            assert kind == "exact"
+        for h in range(heads):
+            check_index_set(idx[0, h], n, ks[0])
+
+
 def test_step_general_filter_large_candidate_sets():
     # A schedule that selects at an intermediate level takes the general
     # filter (per-level candidate lists; token logits spilled to the

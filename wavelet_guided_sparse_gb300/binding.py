@@ -45,7 +45,8 @@ class Plan(ctypes.Structure):
     _fields_ = [("launches", ctypes.c_int32), ("cluster", ctypes.c_int32),
                 ("final_gather", ctypes.c_int32), ("token_logits", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("filter_stages", ctypes.c_int32),
-                ("attend_stages", ctypes.c_int32), ("stream_is_dwt_lowpass", ctypes.c_int32)]
+                ("attend_stages", ctypes.c_int32), ("stream_is_dwt_lowpass", ctypes.c_int32),
+                ("al_stages", ctypes.c_int32)]
 
 
 LOGITS_NAMES = {0: "shared", 1: "workspace", 2: "tensor_memory", 3: "recomputed"}
@@ -196,7 +197,7 @@ def step_plan(dims: Dims, k: Sequence[int]) -> dict:
     return {"launches": p.launches, "cluster": p.cluster, "final_gather": p.final_gather,
             "token_logits": LOGITS_NAMES.get(p.token_logits, p.token_logits),
             "smem_bytes": p.smem_bytes, "filter_stages": p.filter_stages,
-            "attend_stages": p.attend_stages, "stream_is_dwt_lowpass": p.stream_is_dwt_lowpass}
+            "attend_stages": p.attend_stages, "stream_is_dwt_lowpass": p.stream_is_dwt_lowpass, "al_stages": p.al_stages}
 
 
 def inject_wait_timeout(polls: int) -> None:

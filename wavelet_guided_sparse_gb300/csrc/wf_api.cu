@@ -277,6 +277,7 @@ int wf_step_plan(const wf_dims* dims, const int32_t* k_per_level, wf_plan* out) 
   out->filter_stages = plan.f_stages;
   out->attend_stages = plan.a_stages;
   out->stream_is_dwt_lowpass = from_al ? 1 : 0;
+  out->al_stages = from_al && plan.al_stage ? plan.al_ring : 0;
   return WF_OK;
 }
 
