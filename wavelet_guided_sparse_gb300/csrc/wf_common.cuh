@@ -448,24 +448,11 @@ static __device__ __noinline__ TopkResult topk_distributed(const uint32_t* keys,
 // each histogram in its own pre-zeroed buffer, so a round costs one barrier:
 // every warp then finds the round's digit redundantly (vectorised bin sums,
 // a warp scan over lanes and a second warp scan inside the boundary lane's
-// bins).  A fused pass counts, per warp chunk, the keys above the threshold
-// and the ties, and emit(i, slot) receives every selected key with its rank
-// among the selected (ascending index).  A round whose boundary bin is taken
-// whole ends the search early (usually after the second round).
-// Shared-memory histogram increment aggregated over the lanes of a warp that
-// hit the same bin (scores cluster in a few bins in the first round); the
-// count of the bin's range of nb/32 bins is kept alongside.
-__device__ __forceinline__ void hist_add(uint32_t* h, uint32_t* region, bool active, uint32_t bin,
-                                         int per) {
-  const unsigned act = __ballot_sync(0xffffffffu, active);
-  if (!active) return;
-  const unsigned peers = __match_any_sync(act, bin);
-  if ((threadIdx.x & 31) == __ffs(peers) - 1) {
-    atomicAdd(&h[bin], __popc(peers));
-    atomicAdd(&region[bin / per], __popc(peers));
-  }
-}
-
+// bins).  Counts of the keys above the threshold and of the ties per 32-key
+// sub-chunk, scanned, give every selected key its rank among the selected
+// (ascending index), and only the sub-chunks holding slots of the caller's
+// range are emitted.  A round whose boundary bin is taken whole ends the
+// search early (usually after the second round).
 // Digit d of the round with #{digit > d} < need <= #{digit >= d}, found by one
 // warp from the 32 range counts (lane 0 = highest range) and then the bins of
 // the boundary range (descending, per/32 bins per lane).  Every lane returns
@@ -535,9 +522,7 @@ static __device__ __noinline__ void block_select_topk(const uint32_t* keys, int 
       const uint32_t kv = i < n ? keys[i] : 0u;
       const bool active = i < n && (kv & pmask) == prefix;
       const uint32_t bin = (kv >> shift) & (nb - 1);
-      if (round == 0) {
-        hist_add(h, sm.region[round], active, bin, per);  // scores share a few leading bins
-      } else if (active) {  // later rounds: the boundary bin's keys spread out
+      if (active) {
         atomicAdd(&h[bin], 1u);
         atomicAdd(&sm.region[round][bin / per], 1u);
       }
