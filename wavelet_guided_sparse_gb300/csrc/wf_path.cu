@@ -230,7 +230,7 @@ struct PathSmem {
       o = u;
       const size_t stage = static_cast<size_t>(p.a_stages) * p.tile_keys * kRowBytes;
       if (sizeof(T) == 2) {  // warp partials overwrite the stages after the last tile
-        const size_t work = sizeof(float) * (kWarps * 16 * (D + 8) + 2 * kWarps * 16);
+        const size_t work = sizeof(float) * (kWarps * 16 * (D + 8) + 2 * kWarps * 16 + kMaxQ * kWarps);
         a_kst = o;
         a_vst = o + stage;
         a_work = o;
@@ -1722,44 +1722,39 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       // selection is complete and their own stages lie below it), so only
       // this CTA's partials need a barrier.
       __syncthreads();
-      // One warp per query row: the CTA max, the weights 2^(m_w - max) of the
-      // key-group warps (every lane forms them) and the weighted sum of their
-      // partial rows, four columns per lane, pushed straight to the CTA that
-      // finalises the row, with the row's (max, sum).
+      // Per query row: the CTA max, the weights 2^(m_w - max) of the key-group
+      // warps and the weighted sum; (max, sum) go straight to the row's owner.
       const int KGW = kWarps / MB;
-      for (int qi = warp; qi < G; qi += kWarps) {
-        const int qmb = qi >> 4, r = qi & 15;
+      float* wts = lpart + kWarps * 16;  // [G][KGW]
+      if (tid < G) {
+        const int qi = tid, qmb = qi >> 4, r = qi & 15;
         float mx = -INFINITY;
         for (int g = 0; g < KGW; ++g) mx = fmaxf(mx, mpart[(qmb + MB * g) * 16 + r]);
-        float f[kWarps];
         float l = 0.f;
-#pragma unroll
-        for (int g = 0; g < kWarps; ++g) {
-          f[g] = 0.f;
-          if (g < KGW) {
-            const int w = qmb + MB * g;
-            f[g] = safe_exp2_diff(mpart[w * 16 + r], mx);
-            l += f[g] * lpart[w * 16 + r];
-          }
+        for (int g = 0; g < KGW; ++g) {
+          const int w = qmb + MB * g;
+          const float f = safe_exp2_diff(mpart[w * 16 + r], mx);
+          wts[qi * KGW + g] = f;
+          l += f * lpart[w * 16 + r];
         }
         const int owner = qi / rpo, ro = qi - owner * rpo;
-        if (lane == 0) {
-          float* dst = peer(recv_ml, owner) + (rank * rpo + ro) * 2;
-          dst[0] = mx;
-          dst[1] = l;
+        float* dst = peer(recv_ml, owner) + (rank * rpo + ro) * 2;
+        dst[0] = mx;
+        dst[1] = l;
+      }
+      __syncthreads();
+      // CTA partial of row qi, pushed straight to the CTA that finalises it.
+      for (int e = tid; e < G * (D / 4); e += kThreads) {
+        const int qi = e / (D / 4), col = (e % (D / 4)) * 4;
+        const int qmb = qi >> 4, r = qi & 15;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int g = 0; g < KGW; ++g) {
+          const float f = wts[qi * KGW + g];
+          const float4 v = *reinterpret_cast<const float4*>(opart + ((qmb + MB * g) * 16 + r) * OP + col);
+          acc.x += f * v.x; acc.y += f * v.y; acc.z += f * v.z; acc.w += f * v.w;
         }
-        for (int col = lane * 4; col < D; col += 128) {
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int g = 0; g < kWarps; ++g) {
-            if (g < KGW) {
-              const float4 v =
-                  *reinterpret_cast<const float4*>(opart + ((qmb + MB * g) * 16 + r) * OP + col);
-              acc.x += f[g] * v.x; acc.y += f[g] * v.y; acc.z += f[g] * v.z; acc.w += f[g] * v.w;
-            }
-          }
-          *reinterpret_cast<float4*>(peer(recv_o, owner) + (rank * rpo + ro) * D + col) = acc;
-        }
+        const int owner = qi / rpo, ro = qi - owner * rpo;
+        *reinterpret_cast<float4*>(peer(recv_o, owner) + (rank * rpo + ro) * D + col) = acc;
       }
     } else {
       // ------------------------------------------------ fp32 FMA path
