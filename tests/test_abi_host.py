@@ -267,3 +267,25 @@ def test_basis_entry_points_reject_before_launch(lib):
     assert step(k=k_sel, wsb=n_sel.value - 1) == 4
     assert step(k=bd._k_array([512, 512, 256, 128, 300])) == 2
     assert step(dims=_dims(n_prompt=4100)) == 2
+
+
+@pytest.mark.parametrize("name,launches,stream_is_dwt,al_stages", [
+    ("llada8b_layer", 1, 0, 0),       # one launch: the stream fused into the path kernel
+    ("long_prompt", 2, 1, 4),         # wf_dwt_lowpass + the cached-A_L launch, 4 stages
+    ("full_step", 2, 1, 4),
+    ("batched_long_10pct", 2, 0, 0),  # 512 positions per CTA: the stream forms the logits
+])
+def test_step_plan_routes(name, launches, stream_is_dwt, al_stages):
+    # wf_step's launch plan on a 152-SM device for the workloads' shapes (host
+    # only): which of the three routes each takes.
+    cfg = wl.CONFIGS[name]
+    dims = bd.Dims(cfg.batch, cfg.heads, cfg.n_prompt, cfg.n_gen, cfg.head_dim, cfg.levels,
+                   bd.WF_BF16)
+    plan = bd.step_plan(dims, cfg.k_per_level())
+    assert plan["launches"] == launches
+    assert plan["stream_is_dwt_lowpass"] == stream_is_dwt
+    assert plan["al_stages"] == al_stages
+    n = ctypes.c_int32(0)
+    assert bd.lib().wf_step_launch_count(ctypes.byref(dims), bd._k_array(cfg.k_per_level()),
+                                         ctypes.byref(n)) == 0
+    assert n.value == launches
