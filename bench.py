@@ -463,20 +463,25 @@ def run_ours(args, cfg):
     layer_us = ms_per_step * 1e3 / cfg.layers
 
     # ---- the first launch of a two-launch step, alone (the standalone DWT
-    # entry point over the same keys): back-to-back launches over the sets.
+    # entry point over the same keys): a CUDA graph of back-to-back launches
+    # over the sets (host call overhead stays out of short launches).
     lib = bd.lib()
     sp = bd._stream(stream)
     al = torch.empty((cfg.batch, cfg.heads, cfg.n_prompt >> cfg.levels, cfg.head_dim),
                      dtype=torch.float32, device=dev)
     n_dwt = max(20, len(sets))
-    d0, d1 = _event(), _event()
-    d0.record(stream)
-    for i in range(n_dwt):
-        lib.wf_dwt_lowpass(bd.ctypes.byref(dims), bd._ptr(sets[i % len(sets)]["Kp"]), bd._ptr(al),
-                           None, sp)
-    d1.record(stream)
+
+    def dwt_cycle():
+        for i in range(n_dwt):
+            lib.wf_dwt_lowpass(bd.ctypes.byref(dims), bd._ptr(sets[i % len(sets)]["Kp"]),
+                               bd._ptr(al), None, bd._stream())
+
+    dwt_graph = _capture(dwt_cycle, cap_stream)
+    dwt_graph.replay()
     torch.cuda.synchronize()
-    dwt_us = 1e3 * d0.elapsed_time(d1) / n_dwt
+    d_reps = 3
+    dwt_us = 1e3 * _time_cycles(dwt_graph, [], d_reps, 1, stream) / (d_reps * n_dwt)
+    del dwt_graph
 
     # ---- steps 2-5 with A_L cached from an earlier step (unchanged prompt keys)
     als = [bd.dwt_lowpass(c["Kp"], cfg.levels) for c in sets]
@@ -534,34 +539,92 @@ def run_ours(args, cfg):
     cached_layer_us = cached_ms * 1e3 / cfg.layers
     del cyc_cached
 
-    # ---- per-stage kernel durations (staged entry points, events on the launch stream)
+    # ---- per-stage kernel durations (the staged entry points in order, per
+    # input set): a CUDA graph with events recorded as graph nodes around
+    # every launch where this torch has them, else host-launched with events
+    # on the stream (those durations then include any gap while the host
+    # enqueues the next call).
     stage_ms = {"dwt": [], "score": [], "filter": [], "attn": []}
     idx_l = torch.empty((cfg.batch, cfg.heads, ks[-1]), dtype=torch.int32, device=dev)
     karr = bd._k_array(ks)
-    n_stage = 20
-    evs = [[_event() for _ in range(5)] for _ in range(n_stage)]
-    for i in range(n_stage):
-        c = sets[i % len(sets)]
-        e = evs[i]
-        e[0].record(stream)
+    n_stage = min(len(sets), 32)
+    try:
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
+               for _ in range(n_stage)]
+        stage_graphed = True
+    except TypeError:  # a torch without graph-node events
+        evs = [[_event() for _ in range(5)] for _ in range(n_stage)]
+        stage_graphed = False
+
+    def stage_cycle():
+        for i in range(n_stage):
+            c, e, cs = sets[i], evs[i], bd._stream()
+            e[0].record()
+            lib.wf_dwt_lowpass(bd.ctypes.byref(dims), bd._ptr(c["Kp"]), bd._ptr(al), None, cs)
+            e[1].record()
+            lib.wf_score_topk(bd.ctypes.byref(dims), bd._ptr(c["Q"]), bd._ptr(al), ks[-1],
+                              bd._ptr(idx_l), None, bd._ptr(ws), ws.numel(), cs)
+            e[2].record()
+            lib.wf_recursive_filter(bd.ctypes.byref(dims), bd._ptr(c["Q"]), bd._ptr(c["Kp"]),
+                                    bd._ptr(idx_l), karr, bd._ptr(idx), bd._ptr(ws), ws.numel(),
+                                    cs)
+            e[3].record()
+            lib.wf_sparse_gather_attn(bd.ctypes.byref(dims), bd._ptr(c["Q"]), bd._ptr(c["Kp"]),
+                                      bd._ptr(c["Vp"]), bd._ptr(c["Kg"]), bd._ptr(c["Vg"]),
+                                      bd._ptr(idx), ks[0], bd._ptr(out), bd._ptr(lse),
+                                      bd._ptr(ws), ws.numel(), cs)
+            e[4].record()
+
+    def stage_collect(first):
+        for e in evs[first:]:
+            for j, name in enumerate(("dwt", "score", "filter", "attn")):
+                stage_ms[name].append(e[j].elapsed_time(e[j + 1]))
+
+    if stage_graphed:
+        stage_graph = _capture(stage_cycle, cap_stream)
+        for rep in range(3):
+            stage_graph.replay()
+            torch.cuda.synchronize()
+            if rep:  # the first replay includes one-time effects
+                stage_collect(0)
+        del stage_graph
+    else:
+        stage_cycle()
+        torch.cuda.synchronize()
+        stage_collect(min(3, n_stage - 1))
+    stage_us = {k: 1e3 * statistics.mean(v) for k, v in stage_ms.items()}
+
+    # ---- the gather + eq. (3) attention launch on its own: the index lists
+    # of (up to) eight input sets, formed once by the staged entry points,
+    # then a CUDA graph of back-to-back wf_sparse_gather_attn launches that
+    # cycles through the sets (each set's K/V rows are read again only after
+    # the other sets', so no launch finds its rows in L2).
+    gsets = sets[:8]
+    g_idx = []
+    for c in gsets:
+        gi = torch.empty((cfg.batch, cfg.heads, ks[0]), dtype=torch.int32, device=dev)
         lib.wf_dwt_lowpass(bd.ctypes.byref(dims), bd._ptr(c["Kp"]), bd._ptr(al), None, sp)
-        e[1].record(stream)
         lib.wf_score_topk(bd.ctypes.byref(dims), bd._ptr(c["Q"]), bd._ptr(al), ks[-1],
                           bd._ptr(idx_l), None, bd._ptr(ws), ws.numel(), sp)
-        e[2].record(stream)
         lib.wf_recursive_filter(bd.ctypes.byref(dims), bd._ptr(c["Q"]), bd._ptr(c["Kp"]),
-                                bd._ptr(idx_l), karr, bd._ptr(idx), bd._ptr(ws), ws.numel(), sp)
-        e[3].record(stream)
-        lib.wf_sparse_gather_attn(bd.ctypes.byref(dims), bd._ptr(c["Q"]), bd._ptr(c["Kp"]),
-                                  bd._ptr(c["Vp"]), bd._ptr(c["Kg"]), bd._ptr(c["Vg"]),
-                                  bd._ptr(idx), ks[0], bd._ptr(out), bd._ptr(lse), bd._ptr(ws),
-                                  ws.numel(), sp)
-        e[4].record(stream)
+                                bd._ptr(idx_l), karr, bd._ptr(gi), bd._ptr(ws), ws.numel(), sp)
+        g_idx.append(gi)
     torch.cuda.synchronize()
-    for e in evs[3:]:  # the first launches include one-time effects
-        for j, name in enumerate(("dwt", "score", "filter", "attn")):
-            stage_ms[name].append(e[j].elapsed_time(e[j + 1]))
-    stage_us = {k: 1e3 * statistics.mean(v) for k, v in stage_ms.items()}
+
+    def gather_cycle():
+        for c, gi in zip(gsets, g_idx):
+            lib.wf_sparse_gather_attn(bd.ctypes.byref(dims), bd._ptr(c["Q"]), bd._ptr(c["Kp"]),
+                                      bd._ptr(c["Vp"]), bd._ptr(c["Kg"]), bd._ptr(c["Vg"]),
+                                      bd._ptr(gi), ks[0], bd._ptr(out), bd._ptr(lse),
+                                      bd._ptr(ws), ws.numel(), bd._stream())
+
+    gather_graph = _capture(gather_cycle, cap_stream)
+    for _ in range(3):
+        gather_graph.replay()
+    torch.cuda.synchronize()
+    g_reps = max(2, min(20, 160 // len(gsets)))
+    gather_us = 1e3 * _time_cycles(gather_graph, [], g_reps, 1, stream) / (g_reps * len(gsets))
+    del gather_graph, g_idx
 
     # ---- first-step cache write (eq. (2)) with A_L, from token-major K/V:
     # two input/output sets alternate (each launch touches more than L2),
@@ -703,7 +766,23 @@ def run_ours(args, cfg):
                     "unit": "GB/s", "frac": sbytes / (dwt_us * 1e-6) / 1e9 / peak,
                     "peak_source": peak_source, "traffic": _traffic("dwt", cfg),
                     "algorithmic_bytes_per_launch": sbytes, "launch_us": dwt_us,
-                    "timing": f"{n_dwt} back-to-back launches over the input sets"}
+                    "timing": f"CUDA graph of {n_dwt} back-to-back launches over the input "
+                              "sets, events around its replays"}
+    gbytes = path_bytes(cfg)["attn"]
+    gather_roofline = {"kernel": "path_kernel, gather + attention phase only (wf_sparse_gather_attn: "
+                                 "selected K/V rows, K_g/V_g, Q in; O, lse out)",
+                       "bound": "hbm", "achieved": gbytes / (gather_us * 1e-6) / 1e9,
+                       "peak": peak, "unit": "GB/s",
+                       "frac": gbytes / (gather_us * 1e-6) / 1e9 / peak,
+                       "peak_source": peak_source, "traffic": None,
+                       "algorithmic_bytes_per_launch": gbytes, "launch_us": gather_us,
+                       "timing": f"CUDA graph of back-to-back launches over {len(gsets)} input "
+                                 "sets' index lists, events around its replays"}
+    dg_bytes, dg_us = sbytes + gbytes, dwt_us + gather_us
+    dwt_gather = {"what": "the K_p stream (wf_dwt_lowpass) and the gather + attention "
+                          "(wf_sparse_gather_attn) of one layer, each launch timed on its own",
+                  "bytes": dg_bytes, "us": dg_us, "achieved": dg_bytes / (dg_us * 1e-6) / 1e9,
+                  "peak": peak, "unit": "GB/s", "frac": dg_bytes / (dg_us * 1e-6) / 1e9 / peak}
     if launches == 1:
         # One kernel per layer-step: its average duration is the timed region
         # divided by the layer-steps in it.
@@ -762,6 +841,8 @@ def run_ours(args, cfg):
                           "achieved": lbytes / (layer_us * 1e-6) / 1e9, "peak": peak,
                           "unit": "GB/s", "frac": lbytes / (layer_us * 1e-6) / 1e9 / peak},
         "dwt_roofline": dwt_roofline,
+        "gather_roofline": gather_roofline,
+        "dwt_gather": dwt_gather,
         "plan": plan,
         "layer_step_us": layer_us,
         "cached_al_step": {
@@ -789,6 +870,9 @@ def run_ours(args, cfg):
             "value": tokens_per_step(cfg) / cfg.layers / (basis_ms * 1e-3), "unit": "tokens/s",
             "layer_step_ms": basis_ms, "launches_per_layer_step": basis_launches},
         "stages_us": stage_us,
+        "stages_timing": ("CUDA graph of the four staged entry points per input set, events "
+                          "recorded as graph nodes around every launch" if stage_graphed else
+                          "host-launched, events on the stream around every launch"),
         "cpu_baseline": None if cpu_rate is None else {
             "value": cpu_rate, "unit": "tokens/s", "cores": workers, "kind": "oracle",
             "sample": f"{cpu_units} (sequence, layer, head) units of this workload in "

@@ -389,7 +389,8 @@ int wf_score_topk(const wf_dims* dims, const void* Q, const float* AL, int32_t k
   const Layout L = layout(ld, nullptr, nullptr);
   if (workspace_bytes < L.total) return WF_ERR_WORKSPACE;
   wf::PathPlan plan;
-  if (!wf::plan_path(ld, wf::kPhaseScore, nullptr, k_L, 0, wf::device_sm_count(), &plan))
+  if (!wf::plan_path(ld, wf::kPhaseScore | wf::kPhaseCachedAl, nullptr, k_L, 0,
+                     wf::device_sm_count(), &plan))
     return WF_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   wf::PathArgs a = {};

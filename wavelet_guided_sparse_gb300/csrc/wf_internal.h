@@ -30,8 +30,9 @@ enum : int { kPhaseScore = 1, kPhaseFilter = 2, kPhaseAttend = 4, kPhaseAll = 7 
 // Request bit for plan_path with kPhaseAll: compute A_L inside the path
 // kernel (step 1 fused into the scoring) where the plan allows it.
 enum : int { kPhaseFuseDwt = 8 };
-// Request bit for plan_path with kPhaseAll when the caller passes a cached
-// fp32 A_L: stage its rows by one bulk copy per CTA where the plan allows it.
+// Request bit for plan_path with kPhaseAll or kPhaseScore when the caller
+// passes a cached fp32 A_L: stage its rows by tensor copies where the plan
+// allows it.
 enum : int { kPhaseCachedAl = 16 };
 
 // Launch plan of the path kernel; a pure function of the sizes and the

@@ -402,9 +402,11 @@ __device__ __forceinline__ float safe_exp2_diff(float m, float mx) {
 }
 
 // Prompt row of key slot g (g < B) of this unit, or -1 if out of range.
-__device__ __forceinline__ int prompt_row(const PathParams& p, int mode, const Ctx& c,
-                                          const int32_t* klist, int k0, int g) {
-  const int row = (mode & kModeFilter) ? klist[g - k0] : __ldg(p.idx_in + c.unit * p.budget + g);
+// klist holds the rows of this CTA's slots [k0, k1): the filter's list, or
+// the caller's copied there at the start of the attend phase.
+__device__ __forceinline__ int prompt_row(const PathParams& p, const int32_t* klist, int k0,
+                                          int g) {
+  const int row = klist[g - k0];
   return (row >= 0 && row < p.n_prompt) ? row : -1;
 }
 
@@ -422,7 +424,7 @@ __device__ __forceinline__ bool attn_key_valid(const PathParams& p, int mode, co
                                                const AttnRows<T>& ar, int g) {
   if (g >= ar.k1) return false;
   if (g >= ar.B) return true;
-  return prompt_row(p, mode, c, ar.klist, ar.k0, g) >= 0;
+  return prompt_row(p, ar.klist, ar.k0, g) >= 0;
 }
 
 // Gathers the key and value rows of slots [k0 + tile TK, ...) into ring stage
@@ -444,7 +446,7 @@ __device__ __forceinline__ void attn_issue(const PathParams& p, int mode, const 
         ks = ar.kg + static_cast<int64_t>(g - ar.B) * D;
         vs = ar.vg + static_cast<int64_t>(g - ar.B) * D;
       } else {
-        const int row = prompt_row(p, mode, c, ar.klist, ar.k0, g);
+        const int row = prompt_row(p, ar.klist, ar.k0, g);
         if (row >= 0) {
           ks = ar.kp + static_cast<int64_t>(row) * D;
           vs = ar.vp + static_cast<int64_t>(row) * D;
@@ -1589,9 +1591,17 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
     const T* vgp = static_cast<const T*>(p.vg) + unit * G * D;
     const T* kpp = static_cast<const T*>(p.kp) + unit * p.n_prompt * D;
     const T* vpp = static_cast<const T*>(p.vp) + unit * p.n_prompt * D;
-    if (!(mode & kModeFilter)) {  // report bad caller indices of this slot range
-      for (int g = k0 + tid; g < min(k1, B); g += kThreads)
-        if (prompt_row(p, mode, c, klist, k0, g) < 0) raise_flag(p.status, WF_DEV_BAD_INDEX);
+    if (!(mode & kModeFilter)) {
+      // The caller's rows of this slot range, staged once (the copies below
+      // then need no dependent global load); bad ones are reported.
+      const int32_t* src = p.idx_in + unit * B;
+      bool bad = false;
+      for (int g = k0 + tid; g < min(k1, B); g += kThreads) {
+        const int row = __ldg(src + g);
+        klist[g - k0] = row;
+        bad |= row < 0 || row >= p.n_prompt;
+      }
+      if (bad) raise_flag(p.status, WF_DEV_BAD_INDEX);
     }
     // Every slot of a tile is filled (invalid slots with a finite dummy row),
     // so masked probabilities multiply finite values.
@@ -2021,7 +2031,7 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
                int sm_count, PathPlan* plan) {
   PathParams p = {};
   const bool want_fuse = mode == (kPhaseAll | kPhaseFuseDwt);
-  const bool want_al = mode == (kPhaseAll | kPhaseCachedAl);
+  const bool want_al = mode == (kPhaseAll | kPhaseCachedAl) || mode == (kPhaseScore | kPhaseCachedAl);
   mode &= kPhaseAll;
   p.mode = mode;
   p.G = ld.n_gen;
@@ -2039,7 +2049,6 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
   int cs0 = pow2_floor(std::max(1, static_cast<int>(std::min<int64_t>(kMaxCluster, sm_count / std::max<int64_t>(1, ld.units)))));
   auto cluster_ok = [&](int c) {
     if ((mode & kModeScore) && (p.P % c != 0 || p.P / c < 8)) return false;
-    if (mode == kModeScore && c > 1) return false;  // scoring alone needs no cluster
     if ((mode & kModeFilter) && k_l < c) return false;
     if ((mode & kModeAttend) && p.n_keys < 16 * c) return false;
     return true;
