@@ -313,6 +313,9 @@ __device__ __noinline__ void umma_logits(const unsigned char* a, int nplanes, in
     umma_commit(bar);
   }
   const bool ok = mbar_wait_bounded(bar, phase & 1u, status);
+  // The count advances even after a wait gave up: the commit still completes
+  // this phase when the multiply ends, so the next wait is for the next
+  // commit; if it never comes, every later wait gives up as well.
   ++phase;
   tc_fence_after();
   if (ok) {
@@ -1349,13 +1352,16 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
       }
       if (ntiles <= FS && sizeof(T) == 2) {
         // Every row is in flight: one wait, then one tensor-core pass over all
-        // R rows (tiles sit back to back in the ring).
+        // R rows (tiles sit back to back in the ring).  If the wait gives up
+        // (the status word reports it) no multiply reads the ring.
+        bool rows_ok = true;
         if (tma_spans)
-          (void)mbar_wait_bounded(span_bar, 0, p.status);
+          rows_ok = mbar_wait_bounded(span_bar, 0, p.status);
         else
           cp_async_wait<0>();
-        umma_logits<D>(kst, 1, 0, FS * kTileRows, R, qs, G, t, 0, TT, 1.f, tmem, mma_bar, mma_phase,
-                       p.status);
+        if (!__syncthreads_or(!rows_ok))
+          umma_logits<D>(kst, 1, 0, FS * kTileRows, R, qs, G, t, 0, TT, 1.f, tmem, mma_bar,
+                         mma_phase, p.status);
         __syncthreads();
       } else
       for (int tile = 0; tile < ntiles; ++tile) {
