@@ -464,6 +464,42 @@ def test_step_staged_al_decisive(heads, n, levels, g, k_l, stages):
             check_index_set(idx[0, h], n, ks[0])
 
 
+@pytest.mark.parametrize("g", [32, 64])
+def test_score_topk_staged_al_decisive(g):
+    # The stand-alone scorer on four-CTA clusters of 256 coarse positions each
+    # (38 units of 1024 positions): every CTA stages its A_L rows in four
+    # tensor-copy stages and forms the logits on the tensor cores.  Scores
+    # against the oracle's level-L attention mass; planted units' index sets
+    # exactly, every unit's checked for validity.
+    heads, n, levels, k_l, d = 38, 16384, 4, 128, 128
+    checked = sorted({0, heads // 2, heads - 1})
+    planted = _planted_inputs(7 * g, len(checked), n, g, d, levels, k_l)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(g)
+    dev = {k: (0.2 * torch.randn((1, heads) + planted[k].shape[2:], generator=gen,
+                                 device="cuda")).to(torch.bfloat16) for k in ("Q", "Kp")}
+    for i, h in enumerate(checked):
+        for k in ("Q", "Kp"):
+            dev[k][0, h] = torch.from_numpy(planted[k][0, i]).to("cuda", torch.bfloat16)
+    ks = bd.default_k_per_level(n, levels, k_l * (1 << levels) // 2)
+    dims = bd.make_dims(dev["Q"], dev["Kp"], levels)
+    ws = bd.alloc_workspace(dims, ks, dev["Q"].device)
+    al = bd.dwt_lowpass(dev["Kp"], levels)
+    idx, scores = bd.score_topk(dev["Q"], al, n, levels, k_l, ws, return_scores=True)
+    idx, scores = idx.cpu().numpy(), scores.cpu().numpy()
+    assert bd.read_device_status(ws) == 0
+    for i, h in enumerate(checked):
+        res = wo.recursive_filter(planted["Q"][0, i], planted["Kp"][0, i], levels, ks)
+        top = res["levels"][levels]
+        assert top["gap"] > 0.1, "inputs not decisive"
+        np.testing.assert_allclose(scores[0, h], top["scores"], rtol=1e-4,
+                                   atol=1e-6 * top["scores"].max())
+        np.testing.assert_array_equal(idx[0, h], top["sel"])
+    for h in range(heads):
+        assert (np.diff(idx[0, h]) > 0).all()
+        assert idx[0, h].min() >= 0 and idx[0, h].max() < n >> levels
+
+
 def test_step_general_filter_large_candidate_sets():
     # A schedule that selects at an intermediate level takes the general
     # filter (per-level candidate lists; token logits spilled to the
