@@ -42,3 +42,16 @@ def test_cache_init_bytes():
     # K and V of every position read once and written once, plus fp32 A_L.
     assert bench.cache_init_bytes(wl.CONFIGS["llada8b_layer"]) == (
         4 * U * (N + G) * D * E + U * P * D * 4) == 139_460_608
+
+
+def test_gather_bytes_term_by_term():
+    # The stand-alone gather + attention launch: the selected key and value
+    # rows, K_g/V_g, Q, O and the indices; with the K_p stream it is the
+    # "DWT + gather" figure.
+    gathered = U * 2 * B * D * E
+    small = U * (2 * G * D * E + G * D * E + G * D * 4 + 4 * B)
+    cfg = wl.CONFIGS["llada8b_layer"]
+    assert bench.path_bytes(cfg)["attn"] == gathered + small
+    full = wl.CONFIGS["full_step"]
+    assert bench.path_bytes(full)["attn"] == 68_943_872
+    assert bench.stream_bytes(full) + bench.path_bytes(full)["attn"] == 622_592_000
