@@ -1621,7 +1621,14 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
 
     if constexpr (sizeof(T) == 2) {
       const int MB = G <= 16 ? 1 : (G <= 32 ? 2 : 4);
-      const int mb = warp % MB, kgrp = warp / MB;  // 16 keys per warp per tile
+      // Keys per warp per tile (the plan's tile / key-group warps): 16, or 32
+      // with four query-row blocks in the general instantiation, so a tile
+      // still holds 64 keys and its fixed cost (wait, barrier, copies) is
+      // spread over as many keys as with fewer queries.  The constant-folded
+      // instantiations keep the 16-key body (their code stays smaller).
+      const bool two = !kFast && TK * MB / kWarps == 32;
+      const int KB = two ? 32 : 16;
+      const int mb = warp % MB, kgrp = warp / MB;
       uint32_t qa[D / 16][4];
       {
         // Q rows mb * 16 + (lane & 15), chunk 2 ks + (lane >> 4), core-matrix layout.
@@ -1640,11 +1647,12 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         // Tiles issued before this iteration's refill: 0 .. min(ntiles, AS + tile - 1) - 1.
         cp_async_wait_pending(tile == 0 ? min(ntiles, AS) - 1 : min(ntiles - tile - 1, AS - 2));
         __syncthreads();  // this tile's rows are visible; every warp is done with tile - 1
-        const uint32_t kb = smem_u32(kst + (stage * TK + kgrp * 16) * RB);
-        const uint32_t vb = smem_u32(vst + (stage * TK + kgrp * 16) * RB);
-        float s[2][4];
+        const uint32_t kb = smem_u32(kst + (stage * TK + kgrp * KB) * RB);
+        const uint32_t vb = smem_u32(vst + (stage * TK + kgrp * KB) * RB);
+        // Logits of the warp's keys: n-blocks of 8 keys (two per 16-key block).
+        float s[4][4];
 #pragma unroll
-        for (int nb = 0; nb < 2; ++nb)
+        for (int nb = 0; nb < 4; ++nb)
 #pragma unroll
           for (int e = 0; e < 4; ++e) s[nb][e] = 0.f;
         const uint32_t kaddr = kb + ((lane & 7) + ((lane >> 4) << 3)) * RB + ((lane >> 3) & 1) * 16;
@@ -1654,13 +1662,21 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           ldsm_x4(kaddr + ks * 32, b);
           mma_bf16(s[0], qa[ks], b);
           mma_bf16(s[1], qa[ks], b + 2);
+          if (two) {
+            uint32_t b2[4];
+            ldsm_x4(kaddr + 16 * RB + ks * 32, b2);
+            mma_bf16(s[2], qa[ks], b2);
+            mma_bf16(s[3], qa[ks], b2 + 2);
+          }
         }
-        const int jbase = k0 + tile * TK + kgrp * 16 + (lane & 3) * 2;
+        const int NB = two ? 4 : 2;
+        const int jbase = k0 + tile * TK + kgrp * KB + (lane & 3) * 2;
         float mx_lo = -INFINITY, mx_hi = -INFINITY;
 #pragma unroll
-        for (int nb = 0; nb < 2; ++nb)
+        for (int nb = 0; nb < 4; ++nb)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
+            if (nb >= NB) continue;
             const bool v = attn_key_valid(p, mode, c, ar, jbase + nb * 8 + e);
             s[nb][e] = v ? s[nb][e] * p.scale_log2 : -INFINITY;
             s[nb][e + 2] = v ? s[nb][e + 2] * p.scale_log2 : -INFINITY;
@@ -1677,9 +1693,10 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         const float corr_lo = fast_exp2(m_lo - base_lo), corr_hi = fast_exp2(m_hi - base_hi);
         float sum_lo = 0.f, sum_hi = 0.f;
 #pragma unroll
-        for (int nb = 0; nb < 2; ++nb)
+        for (int nb = 0; nb < 4; ++nb)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
+            if (nb >= NB) continue;
             s[nb][e] = fast_exp2(s[nb][e] - base_lo);
             s[nb][e + 2] = fast_exp2(s[nb][e + 2] - base_hi);
             sum_lo += s[nb][e];
@@ -1693,11 +1710,15 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
         l_hi = l_hi * corr_hi + sum_hi;
         m_lo = mn_lo;
         m_hi = mn_hi;
-        uint32_t pa[4];
-        pa[0] = pack_bf16(s[0][0], s[0][1]);
-        pa[1] = pack_bf16(s[0][2], s[0][3]);
-        pa[2] = pack_bf16(s[1][0], s[1][1]);
-        pa[3] = pack_bf16(s[1][2], s[1][3]);
+        // Probabilities as the A operand (16 rows x 16 keys per block).
+        uint32_t pa[2][4];
+#pragma unroll
+        for (int kb2 = 0; kb2 < 2; ++kb2) {
+          pa[kb2][0] = pack_bf16(s[2 * kb2][0], s[2 * kb2][1]);
+          pa[kb2][1] = pack_bf16(s[2 * kb2][2], s[2 * kb2][3]);
+          pa[kb2][2] = pack_bf16(s[2 * kb2 + 1][0], s[2 * kb2 + 1][1]);
+          pa[kb2][3] = pack_bf16(s[2 * kb2 + 1][2], s[2 * kb2 + 1][3]);
+        }
         const uint32_t vaddr = vb + (lane & 15) * RB + (lane >> 4) * 16;
 #pragma unroll
         for (int dn = 0; dn < D / 8; dn += 2) {
@@ -1707,8 +1728,14 @@ __global__ void __launch_bounds__(kThreads, 1) path_kernel(const __grid_constant
           oacc[dn + 1][2] *= corr_hi; oacc[dn + 1][3] *= corr_hi;
           uint32_t b[4];
           ldsm_x4_t(vaddr + dn * 16, b);
-          mma_bf16(oacc[dn], pa, b);
-          mma_bf16(oacc[dn + 1], pa, b + 2);
+          mma_bf16(oacc[dn], pa[0], b);
+          mma_bf16(oacc[dn + 1], pa[0], b + 2);
+          if (two) {
+            uint32_t b2[4];
+            ldsm_x4_t(vaddr + 16 * RB + dn * 16, b2);
+            mma_bf16(oacc[dn], pa[1], b2);
+            mma_bf16(oacc[dn + 1], pa[1], b2 + 2);
+          }
         }
         // Refill the stage tile - 1 used (every warp left it before this
         // iteration's barrier) after this warp's multiplies: the warps reach
@@ -1926,6 +1953,14 @@ cudaError_t launch_typed(int64_t units, const PathParams& prm, size_t smem, cuda
     if (var == 1) kern = path_kernel<T, D, 1>;
     if (var == 2) kern = path_kernel<T, D, 2>;
   }
+  // The constant-folded instantiations take 16 keys per warp per tile: a plan
+  // of 32 (four query-row blocks) runs as half-size tiles in twice the
+  // stages, the same shared-memory bytes.
+  PathParams pk = prm;
+  if (var != 0 && pk.G > 32 && pk.tile_keys == 64) {
+    pk.tile_keys = 32;
+    pk.a_stages = std::min(6, 2 * pk.a_stages);
+  }
   cudaError_t e = cudaSuccess;
   if (var == 1) {
     if constexpr (sizeof(T) == 2) e = ensure_max_smem<path_kernel<T, D, 1>>();
@@ -1947,7 +1982,7 @@ cudaError_t launch_typed(int64_t units, const PathParams& prm, size_t smem, cuda
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, prm);
+  return cudaLaunchKernelEx(&cfg, kern, pk);
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once (no link-time
@@ -2092,7 +2127,7 @@ bool plan_path(const LaunchDims& ld, int mode, const int32_t* k, int k_l, int bu
     p.klist_cap = (mode & kModeAttend) ? (p.n_keys + cs - 1) / cs + 1 : 0;
     if (ld.dtype == WF_BF16) {
       const int mb = ld.n_gen <= 16 ? 1 : (ld.n_gen <= 32 ? 2 : 4);
-      p.tile_keys = 16 * (kWarps / mb);
+      p.tile_keys = (mb == 4 ? 32 : 16) * (kWarps / mb);  // 64 keys: 16 or 32 per warp
     } else {
       p.tile_keys = 32;
     }
