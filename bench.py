@@ -48,11 +48,11 @@ TRAFFIC = {
     "dwt": {"sources": ("wf_dwt.cu", "wf_common.cuh", "wf_mma.cuh", "wf_internal.h"),
             "source_sha": "e40d91781866bcc9",
             "bytes": {"full_step": 553035520, "long_prompt": 280975872}},
-    # 122.2 MB read + 0.1 MB written (full step); 68.1 MB read (long prompt)
+    # 122.3 MB read + 0.1 MB written (full step); 68.1 MB read (long prompt)
     "path": {"sources": ("wf_path.cu", "wf_common.cuh", "wf_mma.cuh", "wf_umma.cuh",
                          "wf_internal.h"),
-             "source_sha": "c4e1fc9f5755e549",
-             "bytes": {"full_step": 122331904, "long_prompt": 68080640}},
+             "source_sha": "7f6aa126a9aa4548",
+             "bytes": {"full_step": 122388224, "long_prompt": 68129536}},
     # 1076.7 MB read + 1042.5 MB written (one full-step layer)
     "cache": {"sources": ("wf_cache.cu", "wf_common.cuh", "wf_internal.h"),
               "source_sha": "167dcdf5ab135297", "bytes": {"full_step": 2119244544}},
